@@ -1,0 +1,231 @@
+/*
+ * CPU oracle for the NVFP4 (nvfp4/g16) weight-only GEMV.
+ *
+ * TEST INFRASTRUCTURE. Only the test suite, the smoke check and the benchmark's
+ * CPU-baseline leg may load this library. The CUDA library never links, includes
+ * or calls it, and this file includes no header of the CUDA library.
+ *
+ * What it computes (plain definition, fp64, no blocking or reordering):
+ *
+ *     y[m, n] = g * sum_k E2M1(q[n, k]) * E4M3(s[n, k / 16]) * bf16(x[m, k])
+ *
+ * Sources on the pages:
+ *   - "glm-5.3-flash-nvfp4-tp3-512k--gb10 card.json", performance[4], [6], [8],
+ *     [9] and [33], field `note`: the W4A16 weight is NVFP4, i.e. E2M1 values
+ *     with an unsigned E4M3 scale for every 16 weights; the activation is BF16.
+ *   - "glm-5.3-flash-nvfp4-tp3-512k--gb10 graph.json", node l0.kda.q, field
+ *     `steps`: activation read as bf16, the nvfp4/g16 weight widened to bf16,
+ *     bf16 x bf16 products accumulated in f32, then an f32 scale.
+ *   - "GLM-5.3-Flash-NVFP4" blueprint page, section Precision, table of weight
+ *     and activation formats: nvfp4/g16 weight with bf16 activation.
+ * Readings where the pages are silent (each listed in the design notes):
+ *   - element 2j of a row is the LOW nibble of byte j, element 2j+1 the high one;
+ *   - packed codes are [N, K/2] bytes and scales [N, K/16] bytes, row-major;
+ *   - g is one FP32 scale per weight tensor, applied after the sum;
+ *   - the E4M3 sign bit is decoded as in standard E4M3 (the pages say the
+ *     scale is unsigned, so valid data never sets it); 0x7F/0xFF are NaN;
+ *   - MoE: slot s = t * top_k + j uses expert ids[s] and its own g; x row t
+ *     (shared per token) or row s (one row per slot).
+ *
+ * Decoders follow the bit definitions of the two minifloat formats (OCP
+ * Microscaling Formats v1.0): E2M1 has 1 sign, 2 exponent (bias 1) and
+ * 1 mantissa bit; E4M3 has 1 sign, 4 exponent (bias 7) and 3 mantissa bits,
+ * no infinities, and NaN where all exponent and mantissa bits are set.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* E2M1: bit 3 sign, bits 2..1 exponent (bias 1), bit 0 mantissa. */
+double nvfp4_oracle_e2m1(int code) {
+    int sign = (code >> 3) & 1;
+    int exp_field = (code >> 1) & 3;
+    int mant = code & 1;
+    double mag;
+    if (exp_field == 0) {
+        /* subnormal: (mant / 2) * 2^(1 - bias) with bias 1 */
+        mag = 0.5 * (double)mant;
+    } else {
+        mag = ldexp(1.0 + 0.5 * (double)mant, exp_field - 1);
+    }
+    return sign ? -mag : mag;
+}
+
+/* E4M3 (FN variant): bit 7 sign, bits 6..3 exponent (bias 7), bits 2..0 mantissa. */
+double nvfp4_oracle_e4m3(int code) {
+    int sign = (code >> 7) & 1;
+    int exp_field = (code >> 3) & 15;
+    int mant = code & 7;
+    double mag;
+    if (exp_field == 15 && mant == 7) return NAN;
+    if (exp_field == 0) {
+        /* subnormal: (mant / 8) * 2^(1 - bias) */
+        mag = ldexp((double)mant / 8.0, -6);
+    } else {
+        mag = ldexp(1.0 + (double)mant / 8.0, exp_field - 7);
+    }
+    return sign ? -mag : mag;
+}
+
+/* bf16 is the top half of an IEEE binary32. */
+double nvfp4_oracle_bf16(uint16_t bits) {
+    uint32_t u = (uint32_t)bits << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+int nvfp4_oracle_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+void nvfp4_oracle_set_threads(int n) {
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
+/* Code n of the packed row: the low nibble of byte j is element 2j. */
+static int nibble_at(const uint8_t *wrow, int64_t k) {
+    return (wrow[k / 2] >> (4 * (k & 1))) & 0xF;
+}
+
+/* One output element: returns sum_k E2M1 * E4M3 * x and sum_k |E2M1 * E4M3 * x|. */
+static void dot_row(const uint8_t *wrow, const uint8_t *srow, const uint16_t *xrow,
+                    int64_t K, double *sum_out, double *abs_out) {
+    double sum = 0.0, abs_sum = 0.0;
+    for (int64_t k = 0; k < K; ++k) {
+        double q = nvfp4_oracle_e2m1(nibble_at(wrow, k));
+        double s = nvfp4_oracle_e4m3(srow[k / 16]);
+        double xv = nvfp4_oracle_bf16(xrow[k]);
+        double term = q * s * xv;
+        sum += term;
+        abs_sum += fabs(term);
+    }
+    *sum_out = sum;
+    *abs_out = abs_sum;
+}
+
+/*
+ * Dense GEMV.  w: [N, K/2] bytes, s: [N, K/16] bytes, x: [M, K] bf16 bits.
+ * rows: the output columns n to compute (NULL = all N, in order); nrows their count.
+ * y, yabs: [M, nrows] row-major; yabs[m, i] = |g| * sum_k |term|.
+ * Returns 0, or -1 on a bad argument.
+ */
+int nvfp4_oracle_gemv(const uint8_t *w, const uint8_t *s, double g, const uint16_t *x,
+                      int64_t M, int64_t N, int64_t K, const int64_t *rows, int64_t nrows,
+                      double *y, double *yabs) {
+    if (K % 16 != 0 || M < 0 || N < 0 || K < 0) return -1;
+    if (rows == NULL) nrows = N;
+    for (int64_t i = 0; i < nrows; ++i) {
+        int64_t n = rows ? rows[i] : i;
+        if (n < 0 || n >= N) return -1;
+    }
+    int64_t i;
+#pragma omp parallel for schedule(static)
+    for (i = 0; i < nrows; ++i) {
+        int64_t n = rows ? rows[i] : i;
+        const uint8_t *wrow = w + n * (K / 2);
+        const uint8_t *srow = s + n * (K / 16);
+        for (int64_t m = 0; m < M; ++m) {
+            double sum, abs_sum;
+            dot_row(wrow, srow, x + m * K, K, &sum, &abs_sum);
+            y[m * nrows + i] = g * sum;
+            yabs[m * nrows + i] = fabs(g) * abs_sum;
+        }
+    }
+    return 0;
+}
+
+/*
+ * Gate and up projections of one input, written side by side:
+ * y[m, 0:N] = gate GEMV, y[m, N:2N] = up GEMV (the fused "gate|up" projection
+ * of "glm-5.3-flash-nvfp4-tp3-512k--gb10 card.json", performance[9] shape).
+ * rows index the 2N concatenated outputs (NULL = all).
+ */
+int nvfp4_oracle_gemv_gate_up(const uint8_t *wg, const uint8_t *sg, double gg,
+                              const uint8_t *wu, const uint8_t *su, double gu,
+                              const uint16_t *x, int64_t M, int64_t N, int64_t K,
+                              const int64_t *rows, int64_t nrows, double *y, double *yabs) {
+    if (K % 16 != 0 || M < 0 || N < 0 || K < 0) return -1;
+    if (rows == NULL) nrows = 2 * N;
+    for (int64_t i = 0; i < nrows; ++i) {
+        int64_t r = rows ? rows[i] : i;
+        if (r < 0 || r >= 2 * N) return -1;
+    }
+    int64_t i;
+#pragma omp parallel for schedule(static)
+    for (i = 0; i < nrows; ++i) {
+        int64_t r = rows ? rows[i] : i;
+        int up = r >= N;
+        int64_t n = up ? r - N : r;
+        const uint8_t *wrow = (up ? wu : wg) + n * (K / 2);
+        const uint8_t *srow = (up ? su : sg) + n * (K / 16);
+        double g = up ? gu : gg;
+        for (int64_t m = 0; m < M; ++m) {
+            double sum, abs_sum;
+            dot_row(wrow, srow, x + m * K, K, &sum, &abs_sum);
+            y[m * nrows + i] = g * sum;
+            yabs[m * nrows + i] = fabs(g) * abs_sum;
+        }
+    }
+    return 0;
+}
+
+/*
+ * Routed-expert GEMV over slots (the routed gate/up slot GEMV of
+ * "glm-5.3-flash-nvfp4-tp3-512k--gb10 card.json", performance[33]).
+ * w: [E, N, K/2], s: [E, N, K/16], gs: [E] per-expert global scales (float).
+ * ids: [T * top_k], slot s = t * top_k + j, token-major.
+ * x: [T, K] when x_per_slot == 0 (row t), [T * top_k, K] when 1 (row s).
+ * rows: output columns to compute (NULL = all N).  y, yabs: [T * top_k, nrows].
+ * A slot whose id is outside [0, E) gets zeros and is counted in *bad_ids.
+ */
+int nvfp4_oracle_moe_gemv(const uint8_t *w, const uint8_t *s, const float *gs, int64_t E,
+                          const int32_t *ids, int64_t T, int64_t top_k,
+                          const uint16_t *x, int x_per_slot, int64_t N, int64_t K,
+                          const int64_t *rows, int64_t nrows, double *y, double *yabs,
+                          int64_t *bad_ids) {
+    if (K % 16 != 0 || E < 0 || T < 0 || top_k < 0 || N < 0 || K < 0) return -1;
+    if (rows == NULL) nrows = N;
+    for (int64_t i = 0; i < nrows; ++i) {
+        int64_t n = rows ? rows[i] : i;
+        if (n < 0 || n >= N) return -1;
+    }
+    int64_t slots = T * top_k;
+    int64_t bad = 0;
+    for (int64_t sl = 0; sl < slots; ++sl)
+        if (ids[sl] < 0 || ids[sl] >= E) ++bad;
+    if (bad_ids) *bad_ids = bad;
+    int64_t sl;
+#pragma omp parallel for schedule(static)
+    for (sl = 0; sl < slots; ++sl) {
+        int64_t e = ids[sl];
+        int64_t xrow = x_per_slot ? sl : sl / top_k;
+        for (int64_t i = 0; i < nrows; ++i) {
+            if (e < 0 || e >= E) {
+                y[sl * nrows + i] = 0.0;
+                yabs[sl * nrows + i] = 0.0;
+                continue;
+            }
+            int64_t n = rows ? rows[i] : i;
+            const uint8_t *wrow = w + (e * N + n) * (K / 2);
+            const uint8_t *srow = s + (e * N + n) * (K / 16);
+            double g = (double)gs[e];
+            double sum, abs_sum;
+            dot_row(wrow, srow, x + xrow * K, K, &sum, &abs_sum);
+            y[sl * nrows + i] = g * sum;
+            yabs[sl * nrows + i] = fabs(g) * abs_sum;
+        }
+    }
+    return 0;
+}

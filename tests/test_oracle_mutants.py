@@ -1,0 +1,103 @@
+"""The oracle's pins catch plausible mistakes.
+
+Each case copies the oracle's C source and plants one mistake in the copy: a
+swapped nibble order, a dropped sign, a wrong exponent bias, a wrong scale
+index, a dropped term, a transposed operand, and so on. It then builds the copy
+into a scratch library and checks that the pin battery below rejects it. The
+unmodified source must pass the same battery. Everything runs on the CPU.
+"""
+import os
+import subprocess
+
+import numpy as np
+import pytest
+
+import oracle
+from nvfp4_weight_only_gemv_gb300 import synth
+
+from test_oracle_pins import E2M1_TABLE, _arrays, _golden, dequant, torch_bf16, torch_e4m3
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "nvfp4_oracle.c")
+
+MUTANTS = {
+    "nibble_order": ("(wrow[k / 2] >> (4 * (k & 1)))", "(wrow[k / 2] >> (4 * (1 - (k & 1))))", 1),
+    "e2m1_sign_dropped": ("return sign ? -mag : mag;", "return mag;", 1),
+    "e2m1_bias": ("exp_field - 1)", "exp_field - 2)", 1),
+    "e2m1_subnormal": ("mag = 0.5 * (double)mant;", "mag = 1.0 * (double)mant;", 1),
+    "e4m3_bias": ("exp_field - 7)", "exp_field - 8)", 1),
+    "e4m3_subnormal": ("ldexp((double)mant / 8.0, -6)", "ldexp((double)mant / 8.0, -7)", 1),
+    "e4m3_no_nan": ("if (exp_field == 15 && mant == 7) return NAN;", "", 1),
+    "scale_index": ("srow[k / 16]", "srow[k / 32]", 1),
+    "scale_row_stride": ("const uint8_t *srow = s + n * (K / 16);", "const uint8_t *srow = s + n * (K / 32);", 1),
+    "global_scale_dropped": ("y[m * nrows + i] = g * sum;", "y[m * nrows + i] = sum;", 1),
+    "x_row_transposed": ("dot_row(wrow, srow, x + m * K, K, &sum, &abs_sum);",
+                         "dot_row(wrow, srow, x + m, K, &sum, &abs_sum);", 1),
+    "dropped_last_term": ("for (int64_t k = 0; k < K; ++k)", "for (int64_t k = 0; k < K - 1; ++k)", 1),
+    "gate_up_swapped": ("int up = r >= N;", "int up = r < N;", 1),
+    "moe_x_row": ("int64_t xrow = x_per_slot ? sl : sl / top_k;", "int64_t xrow = x_per_slot ? sl : 0;", 1),
+    "moe_global_scale": ("double g = (double)gs[e];", "double g = (double)gs[0];", 1),
+}
+
+
+def battery(lib):
+    """Return the names of the pins that ``lib`` fails (empty when all hold)."""
+    fails = []
+    if any(oracle.e2m1(c, lib) != E2M1_TABLE[c] or
+           np.signbit(oracle.e2m1(c, lib)) != np.signbit(E2M1_TABLE[c]) for c in range(16)):
+        fails.append("e2m1")
+    ref = torch_e4m3(np.arange(256))
+    got = np.array([oracle.e4m3(c, lib) for c in range(256)])
+    if not np.array_equal(np.isnan(got), np.isnan(ref)) or \
+            not np.array_equal(got[~np.isnan(ref)], ref[~np.isnan(ref)]):
+        fails.append("e4m3")
+    for ex in _golden("hand_worked.json")["examples"]:
+        w, s, x = _arrays(ex)
+        y, _ = oracle.gemv(w, s, ex["g"], x, lib=lib)
+        if not np.array_equal(y, np.array(ex["y"])):
+            fails.append("hand_worked:" + ex["name"])
+    p = synth.dense_problem(48, 160, 3, 51)
+    w, s, x = p["w"].numpy(), p["s"].numpy(), synth.bf16_bits(p["x"])
+    y, ya = oracle.gemv(w, s, p["g"], x, lib=lib)
+    refd = p["g"] * (torch_bf16(x) @ dequant(w, s).T)
+    if not np.all(np.abs(y - refd) <= 1e-12 * np.maximum(ya, 1e-300)):
+        fails.append("numpy_matmul")
+    q = synth.gate_up_problem(24, 64, 2, 52)
+    wg, sg, wu, su = (q[k].numpy() for k in ("wg", "sg", "wu", "su"))
+    xq = synth.bf16_bits(q["x"])
+    y, ya = oracle.gemv_gate_up(wg, sg, q["gg"], wu, su, q["gu"], xq, lib=lib)
+    xv = torch_bf16(xq)
+    refg = np.concatenate([q["gg"] * (xv @ dequant(wg, sg).T), q["gu"] * (xv @ dequant(wu, su).T)], 1)
+    if not np.all(np.abs(y - refg) <= 1e-12 * np.maximum(ya, 1e-300)):
+        fails.append("gate_up")
+    for xps in (False, True):
+        r = synth.moe_problem(9, 16, 48, 3, 3, xps, seed=53)
+        wm, sm, gs, ids = r["w"].numpy(), r["s"].numpy(), r["gs"].numpy(), r["ids"].numpy()
+        xm = synth.bf16_bits(r["x"])
+        y, ya, _ = oracle.moe_gemv(wm, sm, gs, ids, xm, xps, 3, lib=lib)
+        xv = torch_bf16(xm)
+        for sl in range(9):
+            e = ids[sl]
+            refm = float(gs[e]) * (dequant(wm[e], sm[e]) @ xv[sl if xps else sl // 3])
+            if not np.all(np.abs(y[sl] - refm) <= 1e-12 * np.maximum(ya[sl], 1e-300)):
+                fails.append(f"moe(x_per_slot={xps})")
+                break
+    return fails
+
+
+def test_unmodified_oracle_passes_battery():
+    assert battery(oracle.load()) == []
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, tmp_path):
+    old, new, count = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) >= count, f"mutation site for {name} not found"
+    mutated = src.replace(old, new, count)
+    path = tmp_path / f"mutant_{name}.c"
+    path.write_text(mutated)
+    so = str(tmp_path / f"libmutant_{name}.so")
+    subprocess.run(["gcc", "-O1", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-o", so, str(path),
+                    "-lm"], check=True, capture_output=True)
+    fails = battery(oracle.load(so))
+    assert fails, f"mutant {name} passed every pin"
