@@ -1,0 +1,161 @@
+/*
+ * nvfp4_gemv.h: C ABI of the NVFP4 (nvfp4/g16) weight-only GEMV library for GB300 (sm_103a).
+ *
+ * Operation (all entry points):
+ *
+ *     y[m, n] = g * sum_k E2M1(q[n, k]) * E4M3(s[n, k / 16]) * x[m, k]
+ *
+ * The weight is NVFP4: 4-bit E2M1 codes with one E4M3 block scale per 16 consecutive
+ * weights along K, plus one FP32 scale g per weight tensor. The activation x is bf16.
+ * Accumulation is in fp32 and the output is fp32 or bf16. Sources:
+ *   - "glm-5.3-flash-nvfp4-tp3-512k--gb10 card.json", performance[4], [6], [8], [9] and
+ *     [33], field `note`: the W4A16 GEMV kernels read an NVFP4 weight (E2M1 elements and a
+ *     UE4M3 scale per 16) and a BF16 activation;
+ *   - "glm-5.3-flash-nvfp4-tp3-512k--gb10 graph.json", node l0.kda.q, `steps`: bf16
+ *     activation; the nvfp4/g16 weight is widened to bf16; bf16 x bf16 products are
+ *     accumulated in f32; an f32 scale is applied last;
+ *   - "GLM-5.3-Flash-NVFP4" blueprint page, section Precision: nvfp4/g16 weight with
+ *     bf16 activation is the most common weighted-node format.
+ *
+ * Layout (a reading: the pages fix none of it):
+ *   - w_packed [N, K/2] bytes, row-major. Element 2j of a row is the LOW nibble of byte j.
+ *   - w_scales [N, K/16] bytes, row-major, no swizzle. Byte b covers elements 16b..16b+15.
+ *   - x [M, K] bf16 (passed as uint16 bit patterns), row-major, rows K elements apart.
+ *   - y [M, ldy] with ldy = N (gate_up: 2N; MoE: one row of N per slot), fp32 or bf16.
+ *   - Scale codes 0x7F and 0xFF are NaN and propagate to their output column.
+ *
+ * Ownership and execution:
+ *   - Every pointer is caller-owned DEVICE memory on the current CUDA device, except
+ *     where a comment says otherwise. The library frees nothing it did not allocate.
+ *   - A call allocates no memory and does not synchronise. It validates its arguments on
+ *     the host, enqueues its kernel(s) on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and returns. Calls can be captured into CUDA graphs.
+ *   - Shapes: 0 <= M <= 8, N >= 0, K >= 0, K % 16 == 0. M == 0, N == 0 or an empty MoE
+ *     routing launch nothing. K == 0 sets y to zero.
+ *   - Fast path: w/s base pointers 16-byte aligned and K % 32 == 0. Anything else runs a
+ *     slower kernel with byte loads, which gives the same results within tolerance.
+ *
+ * Errors: a non-zero nvfp4_status is returned before anything is enqueued, except
+ * NVFP4_ERR_CUDA (a launch error reported by the runtime after the launch). Problems that
+ * are only visible on the device (an out-of-range expert id, a pipeline wait that ran
+ * past its time budget) never trap. They set bits in a device status word that
+ * nvfp4_device_status() reads, and they leave the affected outputs unspecified (bad ids:
+ * zero).
+ */
+#ifndef NVFP4_GEMV_H_
+#define NVFP4_GEMV_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    NVFP4_OK = 0,
+    NVFP4_ERR_NULL = 1,        /* a required pointer is NULL */
+    NVFP4_ERR_SHAPE = 2,       /* M > 8, negative size, K % 16 != 0, top_k/T/E invalid */
+    NVFP4_ERR_ALIGN = 3,       /* reserved: misalignment is handled by the byte-load kernel */
+    NVFP4_ERR_DTYPE = 4,       /* y_type is not one of nvfp4_out_t */
+    NVFP4_ERR_UNSUPPORTED = 5, /* a size beyond what any kernel here can take */
+    NVFP4_ERR_CUDA = 6,        /* the CUDA runtime reported an error (see nvfp4_last_cuda_error) */
+    NVFP4_ERR_TIMEOUT = 7      /* reported by nvfp4_device_status(): a device wait timed out */
+} nvfp4_status;
+
+typedef enum {
+    NVFP4_OUT_F32 = 0,
+    NVFP4_OUT_BF16 = 1         /* round to nearest even from the fp32 result */
+} nvfp4_out_t;
+
+/* Device status bits (see nvfp4_device_status). */
+#define NVFP4_DEV_TIMEOUT 1    /* a pipeline wait exceeded its time budget; y unspecified */
+#define NVFP4_DEV_BAD_EXPERT 2 /* an expert id outside [0, E); those slots are zero */
+
+/*
+ * Dense GEMV: y[M, N] = g * W[N, K] . x[M, K]^T (per element as above).
+ *   w_packed [N, K/2] u8, w_scales [N, K/16] u8, global_scale = g (by value),
+ *   x [M, K] bf16 bits, y [M, N] of y_type.
+ * This is the M = 1..8 decode projection GEMV (w4a16_gemv_pipe_m1/_m2 family,
+ * "glm-5.3-flash-nvfp4-tp3-512k--gb10 card.json" performance[6], [8]), for example
+ * attention projections of the shapes in "llama.cpp eval-callback — ggml op level"
+ * (MUL_MAT attn_q {4096, 4096}, attn_k/attn_v {4096, 1024}).
+ */
+nvfp4_status nvfp4_gemv(const uint8_t* w_packed, const uint8_t* w_scales, float global_scale,
+                        const uint16_t* x, void* y, nvfp4_out_t y_type,
+                        int M, int N, int K, void* stream);
+
+/*
+ * Gate and up projections in one launch (the fused "gate|up N=768+768" projection of
+ * "glm-5.3-flash-nvfp4-tp3-512k--gb10 card.json" performance[9]):
+ *   y[m, 0:N]  = g_gate * W_gate . x[m],   y[m, N:2N] = g_up * W_up . x[m].
+ * Each weight is [N, K/2] + [N, K/16] with its own global scale. y is [M, 2N].
+ */
+nvfp4_status nvfp4_gemv_gate_up(const uint8_t* w_gate, const uint8_t* s_gate, float g_gate,
+                                const uint8_t* w_up, const uint8_t* s_up, float g_up,
+                                const uint16_t* x, void* y, nvfp4_out_t y_type,
+                                int M, int N, int K, void* stream);
+
+/*
+ * Routed-expert GEMV over slots (w4a16_gemv_sw_moe, "glm-5.3-flash-nvfp4-tp3-512k--gb10
+ * card.json" performance[33]: routed gate or up, 8 slots). For slot s = t*top_k + j
+ * (token-major), with e = expert_ids[s]:
+ *     y[s, n] = global_scales[e] * sum_k W_e[n, k] * x[r, k],  r = s if x_per_slot else t.
+ *   w_packed [E, N, K/2], w_scales [E, N, K/16]: all experts' weights back to back.
+ *   global_scales [E] f32 (device), expert_ids [T*top_k] int32 (device).
+ *   x [T, K] (x_per_slot = 0: gate/up, shared by a token's slots) or [T*top_k, K]
+ *   (x_per_slot = 1: down, one row per slot). y [T*top_k, N].
+ * Slots routed to the same expert are served from one read of that expert's weights
+ * (the union of the routed experts, as in glm5next_moe_row_union, card performance[31]).
+ * An id outside [0, E) zeroes its slot's row and sets NVFP4_DEV_BAD_EXPERT in the device
+ * status word and, if status_dev is not NULL, in *status_dev (device int32, OR-ed in).
+ */
+nvfp4_status nvfp4_moe_gemv(const uint8_t* w_packed, const uint8_t* w_scales,
+                            const float* global_scales, int E,
+                            const int32_t* expert_ids, int T, int top_k,
+                            const uint16_t* x, int x_per_slot,
+                            void* y, nvfp4_out_t y_type, int N, int K,
+                            int32_t* status_dev, void* stream);
+
+/* Human-readable name of a status code. The returned string is static. */
+const char* nvfp4_status_string(int status);
+
+/* The last CUDA runtime error code seen by this library in the calling process (0 = none). */
+int nvfp4_last_cuda_error(void);
+
+/*
+ * Reads and clears the library's device status word for the current device. It
+ * synchronises `stream` first. *flags_out (host memory) receives NVFP4_DEV_* bits.
+ * Returns NVFP4_OK, NVFP4_ERR_TIMEOUT if the timeout bit was set, or NVFP4_ERR_CUDA.
+ */
+nvfp4_status nvfp4_device_status(int32_t* flags_out, void* stream);
+
+/*
+ * Time budget of every device-side pipeline wait, in nanoseconds (process-wide; default
+ * 1e9). A wait that runs past it makes the kernel set NVFP4_DEV_TIMEOUT, drain the copies
+ * it has in flight and return. Passing 0 forces the timeout path (used by tests).
+ * Passing UINT64_MAX restores the default.
+ */
+void nvfp4_set_wait_budget_ns(uint64_t ns);
+
+/*
+ * Kernel selection (process-wide): 0 = automatic (default), 1 = always the byte-load
+ * kernel. Used by tests to check both kernels against the oracle.
+ */
+void nvfp4_set_variant(int variant);
+
+/*
+ * Describes the launch the next call with these arguments would make. It writes
+ * "kernel grid block smem split rows_per_item k_warps" into buf (host memory, NUL-terminated).
+ * Returns the number of characters, or -1.
+ */
+int nvfp4_describe_plan(int kind /* 0 dense, 1 gate_up, 2 moe */, int M, int N, int K,
+                        int T, int top_k, char* buf, int buflen);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int nvfp4_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NVFP4_GEMV_H_ */

@@ -1,0 +1,244 @@
+"""NVFP4 (nvfp4/g16) weight-only GEMV for GB300: thin Python binding over ``libnvfp4gemv.so``.
+
+Every function here only checks tensors and passes pointers, sizes and the current CUDA
+stream to the C ABI declared in ``include/nvfp4_gemv.h``. All arithmetic runs in that
+library's CUDA kernels. There is no CPU or PyTorch fallback. If the library cannot be
+loaded, every call raises.
+
+Tensors (CUDA, contiguous):
+  w  uint8 [N, K/2]   E2M1 codes, element 2j in the low nibble of byte j
+  s  uint8 [N, K/16]  E4M3 block scales
+  x  bfloat16 [M, K]  activations, M <= 8
+  y  float32 or bfloat16 [M, N]
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+__all__ = ["gemv", "gemv_gate_up", "moe_gemv", "device_status", "set_wait_budget_ns",
+           "set_variant", "describe_plan", "library", "library_path", "NVFP4Error",
+           "OUT_F32", "OUT_BF16", "DEV_TIMEOUT", "DEV_BAD_EXPERT"]
+
+OUT_F32 = 0
+OUT_BF16 = 1
+DEV_TIMEOUT = 1
+DEV_BAD_EXPERT = 2
+
+_lock = threading.Lock()
+_lib = None
+
+
+class NVFP4Error(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def _declare(lib):
+    vp, u8p, u16p = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p
+    i32 = ctypes.c_int
+    lib.nvfp4_gemv.argtypes = [u8p, u8p, ctypes.c_float, u16p, vp, i32, i32, i32, i32, vp]
+    lib.nvfp4_gemv.restype = i32
+    lib.nvfp4_gemv_gate_up.argtypes = [u8p, u8p, ctypes.c_float, u8p, u8p, ctypes.c_float, u16p, vp,
+                                       i32, i32, i32, i32, vp]
+    lib.nvfp4_gemv_gate_up.restype = i32
+    lib.nvfp4_moe_gemv.argtypes = [u8p, u8p, vp, i32, vp, i32, i32, u16p, i32, vp, i32, i32, i32,
+                                   vp, vp]
+    lib.nvfp4_moe_gemv.restype = i32
+    lib.nvfp4_status_string.argtypes = [i32]
+    lib.nvfp4_status_string.restype = ctypes.c_char_p
+    lib.nvfp4_last_cuda_error.argtypes = []
+    lib.nvfp4_last_cuda_error.restype = i32
+    lib.nvfp4_device_status.argtypes = [ctypes.POINTER(ctypes.c_int32), vp]
+    lib.nvfp4_device_status.restype = i32
+    lib.nvfp4_set_wait_budget_ns.argtypes = [ctypes.c_uint64]
+    lib.nvfp4_set_wait_budget_ns.restype = None
+    lib.nvfp4_set_variant.argtypes = [i32]
+    lib.nvfp4_set_variant.restype = None
+    lib.nvfp4_describe_plan.argtypes = [i32, i32, i32, i32, i32, i32, ctypes.c_char_p, i32]
+    lib.nvfp4_describe_plan.restype = i32
+    lib.nvfp4_version.argtypes = []
+    lib.nvfp4_version.restype = i32
+    return lib
+
+
+def library(build_if_missing: bool = True):
+    """The loaded ctypes library (built first when missing or stale and nvcc exists)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.LIB_PATH
+            if build_if_missing and _build.is_stale():
+                try:
+                    _build.build()
+                except RuntimeError:
+                    if not os.path.exists(path):
+                        raise
+            if not os.path.exists(path):
+                raise RuntimeError(f"NVFP4 GEMV CUDA library not found at {path}; run "
+                                   "`python -m nvfp4_weight_only_gemv_gb300.build`")
+            _lib = _declare(ctypes.CDLL(path))
+    return _lib
+
+
+def status_string(status: int) -> str:
+    try:
+        return library(build_if_missing=False).nvfp4_status_string(int(status)).decode()
+    except Exception:  # pragma: no cover
+        return "unknown"
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        raise NVFP4Error(status, what)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _need(t: torch.Tensor, name: str, dtype, ndim: int):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor (got {t.device})")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype} (got {t.dtype})")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims (got {tuple(t.shape)})")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _out(out, shape, out_dtype, device):
+    if out is None:
+        return torch.empty(shape, dtype=out_dtype, device=device)
+    _need(out, "out", out_dtype, len(shape))
+    if tuple(out.shape) != tuple(shape):
+        raise ValueError(f"out must have shape {tuple(shape)} (got {tuple(out.shape)})")
+    return out
+
+
+def _out_code(dtype) -> int:
+    if dtype == torch.float32:
+        return OUT_F32
+    if dtype == torch.bfloat16:
+        return OUT_BF16
+    raise TypeError("out_dtype must be torch.float32 or torch.bfloat16")
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t.numel() else ctypes.c_void_p(t.data_ptr() or 16)
+
+
+def gemv(w: torch.Tensor, s: torch.Tensor, g: float, x: torch.Tensor, out=None,
+         out_dtype=torch.float32, stream=None) -> torch.Tensor:
+    """y[M, N] = g * dequant(w, s) @ x^T on the current (or given) CUDA stream."""
+    _need(w, "w", torch.uint8, 2)
+    _need(s, "s", torch.uint8, 2)
+    _need(x, "x", torch.bfloat16, 2)
+    N, K = w.shape[0], w.shape[1] * 2
+    M = x.shape[0]
+    if tuple(s.shape) != (N, K // 16) or x.shape[1] != K:
+        raise ValueError(f"shape mismatch: w {tuple(w.shape)}, s {tuple(s.shape)}, x {tuple(x.shape)}")
+    y = _out(out, (M, N), out_dtype, x.device)
+    st = library().nvfp4_gemv(_ptr(w), _ptr(s), float(g), _ptr(x), _ptr(y), _out_code(y.dtype),
+                              M, N, K, ctypes.c_void_p(_stream(stream)))
+    _check(st, "nvfp4_gemv")
+    return y
+
+
+def gemv_gate_up(wg, sg, gg, wu, su, gu, x, out=None, out_dtype=torch.float32,
+                 stream=None) -> torch.Tensor:
+    """y[M, 2N] = [gg * W_gate . x | gu * W_up . x] in one launch."""
+    for t, n in ((wg, "w_gate"), (wu, "w_up")):
+        _need(t, n, torch.uint8, 2)
+    for t, n in ((sg, "s_gate"), (su, "s_up")):
+        _need(t, n, torch.uint8, 2)
+    _need(x, "x", torch.bfloat16, 2)
+    N, K = wg.shape[0], wg.shape[1] * 2
+    M = x.shape[0]
+    if tuple(wu.shape) != tuple(wg.shape) or tuple(sg.shape) != (N, K // 16) or \
+            tuple(su.shape) != (N, K // 16) or x.shape[1] != K:
+        raise ValueError("shape mismatch between gate, up and x")
+    y = _out(out, (M, 2 * N), out_dtype, x.device)
+    st = library().nvfp4_gemv_gate_up(_ptr(wg), _ptr(sg), float(gg), _ptr(wu), _ptr(su), float(gu),
+                                      _ptr(x), _ptr(y), _out_code(y.dtype), M, N, K,
+                                      ctypes.c_void_p(_stream(stream)))
+    _check(st, "nvfp4_gemv_gate_up")
+    return y
+
+
+def moe_gemv(w, s, gs, ids, x, x_per_slot: bool, top_k: int, out=None, out_dtype=torch.float32,
+             status=None, stream=None) -> torch.Tensor:
+    """Routed-expert GEMV: y[T*top_k, N]; slot t*top_k+j uses expert ids[t*top_k+j].
+
+    w uint8 [E, N, K/2], s uint8 [E, N, K/16], gs float32 [E], ids int32 [T*top_k],
+    x bf16 [T, K] (x_per_slot False) or [T*top_k, K] (True). ``status`` is an optional
+    int32 CUDA tensor of one element that receives device status bits.
+    """
+    _need(w, "w", torch.uint8, 3)
+    _need(s, "s", torch.uint8, 3)
+    _need(gs, "global_scales", torch.float32, 1)
+    _need(ids, "expert_ids", torch.int32, 1)
+    _need(x, "x", torch.bfloat16, 2)
+    E, N, K = w.shape[0], w.shape[1], w.shape[2] * 2
+    slots = ids.shape[0]
+    if top_k <= 0 or slots % top_k:
+        raise ValueError("expert_ids length must be a multiple of top_k")
+    T = slots // top_k
+    rows = slots if x_per_slot else T
+    if tuple(s.shape) != (E, N, K // 16) or gs.shape[0] != E or tuple(x.shape) != (rows, K):
+        raise ValueError("shape mismatch in moe_gemv arguments")
+    if status is not None:
+        _need(status, "status", torch.int32, 1)
+    y = _out(out, (slots, N), out_dtype, x.device)
+    st = library().nvfp4_moe_gemv(_ptr(w), _ptr(s), _ptr(gs), E, _ptr(ids), T, top_k, _ptr(x),
+                                  int(bool(x_per_slot)), _ptr(y), _out_code(y.dtype), N, K,
+                                  ctypes.c_void_p(status.data_ptr()) if status is not None else None,
+                                  ctypes.c_void_p(_stream(stream)))
+    _check(st, "nvfp4_moe_gemv")
+    return y
+
+
+def device_status(stream=None) -> int:
+    """Synchronise the stream, then read and clear the library's device status bits."""
+    v = ctypes.c_int32(0)
+    st = library().nvfp4_device_status(ctypes.byref(v), ctypes.c_void_p(_stream(stream)))
+    if st not in (0, 7):
+        _check(st, "nvfp4_device_status")
+    return int(v.value)
+
+
+def set_wait_budget_ns(ns) -> None:
+    """Budget of every device pipeline wait (None restores the default of 1 s)."""
+    library().nvfp4_set_wait_budget_ns(ctypes.c_uint64((1 << 64) - 1 if ns is None else int(ns)))
+
+
+def set_variant(variant: int) -> None:
+    """0 = automatic kernel choice, 1 = force the byte-load kernel."""
+    library().nvfp4_set_variant(int(variant))
+
+
+def describe_plan(kind: str, M: int, N: int, K: int, T: int = 0, top_k: int = 0) -> str:
+    """Launch the library would pick: kind in {"dense", "gate_up", "moe"}."""
+    code = {"dense": 0, "gate_up": 1, "moe": 2}[kind]
+    buf = ctypes.create_string_buffer(256)
+    n = library().nvfp4_describe_plan(code, M, N, K, T, top_k, buf, 256)
+    if n < 0:
+        raise RuntimeError("describe_plan failed (no CUDA device?)")
+    return buf.value.decode()

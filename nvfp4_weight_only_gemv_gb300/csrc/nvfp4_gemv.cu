@@ -1,0 +1,1267 @@
+// NVFP4 (nvfp4/g16) weight-only GEMV for GB300 (sm_103a): kernels and the C ABI.
+//
+//   y[m, n] = g * sum_k E2M1(q[n, k]) * E4M3(s[n, k / 16]) * x[m, k]      (m < M <= 8)
+//
+// This is the decode-time W4A16 projection GEMV ("glm-5.3-flash-nvfp4-tp3-512k--gb10
+// card.json", performance[6], [8], [9], [33]: W4A16 NVFP4 weight with E2M1 elements and
+// a UE4M3 scale per 16, BF16 activation). Each term follows node l0.kda.q of
+// "glm-5.3-flash-nvfp4-tp3-512k--gb10 graph.json": the weight is widened, multiplied by
+// the bf16 activation and accumulated in f32, and the f32 tensor scale is applied last.
+//
+// Design (a bandwidth-bound GEMV at M <= 8, so CUDA cores rather than tensor cores):
+//   * One persistent CTA per SM. The grid is sized from the SM count and covers a
+//     balanced, contiguous block of "items" (an item is up to 32 KB of whole weight rows).
+//   * Warp 8 (producer): streams each item's packed codes and scales from HBM into a
+//     4-stage shared-memory ring with cp.async.bulk (TMA bulk copies) that complete on
+//     per-stage mbarriers.
+//   * Warps 0..7 (consumers): x is staged once per CTA in shared memory as fp32, in a
+//     layout without bank conflicts. Each lane decodes 32 weights per step with
+//     cvt.rn.f16x2.e2m1x2, widens them times the block scale with the mixed-precision
+//     fma.rn.f32.f16, and accumulates with packed fma.rn.f32x2 in fp32.
+//     A warp-level transposed butterfly reduces R rows x M outputs at once.
+//   * Warp 9 (epilogue): adds the per-warp partials in a fixed order (deterministic),
+//     applies g and stores fp32 or bf16 (round to nearest even).
+//   * When fp32 x does not fit next to the ring (large M * K), K is split across a thread
+//     block cluster of S CTAs. Each CTA keeps partial sums for its rows, and after a
+//     cluster barrier the partials are summed over DSMEM (ld.shared::cluster).
+//   * Every mbarrier wait is bounded by a %globaltimer budget. On expiry the kernel sets
+//     a device status bit, waits for the copies it has in flight and returns: it never traps.
+//   * A plain byte-load kernel covers shapes and alignments that the bulk-copy path does
+//     not take (K % 32 != 0, unaligned base pointers, very large M * K, > 256 MoE slots).
+
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <cuda_bf16.h>
+
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <algorithm>
+#include <mutex>
+
+#include "nvfp4_gemv.h"
+
+namespace nvfp4 {
+
+constexpr int kConsumerWarps = 8;
+constexpr int kProducerWarp = kConsumerWarps;
+constexpr int kEpilogueWarp = kConsumerWarps + 1;
+constexpr int kThreads = (kConsumerWarps + 2) * 32;
+constexpr int kStages = 4;
+constexpr int kStageData = 32 * 1024;      // weight bytes (codes + scales) per stage
+constexpr int kStageStride = kStageData + 128;  // + room for an unaligned scale head
+constexpr int kStepElems = 1024;           // K elements per warp step (32 lanes x 32)
+constexpr int kMaxMoeSlots = 256;
+constexpr int kSimpleThreads = 256;
+constexpr uint64_t kDefaultWaitNs = 1000000000ull;
+constexpr uint64_t kDrainWaitNs = 2000000000ull;
+
+enum : int { kModeDense = 0, kModeMoe = 1 };
+
+__device__ int g_device_status;
+
+// ------------------------------------------------------------------ parameters
+
+struct Params {
+    const uint8_t* w[2];      // dense: weight codes per group (gate, up); MoE: w[0] = all experts
+    const uint8_t* s[2];      // scales, same layout
+    float g[2];               // dense global scales
+    const float* g_dev;       // MoE per-expert global scales
+    const int32_t* ids;       // MoE expert ids [slots]
+    int32_t* status_user;     // MoE optional status word
+    const uint16_t* x;        // bf16 bits
+    void* y;
+    int64_t ldy;              // output row stride in elements
+    int out_bf16;
+    int M, N, K;
+    int groups;               // dense: 1 or 2
+    int E, T, top_k, x_per_slot, slots;
+    int S, Kr, J;             // K split (cluster size), K per CTA, warp steps per CTA K-range
+    int rpi, chunks, items;   // rows per item, items per group, items in total (dense)
+    int ck, cr;               // consumer warps along K and along rows
+    int mstride;              // partial-sum stride per row (>= max rows of x per item)
+    int cl_rows;              // rows of the cluster partial buffer (S > 1)
+    uint32_t x_off, red_off, cl_off, bar_off, tab_off;
+    uint64_t wait_ns;
+};
+
+struct MoeTables {
+    int n_groups;
+    int pad_[3];
+    int expert[kMaxMoeSlots];
+    int count[kMaxMoeSlots];
+    int first[kMaxMoeSlots];                  // index into member_list
+    int member_list[kMaxMoeSlots];            // slots grouped by expert, slot order
+};
+
+// ------------------------------------------------------------------ PTX helpers
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;"
+                 ::"r"(smem_addr(bar)), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n"
+        " mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok) : "r"(smem_addr(bar)), "r"(parity) : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Bounded wait for the phase with the given parity; false when the budget ran out.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t budget_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (global_ns() - t0 > budget_ns) return false;
+    }
+}
+
+// TMA bulk copy global -> shared (this CTA), completion counted in bytes on `bar`.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+    return v;
+}
+
+__device__ __forceinline__ float4 lds128f(uint32_t a) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(a));
+    return v;
+}
+
+__device__ __forceinline__ uint16_t lds16(uint32_t a) {
+    uint16_t v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
+    return v;
+}
+
+__device__ __forceinline__ void bar_sync_consumers() {
+    asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ float ld_cluster_f32(const float* local, uint32_t rank) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(local)), "r"(rank));
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+    return v;
+}
+
+// Four E2M1 pairs (one 32-bit word, 8 codes; element 2i in the low nibble of byte i) ->
+// four f16x2 (low half = even element). Exact: every E2M1 value is an f16.
+__device__ __forceinline__ void cvt_e2m1x8(uint32_t w, uint32_t (&h)[4]) {
+    asm("{\n .reg .b8 b0, b1, b2, b3;\n"
+        " mov.b32 {b0, b1, b2, b3}, %4;\n"
+        " cvt.rn.f16x2.e2m1x2 %0, b0;\n"
+        " cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+        " cvt.rn.f16x2.e2m1x2 %2, b2;\n"
+        " cvt.rn.f16x2.e2m1x2 %3, b3;\n}"
+        : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3]) : "r"(w));
+}
+
+// Two E4M3 scale codes (low byte = first block) -> f16x2. Exact: E4M3 values are f16s.
+__device__ __forceinline__ uint32_t cvt_e4m3x2(uint16_t v) {
+    uint32_t d;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(d) : "h"(v));
+    return d;
+}
+
+// (lo(h2) * s, hi(h2) * s) in fp32. E2M1 * E4M3 has at most 6 significant bits, so the
+// products are exact: this is the weight widened to full precision.
+__device__ __forceinline__ float2 widen_scaled(uint32_t h2, uint16_t s) {
+    float2 r;
+    asm("{\n .reg .f16 a, b;\n"
+        " mov.b32 {a, b}, %2;\n"
+        " fma.rn.f32.f16 %0, a, %3, 0f00000000;\n"
+        " fma.rn.f32.f16 %1, b, %3, 0f00000000;\n}"
+        : "=f"(r.x), "=f"(r.y) : "r"(h2), "h"(s));
+    return r;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
+
+__device__ __forceinline__ void store_out(void* y, int64_t idx, float v, int out_bf16) {
+    if (out_bf16) {
+        reinterpret_cast<__nv_bfloat16*>(y)[idx] = __float2bfloat16_rn(v);
+    } else {
+        reinterpret_cast<float*>(y)[idx] = v;
+    }
+}
+
+__device__ __forceinline__ void raise_status(int bits, int32_t* user) {
+    atomicOr(&g_device_status, bits);
+    if (user) atomicOr(reinterpret_cast<int*>(user), bits);
+}
+
+// ------------------------------------------------------------------ warp reduction
+
+// Transposed butterfly: each lane starts with CNT partials; after the call the sums over
+// the 32 lanes are spread across lanes (see lane_owned_*). CNT must be a power of two.
+template <int CNT, int O>
+__device__ __forceinline__ void reduce_scatter(float* v, int lane) {
+    if constexpr (O > 0) {
+        if constexpr (CNT > 1) {
+            constexpr int H = CNT / 2;
+            const bool up = (lane & O) != 0;
+#pragma unroll
+            for (int i = 0; i < H; ++i) {
+                const float send = up ? v[i] : v[i + H];
+                const float keep = up ? v[i + H] : v[i];
+                v[i] = keep + __shfl_xor_sync(0xffffffffu, send, O);
+            }
+            reduce_scatter<H, O / 2>(v, lane);
+        } else {
+            v[0] += __shfl_xor_sync(0xffffffffu, v[0], O);
+            reduce_scatter<1, O / 2>(v, lane);
+        }
+    }
+}
+
+__host__ __device__ constexpr int next_pow2(int v) { return v <= 1 ? 1 : 2 * next_pow2((v + 1) / 2); }
+__host__ __device__ constexpr int ilog2(int v) { return v <= 1 ? 0 : 1 + ilog2(v / 2); }
+
+// ------------------------------------------------------------------ x staging
+
+// fp32 position of element k (within the CTA's K range) in the staged x row. For warp
+// step j, lane l and word w, elements [4h, 4h + 4) of that word sit at
+// ((j * 8 + w * 2 + h) * 32 + l) * 4: a warp's 128-bit reads cover 512 contiguous bytes.
+__device__ __forceinline__ int x_pos(int k) {
+    return ((((k >> 10) * 8 + ((k >> 3) & 3) * 2) * 32) + ((k >> 5) & 31)) * 4 + (k & 3);
+}
+
+// Converts rows of bf16 x (global) to fp32 in shared memory. src_row(m) gives the global
+// row index for staged row m. Shared by the consumer threads: tid in [0, nthreads).
+template <typename RowFn>
+__device__ void stage_x(const uint16_t* __restrict__ x, int64_t K, int k0, int Kr, int rows,
+                        RowFn src_row, float* x32, int xstride, int tid, int nthreads) {
+    const int per_row = Kr / 8;
+    const int total = rows * per_row;
+    const bool vec = (reinterpret_cast<uintptr_t>(x) & 15) == 0;
+    for (int c = tid; c < total; c += nthreads) {
+        const int m = c / per_row;
+        const int k = (c - m * per_row) * 8;
+        const uint16_t* src = x + static_cast<int64_t>(src_row(m)) * K + k0 + k;
+        uint32_t u[4];
+        if (vec) {
+            const uint4 t = __ldg(reinterpret_cast<const uint4*>(src));
+            u[0] = t.x; u[1] = t.y; u[2] = t.z; u[3] = t.w;
+        } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) u[i] = src[2 * i] | (static_cast<uint32_t>(src[2 * i + 1]) << 16);
+        }
+        float* dst = x32 + static_cast<int64_t>(m) * xstride + x_pos(k);
+        reinterpret_cast<float4*>(dst)[0] = make_float4(bf16_lo(u[0]), bf16_hi(u[0]), bf16_lo(u[1]), bf16_hi(u[1]));
+        reinterpret_cast<float4*>(dst + 128)[0] = make_float4(bf16_lo(u[2]), bf16_hi(u[2]), bf16_lo(u[3]), bf16_hi(u[3]));
+    }
+}
+
+// ------------------------------------------------------------------ consumer compute
+
+// One item's share of one consumer warp: rows rb = wr*R, wr*R + cr*R, ... (batches of R)
+// and warp steps j = wk, wk + ck, ... Partials go to red[(wk * rpi + row) * mstride + m].
+template <int MTE, int R>
+__device__ __forceinline__ void compute_item(uint32_t wst, uint32_t sst, int wrow_bytes, int srow_bytes,
+                                             uint32_t x32, int xstride_bytes, int rows, int Kr, int J,
+                                             int wr, int wk, int cr, int ck, int lane,
+                                             float* red, int rpi, int mstride) {
+    constexpr int V = R * MTE;
+    constexpr int VP = next_pow2(V);
+    for (int rb = wr * R; rb < rows; rb += cr * R) {
+        float2 acc[R][MTE];
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int m = 0; m < MTE; ++m) acc[r][m] = make_float2(0.f, 0.f);
+
+        for (int j = wk; j < J; j += ck) {
+            const int kl = j * kStepElems + lane * 32;
+            if (kl < Kr) {
+                uint4 wv[R];
+                uint32_t sh[R];
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    const int row = rb + r;
+                    if (row < rows) {
+                        wv[r] = lds128(wst + row * wrow_bytes + (kl >> 1));
+                        sh[r] = cvt_e4m3x2(lds16(sst + row * srow_bytes + (kl >> 4)));
+                    } else {
+                        wv[r] = make_uint4(0u, 0u, 0u, 0u);
+                        sh[r] = 0u;
+                    }
+                }
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    float2 xp[MTE][4];
+#pragma unroll
+                    for (int m = 0; m < MTE; ++m) {
+                        const uint32_t xa = x32 + m * xstride_bytes + (((j * 8 + w * 2) * 32 + lane) << 4);
+                        const float4 a = lds128f(xa);
+                        const float4 b = lds128f(xa + 32 * 16);
+                        xp[m][0] = make_float2(a.x, a.y);
+                        xp[m][1] = make_float2(a.z, a.w);
+                        xp[m][2] = make_float2(b.x, b.y);
+                        xp[m][3] = make_float2(b.z, b.w);
+                    }
+#pragma unroll
+                    for (int r = 0; r < R; ++r) {
+                        const uint32_t word = w == 0 ? wv[r].x : (w == 1 ? wv[r].y : (w == 2 ? wv[r].z : wv[r].w));
+                        const uint16_t sc = static_cast<uint16_t>(w < 2 ? (sh[r] & 0xffffu) : (sh[r] >> 16));
+                        uint32_t h[4];
+                        cvt_e2m1x8(word, h);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const float2 q = widen_scaled(h[i], sc);
+#pragma unroll
+                            for (int m = 0; m < MTE; ++m) acc[r][m] = __ffma2_rn(q, xp[m][i], acc[r][m]);
+                        }
+                    }
+                }
+            }
+        }
+
+        float v[VP];
+#pragma unroll
+        for (int i = 0; i < VP; ++i) v[i] = i < V ? acc[i / MTE][i % MTE].x + acc[i / MTE][i % MTE].y : 0.f;
+        reduce_scatter<VP, 16>(v, lane);
+        if constexpr (VP >= 32) {
+#pragma unroll
+            for (int i = 0; i < VP / 32; ++i) {
+                const int idx = lane * (VP / 32) + i;
+                if (idx < V) {
+                    const int row = rb + idx / MTE;
+                    if (row < rows) red[(wk * rpi + row) * mstride + idx % MTE] = v[i];
+                }
+            }
+        } else {
+            constexpr int sh = 5 - ilog2(VP);
+            if ((lane & ((1 << sh) - 1)) == 0) {
+                const int idx = lane >> sh;
+                if (idx < V) {
+                    const int row = rb + idx / MTE;
+                    if (row < rows) red[(wk * rpi + row) * mstride + idx % MTE] = v[0];
+                }
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------ item bookkeeping
+
+struct Item {
+    int group;   // dense: weight tensor (0 gate / 1 up); MoE: expert group
+    int row0;
+    int rows;
+};
+
+__device__ __forceinline__ Item item_at(const Params& p, int it) {
+    Item r;
+    r.group = it / p.chunks;
+    r.row0 = (it - r.group * p.chunks) * p.rpi;
+    r.rows = min(p.rpi, p.N - r.row0);
+    return r;
+}
+
+// MoE: expert groups from the routing (same result in every CTA). A group is up to
+// p.mstride slots routed to one expert; slots of one expert are served by one read.
+__device__ void build_moe_tables(const Params& p, MoeTables* tab, int* scratch) {
+    const int tid = threadIdx.x;
+    int* ids = scratch;                       // [slots]
+    int* ngr = scratch + kMaxMoeSlots;        // groups opened by slot t (leaders only)
+    int* cnt = scratch + 2 * kMaxMoeSlots;    // members of leader t
+    for (int t = tid; t < p.slots; t += blockDim.x) ids[t] = __ldg(p.ids + t);
+    __syncthreads();
+    for (int t = tid; t < p.slots; t += blockDim.x) {
+        const int id = ids[t];
+        const bool valid = id >= 0 && id < p.E;
+        bool leader = valid;
+        for (int u = 0; u < t && leader; ++u) leader = ids[u] != id;
+        int c = 0;
+        if (leader)
+            for (int u = t; u < p.slots; ++u) c += ids[u] == id;
+        cnt[t] = c;
+        ngr[t] = leader ? (c + p.mstride - 1) / p.mstride : 0;
+        if (!valid && blockIdx.x == 0) {
+            raise_status(NVFP4_DEV_BAD_EXPERT, p.status_user);
+            for (int n = 0; n < p.N; ++n) store_out(p.y, static_cast<int64_t>(t) * p.ldy + n, 0.f, p.out_bf16);
+        }
+    }
+    __syncthreads();
+    if (tid < 32) {
+        // exclusive scan of ngr over slots, 8 slots per lane
+        int local[8];
+        int sum = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int t = tid * 8 + i;
+            local[i] = t < p.slots ? ngr[t] : 0;
+            sum += local[i];
+        }
+        int incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (tid >= o) incl += v;
+        }
+        int run = incl - sum;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int t = tid * 8 + i;
+            if (t < p.slots) ngr[t] = run;  // now: first group index of leader t
+            run += local[i];
+        }
+        if (tid == 31) tab->n_groups = incl;
+    }
+    __syncthreads();
+    for (int t = tid; t < p.slots; t += blockDim.x) {
+        int c = cnt[t];
+        if (c == 0) continue;
+        const int id = ids[t];
+        // members of expert id in slot order, written from member_list[first of group]
+        int g = ngr[t];
+        int in_group = 0;
+        int pos = 0;
+        // the member list of this leader occupies a contiguous run; its start is the
+        // number of valid slots whose expert's leader comes before t, found by counting
+        // members of earlier leaders.
+        for (int u = 0; u < t; ++u) pos += cnt[u];
+        for (int u = t; u < p.slots; ++u) {
+            if (ids[u] != id) continue;
+            if (in_group == 0) {
+                tab->expert[g] = id;
+                tab->first[g] = pos;
+                tab->count[g] = min(p.mstride, c);
+            }
+            tab->member_list[pos++] = u;
+            if (++in_group == p.mstride) {
+                in_group = 0;
+                c -= p.mstride;
+                ++g;
+            }
+        }
+    }
+    __syncthreads();
+}
+
+// ------------------------------------------------------------------ the streaming kernel
+
+template <int MODE, int MT, int R>
+__global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const __grid_constant__ Params p) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.bar_off);
+    uint64_t* full = bars;
+    uint64_t* empty = bars + kStages;
+    uint64_t* rfull = bars + 2 * kStages;
+    uint64_t* rempty = bars + 3 * kStages;
+    uint64_t* xready = bars + 4 * kStages;
+    uint64_t* xfree = bars + 4 * kStages + 1;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 4 * kStages + 2);
+    float* x32 = reinterpret_cast<float*>(smem + p.x_off);
+    float* red_base = reinterpret_cast<float*>(smem + p.red_off);
+    float* clpart = reinterpret_cast<float*>(smem + p.cl_off);
+    MoeTables* tab = reinterpret_cast<MoeTables*>(smem + p.tab_off);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int rank = p.S > 1 ? static_cast<int>(cluster_rank()) : 0;
+    const int cluster = blockIdx.x / p.S;
+    const int n_clusters = gridDim.x / p.S;
+    const int k0 = rank * p.Kr;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], kConsumerWarps);
+            mbar_init(&rfull[i], kConsumerWarps);
+            mbar_init(&rempty[i], 1);
+        }
+        mbar_init(xready, kConsumerWarps);
+        mbar_init(xfree, kConsumerWarps);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if constexpr (MODE == kModeMoe) {
+        build_moe_tables(p, tab, reinterpret_cast<int*>(red_base));
+    }
+    __syncthreads();
+
+    const int items = MODE == kModeMoe ? tab->n_groups * p.chunks : p.items;
+    const int ib = static_cast<int>(static_cast<int64_t>(items) * cluster / n_clusters);
+    const int ie = static_cast<int>(static_cast<int64_t>(items) * (cluster + 1) / n_clusters);
+    const int64_t Kh = p.K / 2;
+    const int64_t Ks = p.K / 16;
+    const int wrow_bytes = p.S == 1 ? p.K / 2 : p.Kr / 2;
+    const int srow_bytes = p.S == 1 ? p.K / 16 : p.Kr / 16;
+    const uint32_t scale_region = static_cast<uint32_t>(p.rpi) * wrow_bytes;  // multiple of 16
+
+    if (warp == kProducerWarp) {
+        // ---------------- producer: TMA bulk copies into the ring
+        int issued = 0;
+        for (int it = ib; it < ie; ++it) {
+            const int li = it - ib;
+            const int slot = li % kStages;
+            const int use = li / kStages;
+            if (use > 0 && !mbar_wait(&empty[slot], (use - 1) & 1, p.wait_ns)) {
+                *abort_flag = 1;
+                if (lane == 0) raise_status(NVFP4_DEV_TIMEOUT, p.status_user);
+                break;
+            }
+            if (*abort_flag) break;
+            const Item ii = item_at(p, it);
+            const uint8_t* wsrc;
+            const uint8_t* ssrc;
+            if constexpr (MODE == kModeMoe) {
+                const int64_t e = tab->expert[ii.group];
+                wsrc = p.w[0] + (e * p.N + ii.row0) * Kh;
+                ssrc = p.s[0] + (e * p.N + ii.row0) * Ks;
+            } else {
+                wsrc = p.w[ii.group] + static_cast<int64_t>(ii.row0) * Kh;
+                ssrc = p.s[ii.group] + static_cast<int64_t>(ii.row0) * Ks;
+            }
+            uint8_t* wdst = smem + slot * kStageStride;
+            uint8_t* sdst = wdst + scale_region;
+            if (p.S == 1) {
+                const uint32_t wbytes = static_cast<uint32_t>(ii.rows) * wrow_bytes;
+                const uint32_t sbytes = static_cast<uint32_t>(ii.rows) * srow_bytes;
+                const uint32_t mis = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(ssrc) & 15);
+                uint32_t head = (16 - mis) & 15;
+                if (head > sbytes) head = sbytes;
+                const uint32_t mid = (sbytes - head) & ~15u;
+                const uint32_t tail = sbytes - head - mid;
+                // unaligned head/tail scale bytes by plain copies, ordered before the arrive
+                if (lane < head) sdst[mis + lane] = ssrc[lane];
+                if (lane < tail) sdst[mis + head + mid + lane] = ssrc[head + mid + lane];
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&full[slot], wbytes + mid);
+                    bulk_g2s(wdst, wsrc, wbytes, &full[slot]);
+                    if (mid) bulk_g2s(sdst + mis + head, ssrc + head, mid, &full[slot]);
+                }
+            } else {
+                const uint32_t wb = p.Kr / 2, sb = p.Kr / 16;
+                if (lane == 0) mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(ii.rows) * (wb + sb));
+                __syncwarp();
+                for (int r = lane; r < ii.rows; r += 32) {
+                    bulk_g2s(wdst + r * wb, wsrc + r * Kh + k0 / 2, wb, &full[slot]);
+                    bulk_g2s(sdst + r * sb, ssrc + r * Ks + k0 / 16, sb, &full[slot]);
+                }
+            }
+            __syncwarp();
+            issued = li + 1;
+        }
+        if (*abort_flag) {
+            // drain: every slot's latest issued use must complete before the CTA exits
+            for (int li = issued - 1; li >= 0 && li >= issued - kStages; --li) {
+                mbar_wait(&full[li % kStages], (li / kStages) & 1, kDrainWaitNs);
+            }
+        }
+    } else if (warp == kEpilogueWarp) {
+        // ---------------- epilogue: fixed-order sum over K-warps, scale, store
+        int64_t local_row = 0;
+        for (int it = ib; it < ie; ++it) {
+            const int li = it - ib;
+            const int slot = li % kStages;
+            const int use = li / kStages;
+            if (!mbar_wait(&rfull[slot], use & 1, p.wait_ns)) {
+                *abort_flag = 1;
+                if (lane == 0) raise_status(NVFP4_DEV_TIMEOUT, p.status_user);
+                break;
+            }
+            if (*abort_flag) break;
+            const Item ii = item_at(p, it);
+            const float* red = red_base + slot * (p.ck * p.rpi * p.mstride);
+            int mrows = MT;
+            float gsc = 0.f;
+            if constexpr (MODE == kModeMoe) {
+                mrows = tab->count[ii.group];
+                gsc = __ldg(p.g_dev + tab->expert[ii.group]);
+            } else {
+                gsc = p.g[ii.group];
+            }
+            const int total = mrows * ii.rows;
+            for (int idx = lane; idx < total; idx += 32) {
+                const int m = idx / ii.rows;
+                const int r = idx - m * ii.rows;
+                float v = 0.f;
+                for (int c = 0; c < p.ck; ++c) v += red[(c * p.rpi + r) * p.mstride + m];
+                if (p.S > 1) {
+                    clpart[(local_row + r) * p.mstride + m] = v;
+                } else if constexpr (MODE == kModeMoe) {
+                    const int sl = tab->member_list[tab->first[ii.group] + m];
+                    store_out(p.y, static_cast<int64_t>(sl) * p.ldy + ii.row0 + r, gsc * v, p.out_bf16);
+                } else {
+                    store_out(p.y, m * p.ldy + static_cast<int64_t>(ii.group) * p.N + ii.row0 + r, gsc * v, p.out_bf16);
+                }
+            }
+            local_row += ii.rows;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&rempty[slot]);
+        }
+    } else {
+        // ---------------- consumers
+        const int wk = warp % p.ck;
+        const int wr = warp / p.ck;
+        const int ctid = threadIdx.x;  // consumer warps are 0..7
+        const int xstride = p.J * kStepElems;
+        const uint32_t x32a = smem_addr(x32);
+        int cur_key = -1;
+        int key_index = 0;
+        bool ok = true;
+        for (int it = ib; it < ie && ok; ++it) {
+            const int li = it - ib;
+            const int slot = li % kStages;
+            const int use = li / kStages;
+            const Item ii = item_at(p, it);
+            const int key = MODE == kModeMoe ? ii.group : 0;
+            if (key != cur_key) {
+                // hand over the x buffer: all consumers done with the old rows, then restage
+                if (cur_key >= 0) {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(xfree);
+                    if (!mbar_wait(xfree, (key_index - 1) & 1, p.wait_ns)) { ok = false; break; }
+                }
+                if constexpr (MODE == kModeMoe) {
+                    const int first = tab->first[key];
+                    const int cnt = tab->count[key];
+                    const int tk = p.top_k;
+                    const bool per_slot = p.x_per_slot != 0;
+                    stage_x(p.x, p.K, k0, p.Kr, cnt,
+                            [&](int m) { const int sl = tab->member_list[first + m]; return per_slot ? sl : sl / tk; },
+                            x32, xstride, ctid, kConsumerWarps * 32);
+                } else {
+                    stage_x(p.x, p.K, k0, p.Kr, p.M, [](int m) { return m; }, x32, xstride, ctid,
+                            kConsumerWarps * 32);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(xready);
+                if (!mbar_wait(xready, key_index & 1, p.wait_ns)) { ok = false; break; }
+                cur_key = key;
+                ++key_index;
+            }
+            if (!mbar_wait(&full[slot], use & 1, p.wait_ns)) { ok = false; break; }
+            if (use > 0 && !mbar_wait(&rempty[slot], (use - 1) & 1, p.wait_ns)) { ok = false; break; }
+            if (*abort_flag) { ok = false; break; }
+
+            const uint32_t wst = smem_addr(smem + slot * kStageStride);
+            uint32_t sst = wst + scale_region;
+            if (p.S == 1) {
+                const uint8_t* ssrc;
+                if constexpr (MODE == kModeMoe) {
+                    ssrc = p.s[0] + (static_cast<int64_t>(tab->expert[ii.group]) * p.N + ii.row0) * Ks;
+                } else {
+                    ssrc = p.s[ii.group] + static_cast<int64_t>(ii.row0) * Ks;
+                }
+                sst += static_cast<uint32_t>(reinterpret_cast<uintptr_t>(ssrc) & 15);
+            }
+            float* red = red_base + slot * (p.ck * p.rpi * p.mstride);
+            if constexpr (MODE == kModeMoe) {
+                const int cnt = tab->count[ii.group];
+                switch (cnt) {
+#define NVFP4_MOE_CASE(C)                                                                              \
+    case C:                                                                                            \
+        if constexpr (C <= MT)                                                                         \
+            compute_item<C, R>(wst, sst, wrow_bytes, srow_bytes, x32a, xstride * 4, ii.rows, p.Kr, p.J,  \
+                               wr, wk, p.cr, p.ck, lane, red, p.rpi, p.mstride);                       \
+        break;
+                    NVFP4_MOE_CASE(1)
+                    NVFP4_MOE_CASE(2)
+                    NVFP4_MOE_CASE(3)
+                    NVFP4_MOE_CASE(4)
+                    NVFP4_MOE_CASE(5)
+                    NVFP4_MOE_CASE(6)
+                    NVFP4_MOE_CASE(7)
+                    NVFP4_MOE_CASE(8)
+#undef NVFP4_MOE_CASE
+                    default: break;
+                }
+            } else {
+                compute_item<MT, R>(wst, sst, wrow_bytes, srow_bytes, x32a, xstride * 4, ii.rows, p.Kr, p.J,
+                                    wr, wk, p.cr, p.ck, lane, red, p.rpi, p.mstride);
+            }
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&empty[slot]);
+                mbar_arrive(&rfull[slot]);
+            }
+        }
+        if (!ok) {
+            *abort_flag = 1;
+            if (lane == 0) raise_status(NVFP4_DEV_TIMEOUT, p.status_user);
+        }
+    }
+
+    if (p.S > 1) {
+        // ---------------- cluster: sum the S partials of every row over DSMEM
+        __syncwarp();
+        cluster_sync_all();
+        if (!*abort_flag) {
+            int64_t local_row = 0;
+            for (int it = ib; it < ie; ++it) {
+                const Item ii = item_at(p, it);
+                const float gsc = p.g[ii.group];
+                const int total = ii.rows * p.M;
+                for (int idx = threadIdx.x; idx < total; idx += blockDim.x) {
+                    const int m = idx / ii.rows;
+                    const int r = idx - m * ii.rows;
+                    if ((r % p.S) != rank) continue;
+                    const float* mine = clpart + (local_row + r) * p.mstride + m;
+                    float v = 0.f;
+                    for (int c = 0; c < p.S; ++c) v += ld_cluster_f32(mine, c);
+                    store_out(p.y, m * p.ldy + static_cast<int64_t>(ii.group) * p.N + ii.row0 + r, gsc * v,
+                              p.out_bf16);
+                }
+                local_row += ii.rows;
+            }
+        }
+        cluster_sync_all();
+    }
+}
+
+// ------------------------------------------------------------------ byte-load kernel
+
+struct SimpleParams {
+    const uint8_t* w[2];
+    const uint8_t* s[2];
+    float g[2];
+    const float* g_dev;
+    const int32_t* ids;
+    int32_t* status_user;
+    const uint16_t* x;
+    void* y;
+    int64_t ldy;
+    int out_bf16;
+    int M, N, K, groups;
+    int moe, E, top_k, x_per_slot, slots;
+};
+
+// One warp per output column (all M rows). Lanes stride over the 16-element blocks of K.
+template <int MT>
+__global__ void __launch_bounds__(kSimpleThreads) gemv_simple_kernel(const __grid_constant__ SimpleParams p) {
+    const int lane = threadIdx.x & 31;
+    const int64_t col = static_cast<int64_t>(blockIdx.x) * (kSimpleThreads / 32) + (threadIdx.x >> 5);
+    const int64_t Kh = p.K / 2, Ks = p.K / 16;
+    const uint8_t* wrow;
+    const uint8_t* srow;
+    float g;
+    int64_t xrow0 = 0;
+    int64_t out0, out_step;
+    int mrows = p.M;
+    if (p.moe) {
+        if (col >= static_cast<int64_t>(p.slots) * p.N) return;
+        const int sl = static_cast<int>(col / p.N);
+        const int64_t n = col - static_cast<int64_t>(sl) * p.N;
+        const int e = __ldg(p.ids + sl);
+        if (e < 0 || e >= p.E) {
+            if (lane == 0) {
+                store_out(p.y, sl * p.ldy + n, 0.f, p.out_bf16);
+                raise_status(NVFP4_DEV_BAD_EXPERT, p.status_user);
+            }
+            return;
+        }
+        wrow = p.w[0] + (static_cast<int64_t>(e) * p.N + n) * Kh;
+        srow = p.s[0] + (static_cast<int64_t>(e) * p.N + n) * Ks;
+        g = __ldg(p.g_dev + e);
+        xrow0 = p.x_per_slot ? sl : sl / p.top_k;
+        out0 = sl * p.ldy + n;
+        out_step = 0;
+        mrows = 1;
+    } else {
+        if (col >= static_cast<int64_t>(p.groups) * p.N) return;
+        const int grp = static_cast<int>(col / p.N);
+        const int64_t n = col - static_cast<int64_t>(grp) * p.N;
+        wrow = p.w[grp] + n * Kh;
+        srow = p.s[grp] + n * Ks;
+        g = p.g[grp];
+        out0 = col;
+        out_step = p.ldy;
+    }
+    float acc[MT];
+#pragma unroll
+    for (int m = 0; m < MT; ++m) acc[m] = 0.f;
+    for (int64_t b = lane; b < Ks; b += 32) {
+        const uint32_t shf = cvt_e4m3x2(static_cast<uint16_t>(__ldg(srow + b)));
+        const uint16_t sc = static_cast<uint16_t>(shf & 0xffffu);
+        for (int e = 0; e < 8; ++e) {
+            uint32_t h[4];
+            cvt_e2m1x8(static_cast<uint32_t>(__ldg(wrow + b * 8 + e)), h);
+            const float2 q = widen_scaled(h[0], sc);
+            const int64_t k = b * 16 + 2 * e;
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+                if (m < mrows) {
+                    const uint16_t* xr = p.x + (xrow0 + m) * p.K + k;
+                    const float x0 = __uint_as_float(static_cast<uint32_t>(__ldg(xr)) << 16);
+                    const float x1 = __uint_as_float(static_cast<uint32_t>(__ldg(xr + 1)) << 16);
+                    acc[m] = fmaf(q.x, x0, acc[m]);
+                    acc[m] = fmaf(q.y, x1, acc[m]);
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc[m] += __shfl_xor_sync(0xffffffffu, acc[m], o);
+    }
+    if (lane == 0) {
+#pragma unroll
+        for (int m = 0; m < MT; ++m)
+            if (m < mrows) store_out(p.y, out0 + m * out_step, g * acc[m], p.out_bf16);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+
+struct DeviceInfo {
+    int sm_count = 0;
+    int smem_optin = 0;
+    bool init = false;
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[64];
+uint64_t g_wait_ns = kDefaultWaitNs;
+int g_variant = 0;
+int g_last_cuda_error = 0;
+
+const DeviceInfo* device_info(int* dev_out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceInfo& d = g_dev[dev];
+    if (!d.init) {
+        if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return nullptr;
+        if (cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+            return nullptr;
+        d.init = true;
+    }
+    if (dev_out) *dev_out = dev;
+    return &d;
+}
+
+nvfp4_status cuda_fail(cudaError_t e) {
+    g_last_cuda_error = static_cast<int>(e);
+    return NVFP4_ERR_CUDA;
+}
+
+struct Plan {
+    int kind;      // 0 stream dense, 1 stream MoE, 2 simple
+    int mt, R;
+    Params p;
+    int grid;
+    uint32_t smem;
+};
+
+int pick_r(int mt) { return mt <= 2 ? 8 : 4; }
+
+uint32_t align_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
+
+// Shared-memory layout and counts for a K range; false if it does not fit.
+bool layout(Params& p, int mt, int R, int rows_total_est, int groups_for_items, int sm_count,
+            int n_ctas, int smem_optin, uint32_t* smem_out) {
+    const int row_bytes = p.Kr / 2 + p.Kr / 16;
+    int rpi_max = kStageData / row_bytes;
+    if (rpi_max < 1) return false;
+    const int per_cta = (rows_total_est + n_ctas - 1) / n_ctas;
+    const int n_items_cta = (per_cta + rpi_max - 1) / rpi_max;
+    int rpi = (per_cta + n_items_cta - 1) / n_items_cta;
+    if (rpi < 1) rpi = 1;
+    if (rpi > rpi_max) rpi = rpi_max;
+    p.rpi = rpi;
+    p.chunks = (p.N + rpi - 1) / rpi;
+    p.items = groups_for_items * p.chunks;
+    p.J = (p.Kr + kStepElems - 1) / kStepElems;
+    // warps along K: fewest passes over (row batches x steps); ties go to fewer K-warps
+    int best_ck = 1, best_cost = 1 << 30;
+    for (int ck = 1; ck <= kConsumerWarps; ck *= 2) {
+        const int cr = kConsumerWarps / ck;
+        const int batches = (rpi + R - 1) / R;
+        const int cost = ((p.J + ck - 1) / ck) * ((batches + cr - 1) / cr);
+        if (cost < best_cost) { best_cost = cost; best_ck = ck; }
+    }
+    p.ck = best_ck;
+    p.cr = kConsumerWarps / best_ck;
+    p.mstride = mt;
+    uint32_t off = kStages * kStageStride;
+    p.x_off = off;
+    off += align_up(static_cast<uint32_t>(mt) * p.J * kStepElems * 4, 128);
+    p.red_off = off;
+    uint32_t red_bytes = static_cast<uint32_t>(kStages) * p.ck * rpi * mt * 4;
+    const uint32_t moe_scratch = 3 * kMaxMoeSlots * 4;
+    if (red_bytes < moe_scratch) red_bytes = moe_scratch;  // MoE table build reuses it
+    off += align_up(red_bytes, 128);
+    p.cl_off = off;
+    if (p.S > 1) {
+        const int items_per_cluster = (p.items + n_ctas - 1) / n_ctas;  // n_ctas = clusters here
+        p.cl_rows = items_per_cluster * rpi;
+        off += align_up(static_cast<uint32_t>(p.cl_rows) * mt * 4, 128);
+    } else {
+        p.cl_rows = 0;
+    }
+    p.tab_off = off;
+    off += align_up(sizeof(MoeTables), 128);
+    p.bar_off = off;
+    off += (4 * kStages + 2) * 8 + 16;
+    *smem_out = off;
+    return off <= static_cast<uint32_t>(smem_optin);
+}
+
+// Dense / gate-up plan. groups = 1 (dense) or 2 (gate_up).
+bool plan_dense(Plan& pl, int M, int N, int K, int groups, const DeviceInfo& d, const uint8_t* const* w,
+                const uint8_t* const* s) {
+    if (g_variant == 1) return false;
+    if (K % 32 != 0) return false;
+    for (int i = 0; i < groups; ++i)
+        if ((reinterpret_cast<uintptr_t>(w[i]) & 15) || (reinterpret_cast<uintptr_t>(s[i]) & 1)) return false;
+    const int mt = M;
+    const int R = pick_r(mt);
+    for (int S = 1; S <= 8; ++S) {
+        if (S > 1 && (K % (256 * S) != 0)) continue;
+        Params p{};
+        p.M = M; p.N = N; p.K = K; p.groups = groups; p.S = S; p.Kr = K / S;
+        const int n_ctas = S == 1 ? d.sm_count : d.sm_count / S;
+        if (n_ctas < 1) break;
+        uint32_t smem = 0;
+        if (!layout(p, mt, R, groups * N, groups, d.sm_count, n_ctas, d.smem_optin, &smem)) continue;
+        const int units = std::min(n_ctas, p.items);
+        pl.kind = 0;
+        pl.mt = mt;
+        pl.R = R;
+        pl.p = p;
+        pl.grid = units * S;
+        pl.smem = smem;
+        return true;
+    }
+    return false;
+}
+
+bool plan_moe(Plan& pl, int E, int T, int top_k, int N, int K, const DeviceInfo& d, const uint8_t* w,
+              const uint8_t* s) {
+    if (g_variant == 1) return false;
+    const int slots = T * top_k;
+    if (slots > kMaxMoeSlots || K % 32 != 0) return false;
+    if ((reinterpret_cast<uintptr_t>(w) & 15) || (reinterpret_cast<uintptr_t>(s) & 1)) return false;
+    const int caps[4] = {8, 4, 2, 1};
+    for (int ci = 0; ci < 4; ++ci) {
+        const int mt = caps[ci];
+        if (mt > slots && mt > 1) continue;
+        const int R = pick_r(mt);
+        Params p{};
+        p.N = N; p.K = K; p.S = 1; p.Kr = K; p.E = E; p.T = T; p.top_k = top_k; p.slots = slots;
+        uint32_t smem = 0;
+        if (!layout(p, mt, R, slots * N, slots, d.sm_count, d.sm_count, d.smem_optin, &smem)) continue;
+        pl.kind = 1;
+        pl.mt = mt;
+        pl.R = R;
+        pl.p = p;
+        pl.grid = d.sm_count;  // the item count depends on the routing, known on the device
+        pl.smem = smem;
+        return true;
+    }
+    return false;
+}
+
+template <int MODE, int MT, int R>
+cudaError_t launch_stream(const Plan& pl, cudaStream_t st) {
+    auto kern = gemv_stream_kernel<MODE, MT, R>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(pl.smem));
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(pl.grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = pl.smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    int na = 0;
+    if (pl.p.S > 1) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = pl.p.S;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        na = 1;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
+    return cudaLaunchKernelEx(&cfg, kern, pl.p);
+}
+
+cudaError_t dispatch_stream(const Plan& pl, cudaStream_t st) {
+    if (pl.kind == 1) {
+        switch (pl.mt) {
+            case 1: return launch_stream<kModeMoe, 1, 8>(pl, st);
+            case 2: return launch_stream<kModeMoe, 2, 8>(pl, st);
+            case 4: return launch_stream<kModeMoe, 4, 4>(pl, st);
+            case 8: return launch_stream<kModeMoe, 8, 4>(pl, st);
+            default: return cudaErrorInvalidValue;
+        }
+    }
+    switch (pl.mt) {
+        case 1: return launch_stream<kModeDense, 1, 8>(pl, st);
+        case 2: return launch_stream<kModeDense, 2, 8>(pl, st);
+        case 3: return launch_stream<kModeDense, 3, 4>(pl, st);
+        case 4: return launch_stream<kModeDense, 4, 4>(pl, st);
+        case 5: return launch_stream<kModeDense, 5, 4>(pl, st);
+        case 6: return launch_stream<kModeDense, 6, 4>(pl, st);
+        case 7: return launch_stream<kModeDense, 7, 4>(pl, st);
+        case 8: return launch_stream<kModeDense, 8, 4>(pl, st);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_simple(const SimpleParams& sp, int64_t cols, cudaStream_t st) {
+    const int per_block = kSimpleThreads / 32;
+    const int64_t blocks = (cols + per_block - 1) / per_block;
+    if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
+    const dim3 grid(static_cast<unsigned>(blocks)), block(kSimpleThreads);
+    const int mt = sp.moe ? 1 : sp.M;
+    switch (mt) {
+        case 1: gemv_simple_kernel<1><<<grid, block, 0, st>>>(sp); break;
+        case 2: gemv_simple_kernel<2><<<grid, block, 0, st>>>(sp); break;
+        case 3: gemv_simple_kernel<3><<<grid, block, 0, st>>>(sp); break;
+        case 4: gemv_simple_kernel<4><<<grid, block, 0, st>>>(sp); break;
+        case 5: gemv_simple_kernel<5><<<grid, block, 0, st>>>(sp); break;
+        case 6: gemv_simple_kernel<6><<<grid, block, 0, st>>>(sp); break;
+        case 7: gemv_simple_kernel<7><<<grid, block, 0, st>>>(sp); break;
+        case 8: gemv_simple_kernel<8><<<grid, block, 0, st>>>(sp); break;
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+nvfp4_status check_out(int y_type) {
+    return (y_type == NVFP4_OUT_F32 || y_type == NVFP4_OUT_BF16) ? NVFP4_OK : NVFP4_ERR_DTYPE;
+}
+
+nvfp4_status zero_output(void* y, int64_t elems, int y_type, cudaStream_t st) {
+    const size_t bytes = static_cast<size_t>(elems) * (y_type == NVFP4_OUT_BF16 ? 2 : 4);
+    const cudaError_t e = cudaMemsetAsync(y, 0, bytes, st);
+    return e == cudaSuccess ? NVFP4_OK : cuda_fail(e);
+}
+
+nvfp4_status run_dense(const uint8_t* const* w, const uint8_t* const* s, const float* g, int groups,
+                       const uint16_t* x, void* y, int y_type, int M, int N, int K, cudaStream_t st) {
+    if (!x || !y) return NVFP4_ERR_NULL;
+    for (int i = 0; i < groups; ++i)
+        if (!w[i] || !s[i]) return NVFP4_ERR_NULL;
+    if (M < 0 || N < 0 || K < 0 || M > 8 || K % 16 != 0) return NVFP4_ERR_SHAPE;
+    const nvfp4_status so = check_out(y_type);
+    if (so != NVFP4_OK) return so;
+    if (M == 0 || N == 0) return NVFP4_OK;
+    if (K == 0) return zero_output(y, static_cast<int64_t>(M) * groups * N, y_type, st);
+    int dev = 0;
+    const DeviceInfo* d = device_info(&dev);
+    if (!d) return cuda_fail(cudaGetLastError());
+    Plan pl{};
+    if (plan_dense(pl, M, N, K, groups, *d, w, s)) {
+        Params& p = pl.p;
+        for (int i = 0; i < 2; ++i) {
+            p.w[i] = w[i < groups ? i : 0];
+            p.s[i] = s[i < groups ? i : 0];
+            p.g[i] = g[i < groups ? i : 0];
+        }
+        p.x = x;
+        p.y = y;
+        p.ldy = static_cast<int64_t>(groups) * N;
+        p.out_bf16 = y_type == NVFP4_OUT_BF16;
+        p.wait_ns = g_wait_ns;
+        const cudaError_t e = dispatch_stream(pl, st);
+        if (e != cudaSuccess) return cuda_fail(e);
+        const cudaError_t e2 = cudaGetLastError();
+        return e2 == cudaSuccess ? NVFP4_OK : cuda_fail(e2);
+    }
+    SimpleParams sp{};
+    for (int i = 0; i < 2; ++i) {
+        sp.w[i] = w[i < groups ? i : 0];
+        sp.s[i] = s[i < groups ? i : 0];
+        sp.g[i] = g[i < groups ? i : 0];
+    }
+    sp.x = x; sp.y = y; sp.ldy = static_cast<int64_t>(groups) * N; sp.out_bf16 = y_type == NVFP4_OUT_BF16;
+    sp.M = M; sp.N = N; sp.K = K; sp.groups = groups;
+    const cudaError_t e = launch_simple(sp, static_cast<int64_t>(groups) * N, st);
+    return e == cudaSuccess ? NVFP4_OK : cuda_fail(e);
+}
+
+}  // namespace nvfp4
+
+using namespace nvfp4;
+
+extern "C" {
+
+nvfp4_status nvfp4_gemv(const uint8_t* w_packed, const uint8_t* w_scales, float global_scale,
+                        const uint16_t* x, void* y, nvfp4_out_t y_type, int M, int N, int K, void* stream) {
+    const uint8_t* w[1] = {w_packed};
+    const uint8_t* s[1] = {w_scales};
+    const float g[1] = {global_scale};
+    return run_dense(w, s, g, 1, x, y, y_type, M, N, K, static_cast<cudaStream_t>(stream));
+}
+
+nvfp4_status nvfp4_gemv_gate_up(const uint8_t* w_gate, const uint8_t* s_gate, float g_gate,
+                                const uint8_t* w_up, const uint8_t* s_up, float g_up,
+                                const uint16_t* x, void* y, nvfp4_out_t y_type,
+                                int M, int N, int K, void* stream) {
+    const uint8_t* w[2] = {w_gate, w_up};
+    const uint8_t* s[2] = {s_gate, s_up};
+    const float g[2] = {g_gate, g_up};
+    return run_dense(w, s, g, 2, x, y, y_type, M, N, K, static_cast<cudaStream_t>(stream));
+}
+
+nvfp4_status nvfp4_moe_gemv(const uint8_t* w_packed, const uint8_t* w_scales,
+                            const float* global_scales, int E,
+                            const int32_t* expert_ids, int T, int top_k,
+                            const uint16_t* x, int x_per_slot,
+                            void* y, nvfp4_out_t y_type, int N, int K,
+                            int32_t* status_dev, void* stream) {
+    if (!w_packed || !w_scales || !global_scales || !expert_ids || !x || !y) return NVFP4_ERR_NULL;
+    if (E < 1 || T < 0 || top_k < 0 || N < 0 || K < 0 || K % 16 != 0) return NVFP4_ERR_SHAPE;
+    if (static_cast<int64_t>(T) * top_k > (1 << 24)) return NVFP4_ERR_UNSUPPORTED;
+    const nvfp4_status so = check_out(y_type);
+    if (so != NVFP4_OK) return so;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int slots = T * top_k;
+    if (slots == 0 || N == 0) return NVFP4_OK;
+    if (K == 0) return zero_output(y, static_cast<int64_t>(slots) * N, y_type, st);
+    const DeviceInfo* d = device_info(nullptr);
+    if (!d) return cuda_fail(cudaGetLastError());
+    Plan pl{};
+    if (plan_moe(pl, E, T, top_k, N, K, *d, w_packed, w_scales)) {
+        Params& p = pl.p;
+        p.w[0] = p.w[1] = w_packed;
+        p.s[0] = p.s[1] = w_scales;
+        p.g_dev = global_scales;
+        p.ids = expert_ids;
+        p.status_user = status_dev;
+        p.x = x;
+        p.x_per_slot = x_per_slot ? 1 : 0;
+        p.y = y;
+        p.ldy = N;
+        p.out_bf16 = y_type == NVFP4_OUT_BF16;
+        p.M = 1;
+        p.wait_ns = g_wait_ns;
+        const cudaError_t e = dispatch_stream(pl, st);
+        if (e != cudaSuccess) return cuda_fail(e);
+        const cudaError_t e2 = cudaGetLastError();
+        return e2 == cudaSuccess ? NVFP4_OK : cuda_fail(e2);
+    }
+    SimpleParams sp{};
+    sp.w[0] = sp.w[1] = w_packed;
+    sp.s[0] = sp.s[1] = w_scales;
+    sp.g_dev = global_scales;
+    sp.ids = expert_ids;
+    sp.status_user = status_dev;
+    sp.x = x; sp.y = y; sp.ldy = N; sp.out_bf16 = y_type == NVFP4_OUT_BF16;
+    sp.M = 1; sp.N = N; sp.K = K; sp.groups = 1;
+    sp.moe = 1; sp.E = E; sp.top_k = top_k; sp.x_per_slot = x_per_slot ? 1 : 0; sp.slots = slots;
+    const cudaError_t e = launch_simple(sp, static_cast<int64_t>(slots) * N, st);
+    return e == cudaSuccess ? NVFP4_OK : cuda_fail(e);
+}
+
+const char* nvfp4_status_string(int status) {
+    switch (status) {
+        case NVFP4_OK: return "ok";
+        case NVFP4_ERR_NULL: return "null pointer";
+        case NVFP4_ERR_SHAPE: return "invalid shape (need 0<=M<=8, N>=0, K>=0, K%16==0)";
+        case NVFP4_ERR_ALIGN: return "misaligned pointer";
+        case NVFP4_ERR_DTYPE: return "invalid output type";
+        case NVFP4_ERR_UNSUPPORTED: return "unsupported size";
+        case NVFP4_ERR_CUDA: return "CUDA runtime error";
+        case NVFP4_ERR_TIMEOUT: return "device pipeline wait timed out";
+        default: return "unknown status";
+    }
+}
+
+int nvfp4_last_cuda_error(void) { return g_last_cuda_error; }
+
+nvfp4_status nvfp4_device_status(int32_t* flags_out, void* stream) {
+    if (!flags_out) return NVFP4_ERR_NULL;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int v = 0;
+    cudaError_t e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e);
+    e = cudaMemcpyFromSymbol(&v, g_device_status, sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(e);
+    const int zero = 0;
+    e = cudaMemcpyToSymbol(g_device_status, &zero, sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(e);
+    *flags_out = v;
+    return (v & NVFP4_DEV_TIMEOUT) ? NVFP4_ERR_TIMEOUT : NVFP4_OK;
+}
+
+void nvfp4_set_wait_budget_ns(uint64_t ns) { g_wait_ns = ns == UINT64_MAX ? kDefaultWaitNs : ns; }
+
+void nvfp4_set_variant(int variant) { g_variant = variant; }
+
+int nvfp4_describe_plan(int kind, int M, int N, int K, int T, int top_k, char* buf, int buflen) {
+    if (!buf || buflen < 1) return -1;
+    const DeviceInfo* d = device_info(nullptr);
+    if (!d) return -1;
+    Plan pl{};
+    bool ok = false;
+    // Pointers are only inspected for alignment here; 256-byte aligned stand-ins.
+    const uint8_t* fake = reinterpret_cast<const uint8_t*>(static_cast<uintptr_t>(256));
+    const uint8_t* w[2] = {fake, fake};
+    if (kind == 0 || kind == 1) ok = plan_dense(pl, M, N, K, kind == 0 ? 1 : 2, *d, w, w);
+    if (kind == 2) ok = plan_moe(pl, 288, T, top_k, N, K, *d, fake, fake);
+    int n;
+    if (!ok) {
+        n = snprintf(buf, buflen, "simple grid=%lld block=%d smem=0 split=1 rows_per_item=0 k_warps=0",
+                     static_cast<long long>(((kind == 2 ? static_cast<int64_t>(T) * top_k : (kind == 1 ? 2 : 1)) * N + 7) / 8),
+                     kSimpleThreads);
+    } else {
+        n = snprintf(buf, buflen, "%s grid=%d block=%d smem=%u split=%d rows_per_item=%d k_warps=%d mt=%d",
+                     pl.kind == 1 ? "stream_moe" : "stream", pl.grid, kThreads, pl.smem, pl.p.S, pl.p.rpi,
+                     pl.p.ck, pl.mt);
+    }
+    return n;
+}
+
+int nvfp4_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,326 @@
+"""GPU parity: the CUDA kernels (called through the C ABI) against the CPU oracle.
+
+Tolerance, per output element, with A = |g| * sum_k |w_k x_k| from the oracle:
+  fp32 output:  |y - y_ref| <= 1e-5 * A + 1e-6
+  bf16 output:  the same bound plus one bf16 ulp of y_ref
+y_ref is the oracle's fp64 value (not rounded). NaN must appear exactly where the oracle
+has NaN. Inputs are seeded (generator module). Large cases generate on the GPU with torch's
+CUDA RNG and copy the bytes to the host for the oracle.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import nvfp4_weight_only_gemv_gb300 as nv
+from nvfp4_weight_only_gemv_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+def ulp_bf16(v: np.ndarray) -> np.ndarray:
+    a = np.abs(v)
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    e = np.maximum(e, -126)
+    return np.where(a >= 2.0 ** -126, 2.0 ** (e - 7), 2.0 ** -133)
+
+
+def assert_parity(y_gpu: torch.Tensor, y_ref: np.ndarray, yabs: np.ndarray, what: str = ""):
+    y = y_gpu.detach().float().cpu().numpy().astype(np.float64)
+    assert y.shape == y_ref.shape, (y.shape, y_ref.shape)
+    nan_ref = np.isnan(y_ref)
+    assert np.array_equal(np.isnan(y), nan_ref), f"{what}: NaN positions differ"
+    tol = 1e-5 * yabs + 1e-6
+    if y_gpu.dtype == torch.bfloat16:
+        tol = tol + ulp_bf16(y_ref)
+    err = np.where(nan_ref, 0.0, np.abs(y - y_ref))
+    bad = err > np.where(nan_ref, 1.0, tol)
+    if bad.any():
+        i = np.unravel_index(np.argmax(err - tol), err.shape)
+        raise AssertionError(f"{what}: {bad.sum()} of {bad.size} outside tolerance; worst at {i}: "
+                             f"gpu={y[i]!r} ref={y_ref[i]!r} tol={tol[i]!r}")
+
+
+def host(t):
+    return t.detach().cpu().numpy()
+
+
+def run_dense(N, K, M, seed, out_dtype, device="cpu"):
+    p = synth.dense_problem(N, K, M, seed, device=device)
+    w, s, x = (p[k].to(DEV) for k in ("w", "s", "x"))
+    y = nv.gemv(w, s, p["g"], x, out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    yr, ya = oracle.gemv(host(p["w"]), host(p["s"]), p["g"], synth.bf16_bits(p["x"]))
+    return y, yr, ya
+
+
+@pytest.fixture(autouse=True)
+def _clean_state():
+    nv.set_variant(0)
+    nv.set_wait_budget_ns(None)
+    yield
+    nv.set_variant(0)
+    nv.set_wait_budget_ns(None)
+    assert nv.device_status() == 0
+
+
+# ------------------------------------------------------------------ workload configs
+
+def test_smoke_256x512_m1_fp32():
+    y, yr, ya = run_dense(256, 512, 1, 0, torch.float32)
+    assert_parity(y, yr, ya, "256x512 M=1")
+
+
+@pytest.mark.parametrize("N,K,M,seed", [(4096, 4096, 1, 1), (4096, 4096, 5, 2),
+                                        (1024, 4096, 1, 3), (1024, 4096, 5, 4)])
+def test_attention_projections_bf16(N, K, M, seed):
+    y, yr, ya = run_dense(N, K, M, seed, torch.bfloat16)
+    assert_parity(y, yr, ya, f"{N}x{K} M={M}")
+
+
+@pytest.mark.parametrize("M", [1, 2, 4, 8])
+def test_ffn_gate_up_fused(M):
+    N, K = 12288, 4096
+    p = synth.gate_up_problem(N, K, M, 5, device=DEV)
+    y = nv.gemv_gate_up(p["wg"], p["sg"], p["gg"], p["wu"], p["su"], p["gu"], p["x"])
+    torch.cuda.synchronize()
+    yr, ya = oracle.gemv_gate_up(host(p["wg"]), host(p["sg"]), p["gg"], host(p["wu"]), host(p["su"]),
+                                 p["gu"], synth.bf16_bits(p["x"]))
+    assert_parity(y, yr, ya, f"gate_up M={M}")
+
+
+@pytest.mark.parametrize("M", [1, 2, 4, 8])
+def test_ffn_down(M):
+    y, yr, ya = run_dense(4096, 12288, M, 6, torch.float32, device=DEV)
+    assert_parity(y, yr, ya, f"down M={M}")
+
+
+def test_vocab_head_m1():
+    y, yr, ya = run_dense(151936, 4096, 1, 7, torch.float32, device=DEV)
+    assert_parity(y, yr, ya, "vocab head")
+
+
+@pytest.mark.parametrize("x_per_slot,N,K", [(False, 3072, 4096), (True, 4096, 1536)])
+def test_moe_288_experts_top8(x_per_slot, N, K):
+    p = synth.moe_problem(288, N, K, 4, 8, x_per_slot, seed=8, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    y = nv.moe_gemv(p["w"], p["s"], p["gs"], p["ids"], p["x"], x_per_slot, 8, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    yr, ya, bad = oracle.moe_gemv(host(p["w"]), host(p["s"]), host(p["gs"]), host(p["ids"]),
+                                  synth.bf16_bits(p["x"]), x_per_slot, 8)
+    assert bad == 0
+    assert_parity(y, yr, ya, "moe")
+
+
+# ------------------------------------------------------------------ shapes, tails, edge cases
+
+@pytest.mark.parametrize("M", range(1, 9))
+@pytest.mark.parametrize("N,K", [(1000, 1056), (37, 2816), (300, 512)])
+def test_m_sweep_ragged(N, K, M):
+    y, yr, ya = run_dense(N, K, M, 100 + M, torch.float32)
+    assert_parity(y, yr, ya, f"{N}x{K} M={M}")
+
+
+@pytest.mark.parametrize("N,K,M", [(1, 16, 1), (3, 48, 2), (33, 80, 3), (5, 32, 8), (1, 32, 1),
+                                   (7, 1040, 1), (2, 16, 8), (513, 32, 4)])
+def test_small_and_odd_shapes(N, K, M):
+    for dt in (torch.float32, torch.bfloat16):
+        y, yr, ya = run_dense(N, K, M, 200 + N + K + M, dt)
+        assert_parity(y, yr, ya, f"{N}x{K} M={M} {dt}")
+
+
+def test_empty_inputs():
+    w = torch.empty(0, 8, dtype=torch.uint8, device=DEV)
+    s = torch.empty(0, 1, dtype=torch.uint8, device=DEV)
+    x = torch.zeros(2, 16, dtype=torch.bfloat16, device=DEV)
+    assert nv.gemv(w, s, 1.0, x).shape == (2, 0)
+    p = synth.dense_problem(8, 32, 1, 300)
+    w, s = p["w"].to(DEV), p["s"].to(DEV)
+    x0 = torch.zeros(0, 32, dtype=torch.bfloat16, device=DEV)
+    assert nv.gemv(w, s, p["g"], x0).shape == (0, 8)
+    # K == 0: empty sum
+    wk = torch.empty(4, 0, dtype=torch.uint8, device=DEV)
+    sk = torch.empty(4, 0, dtype=torch.uint8, device=DEV)
+    xk = torch.empty(3, 0, dtype=torch.bfloat16, device=DEV)
+    y = nv.gemv(wk, sk, 1.0, xk, out=torch.full((3, 4), 7.0, device=DEV))
+    assert torch.all(y == 0)
+
+
+def test_unaligned_pointers_use_byte_kernel():
+    N, K, M = 64, 256, 2
+    p = synth.dense_problem(N, K, M, 301)
+    wbuf = torch.zeros(N * K // 2 + 1, dtype=torch.uint8, device=DEV)
+    sbuf = torch.zeros(N * K // 16 + 1, dtype=torch.uint8, device=DEV)
+    wbuf[1:] = p["w"].reshape(-1).to(DEV)
+    sbuf[1:] = p["s"].reshape(-1).to(DEV)
+    w = wbuf[1:].view(N, K // 2)
+    s = sbuf[1:].view(N, K // 16)
+    assert w.data_ptr() % 16 == 1
+    y = nv.gemv(w, s, p["g"], p["x"].to(DEV))
+    torch.cuda.synchronize()
+    yr, ya = oracle.gemv(host(p["w"]), host(p["s"]), p["g"], synth.bf16_bits(p["x"]))
+    assert_parity(y, yr, ya, "unaligned")
+
+
+def test_unaligned_scale_rows_tma_head_tail():
+    # K % 256 != 0: scale rows are not 16-byte multiples, so items start mid-line
+    for N, K, M in ((777, 704, 2), (129, 1120, 1), (50, 96, 3)):
+        y, yr, ya = run_dense(N, K, M, 302 + K, torch.float32)
+        assert_parity(y, yr, ya, f"{N}x{K}")
+
+
+def test_nan_scale_propagates():
+    N, K, M = 300, 512, 2
+    p = synth.dense_problem(N, K, M, 303)
+    s = p["s"].clone()
+    s[17, 3] = 0x7F
+    s[299, 31] = 0xFF
+    y = nv.gemv(p["w"].to(DEV), s.to(DEV), p["g"], p["x"].to(DEV))
+    torch.cuda.synchronize()
+    yr, ya = oracle.gemv(host(p["w"]), host(s), p["g"], synth.bf16_bits(p["x"]))
+    assert np.isnan(yr[:, 17]).all() and np.isnan(yr[:, 299]).all()
+    assert_parity(y, yr, ya, "nan scales")
+
+
+def test_sign_bit_scales_and_extreme_codes():
+    # every E4M3 scale code except NaN, every E2M1 code, large and tiny x
+    N, K, M = 254, 512, 2
+    g = torch.Generator().manual_seed(304)
+    w = torch.randint(0, 256, (N, K // 2), dtype=torch.uint8, generator=g)
+    codes = torch.tensor([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=torch.uint8)
+    s = codes[torch.randint(0, codes.numel(), (N, K // 16), generator=g)]
+    x = (torch.randn(M, K, generator=g) * torch.exp2(torch.randint(-20, 20, (M, K), generator=g).float())
+         ).to(torch.bfloat16)
+    y = nv.gemv(w.to(DEV), s.to(DEV), 0.75, x.to(DEV))
+    torch.cuda.synchronize()
+    yr, ya = oracle.gemv(w.numpy(), s.numpy(), 0.75, synth.bf16_bits(x))
+    assert_parity(y, yr, ya, "extreme codes")
+
+
+def test_byte_kernel_matches_oracle_on_configs():
+    nv.set_variant(1)
+    for N, K, M, dt in ((4096, 4096, 1, torch.bfloat16), (1024, 4096, 5, torch.bfloat16),
+                        (300, 12288, 8, torch.float32)):
+        y, yr, ya = run_dense(N, K, M, 305, dt)
+        assert_parity(y, yr, ya, f"byte kernel {N}x{K} M={M}")
+
+
+def test_deterministic_across_runs():
+    p = synth.dense_problem(4096, 12288, 4, 306, device=DEV)
+    ys = [nv.gemv(p["w"], p["s"], p["g"], p["x"]) for _ in range(3)]
+    torch.cuda.synchronize()
+    assert torch.equal(ys[0], ys[1]) and torch.equal(ys[1], ys[2])
+
+
+def test_gate_up_equals_two_dense_calls():
+    p = synth.gate_up_problem(2000, 2048, 3, 307, device=DEV)
+    y = nv.gemv_gate_up(p["wg"], p["sg"], p["gg"], p["wu"], p["su"], p["gu"], p["x"])
+    yg = nv.gemv(p["wg"], p["sg"], p["gg"], p["x"])
+    yu = nv.gemv(p["wu"], p["su"], p["gu"], p["x"])
+    torch.cuda.synchronize()
+    assert torch.equal(y[:, :2000], yg) and torch.equal(y[:, 2000:], yu)
+
+
+# ------------------------------------------------------------------ MoE edge cases
+
+def _moe_check(p, ids, x_per_slot, top_k, out_dtype=torch.float32):
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    idd = torch.as_tensor(ids, dtype=torch.int32).to(DEV)
+    y = nv.moe_gemv(p["w"].to(DEV), p["s"].to(DEV), p["gs"].to(DEV), idd, p["x"].to(DEV), x_per_slot,
+                    top_k, out_dtype=out_dtype, status=st)
+    torch.cuda.synchronize()
+    yr, ya, bad = oracle.moe_gemv(host(p["w"]), host(p["s"]), host(p["gs"]), np.asarray(ids, np.int32),
+                                  synth.bf16_bits(p["x"]), x_per_slot, top_k)
+    assert_parity(y, yr, ya, "moe")
+    return int(st.item()), bad
+
+
+@pytest.mark.parametrize("x_per_slot", [False, True])
+def test_moe_repeated_experts_are_shared(x_per_slot):
+    E, N, K, T, top_k = 16, 200, 1024, 5, 3
+    p = synth.moe_problem(E, N, K, T, top_k, x_per_slot, seed=310, fill="all")
+    ids = [3, 3, 7, 3, 9, 7, 3, 3, 3, 1, 3, 5, 0, 3, 15]   # expert 3 in 8 slots (> one group)
+    st, bad = _moe_check(p, ids, x_per_slot, top_k)
+    assert st == 0 and bad == 0
+
+
+def test_moe_bad_ids_zero_their_rows():
+    E, N, K, T, top_k = 6, 96, 512, 2, 3
+    p = synth.moe_problem(E, N, K, T, top_k, True, seed=311, fill="all")
+    ids = [0, -2, 5, 6, 1, 1]
+    st, bad = _moe_check(p, ids, True, top_k, torch.bfloat16)
+    assert bad == 2 and st & nv.DEV_BAD_EXPERT
+    assert nv.device_status() & nv.DEV_BAD_EXPERT
+
+
+def test_moe_byte_kernel_and_many_slots():
+    E, N, K = 40, 64, 256
+    p = synth.moe_problem(E, N, K, 100, 3, False, seed=312, fill="all")   # 300 slots > 256
+    st, bad = _moe_check(p, p["ids"].tolist(), False, 3)
+    assert st == 0
+    nv.set_variant(1)
+    q = synth.moe_problem(E, N, K, 4, 8, True, seed=313, fill="all")
+    st, bad = _moe_check(q, q["ids"].tolist(), True, 8)
+    assert st == 0
+
+
+def test_moe_odd_k_uses_byte_kernel():
+    p = synth.moe_problem(10, 33, 48, 3, 2, False, seed=314, fill="all")
+    st, _ = _moe_check(p, p["ids"].tolist(), False, 2)
+    assert st == 0
+
+
+# ------------------------------------------------------------------ runtime behaviour
+
+def test_timeout_path_reports_and_recovers():
+    p = synth.dense_problem(4096, 4096, 1, 320, device=DEV)
+    nv.set_wait_budget_ns(0)
+    nv.gemv(p["w"], p["s"], p["g"], p["x"])
+    flags = nv.device_status()
+    nv.set_wait_budget_ns(None)
+    assert flags & nv.DEV_TIMEOUT
+    y = nv.gemv(p["w"], p["s"], p["g"], p["x"])
+    torch.cuda.synchronize()
+    assert nv.device_status() == 0
+    yr, ya = oracle.gemv(host(p["w"]), host(p["s"]), p["g"], synth.bf16_bits(p["x"]))
+    assert_parity(y, yr, ya, "after timeout")
+
+
+def test_cuda_graph_capture_and_replay():
+    p = synth.dense_problem(2048, 4096, 2, 321, device=DEV)
+    y = torch.empty(2, 2048, device=DEV)
+    nv.gemv(p["w"], p["s"], p["g"], p["x"], out=y)     # warm-up outside capture
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            nv.gemv(p["w"], p["s"], p["g"], p["x"], out=y)
+    y.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    yr, ya = oracle.gemv(host(p["w"]), host(p["s"]), p["g"], synth.bf16_bits(p["x"]))
+    assert_parity(y, yr, ya, "graph replay")
+
+
+def test_side_stream_launch():
+    p = synth.dense_problem(1024, 2048, 3, 322, device=DEV)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        y = nv.gemv(p["w"], p["s"], p["g"], p["x"])
+    s.synchronize()
+    yr, ya = oracle.gemv(host(p["w"]), host(p["s"]), p["g"], synth.bf16_bits(p["x"]))
+    assert_parity(y, yr, ya, "side stream")
+
+
+def test_plan_uses_all_sms_for_large_problems():
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    desc = nv.describe_plan("dense", 1, 151936, 4096)
+    assert desc.startswith("stream ") and f"grid={sms} " in desc
+    desc = nv.describe_plan("dense", 8, 4096, 12288)
+    assert "split=" in desc and "split=1 " not in desc
