@@ -139,9 +139,30 @@ void nvfp4_set_wait_budget_ns(uint64_t ns);
 
 /*
  * Kernel selection (process-wide): 0 = automatic (default), 1 = always the byte-load
- * kernel. Used by tests to check both kernels against the oracle.
+ * kernel, 2 = streaming kernel with x always staged in fp32 (the exact path that M >= 5
+ * and inexact-f16 inputs use). Used by tests to check every path against the oracle.
  */
 void nvfp4_set_variant(int variant);
+
+/*
+ * For M <= 4 the streaming kernel stages x in f16 with one power-of-two scale per
+ * 16-element block. That is exact for every bf16 value within 2^26 of its block's largest
+ * magnitude. A CTA that finds any value it cannot hold exactly (a huge dynamic range
+ * inside a block, Inf or NaN) stages x in fp32 instead. This returns how many CTAs did so
+ * since the last call, after synchronising `stream`, and resets the count. Returns -1 on
+ * a CUDA error.
+ */
+long long nvfp4_fp32_fallbacks(void* stream);
+
+/*
+ * Programmatic dependent launch (process-wide; default 1 = on). When on, each GEMV kernel
+ * lets the next kernel in the stream start early, and it starts streaming its own weights
+ * before the preceding kernel has finished. x, the expert ids and y are touched only after
+ * the preceding kernel completes. Weights therefore must not be written by the kernel that
+ * immediately precedes the call on the same stream. 0 turns this off: every launch then
+ * waits for the full completion of its predecessor.
+ */
+void nvfp4_set_pdl(int enable);
 
 /*
  * Describes the launch the next call with these arguments would make. It writes

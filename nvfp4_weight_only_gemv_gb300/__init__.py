@@ -22,7 +22,7 @@ import torch
 from . import build as _build
 
 __all__ = ["gemv", "gemv_gate_up", "moe_gemv", "device_status", "set_wait_budget_ns",
-           "set_variant", "describe_plan", "library", "library_path", "NVFP4Error",
+           "set_variant", "set_pdl", "fp32_fallbacks", "describe_plan", "library", "library_path", "NVFP4Error",
            "OUT_F32", "OUT_BF16", "DEV_TIMEOUT", "DEV_BAD_EXPERT"]
 
 OUT_F32 = 0
@@ -65,6 +65,10 @@ def _declare(lib):
     lib.nvfp4_set_wait_budget_ns.restype = None
     lib.nvfp4_set_variant.argtypes = [i32]
     lib.nvfp4_set_variant.restype = None
+    lib.nvfp4_set_pdl.argtypes = [i32]
+    lib.nvfp4_set_pdl.restype = None
+    lib.nvfp4_fp32_fallbacks.argtypes = [vp]
+    lib.nvfp4_fp32_fallbacks.restype = ctypes.c_longlong
     lib.nvfp4_describe_plan.argtypes = [i32, i32, i32, i32, i32, i32, ctypes.c_char_p, i32]
     lib.nvfp4_describe_plan.restype = i32
     lib.nvfp4_version.argtypes = []
@@ -125,9 +129,12 @@ def _need(t: torch.Tensor, name: str, dtype, ndim: int):
 
 
 def _out(out, shape, out_dtype, device):
+    """The output tensor: ``out`` when given (its own dtype wins), else a new one."""
     if out is None:
         return torch.empty(shape, dtype=out_dtype, device=device)
-    _need(out, "out", out_dtype, len(shape))
+    if out.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError(f"out must be float32 or bfloat16 (got {out.dtype})")
+    _need(out, "out", out.dtype, len(shape))
     if tuple(out.shape) != tuple(shape):
         raise ValueError(f"out must have shape {tuple(shape)} (got {tuple(out.shape)})")
     return out
@@ -230,8 +237,22 @@ def set_wait_budget_ns(ns) -> None:
 
 
 def set_variant(variant: int) -> None:
-    """0 = automatic kernel choice, 1 = force the byte-load kernel."""
+    """0 = automatic kernel choice, 1 = byte-load kernel, 2 = streaming kernel with fp32 x."""
     library().nvfp4_set_variant(int(variant))
+
+
+def fp32_fallbacks(stream=None) -> int:
+    """CTAs that staged x in fp32 because block-scaled f16 could not hold it exactly
+    (read and reset; synchronises the stream)."""
+    v = library().nvfp4_fp32_fallbacks(ctypes.c_void_p(_stream(stream)))
+    if v < 0:
+        raise NVFP4Error(6, "nvfp4_fp32_fallbacks")
+    return int(v)
+
+
+def set_pdl(enable: bool) -> None:
+    """Programmatic dependent launch between consecutive GEMVs (default on)."""
+    library().nvfp4_set_pdl(int(bool(enable)))
 
 
 def describe_plan(kind: str, M: int, N: int, K: int, T: int = 0, top_k: int = 0) -> str:

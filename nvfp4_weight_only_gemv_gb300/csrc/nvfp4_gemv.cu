@@ -47,9 +47,8 @@ constexpr int kConsumerWarps = 8;
 constexpr int kProducerWarp = kConsumerWarps;
 constexpr int kEpilogueWarp = kConsumerWarps + 1;
 constexpr int kThreads = (kConsumerWarps + 2) * 32;
-constexpr int kStages = 4;
-constexpr int kStageData = 32 * 1024;      // weight bytes (codes + scales) per stage
-constexpr int kStageStride = kStageData + 128;  // + room for an unaligned scale head
+constexpr int kMaxStages = 4;
+constexpr int kStageData = 40 * 1024;      // most weight bytes (codes + scales) per stage
 constexpr int kStepElems = 1024;           // K elements per warp step (32 lanes x 32)
 constexpr int kMaxMoeSlots = 256;
 constexpr int kSimpleThreads = 256;
@@ -59,6 +58,7 @@ constexpr uint64_t kDrainWaitNs = 2000000000ull;
 enum : int { kModeDense = 0, kModeMoe = 1 };
 
 __device__ int g_device_status;
+__device__ unsigned long long g_fp32_fallbacks;  // CTAs that staged x in fp32 because f16 was inexact
 
 // ------------------------------------------------------------------ parameters
 
@@ -81,7 +81,10 @@ struct Params {
     int ck, cr;               // consumer warps along K and along rows
     int mstride;              // partial-sum stride per row (>= max rows of x per item)
     int cl_rows;              // rows of the cluster partial buffer (S > 1)
-    uint32_t x_off, red_off, cl_off, bar_off, tab_off;
+    int stages;               // ring depth (2..kMaxStages)
+    uint32_t stage_stride;    // bytes per ring slot (multiple of 128)
+    int force_f32;            // 1: always stage x in fp32 (kernel selection for tests)
+    uint32_t x_off, p2_off, red_off, cl_off, bar_off, tab_off;
     uint64_t wait_ns;
 };
 
@@ -119,11 +122,25 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                  ::"r"(smem_addr(bar)), "r"(bytes) : "memory");
 }
 
+// The suspend-time hint lets a waiting warp sleep until the phase completes (or the hint
+// elapses) instead of spinning on issue slots that the decoding warps need.
+constexpr uint32_t kSuspendHintNs = 1000000;
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n .reg .pred p;\n"
-        " mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
+        " mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n"
+        " selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok) : "r"(smem_addr(bar)), "r"(parity), "n"(kSuspendHintNs) : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n"
+        " mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
         " selp.u32 %0, 1, 0, p;\n}"
         : "=r"(ok) : "r"(smem_addr(bar)), "r"(parity) : "memory");
     return ok != 0;
@@ -136,7 +153,9 @@ __device__ __forceinline__ uint64_t global_ns() {
 }
 
 // Bounded wait for the phase with the given parity; false when the budget ran out.
+// A zero budget polls once without blocking (try_wait may suspend for a while).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t budget_ns) {
+    if (budget_ns == 0) return mbar_test_wait(bar, parity);
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
     while (true) {
@@ -172,9 +191,16 @@ __device__ __forceinline__ uint16_t lds16(uint32_t a) {
     return v;
 }
 
-__device__ __forceinline__ void bar_sync_consumers() {
-    asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+__device__ __forceinline__ float2 lds64f(uint32_t a) {
+    float2 v;
+    asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(a));
+    return v;
 }
+
+// Programmatic dependent launch: wait for the preceding kernel's results / let the next
+// kernel start its prologue. Both are no-ops when the launch did not enable PDL.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 __device__ __forceinline__ uint32_t cluster_rank() {
     uint32_t r;
@@ -225,6 +251,22 @@ __device__ __forceinline__ float2 widen_scaled(uint32_t h2, uint16_t s) {
         : "=f"(r.x), "=f"(r.y) : "r"(h2), "h"(s));
     return r;
 }
+
+// acc + lo(q2) * lo(x2) + hi(q2) * hi(x2): two mixed-precision FMAs (f16 x f16 products,
+// exact in fp32, accumulated in fp32).
+__device__ __forceinline__ float fma2_f16_f32(uint32_t q2, uint32_t x2, float acc) {
+    float r;
+    asm("{\n .reg .f16 a, b, c, d;\n"
+        " mov.b32 {a, b}, %1;\n"
+        " mov.b32 {c, d}, %2;\n"
+        " fma.rn.f32.f16 %0, a, c, %3;\n"
+        " fma.rn.f32.f16 %0, b, d, %0;\n}"
+        : "=f"(r) : "r"(q2), "r"(x2), "f"(acc));
+    return r;
+}
+
+__device__ __forceinline__ float half_lo_f32(uint32_t h2) { return __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xffffu))); }
+__device__ __forceinline__ float half_hi_f32(uint32_t h2) { return __half2float(__ushort_as_half(static_cast<unsigned short>(h2 >> 16))); }
 
 __device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
@@ -304,7 +346,117 @@ __device__ void stage_x(const uint16_t* __restrict__ x, int64_t K, int k0, int K
     }
 }
 
+// Block-scaled f16 staging. For every 16-element block b of the CTA's K range, one power
+// of two 2^E_b (shared by the staged rows) is chosen so that the block's largest |x| lands
+// in [2^12, 2^13). x' = x * 2^-E_b is stored as f16 in the lane layout of h_pos(k), and
+// 2^E_b as f32 in p2[b]. A bf16 value converts exactly unless its scaled magnitude falls
+// below the f16 normal range (more than 2^26 below its block's maximum) or it is not
+// finite. The function returns true if any staged element was not reproduced exactly
+// (x'[k] * 2^E_b != x[k]). The caller then restages x in fp32.
+__device__ __forceinline__ int h_pos(int k) {
+    return ((((k >> 10) * 4 + ((k >> 3) & 3)) * 32) + ((k >> 5) & 31)) * 8 + (k & 7);
+}
+
+__device__ __forceinline__ float pow2f(int e) {  // exact 2^e for e in [-149, 127]
+    return e >= -126 ? __int_as_float((e + 127) << 23) : __int_as_float(1 << (e + 149));
+}
+
+template <typename RowFn>
+__device__ bool stage_x_h(const uint16_t* __restrict__ x, int64_t K, int k0, int Kr, int rows, RowFn src_row,
+                          __half* xh, int xh_stride, float* p2, int tid, int nthreads) {
+    const int nb = Kr / 16;
+    const bool vec = (reinterpret_cast<uintptr_t>(x) & 15) == 0;
+    bool lossy = false;
+    for (int b = tid; b < nb; b += nthreads) {
+        const int k = b * 16;
+        uint32_t amax = 0;  // largest bf16 magnitude pattern (ordered like the magnitudes)
+        for (int m = 0; m < rows; ++m) {
+            const uint16_t* src = x + static_cast<int64_t>(src_row(m)) * K + k0 + k;
+            uint32_t u[8];
+            if (vec) {
+                const uint4 t0 = __ldg(reinterpret_cast<const uint4*>(src));
+                const uint4 t1 = __ldg(reinterpret_cast<const uint4*>(src) + 1);
+                u[0] = t0.x; u[1] = t0.y; u[2] = t0.z; u[3] = t0.w; u[4] = t1.x; u[5] = t1.y; u[6] = t1.z; u[7] = t1.w;
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) u[i] = src[2 * i] | (static_cast<uint32_t>(src[2 * i + 1]) << 16);
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) amax = max(amax, max(u[i] & 0x7fffu, (u[i] >> 16) & 0x7fffu));
+        }
+        int e_max;
+        if (amax >= 0x7f80u || amax == 0) {
+            e_max = 12;                      // Inf/NaN (reported below) or an all-zero block
+        } else if ((amax >> 7) == 0) {
+            e_max = (31 - __clz(amax)) - 133;  // bf16 subnormal: mant * 2^-133
+        } else {
+            e_max = static_cast<int>(amax >> 7) - 127;
+        }
+        const int E = e_max - 12;
+        const float scale_back = pow2f(E);
+        const int a = min(-E, 127);
+        const float sa = pow2f(a);
+        const float sb = pow2f(-E - a);
+        p2[b] = scale_back;
+        for (int m = 0; m < rows; ++m) {
+            const uint16_t* src = x + static_cast<int64_t>(src_row(m)) * K + k0 + k;
+            uint32_t u[8];
+            if (vec) {
+                const uint4 t0 = __ldg(reinterpret_cast<const uint4*>(src));
+                const uint4 t1 = __ldg(reinterpret_cast<const uint4*>(src) + 1);
+                u[0] = t0.x; u[1] = t0.y; u[2] = t0.z; u[3] = t0.w; u[4] = t1.x; u[5] = t1.y; u[6] = t1.z; u[7] = t1.w;
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) u[i] = src[2 * i] | (static_cast<uint32_t>(src[2 * i + 1]) << 16);
+            }
+            uint32_t out[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float f0 = bf16_lo(u[i]), f1 = bf16_hi(u[i]);
+                const __half h0 = __float2half_rn((f0 * sa) * sb);
+                const __half h1 = __float2half_rn((f1 * sa) * sb);
+                lossy |= !isfinite(f0) || !isfinite(f1) || __half2float(h0) * scale_back != f0 ||
+                         __half2float(h1) * scale_back != f1;
+                out[i] = static_cast<uint32_t>(__half_as_ushort(h0)) | (static_cast<uint32_t>(__half_as_ushort(h1)) << 16);
+            }
+            __half* dst = xh + static_cast<int64_t>(m) * xh_stride + h_pos(k);
+            reinterpret_cast<uint4*>(dst)[0] = make_uint4(out[0], out[1], out[2], out[3]);
+            reinterpret_cast<uint4*>(dst + 256)[0] = make_uint4(out[4], out[5], out[6], out[7]);
+        }
+    }
+    return lossy;
+}
+
 // ------------------------------------------------------------------ consumer compute
+
+// Reduces V = R * MTE per-lane partials over the warp and stores the sums of rows
+// rb..rb+R-1 (those below `rows`) at red[row * mstride + m].
+template <int R, int MTE>
+__device__ __forceinline__ void store_partials(float (&v)[next_pow2(R * MTE)], int lane, int rb, int rows,
+                                               float* red, int mstride) {
+    constexpr int V = R * MTE;
+    constexpr int VP = next_pow2(V);
+    reduce_scatter<VP, 16>(v, lane);
+    if constexpr (VP >= 32) {
+#pragma unroll
+        for (int i = 0; i < VP / 32; ++i) {
+            const int idx = lane * (VP / 32) + i;
+            if (idx < V) {
+                const int row = rb + idx / MTE;
+                if (row < rows) red[row * mstride + idx % MTE] = v[i];
+            }
+        }
+    } else {
+        constexpr int sh = 5 - ilog2(VP);
+        if ((lane & ((1 << sh) - 1)) == 0) {
+            const int idx = lane >> sh;
+            if (idx < V) {
+                const int row = rb + idx / MTE;
+                if (row < rows) red[row * mstride + idx % MTE] = v[0];
+            }
+        }
+    }
+}
 
 // One item's share of one consumer warp: rows rb = wr*R, wr*R + cr*R, ... (batches of R)
 // and warp steps j = wk, wk + ck, ... Partials go to red[(wk * rpi + row) * mstride + m].
@@ -371,26 +523,87 @@ __device__ __forceinline__ void compute_item(uint32_t wst, uint32_t sst, int wro
         float v[VP];
 #pragma unroll
         for (int i = 0; i < VP; ++i) v[i] = i < V ? acc[i / MTE][i % MTE].x + acc[i / MTE][i % MTE].y : 0.f;
-        reduce_scatter<VP, 16>(v, lane);
-        if constexpr (VP >= 32) {
+        store_partials<R, MTE>(v, lane, rb, rows, red + wk * rpi * mstride, mstride);
+    }
+}
+
+// One item's share of one consumer warp on the block-scaled f16 x (see stage_x_h): per
+// 16-element block, part = sum E2M1 * x' with mixed f16 x f16 -> f32 FMAs, then
+// acc += part * (E4M3 scale * 2^E_b).
+template <int MTE, int R>
+__device__ __forceinline__ void compute_item_h(uint32_t wst, uint32_t sst, int wrow_bytes, int srow_bytes,
+                                               uint32_t xh, int xh_stride_bytes, uint32_t p2a, int rows, int Kr,
+                                               int J, int wr, int wk, int cr, int ck, int lane,
+                                               float* red, int rpi, int mstride) {
+    constexpr int V = R * MTE;
+    constexpr int VP = next_pow2(V);
+    for (int rb = wr * R; rb < rows; rb += cr * R) {
+        float acc[R][MTE];
 #pragma unroll
-            for (int i = 0; i < VP / 32; ++i) {
-                const int idx = lane * (VP / 32) + i;
-                if (idx < V) {
-                    const int row = rb + idx / MTE;
-                    if (row < rows) red[(wk * rpi + row) * mstride + idx % MTE] = v[i];
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int m = 0; m < MTE; ++m) acc[r][m] = 0.f;
+
+        for (int j = wk; j < J; j += ck) {
+            const int kl = j * kStepElems + lane * 32;
+            if (kl < Kr) {
+                uint4 wv[R];
+                uint32_t sh[R];
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    const int row = rb + r;
+                    if (row < rows) {
+                        wv[r] = lds128(wst + row * wrow_bytes + (kl >> 1));
+                        sh[r] = cvt_e4m3x2(lds16(sst + row * srow_bytes + (kl >> 4)));
+                    } else {
+                        wv[r] = make_uint4(0u, 0u, 0u, 0u);
+                        sh[r] = 0u;
+                    }
                 }
-            }
-        } else {
-            constexpr int sh = 5 - ilog2(VP);
-            if ((lane & ((1 << sh) - 1)) == 0) {
-                const int idx = lane >> sh;
-                if (idx < V) {
-                    const int row = rb + idx / MTE;
-                    if (row < rows) red[(wk * rpi + row) * mstride + idx % MTE] = v[0];
+                const float2 pp = lds64f(p2a + ((kl >> 4) << 2));
+#pragma unroll
+                for (int bb = 0; bb < 2; ++bb) {
+                    float part[R][MTE];
+#pragma unroll
+                    for (int r = 0; r < R; ++r)
+#pragma unroll
+                        for (int m = 0; m < MTE; ++m) part[r][m] = 0.f;
+#pragma unroll
+                    for (int ww = 0; ww < 2; ++ww) {
+                        const int w = bb * 2 + ww;
+                        uint4 xw[MTE];
+#pragma unroll
+                        for (int m = 0; m < MTE; ++m)
+                            xw[m] = lds128(xh + m * xh_stride_bytes + (((j * 4 + w) * 32 + lane) << 4));
+#pragma unroll
+                        for (int r = 0; r < R; ++r) {
+                            const uint32_t word = w == 0 ? wv[r].x : (w == 1 ? wv[r].y : (w == 2 ? wv[r].z : wv[r].w));
+                            uint32_t h[4];
+                            cvt_e2m1x8(word, h);
+#pragma unroll
+                            for (int m = 0; m < MTE; ++m) {
+                                part[r][m] = fma2_f16_f32(h[0], xw[m].x, part[r][m]);
+                                part[r][m] = fma2_f16_f32(h[1], xw[m].y, part[r][m]);
+                                part[r][m] = fma2_f16_f32(h[2], xw[m].z, part[r][m]);
+                                part[r][m] = fma2_f16_f32(h[3], xw[m].w, part[r][m]);
+                            }
+                        }
+                    }
+                    const float pb = bb ? pp.y : pp.x;
+#pragma unroll
+                    for (int r = 0; r < R; ++r) {
+                        const float fac = (bb ? half_hi_f32(sh[r]) : half_lo_f32(sh[r])) * pb;
+#pragma unroll
+                        for (int m = 0; m < MTE; ++m) acc[r][m] = fmaf(part[r][m], fac, acc[r][m]);
+                    }
                 }
             }
         }
+
+        float v[VP];
+#pragma unroll
+        for (int i = 0; i < VP; ++i) v[i] = i < V ? acc[i / MTE][i % MTE] : 0.f;
+        store_partials<R, MTE>(v, lane, rb, rows, red + wk * rpi * mstride, mstride);
     }
 }
 
@@ -493,18 +706,39 @@ __device__ void build_moe_tables(const Params& p, MoeTables* tab, int* scratch) 
 
 // ------------------------------------------------------------------ the streaming kernel
 
-template <int MODE, int MT, int R>
-__global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const __grid_constant__ Params p) {
+__host__ __device__ constexpr int rows_per_batch(int mte) { return mte <= 2 ? 8 : 4; }
+
+// Dispatches one item's consumer work to the f16 path (x staged block-scaled in f16,
+// M <= 4) or the fp32 path.
+template <int MTE>
+__device__ __forceinline__ void compute_dispatch(bool use_h, uint32_t wst, uint32_t sst, int wrow_bytes,
+                                                 int srow_bytes, uint32_t xa, int xstride_elems, uint32_t p2a,
+                                                 int rows, int Kr, int J, int wr, int wk, int cr, int ck,
+                                                 int lane, float* red, int rpi, int mstride) {
+    constexpr int R = rows_per_batch(MTE);
+    if constexpr (MTE <= 4) {
+        if (use_h) {
+            compute_item_h<MTE, R>(wst, sst, wrow_bytes, srow_bytes, xa, xstride_elems * 2, p2a, rows, Kr, J, wr,
+                                   wk, cr, ck, lane, red, rpi, mstride);
+            return;
+        }
+    }
+    compute_item<MTE, R>(wst, sst, wrow_bytes, srow_bytes, xa, xstride_elems * 4, rows, Kr, J, wr, wk, cr, ck,
+                         lane, red, rpi, mstride);
+}
+
+template <int MODE, int MT>
+__global__ void __launch_bounds__(kThreads, (MT <= 1 ? 2 : 1)) gemv_stream_kernel(const __grid_constant__ Params p) {
     extern __shared__ __align__(128) uint8_t smem[];
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.bar_off);
     uint64_t* full = bars;
-    uint64_t* empty = bars + kStages;
-    uint64_t* rfull = bars + 2 * kStages;
-    uint64_t* rempty = bars + 3 * kStages;
-    uint64_t* xready = bars + 4 * kStages;
-    uint64_t* xfree = bars + 4 * kStages + 1;
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 4 * kStages + 2);
-    float* x32 = reinterpret_cast<float*>(smem + p.x_off);
+    uint64_t* empty = bars + kMaxStages;
+    uint64_t* rfull = bars + 2 * kMaxStages;
+    uint64_t* rempty = bars + 3 * kMaxStages;
+    uint64_t* xready = bars + 4 * kMaxStages;
+    uint64_t* xfree = bars + 4 * kMaxStages + 1;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 4 * kMaxStages + 2);
+    volatile int* lossy_flag = abort_flag + 1;
     float* red_base = reinterpret_cast<float*>(smem + p.red_off);
     float* clpart = reinterpret_cast<float*>(smem + p.cl_off);
     MoeTables* tab = reinterpret_cast<MoeTables*>(smem + p.tab_off);
@@ -515,9 +749,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const __grid_c
     const int cluster = blockIdx.x / p.S;
     const int n_clusters = gridDim.x / p.S;
     const int k0 = rank * p.Kr;
+    const int NS = p.stages;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kStages; ++i) {
+        for (int i = 0; i < NS; ++i) {
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], kConsumerWarps);
             mbar_init(&rfull[i], kConsumerWarps);
@@ -526,12 +761,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const __grid_c
         mbar_init(xready, kConsumerWarps);
         mbar_init(xfree, kConsumerWarps);
         *abort_flag = 0;
+        *lossy_flag = 0;
         fence_barrier_init();
     }
     if constexpr (MODE == kModeMoe) {
+        pdl_wait();  // the routing may come from the preceding kernel
         build_moe_tables(p, tab, reinterpret_cast<int*>(red_base));
     }
     __syncthreads();
+    pdl_launch_dependents();
 
     const int items = MODE == kModeMoe ? tab->n_groups * p.chunks : p.items;
     const int ib = static_cast<int>(static_cast<int64_t>(items) * cluster / n_clusters);
@@ -543,12 +781,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const __grid_c
     const uint32_t scale_region = static_cast<uint32_t>(p.rpi) * wrow_bytes;  // multiple of 16
 
     if (warp == kProducerWarp) {
-        // ---------------- producer: TMA bulk copies into the ring
+        // ---------------- producer: TMA bulk copies of the (read-only) weights into the ring.
+        // They may start before the preceding kernel has finished.
         int issued = 0;
         for (int it = ib; it < ie; ++it) {
             const int li = it - ib;
-            const int slot = li % kStages;
-            const int use = li / kStages;
+            const int slot = li % NS;
+            const int use = li / NS;
             if (use > 0 && !mbar_wait(&empty[slot], (use - 1) & 1, p.wait_ns)) {
                 *abort_flag = 1;
                 if (lane == 0) raise_status(NVFP4_DEV_TIMEOUT, p.status_user);
@@ -566,7 +805,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const __grid_c
                 wsrc = p.w[ii.group] + static_cast<int64_t>(ii.row0) * Kh;
                 ssrc = p.s[ii.group] + static_cast<int64_t>(ii.row0) * Ks;
             }
-            uint8_t* wdst = smem + slot * kStageStride;
+            uint8_t* wdst = smem + slot * p.stage_stride;
             uint8_t* sdst = wdst + scale_region;
             if (p.S == 1) {
                 const uint32_t wbytes = static_cast<uint32_t>(ii.rows) * wrow_bytes;
@@ -597,19 +836,18 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const __grid_c
             __syncwarp();
             issued = li + 1;
         }
-        if (*abort_flag) {
-            // drain: every slot's latest issued use must complete before the CTA exits
-            for (int li = issued - 1; li >= 0 && li >= issued - kStages; --li) {
-                mbar_wait(&full[li % kStages], (li / kStages) & 1, kDrainWaitNs);
-            }
+        // Every slot's latest issued copy must land before the CTA can retire, also when the
+        // consumers gave up early. In a normal run these waits return at once.
+        for (int li = issued - 1; li >= 0 && li >= issued - NS; --li) {
+            mbar_wait(&full[li % NS], (li / NS) & 1, kDrainWaitNs);
         }
     } else if (warp == kEpilogueWarp) {
         // ---------------- epilogue: fixed-order sum over K-warps, scale, store
         int64_t local_row = 0;
         for (int it = ib; it < ie; ++it) {
             const int li = it - ib;
-            const int slot = li % kStages;
-            const int use = li / kStages;
+            const int slot = li % NS;
+            const int use = li / NS;
             if (!mbar_wait(&rfull[slot], use & 1, p.wait_ns)) {
                 *abort_flag = 1;
                 if (lane == 0) raise_status(NVFP4_DEV_TIMEOUT, p.status_user);
@@ -650,15 +888,21 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const __grid_c
         const int wk = warp % p.ck;
         const int wr = warp / p.ck;
         const int ctid = threadIdx.x;  // consumer warps are 0..7
-        const int xstride = p.J * kStepElems;
-        const uint32_t x32a = smem_addr(x32);
+        const int xstride = p.J * kStepElems;  // elements per staged x row (fp32 or f16)
+        float* x32 = reinterpret_cast<float*>(smem + p.x_off);
+        __half* xh = reinterpret_cast<__half*>(smem + p.x_off);
+        float* p2 = reinterpret_cast<float*>(smem + p.p2_off);
+        const uint32_t xa = smem_addr(smem + p.x_off);
+        const uint32_t p2a = smem_addr(p2);
         int cur_key = -1;
-        int key_index = 0;
+        int xr = 0, xf = 0;  // completed phases of xready / xfree
+        bool use_h = false;
         bool ok = true;
+        if constexpr (MODE != kModeMoe) pdl_wait();  // x may come from the preceding kernel
         for (int it = ib; it < ie && ok; ++it) {
             const int li = it - ib;
-            const int slot = li % kStages;
-            const int use = li / kStages;
+            const int slot = li % NS;
+            const int use = li / NS;
             const Item ii = item_at(p, it);
             const int key = MODE == kModeMoe ? ii.group : 0;
             if (key != cur_key) {
@@ -666,31 +910,51 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const __grid_c
                 if (cur_key >= 0) {
                     __syncwarp();
                     if (lane == 0) mbar_arrive(xfree);
-                    if (!mbar_wait(xfree, (key_index - 1) & 1, p.wait_ns)) { ok = false; break; }
+                    if (!mbar_wait(xfree, xf & 1, p.wait_ns)) { ok = false; break; }
+                    ++xf;
                 }
+                int nrows = MT;
+                int first = 0;
                 if constexpr (MODE == kModeMoe) {
-                    const int first = tab->first[key];
-                    const int cnt = tab->count[key];
-                    const int tk = p.top_k;
-                    const bool per_slot = p.x_per_slot != 0;
-                    stage_x(p.x, p.K, k0, p.Kr, cnt,
-                            [&](int m) { const int sl = tab->member_list[first + m]; return per_slot ? sl : sl / tk; },
-                            x32, xstride, ctid, kConsumerWarps * 32);
-                } else {
-                    stage_x(p.x, p.K, k0, p.Kr, p.M, [](int m) { return m; }, x32, xstride, ctid,
-                            kConsumerWarps * 32);
+                    nrows = tab->count[key];
+                    first = tab->first[key];
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(xready);
-                if (!mbar_wait(xready, key_index & 1, p.wait_ns)) { ok = false; break; }
+                const int tk = p.top_k;
+                const bool per_slot = p.x_per_slot != 0;
+                auto src_row = [&](int m) {
+                    if constexpr (MODE == kModeMoe) {
+                        const int sl = tab->member_list[first + m];
+                        return per_slot ? sl : sl / tk;
+                    } else {
+                        return m;
+                    }
+                };
+                bool want_h = nrows <= 4 && !p.force_f32;
+                if (want_h) {
+                    if (stage_x_h(p.x, p.K, k0, p.Kr, nrows, src_row, xh, xstride, p2, ctid, kConsumerWarps * 32))
+                        *lossy_flag = xr + 1;
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(xready);
+                    if (!mbar_wait(xready, xr & 1, p.wait_ns)) { ok = false; break; }
+                    ++xr;
+                    want_h = *lossy_flag != xr;
+                    if (!want_h && ctid == 0) atomicAdd(&g_fp32_fallbacks, 1ull);
+                }
+                if (!want_h) {
+                    stage_x(p.x, p.K, k0, p.Kr, nrows, src_row, x32, xstride, ctid, kConsumerWarps * 32);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(xready);
+                    if (!mbar_wait(xready, xr & 1, p.wait_ns)) { ok = false; break; }
+                    ++xr;
+                }
+                use_h = want_h;
                 cur_key = key;
-                ++key_index;
             }
             if (!mbar_wait(&full[slot], use & 1, p.wait_ns)) { ok = false; break; }
             if (use > 0 && !mbar_wait(&rempty[slot], (use - 1) & 1, p.wait_ns)) { ok = false; break; }
             if (*abort_flag) { ok = false; break; }
 
-            const uint32_t wst = smem_addr(smem + slot * kStageStride);
+            const uint32_t wst = smem_addr(smem + slot * p.stage_stride);
             uint32_t sst = wst + scale_region;
             if (p.S == 1) {
                 const uint8_t* ssrc;
@@ -705,11 +969,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const __grid_c
             if constexpr (MODE == kModeMoe) {
                 const int cnt = tab->count[ii.group];
                 switch (cnt) {
-#define NVFP4_MOE_CASE(C)                                                                              \
-    case C:                                                                                            \
-        if constexpr (C <= MT)                                                                         \
-            compute_item<C, R>(wst, sst, wrow_bytes, srow_bytes, x32a, xstride * 4, ii.rows, p.Kr, p.J,  \
-                               wr, wk, p.cr, p.ck, lane, red, p.rpi, p.mstride);                       \
+#define NVFP4_MOE_CASE(C)                                                                                      \
+    case C:                                                                                                    \
+        if constexpr (C <= MT)                                                                                 \
+            compute_dispatch<C>(use_h, wst, sst, wrow_bytes, srow_bytes, xa, xstride, p2a, ii.rows, p.Kr, p.J, \
+                                wr, wk, p.cr, p.ck, lane, red, p.rpi, p.mstride);                              \
         break;
                     NVFP4_MOE_CASE(1)
                     NVFP4_MOE_CASE(2)
@@ -723,8 +987,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const __grid_c
                     default: break;
                 }
             } else {
-                compute_item<MT, R>(wst, sst, wrow_bytes, srow_bytes, x32a, xstride * 4, ii.rows, p.Kr, p.J,
-                                    wr, wk, p.cr, p.ck, lane, red, p.rpi, p.mstride);
+                compute_dispatch<MT>(use_h, wst, sst, wrow_bytes, srow_bytes, xa, xstride, p2a, ii.rows, p.Kr, p.J,
+                                     wr, wk, p.cr, p.ck, lane, red, p.rpi, p.mstride);
             }
             __syncwarp();
             if (lane == 0) {
@@ -862,7 +1126,8 @@ __global__ void __launch_bounds__(kSimpleThreads) gemv_simple_kernel(const __gri
 
 struct DeviceInfo {
     int sm_count = 0;
-    int smem_optin = 0;
+    int smem_optin = 0;   // per block
+    int smem_per_sm = 0;
     bool init = false;
 };
 
@@ -881,6 +1146,8 @@ const DeviceInfo* device_info(int* dev_out) {
         if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return nullptr;
         if (cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
             return nullptr;
+        if (cudaDeviceGetAttribute(&d.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess)
+            return nullptr;
         d.init = true;
     }
     if (dev_out) *dev_out = dev;
@@ -894,31 +1161,45 @@ nvfp4_status cuda_fail(cudaError_t e) {
 
 struct Plan {
     int kind;      // 0 stream dense, 1 stream MoE, 2 simple
-    int mt, R;
+    int mt;
     Params p;
     int grid;
     uint32_t smem;
 };
 
-int pick_r(int mt) { return mt <= 2 ? 8 : 4; }
+bool g_pdl = true;
 
 uint32_t align_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
 
 // Shared-memory layout and counts for a K range; false if it does not fit.
-bool layout(Params& p, int mt, int R, int rows_total_est, int groups_for_items, int sm_count,
-            int n_ctas, int smem_optin, uint32_t* smem_out) {
+// n_units = CTAs (S == 1) or clusters (S > 1) that share the items.
+bool layout(Params& p, int mt, int rows_total_est, int groups_for_items, int n_units, int smem_limit,
+            uint32_t* smem_out) {
+    const int R = rows_per_batch(mt);
     const int row_bytes = p.Kr / 2 + p.Kr / 16;
-    int rpi_max = kStageData / row_bytes;
-    if (rpi_max < 1) return false;
-    const int per_cta = (rows_total_est + n_ctas - 1) / n_ctas;
-    const int n_items_cta = (per_cta + rpi_max - 1) / rpi_max;
-    int rpi = (per_cta + n_items_cta - 1) / n_items_cta;
-    if (rpi < 1) rpi = 1;
-    if (rpi > rpi_max) rpi = rpi_max;
+    const int rpi_cap = kStageData / row_bytes;
+    if (rpi_cap < 1) return false;
+    // Rows per item: the value that minimises the row slots the busiest unit decodes (a
+    // partial batch of R rows still costs R slots) plus a per-item overhead, preferring
+    // larger items on ties.
+    p.J = (p.Kr + kStepElems - 1) / kStepElems;
+    int best_rpi = 1;
+    long long best_rows_cost = -1;
+    for (int rpi = 1; rpi <= rpi_cap; ++rpi) {
+        const long long items = static_cast<long long>(groups_for_items) * ((p.N + rpi - 1) / rpi);
+        const long long per_unit = (items + n_units - 1) / n_units;
+        const long long slots = (rpi + R - 1) / R * R;
+        const long long cost = per_unit * (slots + 2);  // + about two rows' worth of per-item work
+        if (best_rows_cost < 0 || cost <= best_rows_cost) { best_rows_cost = cost; best_rpi = rpi; }
+    }
+    const int rpi = best_rpi;
     p.rpi = rpi;
     p.chunks = (p.N + rpi - 1) / rpi;
     p.items = groups_for_items * p.chunks;
     p.J = (p.Kr + kStepElems - 1) / kStepElems;
+    // a CTA with at most two items needs no deeper ring; fewer stages leave room for a
+    // second CTA (the next GEMV's prologue under programmatic dependent launch)
+    const int items_per_unit = (p.items + n_units - 1) / n_units;
     // warps along K: fewest passes over (row batches x steps); ties go to fewer K-warps
     int best_ck = 1, best_cost = 1 << 30;
     for (int ck = 1; ck <= kConsumerWarps; ck *= 2) {
@@ -930,28 +1211,35 @@ bool layout(Params& p, int mt, int R, int rows_total_est, int groups_for_items, 
     p.ck = best_ck;
     p.cr = kConsumerWarps / best_ck;
     p.mstride = mt;
-    uint32_t off = kStages * kStageStride;
-    p.x_off = off;
-    off += align_up(static_cast<uint32_t>(mt) * p.J * kStepElems * 4, 128);
-    p.red_off = off;
-    uint32_t red_bytes = static_cast<uint32_t>(kStages) * p.ck * rpi * mt * 4;
-    const uint32_t moe_scratch = 3 * kMaxMoeSlots * 4;
-    if (red_bytes < moe_scratch) red_bytes = moe_scratch;  // MoE table build reuses it
-    off += align_up(red_bytes, 128);
-    p.cl_off = off;
-    if (p.S > 1) {
-        const int items_per_cluster = (p.items + n_ctas - 1) / n_ctas;  // n_ctas = clusters here
-        p.cl_rows = items_per_cluster * rpi;
-        off += align_up(static_cast<uint32_t>(p.cl_rows) * mt * 4, 128);
-    } else {
-        p.cl_rows = 0;
+    p.stage_stride = align_up(static_cast<uint32_t>(rpi) * row_bytes + 128, 128);
+    // a CTA with at most two items needs no deeper ring; otherwise the deepest ring that fits
+    for (int stages = items_per_unit <= 2 ? 2 : kMaxStages; stages >= 2; --stages) {
+        p.stages = stages;
+        uint32_t off = static_cast<uint32_t>(p.stages) * p.stage_stride;
+        p.x_off = off;
+        off += align_up(static_cast<uint32_t>(mt) * p.J * kStepElems * 4, 128);  // fp32 size (f16 uses half)
+        p.p2_off = off;
+        off += align_up(static_cast<uint32_t>(p.J) * (kStepElems / 16) * 4, 128);
+        p.red_off = off;
+        uint32_t red_bytes = static_cast<uint32_t>(p.stages) * p.ck * rpi * mt * 4;
+        const uint32_t moe_scratch = 3 * kMaxMoeSlots * 4;
+        if (red_bytes < moe_scratch) red_bytes = moe_scratch;  // MoE table build reuses it
+        off += align_up(red_bytes, 128);
+        p.cl_off = off;
+        if (p.S > 1) {
+            p.cl_rows = items_per_unit * rpi;
+            off += align_up(static_cast<uint32_t>(p.cl_rows) * mt * 4, 128);
+        } else {
+            p.cl_rows = 0;
+        }
+        p.tab_off = off;
+        off += align_up(sizeof(MoeTables), 128);
+        p.bar_off = off;
+        off += (4 * kMaxStages + 2) * 8 + 16;
+        *smem_out = off;
+        if (off <= static_cast<uint32_t>(smem_limit)) return true;
     }
-    p.tab_off = off;
-    off += align_up(sizeof(MoeTables), 128);
-    p.bar_off = off;
-    off += (4 * kStages + 2) * 8 + 16;
-    *smem_out = off;
-    return off <= static_cast<uint32_t>(smem_optin);
+    return false;
 }
 
 // Dense / gate-up plan. groups = 1 (dense) or 2 (gate_up).
@@ -962,19 +1250,26 @@ bool plan_dense(Plan& pl, int M, int N, int K, int groups, const DeviceInfo& d, 
     for (int i = 0; i < groups; ++i)
         if ((reinterpret_cast<uintptr_t>(w[i]) & 15) || (reinterpret_cast<uintptr_t>(s[i]) & 1)) return false;
     const int mt = M;
-    const int R = pick_r(mt);
+    // M = 1 kernels fit two CTAs per SM (registers); use that when two rings fit too
+    const int per_sm_max = mt == 1 ? 2 : 1;
     for (int S = 1; S <= 8; ++S) {
         if (S > 1 && (K % (256 * S) != 0)) continue;
         Params p{};
-        p.M = M; p.N = N; p.K = K; p.groups = groups; p.S = S; p.Kr = K / S;
-        const int n_ctas = S == 1 ? d.sm_count : d.sm_count / S;
-        if (n_ctas < 1) break;
         uint32_t smem = 0;
-        if (!layout(p, mt, R, groups * N, groups, d.sm_count, n_ctas, d.smem_optin, &smem)) continue;
-        const int units = std::min(n_ctas, p.items);
+        int n_units = 0;
+        bool ok = false;
+        for (int per_sm = (S == 1 ? per_sm_max : 1); per_sm >= 1 && !ok; --per_sm) {
+            p = Params{};
+            p.M = M; p.N = N; p.K = K; p.groups = groups; p.S = S; p.Kr = K / S;
+            n_units = S == 1 ? d.sm_count * per_sm : d.sm_count / S;
+            const int limit = per_sm == 1 ? d.smem_optin : d.smem_per_sm / per_sm - 1024;
+            ok = n_units >= 1 && layout(p, mt, groups * N, groups, n_units, limit, &smem);
+        }
+        if (n_units < 1) break;
+        if (!ok) continue;
+        const int units = std::min(n_units, p.items);
         pl.kind = 0;
         pl.mt = mt;
-        pl.R = R;
         pl.p = p;
         pl.grid = units * S;
         pl.smem = smem;
@@ -993,14 +1288,12 @@ bool plan_moe(Plan& pl, int E, int T, int top_k, int N, int K, const DeviceInfo&
     for (int ci = 0; ci < 4; ++ci) {
         const int mt = caps[ci];
         if (mt > slots && mt > 1) continue;
-        const int R = pick_r(mt);
         Params p{};
         p.N = N; p.K = K; p.S = 1; p.Kr = K; p.E = E; p.T = T; p.top_k = top_k; p.slots = slots;
         uint32_t smem = 0;
-        if (!layout(p, mt, R, slots * N, slots, d.sm_count, d.sm_count, d.smem_optin, &smem)) continue;
+        if (!layout(p, mt, slots * N, slots, d.sm_count, d.smem_optin, &smem)) continue;
         pl.kind = 1;
         pl.mt = mt;
-        pl.R = R;
         pl.p = p;
         pl.grid = d.sm_count;  // the item count depends on the routing, known on the device
         pl.smem = smem;
@@ -1009,24 +1302,48 @@ bool plan_moe(Plan& pl, int E, int T, int top_k, int N, int K, const DeviceInfo&
     return false;
 }
 
-template <int MODE, int MT, int R>
+// Raises a kernel's dynamic shared-memory limit to the device maximum once per device and
+// kernel (`done` belongs to the caller's instantiation), so launches with different plans
+// never change the attribute again.
+template <typename Kern>
+cudaError_t allow_max_smem(Kern kern, bool (&done)[64]) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!done[dev]) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, g_dev[dev].smem_optin);
+        if (e != cudaSuccess) return e;
+        done[dev] = true;
+    }
+    return cudaSuccess;
+}
+
+template <int MODE, int MT>
 cudaError_t launch_stream(const Plan& pl, cudaStream_t st) {
-    auto kern = gemv_stream_kernel<MODE, MT, R>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(pl.smem));
+    auto kern = gemv_stream_kernel<MODE, MT>;
+    static bool done[64] = {};
+    cudaError_t e = allow_max_smem(kern, done);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(pl.grid);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = pl.smem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     int na = 0;
     if (pl.p.S > 1) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = pl.p.S;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        na = 1;
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = pl.p.S;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    if (g_pdl) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
@@ -1036,22 +1353,22 @@ cudaError_t launch_stream(const Plan& pl, cudaStream_t st) {
 cudaError_t dispatch_stream(const Plan& pl, cudaStream_t st) {
     if (pl.kind == 1) {
         switch (pl.mt) {
-            case 1: return launch_stream<kModeMoe, 1, 8>(pl, st);
-            case 2: return launch_stream<kModeMoe, 2, 8>(pl, st);
-            case 4: return launch_stream<kModeMoe, 4, 4>(pl, st);
-            case 8: return launch_stream<kModeMoe, 8, 4>(pl, st);
+            case 1: return launch_stream<kModeMoe, 1>(pl, st);
+            case 2: return launch_stream<kModeMoe, 2>(pl, st);
+            case 4: return launch_stream<kModeMoe, 4>(pl, st);
+            case 8: return launch_stream<kModeMoe, 8>(pl, st);
             default: return cudaErrorInvalidValue;
         }
     }
     switch (pl.mt) {
-        case 1: return launch_stream<kModeDense, 1, 8>(pl, st);
-        case 2: return launch_stream<kModeDense, 2, 8>(pl, st);
-        case 3: return launch_stream<kModeDense, 3, 4>(pl, st);
-        case 4: return launch_stream<kModeDense, 4, 4>(pl, st);
-        case 5: return launch_stream<kModeDense, 5, 4>(pl, st);
-        case 6: return launch_stream<kModeDense, 6, 4>(pl, st);
-        case 7: return launch_stream<kModeDense, 7, 4>(pl, st);
-        case 8: return launch_stream<kModeDense, 8, 4>(pl, st);
+        case 1: return launch_stream<kModeDense, 1>(pl, st);
+        case 2: return launch_stream<kModeDense, 2>(pl, st);
+        case 3: return launch_stream<kModeDense, 3>(pl, st);
+        case 4: return launch_stream<kModeDense, 4>(pl, st);
+        case 5: return launch_stream<kModeDense, 5>(pl, st);
+        case 6: return launch_stream<kModeDense, 6>(pl, st);
+        case 7: return launch_stream<kModeDense, 7>(pl, st);
+        case 8: return launch_stream<kModeDense, 8>(pl, st);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -1112,6 +1429,7 @@ nvfp4_status run_dense(const uint8_t* const* w, const uint8_t* const* s, const f
         p.ldy = static_cast<int64_t>(groups) * N;
         p.out_bf16 = y_type == NVFP4_OUT_BF16;
         p.wait_ns = g_wait_ns;
+        p.force_f32 = g_variant == 2;
         const cudaError_t e = dispatch_stream(pl, st);
         if (e != cudaSuccess) return cuda_fail(e);
         const cudaError_t e2 = cudaGetLastError();
@@ -1185,6 +1503,7 @@ nvfp4_status nvfp4_moe_gemv(const uint8_t* w_packed, const uint8_t* w_scales,
         p.out_bf16 = y_type == NVFP4_OUT_BF16;
         p.M = 1;
         p.wait_ns = g_wait_ns;
+        p.force_f32 = g_variant == 2;
         const cudaError_t e = dispatch_stream(pl, st);
         if (e != cudaSuccess) return cuda_fail(e);
         const cudaError_t e2 = cudaGetLastError();
@@ -1238,6 +1557,18 @@ void nvfp4_set_wait_budget_ns(uint64_t ns) { g_wait_ns = ns == UINT64_MAX ? kDef
 
 void nvfp4_set_variant(int variant) { g_variant = variant; }
 
+void nvfp4_set_pdl(int enable) { g_pdl = enable != 0; }
+
+long long nvfp4_fp32_fallbacks(void* stream) {
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    unsigned long long v = 0;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return -1;
+    if (cudaMemcpyFromSymbol(&v, g_fp32_fallbacks, sizeof v) != cudaSuccess) return -1;
+    const unsigned long long zero = 0;
+    if (cudaMemcpyToSymbol(g_fp32_fallbacks, &zero, sizeof zero) != cudaSuccess) return -1;
+    return static_cast<long long>(v);
+}
+
 int nvfp4_describe_plan(int kind, int M, int N, int K, int T, int top_k, char* buf, int buflen) {
     if (!buf || buflen < 1) return -1;
     const DeviceInfo* d = device_info(nullptr);
@@ -1255,9 +1586,9 @@ int nvfp4_describe_plan(int kind, int M, int N, int K, int T, int top_k, char* b
                      static_cast<long long>(((kind == 2 ? static_cast<int64_t>(T) * top_k : (kind == 1 ? 2 : 1)) * N + 7) / 8),
                      kSimpleThreads);
     } else {
-        n = snprintf(buf, buflen, "%s grid=%d block=%d smem=%u split=%d rows_per_item=%d k_warps=%d mt=%d",
+        n = snprintf(buf, buflen, "%s grid=%d block=%d smem=%u split=%d rows_per_item=%d k_warps=%d mt=%d stages=%d",
                      pl.kind == 1 ? "stream_moe" : "stream", pl.grid, kThreads, pl.smem, pl.p.S, pl.p.rpi,
-                     pl.p.ck, pl.mt);
+                     pl.p.ck, pl.mt, pl.p.stages);
     }
     return n;
 }
