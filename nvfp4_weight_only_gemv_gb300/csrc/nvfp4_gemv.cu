@@ -48,7 +48,7 @@ constexpr int kProducerWarp = kConsumerWarps;
 constexpr int kEpilogueWarp = kConsumerWarps + 1;
 constexpr int kThreads = (kConsumerWarps + 2) * 32;
 constexpr int kMaxStages = 4;
-constexpr int kStageData = 40 * 1024;      // most weight bytes (codes + scales) per stage
+constexpr int kStageData = 60 * 1024;      // most weight bytes (codes + scales) per stage
 constexpr int kStepElems = 1024;           // K elements per warp step (32 lanes x 32)
 constexpr int kMaxMoeSlots = 256;
 constexpr int kSimpleThreads = 256;
@@ -78,13 +78,18 @@ struct Params {
     int E, T, top_k, x_per_slot, slots;
     int S, Kr, J;             // K split (cluster size), K per CTA, warp steps per CTA K-range
     int rpi, chunks, items;   // rows per item, items per group, items in total (dense)
+    int items_q, items_r;     // dense: items / units and items % units (units = CTAs or clusters)
+    int s_aligned;            // scale rows are whole 16-byte lines (K % 256 == 0, aligned bases)
     int ck, cr;               // consumer warps along K and along rows
     int mstride;              // partial-sum stride per row (>= max rows of x per item)
     int cl_rows;              // rows of the cluster partial buffer (S > 1)
     int stages;               // ring depth (2..kMaxStages)
     uint32_t stage_stride;    // bytes per ring slot (multiple of 128)
+    long long work;           // planner's estimate of decoded row-elements per unit (host only)
     int force_f32;            // 1: always stage x in fp32 (kernel selection for tests)
-    uint32_t x_off, p2_off, red_off, cl_off, bar_off, tab_off;
+    int wstride;              // bytes between weight rows in a ring slot (padded: 64 mod 128)
+    int xh_stride;            // bytes between staged f16 x rows (tensor-core path; 64 mod 128)
+    uint32_t x_off, xraw_off, misc_off, red_off, cl_off, bar_off, tab_off;
     uint64_t wait_ns;
 };
 
@@ -268,6 +273,30 @@ __device__ __forceinline__ float fma2_f16_f32(uint32_t q2, uint32_t x2, float ac
 __device__ __forceinline__ float half_lo_f32(uint32_t h2) { return __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xffffu))); }
 __device__ __forceinline__ float half_hi_f32(uint32_t h2) { return __half2float(__ushort_as_half(static_cast<unsigned short>(h2 >> 16))); }
 
+// f16x2 product. E2M1 * E4M3 has at most 6 significant bits and stays in the f16 normal
+// range, so this is the exact dequantised weight pair.
+__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, 0, %2;" : "=r"(d) : "r"(a), "r"(sel));
+    return d;
+}
+
+// D += A * B for one m16n8k16 tile: A 16x16 f16 (row), B 16x8 f16 (col), D 16x8 f32.
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                          uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 __device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
 
@@ -313,116 +342,122 @@ __host__ __device__ constexpr int ilog2(int v) { return v <= 1 ? 0 : 1 + ilog2(v
 
 // ------------------------------------------------------------------ x staging
 
-// fp32 position of element k (within the CTA's K range) in the staged x row. For warp
-// step j, lane l and word w, elements [4h, 4h + 4) of that word sit at
-// ((j * 8 + w * 2 + h) * 32 + l) * 4: a warp's 128-bit reads cover 512 contiguous bytes.
-__device__ __forceinline__ int x_pos(int k) {
-    return ((((k >> 10) * 8 + ((k >> 3) & 3) * 2) * 32) + ((k >> 5) & 31)) * 4 + (k & 3);
-}
-
-// Converts rows of bf16 x (global) to fp32 in shared memory. src_row(m) gives the global
-// row index for staged row m. Shared by the consumer threads: tid in [0, nthreads).
-template <typename RowFn>
-__device__ void stage_x(const uint16_t* __restrict__ x, int64_t K, int k0, int Kr, int rows,
-                        RowFn src_row, float* x32, int xstride, int tid, int nthreads) {
-    const int per_row = Kr / 8;
-    const int total = rows * per_row;
-    const bool vec = (reinterpret_cast<uintptr_t>(x) & 15) == 0;
-    for (int c = tid; c < total; c += nthreads) {
-        const int m = c / per_row;
-        const int k = (c - m * per_row) * 8;
-        const uint16_t* src = x + static_cast<int64_t>(src_row(m)) * K + k0 + k;
-        uint32_t u[4];
-        if (vec) {
-            const uint4 t = __ldg(reinterpret_cast<const uint4*>(src));
-            u[0] = t.x; u[1] = t.y; u[2] = t.z; u[3] = t.w;
-        } else {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) u[i] = src[2 * i] | (static_cast<uint32_t>(src[2 * i + 1]) << 16);
-        }
-        float* dst = x32 + static_cast<int64_t>(m) * xstride + x_pos(k);
-        reinterpret_cast<float4*>(dst)[0] = make_float4(bf16_lo(u[0]), bf16_hi(u[0]), bf16_lo(u[1]), bf16_hi(u[1]));
-        reinterpret_cast<float4*>(dst + 128)[0] = make_float4(bf16_lo(u[2]), bf16_hi(u[2]), bf16_lo(u[3]), bf16_hi(u[3]));
-    }
-}
-
-// Block-scaled f16 staging. For every 16-element block b of the CTA's K range, one power
-// of two 2^E_b (shared by the staged rows) is chosen so that the block's largest |x| lands
-// in [2^12, 2^13). x' = x * 2^-E_b is stored as f16 in the lane layout of h_pos(k), and
-// 2^E_b as f32 in p2[b]. A bf16 value converts exactly unless its scaled magnitude falls
-// below the f16 normal range (more than 2^26 below its block's maximum) or it is not
-// finite. The function returns true if any staged element was not reproduced exactly
-// (x'[k] * 2^E_b != x[k]). The caller then restages x in fp32.
-__device__ __forceinline__ int h_pos(int k) {
-    return ((((k >> 10) * 4 + ((k >> 3) & 3)) * 32) + ((k >> 5) & 31)) * 8 + (k & 7);
-}
-
 __device__ __forceinline__ float pow2f(int e) {  // exact 2^e for e in [-149, 127]
     return e >= -126 ? __int_as_float((e + 127) << 23) : __int_as_float(1 << (e + 149));
 }
 
-template <typename RowFn>
-__device__ bool stage_x_h(const uint16_t* __restrict__ x, int64_t K, int k0, int Kr, int rows, RowFn src_row,
-                          __half* xh, int xh_stride, float* p2, int tid, int nthreads) {
-    const int nb = Kr / 16;
-    const bool vec = (reinterpret_cast<uintptr_t>(x) & 15) == 0;
-    bool lossy = false;
-    for (int b = tid; b < nb; b += nthreads) {
-        const int k = b * 16;
-        uint32_t amax = 0;  // largest bf16 magnitude pattern (ordered like the magnitudes)
-        for (int m = 0; m < rows; ++m) {
-            const uint16_t* src = x + static_cast<int64_t>(src_row(m)) * K + k0 + k;
-            uint32_t u[8];
-            if (vec) {
-                const uint4 t0 = __ldg(reinterpret_cast<const uint4*>(src));
-                const uint4 t1 = __ldg(reinterpret_cast<const uint4*>(src) + 1);
-                u[0] = t0.x; u[1] = t0.y; u[2] = t0.z; u[3] = t0.w; u[4] = t1.x; u[5] = t1.y; u[6] = t1.z; u[7] = t1.w;
-            } else {
+// Byte offset of element k inside a staged f16 x row for the tensor-core path. A row is a
+// sequence of 128-element chunks of 256 bytes; within a chunk, the 8 elements
+// 32t + 8q .. 32t + 8q + 7 (t, q in 0..3) sit at byte (q * 4 + t) * 16. Lane t of an MMA
+// quad then reads its 32 elements with four conflict-free 128-bit loads.
+__host__ __device__ __forceinline__ int mma_x_off(int k) {
+    return (k >> 7) * 256 + ((((k >> 3) & 3) * 4 + ((k >> 5) & 3)) << 4) + ((k & 7) << 1);
+}
+
+__device__ __forceinline__ uint32_t bf16_mag_max(uint4 v) {
+    uint32_t a = max(v.x & 0x7fffu, (v.x >> 16) & 0x7fffu);
+    a = max(a, max(v.y & 0x7fffu, (v.y >> 16) & 0x7fffu));
+    a = max(a, max(v.z & 0x7fffu, (v.z >> 16) & 0x7fffu));
+    return max(a, max(v.w & 0x7fffu, (v.w >> 16) & 0x7fffu));
+}
+
+// Row-scaled f16 staging for the tensor-core path. The raw bf16 rows of x (this CTA's K
+// range) sit in shared memory at xraw, Kr * 2 bytes apart (the producer's bulk copies).
+// For each row m one power of two 2^E_m is chosen so that the row's largest |x| lands in
+// [2^12, 2^13); x' = x * 2^-E_m is stored as f16 at mma_x_off, rows xstride bytes apart,
+// zero-padded to whole 128-element chunks, and e2[m] = 2^E_m. Every bf16 value within 2^26
+// of its row's largest magnitude converts exactly. The function returns true if any element
+// was not reproduced exactly (x'[k] * 2^E_m != x[k], Inf or NaN); the caller then uses
+// the fp32 path. The max pass and the convert pass are separated by the consumers' `bar`
+// (bounded wait on `parity`); `wmax` is [kConsumerWarps][8] words of scratch. `ok` turns
+// false if that wait times out.
+template <int MAXR>
+__device__ bool stage_x_mma(const uint8_t* xraw, int Kr, int rows, uint8_t* xh, int xstride, float* e2,
+                            uint32_t* wmax, uint64_t* bar, uint32_t parity, uint64_t budget, int tid, int nthreads,
+                            bool& ok) {
+    const int per_row = Kr / 8;                 // 8-element chunks per row
+    const int padded = ((Kr + 127) >> 7) * 16;  // chunks per row including the zero tail
+    const int total = rows * per_row;
+    const int lane = tid & 31, warp = tid >> 5;
+    const uint32_t raw = smem_addr(xraw);
+    // pass 1: per-row maxima of |x| (as bf16 magnitude patterns, ordered like the values)
+    uint32_t mx[MAXR];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) u[i] = src[2 * i] | (static_cast<uint32_t>(src[2 * i + 1]) << 16);
-            }
+    for (int m = 0; m < MAXR; ++m) mx[m] = 0;
+    for (int c = tid; c < total; c += nthreads) {
+        const int m = c / per_row;
+        const uint32_t a = bf16_mag_max(lds128(raw + c * 16));
 #pragma unroll
-            for (int i = 0; i < 8; ++i) amax = max(amax, max(u[i] & 0x7fffu, (u[i] >> 16) & 0x7fffu));
-        }
+        for (int r = 0; r < MAXR; ++r)
+            if (m == r) mx[r] = max(mx[r], a);
+    }
+#pragma unroll
+    for (int m = 0; m < MAXR; ++m) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx[m] = max(mx[m], __shfl_xor_sync(0xffffffffu, mx[m], o));
+    }
+    if (lane == 0) {
+#pragma unroll
+        for (int m = 0; m < MAXR; ++m) wmax[warp * 8 + m] = mx[m];
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar);
+    if (!mbar_wait(bar, parity, budget)) {
+        ok = false;
+        return false;
+    }
+    // the row's exponent, same in every thread
+    int E[MAXR];
+#pragma unroll
+    for (int m = 0; m < MAXR; ++m) {
+        uint32_t amax = 0;
+        for (int w = 0; w < nthreads / 32; ++w) amax = max(amax, wmax[w * 8 + m]);
         int e_max;
         if (amax >= 0x7f80u || amax == 0) {
-            e_max = 12;                      // Inf/NaN (reported below) or an all-zero block
+            e_max = 12;                        // Inf/NaN (reported below) or an all-zero row
         } else if ((amax >> 7) == 0) {
             e_max = (31 - __clz(amax)) - 133;  // bf16 subnormal: mant * 2^-133
         } else {
             e_max = static_cast<int>(amax >> 7) - 127;
         }
-        const int E = e_max - 12;
-        const float scale_back = pow2f(E);
-        const int a = min(-E, 127);
-        const float sa = pow2f(a);
-        const float sb = pow2f(-E - a);
-        p2[b] = scale_back;
-        for (int m = 0; m < rows; ++m) {
-            const uint16_t* src = x + static_cast<int64_t>(src_row(m)) * K + k0 + k;
-            uint32_t u[8];
-            if (vec) {
-                const uint4 t0 = __ldg(reinterpret_cast<const uint4*>(src));
-                const uint4 t1 = __ldg(reinterpret_cast<const uint4*>(src) + 1);
-                u[0] = t0.x; u[1] = t0.y; u[2] = t0.z; u[3] = t0.w; u[4] = t1.x; u[5] = t1.y; u[6] = t1.z; u[7] = t1.w;
-            } else {
+        E[m] = e_max - 12;
+    }
+    if (tid < rows) {
 #pragma unroll
-                for (int i = 0; i < 8; ++i) u[i] = src[2 * i] | (static_cast<uint32_t>(src[2 * i + 1]) << 16);
-            }
-            uint32_t out[8];
+        for (int m = 0; m < MAXR; ++m)
+            if (m == tid) e2[m] = pow2f(E[m]);
+    }
+    // pass 2: scale, convert, check, store
+    bool lossy = false;
+    for (int c = tid; c < total; c += nthreads) {
+        const int m = c / per_row;
+        const int k = (c - m * per_row) * 8;
+        int e = 0;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float f0 = bf16_lo(u[i]), f1 = bf16_hi(u[i]);
-                const __half h0 = __float2half_rn((f0 * sa) * sb);
-                const __half h1 = __float2half_rn((f1 * sa) * sb);
-                lossy |= !isfinite(f0) || !isfinite(f1) || __half2float(h0) * scale_back != f0 ||
-                         __half2float(h1) * scale_back != f1;
-                out[i] = static_cast<uint32_t>(__half_as_ushort(h0)) | (static_cast<uint32_t>(__half_as_ushort(h1)) << 16);
-            }
-            __half* dst = xh + static_cast<int64_t>(m) * xh_stride + h_pos(k);
-            reinterpret_cast<uint4*>(dst)[0] = make_uint4(out[0], out[1], out[2], out[3]);
-            reinterpret_cast<uint4*>(dst + 256)[0] = make_uint4(out[4], out[5], out[6], out[7]);
+        for (int r = 0; r < MAXR; ++r)
+            if (m == r) e = E[r];
+        const float back = pow2f(e);
+        const int a = min(-e, 127);
+        const float sa = pow2f(a), sb = pow2f(-e - a);
+        const uint4 v = lds128(raw + c * 16);
+        const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+        uint32_t out[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float f0 = bf16_lo(u[i]), f1 = bf16_hi(u[i]);
+            const __half h0 = __float2half_rn((f0 * sa) * sb);
+            const __half h1 = __float2half_rn((f1 * sa) * sb);
+            lossy |= !isfinite(f0) || !isfinite(f1) || __half2float(h0) * back != f0 || __half2float(h1) * back != f1;
+            out[i] = static_cast<uint32_t>(__half_as_ushort(h0)) | (static_cast<uint32_t>(__half_as_ushort(h1)) << 16);
         }
+        *reinterpret_cast<uint4*>(xh + m * xstride + mma_x_off(k)) = make_uint4(out[0], out[1], out[2], out[3]);
+    }
+    // zero tail up to the next 128-element chunk
+    const int tail = padded - per_row;
+    for (int c = tid; c < rows * tail; c += nthreads) {
+        const int m = c / tail;
+        const int k = (per_row + (c - m * tail)) * 8;
+        *reinterpret_cast<uint4*>(xh + m * xstride + mma_x_off(k)) = make_uint4(0u, 0u, 0u, 0u);
     }
     return lossy;
 }
@@ -458,13 +493,16 @@ __device__ __forceinline__ void store_partials(float (&v)[next_pow2(R * MTE)], i
     }
 }
 
-// One item's share of one consumer warp: rows rb = wr*R, wr*R + cr*R, ... (batches of R)
-// and warp steps j = wk, wk + ck, ... Partials go to red[(wk * rpi + row) * mstride + m].
+// Exact fp32 path (used when x does not fit the row-scaled f16 staging exactly): one item's
+// share of one consumer warp, rows rb = wr*R, wr*R + cr*R, ... in batches of R and
+// 1024-element steps j = wk, wk + ck, ... x is read straight from global memory (bf16, L2
+// resident); xrow[m] points at row m's element k0. Partials go to
+// red[(wk * rpi + row) * mstride + m].
 template <int MTE, int R>
-__device__ __forceinline__ void compute_item(uint32_t wst, uint32_t sst, int wrow_bytes, int srow_bytes,
-                                             uint32_t x32, int xstride_bytes, int rows, int Kr, int J,
-                                             int wr, int wk, int cr, int ck, int lane,
-                                             float* red, int rpi, int mstride) {
+__device__ __noinline__ void compute_item_f32(uint32_t wst, uint32_t sst, int wstride, int srow_bytes,
+                                                 const uint16_t* const (&xrow)[8], int rows, int Kr, int J, int wr,
+                                                 int wk, int cr, int ck, int lane, float* red, int rpi,
+                                                 int mstride) {
     constexpr int V = R * MTE;
     constexpr int VP = next_pow2(V);
     for (int rb = wr * R; rb < rows; rb += cr * R) {
@@ -483,7 +521,7 @@ __device__ __forceinline__ void compute_item(uint32_t wst, uint32_t sst, int wro
                 for (int r = 0; r < R; ++r) {
                     const int row = rb + r;
                     if (row < rows) {
-                        wv[r] = lds128(wst + row * wrow_bytes + (kl >> 1));
+                        wv[r] = lds128(wst + row * wstride + (kl >> 1));
                         sh[r] = cvt_e4m3x2(lds16(sst + row * srow_bytes + (kl >> 4)));
                     } else {
                         wv[r] = make_uint4(0u, 0u, 0u, 0u);
@@ -495,13 +533,12 @@ __device__ __forceinline__ void compute_item(uint32_t wst, uint32_t sst, int wro
                     float2 xp[MTE][4];
 #pragma unroll
                     for (int m = 0; m < MTE; ++m) {
-                        const uint32_t xa = x32 + m * xstride_bytes + (((j * 8 + w * 2) * 32 + lane) << 4);
-                        const float4 a = lds128f(xa);
-                        const float4 b = lds128f(xa + 32 * 16);
-                        xp[m][0] = make_float2(a.x, a.y);
-                        xp[m][1] = make_float2(a.z, a.w);
-                        xp[m][2] = make_float2(b.x, b.y);
-                        xp[m][3] = make_float2(b.z, b.w);
+                        const uint16_t* src = xrow[m] + kl + w * 8;
+                        uint32_t u[4];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) u[i] = src[2 * i] | (static_cast<uint32_t>(src[2 * i + 1]) << 16);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) xp[m][i] = make_float2(bf16_lo(u[i]), bf16_hi(u[i]));
                     }
 #pragma unroll
                     for (int r = 0; r < R; ++r) {
@@ -527,83 +564,82 @@ __device__ __forceinline__ void compute_item(uint32_t wst, uint32_t sst, int wro
     }
 }
 
-// One item's share of one consumer warp on the block-scaled f16 x (see stage_x_h): per
-// 16-element block, part = sum E2M1 * x' with mixed f16 x f16 -> f32 FMAs, then
-// acc += part * (E4M3 scale * 2^E_b).
-template <int MTE, int R>
-__device__ __forceinline__ void compute_item_h(uint32_t wst, uint32_t sst, int wrow_bytes, int srow_bytes,
-                                               uint32_t xh, int xh_stride_bytes, uint32_t p2a, int rows, int Kr,
-                                               int J, int wr, int wk, int cr, int ck, int lane,
-                                               float* red, int rpi, int mstride) {
-    constexpr int V = R * MTE;
-    constexpr int VP = next_pow2(V);
-    for (int rb = wr * R; rb < rows; rb += cr * R) {
-        float acc[R][MTE];
+// One item's share of one consumer warp on the tensor-core path. The item's rows form
+// 16-row tiles (the MMA's M); warp (wr, wk) takes tiles wr, wr + cr, ... and 128-element
+// K steps wk, wk + ck, ... Lane (g, t) of the MMA quad layout decodes the 32 nibbles
+// 32t .. 32t + 31 of each step for rows g and g + 8 (one 128-bit load each). The MMA's
+// logical k index is a fixed permutation of these physical positions, and the staged x
+// (stage_x_mma) uses the same one, so the dot product is unchanged. A holds
+// E2M1 * E4M3 in f16 (exact), B the row-scaled f16 x, D accumulates in f32. The partial
+// sums, times each x row's 2^E_m, go to red[(wk * rpi + row) * mstride + m].
+template <int MTE>
+__device__ __forceinline__ void compute_item_mma(uint32_t wst, int wstride, uint32_t sst, int srow_bytes,
+                                                 uint32_t xa, int xstride, const float* e2, int rows, int Kr,
+                                                 int wr, int wk, int cr, int ck, int lane, float* red, int rpi,
+                                                 int mstride) {
+    const int g = lane >> 2, t = lane & 3;
+    const int nsteps = (Kr + 127) >> 7;
+    const int ntiles = (rows + 15) >> 4;
+    const bool xcol = g < MTE;
+    const int m0 = 2 * t;
+    const float e2a = m0 < MTE ? e2[m0] : 0.f;
+    const float e2b = m0 + 1 < MTE ? e2[m0 + 1] : 0.f;
+    for (int tile = wr; tile < ntiles; tile += cr) {
+        const int ra = tile * 16 + g, rb = ra + 8;
+        const bool va = ra < rows, vb = rb < rows;
+        const bool upper = tile * 16 + 8 < rows;  // warp-uniform: the tile's rows 8..15 exist
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int j = wk; j < nsteps; j += ck) {
+            const int kt = (j << 7) + (t << 5);
+            const bool vk = kt < Kr;
+            uint4 wa = make_uint4(0u, 0u, 0u, 0u), wb = wa;
+            uint32_t sa = 0u, sb = 0u;
+            if (vk && va) {
+                wa = lds128(wst + ra * wstride + (kt >> 1));
+                sa = cvt_e4m3x2(lds16(sst + ra * srow_bytes + (kt >> 4)));
+            }
+            if (vk && vb) {
+                wb = lds128(wst + rb * wstride + (kt >> 1));
+                sb = cvt_e4m3x2(lds16(sst + rb * srow_bytes + (kt >> 4)));
+            }
+            uint4 xq[4];
 #pragma unroll
-        for (int r = 0; r < R; ++r)
+            for (int q = 0; q < 4; ++q)
+                xq[q] = xcol ? lds128(xa + g * xstride + (j << 8) + ((q * 4 + t) << 4)) : make_uint4(0u, 0u, 0u, 0u);
+            const uint32_t sa0 = prmt(sa, 0x1010u), sa1 = prmt(sa, 0x3232u);
+            const uint32_t sb0 = prmt(sb, 0x1010u), sb1 = prmt(sb, 0x3232u);
+            if (upper) {
 #pragma unroll
-            for (int m = 0; m < MTE; ++m) acc[r][m] = 0.f;
-
-        for (int j = wk; j < J; j += ck) {
-            const int kl = j * kStepElems + lane * 32;
-            if (kl < Kr) {
-                uint4 wv[R];
-                uint32_t sh[R];
-#pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    const int row = rb + r;
-                    if (row < rows) {
-                        wv[r] = lds128(wst + row * wrow_bytes + (kl >> 1));
-                        sh[r] = cvt_e4m3x2(lds16(sst + row * srow_bytes + (kl >> 4)));
-                    } else {
-                        wv[r] = make_uint4(0u, 0u, 0u, 0u);
-                        sh[r] = 0u;
-                    }
+                for (int w = 0; w < 4; ++w) {
+                    uint32_t ha[4], hb[4];
+                    cvt_e2m1x8(w == 0 ? wa.x : (w == 1 ? wa.y : (w == 2 ? wa.z : wa.w)), ha);
+                    cvt_e2m1x8(w == 0 ? wb.x : (w == 1 ? wb.y : (w == 2 ? wb.z : wb.w)), hb);
+                    const uint32_t s_a = w < 2 ? sa0 : sa1, s_b = w < 2 ? sb0 : sb1;
+                    mma_16816(d, hmul2_u32(ha[0], s_a), hmul2_u32(hb[0], s_b), hmul2_u32(ha[1], s_a),
+                              hmul2_u32(hb[1], s_b), xq[w].x, xq[w].y);
+                    mma_16816(d, hmul2_u32(ha[2], s_a), hmul2_u32(hb[2], s_b), hmul2_u32(ha[3], s_a),
+                              hmul2_u32(hb[3], s_b), xq[w].z, xq[w].w);
                 }
-                const float2 pp = lds64f(p2a + ((kl >> 4) << 2));
+            } else {  // rows 8..15 of the tile are empty: their A halves are zero
 #pragma unroll
-                for (int bb = 0; bb < 2; ++bb) {
-                    float part[R][MTE];
-#pragma unroll
-                    for (int r = 0; r < R; ++r)
-#pragma unroll
-                        for (int m = 0; m < MTE; ++m) part[r][m] = 0.f;
-#pragma unroll
-                    for (int ww = 0; ww < 2; ++ww) {
-                        const int w = bb * 2 + ww;
-                        uint4 xw[MTE];
-#pragma unroll
-                        for (int m = 0; m < MTE; ++m)
-                            xw[m] = lds128(xh + m * xh_stride_bytes + (((j * 4 + w) * 32 + lane) << 4));
-#pragma unroll
-                        for (int r = 0; r < R; ++r) {
-                            const uint32_t word = w == 0 ? wv[r].x : (w == 1 ? wv[r].y : (w == 2 ? wv[r].z : wv[r].w));
-                            uint32_t h[4];
-                            cvt_e2m1x8(word, h);
-#pragma unroll
-                            for (int m = 0; m < MTE; ++m) {
-                                part[r][m] = fma2_f16_f32(h[0], xw[m].x, part[r][m]);
-                                part[r][m] = fma2_f16_f32(h[1], xw[m].y, part[r][m]);
-                                part[r][m] = fma2_f16_f32(h[2], xw[m].z, part[r][m]);
-                                part[r][m] = fma2_f16_f32(h[3], xw[m].w, part[r][m]);
-                            }
-                        }
-                    }
-                    const float pb = bb ? pp.y : pp.x;
-#pragma unroll
-                    for (int r = 0; r < R; ++r) {
-                        const float fac = (bb ? half_hi_f32(sh[r]) : half_lo_f32(sh[r])) * pb;
-#pragma unroll
-                        for (int m = 0; m < MTE; ++m) acc[r][m] = fmaf(part[r][m], fac, acc[r][m]);
-                    }
+                for (int w = 0; w < 4; ++w) {
+                    uint32_t ha[4];
+                    cvt_e2m1x8(w == 0 ? wa.x : (w == 1 ? wa.y : (w == 2 ? wa.z : wa.w)), ha);
+                    const uint32_t s_a = w < 2 ? sa0 : sa1;
+                    mma_16816(d, hmul2_u32(ha[0], s_a), 0u, hmul2_u32(ha[1], s_a), 0u, xq[w].x, xq[w].y);
+                    mma_16816(d, hmul2_u32(ha[2], s_a), 0u, hmul2_u32(ha[3], s_a), 0u, xq[w].z, xq[w].w);
                 }
             }
         }
-
-        float v[VP];
-#pragma unroll
-        for (int i = 0; i < VP; ++i) v[i] = i < V ? acc[i / MTE][i % MTE] : 0.f;
-        store_partials<R, MTE>(v, lane, rb, rows, red + wk * rpi * mstride, mstride);
+        float* base = red + wk * rpi * mstride;
+        if (va) {
+            if (m0 < MTE) base[ra * mstride + m0] = d[0] * e2a;
+            if (m0 + 1 < MTE) base[ra * mstride + m0 + 1] = d[1] * e2b;
+        }
+        if (vb) {
+            if (m0 < MTE) base[rb * mstride + m0] = d[2] * e2a;
+            if (m0 + 1 < MTE) base[rb * mstride + m0 + 1] = d[3] * e2b;
+        }
     }
 }
 
@@ -615,13 +651,24 @@ struct Item {
     int rows;
 };
 
-__device__ __forceinline__ Item item_at(const Params& p, int it) {
-    Item r;
-    r.group = it / p.chunks;
-    r.row0 = (it - r.group * p.chunks) * p.rpi;
-    r.rows = min(p.rpi, p.N - r.row0);
-    return r;
-}
+// Walks a contiguous block of items in order without per-item divisions.
+struct ItemWalk {
+    int group, chunk;
+    __device__ __forceinline__ ItemWalk(const Params& p, int it) : group(it / p.chunks), chunk(it - (it / p.chunks) * p.chunks) {}
+    __device__ __forceinline__ Item get(const Params& p) const {
+        Item r;
+        r.group = group;
+        r.row0 = chunk * p.rpi;
+        r.rows = min(p.rpi, p.N - r.row0);
+        return r;
+    }
+    __device__ __forceinline__ void next(const Params& p) {
+        if (++chunk == p.chunks) {
+            chunk = 0;
+            ++group;
+        }
+    }
+};
 
 // MoE: expert groups from the routing (same result in every CTA). A group is up to
 // p.mstride slots routed to one expert; slots of one expert are served by one read.
@@ -707,28 +754,28 @@ __device__ void build_moe_tables(const Params& p, MoeTables* tab, int* scratch) 
 // ------------------------------------------------------------------ the streaming kernel
 
 __host__ __device__ constexpr int rows_per_batch(int mte) { return mte <= 2 ? 8 : 4; }
+constexpr int kTileRows = 16;  // rows of one MMA tile (tensor-core path)
+constexpr int kNumBars = 4 * kMaxStages + 5;
 
-// Dispatches one item's consumer work to the f16 path (x staged block-scaled in f16,
-// M <= 4) or the fp32 path.
+// Dispatches one item's consumer work to the tensor-core path (x staged row-scaled in f16)
+// or the exact fp32 path.
 template <int MTE>
-__device__ __forceinline__ void compute_dispatch(bool use_h, uint32_t wst, uint32_t sst, int wrow_bytes,
-                                                 int srow_bytes, uint32_t xa, int xstride_elems, uint32_t p2a,
-                                                 int rows, int Kr, int J, int wr, int wk, int cr, int ck,
-                                                 int lane, float* red, int rpi, int mstride) {
-    constexpr int R = rows_per_batch(MTE);
-    if constexpr (MTE <= 4) {
-        if (use_h) {
-            compute_item_h<MTE, R>(wst, sst, wrow_bytes, srow_bytes, xa, xstride_elems * 2, p2a, rows, Kr, J, wr,
-                                   wk, cr, ck, lane, red, rpi, mstride);
-            return;
-        }
+__device__ __forceinline__ void compute_dispatch(bool use_mma, uint32_t wst, int wstride, uint32_t sst,
+                                                 int srow_bytes, uint32_t xa, int xh_stride,
+                                                 const uint16_t* const (&xrow)[8], const float* e2, int rows, int Kr,
+                                                 int J, int wr, int wk, int cr, int ck, int lane, float* red, int rpi,
+                                                 int mstride) {
+    if (use_mma) {
+        compute_item_mma<MTE>(wst, wstride, sst, srow_bytes, xa, xh_stride, e2, rows, Kr, wr, wk, cr, ck, lane, red,
+                              rpi, mstride);
+    } else {
+        compute_item_f32<MTE, rows_per_batch(MTE)>(wst, sst, wstride, srow_bytes, xrow, rows, Kr, J, wr, wk, cr, ck,
+                                                   lane, red, rpi, mstride);
     }
-    compute_item<MTE, R>(wst, sst, wrow_bytes, srow_bytes, xa, xstride_elems * 4, rows, Kr, J, wr, wk, cr, ck,
-                         lane, red, rpi, mstride);
 }
 
 template <int MODE, int MT>
-__global__ void __launch_bounds__(kThreads, (MT <= 1 ? 2 : 1)) gemv_stream_kernel(const __grid_constant__ Params p) {
+__global__ void __launch_bounds__(kThreads, 2) gemv_stream_kernel(const __grid_constant__ Params p) {
     extern __shared__ __align__(128) uint8_t smem[];
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.bar_off);
     uint64_t* full = bars;
@@ -737,11 +784,16 @@ __global__ void __launch_bounds__(kThreads, (MT <= 1 ? 2 : 1)) gemv_stream_kerne
     uint64_t* rempty = bars + 3 * kMaxStages;
     uint64_t* xready = bars + 4 * kMaxStages;
     uint64_t* xfree = bars + 4 * kMaxStages + 1;
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 4 * kMaxStages + 2);
+    uint64_t* xmax = bars + 4 * kMaxStages + 2;
+    uint64_t* xraw_full = bars + 4 * kMaxStages + 3;   // raw x rows landed (bulk copies)
+    uint64_t* xraw_empty = bars + 4 * kMaxStages + 4;  // consumers converted them
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + kNumBars);
     volatile int* lossy_flag = abort_flag + 1;
     float* red_base = reinterpret_cast<float*>(smem + p.red_off);
     float* clpart = reinterpret_cast<float*>(smem + p.cl_off);
     MoeTables* tab = reinterpret_cast<MoeTables*>(smem + p.tab_off);
+    float* e2 = reinterpret_cast<float*>(smem + p.misc_off);              // [8]
+    uint32_t* wmax = reinterpret_cast<uint32_t*>(smem + p.misc_off) + 8;  // [kConsumerWarps][8]
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -760,6 +812,9 @@ __global__ void __launch_bounds__(kThreads, (MT <= 1 ? 2 : 1)) gemv_stream_kerne
         }
         mbar_init(xready, kConsumerWarps);
         mbar_init(xfree, kConsumerWarps);
+        mbar_init(xmax, kConsumerWarps);
+        mbar_init(xraw_full, 1);
+        mbar_init(xraw_empty, kConsumerWarps);
         *abort_flag = 0;
         *lossy_flag = 0;
         fence_barrier_init();
@@ -771,30 +826,40 @@ __global__ void __launch_bounds__(kThreads, (MT <= 1 ? 2 : 1)) gemv_stream_kerne
     __syncthreads();
     pdl_launch_dependents();
 
-    const int items = MODE == kModeMoe ? tab->n_groups * p.chunks : p.items;
-    const int ib = static_cast<int>(static_cast<int64_t>(items) * cluster / n_clusters);
-    const int ie = static_cast<int>(static_cast<int64_t>(items) * (cluster + 1) / n_clusters);
+    // this cluster's contiguous block of items: q or q + 1 of them
+    int ib, ie;
+    if constexpr (MODE == kModeMoe) {
+        const int items = tab->n_groups * p.chunks;
+        const int q = items / n_clusters, r = items - q * n_clusters;
+        ib = cluster * q + min(cluster, r);
+        ie = ib + q + (cluster < r ? 1 : 0);
+    } else {
+        ib = cluster * p.items_q + min(cluster, p.items_r);
+        ie = ib + p.items_q + (cluster < p.items_r ? 1 : 0);
+    }
     const int64_t Kh = p.K / 2;
     const int64_t Ks = p.K / 16;
-    const int wrow_bytes = p.S == 1 ? p.K / 2 : p.Kr / 2;
     const int srow_bytes = p.S == 1 ? p.K / 16 : p.Kr / 16;
-    const uint32_t scale_region = static_cast<uint32_t>(p.rpi) * wrow_bytes;  // multiple of 16
+    const uint32_t scale_region = static_cast<uint32_t>(p.rpi) * p.wstride;  // multiple of 64
 
     if (warp == kProducerWarp) {
-        // ---------------- producer: TMA bulk copies of the (read-only) weights into the ring.
-        // They may start before the preceding kernel has finished.
+        // ---------------- producer: TMA bulk copies of the (read-only) weights into the ring,
+        // and of the raw x rows. Weights may stream before the preceding kernel has finished;
+        // x is copied only after it has (pdl_wait).
         int issued = 0;
-        for (int it = ib; it < ie; ++it) {
+        int xkey = -1, xq = 0;  // rows whose x copy was issued; copies issued so far
+        bool xfirst_pending = true;
+        ItemWalk walk(p, ib);
+        int slot = 0, use = 0;
+        for (int it = ib; it < ie; ++it, walk.next(p), slot = slot + 1 == NS ? 0 : slot + 1, use += slot == 0) {
             const int li = it - ib;
-            const int slot = li % NS;
-            const int use = li / NS;
             if (use > 0 && !mbar_wait(&empty[slot], (use - 1) & 1, p.wait_ns)) {
                 *abort_flag = 1;
                 if (lane == 0) raise_status(NVFP4_DEV_TIMEOUT, p.status_user);
                 break;
             }
             if (*abort_flag) break;
-            const Item ii = item_at(p, it);
+            const Item ii = walk.get(p);
             const uint8_t* wsrc;
             const uint8_t* ssrc;
             if constexpr (MODE == kModeMoe) {
@@ -807,35 +872,76 @@ __global__ void __launch_bounds__(kThreads, (MT <= 1 ? 2 : 1)) gemv_stream_kerne
             }
             uint8_t* wdst = smem + slot * p.stage_stride;
             uint8_t* sdst = wdst + scale_region;
-            if (p.S == 1) {
-                const uint32_t wbytes = static_cast<uint32_t>(ii.rows) * wrow_bytes;
+            const uint32_t wb = p.Kr / 2;
+            uint32_t sbytes_tx = 0;
+            uint32_t mis = 0, head = 0, mid = 0, tail = 0;
+            if (p.S > 1 || p.s_aligned) {
+                sbytes_tx = static_cast<uint32_t>(ii.rows) * srow_bytes;
+            } else {
+                // unaligned scale range: plain copies of the head and tail bytes, TMA for the rest
                 const uint32_t sbytes = static_cast<uint32_t>(ii.rows) * srow_bytes;
-                const uint32_t mis = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(ssrc) & 15);
-                uint32_t head = (16 - mis) & 15;
+                mis = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(ssrc) & 15);
+                head = (16 - mis) & 15;
                 if (head > sbytes) head = sbytes;
-                const uint32_t mid = (sbytes - head) & ~15u;
-                const uint32_t tail = sbytes - head - mid;
-                // unaligned head/tail scale bytes by plain copies, ordered before the arrive
+                mid = (sbytes - head) & ~15u;
+                tail = sbytes - head - mid;
                 if (lane < head) sdst[mis + lane] = ssrc[lane];
                 if (lane < tail) sdst[mis + head + mid + lane] = ssrc[head + mid + lane];
-                __syncwarp();
+                sbytes_tx = mid;
+            }
+            __syncwarp();  // the plain copies are ordered before the arrive below
+            if (lane == 0) mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(ii.rows) * wb + sbytes_tx);
+            __syncwarp();
+            if (p.S == 1) {
+                // whole rows are contiguous in HBM and in the slot: one copy for the codes
                 if (lane == 0) {
-                    mbar_arrive_expect_tx(&full[slot], wbytes + mid);
-                    bulk_g2s(wdst, wsrc, wbytes, &full[slot]);
-                    if (mid) bulk_g2s(sdst + mis + head, ssrc + head, mid, &full[slot]);
+                    bulk_g2s(wdst, wsrc, static_cast<uint32_t>(ii.rows) * wb, &full[slot]);
+                    if (p.s_aligned) bulk_g2s(sdst, ssrc, sbytes_tx, &full[slot]);
+                    else if (mid) bulk_g2s(sdst + mis + head, ssrc + head, mid, &full[slot]);
                 }
             } else {
-                const uint32_t wb = p.Kr / 2, sb = p.Kr / 16;
-                if (lane == 0) mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(ii.rows) * (wb + sb));
-                __syncwarp();
                 for (int r = lane; r < ii.rows; r += 32) {
-                    bulk_g2s(wdst + r * wb, wsrc + r * Kh + k0 / 2, wb, &full[slot]);
-                    bulk_g2s(sdst + r * sb, ssrc + r * Ks + k0 / 16, sb, &full[slot]);
+                    bulk_g2s(wdst + r * p.wstride, wsrc + r * Kh + k0 / 2, wb, &full[slot]);
+                    bulk_g2s(sdst + r * srow_bytes, ssrc + r * Ks + k0 / 16, srow_bytes, &full[slot]);
                 }
             }
             __syncwarp();
             issued = li + 1;
+            // raw x rows: dense x once, after the first slots' weights are on their way; MoE
+            // each time the expert group changes, once the consumers have released the buffer
+            const int key = MODE == kModeMoe ? ii.group : 0;
+            const bool want_x = MODE == kModeMoe ? key != xkey
+                                                 : (xfirst_pending && (li == NS - 1 || it == ie - 1));
+            if (want_x) {
+                if (xq > 0 && !mbar_wait(xraw_empty, (xq - 1) & 1, p.wait_ns)) {
+                    *abort_flag = 1;
+                    if (lane == 0) raise_status(NVFP4_DEV_TIMEOUT, p.status_user);
+                    break;
+                }
+                if constexpr (MODE != kModeMoe) pdl_wait();  // x may come from the preceding kernel
+                int nrows = MT, first = 0;
+                if constexpr (MODE == kModeMoe) {
+                    nrows = tab->count[key];
+                    first = tab->first[key];
+                }
+                const uint32_t rb = static_cast<uint32_t>(p.Kr) * 2;
+                if (lane == 0) mbar_arrive_expect_tx(xraw_full, static_cast<uint32_t>(nrows) * rb);
+                __syncwarp();
+                for (int m = lane; m < nrows; m += 32) {
+                    int row = m;
+                    if constexpr (MODE == kModeMoe) {
+                        const int sl = tab->member_list[first + m];
+                        row = p.x_per_slot ? sl : sl / p.top_k;
+                    }
+                    bulk_g2s(smem + p.xraw_off + m * rb, p.x + static_cast<int64_t>(row) * p.K + k0, rb, xraw_full);
+                }
+                __syncwarp();
+                xkey = key;
+                ++xq;
+                xfirst_pending = false;
+            }
         }
+        if (xq > 0) mbar_wait(xraw_full, (xq - 1) & 1, kDrainWaitNs);
         // Every slot's latest issued copy must land before the CTA can retire, also when the
         // consumers gave up early. In a normal run these waits return at once.
         for (int li = issued - 1; li >= 0 && li >= issued - NS; --li) {
@@ -844,17 +950,16 @@ __global__ void __launch_bounds__(kThreads, (MT <= 1 ? 2 : 1)) gemv_stream_kerne
     } else if (warp == kEpilogueWarp) {
         // ---------------- epilogue: fixed-order sum over K-warps, scale, store
         int64_t local_row = 0;
-        for (int it = ib; it < ie; ++it) {
-            const int li = it - ib;
-            const int slot = li % NS;
-            const int use = li / NS;
+        ItemWalk walk(p, ib);
+        int slot = 0, use = 0;
+        for (int it = ib; it < ie; ++it, walk.next(p), slot = slot + 1 == NS ? 0 : slot + 1, use += slot == 0) {
             if (!mbar_wait(&rfull[slot], use & 1, p.wait_ns)) {
                 *abort_flag = 1;
                 if (lane == 0) raise_status(NVFP4_DEV_TIMEOUT, p.status_user);
                 break;
             }
             if (*abort_flag) break;
-            const Item ii = item_at(p, it);
+            const Item ii = walk.get(p);
             const float* red = red_base + slot * (p.ck * p.rpi * p.mstride);
             int mrows = MT;
             float gsc = 0.f;
@@ -888,22 +993,17 @@ __global__ void __launch_bounds__(kThreads, (MT <= 1 ? 2 : 1)) gemv_stream_kerne
         const int wk = warp % p.ck;
         const int wr = warp / p.ck;
         const int ctid = threadIdx.x;  // consumer warps are 0..7
-        const int xstride = p.J * kStepElems;  // elements per staged x row (fp32 or f16)
-        float* x32 = reinterpret_cast<float*>(smem + p.x_off);
-        __half* xh = reinterpret_cast<__half*>(smem + p.x_off);
-        float* p2 = reinterpret_cast<float*>(smem + p.p2_off);
         const uint32_t xa = smem_addr(smem + p.x_off);
-        const uint32_t p2a = smem_addr(p2);
+        const uint16_t* xrow[8];
         int cur_key = -1;
-        int xr = 0, xf = 0;  // completed phases of xready / xfree
-        bool use_h = false;
+        int xr = 0, xf = 0, xm = 0, xq = 0;  // completed phases of xready / xfree / xmax / xraw_full
+        bool use_mma = false;
         bool ok = true;
         if constexpr (MODE != kModeMoe) pdl_wait();  // x may come from the preceding kernel
-        for (int it = ib; it < ie && ok; ++it) {
-            const int li = it - ib;
-            const int slot = li % NS;
-            const int use = li / NS;
-            const Item ii = item_at(p, it);
+        ItemWalk walk(p, ib);
+        int slot = 0, use = 0;
+        for (int it = ib; it < ie && ok; ++it, walk.next(p), slot = slot + 1 == NS ? 0 : slot + 1, use += slot == 0) {
+            const Item ii = walk.get(p);
             const int key = MODE == kModeMoe ? ii.group : 0;
             if (key != cur_key) {
                 // hand over the x buffer: all consumers done with the old rows, then restage
@@ -929,25 +1029,31 @@ __global__ void __launch_bounds__(kThreads, (MT <= 1 ? 2 : 1)) gemv_stream_kerne
                         return m;
                     }
                 };
-                bool want_h = nrows <= 4 && !p.force_f32;
-                if (want_h) {
-                    if (stage_x_h(p.x, p.K, k0, p.Kr, nrows, src_row, xh, xstride, p2, ctid, kConsumerWarps * 32))
-                        *lossy_flag = xr + 1;
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(xready);
-                    if (!mbar_wait(xready, xr & 1, p.wait_ns)) { ok = false; break; }
-                    ++xr;
-                    want_h = *lossy_flag != xr;
-                    if (!want_h && ctid == 0) atomicAdd(&g_fp32_fallbacks, 1ull);
+#pragma unroll
+                for (int m = 0; m < 8; ++m)
+                    xrow[m] = p.x + static_cast<int64_t>(m < nrows ? src_row(m) : 0) * p.K + k0;
+                bool lossy = true;
+                if (!p.force_f32) {
+                    if (!mbar_wait(xraw_full, xq & 1, p.wait_ns)) { ok = false; break; }
+                    bool sok = true;
+                    lossy = stage_x_mma<MT>(smem + p.xraw_off, p.Kr, nrows, smem + p.x_off, p.xh_stride, e2, wmax,
+                                            xmax, xm & 1, p.wait_ns, ctid, kConsumerWarps * 32, sok);
+                    ++xm;
+                    if (!sok) { ok = false; break; }
+                } else if (!mbar_wait(xraw_full, xq & 1, p.wait_ns)) {
+                    ok = false;
+                    break;
                 }
-                if (!want_h) {
-                    stage_x(p.x, p.K, k0, p.Kr, nrows, src_row, x32, xstride, ctid, kConsumerWarps * 32);
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(xready);
-                    if (!mbar_wait(xready, xr & 1, p.wait_ns)) { ok = false; break; }
-                    ++xr;
-                }
-                use_h = want_h;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(xraw_empty);  // the raw rows may be replaced now
+                ++xq;
+                if (lossy) *lossy_flag = xr + 1;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(xready);
+                if (!mbar_wait(xready, xr & 1, p.wait_ns)) { ok = false; break; }
+                ++xr;
+                use_mma = *lossy_flag != xr;
+                if (!use_mma && !p.force_f32 && ctid == 0) atomicAdd(&g_fp32_fallbacks, 1ull);
                 cur_key = key;
             }
             if (!mbar_wait(&full[slot], use & 1, p.wait_ns)) { ok = false; break; }
@@ -956,7 +1062,7 @@ __global__ void __launch_bounds__(kThreads, (MT <= 1 ? 2 : 1)) gemv_stream_kerne
 
             const uint32_t wst = smem_addr(smem + slot * p.stage_stride);
             uint32_t sst = wst + scale_region;
-            if (p.S == 1) {
+            if (p.S == 1 && !p.s_aligned) {
                 const uint8_t* ssrc;
                 if constexpr (MODE == kModeMoe) {
                     ssrc = p.s[0] + (static_cast<int64_t>(tab->expert[ii.group]) * p.N + ii.row0) * Ks;
@@ -969,11 +1075,11 @@ __global__ void __launch_bounds__(kThreads, (MT <= 1 ? 2 : 1)) gemv_stream_kerne
             if constexpr (MODE == kModeMoe) {
                 const int cnt = tab->count[ii.group];
                 switch (cnt) {
-#define NVFP4_MOE_CASE(C)                                                                                      \
-    case C:                                                                                                    \
-        if constexpr (C <= MT)                                                                                 \
-            compute_dispatch<C>(use_h, wst, sst, wrow_bytes, srow_bytes, xa, xstride, p2a, ii.rows, p.Kr, p.J, \
-                                wr, wk, p.cr, p.ck, lane, red, p.rpi, p.mstride);                              \
+#define NVFP4_MOE_CASE(C)                                                                                        \
+    case C:                                                                                                      \
+        if constexpr (C <= MT)                                                                                   \
+            compute_dispatch<C>(use_mma, wst, p.wstride, sst, srow_bytes, xa, p.xh_stride, xrow, e2, ii.rows,    \
+                                p.Kr, p.J, wr, wk, p.cr, p.ck, lane, red, p.rpi, p.mstride);                     \
         break;
                     NVFP4_MOE_CASE(1)
                     NVFP4_MOE_CASE(2)
@@ -987,8 +1093,8 @@ __global__ void __launch_bounds__(kThreads, (MT <= 1 ? 2 : 1)) gemv_stream_kerne
                     default: break;
                 }
             } else {
-                compute_dispatch<MT>(use_h, wst, sst, wrow_bytes, srow_bytes, xa, xstride, p2a, ii.rows, p.Kr, p.J,
-                                     wr, wk, p.cr, p.ck, lane, red, p.rpi, p.mstride);
+                compute_dispatch<MT>(use_mma, wst, p.wstride, sst, srow_bytes, xa, p.xh_stride, xrow, e2, ii.rows, p.Kr,
+                                     p.J, wr, wk, p.cr, p.ck, lane, red, p.rpi, p.mstride);
             }
             __syncwarp();
             if (lane == 0) {
@@ -1008,8 +1114,9 @@ __global__ void __launch_bounds__(kThreads, (MT <= 1 ? 2 : 1)) gemv_stream_kerne
         cluster_sync_all();
         if (!*abort_flag) {
             int64_t local_row = 0;
-            for (int it = ib; it < ie; ++it) {
-                const Item ii = item_at(p, it);
+            ItemWalk walk(p, ib);
+            for (int it = ib; it < ie; ++it, walk.next(p)) {
+                const Item ii = walk.get(p);
                 const float gsc = p.g[ii.group];
                 const int total = ii.rows * p.M;
                 for (int idx = threadIdx.x; idx < total; idx += blockDim.x) {
@@ -1171,25 +1278,30 @@ bool g_pdl = true;
 
 uint32_t align_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
 
+// Bytes between weight rows in a ring slot: rows are stored as they sit in HBM, so one bulk
+// copy moves a whole item (S == 1).
+int padded_wstride(int Kr) { return Kr / 2; }
+
 // Shared-memory layout and counts for a K range; false if it does not fit.
 // n_units = CTAs (S == 1) or clusters (S > 1) that share the items.
 bool layout(Params& p, int mt, int rows_total_est, int groups_for_items, int n_units, int smem_limit,
             uint32_t* smem_out) {
-    const int R = rows_per_batch(mt);
-    const int row_bytes = p.Kr / 2 + p.Kr / 16;
+    const int R = kTileRows;
+    p.wstride = padded_wstride(p.Kr);
+    const int srow = p.S == 1 ? p.K / 16 : p.Kr / 16;
+    const int row_bytes = p.wstride + srow;
     const int rpi_cap = kStageData / row_bytes;
     if (rpi_cap < 1) return false;
-    // Rows per item: the value that minimises the row slots the busiest unit decodes (a
-    // partial batch of R rows still costs R slots) plus a per-item overhead, preferring
-    // larger items on ties.
-    p.J = (p.Kr + kStepElems - 1) / kStepElems;
+    // Rows per item: the value that minimises, for the busiest unit, the row slots it
+    // decodes (a partial 16-row MMA tile still costs 16) plus the rows it streams plus a
+    // per-item overhead, preferring larger items on ties.
     int best_rpi = 1;
     long long best_rows_cost = -1;
     for (int rpi = 1; rpi <= rpi_cap; ++rpi) {
         const long long items = static_cast<long long>(groups_for_items) * ((p.N + rpi - 1) / rpi);
         const long long per_unit = (items + n_units - 1) / n_units;
-        const long long slots = (rpi + R - 1) / R * R;
-        const long long cost = per_unit * (slots + 2);  // + about two rows' worth of per-item work
+        const long long slots = rpi <= 8 ? 8 : (rpi + R - 1) / R * R;  // a tile with <= 8 rows decodes half
+        const long long cost = per_unit * (slots + rpi + 2);  // decode slots + streamed rows + per-item work
         if (best_rows_cost < 0 || cost <= best_rows_cost) { best_rows_cost = cost; best_rpi = rpi; }
     }
     const int rpi = best_rpi;
@@ -1197,29 +1309,32 @@ bool layout(Params& p, int mt, int rows_total_est, int groups_for_items, int n_u
     p.chunks = (p.N + rpi - 1) / rpi;
     p.items = groups_for_items * p.chunks;
     p.J = (p.Kr + kStepElems - 1) / kStepElems;
-    // a CTA with at most two items needs no deeper ring; fewer stages leave room for a
-    // second CTA (the next GEMV's prologue under programmatic dependent launch)
+    p.work = static_cast<long long>((p.items + n_units - 1) / n_units) * ((rpi <= 8 ? 8 : (rpi + R - 1) / R * R) + rpi + 2) * p.Kr;
+    if (p.S > 1) p.work += p.work / 2;  // per-row copies, cluster reduction and co-scheduling
     const int items_per_unit = (p.items + n_units - 1) / n_units;
-    // warps along K: fewest passes over (row batches x steps); ties go to fewer K-warps
+    // warps along K: fewest passes over (16-row tiles x 128-element steps); ties go to fewer
+    const int steps = (p.Kr + 127) / 128, tiles = (rpi + R - 1) / R;
     int best_ck = 1, best_cost = 1 << 30;
     for (int ck = 1; ck <= kConsumerWarps; ck *= 2) {
         const int cr = kConsumerWarps / ck;
-        const int batches = (rpi + R - 1) / R;
-        const int cost = ((p.J + ck - 1) / ck) * ((batches + cr - 1) / cr);
+        const int cost = ((steps + ck - 1) / ck) * ((tiles + cr - 1) / cr);
         if (cost < best_cost) { best_cost = cost; best_ck = ck; }
     }
     p.ck = best_ck;
     p.cr = kConsumerWarps / best_ck;
     p.mstride = mt;
+    p.xh_stride = steps * 256 + 64;
     p.stage_stride = align_up(static_cast<uint32_t>(rpi) * row_bytes + 128, 128);
     // a CTA with at most two items needs no deeper ring; otherwise the deepest ring that fits
     for (int stages = items_per_unit <= 2 ? 2 : kMaxStages; stages >= 2; --stages) {
         p.stages = stages;
         uint32_t off = static_cast<uint32_t>(p.stages) * p.stage_stride;
         p.x_off = off;
-        off += align_up(static_cast<uint32_t>(mt) * p.J * kStepElems * 4, 128);  // fp32 size (f16 uses half)
-        p.p2_off = off;
-        off += align_up(static_cast<uint32_t>(p.J) * (kStepElems / 16) * 4, 128);
+        off += align_up(static_cast<uint32_t>(mt) * p.xh_stride, 128);
+        p.xraw_off = off;
+        off += align_up(static_cast<uint32_t>(mt) * p.Kr * 2, 128);
+        p.misc_off = off;
+        off += align_up((8 + 8 * kConsumerWarps) * 4, 128);
         p.red_off = off;
         uint32_t red_bytes = static_cast<uint32_t>(p.stages) * p.ck * rpi * mt * 4;
         const uint32_t moe_scratch = 3 * kMaxMoeSlots * 4;
@@ -1235,7 +1350,7 @@ bool layout(Params& p, int mt, int rows_total_est, int groups_for_items, int n_u
         p.tab_off = off;
         off += align_up(sizeof(MoeTables), 128);
         p.bar_off = off;
-        off += (4 * kMaxStages + 2) * 8 + 16;
+        off += kNumBars * 8 + 16;
         *smem_out = off;
         if (off <= static_cast<uint32_t>(smem_limit)) return true;
     }
@@ -1244,60 +1359,74 @@ bool layout(Params& p, int mt, int rows_total_est, int groups_for_items, int n_u
 
 // Dense / gate-up plan. groups = 1 (dense) or 2 (gate_up).
 bool plan_dense(Plan& pl, int M, int N, int K, int groups, const DeviceInfo& d, const uint8_t* const* w,
-                const uint8_t* const* s) {
+                const uint8_t* const* s, const void* x) {
     if (g_variant == 1) return false;
-    if (K % 32 != 0) return false;
+    if (K % 32 != 0 || (reinterpret_cast<uintptr_t>(x) & 15)) return false;  // x rows are bulk-copied
     for (int i = 0; i < groups; ++i)
         if ((reinterpret_cast<uintptr_t>(w[i]) & 15) || (reinterpret_cast<uintptr_t>(s[i]) & 1)) return false;
     const int mt = M;
-    // M = 1 kernels fit two CTAs per SM (registers); use that when two rings fit too
-    const int per_sm_max = mt == 1 ? 2 : 1;
+    // Try every K split; keep the one whose busiest unit decodes the fewest row-elements
+    // (partial 16-row tiles included), the smaller split on ties. Two CTAs per SM when two
+    // rings fit, so their decoding warps hide each other's latencies.
+    bool found = false;
     for (int S = 1; S <= 8; ++S) {
         if (S > 1 && (K % (256 * S) != 0)) continue;
         Params p{};
         uint32_t smem = 0;
         int n_units = 0;
         bool ok = false;
-        for (int per_sm = (S == 1 ? per_sm_max : 1); per_sm >= 1 && !ok; --per_sm) {
+        for (int per_sm = (S == 1 ? 2 : 1); per_sm >= 1 && !ok; --per_sm) {
             p = Params{};
             p.M = M; p.N = N; p.K = K; p.groups = groups; p.S = S; p.Kr = K / S;
             n_units = S == 1 ? d.sm_count * per_sm : d.sm_count / S;
             const int limit = per_sm == 1 ? d.smem_optin : d.smem_per_sm / per_sm - 1024;
             ok = n_units >= 1 && layout(p, mt, groups * N, groups, n_units, limit, &smem);
+            if (ok && per_sm == 2) p.work /= 2;  // two units share one SM's time
         }
         if (n_units < 1) break;
         if (!ok) continue;
+        if (found && p.work >= pl.p.work) continue;
         const int units = std::min(n_units, p.items);
+        p.items_q = p.items / units;
+        p.items_r = p.items - p.items_q * units;
+        p.s_aligned = K % 256 == 0;
+        for (int i = 0; i < groups; ++i) p.s_aligned &= (reinterpret_cast<uintptr_t>(s[i]) & 15) == 0;
         pl.kind = 0;
         pl.mt = mt;
         pl.p = p;
         pl.grid = units * S;
         pl.smem = smem;
-        return true;
+        found = true;
     }
-    return false;
+    return found;
 }
 
 bool plan_moe(Plan& pl, int E, int T, int top_k, int N, int K, const DeviceInfo& d, const uint8_t* w,
-              const uint8_t* s) {
+              const uint8_t* s, const void* x) {
     if (g_variant == 1) return false;
+    if (reinterpret_cast<uintptr_t>(x) & 15) return false;  // x rows are bulk-copied
     const int slots = T * top_k;
     if (slots > kMaxMoeSlots || K % 32 != 0) return false;
     if ((reinterpret_cast<uintptr_t>(w) & 15) || (reinterpret_cast<uintptr_t>(s) & 1)) return false;
+    // largest member cap that fits two CTAs per SM, else one CTA per SM
     const int caps[4] = {8, 4, 2, 1};
-    for (int ci = 0; ci < 4; ++ci) {
-        const int mt = caps[ci];
-        if (mt > slots && mt > 1) continue;
-        Params p{};
-        p.N = N; p.K = K; p.S = 1; p.Kr = K; p.E = E; p.T = T; p.top_k = top_k; p.slots = slots;
-        uint32_t smem = 0;
-        if (!layout(p, mt, slots * N, slots, d.sm_count, d.smem_optin, &smem)) continue;
-        pl.kind = 1;
-        pl.mt = mt;
-        pl.p = p;
-        pl.grid = d.sm_count;  // the item count depends on the routing, known on the device
-        pl.smem = smem;
-        return true;
+    for (int per_sm = 2; per_sm >= 1; --per_sm) {
+        for (int ci = 0; ci < 4; ++ci) {
+            const int mt = caps[ci];
+            if (mt > slots && mt > 1) continue;
+            Params p{};
+            p.N = N; p.K = K; p.S = 1; p.Kr = K; p.E = E; p.T = T; p.top_k = top_k; p.slots = slots;
+            uint32_t smem = 0;
+            const int limit = per_sm == 1 ? d.smem_optin : d.smem_per_sm / per_sm - 1024;
+            if (!layout(p, mt, slots * N, slots, d.sm_count * per_sm, limit, &smem)) continue;
+            p.s_aligned = K % 256 == 0 && (reinterpret_cast<uintptr_t>(s) & 15) == 0;
+            pl.kind = 1;
+            pl.mt = mt;
+            pl.p = p;
+            pl.grid = d.sm_count * per_sm;  // the item count depends on the routing, known on the device
+            pl.smem = smem;
+            return true;
+        }
     }
     return false;
 }
@@ -1417,7 +1546,7 @@ nvfp4_status run_dense(const uint8_t* const* w, const uint8_t* const* s, const f
     const DeviceInfo* d = device_info(&dev);
     if (!d) return cuda_fail(cudaGetLastError());
     Plan pl{};
-    if (plan_dense(pl, M, N, K, groups, *d, w, s)) {
+    if (plan_dense(pl, M, N, K, groups, *d, w, s, x)) {
         Params& p = pl.p;
         for (int i = 0; i < 2; ++i) {
             p.w[i] = w[i < groups ? i : 0];
@@ -1489,7 +1618,7 @@ nvfp4_status nvfp4_moe_gemv(const uint8_t* w_packed, const uint8_t* w_scales,
     const DeviceInfo* d = device_info(nullptr);
     if (!d) return cuda_fail(cudaGetLastError());
     Plan pl{};
-    if (plan_moe(pl, E, T, top_k, N, K, *d, w_packed, w_scales)) {
+    if (plan_moe(pl, E, T, top_k, N, K, *d, w_packed, w_scales, x)) {
         Params& p = pl.p;
         p.w[0] = p.w[1] = w_packed;
         p.s[0] = p.s[1] = w_scales;
@@ -1578,8 +1707,8 @@ int nvfp4_describe_plan(int kind, int M, int N, int K, int T, int top_k, char* b
     // Pointers are only inspected for alignment here; 256-byte aligned stand-ins.
     const uint8_t* fake = reinterpret_cast<const uint8_t*>(static_cast<uintptr_t>(256));
     const uint8_t* w[2] = {fake, fake};
-    if (kind == 0 || kind == 1) ok = plan_dense(pl, M, N, K, kind == 0 ? 1 : 2, *d, w, w);
-    if (kind == 2) ok = plan_moe(pl, 288, T, top_k, N, K, *d, fake, fake);
+    if (kind == 0 || kind == 1) ok = plan_dense(pl, M, N, K, kind == 0 ? 1 : 2, *d, w, w, fake);
+    if (kind == 2) ok = plan_moe(pl, 288, T, top_k, N, K, *d, fake, fake, fake);
     int n;
     if (!ok) {
         n = snprintf(buf, buflen, "simple grid=%lld block=%d smem=0 split=1 rows_per_item=0 k_warps=0",
