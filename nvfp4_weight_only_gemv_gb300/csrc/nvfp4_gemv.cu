@@ -365,40 +365,47 @@ __device__ __forceinline__ uint32_t bf16_mag_max(uint4 v) {
 // range) sit in shared memory at xraw, Kr * 2 bytes apart (the producer's bulk copies).
 // For each row m one power of two 2^E_m is chosen so that the row's largest |x| lands in
 // [2^12, 2^13); x' = x * 2^-E_m is stored as f16 at mma_x_off, rows xstride bytes apart,
-// zero-padded to whole 128-element chunks, and e2[m] = 2^E_m. Every bf16 value within 2^26
-// of its row's largest magnitude converts exactly. The function returns true if any element
-// was not reproduced exactly (x'[k] * 2^E_m != x[k], Inf or NaN); the caller then uses
-// the fp32 path. The max pass and the convert pass are separated by the consumers' `bar`
-// (bounded wait on `parity`); `wmax` is [kConsumerWarps][8] words of scratch. `ok` turns
-// false if that wait times out.
+// zero-padded to whole 128-element chunks, and e2[m] = 2^E_m. A bf16 value converts
+// exactly when x' is zero or a normal f16, i.e. when |x| >= 2^(E_m - 14), at most 2^26
+// below the row's largest magnitude. Pass 1 finds each row's largest and smallest nonzero
+// magnitude, so the function can return (the same value in every thread) whether any row
+// holds a value that would not convert exactly, or Inf/NaN; the caller then uses the fp32
+// path. The passes are separated by the consumers' `bar` (bounded wait on `parity`);
+// `wmax` is [kConsumerWarps][16] words of scratch. `ok` turns false if that wait times out.
 template <int MAXR>
 __device__ bool stage_x_mma(const uint8_t* xraw, int Kr, int rows, uint8_t* xh, int xstride, float* e2,
                             uint32_t* wmax, uint64_t* bar, uint32_t parity, uint64_t budget, int tid, int nthreads,
                             bool& ok) {
     const int per_row = Kr / 8;                 // 8-element chunks per row
     const int padded = ((Kr + 127) >> 7) * 16;  // chunks per row including the zero tail
-    const int total = rows * per_row;
     const int lane = tid & 31, warp = tid >> 5;
     const uint32_t raw = smem_addr(xraw);
-    // pass 1: per-row maxima of |x| (as bf16 magnitude patterns, ordered like the values)
-    uint32_t mx[MAXR];
-#pragma unroll
-    for (int m = 0; m < MAXR; ++m) mx[m] = 0;
-    for (int c = tid; c < total; c += nthreads) {
-        const int m = c / per_row;
-        const uint32_t a = bf16_mag_max(lds128(raw + c * 16));
-#pragma unroll
-        for (int r = 0; r < MAXR; ++r)
-            if (m == r) mx[r] = max(mx[r], a);
-    }
+    // pass 1: per row, the largest and the smallest nonzero bf16 magnitude (bit patterns of
+    // non-negative values order like the values; two per word, compared as 16-bit lanes)
 #pragma unroll
     for (int m = 0; m < MAXR; ++m) {
+        if (m >= rows) break;
+        uint32_t mx = 0u, mn = 0x7fff7fffu;
+        for (int c = tid; c < per_row; c += nthreads) {
+            const uint4 v = lds128(raw + (m * per_row + c) * 16);
+            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) mx[m] = max(mx[m], __shfl_xor_sync(0xffffffffu, mx[m], o));
-    }
-    if (lane == 0) {
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t mag = w4[i] & 0x7fff7fffu;
+                mx = __vmaxu2(mx, mag);
+                mn = __vminu2(mn, mag | (__vcmpeq2(mag, 0u) & 0x7fff7fffu));
+            }
+        }
+        uint32_t a = max(mx & 0xffffu, mx >> 16), z = min(mn & 0xffffu, mn >> 16);
 #pragma unroll
-        for (int m = 0; m < MAXR; ++m) wmax[warp * 8 + m] = mx[m];
+        for (int o = 16; o > 0; o >>= 1) {
+            a = max(a, __shfl_xor_sync(0xffffffffu, a, o));
+            z = min(z, __shfl_xor_sync(0xffffffffu, z, o));
+        }
+        if (lane == 0) {
+            wmax[warp * 16 + m] = a;
+            wmax[warp * 16 + 8 + m] = z;
+        }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(bar);
@@ -406,58 +413,47 @@ __device__ bool stage_x_mma(const uint8_t* xraw, int Kr, int rows, uint8_t* xh, 
         ok = false;
         return false;
     }
-    // the row's exponent, same in every thread
-    int E[MAXR];
+    bool lossy = false;
 #pragma unroll
     for (int m = 0; m < MAXR; ++m) {
-        uint32_t amax = 0;
-        for (int w = 0; w < nthreads / 32; ++w) amax = max(amax, wmax[w * 8 + m]);
+        if (m >= rows) break;
+        uint32_t amax = 0, amin = 0x7fffu;
+        for (int w = 0; w < nthreads / 32; ++w) {
+            amax = max(amax, wmax[w * 16 + m]);
+            amin = min(amin, wmax[w * 16 + 8 + m]);
+        }
         int e_max;
         if (amax >= 0x7f80u || amax == 0) {
             e_max = 12;                        // Inf/NaN (reported below) or an all-zero row
+            lossy |= amax >= 0x7f80u;
         } else if ((amax >> 7) == 0) {
             e_max = (31 - __clz(amax)) - 133;  // bf16 subnormal: mant * 2^-133
         } else {
             e_max = static_cast<int>(amax >> 7) - 127;
         }
-        E[m] = e_max - 12;
-    }
-    if (tid < rows) {
+        const int E = e_max - 12;
+        // smallest exact magnitude 2^(E - 14) as a bf16 pattern; bf16 subnormals count as inexact
+        const int tb = E - 14 + 127;
+        const uint32_t thresh = tb >= 1 ? static_cast<uint32_t>(tb) << 7 : 0x80u;
+        lossy |= amin != 0x7fffu && amin < thresh;
+        if (tid == 0) e2[m] = pow2f(E);
+        // pass 2: x' = x * 2^-E, two f32 -> f16x2 conversions per word
+        const int a2 = min(-E, 127);
+        const float sa = pow2f(a2), sb = pow2f(-E - a2);  // sb == 1 unless the row is tiny
+        for (int c = tid; c < per_row; c += nthreads) {
+            const uint4 v = lds128(raw + (m * per_row + c) * 16);
+            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+            uint32_t out[4];
 #pragma unroll
-        for (int m = 0; m < MAXR; ++m)
-            if (m == tid) e2[m] = pow2f(E[m]);
-    }
-    // pass 2: scale, convert, check, store
-    bool lossy = false;
-    for (int c = tid; c < total; c += nthreads) {
-        const int m = c / per_row;
-        const int k = (c - m * per_row) * 8;
-        int e = 0;
-#pragma unroll
-        for (int r = 0; r < MAXR; ++r)
-            if (m == r) e = E[r];
-        const float back = pow2f(e);
-        const int a = min(-e, 127);
-        const float sa = pow2f(a), sb = pow2f(-e - a);
-        const uint4 v = lds128(raw + c * 16);
-        const uint32_t u[4] = {v.x, v.y, v.z, v.w};
-        uint32_t out[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float f0 = bf16_lo(u[i]), f1 = bf16_hi(u[i]);
-            const __half h0 = __float2half_rn((f0 * sa) * sb);
-            const __half h1 = __float2half_rn((f1 * sa) * sb);
-            lossy |= !isfinite(f0) || !isfinite(f1) || __half2float(h0) * back != f0 || __half2float(h1) * back != f1;
-            out[i] = static_cast<uint32_t>(__half_as_ushort(h0)) | (static_cast<uint32_t>(__half_as_ushort(h1)) << 16);
+            for (int i = 0; i < 4; ++i) {
+                const __half2 h = __floats2half2_rn(bf16_lo(w4[i]) * sa * sb, bf16_hi(w4[i]) * sa * sb);
+                out[i] = *reinterpret_cast<const uint32_t*>(&h);
+            }
+            *reinterpret_cast<uint4*>(xh + m * xstride + mma_x_off(c * 8)) = make_uint4(out[0], out[1], out[2], out[3]);
         }
-        *reinterpret_cast<uint4*>(xh + m * xstride + mma_x_off(k)) = make_uint4(out[0], out[1], out[2], out[3]);
-    }
-    // zero tail up to the next 128-element chunk
-    const int tail = padded - per_row;
-    for (int c = tid; c < rows * tail; c += nthreads) {
-        const int m = c / tail;
-        const int k = (per_row + (c - m * tail)) * 8;
-        *reinterpret_cast<uint4*>(xh + m * xstride + mma_x_off(k)) = make_uint4(0u, 0u, 0u, 0u);
+        // zero tail up to the next 128-element chunk
+        for (int c = per_row + tid; c < padded; c += nthreads)
+            *reinterpret_cast<uint4*>(xh + m * xstride + mma_x_off(c * 8)) = make_uint4(0u, 0u, 0u, 0u);
     }
     return lossy;
 }
@@ -793,7 +789,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_stream_kernel(const __grid_c
     float* clpart = reinterpret_cast<float*>(smem + p.cl_off);
     MoeTables* tab = reinterpret_cast<MoeTables*>(smem + p.tab_off);
     float* e2 = reinterpret_cast<float*>(smem + p.misc_off);              // [8]
-    uint32_t* wmax = reinterpret_cast<uint32_t*>(smem + p.misc_off) + 8;  // [kConsumerWarps][8]
+    uint32_t* wmax = reinterpret_cast<uint32_t*>(smem + p.misc_off) + 8;  // [kConsumerWarps][16]
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -907,11 +903,10 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_stream_kernel(const __grid_c
             }
             __syncwarp();
             issued = li + 1;
-            // raw x rows: dense x once, after the first slots' weights are on their way; MoE
-            // each time the expert group changes, once the consumers have released the buffer
+            // raw x rows: dense x once, right after the first item's weights are on their way;
+            // MoE each time the expert group changes, once the consumers have released the buffer
             const int key = MODE == kModeMoe ? ii.group : 0;
-            const bool want_x = MODE == kModeMoe ? key != xkey
-                                                 : (xfirst_pending && (li == NS - 1 || it == ie - 1));
+            const bool want_x = MODE == kModeMoe ? key != xkey : xfirst_pending;
             if (want_x) {
                 if (xq > 0 && !mbar_wait(xraw_empty, (xq - 1) & 1, p.wait_ns)) {
                     *abort_flag = 1;
@@ -1334,7 +1329,7 @@ bool layout(Params& p, int mt, int rows_total_est, int groups_for_items, int n_u
         p.xraw_off = off;
         off += align_up(static_cast<uint32_t>(mt) * p.Kr * 2, 128);
         p.misc_off = off;
-        off += align_up((8 + 8 * kConsumerWarps) * 4, 128);
+        off += align_up((8 + 16 * kConsumerWarps) * 4, 128);
         p.red_off = off;
         uint32_t red_bytes = static_cast<uint32_t>(p.stages) * p.ck * rpi * mt * 4;
         const uint32_t moe_scratch = 3 * kMaxMoeSlots * 4;
