@@ -71,6 +71,26 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def kernel_source_sha256():
+    import hashlib
+    with open(os.path.join(ROOT, "nvfp4_weight_only_gemv_gb300", "csrc", "nvfp4_gemv.cu"), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+def kernel_traffic(workload):
+    """DRAM bytes (read + write) per launch from the committed ncu summary, or None when
+    the summary was taken on another version of the kernel source (or is absent)."""
+    prof = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(prof) as f:
+            rec = json.load(f)
+        if rec.get("kernel_source_sha256") != kernel_source_sha256():
+            return None
+        return rec.get("dram_bytes_per_launch", {}).get(workload)
+    except (OSError, ValueError):
+        return None
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -451,14 +471,7 @@ def run_ours(args):
     launches = args.steps * len(calls)
     us_per_launch = region_ms * 1e3 / launches
     achieved = step_alg * args.steps / (region_ms * 1e-3) / 1e9
-    traffic = None
-    prof = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(prof):
-        try:
-            with open(prof) as f:
-                traffic = json.load(f).get(args.workload)
-        except Exception:
-            traffic = None
+    traffic = kernel_traffic(args.workload)
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": traffic,
                 "kernel": "gemv_stream_kernel (every launch of the step)",

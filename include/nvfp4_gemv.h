@@ -139,18 +139,19 @@ void nvfp4_set_wait_budget_ns(uint64_t ns);
 
 /*
  * Kernel selection (process-wide): 0 = automatic (default), 1 = always the byte-load
- * kernel, 2 = streaming kernel with x always staged in fp32 (the exact path that M >= 5
- * and inexact-f16 inputs use). Used by tests to check every path against the oracle.
+ * kernel, 2 = streaming kernel with the exact fp32 x path forced (the path a CTA takes
+ * when x cannot be staged exactly in f16). Used by tests to check every path against
+ * the oracle.
  */
 void nvfp4_set_variant(int variant);
 
 /*
- * For M <= 4 the streaming kernel stages x in f16 with one power-of-two scale per
- * 16-element block. That is exact for every bf16 value within 2^26 of its block's largest
- * magnitude. A CTA that finds any value it cannot hold exactly (a huge dynamic range
- * inside a block, Inf or NaN) stages x in fp32 instead. This returns how many CTAs did so
- * since the last call, after synchronising `stream`, and resets the count. Returns -1 on
- * a CUDA error.
+ * The streaming kernel feeds the tensor cores x in f16, with one power-of-two scale per x
+ * row. That is exact for every bf16 value within 2^26 of its row's largest magnitude. A
+ * CTA that finds a value it cannot hold exactly (a huge dynamic range inside a row, Inf or
+ * NaN) computes with x in fp32 on the CUDA cores instead. This returns how many CTAs did
+ * so since the last call, after synchronising `stream`, and resets the count. Returns -1
+ * on a CUDA error.
  */
 long long nvfp4_fp32_fallbacks(void* stream);
 
