@@ -139,9 +139,9 @@ void nvfp4_set_wait_budget_ns(uint64_t ns);
 
 /*
  * Kernel selection (process-wide): 0 = automatic (default), 1 = always the byte-load
- * kernel, 2 = streaming kernel with the exact fp32 x path forced (the path a CTA takes
- * when x cannot be staged exactly in f16). Used by tests to check every path against
- * the oracle.
+ * kernel, 2 = automatic kernel with the exact fp32 x path forced (the path a CTA takes
+ * when x cannot be staged exactly in f16), 3 = the bulk-copy streaming kernel even where
+ * the warp-tile kernel applies. Used by tests to check every path against the oracle.
  */
 void nvfp4_set_variant(int variant);
 

@@ -29,6 +29,8 @@
 //   * A plain byte-load kernel covers shapes and alignments that the bulk-copy path does
 //     not take (K % 32 != 0, unaligned base pointers, very large M * K, > 256 MoE slots).
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <cuda_fp16.h>
 #include <cuda_bf16.h>
@@ -1131,6 +1133,417 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_stream_kernel(const __grid_c
     }
 }
 
+// ------------------------------------------------------------------ the tile kernel
+
+// Warp-tile GEMV (dense and gate/up, K % 256 == 0, 16-byte aligned operands). Every warp
+// computes: there is no producer or epilogue warp.
+//   * Work unit = one 16-row tile (the MMA's M) times one K slice. A CTA walks a contiguous
+//     block of items; an item is `tpi` tiles, and each tile is shared by `ksplit` warps,
+//     each owning a contiguous range of the row's TMA boxes.
+//   * Each warp streams its own units through a private ring of `stages` slots. Lane 0
+//     issues one 3-D TMA tensor copy for the codes (16 rows x NC 128-byte segments, 128-byte
+//     swizzle) and one for the scales (16 rows x NC 16-byte segments) per slot. The rows land
+//     in shared memory in the order MMA row g <-> physical row perm(g), which makes the
+//     swizzled 128-bit reads of an MMA quad free of bank conflicts.
+//   * Weights are requested before griddepcontrol.wait, so under programmatic dependent
+//     launch they stream while the preceding kernel finishes. x is read only afterwards.
+//   * x is read from global memory by the whole CTA once and staged in f16, one power of
+//     two per row (exactness is checked; otherwise the CTA computes in fp32 on CUDA cores).
+//   * Partial sums of a tile's K slices are added in a fixed order through shared memory;
+//     with ksplit == 1 each warp stores its tile directly.
+
+namespace tk {
+constexpr int kWarps = 8;
+constexpr int kThreads = kWarps * 32;
+constexpr int kMaxStages = 4;
+constexpr int kRedFloats = kWarps * 16 * 8;  // one item's partial sums: [warp][row][m]
+}  // namespace tk
+
+struct TileParams {
+    CUtensorMap wmap[2];      // codes of each group viewed as (128 B, K/256, rows)
+    CUtensorMap smap[2];      // scales viewed as (16 B, K/256, rows)
+    const uint16_t* x;        // bf16 bits [M, K]
+    void* y;
+    float g[2];
+    int64_t ldy;              // y row stride in elements
+    int out_bf16;
+    int M, N, K;
+    int tiles;                // 16-row tiles per group
+    int ksplit;               // warps sharing one tile (K slices)
+    int tpi;                  // tiles per item (= kWarps / ksplit)
+    int ipg;                  // items per group
+    int items;                // items of all groups
+    int nsm;                  // SM slots the items are spread over
+    int per_sm;               // CTAs per SM slot
+    int nbox;                 // TMA boxes per row
+    int stages;               // ring slots per warp
+    int force_f32;
+    uint32_t xstride;         // bytes between staged x rows (64 mod 128)
+    uint32_t ring_w, ring_s, x_off, red_off, misc_off, bar_off;  // offsets from the 1024-aligned base
+    uint64_t wait_ns;
+};
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ uint4 ldg128(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+
+// Shared-memory row of MMA row g (0..7) for a box of NC 128-byte segments per row. The
+// 128-byte swizzle XORs the 16-byte unit index with bits 7..9 of the address, i.e. with
+// (row * NC + segment) & 7. The two MMA rows served by one 8-lane phase of a 128-bit load
+// (g = 2p, 2p + 1) then differ in bit 2 of that value, so they hit disjoint bank halves.
+template <int NC>
+__host__ __device__ __forceinline__ int tile_row_perm(int g) {
+    if constexpr (NC == 1) return ((g & 1) << 2) | (g >> 1);
+    else if constexpr (NC == 2) return (g & 4) | ((g & 1) << 1) | ((g >> 1) & 1);
+    else return g;
+}
+
+// Stages x for the tensor-core path (see stage_x_mma for the exactness rule): the whole CTA
+// reads x [M, K] from global memory, finds each row's largest and smallest nonzero
+// magnitude, and stores x' = x * 2^-E_m in f16 at mma_x_off, rows `xstride` bytes apart,
+// with e2[m] = 2^E_m. Returns (CTA-uniform) whether some row cannot be held exactly.
+__device__ bool stage_x_tile(const uint16_t* __restrict__ x, int M, int K, uint8_t* xh, uint32_t xstride,
+                             float* e2, uint32_t* wmax, int tid) {
+    const int per_row = K >> 3;  // 8-element (16-byte) chunks per row
+    const int lane = tid & 31, warp = tid >> 5;
+    for (int m = 0; m < M; ++m) {
+        uint32_t mx = 0u, mn = 0x7fff7fffu;
+        const uint16_t* row = x + static_cast<int64_t>(m) * K;
+        for (int c = tid; c < per_row; c += tk::kThreads) {
+            const uint4 v = ldg128(row + c * 8);
+            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t mag = w4[i] & 0x7fff7fffu;
+                mx = __vmaxu2(mx, mag);
+                mn = __vminu2(mn, mag | (__vcmpeq2(mag, 0u) & 0x7fff7fffu));
+            }
+        }
+        uint32_t a = max(mx & 0xffffu, mx >> 16), z = min(mn & 0xffffu, mn >> 16);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            a = max(a, __shfl_xor_sync(0xffffffffu, a, o));
+            z = min(z, __shfl_xor_sync(0xffffffffu, z, o));
+        }
+        if (lane == 0) {
+            wmax[warp * 16 + m] = a;
+            wmax[warp * 16 + 8 + m] = z;
+        }
+    }
+    named_bar_sync(1, tk::kThreads);
+    bool lossy = false;
+    for (int m = 0; m < M; ++m) {
+        uint32_t amax = 0, amin = 0x7fffu;
+#pragma unroll
+        for (int w = 0; w < tk::kWarps; ++w) {
+            amax = max(amax, wmax[w * 16 + m]);
+            amin = min(amin, wmax[w * 16 + 8 + m]);
+        }
+        int e_max;
+        if (amax >= 0x7f80u || amax == 0) {
+            e_max = 12;                        // Inf/NaN (reported as lossy) or an all-zero row
+            lossy |= amax >= 0x7f80u;
+        } else if ((amax >> 7) == 0) {
+            e_max = (31 - __clz(amax)) - 133;  // bf16 subnormal: mant * 2^-133
+        } else {
+            e_max = static_cast<int>(amax >> 7) - 127;
+        }
+        const int E = e_max - 12;
+        const int tb = E - 14 + 127;           // smallest exact magnitude 2^(E - 14) as a bf16 pattern
+        const uint32_t thresh = tb >= 1 ? static_cast<uint32_t>(tb) << 7 : 0x80u;
+        lossy |= amin != 0x7fffu && amin < thresh;
+        if (tid == 0) e2[m] = pow2f(E);
+        const int a2 = min(-E, 127);
+        const float sa = pow2f(a2), sb = pow2f(-E - a2);
+        const uint16_t* row = x + static_cast<int64_t>(m) * K;
+        for (int c = tid; c < per_row; c += tk::kThreads) {
+            const uint4 v = ldg128(row + c * 8);
+            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+            uint32_t out[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const __half2 h = __floats2half2_rn(bf16_lo(w4[i]) * sa * sb, bf16_hi(w4[i]) * sa * sb);
+                out[i] = *reinterpret_cast<const uint32_t*>(&h);
+            }
+            *reinterpret_cast<uint4*>(xh + m * xstride + mma_x_off(c * 8)) = make_uint4(out[0], out[1], out[2], out[3]);
+        }
+    }
+    named_bar_sync(1, tk::kThreads);
+    return lossy;
+}
+
+// One ring slot on the tensor cores: NC segments x 2 steps of 128 elements. Lane (g, t)
+// takes the 32 codes 32t .. 32t + 31 of each step for its rows ra = perm(g), rb = ra + 8
+// (see compute_item_mma for the k permutation shared with the staged x). Two accumulator
+// sets shorten the MMA dependency chain.
+template <int NC>
+__device__ __forceinline__ void tile_slot_mma(uint32_t wst, uint32_t sst, uint32_t xa, int kseg0, int ra, int g,
+                                              int t, bool xcol, float (&d0)[4], float (&d1)[4]) {
+    const int rb = ra + 8;
+#pragma unroll
+    for (int c = 0; c < NC; ++c) {
+        const int la = ra * NC + c, lb = rb * NC + c;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int u = h * 4 + t;
+            const uint4 wa = lds128(wst + la * 128 + ((u ^ (la & 7)) << 4));
+            const uint4 wb = lds128(wst + lb * 128 + ((u ^ (lb & 7)) << 4));
+            const uint32_t sa = cvt_e4m3x2(lds16(sst + la * 16 + h * 8 + 2 * t));
+            const uint32_t sb = cvt_e4m3x2(lds16(sst + lb * 16 + h * 8 + 2 * t));
+            const int chunk = (kseg0 + c) * 2 + h;  // 128-element chunk of the staged x
+            uint4 xq[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                xq[q] = xcol ? lds128(xa + chunk * 256 + ((q * 4 + t) << 4)) : make_uint4(0u, 0u, 0u, 0u);
+            const uint32_t sa0 = prmt(sa, 0x1010u), sa1 = prmt(sa, 0x3232u);
+            const uint32_t sb0 = prmt(sb, 0x1010u), sb1 = prmt(sb, 0x3232u);
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                uint32_t ha[4], hb[4];
+                cvt_e2m1x8(w == 0 ? wa.x : (w == 1 ? wa.y : (w == 2 ? wa.z : wa.w)), ha);
+                cvt_e2m1x8(w == 0 ? wb.x : (w == 1 ? wb.y : (w == 2 ? wb.z : wb.w)), hb);
+                const uint32_t s_a = w < 2 ? sa0 : sa1, s_b = w < 2 ? sb0 : sb1;
+                mma_16816(d0, hmul2_u32(ha[0], s_a), hmul2_u32(hb[0], s_b), hmul2_u32(ha[1], s_a),
+                          hmul2_u32(hb[1], s_b), xq[w].x, xq[w].y);
+                mma_16816(d1, hmul2_u32(ha[2], s_a), hmul2_u32(hb[2], s_b), hmul2_u32(ha[3], s_a),
+                          hmul2_u32(hb[3], s_b), xq[w].z, xq[w].w);
+            }
+        }
+    }
+}
+
+// The same slot in exact fp32 on the CUDA cores, x read from global memory (bf16). acc[r][m]
+// collects rows ra (r = 0) and rb (r = 1) for x row m, over this lane's 32-code pieces.
+template <int NC>
+__device__ __noinline__ void tile_slot_f32(uint32_t wst, uint32_t sst, const uint16_t* __restrict__ x, int K,
+                                           int M, int kseg0, int ra, int t, float* acc) {
+    const int rb = ra + 8;
+    for (int c = 0; c < NC; ++c) {
+        const int la = ra * NC + c, lb = rb * NC + c;
+        for (int h = 0; h < 2; ++h) {
+            const int u = h * 4 + t;
+            const uint4 wv[2] = {lds128(wst + la * 128 + ((u ^ (la & 7)) << 4)),
+                                 lds128(wst + lb * 128 + ((u ^ (lb & 7)) << 4))};
+            const uint32_t sh[2] = {cvt_e4m3x2(lds16(sst + la * 16 + h * 8 + 2 * t)),
+                                    cvt_e4m3x2(lds16(sst + lb * 16 + h * 8 + 2 * t))};
+            const int k0 = ((kseg0 + c) * 2 + h) * 128 + 32 * t;
+            for (int w = 0; w < 4; ++w) {
+                for (int m = 0; m < M; ++m) {
+                    const uint4 xv = ldg128(x + static_cast<int64_t>(m) * K + k0 + w * 8);
+                    const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+                    for (int r = 0; r < 2; ++r) {
+                        const uint32_t word = w == 0 ? wv[r].x : (w == 1 ? wv[r].y : (w == 2 ? wv[r].z : wv[r].w));
+                        const uint16_t sc = static_cast<uint16_t>(w < 2 ? (sh[r] & 0xffffu) : (sh[r] >> 16));
+                        uint32_t hq[4];
+                        cvt_e2m1x8(word, hq);
+                        float a = acc[r * 8 + m];
+                        for (int i = 0; i < 4; ++i) {
+                            const float2 q = widen_scaled(hq[i], sc);
+                            a = fmaf(q.x, bf16_lo(xw[i]), a);
+                            a = fmaf(q.y, bf16_hi(xw[i]), a);
+                        }
+                        acc[r * 8 + m] = a;
+                    }
+                }
+            }
+        }
+    }
+}
+
+template <int NC>
+__global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_kernel(const __grid_constant__ TileParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    constexpr uint32_t kWBox = NC * 2048;  // 16 rows x NC x 128 B
+    constexpr uint32_t kSBox = NC * 256;   // 16 rows x NC x 16 B
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g = lane >> 2, t = lane & 3;
+    const uint32_t raw_base = smem_addr(smem_raw);
+    const uint32_t base = (raw_base + 1023u) & ~1023u;
+    uint8_t* const sbase = smem_raw + (base - raw_base);
+    uint64_t* const bars = reinterpret_cast<uint64_t*>(sbase + p.bar_off) + warp * tk::kMaxStages;
+    float* const e2 = reinterpret_cast<float*>(sbase + p.misc_off);
+    uint32_t* const wmax = reinterpret_cast<uint32_t*>(sbase + p.misc_off + 64);
+    float* const red = reinterpret_cast<float*>(sbase + p.red_off);
+    const uint32_t ring_w = base + p.ring_w + static_cast<uint32_t>(warp * p.stages) * kWBox;
+    const uint32_t ring_s = base + p.ring_s + static_cast<uint32_t>(warp * p.stages) * kSBox;
+    const uint64_t budget = p.wait_ns;
+
+    // this CTA's items: the SM slot's balanced share, split between the CTAs of that slot
+    int ib, ie;
+    {
+        const int slot = blockIdx.x % p.nsm, sub = blockIdx.x / p.nsm;
+        const int q = p.items / p.nsm, r = p.items - q * p.nsm;
+        const int s0 = slot * q + min(slot, r), sn = q + (slot < r ? 1 : 0);
+        const int q2 = sn / p.per_sm, r2 = sn - q2 * p.per_sm;
+        ib = s0 + sub * q2 + min(sub, r2);
+        ie = ib + q2 + (sub < r2 ? 1 : 0);
+    }
+    const int kslice = warp % p.ksplit, tin = warp / p.ksplit;
+    const int b_lo = kslice * p.nbox / p.ksplit, b_hi = (kslice + 1) * p.nbox / p.ksplit;
+    const int nb = b_hi - b_lo;
+
+    if (lane == 0) {
+        for (int s = 0; s < p.stages; ++s) mbar_init(&bars[s], 1);
+        fence_barrier_init();
+    }
+    __syncwarp();
+
+    // issue cursor (lane 0 only): the next (item, box) of this warp's units
+    int iss_item = ib, iss_box = 0;
+    uint32_t issued = 0, consumed = 0;
+    bool dead = false;
+    auto unit_tile = [&](int item) { return (item % p.ipg) * p.tpi + tin; };
+    auto issue_next = [&]() {
+        while (iss_item < ie && (iss_box >= nb || unit_tile(iss_item) >= p.tiles)) {
+            ++iss_item;
+            iss_box = 0;
+        }
+        if (iss_item >= ie) return;
+        const int grp = iss_item / p.ipg;
+        const int row0 = unit_tile(iss_item) * 16;
+        const uint32_t st = issued % p.stages;
+        const uint32_t bar = smem_addr(&bars[st]);
+        mbar_arrive_expect_tx(&bars[st], kWBox + kSBox);
+        const int seg = (b_lo + iss_box) * NC;
+        tma_load_3d(ring_w + st * kWBox, &p.wmap[grp], 0, seg, row0, bar);
+        tma_load_3d(ring_s + st * kSBox, &p.smap[grp], 0, seg, row0, bar);
+        ++iss_box;
+        ++issued;
+    };
+    if (lane == 0) {
+        prefetch_tensormap(&p.wmap[0]);
+        prefetch_tensormap(&p.smap[0]);
+        for (int s = 0; s < p.stages; ++s) issue_next();
+    }
+    pdl_launch_dependents();
+    pdl_wait();
+
+    const bool lossy = stage_x_tile(p.x, p.M, p.K, sbase + p.x_off, p.xstride, e2, wmax, tid);
+    const bool use_f32 = lossy || p.force_f32;
+    if (use_f32 && tid == 0) atomicAdd(&g_fp32_fallbacks, 1ull);
+
+    const int ra = tile_row_perm<NC>(g), rb = ra + 8;
+    const bool xcol = g < p.M;
+    const uint32_t xa = base + p.x_off + static_cast<uint32_t>(g) * p.xstride;
+    const int m0 = 2 * t;
+    const float e2a = use_f32 ? 1.f : (m0 < p.M ? e2[m0] : 0.f);
+    const float e2b = use_f32 ? 1.f : (m0 + 1 < p.M ? e2[m0 + 1] : 0.f);
+
+    for (int item = ib; item < ie; ++item) {
+        const int grp = item / p.ipg;
+        const int tile = unit_tile(item);
+        const bool valid = tile < p.tiles && nb > 0;
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+        if (valid && !dead) {
+            float d1[4] = {0.f, 0.f, 0.f, 0.f};
+            float acc[16];
+            if (use_f32) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+            }
+            for (int b = 0; b < nb; ++b) {
+                const uint32_t st = consumed % p.stages;
+                const uint32_t ph = (consumed / p.stages) & 1u;
+                // a zero budget takes the timeout path deterministically (the copies issued
+                // before x staging have usually landed by now, so one poll would succeed)
+                if (!__all_sync(0xffffffffu, budget != 0 && mbar_wait(&bars[st], ph, budget))) {
+                    dead = true;  // warp-uniform: stop computing, keep the CTA's barrier count
+                    break;
+                }
+                const int kseg0 = (b_lo + b) * NC;
+                if (!use_f32) {
+                    tile_slot_mma<NC>(ring_w + st * kWBox, ring_s + st * kSBox, xa, kseg0, ra, g, t, xcol, d, d1);
+                } else {
+                    tile_slot_f32<NC>(ring_w + st * kWBox, ring_s + st * kSBox, p.x, p.K, p.M, kseg0, ra, t, acc);
+                }
+                ++consumed;
+                __syncwarp();
+                if (lane == 0) issue_next();
+            }
+            if (use_f32) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], 1);
+                    acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], 2);
+                }
+                // the MMA's accumulator layout: (ra, 2t), (ra, 2t+1), (rb, 2t), (rb, 2t+1)
+#pragma unroll
+                for (int m = 0; m < 8; ++m) {
+                    if (m == m0) { d[0] = acc[m]; d[2] = acc[8 + m]; }
+                    if (m == m0 + 1) { d[1] = acc[m]; d[3] = acc[8 + m]; }
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) d[i] += d1[i];
+            }
+            if (dead) raise_status(NVFP4_DEV_TIMEOUT, nullptr);
+        }
+        const float gs = p.g[grp];
+        if (p.ksplit == 1) {
+            if (valid) {
+                const int rowa = tile * 16 + ra, rowb = tile * 16 + rb;
+                const int64_t col = static_cast<int64_t>(grp) * p.N;
+                if (m0 < p.M) {
+                    if (rowa < p.N) store_out(p.y, m0 * p.ldy + col + rowa, d[0] * e2a * gs, p.out_bf16);
+                    if (rowb < p.N) store_out(p.y, m0 * p.ldy + col + rowb, d[2] * e2a * gs, p.out_bf16);
+                }
+                if (m0 + 1 < p.M) {
+                    if (rowa < p.N) store_out(p.y, (m0 + 1) * p.ldy + col + rowa, d[1] * e2b * gs, p.out_bf16);
+                    if (rowb < p.N) store_out(p.y, (m0 + 1) * p.ldy + col + rowb, d[3] * e2b * gs, p.out_bf16);
+                }
+            }
+        } else {
+            float* rbuf = red + ((item - ib) & 1) * tk::kRedFloats + warp * 128;
+            rbuf[ra * 8 + m0] = d[0];
+            rbuf[ra * 8 + m0 + 1] = d[1];
+            rbuf[rb * 8 + m0] = d[2];
+            rbuf[rb * 8 + m0 + 1] = d[3];
+            named_bar_sync(1, tk::kThreads);
+            const float* rb0 = red + ((item - ib) & 1) * tk::kRedFloats;
+            const int outs = p.tpi * 16 * p.M;
+            for (int i = tid; i < outs; i += tk::kThreads) {
+                const int ti = i / (16 * p.M), rem = i - ti * 16 * p.M;
+                const int r = rem / p.M, m = rem - r * p.M;
+                const int tl = (item % p.ipg) * p.tpi + ti;
+                const int row = tl * 16 + r;
+                if (tl < p.tiles && row < p.N) {
+                    float s = 0.f;
+                    for (int j = 0; j < p.ksplit; ++j) s += rb0[(ti * p.ksplit + j) * 128 + r * 8 + m];
+                    const float sc = use_f32 ? 1.f : e2[m];
+                    store_out(p.y, m * p.ldy + static_cast<int64_t>(grp) * p.N + row, s * sc * gs, p.out_bf16);
+                }
+            }
+        }
+    }
+    // copies still in flight (only after a timeout) must land before the CTA exits
+    if (lane == 0) {
+        while (consumed < issued) {
+            const uint32_t st = consumed % p.stages;
+            mbar_wait(&bars[st], (consumed / p.stages) & 1u, kDrainWaitNs);
+            ++consumed;
+        }
+    }
+    __syncwarp();
+}
+
 // ------------------------------------------------------------------ byte-load kernel
 
 struct SimpleParams {
@@ -1497,6 +1910,190 @@ cudaError_t dispatch_stream(const Plan& pl, cudaStream_t st) {
     }
 }
 
+// ------------------------------------------------------------------ tile kernel: host side
+
+// Build-time planner overrides for tuning experiments (0 = let the cost model choose).
+#ifndef NVFP4_TILE_KSPLIT
+#define NVFP4_TILE_KSPLIT 0
+#endif
+#ifndef NVFP4_TILE_NC
+#define NVFP4_TILE_NC 0
+#endif
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+struct TilePlan {
+    TileParams p;
+    int nc;
+    int grid;
+    uint32_t smem;
+};
+
+// Tile-kernel plan for a dense (groups = 1) or gate/up (groups = 2) call; false when the
+// call does not meet the kernel's preconditions or its x does not fit next to the rings.
+// The cost of a candidate is the larger of a latency term (rounds of items a CTA runs times
+// the 128-element steps of one warp per item) and a throughput term (items on the busiest
+// SM times the steps each of its warps decodes), both in units of one warp step.
+bool plan_tile(TilePlan& tp, int M, int N, int K, int groups, const DeviceInfo& d, const uint8_t* const* w,
+               const uint8_t* const* s, const void* x) {
+    if (g_variant == 1 || g_variant == 3) return false;
+    if (K <= 0 || K % 256 != 0 || M < 1 || M > 8 || N < 1 || N > (1 << 27)) return false;
+    if (reinterpret_cast<uintptr_t>(x) & 15) return false;
+    for (int i = 0; i < groups; ++i)
+        if ((reinterpret_cast<uintptr_t>(w[i]) & 15) || (reinterpret_cast<uintptr_t>(s[i]) & 15)) return false;
+    if (!tensor_map_encoder()) return false;
+    const int segs = K / 256;
+    const int tiles = (N + 15) / 16;
+    const uint32_t xstride = 2u * static_cast<uint32_t>(K) + 64u;
+    const uint32_t x_bytes = align_up(static_cast<uint32_t>(M) * xstride, 128);
+    bool found = false;
+    double best = 0.0;
+    for (int nc = 2; nc >= 1; --nc) {
+        if (segs % nc) continue;
+        const int nbox = segs / nc;
+        for (int ksplit = 1; ksplit <= tk::kWarps; ksplit *= 2) {
+            if (ksplit > nbox) break;
+            if (NVFP4_TILE_KSPLIT && ksplit != NVFP4_TILE_KSPLIT) continue;
+            if (NVFP4_TILE_NC && nc != NVFP4_TILE_NC) continue;
+            const int tpi = tk::kWarps / ksplit;
+            const int ipg = (tiles + tpi - 1) / tpi;
+            const long long items = static_cast<long long>(groups) * ipg;
+            if (items > (1LL << 30)) continue;
+            // deepest ring that still allows two CTAs per SM, else the deepest that fits one
+            int stages = 0, per_sm = 0;
+            uint32_t smem = 0;
+            TileParams lp{};
+            for (int want = 2; want >= 1 && !stages; --want) {
+                for (int st = tk::kMaxStages; st >= 2; --st) {
+                    TileParams q{};
+                    uint32_t off = 0;
+                    q.ring_w = off;
+                    off += static_cast<uint32_t>(tk::kWarps * st * nc) * 2048u;
+                    q.ring_s = off;
+                    off += static_cast<uint32_t>(tk::kWarps * st * nc) * 256u;
+                    q.x_off = off;
+                    off += x_bytes;
+                    q.red_off = off;
+                    if (ksplit > 1) off += 2u * tk::kRedFloats * 4u;
+                    q.misc_off = off;
+                    off += align_up(64 + tk::kWarps * 16 * 4, 128);
+                    q.bar_off = off;
+                    off += tk::kWarps * tk::kMaxStages * 8;
+                    const uint32_t total = off + 1024;  // slack to align the base to 1024 bytes
+                    const uint32_t limit = want == 2 ? static_cast<uint32_t>(d.smem_per_sm / 2 - 1024)
+                                                     : static_cast<uint32_t>(d.smem_optin);
+                    if (total <= limit) {
+                        stages = st;
+                        per_sm = want;
+                        smem = total;
+                        lp = q;
+                        break;
+                    }
+                }
+            }
+            if (!stages) continue;
+            const int nsm = static_cast<int>(std::min<long long>(d.sm_count, items));
+            const long long per_slot = (items + nsm - 1) / nsm;
+            const int per_sm_eff = static_cast<int>(std::min<long long>(per_sm, per_slot));
+            const int boxes = (nbox + ksplit - 1) / ksplit;
+            const double spw = 2.0 * nc * boxes;  // 128-element steps per warp per item
+            const double item_ovh = ksplit > 1 ? 1.5 : 0.3;  // reduction barrier and epilogue, in warp steps
+            const double lat = static_cast<double>((per_slot + per_sm_eff - 1) / per_sm_eff) * (spw + 2 * item_ovh);
+            const double thr = static_cast<double>(per_slot) * (spw * 1.1 + item_ovh);
+            const double cost = std::max(lat, thr);
+            if (!found || cost < best - 1e-9) {
+                found = true;
+                best = cost;
+                tp.p = lp;
+                tp.p.M = M;
+                tp.p.N = N;
+                tp.p.K = K;
+                tp.p.tiles = tiles;
+                tp.p.ksplit = ksplit;
+                tp.p.tpi = tpi;
+                tp.p.ipg = ipg;
+                tp.p.items = static_cast<int>(items);
+                tp.p.nsm = nsm;
+                tp.p.per_sm = per_sm_eff;
+                tp.p.nbox = nbox;
+                tp.p.stages = stages;
+                tp.p.xstride = xstride;
+                tp.nc = nc;
+                tp.grid = nsm * per_sm_eff;
+                tp.smem = smem;
+            }
+        }
+    }
+    return found;
+}
+
+// Codes [rows, K/2] as (128 B, K/256, rows) with a 128-byte swizzle, scales [rows, K/16] as
+// (16 B, K/256, rows); boxes of NC segments x 16 rows.
+bool encode_tile_maps(CUtensorMap* wmap, CUtensorMap* smap, const uint8_t* w, const uint8_t* s, int64_t rows,
+                      int K, int nc) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint32_t estr[3] = {1, 1, 1};
+    {
+        const cuuint64_t dims[3] = {128, static_cast<cuuint64_t>(K / 256), static_cast<cuuint64_t>(rows)};
+        const cuuint64_t strides[2] = {128, static_cast<cuuint64_t>(K / 2)};
+        const cuuint32_t box[3] = {128, static_cast<cuuint32_t>(nc), 16};
+        if (enc(wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(w), dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return false;
+    }
+    {
+        const cuuint64_t dims[3] = {16, static_cast<cuuint64_t>(K / 256), static_cast<cuuint64_t>(rows)};
+        const cuuint64_t strides[2] = {16, static_cast<cuuint64_t>(K / 16)};
+        const cuuint32_t box[3] = {16, static_cast<cuuint32_t>(nc), 16};
+        if (enc(smap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(s), dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return false;
+    }
+    return true;
+}
+
+template <int NC>
+cudaError_t launch_tile_nc(const TilePlan& tp, cudaStream_t st) {
+    auto kern = gemv_tile_kernel<NC>;
+    static bool done[64] = {};
+    cudaError_t e = allow_max_smem(kern, done);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(tp.grid);
+    cfg.blockDim = dim3(tk::kThreads);
+    cfg.dynamicSmemBytes = tp.smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    int na = 0;
+    if (g_pdl) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
+    return cudaLaunchKernelEx(&cfg, kern, tp.p);
+}
+
+cudaError_t launch_tile(const TilePlan& tp, cudaStream_t st) {
+    return tp.nc == 2 ? launch_tile_nc<2>(tp, st) : launch_tile_nc<1>(tp, st);
+}
+
 cudaError_t launch_simple(const SimpleParams& sp, int64_t cols, cudaStream_t st) {
     const int per_block = kSimpleThreads / 32;
     const int64_t blocks = (cols + per_block - 1) / per_block;
@@ -1540,6 +2137,30 @@ nvfp4_status run_dense(const uint8_t* const* w, const uint8_t* const* s, const f
     int dev = 0;
     const DeviceInfo* d = device_info(&dev);
     if (!d) return cuda_fail(cudaGetLastError());
+    TilePlan tpl{};
+    if (plan_tile(tpl, M, N, K, groups, *d, w, s, x)) {
+        TileParams& p = tpl.p;
+        bool ok = true;
+        for (int i = 0; i < groups && ok; ++i) ok = encode_tile_maps(&p.wmap[i], &p.smap[i], w[i], s[i], N, K, tpl.nc);
+        if (ok) {
+            if (groups == 1) {
+                p.wmap[1] = p.wmap[0];
+                p.smap[1] = p.smap[0];
+            }
+            p.x = x;
+            p.y = y;
+            p.g[0] = g[0];
+            p.g[1] = g[groups > 1 ? 1 : 0];
+            p.ldy = static_cast<int64_t>(groups) * N;
+            p.out_bf16 = y_type == NVFP4_OUT_BF16;
+            p.force_f32 = g_variant == 2;
+            p.wait_ns = g_wait_ns;
+            const cudaError_t e = launch_tile(tpl, st);
+            if (e != cudaSuccess) return cuda_fail(e);
+            const cudaError_t e2 = cudaGetLastError();
+            return e2 == cudaSuccess ? NVFP4_OK : cuda_fail(e2);
+        }
+    }
     Plan pl{};
     if (plan_dense(pl, M, N, K, groups, *d, w, s, x)) {
         Params& p = pl.p;
@@ -1702,7 +2323,16 @@ int nvfp4_describe_plan(int kind, int M, int N, int K, int T, int top_k, char* b
     // Pointers are only inspected for alignment here; 256-byte aligned stand-ins.
     const uint8_t* fake = reinterpret_cast<const uint8_t*>(static_cast<uintptr_t>(256));
     const uint8_t* w[2] = {fake, fake};
-    if (kind == 0 || kind == 1) ok = plan_dense(pl, M, N, K, kind == 0 ? 1 : 2, *d, w, w, fake);
+    if (kind == 0 || kind == 1) {
+        TilePlan tpl{};
+        if (plan_tile(tpl, M, N, K, kind == 0 ? 1 : 2, *d, w, w, fake)) {
+            return snprintf(buf, buflen,
+                            "tile grid=%d block=%d smem=%u split=%d rows_per_item=%d k_warps=%d mt=%d stages=%d nc=%d",
+                            tpl.grid, tk::kThreads, tpl.smem, 1, tpl.p.tpi * 16, tpl.p.ksplit, M, tpl.p.stages,
+                            tpl.nc);
+        }
+        ok = plan_dense(pl, M, N, K, kind == 0 ? 1 : 2, *d, w, w, fake);
+    }
     if (kind == 2) ok = plan_moe(pl, 288, T, top_k, N, K, *d, fake, fake, fake);
     int n;
     if (!ok) {

@@ -134,6 +134,31 @@ def test_small_and_odd_shapes(N, K, M):
         assert_parity(y, yr, ya, f"{N}x{K} M={M} {dt}")
 
 
+@pytest.mark.parametrize("N,K,M", [(1000, 1024, 1), (1000, 1024, 3), (37, 2560, 8), (513, 768, 2),
+                                   (1, 256, 1), (5, 256, 7), (4096, 768, 4), (300, 12288, 1), (2000, 2048, 6)])
+def test_tile_kernel_ragged_rows(N, K, M):
+    # K % 256 == 0 runs the warp-tile kernel; N % 16 != 0 leaves zero-filled rows in the last tile
+    assert nv.describe_plan("dense", M, N, K).startswith("tile ")
+    for dt in (torch.float32, torch.bfloat16):
+        y, yr, ya = run_dense(N, K, M, 400 + N + K + M, dt)
+        assert_parity(y, yr, ya, f"{N}x{K} M={M} {dt}")
+
+
+@pytest.mark.parametrize("N,K,M", [(4096, 4096, 1), (1024, 4096, 5), (4096, 12288, 2), (256, 512, 1)])
+def test_stream_kernel_on_tile_shapes(N, K, M):
+    # the bulk-copy streaming kernel stays correct on shapes the tile kernel normally takes
+    nv.set_variant(3)
+    assert nv.describe_plan("dense", M, N, K).startswith("stream ")
+    y, yr, ya = run_dense(N, K, M, 500 + M, torch.bfloat16, device=DEV)
+    assert_parity(y, yr, ya, f"stream {N}x{K} M={M}")
+    p = synth.gate_up_problem(2000, 2048, 3, 307, device=DEV)
+    y = nv.gemv_gate_up(p["wg"], p["sg"], p["gg"], p["wu"], p["su"], p["gu"], p["x"])
+    torch.cuda.synchronize()
+    yr, ya = oracle.gemv_gate_up(host(p["wg"]), host(p["sg"]), p["gg"], host(p["wu"]), host(p["su"]),
+                                 p["gu"], synth.bf16_bits(p["x"]))
+    assert_parity(y, yr, ya, "stream gate_up")
+
+
 def test_empty_inputs():
     w = torch.empty(0, 8, dtype=torch.uint8, device=DEV)
     s = torch.empty(0, 1, dtype=torch.uint8, device=DEV)
@@ -356,7 +381,11 @@ def test_moe_odd_k_uses_byte_kernel():
 
 # ------------------------------------------------------------------ runtime behaviour
 
-def test_timeout_path_reports_and_recovers():
+@pytest.mark.parametrize("variant", [0, 3])
+def test_timeout_path_reports_and_recovers(variant):
+    # a zero wait budget makes the pipeline waits give up: the kernel must report it, drain its
+    # copies and leave the context usable (variant 3: the bulk-copy streaming kernel)
+    nv.set_variant(variant)
     p = synth.dense_problem(4096, 4096, 1, 320, device=DEV)
     nv.set_wait_budget_ns(0)
     nv.gemv(p["w"], p["s"], p["g"], p["x"])
@@ -401,6 +430,6 @@ def test_plan_uses_all_sms_for_large_problems():
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     desc = nv.describe_plan("dense", 1, 151936, 4096)
     grid = int(desc.split("grid=")[1].split()[0])
-    assert desc.startswith("stream ") and grid % sms == 0 and grid >= sms
+    assert desc.split()[0] in ("tile", "stream") and grid % sms == 0 and grid >= sms
     desc = nv.describe_plan("dense", 8, 4096, 12288)
     assert "split=" in desc and "split=1 " not in desc
