@@ -292,7 +292,7 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t sel) {
 // D += A * B for one m16n8k16 tile: A 16x16 f16 (row), B 16x8 f16 (col), D 16x8 f32.
 __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                           uint32_t b0, uint32_t b1) {
-    asm volatile(
+    asm(
         "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
         "{%0, %1, %2, %3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
@@ -1147,8 +1147,9 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_stream_kernel(const __grid_c
 //     swizzled 128-bit reads of an MMA quad free of bank conflicts.
 //   * Weights are requested before griddepcontrol.wait, so under programmatic dependent
 //     launch they stream while the preceding kernel finishes. x is read only afterwards.
-//   * x is read from global memory by the whole CTA once and staged in f16, one power of
-//     two per row (exactness is checked; otherwise the CTA computes in fp32 on CUDA cores).
+//   * x is read from global memory and staged in f16 by the warps that share a K slice, for
+//     that slice only, with one power of two per row and slice (exactness is checked;
+//     otherwise those warps compute in fp32 on CUDA cores).
 //   * Partial sums of a tile's K slices are added in a fixed order through shared memory;
 //     with ksplit == 1 each warp stores its tile directly.
 
@@ -1169,17 +1170,16 @@ struct TileParams {
     int out_bf16;
     int M, N, K;
     int tiles;                // 16-row tiles per group
-    int ksplit;               // warps sharing one tile (K slices)
+    int ksplit_log2;          // warps sharing one tile (K slices) = 1 << ksplit_log2
     int tpi;                  // tiles per item (= kWarps / ksplit)
     int ipg;                  // items per group
-    int items;                // items of all groups
-    int nsm;                  // SM slots the items are spread over
-    int per_sm;               // CTAs per SM slot
+    int items_q, items_r;     // items per unit (a CTA, or a cluster of S CTAs): q, plus one for the first r
+    int s_log2;               // CTAs per cluster S = 1 << s_log2; rank r takes the r-th of S K ranges
     int nbox;                 // TMA boxes per row
     int stages;               // ring slots per warp
     int force_f32;
-    uint32_t xstride;         // bytes between staged x rows (64 mod 128)
-    uint32_t ring_w, ring_s, x_off, red_off, misc_off, bar_off;  // offsets from the 1024-aligned base
+    uint32_t sstride;         // bytes between staged x rows of one K slice (64 mod 128)
+    uint32_t ring_w, ring_s, x_off, red_off, cpart_off, misc_off, bar_off;  // offsets from the 1024-aligned base
     uint64_t wait_ns;
 };
 
@@ -1188,10 +1188,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
     asm volatile(
         "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
         ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar) : "memory");
-}
-
-__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
 __device__ __forceinline__ void named_bar_sync(int id, int count) {
@@ -1205,6 +1201,20 @@ __device__ __forceinline__ uint4 ldg128(const void* p) {
     return v;
 }
 
+// Brings [p, p + bytes) into L2 (a hint: no data is returned, so it is safe even while
+// another kernel may still write that memory; L2 stays coherent with those writes).
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
+__device__ __forceinline__ void prefetch_l1(const void* p) {
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+}
+
 // Shared-memory row of MMA row g (0..7) for a box of NC 128-byte segments per row. The
 // 128-byte swizzle XORs the 16-byte unit index with bits 7..9 of the address, i.e. with
 // (row * NC + segment) & 7. The two MMA rows served by one 8-lane phase of a 128-bit load
@@ -1216,87 +1226,186 @@ __host__ __device__ __forceinline__ int tile_row_perm(int g) {
     else return g;
 }
 
-// Stages x for the tensor-core path (see stage_x_mma for the exactness rule): the whole CTA
-// reads x [M, K] from global memory, finds each row's largest and smallest nonzero
-// magnitude, and stores x' = x * 2^-E_m in f16 at mma_x_off, rows `xstride` bytes apart,
-// with e2[m] = 2^E_m. Returns (CTA-uniform) whether some row cannot be held exactly.
-__device__ bool stage_x_tile(const uint16_t* __restrict__ x, int M, int K, uint8_t* xh, uint32_t xstride,
-                             float* e2, uint32_t* wmax, int tid) {
-    const int per_row = K >> 3;  // 8-element (16-byte) chunks per row
-    const int lane = tid & 31, warp = tid >> 5;
-    for (int m = 0; m < M; ++m) {
-        uint32_t mx = 0u, mn = 0x7fff7fffu;
-        const uint16_t* row = x + static_cast<int64_t>(m) * K;
-        for (int c = tid; c < per_row; c += tk::kThreads) {
-            const uint4 v = ldg128(row + c * 8);
-            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+// Fast staging of x[:, k0 : k0 + kn] for the warps of one K slice: every bf16 value is
+// converted to f16 unscaled, which is exact when it is zero or 2^-17 <= |x| < 2^16 (a bf16
+// value has 8 significant bits; f16 keeps them down to its subnormal step 2^-24). One pass,
+// no reduction: each lane checks its own values and the slice votes. Returns true when every
+// value converted exactly (uniform over the slice's warps); otherwise the caller re-stages
+// with a power-of-two scale. `vote` is gw words of shared scratch; bar_id < 0: one warp.
+__device__ bool stage_x_direct(const uint16_t* __restrict__ x, int M, int K, int k0, int kn, uint8_t* xs,
+                               uint32_t sstride, uint32_t* vote, int gi, int gw, int bar_id, int lane) {
+    constexpr int kPre = 12;
+    const int cpr = kn >> 3;
+    const int tl = gi * 32 + lane, nt = gw * 32;
+    int m = 0, c = tl;
+    while (c >= cpr) {
+        c -= cpr;
+        ++m;
+    }
+    uint32_t bad = 0u;
+    auto convert = [&](const uint4& q, int mm, int cc) {
+        const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
+        uint32_t out[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const uint32_t mag = w4[i] & 0x7fff7fffu;
-                mx = __vmaxu2(mx, mag);
-                mn = __vminu2(mn, mag | (__vcmpeq2(mag, 0u) & 0x7fff7fffu));
-            }
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t mag = w4[i] & 0x7fff7fffu;
+            // lanes (16-bit halves) that are nonzero and below 2^-17 (0x3700), or >= 2^16 (0x4780)
+            bad |= (__vcmpltu2(mag, 0x37003700u) & ~__vcmpeq2(mag, 0u)) | __vcmpgeu2(mag, 0x47804780u);
+            const __half2 h = __floats2half2_rn(bf16_lo(w4[i]), bf16_hi(w4[i]));
+            out[i] = *reinterpret_cast<const uint32_t*>(&h);
         }
-        uint32_t a = max(mx & 0xffffu, mx >> 16), z = min(mn & 0xffffu, mn >> 16);
+        *reinterpret_cast<uint4*>(xs + mm * sstride + mma_x_off(cc * 8)) = make_uint4(out[0], out[1], out[2], out[3]);
+    };
+    auto advance = [&]() {
+        c += nt;
+        while (c >= cpr) {
+            c -= cpr;
+            ++m;
+        }
+    };
+    {
+        uint4 v[kPre];
+        int mi[kPre], ci[kPre];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            a = max(a, __shfl_xor_sync(0xffffffffu, a, o));
-            z = min(z, __shfl_xor_sync(0xffffffffu, z, o));
+        for (int i = 0; i < kPre; ++i) {
+            mi[i] = m;
+            ci[i] = c;
+            v[i] = m < M ? ldg128(x + static_cast<int64_t>(m) * K + k0 + c * 8) : make_uint4(0u, 0u, 0u, 0u);
+            advance();
         }
+#pragma unroll
+        for (int i = 0; i < kPre; ++i)
+            if (mi[i] < M) convert(v[i], mi[i], ci[i]);
+    }
+    for (; m < M; advance()) convert(ldg128(x + static_cast<int64_t>(m) * K + k0 + c * 8), m, c);
+    bool ok = !__any_sync(0xffffffffu, bad != 0u);
+    if (bar_id >= 0) {
+        if (lane == 0) vote[gi] = ok ? 1u : 0u;
+        named_bar_sync(bar_id, gw * 32);
+        for (int w = 0; w < gw; ++w) ok = ok && vote[w] != 0u;
+    } else {
+        __syncwarp();
+    }
+    return ok;
+}
+
+// Stages x[:, k0 : k0 + kn] for the warps of one K slice (gw warps; this one is number gi
+// of them) in f16 for the tensor cores: rows `sstride` bytes apart at xs, elements at
+// mma_x_off. The slice gets one power of two, x' = x * 2^-E with its largest |x| in
+// [2^12, 2^13), and *e2 = 2^E. Exact for every value at most 2^26 below that largest one
+// (see stage_x_mma); a slice holding a smaller nonzero value, Inf or NaN is reported lossy
+// and its warps compute in fp32 instead. Because each slice's partial sums are multiplied by
+// its own e2 before slices are added, slices need no common scale and no CTA-wide step.
+// The slice's rows are walked as one flat sequence of 16-byte chunks; the first kPre of each
+// lane are loaded at once and kept in registers for the conversion. Returns (uniform over
+// the slice's warps) the lossy flag. bar_id < 0: a single warp (no named barrier).
+__device__ bool stage_x_slice(const uint16_t* __restrict__ x, int M, int K, int k0, int kn, uint8_t* xs,
+                              uint32_t sstride, float* e2, uint32_t* gmax, int gi, int gw, int bar_id,
+                              int lane) {
+    constexpr int kPre = 12;
+    const int cpr = kn >> 3;                      // 16-byte chunks per row of the slice
+    const int total = M * cpr;
+    const int tl = gi * 32 + lane, nt = gw * 32;  // this lane among the slice's lanes
+    int m0 = 0, c0 = tl;                          // flat chunk tl as (row, chunk)
+    while (c0 >= cpr) {
+        c0 -= cpr;
+        ++m0;
+    }
+    auto advance = [&](int& m, int& c) {
+        c += nt;
+        while (c >= cpr) {
+            c -= cpr;
+            ++m;
+        }
+    };
+    uint4 v[kPre];
+    uint32_t mx = 0u, mn = 0x7fff7fffu;
+    auto scan = [&](const uint4& q) {
+        const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t mag = w4[i] & 0x7fff7fffu;
+            mx = __vmaxu2(mx, mag);
+            mn = __vminu2(mn, mag | (__vcmpeq2(mag, 0u) & 0x7fff7fffu));
+        }
+    };
+    {
+        int m = m0, c = c0;
+#pragma unroll
+        for (int i = 0; i < kPre; ++i) {
+            v[i] = m < M ? ldg128(x + static_cast<int64_t>(m) * K + k0 + c * 8) : make_uint4(0u, 0u, 0u, 0u);
+            advance(m, c);
+        }
+#pragma unroll
+        for (int i = 0; i < kPre; ++i) scan(v[i]);  // zero padding does not move max or min-nonzero
+        for (; m < M; advance(m, c)) scan(ldg128(x + static_cast<int64_t>(m) * K + k0 + c * 8));
+    }
+    uint32_t a = max(mx & 0xffffu, mx >> 16), z = min(mn & 0xffffu, mn >> 16);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        a = max(a, __shfl_xor_sync(0xffffffffu, a, o));
+        z = min(z, __shfl_xor_sync(0xffffffffu, z, o));
+    }
+    if (gw > 1) {
         if (lane == 0) {
-            wmax[warp * 16 + m] = a;
-            wmax[warp * 16 + 8 + m] = z;
+            gmax[gi] = a;
+            gmax[8 + gi] = z;
+        }
+        named_bar_sync(bar_id, gw * 32);
+        for (int w = 0; w < gw; ++w) {
+            a = max(a, gmax[w]);
+            z = min(z, gmax[8 + w]);
         }
     }
-    named_bar_sync(1, tk::kThreads);
     bool lossy = false;
-    for (int m = 0; m < M; ++m) {
-        uint32_t amax = 0, amin = 0x7fffu;
-#pragma unroll
-        for (int w = 0; w < tk::kWarps; ++w) {
-            amax = max(amax, wmax[w * 16 + m]);
-            amin = min(amin, wmax[w * 16 + 8 + m]);
-        }
-        int e_max;
-        if (amax >= 0x7f80u || amax == 0) {
-            e_max = 12;                        // Inf/NaN (reported as lossy) or an all-zero row
-            lossy |= amax >= 0x7f80u;
-        } else if ((amax >> 7) == 0) {
-            e_max = (31 - __clz(amax)) - 133;  // bf16 subnormal: mant * 2^-133
-        } else {
-            e_max = static_cast<int>(amax >> 7) - 127;
-        }
-        const int E = e_max - 12;
-        const int tb = E - 14 + 127;           // smallest exact magnitude 2^(E - 14) as a bf16 pattern
-        const uint32_t thresh = tb >= 1 ? static_cast<uint32_t>(tb) << 7 : 0x80u;
-        lossy |= amin != 0x7fffu && amin < thresh;
-        if (tid == 0) e2[m] = pow2f(E);
-        const int a2 = min(-E, 127);
-        const float sa = pow2f(a2), sb = pow2f(-E - a2);
-        const uint16_t* row = x + static_cast<int64_t>(m) * K;
-        for (int c = tid; c < per_row; c += tk::kThreads) {
-            const uint4 v = ldg128(row + c * 8);
-            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-            uint32_t out[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const __half2 h = __floats2half2_rn(bf16_lo(w4[i]) * sa * sb, bf16_hi(w4[i]) * sa * sb);
-                out[i] = *reinterpret_cast<const uint32_t*>(&h);
-            }
-            *reinterpret_cast<uint4*>(xh + m * xstride + mma_x_off(c * 8)) = make_uint4(out[0], out[1], out[2], out[3]);
-        }
+    int e_max;
+    if (a >= 0x7f80u || a == 0) {
+        e_max = 12;                        // Inf/NaN (reported as lossy) or an all-zero slice
+        lossy = a >= 0x7f80u;
+    } else if ((a >> 7) == 0) {
+        e_max = (31 - __clz(a)) - 133;     // bf16 subnormal: mant * 2^-133
+    } else {
+        e_max = static_cast<int>(a >> 7) - 127;
     }
-    named_bar_sync(1, tk::kThreads);
+    const int E = e_max - 12;
+    const int tb = E - 14 + 127;           // smallest exact magnitude 2^(E - 14) as a bf16 pattern
+    const uint32_t thresh = tb >= 1 ? static_cast<uint32_t>(tb) << 7 : 0x80u;
+    lossy |= z != 0x7fffu && z < thresh;
+    if (gi == 0 && lane == 0) *e2 = pow2f(E);
+    const int a2 = min(-E, 127);
+    const float sa = pow2f(a2), sb = pow2f(-E - a2);  // sb == 1 unless the slice is tiny
+    auto store = [&](const uint4& q, int m, int c) {
+        const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
+        uint32_t out[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const __half2 h = __floats2half2_rn(bf16_lo(w4[i]) * sa * sb, bf16_hi(w4[i]) * sa * sb);
+            out[i] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+        *reinterpret_cast<uint4*>(xs + m * sstride + mma_x_off(c * 8)) = make_uint4(out[0], out[1], out[2], out[3]);
+    };
+    {
+        int m = m0, c = c0;
+#pragma unroll
+        for (int i = 0; i < kPre; ++i) {
+            if (m < M) store(v[i], m, c);
+            advance(m, c);
+        }
+        for (; m < M; advance(m, c)) store(ldg128(x + static_cast<int64_t>(m) * K + k0 + c * 8), m, c);
+    }
+    if (bar_id >= 0) named_bar_sync(bar_id, gw * 32);
+    else __syncwarp();
     return lossy;
 }
 
 // One ring slot on the tensor cores: NC segments x 2 steps of 128 elements. Lane (g, t)
 // takes the 32 codes 32t .. 32t + 31 of each step for its rows ra = perm(g), rb = ra + 8
-// (see compute_item_mma for the k permutation shared with the staged x). Two accumulator
-// sets shorten the MMA dependency chain.
+// (see compute_item_mma for the k permutation shared with the staged x; xa points at this
+// lane's x row, `chunk0` is the slot's first 128-element chunk within the staged slice).
+// Two accumulator sets shorten the MMA dependency chain.
 template <int NC>
-__device__ __forceinline__ void tile_slot_mma(uint32_t wst, uint32_t sst, uint32_t xa, int kseg0, int ra, int g,
-                                              int t, bool xcol, float (&d0)[4], float (&d1)[4]) {
+__device__ __forceinline__ void tile_slot_mma(uint32_t wst, uint32_t sst, uint32_t xa, int chunk0, int ra, int t,
+                                              float (&d0)[4], float (&d1)[4]) {
     const int rb = ra + 8;
 #pragma unroll
     for (int c = 0; c < NC; ++c) {
@@ -1308,11 +1417,10 @@ __device__ __forceinline__ void tile_slot_mma(uint32_t wst, uint32_t sst, uint32
             const uint4 wb = lds128(wst + lb * 128 + ((u ^ (lb & 7)) << 4));
             const uint32_t sa = cvt_e4m3x2(lds16(sst + la * 16 + h * 8 + 2 * t));
             const uint32_t sb = cvt_e4m3x2(lds16(sst + lb * 16 + h * 8 + 2 * t));
-            const int chunk = (kseg0 + c) * 2 + h;  // 128-element chunk of the staged x
+            const int chunk = chunk0 + c * 2 + h;
             uint4 xq[4];
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-                xq[q] = xcol ? lds128(xa + chunk * 256 + ((q * 4 + t) << 4)) : make_uint4(0u, 0u, 0u, 0u);
+            for (int q = 0; q < 4; ++q) xq[q] = lds128(xa + chunk * 256 + ((q * 4 + t) << 4));
             const uint32_t sa0 = prmt(sa, 0x1010u), sa1 = prmt(sa, 0x3232u);
             const uint32_t sb0 = prmt(sb, 0x1010u), sb1 = prmt(sb, 0x3232u);
 #pragma unroll
@@ -1368,89 +1476,118 @@ __device__ __noinline__ void tile_slot_f32(uint32_t wst, uint32_t sst, const uin
     }
 }
 
+// Position in a CTA's block of items, walked without divisions.
+struct TileItemWalk {
+    int grp, t;  // group (0 gate / 1 up) and item index within the group
+    __device__ __forceinline__ void next(int ipg) {
+        if (++t == ipg) {
+            t = 0;
+            ++grp;
+        }
+    }
+};
+
 template <int NC>
 __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_kernel(const __grid_constant__ TileParams p) {
     extern __shared__ uint8_t smem_raw[];
     constexpr uint32_t kWBox = NC * 2048;  // 16 rows x NC x 128 B
     constexpr uint32_t kSBox = NC * 256;   // 16 rows x NC x 16 B
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int g = lane >> 2, t = lane & 3;
+    const int t = lane & 3;
     const uint32_t raw_base = smem_addr(smem_raw);
     const uint32_t base = (raw_base + 1023u) & ~1023u;
     uint8_t* const sbase = smem_raw + (base - raw_base);
+    const int stages = p.stages;
     uint64_t* const bars = reinterpret_cast<uint64_t*>(sbase + p.bar_off) + warp * tk::kMaxStages;
-    float* const e2 = reinterpret_cast<float*>(sbase + p.misc_off);
-    uint32_t* const wmax = reinterpret_cast<uint32_t*>(sbase + p.misc_off + 64);
-    float* const red = reinterpret_cast<float*>(sbase + p.red_off);
-    const uint32_t ring_w = base + p.ring_w + static_cast<uint32_t>(warp * p.stages) * kWBox;
-    const uint32_t ring_s = base + p.ring_s + static_cast<uint32_t>(warp * p.stages) * kSBox;
-    const uint64_t budget = p.wait_ns;
+    const uint32_t ring_w = base + p.ring_w + static_cast<uint32_t>(warp * stages) * kWBox;
+    const uint32_t ring_s = base + p.ring_s + static_cast<uint32_t>(warp * stages) * kSBox;
 
-    // this CTA's items: the SM slot's balanced share, split between the CTAs of that slot
-    int ib, ie;
-    {
-        const int slot = blockIdx.x % p.nsm, sub = blockIdx.x / p.nsm;
-        const int q = p.items / p.nsm, r = p.items - q * p.nsm;
-        const int s0 = slot * q + min(slot, r), sn = q + (slot < r ? 1 : 0);
-        const int q2 = sn / p.per_sm, r2 = sn - q2 * p.per_sm;
-        ib = s0 + sub * q2 + min(sub, r2);
-        ie = ib + q2 + (sub < r2 ? 1 : 0);
-    }
-    const int kslice = warp % p.ksplit, tin = warp / p.ksplit;
-    const int b_lo = kslice * p.nbox / p.ksplit, b_hi = (kslice + 1) * p.nbox / p.ksplit;
+    // this unit's items (a balanced contiguous block) and this CTA's K range within them
+    const int S = 1 << p.s_log2;
+    const int rank = S > 1 ? static_cast<int>(cluster_rank()) : 0;
+    const int unit = blockIdx.x >> p.s_log2;
+    const int ib = unit * p.items_q + min(unit, p.items_r);
+    const int ie = ib + p.items_q + (unit < p.items_r ? 1 : 0);
+    const int c_lo = (rank * p.nbox) >> p.s_log2, c_n = (((rank + 1) * p.nbox) >> p.s_log2) - c_lo;
+    const int ksplit = 1 << p.ksplit_log2;
+    const int kslice = warp & (ksplit - 1), tin = warp >> p.ksplit_log2;
+    const int b_lo = c_lo + ((kslice * c_n) >> p.ksplit_log2), b_hi = c_lo + (((kslice + 1) * c_n) >> p.ksplit_log2);
     const int nb = b_hi - b_lo;
+    TileItemWalk first;
+    first.grp = ib >= p.ipg ? 1 : 0;  // at most two groups
+    first.t = ib - first.grp * p.ipg;
 
     if (lane == 0) {
-        for (int s = 0; s < p.stages; ++s) mbar_init(&bars[s], 1);
+        for (int s = 0; s < stages; ++s) mbar_init(&bars[s], 1);
         fence_barrier_init();
     }
     __syncwarp();
 
-    // issue cursor (lane 0 only): the next (item, box) of this warp's units
-    int iss_item = ib, iss_box = 0;
+    // issue cursor (lane 0): the next (item, box) of this warp's units
+    TileItemWalk iw = first;
+    int iss_left = ie - ib, iss_box = 0;
     uint32_t issued = 0, consumed = 0;
-    bool dead = false;
-    auto unit_tile = [&](int item) { return (item % p.ipg) * p.tpi + tin; };
     auto issue_next = [&]() {
-        while (iss_item < ie && (iss_box >= nb || unit_tile(iss_item) >= p.tiles)) {
-            ++iss_item;
+        while (iss_left > 0 && (iss_box >= nb || iw.t * p.tpi + tin >= p.tiles)) {
+            iw.next(p.ipg);
+            --iss_left;
             iss_box = 0;
         }
-        if (iss_item >= ie) return;
-        const int grp = iss_item / p.ipg;
-        const int row0 = unit_tile(iss_item) * 16;
-        const uint32_t st = issued % p.stages;
+        if (iss_left <= 0) return;
+        const uint32_t st = issued % stages;
         const uint32_t bar = smem_addr(&bars[st]);
         mbar_arrive_expect_tx(&bars[st], kWBox + kSBox);
         const int seg = (b_lo + iss_box) * NC;
-        tma_load_3d(ring_w + st * kWBox, &p.wmap[grp], 0, seg, row0, bar);
-        tma_load_3d(ring_s + st * kSBox, &p.smap[grp], 0, seg, row0, bar);
+        const int row0 = (iw.t * p.tpi + tin) * 16;
+        tma_load_3d(ring_w + st * kWBox, &p.wmap[iw.grp], 0, seg, row0, bar);
+        tma_load_3d(ring_s + st * kSBox, &p.smap[iw.grp], 0, seg, row0, bar);
         ++iss_box;
         ++issued;
     };
-    if (lane == 0) {
-        prefetch_tensormap(&p.wmap[0]);
-        prefetch_tensormap(&p.smap[0]);
-        for (int s = 0; s < p.stages; ++s) issue_next();
+    // weights never come from the preceding kernel: request them before the dependency wait;
+    // x may, so only an L2 prefetch of this CTA's K range of it goes out before the wait
+    if (lane == 0)
+        for (int s = 0; s < stages; ++s) issue_next();
+    if (warp == tk::kWarps - 1 && lane < p.M) {
+        const int kb = c_lo * NC * 256, kbytes = c_n * NC * 512;
+        const uint16_t* xr = p.x + static_cast<int64_t>(lane) * p.K + kb;
+        prefetch_l2_bulk(xr, static_cast<uint32_t>(kbytes));
+        prefetch_l2(xr);  // through this SM's own path too, so its address translation is warm
     }
     pdl_launch_dependents();
     pdl_wait();
 
-    const bool lossy = stage_x_tile(p.x, p.M, p.K, sbase + p.x_off, p.xstride, e2, wmax, tid);
+    // x for this warp's K slice, staged by the tpi warps that share the slice
+    const uint32_t slice_bytes = static_cast<uint32_t>(p.M) * p.sstride;
+    uint8_t* const xs = sbase + p.x_off + kslice * slice_bytes;
+    float* const e2 = reinterpret_cast<float*>(sbase + p.misc_off) + kslice * 8;
+    // per slice: 16 words of extremes for the scaled staging, then 8 words of votes
+    uint32_t* const gmax = reinterpret_cast<uint32_t*>(sbase + p.misc_off + tk::kWarps * 32) + kslice * 32;
+    const int k0 = b_lo * NC * 256, kn = nb * NC * 256;
+    const int xbar = p.tpi > 1 ? 2 + kslice : -1;
+    bool lossy = false;
+    float e2v = 1.f;
+    if (!stage_x_direct(p.x, p.M, p.K, k0, kn, xs, p.sstride, gmax + 16, tin, p.tpi, xbar, lane)) {
+        lossy = stage_x_slice(p.x, p.M, p.K, k0, kn, xs, p.sstride, e2, gmax, tin, p.tpi, xbar, lane);
+        e2v = e2[0];
+    }
     const bool use_f32 = lossy || p.force_f32;
-    if (use_f32 && tid == 0) atomicAdd(&g_fp32_fallbacks, 1ull);
+    if (use_f32 && tin == 0 && lane == 0) atomicAdd(&g_fp32_fallbacks, 1ull);
 
+    const int g = lane >> 2;
     const int ra = tile_row_perm<NC>(g), rb = ra + 8;
-    const bool xcol = g < p.M;
-    const uint32_t xa = base + p.x_off + static_cast<uint32_t>(g) * p.xstride;
+    const uint32_t xa = base + p.x_off + kslice * slice_bytes + static_cast<uint32_t>(min(g, p.M - 1)) * p.sstride;
     const int m0 = 2 * t;
-    const float e2a = use_f32 ? 1.f : (m0 < p.M ? e2[m0] : 0.f);
-    const float e2b = use_f32 ? 1.f : (m0 + 1 < p.M ? e2[m0 + 1] : 0.f);
+    const float e2s = use_f32 ? 1.f : e2v;  // the slice's power of two
+    float* const red = reinterpret_cast<float*>(sbase + p.red_off);
+    const uint64_t budget = p.wait_ns;
+    bool dead = false;
 
-    for (int item = ib; item < ie; ++item) {
-        const int grp = item / p.ipg;
-        const int tile = unit_tile(item);
-        const bool valid = tile < p.tiles && nb > 0;
+    TileItemWalk cw = first;
+    for (int item = ib; item < ie; ++item, cw.next(p.ipg)) {
+        const int grp = cw.grp;
+        const int tile = cw.t * p.tpi + tin;
+        const bool valid = tile < p.tiles;
         float d[4] = {0.f, 0.f, 0.f, 0.f};
         if (valid && !dead) {
             float d1[4] = {0.f, 0.f, 0.f, 0.f};
@@ -1460,19 +1597,19 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_kernel(const __grid
                 for (int i = 0; i < 16; ++i) acc[i] = 0.f;
             }
             for (int b = 0; b < nb; ++b) {
-                const uint32_t st = consumed % p.stages;
-                const uint32_t ph = (consumed / p.stages) & 1u;
-                // a zero budget takes the timeout path deterministically (the copies issued
-                // before x staging have usually landed by now, so one poll would succeed)
+                const uint32_t st = consumed % stages;
+                const uint32_t ph = (consumed / stages) & 1u;
+                // a zero budget takes the timeout path deterministically (copies issued before
+                // x staging have usually landed by now, so one poll would succeed)
                 if (!__all_sync(0xffffffffu, budget != 0 && mbar_wait(&bars[st], ph, budget))) {
                     dead = true;  // warp-uniform: stop computing, keep the CTA's barrier count
                     break;
                 }
-                const int kseg0 = (b_lo + b) * NC;
                 if (!use_f32) {
-                    tile_slot_mma<NC>(ring_w + st * kWBox, ring_s + st * kSBox, xa, kseg0, ra, g, t, xcol, d, d1);
+                    tile_slot_mma<NC>(ring_w + st * kWBox, ring_s + st * kSBox, xa, b * NC * 2, ra, t, d, d1);
                 } else {
-                    tile_slot_f32<NC>(ring_w + st * kWBox, ring_s + st * kSBox, p.x, p.K, p.M, kseg0, ra, t, acc);
+                    tile_slot_f32<NC>(ring_w + st * kWBox, ring_s + st * kSBox, p.x, p.K, p.M, (b_lo + b) * NC, ra,
+                                      t, acc);
                 }
                 ++consumed;
                 __syncwarp();
@@ -1496,48 +1633,80 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_kernel(const __grid
             }
             if (dead) raise_status(NVFP4_DEV_TIMEOUT, nullptr);
         }
+        // this slice's partial sums in x units: times its power of two
+#pragma unroll
+        for (int i = 0; i < 4; ++i) d[i] *= e2s;
         const float gs = p.g[grp];
-        if (p.ksplit == 1) {
+        const int par = (item - ib) & 1;
+        float* const cpart = reinterpret_cast<float*>(sbase + p.cpart_off) + par * (tk::kWarps * 16 * 8);
+        if (ksplit == 1 && S == 1) {
             if (valid) {
                 const int rowa = tile * 16 + ra, rowb = tile * 16 + rb;
                 const int64_t col = static_cast<int64_t>(grp) * p.N;
                 if (m0 < p.M) {
-                    if (rowa < p.N) store_out(p.y, m0 * p.ldy + col + rowa, d[0] * e2a * gs, p.out_bf16);
-                    if (rowb < p.N) store_out(p.y, m0 * p.ldy + col + rowb, d[2] * e2a * gs, p.out_bf16);
+                    if (rowa < p.N) store_out(p.y, m0 * p.ldy + col + rowa, d[0] * gs, p.out_bf16);
+                    if (rowb < p.N) store_out(p.y, m0 * p.ldy + col + rowb, d[2] * gs, p.out_bf16);
                 }
                 if (m0 + 1 < p.M) {
-                    if (rowa < p.N) store_out(p.y, (m0 + 1) * p.ldy + col + rowa, d[1] * e2b * gs, p.out_bf16);
-                    if (rowb < p.N) store_out(p.y, (m0 + 1) * p.ldy + col + rowb, d[3] * e2b * gs, p.out_bf16);
+                    if (rowa < p.N) store_out(p.y, (m0 + 1) * p.ldy + col + rowa, d[1] * gs, p.out_bf16);
+                    if (rowb < p.N) store_out(p.y, (m0 + 1) * p.ldy + col + rowb, d[3] * gs, p.out_bf16);
                 }
             }
+            continue;
+        }
+        const int outs = p.tpi * 16 * p.M;  // this item's outputs, as (tile, row, m)
+        if (ksplit == 1) {
+            // one warp per tile: its sums are this CTA's part (cpart is [tile * 16 + row][m])
+            float* cp = cpart + tin * 128;
+            cp[ra * 8 + m0] = d[0];
+            cp[ra * 8 + m0 + 1] = d[1];
+            cp[rb * 8 + m0] = d[2];
+            cp[rb * 8 + m0 + 1] = d[3];
         } else {
-            float* rbuf = red + ((item - ib) & 1) * tk::kRedFloats + warp * 128;
+            float* rbuf = red + par * tk::kRedFloats + warp * 128;
             rbuf[ra * 8 + m0] = d[0];
             rbuf[ra * 8 + m0 + 1] = d[1];
             rbuf[rb * 8 + m0] = d[2];
             rbuf[rb * 8 + m0 + 1] = d[3];
             named_bar_sync(1, tk::kThreads);
-            const float* rb0 = red + ((item - ib) & 1) * tk::kRedFloats;
-            const int outs = p.tpi * 16 * p.M;
+            const float* rb0 = red + par * tk::kRedFloats;
             for (int i = tid; i < outs; i += tk::kThreads) {
                 const int ti = i / (16 * p.M), rem = i - ti * 16 * p.M;
                 const int r = rem / p.M, m = rem - r * p.M;
-                const int tl = (item % p.ipg) * p.tpi + ti;
-                const int row = tl * 16 + r;
-                if (tl < p.tiles && row < p.N) {
-                    float s = 0.f;
-                    for (int j = 0; j < p.ksplit; ++j) s += rb0[(ti * p.ksplit + j) * 128 + r * 8 + m];
-                    const float sc = use_f32 ? 1.f : e2[m];
-                    store_out(p.y, m * p.ldy + static_cast<int64_t>(grp) * p.N + row, s * sc * gs, p.out_bf16);
+                float sum = 0.f;
+                for (int j = 0; j < ksplit; ++j) sum += rb0[((ti << p.ksplit_log2) + j) * 128 + r * 8 + m];
+                if (S == 1) {
+                    const int tl = cw.t * p.tpi + ti, row = tl * 16 + r;
+                    if (tl < p.tiles && row < p.N)
+                        store_out(p.y, m * p.ldy + static_cast<int64_t>(grp) * p.N + row, sum * gs, p.out_bf16);
+                } else {
+                    cpart[ti * 128 + r * 8 + m] = sum;
                 }
+            }
+            if (S == 1) continue;
+        }
+        // the cluster's K ranges: after the barrier, rank r adds the r-th share of the outputs
+        // over all ranks in rank order (DSMEM), so the sum does not depend on timing
+        cluster_sync_all();
+        const int o_lo = (rank * outs) >> p.s_log2, o_hi = ((rank + 1) * outs) >> p.s_log2;
+        for (int i = o_lo + tid; i < o_hi; i += tk::kThreads) {
+            const int ti = i / (16 * p.M), rem = i - ti * 16 * p.M;
+            const int r = rem / p.M, m = rem - r * p.M;
+            const int tl = cw.t * p.tpi + ti, row = tl * 16 + r;
+            if (tl < p.tiles && row < p.N) {
+                float sum = 0.f;
+                for (int j = 0; j < S; ++j) sum += ld_cluster_f32(cpart + ti * 128 + r * 8 + m, j);
+                store_out(p.y, m * p.ldy + static_cast<int64_t>(grp) * p.N + row, sum * gs, p.out_bf16);
             }
         }
     }
+    // no CTA may leave while another rank of its cluster can still read its partial sums
+    if (S > 1) cluster_sync_all();
     // copies still in flight (only after a timeout) must land before the CTA exits
     if (lane == 0) {
         while (consumed < issued) {
-            const uint32_t st = consumed % p.stages;
-            mbar_wait(&bars[st], (consumed / p.stages) & 1u, kDrainWaitNs);
+            const uint32_t st = consumed % stages;
+            mbar_wait(&bars[st], (consumed / stages) & 1u, kDrainWaitNs);
             ++consumed;
         }
     }
@@ -1919,6 +2088,9 @@ cudaError_t dispatch_stream(const Plan& pl, cudaStream_t st) {
 #ifndef NVFP4_TILE_NC
 #define NVFP4_TILE_NC 0
 #endif
+#ifndef NVFP4_TILE_S
+#define NVFP4_TILE_S 0
+#endif
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -1937,7 +2109,7 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 struct TilePlan {
     TileParams p;
     int nc;
-    int grid;
+    int grid_x, grid_y;  // SM slots x CTAs per slot
     uint32_t smem;
 };
 
@@ -1956,83 +2128,99 @@ bool plan_tile(TilePlan& tp, int M, int N, int K, int groups, const DeviceInfo& 
     if (!tensor_map_encoder()) return false;
     const int segs = K / 256;
     const int tiles = (N + 15) / 16;
-    const uint32_t xstride = 2u * static_cast<uint32_t>(K) + 64u;
-    const uint32_t x_bytes = align_up(static_cast<uint32_t>(M) * xstride, 128);
     bool found = false;
     double best = 0.0;
     for (int nc = 2; nc >= 1; --nc) {
         if (segs % nc) continue;
         const int nbox = segs / nc;
-        for (int ksplit = 1; ksplit <= tk::kWarps; ksplit *= 2) {
-            if (ksplit > nbox) break;
-            if (NVFP4_TILE_KSPLIT && ksplit != NVFP4_TILE_KSPLIT) continue;
-            if (NVFP4_TILE_NC && nc != NVFP4_TILE_NC) continue;
-            const int tpi = tk::kWarps / ksplit;
-            const int ipg = (tiles + tpi - 1) / tpi;
-            const long long items = static_cast<long long>(groups) * ipg;
-            if (items > (1LL << 30)) continue;
-            // deepest ring that still allows two CTAs per SM, else the deepest that fits one
-            int stages = 0, per_sm = 0;
-            uint32_t smem = 0;
-            TileParams lp{};
-            for (int want = 2; want >= 1 && !stages; --want) {
-                for (int st = tk::kMaxStages; st >= 2; --st) {
-                    TileParams q{};
-                    uint32_t off = 0;
-                    q.ring_w = off;
-                    off += static_cast<uint32_t>(tk::kWarps * st * nc) * 2048u;
-                    q.ring_s = off;
-                    off += static_cast<uint32_t>(tk::kWarps * st * nc) * 256u;
-                    q.x_off = off;
-                    off += x_bytes;
-                    q.red_off = off;
-                    if (ksplit > 1) off += 2u * tk::kRedFloats * 4u;
-                    q.misc_off = off;
-                    off += align_up(64 + tk::kWarps * 16 * 4, 128);
-                    q.bar_off = off;
-                    off += tk::kWarps * tk::kMaxStages * 8;
-                    const uint32_t total = off + 1024;  // slack to align the base to 1024 bytes
-                    const uint32_t limit = want == 2 ? static_cast<uint32_t>(d.smem_per_sm / 2 - 1024)
-                                                     : static_cast<uint32_t>(d.smem_optin);
-                    if (total <= limit) {
-                        stages = st;
-                        per_sm = want;
-                        smem = total;
-                        lp = q;
-                        break;
+        for (int sl = 0; (1 << sl) <= 8; ++sl) {
+            const int S = 1 << sl;
+            if (S > nbox) break;
+            if (NVFP4_TILE_S && S != NVFP4_TILE_S) continue;
+            const int nbs = (nbox + S - 1) / S;  // most boxes of one rank
+            for (int lg = 0; (1 << lg) <= tk::kWarps; ++lg) {
+                const int ksplit = 1 << lg;
+                if (S * ksplit > nbox) break;
+                if (NVFP4_TILE_KSPLIT && ksplit != NVFP4_TILE_KSPLIT) continue;
+                if (NVFP4_TILE_NC && nc != NVFP4_TILE_NC) continue;
+                const int tpi = tk::kWarps / ksplit;
+                const int ipg = (tiles + tpi - 1) / tpi;
+                const long long items = static_cast<long long>(groups) * ipg;
+                if (items > (1LL << 30)) continue;
+                const int nbmax = (nbs + ksplit - 1) / ksplit;  // most boxes of one warp per item
+                const uint32_t sstride = static_cast<uint32_t>(nbmax) * nc * 512u + 64u;
+                const uint32_t x_bytes = align_up(static_cast<uint32_t>(ksplit * M) * sstride, 128);
+                // deepest ring that still allows two CTAs per SM, else the deepest that fits one
+                int stages = 0, per_sm = 0;
+                uint32_t smem = 0;
+                TileParams lp{};
+                for (int want = 2; want >= 1 && !stages; --want) {
+                    for (int st = tk::kMaxStages; st >= 2; --st) {
+                        TileParams q{};
+                        uint32_t off = 0;
+                        q.ring_w = off;
+                        off += static_cast<uint32_t>(tk::kWarps * st * nc) * 2048u;
+                        q.ring_s = off;
+                        off += static_cast<uint32_t>(tk::kWarps * st * nc) * 256u;
+                        q.x_off = off;
+                        off += x_bytes;
+                        q.red_off = off;
+                        if (ksplit > 1) off += 2u * tk::kRedFloats * 4u;
+                        q.cpart_off = off;
+                        if (S > 1) off += 2u * tk::kWarps * 16 * 8 * 4u;
+                        q.misc_off = off;
+                        off += align_up(tk::kWarps * 32 + tk::kWarps * 32 * 4, 128);  // e2, extremes, votes
+                        q.bar_off = off;
+                        off += tk::kWarps * tk::kMaxStages * 8;
+                        const uint32_t total = off + 1024;  // slack to align the base to 1024 bytes
+                        const uint32_t limit = want == 2 ? static_cast<uint32_t>(d.smem_per_sm / 2 - 1024)
+                                                         : static_cast<uint32_t>(d.smem_optin);
+                        if (total <= limit) {
+                            stages = st;
+                            per_sm = want;
+                            smem = total;
+                            lp = q;
+                            break;
+                        }
                     }
                 }
-            }
-            if (!stages) continue;
-            const int nsm = static_cast<int>(std::min<long long>(d.sm_count, items));
-            const long long per_slot = (items + nsm - 1) / nsm;
-            const int per_sm_eff = static_cast<int>(std::min<long long>(per_sm, per_slot));
-            const int boxes = (nbox + ksplit - 1) / ksplit;
-            const double spw = 2.0 * nc * boxes;  // 128-element steps per warp per item
-            const double item_ovh = ksplit > 1 ? 1.5 : 0.3;  // reduction barrier and epilogue, in warp steps
-            const double lat = static_cast<double>((per_slot + per_sm_eff - 1) / per_sm_eff) * (spw + 2 * item_ovh);
-            const double thr = static_cast<double>(per_slot) * (spw * 1.1 + item_ovh);
-            const double cost = std::max(lat, thr);
-            if (!found || cost < best - 1e-9) {
-                found = true;
-                best = cost;
-                tp.p = lp;
-                tp.p.M = M;
-                tp.p.N = N;
-                tp.p.K = K;
-                tp.p.tiles = tiles;
-                tp.p.ksplit = ksplit;
-                tp.p.tpi = tpi;
-                tp.p.ipg = ipg;
-                tp.p.items = static_cast<int>(items);
-                tp.p.nsm = nsm;
-                tp.p.per_sm = per_sm_eff;
-                tp.p.nbox = nbox;
-                tp.p.stages = stages;
-                tp.p.xstride = xstride;
-                tp.nc = nc;
-                tp.grid = nsm * per_sm_eff;
-                tp.smem = smem;
+                if (!stages) continue;
+                // Cost in units of one warp's 128-element step: the larger of a latency term (the
+                // items one unit runs in sequence, each with its steps, reductions and barriers)
+                // and a throughput term (all warp steps spread over the SMs at 16 warps each),
+                // plus the staging of x, which shrinks with the K range of one CTA.
+                const long long max_units = std::max<long long>(1, static_cast<long long>(d.sm_count) * per_sm / S);
+                const long long units = std::min(items, max_units);
+                const long long ipu = (items + units - 1) / units;
+                const double spw = 2.0 * nc * nbmax;
+                // measured: a reduction over warps costs ~2 steps, one over a cluster ~10
+                const double ovh = (ksplit > 1 ? 2.0 : 0.3) + (S > 1 ? 10.0 : 0.0);
+                const double lat = static_cast<double>(ipu) * (spw + ovh);
+                const double thr = static_cast<double>(items) * tk::kWarps * S * spw / (d.sm_count * 16.0) * 1.1;
+                const double stage = static_cast<double>(M) * K / (2048.0 * S);
+                const double cost = std::max(lat, thr) + stage;
+                if (!found || cost < best - 1e-9) {
+                    found = true;
+                    best = cost;
+                    tp.p = lp;
+                    tp.p.M = M;
+                    tp.p.N = N;
+                    tp.p.K = K;
+                    tp.p.tiles = tiles;
+                    tp.p.ksplit_log2 = lg;
+                    tp.p.s_log2 = sl;
+                    tp.p.tpi = tpi;
+                    tp.p.ipg = ipg;
+                    tp.p.items_q = static_cast<int>(items / units);
+                    tp.p.items_r = static_cast<int>(items % units);
+                    tp.p.nbox = nbox;
+                    tp.p.stages = stages;
+                    tp.p.sstride = sstride;
+                    tp.nc = nc;
+                    tp.grid_x = static_cast<int>(units) * S;
+                    tp.grid_y = 1;
+                    tp.smem = smem;
+                }
             }
         }
     }
@@ -2074,12 +2262,19 @@ cudaError_t launch_tile_nc(const TilePlan& tp, cudaStream_t st) {
     cudaError_t e = allow_max_smem(kern, done);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3(tp.grid);
+    cfg.gridDim = dim3(tp.grid_x, tp.grid_y);
     cfg.blockDim = dim3(tk::kThreads);
     cfg.dynamicSmemBytes = tp.smem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     int na = 0;
+    if (tp.p.s_log2 > 0) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = 1u << tp.p.s_log2;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
     if (g_pdl) {
         attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[na].val.programmaticStreamSerializationAllowed = 1;
@@ -2328,7 +2523,8 @@ int nvfp4_describe_plan(int kind, int M, int N, int K, int T, int top_k, char* b
         if (plan_tile(tpl, M, N, K, kind == 0 ? 1 : 2, *d, w, w, fake)) {
             return snprintf(buf, buflen,
                             "tile grid=%d block=%d smem=%u split=%d rows_per_item=%d k_warps=%d mt=%d stages=%d nc=%d",
-                            tpl.grid, tk::kThreads, tpl.smem, 1, tpl.p.tpi * 16, tpl.p.ksplit, M, tpl.p.stages,
+                            tpl.grid_x * tpl.grid_y, tk::kThreads, tpl.smem, 1 << tpl.p.s_log2, tpl.p.tpi * 16,
+                            1 << tpl.p.ksplit_log2, M, tpl.p.stages,
                             tpl.nc);
         }
         ok = plan_dense(pl, M, N, K, kind == 0 ? 1 : 2, *d, w, w, fake);
