@@ -1181,6 +1181,26 @@ struct TileParams {
     uint32_t sstride;         // bytes between staged x rows of one K slice (64 mod 128)
     uint32_t ring_w, ring_s, x_off, red_off, cpart_off, misc_off, bar_off;  // offsets from the 1024-aligned base
     uint64_t wait_ns;
+    // routed experts (MoE launches only)
+    const int32_t* ids;       // expert per slot [slots]
+    const float* g_dev;       // global scale per expert [E]
+    int32_t* status_user;     // optional device status word
+    int E, top_k, slots, x_per_slot;
+    uint32_t moe_off;         // TileMoe tables
+};
+
+// Routed-expert groups of one launch, built by every CTA from the ids: a group is one expert
+// and up to 8 of its slots (the MMA's 8 columns), groups ordered by their first slot.
+constexpr int kTileMoeSlots = 32;
+struct TileMoe {
+    int n_groups;
+    int nrows;                                // x rows this CTA stages
+    int expert[kTileMoeSlots];
+    int count[kTileMoeSlots];
+    int slot[kTileMoeSlots][8];               // member slots, slot order
+    int col[kTileMoeSlots][8];                // staged x row of each member
+    int xrow[kTileMoeSlots][8];               // x row (global) of each member
+    int rows[kTileMoeSlots];                  // global x row of each staged row
 };
 
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2,
@@ -1232,8 +1252,8 @@ __host__ __device__ __forceinline__ int tile_row_perm(int g) {
 // no reduction: each lane checks its own values and the slice votes. Returns true when every
 // value converted exactly (uniform over the slice's warps); otherwise the caller re-stages
 // with a power-of-two scale. `vote` is gw words of shared scratch; bar_id < 0: one warp.
-__device__ bool stage_x_direct(const uint16_t* __restrict__ x, int M, int K, int k0, int kn, uint8_t* xs,
-                               uint32_t sstride, uint32_t* vote, int gi, int gw, int bar_id, int lane) {
+__device__ bool stage_x_direct(const uint16_t* __restrict__ x, const int* rowsel, int M, int K, int k0, int kn,
+                               uint8_t* xs, uint32_t sstride, uint32_t* vote, int gi, int gw, int bar_id, int lane) {
     constexpr int kPre = 12;
     const int cpr = kn >> 3;
     const int tl = gi * 32 + lane, nt = gw * 32;
@@ -1270,14 +1290,15 @@ __device__ bool stage_x_direct(const uint16_t* __restrict__ x, int M, int K, int
         for (int i = 0; i < kPre; ++i) {
             mi[i] = m;
             ci[i] = c;
-            v[i] = m < M ? ldg128(x + static_cast<int64_t>(m) * K + k0 + c * 8) : make_uint4(0u, 0u, 0u, 0u);
+            v[i] = m < M ? ldg128(x + static_cast<int64_t>(rowsel ? rowsel[m] : m) * K + k0 + c * 8)
+                         : make_uint4(0u, 0u, 0u, 0u);
             advance();
         }
 #pragma unroll
         for (int i = 0; i < kPre; ++i)
             if (mi[i] < M) convert(v[i], mi[i], ci[i]);
     }
-    for (; m < M; advance()) convert(ldg128(x + static_cast<int64_t>(m) * K + k0 + c * 8), m, c);
+    for (; m < M; advance()) convert(ldg128(x + static_cast<int64_t>(rowsel ? rowsel[m] : m) * K + k0 + c * 8), m, c);
     bool ok = !__any_sync(0xffffffffu, bad != 0u);
     if (bar_id >= 0) {
         if (lane == 0) vote[gi] = ok ? 1u : 0u;
@@ -1299,8 +1320,8 @@ __device__ bool stage_x_direct(const uint16_t* __restrict__ x, int M, int K, int
 // The slice's rows are walked as one flat sequence of 16-byte chunks; the first kPre of each
 // lane are loaded at once and kept in registers for the conversion. Returns (uniform over
 // the slice's warps) the lossy flag. bar_id < 0: a single warp (no named barrier).
-__device__ bool stage_x_slice(const uint16_t* __restrict__ x, int M, int K, int k0, int kn, uint8_t* xs,
-                              uint32_t sstride, float* e2, uint32_t* gmax, int gi, int gw, int bar_id,
+__device__ bool stage_x_slice(const uint16_t* __restrict__ x, const int* rowsel, int M, int K, int k0, int kn,
+                              uint8_t* xs, uint32_t sstride, float* e2, uint32_t* gmax, int gi, int gw, int bar_id,
                               int lane) {
     constexpr int kPre = 12;
     const int cpr = kn >> 3;                      // 16-byte chunks per row of the slice
@@ -1333,12 +1354,13 @@ __device__ bool stage_x_slice(const uint16_t* __restrict__ x, int M, int K, int 
         int m = m0, c = c0;
 #pragma unroll
         for (int i = 0; i < kPre; ++i) {
-            v[i] = m < M ? ldg128(x + static_cast<int64_t>(m) * K + k0 + c * 8) : make_uint4(0u, 0u, 0u, 0u);
+            v[i] = m < M ? ldg128(x + static_cast<int64_t>(rowsel ? rowsel[m] : m) * K + k0 + c * 8)
+                         : make_uint4(0u, 0u, 0u, 0u);
             advance(m, c);
         }
 #pragma unroll
         for (int i = 0; i < kPre; ++i) scan(v[i]);  // zero padding does not move max or min-nonzero
-        for (; m < M; advance(m, c)) scan(ldg128(x + static_cast<int64_t>(m) * K + k0 + c * 8));
+        for (; m < M; advance(m, c)) scan(ldg128(x + static_cast<int64_t>(rowsel ? rowsel[m] : m) * K + k0 + c * 8));
     }
     uint32_t a = max(mx & 0xffffu, mx >> 16), z = min(mn & 0xffffu, mn >> 16);
 #pragma unroll
@@ -1391,7 +1413,8 @@ __device__ bool stage_x_slice(const uint16_t* __restrict__ x, int M, int K, int 
             if (m < M) store(v[i], m, c);
             advance(m, c);
         }
-        for (; m < M; advance(m, c)) store(ldg128(x + static_cast<int64_t>(m) * K + k0 + c * 8), m, c);
+        for (; m < M; advance(m, c))
+            store(ldg128(x + static_cast<int64_t>(rowsel ? rowsel[m] : m) * K + k0 + c * 8), m, c);
     }
     if (bar_id >= 0) named_bar_sync(bar_id, gw * 32);
     else __syncwarp();
@@ -1438,11 +1461,12 @@ __device__ __forceinline__ void tile_slot_mma(uint32_t wst, uint32_t sst, uint32
     }
 }
 
-// The same slot in exact fp32 on the CUDA cores, x read from global memory (bf16). acc[r][m]
-// collects rows ra (r = 0) and rb (r = 1) for x row m, over this lane's 32-code pieces.
+// The same slot in exact fp32 on the CUDA cores, x read from global memory (bf16): column m
+// uses x row xrow[m] (row m when xrow is null). acc[r][m] collects rows ra (r = 0) and
+// rb (r = 1) for column m, over this lane's 32-code pieces.
 template <int NC>
-__device__ __noinline__ void tile_slot_f32(uint32_t wst, uint32_t sst, const uint16_t* __restrict__ x, int K,
-                                           int M, int kseg0, int ra, int t, float* acc) {
+__device__ __noinline__ void tile_slot_f32(uint32_t wst, uint32_t sst, const uint16_t* __restrict__ x,
+                                           const int* xrow, int K, int M, int kseg0, int ra, int t, float* acc) {
     const int rb = ra + 8;
     for (int c = 0; c < NC; ++c) {
         const int la = ra * NC + c, lb = rb * NC + c;
@@ -1455,7 +1479,7 @@ __device__ __noinline__ void tile_slot_f32(uint32_t wst, uint32_t sst, const uin
             const int k0 = ((kseg0 + c) * 2 + h) * 128 + 32 * t;
             for (int w = 0; w < 4; ++w) {
                 for (int m = 0; m < M; ++m) {
-                    const uint4 xv = ldg128(x + static_cast<int64_t>(m) * K + k0 + w * 8);
+                    const uint4 xv = ldg128(x + static_cast<int64_t>(xrow ? xrow[m] : m) * K + k0 + w * 8);
                     const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
                     for (int r = 0; r < 2; ++r) {
                         const uint32_t word = w == 0 ? wv[r].x : (w == 1 ? wv[r].y : (w == 2 ? wv[r].z : wv[r].w));
@@ -1478,7 +1502,7 @@ __device__ __noinline__ void tile_slot_f32(uint32_t wst, uint32_t sst, const uin
 
 // Position in a CTA's block of items, walked without divisions.
 struct TileItemWalk {
-    int grp, t;  // group (0 gate / 1 up) and item index within the group
+    int grp, t;  // group (dense: 0 gate / 1 up; MoE: expert group) and item index within it
     __device__ __forceinline__ void next(int ipg) {
         if (++t == ipg) {
             t = 0;
@@ -1487,7 +1511,54 @@ struct TileItemWalk {
     }
 };
 
-template <int NC>
+// Builds the routed-expert groups (warp 0; slots <= 32). Slot s with expert e joins the
+// group that holds e's slots of ranks 8q .. 8q + 7, where its rank counts the earlier slots
+// routed to e; groups are numbered in the order of their first slots. Invalid ids form no
+// group: CTA 0 zeroes their outputs and flags them.
+__device__ void tile_moe_groups(const TileParams& p, TileMoe* tab, int lane) {
+    const int s = lane;
+    const int id = s < p.slots ? __ldg(p.ids + s) : -1;
+    const bool valid = s < p.slots && id >= 0 && id < p.E;
+    const uint32_t same = __match_any_sync(0xffffffffu, valid ? id : -1 - lane);  // invalid lanes stay alone
+    const uint32_t lower = (1u << lane) - 1u;
+    const int rank = __popc(same & lower);
+    const bool leader = valid && (rank & 7) == 0;
+    const uint32_t leaders = __ballot_sync(0xffffffffu, leader);
+    if (valid) {
+        uint32_t rest = same;  // drop the members ranked below this group's first one
+        for (int i = 0; i < (rank & ~7); ++i) rest &= rest - 1u;
+        const int lead_lane = __ffs(rest) - 1;
+        const int g = __popc(leaders & ((1u << lead_lane) - 1u));
+        const int j = rank & 7;
+        tab->slot[g][j] = s;
+        tab->xrow[g][j] = p.x_per_slot ? s : s / p.top_k;
+        if (j == 0) {
+            tab->expert[g] = id;
+            tab->count[g] = min(8, __popc(same) - rank);
+        }
+    }
+    if (lane == 0) tab->n_groups = __popc(leaders);
+    if (!valid && s < p.slots && blockIdx.x == 0) {
+        raise_status(NVFP4_DEV_BAD_EXPERT, p.status_user);
+        for (int n = 0; n < p.N; ++n) store_out(p.y, static_cast<int64_t>(s) * p.N + n, 0.f, p.out_bf16);
+    }
+    __syncwarp();
+}
+
+// The x rows that groups [g0, g1] need, staged in increasing row order (at most 32 rows).
+__device__ void tile_moe_rows(const TileParams& p, TileMoe* tab, int g0, int g1, int lane) {
+    uint32_t want = 0u;
+    for (int g = g0; g <= g1; ++g)
+        for (int j = 0; j < tab->count[g]; ++j) want |= 1u << tab->xrow[g][j];
+    if (lane == 0) tab->nrows = __popc(want);
+    if (lane < 32 && ((want >> lane) & 1u)) tab->rows[__popc(want & ((1u << lane) - 1u))] = lane;
+    __syncwarp();
+    for (int g = g0; g <= g1; ++g)
+        if (lane < tab->count[g]) tab->col[g][lane] = __popc(want & ((1u << tab->xrow[g][lane]) - 1u));
+    __syncwarp();
+}
+
+template <int NC, bool MOE>
 __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_kernel(const __grid_constant__ TileParams p) {
     extern __shared__ uint8_t smem_raw[];
     constexpr uint32_t kWBox = NC * 2048;  // 16 rows x NC x 128 B
@@ -1501,21 +1572,16 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_kernel(const __grid
     uint64_t* const bars = reinterpret_cast<uint64_t*>(sbase + p.bar_off) + warp * tk::kMaxStages;
     const uint32_t ring_w = base + p.ring_w + static_cast<uint32_t>(warp * stages) * kWBox;
     const uint32_t ring_s = base + p.ring_s + static_cast<uint32_t>(warp * stages) * kSBox;
+    TileMoe* const tab = reinterpret_cast<TileMoe*>(sbase + p.moe_off);
 
-    // this unit's items (a balanced contiguous block) and this CTA's K range within them
     const int S = 1 << p.s_log2;
     const int rank = S > 1 ? static_cast<int>(cluster_rank()) : 0;
-    const int unit = blockIdx.x >> p.s_log2;
-    const int ib = unit * p.items_q + min(unit, p.items_r);
-    const int ie = ib + p.items_q + (unit < p.items_r ? 1 : 0);
+    const int unit = blockIdx.x >> p.s_log2, units = gridDim.x >> p.s_log2;
     const int c_lo = (rank * p.nbox) >> p.s_log2, c_n = (((rank + 1) * p.nbox) >> p.s_log2) - c_lo;
     const int ksplit = 1 << p.ksplit_log2;
     const int kslice = warp & (ksplit - 1), tin = warp >> p.ksplit_log2;
     const int b_lo = c_lo + ((kslice * c_n) >> p.ksplit_log2), b_hi = c_lo + (((kslice + 1) * c_n) >> p.ksplit_log2);
     const int nb = b_hi - b_lo;
-    TileItemWalk first;
-    first.grp = ib >= p.ipg ? 1 : 0;  // at most two groups
-    first.t = ib - first.grp * p.ipg;
 
     if (lane == 0) {
         for (int s = 0; s < stages; ++s) mbar_init(&bars[s], 1);
@@ -1523,9 +1589,24 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_kernel(const __grid
     }
     __syncwarp();
 
+    // this unit's items: a balanced contiguous block (MoE: counted once the groups are known)
+    int ib = 0, ie = 0;
+    auto unit_range = [&](int items) {
+        const int q = items / units, r = items - q * units;
+        ib = unit * q + min(unit, r);
+        ie = ib + q + (unit < r ? 1 : 0);
+    };
+    if constexpr (!MOE) unit_range(p.items_q * units + p.items_r);
+    TileItemWalk first{0, 0};
+    auto set_first = [&]() {
+        first.grp = ib / p.ipg;
+        first.t = ib - first.grp * p.ipg;
+    };
+    if constexpr (!MOE) set_first();
+
     // issue cursor (lane 0): the next (item, box) of this warp's units
     TileItemWalk iw = first;
-    int iss_left = ie - ib, iss_box = 0;
+    int iss_left = 0, iss_box = 0;
     uint32_t issued = 0, consumed = 0;
     auto issue_next = [&]() {
         while (iss_left > 0 && (iss_box >= nb || iw.t * p.tpi + tin >= p.tiles)) {
@@ -1538,27 +1619,54 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_kernel(const __grid
         const uint32_t bar = smem_addr(&bars[st]);
         mbar_arrive_expect_tx(&bars[st], kWBox + kSBox);
         const int seg = (b_lo + iss_box) * NC;
-        const int row0 = (iw.t * p.tpi + tin) * 16;
-        tma_load_3d(ring_w + st * kWBox, &p.wmap[iw.grp], 0, seg, row0, bar);
-        tma_load_3d(ring_s + st * kSBox, &p.smap[iw.grp], 0, seg, row0, bar);
+        int row0 = (iw.t * p.tpi + tin) * 16;
+        int map = iw.grp;
+        if constexpr (MOE) {
+            row0 += tab->expert[iw.grp] * p.N;  // experts' rows are back to back
+            map = 0;
+        }
+        tma_load_3d(ring_w + st * kWBox, &p.wmap[map], 0, seg, row0, bar);
+        tma_load_3d(ring_s + st * kSBox, &p.smap[map], 0, seg, row0, bar);
         ++iss_box;
         ++issued;
     };
-    // weights never come from the preceding kernel: request them before the dependency wait;
-    // x may, so only an L2 prefetch of this CTA's K range of it goes out before the wait
-    if (lane == 0)
-        for (int s = 0; s < stages; ++s) issue_next();
-    if (warp == tk::kWarps - 1 && lane < p.M) {
-        const int kb = c_lo * NC * 256, kbytes = c_n * NC * 512;
-        const uint16_t* xr = p.x + static_cast<int64_t>(lane) * p.K + kb;
-        prefetch_l2_bulk(xr, static_cast<uint32_t>(kbytes));
-        prefetch_l2(xr);  // through this SM's own path too, so its address translation is warm
+    if constexpr (!MOE) {
+        // weights never come from the preceding kernel: request them before the dependency
+        // wait; x may, so only an L2 prefetch of this CTA's K range of it goes out before it
+        iss_left = ie - ib;
+        iw = first;
+        if (lane == 0)
+            for (int s = 0; s < stages; ++s) issue_next();
+        if (warp == tk::kWarps - 1 && lane < p.M) {
+            const int kb = c_lo * NC * 256, kbytes = c_n * NC * 512;
+            const uint16_t* xr = p.x + static_cast<int64_t>(lane) * p.K + kb;
+            prefetch_l2_bulk(xr, static_cast<uint32_t>(kbytes));
+            prefetch_l2(xr);  // through this SM's own path too, so its address translation is warm
+        }
     }
     pdl_launch_dependents();
     pdl_wait();
 
+    int M = p.M;                 // x rows staged by this CTA
+    const int* rowsel = nullptr; // their global row numbers (MoE)
+    if constexpr (MOE) {
+        // the expert ids may come from the preceding kernel: groups, items and weights only now
+        if (warp == 0) tile_moe_groups(p, tab, lane);
+        __syncthreads();
+        unit_range(tab->n_groups * p.ipg);
+        set_first();
+        if (warp == 0 && ib < ie) tile_moe_rows(p, tab, ib / p.ipg, (ie - 1) / p.ipg, lane);
+        iss_left = ie - ib;
+        iw = first;
+        if (lane == 0)
+            for (int s = 0; s < stages; ++s) issue_next();
+        __syncthreads();
+        M = ib < ie ? tab->nrows : 0;
+        rowsel = tab->rows;
+    }
+
     // x for this warp's K slice, staged by the tpi warps that share the slice
-    const uint32_t slice_bytes = static_cast<uint32_t>(p.M) * p.sstride;
+    const uint32_t slice_bytes = static_cast<uint32_t>(p.M) * p.sstride;  // p.M: staged-row capacity
     uint8_t* const xs = sbase + p.x_off + kslice * slice_bytes;
     float* const e2 = reinterpret_cast<float*>(sbase + p.misc_off) + kslice * 8;
     // per slice: 16 words of extremes for the scaled staging, then 8 words of votes
@@ -1567,16 +1675,17 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_kernel(const __grid
     const int xbar = p.tpi > 1 ? 2 + kslice : -1;
     bool lossy = false;
     float e2v = 1.f;
-    if (!stage_x_direct(p.x, p.M, p.K, k0, kn, xs, p.sstride, gmax + 16, tin, p.tpi, xbar, lane)) {
-        lossy = stage_x_slice(p.x, p.M, p.K, k0, kn, xs, p.sstride, e2, gmax, tin, p.tpi, xbar, lane);
+    if (M > 0 && !stage_x_direct(p.x, rowsel, M, p.K, k0, kn, xs, p.sstride, gmax + 16, tin, p.tpi, xbar, lane)) {
+        lossy = stage_x_slice(p.x, rowsel, M, p.K, k0, kn, xs, p.sstride, e2, gmax, tin, p.tpi, xbar, lane);
         e2v = e2[0];
     }
     const bool use_f32 = lossy || p.force_f32;
-    if (use_f32 && tin == 0 && lane == 0) atomicAdd(&g_fp32_fallbacks, 1ull);
+    if (use_f32 && M > 0 && tin == 0 && lane == 0) atomicAdd(&g_fp32_fallbacks, 1ull);
 
     const int g = lane >> 2;
     const int ra = tile_row_perm<NC>(g), rb = ra + 8;
-    const uint32_t xa = base + p.x_off + kslice * slice_bytes + static_cast<uint32_t>(min(g, p.M - 1)) * p.sstride;
+    const uint32_t xslice = base + p.x_off + kslice * slice_bytes;
+    uint32_t xa = xslice + static_cast<uint32_t>(min(g, max(M - 1, 0))) * p.sstride;
     const int m0 = 2 * t;
     const float e2s = use_f32 ? 1.f : e2v;  // the slice's power of two
     float* const red = reinterpret_cast<float*>(sbase + p.red_off);
@@ -1588,6 +1697,13 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_kernel(const __grid
         const int grp = cw.grp;
         const int tile = cw.t * p.tpi + tin;
         const bool valid = tile < p.tiles;
+        int ncols = p.M;                       // output columns of this item
+        const int* xrow = nullptr;             // global x row of each column (fp32 path)
+        if constexpr (MOE) {
+            ncols = tab->count[grp];
+            xrow = tab->xrow[grp];
+            xa = xslice + static_cast<uint32_t>(tab->col[grp][min(g, ncols - 1)]) * p.sstride;
+        }
         float d[4] = {0.f, 0.f, 0.f, 0.f};
         if (valid && !dead) {
             float d1[4] = {0.f, 0.f, 0.f, 0.f};
@@ -1608,8 +1724,8 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_kernel(const __grid
                 if (!use_f32) {
                     tile_slot_mma<NC>(ring_w + st * kWBox, ring_s + st * kSBox, xa, b * NC * 2, ra, t, d, d1);
                 } else {
-                    tile_slot_f32<NC>(ring_w + st * kWBox, ring_s + st * kSBox, p.x, p.K, p.M, (b_lo + b) * NC, ra,
-                                      t, acc);
+                    tile_slot_f32<NC>(ring_w + st * kWBox, ring_s + st * kSBox, p.x, xrow, p.K, ncols,
+                                      (b_lo + b) * NC, ra, t, acc);
                 }
                 ++consumed;
                 __syncwarp();
@@ -1636,25 +1752,31 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_kernel(const __grid
         // this slice's partial sums in x units: times its power of two
 #pragma unroll
         for (int i = 0; i < 4; ++i) d[i] *= e2s;
-        const float gs = p.g[grp];
+        float gs;
+        if constexpr (MOE) gs = __ldg(p.g_dev + tab->expert[grp]);
+        else gs = p.g[grp];
+        // where output (column m, row `row` of the group) goes
+        auto out_at = [&](int m, int row) -> int64_t {
+            if constexpr (MOE) return static_cast<int64_t>(tab->slot[grp][m]) * p.N + row;
+            else return m * p.ldy + static_cast<int64_t>(grp) * p.N + row;
+        };
         const int par = (item - ib) & 1;
         float* const cpart = reinterpret_cast<float*>(sbase + p.cpart_off) + par * (tk::kWarps * 16 * 8);
         if (ksplit == 1 && S == 1) {
             if (valid) {
                 const int rowa = tile * 16 + ra, rowb = tile * 16 + rb;
-                const int64_t col = static_cast<int64_t>(grp) * p.N;
-                if (m0 < p.M) {
-                    if (rowa < p.N) store_out(p.y, m0 * p.ldy + col + rowa, d[0] * gs, p.out_bf16);
-                    if (rowb < p.N) store_out(p.y, m0 * p.ldy + col + rowb, d[2] * gs, p.out_bf16);
+                if (m0 < ncols) {
+                    if (rowa < p.N) store_out(p.y, out_at(m0, rowa), d[0] * gs, p.out_bf16);
+                    if (rowb < p.N) store_out(p.y, out_at(m0, rowb), d[2] * gs, p.out_bf16);
                 }
-                if (m0 + 1 < p.M) {
-                    if (rowa < p.N) store_out(p.y, (m0 + 1) * p.ldy + col + rowa, d[1] * gs, p.out_bf16);
-                    if (rowb < p.N) store_out(p.y, (m0 + 1) * p.ldy + col + rowb, d[3] * gs, p.out_bf16);
+                if (m0 + 1 < ncols) {
+                    if (rowa < p.N) store_out(p.y, out_at(m0 + 1, rowa), d[1] * gs, p.out_bf16);
+                    if (rowb < p.N) store_out(p.y, out_at(m0 + 1, rowb), d[3] * gs, p.out_bf16);
                 }
             }
             continue;
         }
-        const int outs = p.tpi * 16 * p.M;  // this item's outputs, as (tile, row, m)
+        const int outs = p.tpi * 16 * ncols;  // this item's outputs, as (tile, row, m)
         if (ksplit == 1) {
             // one warp per tile: its sums are this CTA's part (cpart is [tile * 16 + row][m])
             float* cp = cpart + tin * 128;
@@ -1671,14 +1793,13 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_kernel(const __grid
             named_bar_sync(1, tk::kThreads);
             const float* rb0 = red + par * tk::kRedFloats;
             for (int i = tid; i < outs; i += tk::kThreads) {
-                const int ti = i / (16 * p.M), rem = i - ti * 16 * p.M;
-                const int r = rem / p.M, m = rem - r * p.M;
+                const int ti = i / (16 * ncols), rem = i - ti * 16 * ncols;
+                const int r = rem / ncols, m = rem - r * ncols;
                 float sum = 0.f;
                 for (int j = 0; j < ksplit; ++j) sum += rb0[((ti << p.ksplit_log2) + j) * 128 + r * 8 + m];
                 if (S == 1) {
                     const int tl = cw.t * p.tpi + ti, row = tl * 16 + r;
-                    if (tl < p.tiles && row < p.N)
-                        store_out(p.y, m * p.ldy + static_cast<int64_t>(grp) * p.N + row, sum * gs, p.out_bf16);
+                    if (tl < p.tiles && row < p.N) store_out(p.y, out_at(m, row), sum * gs, p.out_bf16);
                 } else {
                     cpart[ti * 128 + r * 8 + m] = sum;
                 }
@@ -1690,13 +1811,13 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_kernel(const __grid
         cluster_sync_all();
         const int o_lo = (rank * outs) >> p.s_log2, o_hi = ((rank + 1) * outs) >> p.s_log2;
         for (int i = o_lo + tid; i < o_hi; i += tk::kThreads) {
-            const int ti = i / (16 * p.M), rem = i - ti * 16 * p.M;
-            const int r = rem / p.M, m = rem - r * p.M;
+            const int ti = i / (16 * ncols), rem = i - ti * 16 * ncols;
+            const int r = rem / ncols, m = rem - r * ncols;
             const int tl = cw.t * p.tpi + ti, row = tl * 16 + r;
             if (tl < p.tiles && row < p.N) {
                 float sum = 0.f;
                 for (int j = 0; j < S; ++j) sum += ld_cluster_f32(cpart + ti * 128 + r * 8 + m, j);
-                store_out(p.y, m * p.ldy + static_cast<int64_t>(grp) * p.N + row, sum * gs, p.out_bf16);
+                store_out(p.y, out_at(m, row), sum * gs, p.out_bf16);
             }
         }
     }
@@ -2119,11 +2240,15 @@ struct TilePlan {
 // the 128-element steps of one warp per item) and a throughput term (items on the busiest
 // SM times the steps each of its warps decodes), both in units of one warp step.
 bool plan_tile(TilePlan& tp, int M, int N, int K, int groups, const DeviceInfo& d, const uint8_t* const* w,
-               const uint8_t* const* s, const void* x) {
+               const uint8_t* const* s, const void* x, bool moe = false, int moe_rows = 0) {
     if (g_variant == 1 || g_variant == 3) return false;
     if (K <= 0 || K % 256 != 0 || M < 1 || M > 8 || N < 1 || N > (1 << 27)) return false;
+    // MoE: M is the largest number of columns of a group (8), groups the estimated number of
+    // groups; moe_rows x rows may have to be staged by one CTA
+    const int xrows = moe ? moe_rows : M;
     if (reinterpret_cast<uintptr_t>(x) & 15) return false;
-    for (int i = 0; i < groups; ++i)
+    const int tensors = moe ? 1 : groups;  // weight tensors: one for all experts, else one per group
+    for (int i = 0; i < tensors; ++i)
         if ((reinterpret_cast<uintptr_t>(w[i]) & 15) || (reinterpret_cast<uintptr_t>(s[i]) & 15)) return false;
     if (!tensor_map_encoder()) return false;
     const int segs = K / 256;
@@ -2135,7 +2260,7 @@ bool plan_tile(TilePlan& tp, int M, int N, int K, int groups, const DeviceInfo& 
         const int nbox = segs / nc;
         for (int sl = 0; (1 << sl) <= 8; ++sl) {
             const int S = 1 << sl;
-            if (S > nbox) break;
+            if (S > nbox || (moe && S > 1)) break;
             if (NVFP4_TILE_S && S != NVFP4_TILE_S) continue;
             const int nbs = (nbox + S - 1) / S;  // most boxes of one rank
             for (int lg = 0; (1 << lg) <= tk::kWarps; ++lg) {
@@ -2149,7 +2274,16 @@ bool plan_tile(TilePlan& tp, int M, int N, int K, int groups, const DeviceInfo& 
                 if (items > (1LL << 30)) continue;
                 const int nbmax = (nbs + ksplit - 1) / ksplit;  // most boxes of one warp per item
                 const uint32_t sstride = static_cast<uint32_t>(nbmax) * nc * 512u + 64u;
-                const uint32_t x_bytes = align_up(static_cast<uint32_t>(ksplit * M) * sstride, 128);
+                int rows_cap = xrows;
+                if (moe) {
+                    // a unit runs at most ipu contiguous items (units >= min(SMs, items)), so it
+                    // touches at most ceil(ipu / ipg) + 1 groups of at most 8 columns each
+                    const long long ipu = (items + std::min<long long>(d.sm_count, items) - 1) /
+                                          std::min<long long>(d.sm_count, items);
+                    const long long span = (ipu + ipg - 1) / ipg + 1;
+                    rows_cap = static_cast<int>(std::min<long long>(xrows, 8 * span));
+                }
+                const uint32_t x_bytes = align_up(static_cast<uint32_t>(ksplit * rows_cap) * sstride, 128);
                 // deepest ring that still allows two CTAs per SM, else the deepest that fits one
                 int stages = 0, per_sm = 0;
                 uint32_t smem = 0;
@@ -2172,6 +2306,8 @@ bool plan_tile(TilePlan& tp, int M, int N, int K, int groups, const DeviceInfo& 
                         off += align_up(tk::kWarps * 32 + tk::kWarps * 32 * 4, 128);  // e2, extremes, votes
                         q.bar_off = off;
                         off += tk::kWarps * tk::kMaxStages * 8;
+                        q.moe_off = align_up(off, 16);
+                        if (moe) off = q.moe_off + static_cast<uint32_t>(sizeof(TileMoe));
                         const uint32_t total = off + 1024;  // slack to align the base to 1024 bytes
                         const uint32_t limit = want == 2 ? static_cast<uint32_t>(d.smem_per_sm / 2 - 1024)
                                                          : static_cast<uint32_t>(d.smem_optin);
@@ -2197,13 +2333,13 @@ bool plan_tile(TilePlan& tp, int M, int N, int K, int groups, const DeviceInfo& 
                 const double ovh = (ksplit > 1 ? 2.0 : 0.3) + (S > 1 ? 10.0 : 0.0);
                 const double lat = static_cast<double>(ipu) * (spw + ovh);
                 const double thr = static_cast<double>(items) * tk::kWarps * S * spw / (d.sm_count * 16.0) * 1.1;
-                const double stage = static_cast<double>(M) * K / (2048.0 * S);
+                const double stage = static_cast<double>(moe ? std::min(rows_cap, 8) : xrows) * K / (2048.0 * S);
                 const double cost = std::max(lat, thr) + stage;
                 if (!found || cost < best - 1e-9) {
                     found = true;
                     best = cost;
                     tp.p = lp;
-                    tp.p.M = M;
+                    tp.p.M = rows_cap;
                     tp.p.N = N;
                     tp.p.K = K;
                     tp.p.tiles = tiles;
@@ -2255,9 +2391,9 @@ bool encode_tile_maps(CUtensorMap* wmap, CUtensorMap* smap, const uint8_t* w, co
     return true;
 }
 
-template <int NC>
+template <int NC, bool MOE>
 cudaError_t launch_tile_nc(const TilePlan& tp, cudaStream_t st) {
-    auto kern = gemv_tile_kernel<NC>;
+    auto kern = gemv_tile_kernel<NC, MOE>;
     static bool done[64] = {};
     cudaError_t e = allow_max_smem(kern, done);
     if (e != cudaSuccess) return e;
@@ -2285,8 +2421,9 @@ cudaError_t launch_tile_nc(const TilePlan& tp, cudaStream_t st) {
     return cudaLaunchKernelEx(&cfg, kern, tp.p);
 }
 
-cudaError_t launch_tile(const TilePlan& tp, cudaStream_t st) {
-    return tp.nc == 2 ? launch_tile_nc<2>(tp, st) : launch_tile_nc<1>(tp, st);
+cudaError_t launch_tile(const TilePlan& tp, cudaStream_t st, bool moe) {
+    if (moe) return tp.nc == 2 ? launch_tile_nc<2, true>(tp, st) : launch_tile_nc<1, true>(tp, st);
+    return tp.nc == 2 ? launch_tile_nc<2, false>(tp, st) : launch_tile_nc<1, false>(tp, st);
 }
 
 cudaError_t launch_simple(const SimpleParams& sp, int64_t cols, cudaStream_t st) {
@@ -2350,7 +2487,7 @@ nvfp4_status run_dense(const uint8_t* const* w, const uint8_t* const* s, const f
             p.out_bf16 = y_type == NVFP4_OUT_BF16;
             p.force_f32 = g_variant == 2;
             p.wait_ns = g_wait_ns;
-            const cudaError_t e = launch_tile(tpl, st);
+            const cudaError_t e = launch_tile(tpl, st, false);
             if (e != cudaSuccess) return cuda_fail(e);
             const cudaError_t e2 = cudaGetLastError();
             return e2 == cudaSuccess ? NVFP4_OK : cuda_fail(e2);
@@ -2428,6 +2565,37 @@ nvfp4_status nvfp4_moe_gemv(const uint8_t* w_packed, const uint8_t* w_scales,
     if (K == 0) return zero_output(y, static_cast<int64_t>(slots) * N, y_type, st);
     const DeviceInfo* d = device_info(nullptr);
     if (!d) return cuda_fail(cudaGetLastError());
+    if (slots <= kTileMoeSlots && static_cast<int64_t>(E) * N <= (1 << 30)) {
+        // warp-tile kernel: every routed expert's slab is read once for all of its slots
+        TilePlan tpl{};
+        const uint8_t* wv[1] = {w_packed};
+        const uint8_t* sv[1] = {w_scales};
+        const int xrows = x_per_slot ? slots : T;
+        if (plan_tile(tpl, 8, N, K, slots, *d, wv, sv, x, true, xrows) &&
+            encode_tile_maps(&tpl.p.wmap[0], &tpl.p.smap[0], w_packed, w_scales, static_cast<int64_t>(E) * N, K,
+                             tpl.nc)) {
+            TileParams& p = tpl.p;
+            p.wmap[1] = p.wmap[0];
+            p.smap[1] = p.smap[0];
+            p.x = x;
+            p.y = y;
+            p.ldy = N;
+            p.out_bf16 = y_type == NVFP4_OUT_BF16;
+            p.force_f32 = g_variant == 2;
+            p.wait_ns = g_wait_ns;
+            p.ids = expert_ids;
+            p.g_dev = global_scales;
+            p.status_user = status_dev;
+            p.E = E;
+            p.top_k = top_k;
+            p.slots = slots;
+            p.x_per_slot = x_per_slot ? 1 : 0;
+            const cudaError_t e = launch_tile(tpl, st, true);
+            if (e != cudaSuccess) return cuda_fail(e);
+            const cudaError_t e2 = cudaGetLastError();
+            return e2 == cudaSuccess ? NVFP4_OK : cuda_fail(e2);
+        }
+    }
     Plan pl{};
     if (plan_moe(pl, E, T, top_k, N, K, *d, w_packed, w_scales, x)) {
         Params& p = pl.p;
@@ -2529,7 +2697,17 @@ int nvfp4_describe_plan(int kind, int M, int N, int K, int T, int top_k, char* b
         }
         ok = plan_dense(pl, M, N, K, kind == 0 ? 1 : 2, *d, w, w, fake);
     }
-    if (kind == 2) ok = plan_moe(pl, 288, T, top_k, N, K, *d, fake, fake, fake);
+    if (kind == 2) {
+        TilePlan tpl{};
+        const int slots = T * top_k;
+        if (slots <= kTileMoeSlots && plan_tile(tpl, 8, N, K, slots, *d, w, w, fake, true, slots)) {
+            return snprintf(buf, buflen,
+                            "tile_moe grid=%d block=%d smem=%u split=1 rows_per_item=%d k_warps=%d mt=8 stages=%d nc=%d",
+                            tpl.grid_x, tk::kThreads, tpl.smem, tpl.p.tpi * 16, 1 << tpl.p.ksplit_log2, tpl.p.stages,
+                            tpl.nc);
+        }
+        ok = plan_moe(pl, 288, T, top_k, N, K, *d, fake, fake, fake);
+    }
     int n;
     if (!ok) {
         n = snprintf(buf, buflen, "simple grid=%lld block=%d smem=0 split=1 rows_per_item=0 k_warps=0",

@@ -104,8 +104,11 @@ def test_vocab_head_m1():
     assert_parity(y, yr, ya, "vocab head")
 
 
+@pytest.mark.parametrize("variant", [0, 3])
 @pytest.mark.parametrize("x_per_slot,N,K", [(False, 3072, 4096), (True, 4096, 1536)])
-def test_moe_288_experts_top8(x_per_slot, N, K):
+def test_moe_288_experts_top8(x_per_slot, N, K, variant):
+    # variant 3: the bulk-copy streaming kernel instead of the warp-tile kernel
+    nv.set_variant(variant)
     p = synth.moe_problem(288, N, K, 4, 8, x_per_slot, seed=8, device=DEV)
     st = torch.zeros(1, dtype=torch.int32, device=DEV)
     y = nv.moe_gemv(p["w"], p["s"], p["gs"], p["ids"], p["x"], x_per_slot, 8, status=st)
@@ -350,6 +353,18 @@ def test_moe_repeated_experts_are_shared(x_per_slot):
     p = synth.moe_problem(E, N, K, T, top_k, x_per_slot, seed=310, fill="all")
     ids = [3, 3, 7, 3, 9, 7, 3, 3, 3, 1, 3, 5, 0, 3, 15]   # expert 3 in 8 slots (> one group)
     st, bad = _moe_check(p, ids, x_per_slot, top_k)
+    assert st == 0 and bad == 0
+
+
+@pytest.mark.parametrize("x_per_slot", [False, True])
+def test_moe_tile_groups_32_slots(x_per_slot):
+    # 32 slots (the tile kernel's limit): one expert in 20 slots (three groups of <= 8), the
+    # rest spread, a ragged N and bf16 output
+    E, N, K, T, top_k = 12, 200, 1024, 4, 8
+    p = synth.moe_problem(E, N, K, T, top_k, x_per_slot, seed=315, fill="all")
+    ids = [5] * 20 + [0, 1, 2, 3, 4, 6, 7, 8, 9, 10, 11, 1]
+    assert nv.describe_plan("moe", 8, N, K, T, top_k).startswith("tile_moe ")
+    st, bad = _moe_check(p, ids, x_per_slot, top_k, torch.bfloat16)
     assert st == 0 and bad == 0
 
 
