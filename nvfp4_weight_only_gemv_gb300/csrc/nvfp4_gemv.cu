@@ -1252,8 +1252,11 @@ __host__ __device__ __forceinline__ int tile_row_perm(int g) {
 // no reduction: each lane checks its own values and the slice votes. Returns true when every
 // value converted exactly (uniform over the slice's warps); otherwise the caller re-stages
 // with a power-of-two scale. `vote` is gw words of shared scratch; bar_id < 0: one warp.
+// after_issue() runs once the first loads are out (M > 0 or not).
+template <typename F>
 __device__ bool stage_x_direct(const uint16_t* __restrict__ x, const int* rowsel, int M, int K, int k0, int kn,
-                               uint8_t* xs, uint32_t sstride, uint32_t* vote, int gi, int gw, int bar_id, int lane) {
+                               uint8_t* xs, uint32_t sstride, uint32_t* vote, int gi, int gw, int bar_id, int lane,
+                               F&& after_issue) {
     constexpr int kPre = 12;
     const int cpr = kn >> 3;
     const int tl = gi * 32 + lane, nt = gw * 32;
@@ -1294,6 +1297,7 @@ __device__ bool stage_x_direct(const uint16_t* __restrict__ x, const int* rowsel
                          : make_uint4(0u, 0u, 0u, 0u);
             advance();
         }
+        after_issue();  // the caller's own requests queue behind these loads, not in front
 #pragma unroll
         for (int i = 0; i < kPre; ++i)
             if (mi[i] < M) convert(v[i], mi[i], ci[i]);
@@ -1313,8 +1317,8 @@ __device__ bool stage_x_direct(const uint16_t* __restrict__ x, const int* rowsel
 // Stages x[:, k0 : k0 + kn] for the warps of one K slice (gw warps; this one is number gi
 // of them) in f16 for the tensor cores: rows `sstride` bytes apart at xs, elements at
 // mma_x_off. The slice gets one power of two, x' = x * 2^-E with its largest |x| in
-// [2^12, 2^13), and *e2 = 2^E. Exact for every value at most 2^26 below that largest one
-// (see stage_x_mma); a slice holding a smaller nonzero value, Inf or NaN is reported lossy
+// [2^15, 2^16), and *e2 = 2^E. Exact for every value at most 2^32 below that largest one;
+// a slice holding a smaller nonzero value, Inf or NaN is reported lossy
 // and its warps compute in fp32 instead. Because each slice's partial sums are multiplied by
 // its own e2 before slices are added, slices need no common scale and no CTA-wide step.
 // The slice's rows are walked as one flat sequence of 16-byte chunks; the first kPre of each
@@ -1389,8 +1393,10 @@ __device__ bool stage_x_slice(const uint16_t* __restrict__ x, const int* rowsel,
     } else {
         e_max = static_cast<int>(a >> 7) - 127;
     }
-    const int E = e_max - 12;
-    const int tb = E - 14 + 127;           // smallest exact magnitude 2^(E - 14) as a bf16 pattern
+    // largest |x'| in [2^15, 2^16): every bf16 value there (<= 65280) is an f16. Down to 2^-17
+    // a bf16 value's last bit is a multiple of 2^-24, the f16 subnormal step, so it is exact too
+    const int E = e_max - 15;
+    const int tb = E - 17 + 127;           // smallest certainly exact magnitude 2^(E - 17), as bf16 bits
     const uint32_t thresh = tb >= 1 ? static_cast<uint32_t>(tb) << 7 : 0x80u;
     lossy |= z != 0x7fffu && z < thresh;
     if (gi == 0 && lane == 0) *e2 = pow2f(E);
@@ -1643,6 +1649,14 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_kernel(const __grid
             prefetch_l2_bulk(xr, static_cast<uint32_t>(kbytes));
             prefetch_l2(xr);  // through this SM's own path too, so its address translation is warm
         }
+    } else {
+        // which experts and rows are needed is known only from the ids: prefetch them and x
+        if (warp == tk::kWarps - 1 && lane == 0) prefetch_l2(p.ids);
+        const int xrows_all = p.x_per_slot ? p.slots : (p.slots + p.top_k - 1) / p.top_k;
+        if (warp == tk::kWarps - 2 && lane < xrows_all) {
+            const int kb = c_lo * NC * 256, kbytes = c_n * NC * 512;
+            prefetch_l2_bulk(p.x + static_cast<int64_t>(lane) * p.K + kb, static_cast<uint32_t>(kbytes));
+        }
     }
     pdl_launch_dependents();
     pdl_wait();
@@ -1658,8 +1672,6 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_kernel(const __grid
         if (warp == 0 && ib < ie) tile_moe_rows(p, tab, ib / p.ipg, (ie - 1) / p.ipg, lane);
         iss_left = ie - ib;
         iw = first;
-        if (lane == 0)
-            for (int s = 0; s < stages; ++s) issue_next();
         __syncthreads();
         M = ib < ie ? tab->nrows : 0;
         rowsel = tab->rows;
@@ -1675,9 +1687,16 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_kernel(const __grid
     const int xbar = p.tpi > 1 ? 2 + kslice : -1;
     bool lossy = false;
     float e2v = 1.f;
-    if (M > 0 && !stage_x_direct(p.x, rowsel, M, p.K, k0, kn, xs, p.sstride, gmax + 16, tin, p.tpi, xbar, lane)) {
+    if (M > 0 && !stage_x_direct(p.x, rowsel, M, p.K, k0, kn, xs, p.sstride, gmax + 16, tin, p.tpi, xbar, lane,
+                                 [] {})) {
         lossy = stage_x_slice(p.x, rowsel, M, p.K, k0, kn, xs, p.sstride, e2, gmax, tin, p.tpi, xbar, lane);
         e2v = e2[0];
+    }
+    if constexpr (MOE) {
+        // the weights of this CTA's experts: issued after staging, because a thread that issues
+        // bulk copies can stall while the copy engine is busy, and staging waits for every warp
+        if (lane == 0)
+            for (int s = 0; s < stages; ++s) issue_next();
     }
     const bool use_f32 = lossy || p.force_f32;
     if (use_f32 && M > 0 && tin == 0 && lane == 0) atomicAdd(&g_fp32_fallbacks, 1ull);
@@ -2227,6 +2246,18 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
+// Groups a routing of T tokens to top_k distinct experts each, out of E, is expected to
+// form when the experts are uniform: the expected number of distinct experts (each with at
+// most 8 slots, so one group each), E * (1 - (1 - top_k / E)^T), rounded, at least 1.
+int expected_groups(int E, int T, int top_k) {
+    if (E <= 0 || T <= 0 || top_k <= 0) return 1;
+    const double q = 1.0 - std::min(1.0, static_cast<double>(top_k) / E);
+    double miss = 1.0;
+    for (int i = 0; i < T; ++i) miss *= q;
+    const double g = E * (1.0 - miss);
+    return std::max(1, std::min(T * top_k, static_cast<int>(g + 0.5)));
+}
+
 struct TilePlan {
     TileParams p;
     int nc;
@@ -2240,11 +2271,11 @@ struct TilePlan {
 // the 128-element steps of one warp per item) and a throughput term (items on the busiest
 // SM times the steps each of its warps decodes), both in units of one warp step.
 bool plan_tile(TilePlan& tp, int M, int N, int K, int groups, const DeviceInfo& d, const uint8_t* const* w,
-               const uint8_t* const* s, const void* x, bool moe = false, int moe_rows = 0) {
+               const uint8_t* const* s, const void* x, bool moe = false, int moe_rows = 0, int moe_groups_max = 0) {
     if (g_variant == 1 || g_variant == 3) return false;
     if (K <= 0 || K % 256 != 0 || M < 1 || M > 8 || N < 1 || N > (1 << 27)) return false;
-    // MoE: M is the largest number of columns of a group (8), groups the estimated number of
-    // groups; moe_rows x rows may have to be staged by one CTA
+    // MoE: M is the largest number of columns of a group (8), groups the expected number of
+    // groups (cost only), moe_groups_max the most there can be; moe_rows x rows exist in all
     const int xrows = moe ? moe_rows : M;
     if (reinterpret_cast<uintptr_t>(x) & 15) return false;
     const int tensors = moe ? 1 : groups;  // weight tensors: one for all experts, else one per group
@@ -2276,10 +2307,12 @@ bool plan_tile(TilePlan& tp, int M, int N, int K, int groups, const DeviceInfo& 
                 const uint32_t sstride = static_cast<uint32_t>(nbmax) * nc * 512u + 64u;
                 int rows_cap = xrows;
                 if (moe) {
-                    // a unit runs at most ipu contiguous items (units >= min(SMs, items)), so it
+                    // the launch has units >= min(SMs, items) (items: the expected count), so a
+                    // unit runs at most ipu contiguous items of the largest possible count, and
                     // touches at most ceil(ipu / ipg) + 1 groups of at most 8 columns each
-                    const long long ipu = (items + std::min<long long>(d.sm_count, items) - 1) /
-                                          std::min<long long>(d.sm_count, items);
+                    const long long items_max = static_cast<long long>(std::max(moe_groups_max, groups)) * ipg;
+                    const long long units_lo = std::min<long long>(d.sm_count, items);
+                    const long long ipu = (items_max + units_lo - 1) / units_lo;
                     const long long span = (ipu + ipg - 1) / ipg + 1;
                     rows_cap = static_cast<int>(std::min<long long>(xrows, 8 * span));
                 }
@@ -2330,7 +2363,7 @@ bool plan_tile(TilePlan& tp, int M, int N, int K, int groups, const DeviceInfo& 
                 const long long ipu = (items + units - 1) / units;
                 const double spw = 2.0 * nc * nbmax;
                 // measured: a reduction over warps costs ~2 steps, one over a cluster ~10
-                const double ovh = (ksplit > 1 ? 2.0 : 0.3) + (S > 1 ? 10.0 : 0.0);
+                const double ovh = (ksplit > 1 ? (moe ? 4.0 : 2.0) : 0.3) + (S > 1 ? 10.0 : 0.0);
                 const double lat = static_cast<double>(ipu) * (spw + ovh);
                 const double thr = static_cast<double>(items) * tk::kWarps * S * spw / (d.sm_count * 16.0) * 1.1;
                 const double stage = static_cast<double>(moe ? std::min(rows_cap, 8) : xrows) * K / (2048.0 * S);
@@ -2571,7 +2604,7 @@ nvfp4_status nvfp4_moe_gemv(const uint8_t* w_packed, const uint8_t* w_scales,
         const uint8_t* wv[1] = {w_packed};
         const uint8_t* sv[1] = {w_scales};
         const int xrows = x_per_slot ? slots : T;
-        if (plan_tile(tpl, 8, N, K, slots, *d, wv, sv, x, true, xrows) &&
+        if (plan_tile(tpl, 8, N, K, expected_groups(E, T, top_k), *d, wv, sv, x, true, xrows, slots) &&
             encode_tile_maps(&tpl.p.wmap[0], &tpl.p.smap[0], w_packed, w_scales, static_cast<int64_t>(E) * N, K,
                              tpl.nc)) {
             TileParams& p = tpl.p;
@@ -2700,7 +2733,8 @@ int nvfp4_describe_plan(int kind, int M, int N, int K, int T, int top_k, char* b
     if (kind == 2) {
         TilePlan tpl{};
         const int slots = T * top_k;
-        if (slots <= kTileMoeSlots && plan_tile(tpl, 8, N, K, slots, *d, w, w, fake, true, slots)) {
+        if (slots <= kTileMoeSlots &&
+            plan_tile(tpl, 8, N, K, expected_groups(288, T, top_k), *d, w, w, fake, true, slots, slots)) {
             return snprintf(buf, buflen,
                             "tile_moe grid=%d block=%d smem=%u split=1 rows_per_item=%d k_warps=%d mt=8 stages=%d nc=%d",
                             tpl.grid_x, tk::kThreads, tpl.smem, tpl.p.tpi * 16, 1 << tpl.p.ksplit_log2, tpl.p.stages,
