@@ -91,6 +91,23 @@ def kernel_traffic(workload):
         return None
 
 
+def kernels_of(calls):
+    """Names of the library kernels the step's calls launch (from the library's own plan)."""
+    import nvfp4_weight_only_gemv_gb300 as nv
+    names = {"tile": "gemv_tile_kernel", "tile_moe": "gemv_tile_kernel (MoE)", "stream": "gemv_stream_kernel",
+             "stream_moe": "gemv_stream_kernel (MoE)", "simple": "gemv_simple_kernel"}
+    seen = []
+    for c in calls:
+        if c.kind.startswith("moe"):
+            desc = nv.describe_plan("moe", 8, c.N, c.K, c.T, c.top_k)
+        else:
+            desc = nv.describe_plan("gate_up" if c.kind == "gate_up" else "dense", c.M, c.N, c.K)
+        name = names.get(desc.split()[0], desc.split()[0])
+        if name not in seen:
+            seen.append(name)
+    return ", ".join(seen) + " (every launch of the step)"
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -474,7 +491,7 @@ def run_ours(args):
     traffic = kernel_traffic(args.workload)
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": traffic,
-                "kernel": "gemv_stream_kernel (every launch of the step)",
+                "kernel": kernels_of(calls),
                 "us_per_launch": round(us_per_launch, 3),
                 "pct_of_8TBps": round(100 * achieved / NOMINAL_HBM_GBS, 2),
                 "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs: copy bandwidth)"}

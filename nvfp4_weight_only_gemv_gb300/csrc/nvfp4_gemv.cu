@@ -8,26 +8,19 @@
 // "glm-5.3-flash-nvfp4-tp3-512k--gb10 graph.json": the weight is widened, multiplied by
 // the bf16 activation and accumulated in f32, and the f32 tensor scale is applied last.
 //
-// Design (a bandwidth-bound GEMV at M <= 8, so CUDA cores rather than tensor cores):
-//   * One persistent CTA per SM. The grid is sized from the SM count and covers a
-//     balanced, contiguous block of "items" (an item is up to 32 KB of whole weight rows).
-//   * Warp 8 (producer): streams each item's packed codes and scales from HBM into a
-//     4-stage shared-memory ring with cp.async.bulk (TMA bulk copies) that complete on
-//     per-stage mbarriers.
-//   * Warps 0..7 (consumers): x is staged once per CTA in shared memory as fp32, in a
-//     layout without bank conflicts. Each lane decodes 32 weights per step with
-//     cvt.rn.f16x2.e2m1x2, widens them times the block scale with the mixed-precision
-//     fma.rn.f32.f16, and accumulates with packed fma.rn.f32x2 in fp32.
-//     A warp-level transposed butterfly reduces R rows x M outputs at once.
-//   * Warp 9 (epilogue): adds the per-warp partials in a fixed order (deterministic),
-//     applies g and stores fp32 or bf16 (round to nearest even).
-//   * When fp32 x does not fit next to the ring (large M * K), K is split across a thread
-//     block cluster of S CTAs. Each CTA keeps partial sums for its rows, and after a
-//     cluster barrier the partials are summed over DSMEM (ld.shared::cluster).
-//   * Every mbarrier wait is bounded by a %globaltimer budget. On expiry the kernel sets
-//     a device status bit, waits for the copies it has in flight and returns: it never traps.
-//   * A plain byte-load kernel covers shapes and alignments that the bulk-copy path does
-//     not take (K % 32 != 0, unaligned base pointers, very large M * K, > 256 MoE slots).
+// Three kernels:
+//   * gemv_tile_kernel (default for K % 256 == 0, aligned operands; dense, gate/up and up to
+//     32 MoE slots): every warp owns 16-row tiles and keeps its own ring of TMA tensor copies
+//     (128-byte swizzled codes + scales) full; the products run on the tensor cores as
+//     mma.sync.m16n8k16 with the weights decoded exactly to f16 (E2M1 * E4M3) and x staged in
+//     f16 per K slice. K may be split over warps (shared-memory reduction) or over a cluster
+//     (DSMEM reduction), both in a fixed order. See the comment above the kernel.
+//   * gemv_stream_kernel (K % 32 == 0 otherwise, or up to 256 MoE slots): a producer warp
+//     bulk-copies whole items of rows into a ring, consumer warps decode with the same MMA
+//     scheme and an epilogue warp reduces in a fixed order.
+//   * gemv_simple_kernel: byte loads for every other alignment and size.
+// Every mbarrier wait is bounded by a %globaltimer budget. On expiry a kernel sets a device
+// status bit, drains the copies it has in flight and finishes: it never traps.
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
