@@ -1239,6 +1239,10 @@ __host__ __device__ __forceinline__ int tile_row_perm(int g) {
     else return g;
 }
 
+#ifndef NVFP4_STAGE_PRE
+#define NVFP4_STAGE_PRE 2
+#endif
+
 // Fast staging of x[:, k0 : k0 + kn] for the warps of one K slice: every bf16 value is
 // converted to f16 unscaled, which is exact when it is zero or 2^-17 <= |x| < 2^16 (a bf16
 // value has 8 significant bits; f16 keeps them down to its subnormal step 2^-24). One pass,
@@ -1250,7 +1254,7 @@ template <typename F>
 __device__ bool stage_x_direct(const uint16_t* __restrict__ x, const int* rowsel, int M, int K, int k0, int kn,
                                uint8_t* xs, uint32_t sstride, uint32_t* vote, int gi, int gw, int bar_id, int lane,
                                F&& after_issue) {
-    constexpr int kPre = 12;
+    constexpr int kPre = NVFP4_STAGE_PRE;
     const int cpr = kn >> 3;
     const int tl = gi * 32 + lane, nt = gw * 32;
     int m = 0, c = tl;
@@ -1320,7 +1324,7 @@ __device__ bool stage_x_direct(const uint16_t* __restrict__ x, const int* rowsel
 __device__ bool stage_x_slice(const uint16_t* __restrict__ x, const int* rowsel, int M, int K, int k0, int kn,
                               uint8_t* xs, uint32_t sstride, float* e2, uint32_t* gmax, int gi, int gw, int bar_id,
                               int lane) {
-    constexpr int kPre = 12;
+    constexpr int kPre = NVFP4_STAGE_PRE;
     const int cpr = kn >> 3;                      // 16-byte chunks per row of the slice
     const int total = M * cpr;
     const int tl = gi * 32 + lane, nt = gw * 32;  // this lane among the slice's lanes
@@ -1424,10 +1428,15 @@ __device__ bool stage_x_slice(const uint16_t* __restrict__ x, const int* rowsel,
 // takes the 32 codes 32t .. 32t + 31 of each step for its rows ra = perm(g), rb = ra + 8
 // (see compute_item_mma for the k permutation shared with the staged x; xa points at this
 // lane's x row, `chunk0` is the slot's first 128-element chunk within the staged slice).
-// Two accumulator sets shorten the MMA dependency chain.
+// Several accumulator sets (kTileChains) shorten the MMA dependency chain.
+#ifndef NVFP4_TILE_CHAINS
+#define NVFP4_TILE_CHAINS 4
+#endif
+constexpr int kTileChains = NVFP4_TILE_CHAINS;  // independent MMA accumulator chains per warp
+
 template <int NC>
 __device__ __forceinline__ void tile_slot_mma(uint32_t wst, uint32_t sst, uint32_t xa, int chunk0, int ra, int t,
-                                              float (&d0)[4], float (&d1)[4]) {
+                                              float (&dd)[kTileChains][4]) {
     const int rb = ra + 8;
 #pragma unroll
     for (int c = 0; c < NC; ++c) {
@@ -1451,10 +1460,10 @@ __device__ __forceinline__ void tile_slot_mma(uint32_t wst, uint32_t sst, uint32
                 cvt_e2m1x8(w == 0 ? wa.x : (w == 1 ? wa.y : (w == 2 ? wa.z : wa.w)), ha);
                 cvt_e2m1x8(w == 0 ? wb.x : (w == 1 ? wb.y : (w == 2 ? wb.z : wb.w)), hb);
                 const uint32_t s_a = w < 2 ? sa0 : sa1, s_b = w < 2 ? sb0 : sb1;
-                mma_16816(d0, hmul2_u32(ha[0], s_a), hmul2_u32(hb[0], s_b), hmul2_u32(ha[1], s_a),
-                          hmul2_u32(hb[1], s_b), xq[w].x, xq[w].y);
-                mma_16816(d1, hmul2_u32(ha[2], s_a), hmul2_u32(hb[2], s_b), hmul2_u32(ha[3], s_a),
-                          hmul2_u32(hb[3], s_b), xq[w].z, xq[w].w);
+                mma_16816(dd[(2 * w) % kTileChains], hmul2_u32(ha[0], s_a), hmul2_u32(hb[0], s_b),
+                          hmul2_u32(ha[1], s_a), hmul2_u32(hb[1], s_b), xq[w].x, xq[w].y);
+                mma_16816(dd[(2 * w + 1) % kTileChains], hmul2_u32(ha[2], s_a), hmul2_u32(hb[2], s_b),
+                          hmul2_u32(ha[3], s_a), hmul2_u32(hb[3], s_b), xq[w].z, xq[w].w);
             }
         }
     }
@@ -1718,7 +1727,11 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_kernel(const __grid
         }
         float d[4] = {0.f, 0.f, 0.f, 0.f};
         if (valid && !dead) {
-            float d1[4] = {0.f, 0.f, 0.f, 0.f};
+            float dd[kTileChains][4];
+#pragma unroll
+            for (int c = 0; c < kTileChains; ++c)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) dd[c][i] = 0.f;
             float acc[16];
             if (use_f32) {
 #pragma unroll
@@ -1734,7 +1747,7 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_kernel(const __grid
                     break;
                 }
                 if (!use_f32) {
-                    tile_slot_mma<NC>(ring_w + st * kWBox, ring_s + st * kSBox, xa, b * NC * 2, ra, t, d, d1);
+                    tile_slot_mma<NC>(ring_w + st * kWBox, ring_s + st * kSBox, xa, b * NC * 2, ra, t, dd);
                 } else {
                     tile_slot_f32<NC>(ring_w + st * kWBox, ring_s + st * kSBox, p.x, xrow, p.K, ncols,
                                       (b_lo + b) * NC, ra, t, acc);
@@ -1757,7 +1770,9 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_kernel(const __grid
                 }
             } else {
 #pragma unroll
-                for (int i = 0; i < 4; ++i) d[i] += d1[i];
+                for (int c = 0; c < kTileChains; ++c)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) d[i] += dd[c][i];
             }
             if (dead) raise_status(NVFP4_DEV_TIMEOUT, nullptr);
         }
