@@ -99,7 +99,7 @@ def kernels_of(calls):
     seen = []
     for c in calls:
         if c.kind.startswith("moe"):
-            desc = nv.describe_plan("moe", 8, c.N, c.K, c.T, c.top_k)
+            desc = nv.describe_plan("moe_per_slot" if c.x_per_slot else "moe", c.E, c.N, c.K, c.T, c.top_k)
         else:
             desc = nv.describe_plan("gate_up" if c.kind == "gate_up" else "dense", c.M, c.N, c.K)
         name = names.get(desc.split()[0], desc.split()[0])

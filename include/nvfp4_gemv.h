@@ -167,11 +167,12 @@ void nvfp4_set_pdl(int enable);
 
 /*
  * Describes the launch the next call with these arguments would make. It writes
- * "kernel grid block smem split rows_per_item k_warps" into buf (host memory, NUL-terminated).
- * Returns the number of characters, or -1.
+ * "kernel grid block smem split rows_per_item k_warps ..." into buf (host memory,
+ * NUL-terminated). kind: 0 dense, 1 gate_up, 2 MoE with x shared by a token's slots,
+ * 3 MoE with one x row per slot; for the MoE kinds M is the number of experts E.
+ * Pointers are assumed 256-byte aligned. Returns the number of characters, or -1.
  */
-int nvfp4_describe_plan(int kind /* 0 dense, 1 gate_up, 2 moe */, int M, int N, int K,
-                        int T, int top_k, char* buf, int buflen);
+int nvfp4_describe_plan(int kind, int M, int N, int K, int T, int top_k, char* buf, int buflen);
 
 /* Library version: major * 10000 + minor * 100 + patch. */
 int nvfp4_version(void);

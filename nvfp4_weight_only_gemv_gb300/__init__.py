@@ -256,8 +256,9 @@ def set_pdl(enable: bool) -> None:
 
 
 def describe_plan(kind: str, M: int, N: int, K: int, T: int = 0, top_k: int = 0) -> str:
-    """Launch the library would pick: kind in {"dense", "gate_up", "moe"}."""
-    code = {"dense": 0, "gate_up": 1, "moe": 2}[kind]
+    """Launch the library would pick: kind in {"dense", "gate_up", "moe", "moe_per_slot"}; for the
+    MoE kinds M is the number of experts (moe_per_slot: one x row per slot)."""
+    code = {"dense": 0, "gate_up": 1, "moe": 2, "moe_per_slot": 3}[kind]
     buf = ctypes.create_string_buffer(256)
     n = library().nvfp4_describe_plan(code, M, N, K, T, top_k, buf, 256)
     if n < 0:

@@ -1861,6 +1861,313 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_kernel(const __grid
     __syncwarp();
 }
 
+// Stream-K form of the warp-tile kernel, for launches with many tiles per CTA (all 8 warps
+// share one K range: the whole of K). The jobs (group, 16-row tile), group-major, are split
+// into balanced contiguous ranges of whole jobs per CTA; inside a CTA the jobs' TMA boxes are
+// split evenly over the 8 warps, so a warp's range may start or end inside a job. A warp that
+// covers a whole job stores it directly. A job split between warps leaves a partial record (at
+// most two per warp: its first and its last job; the first is held in registers) that the warp
+// writes into its own ring once all its copies are consumed. After one CTA barrier the warp
+// that holds a job's first box adds the records of the following warps in warp order and
+// stores the sum. Balance is one TMA box per warp instead of one item per CTA.
+template <int NC, bool MOE>
+__global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_sk_kernel(const __grid_constant__ TileParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    constexpr uint32_t kWBox = NC * 2048;
+    constexpr uint32_t kSBox = NC * 256;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int t = lane & 3;
+    const uint32_t raw_base = smem_addr(smem_raw);
+    const uint32_t base = (raw_base + 1023u) & ~1023u;
+    uint8_t* const sbase = smem_raw + (base - raw_base);
+    const int stages = p.stages, nbox = p.nbox, tiles = p.tiles;
+    uint64_t* const bars = reinterpret_cast<uint64_t*>(sbase + p.bar_off) + warp * tk::kMaxStages;
+    const uint32_t ring_w = base + p.ring_w + static_cast<uint32_t>(warp * stages) * kWBox;
+    const uint32_t ring_s = base + p.ring_s + static_cast<uint32_t>(warp * stages) * kSBox;
+    TileMoe* const tab = reinterpret_cast<TileMoe*>(sbase + p.moe_off);
+    // partial records of warp w: the first 1 KB of its own ring, free once its boxes are consumed
+    auto rec_of = [&](int w, int slot) -> float* {
+        return reinterpret_cast<float*>(sbase + p.ring_w + static_cast<uint32_t>(w * stages) * kWBox) + slot * 128;
+    };
+
+    if (lane == 0) {
+        for (int s = 0; s < stages; ++s) mbar_init(&bars[s], 1);
+        fence_barrier_init();
+    }
+    __syncwarp();
+
+    // this CTA's jobs [j0, j1) and this warp's boxes [bs, be) of them (box b: job j0 + b / nbox)
+    int j0 = 0, j1 = 0, bs = 0, be = 0;
+    auto set_ranges = [&](int jobs) {
+        const int q = jobs / static_cast<int>(gridDim.x), r = jobs - q * static_cast<int>(gridDim.x);
+        j0 = blockIdx.x * q + min(static_cast<int>(blockIdx.x), r);
+        j1 = j0 + q + (static_cast<int>(blockIdx.x) < r ? 1 : 0);
+        const int total = (j1 - j0) * nbox;
+        bs = (warp * total) >> 3;
+        be = ((warp + 1) * total) >> 3;
+    };
+    // issue cursor (lane 0)
+    int is_b = 0, is_box = 0, is_tile = 0, is_grp = 0;
+    uint32_t issued = 0, consumed = 0;
+    auto start_cursor = [&]() {
+        is_b = bs;
+        const int job = j0 + bs / nbox;
+        is_box = bs - (bs / nbox) * nbox;
+        is_grp = job / tiles;
+        is_tile = job - is_grp * tiles;
+    };
+    auto issue_next = [&]() {
+        if (is_b >= be) return;
+        const uint32_t st = issued % stages;
+        const uint32_t bar = smem_addr(&bars[st]);
+        mbar_arrive_expect_tx(&bars[st], kWBox + kSBox);
+        int row0 = is_tile * 16, map = is_grp;
+        if constexpr (MOE) {
+            row0 += tab->expert[is_grp] * p.N;
+            map = 0;
+        }
+        tma_load_3d(ring_w + st * kWBox, &p.wmap[map], 0, is_box * NC, row0, bar);
+        tma_load_3d(ring_s + st * kSBox, &p.smap[map], 0, is_box * NC, row0, bar);
+        ++issued;
+        ++is_b;
+        if (++is_box == nbox) {
+            is_box = 0;
+            if (++is_tile == tiles) {
+                is_tile = 0;
+                ++is_grp;
+            }
+        }
+    };
+    if constexpr (!MOE) {
+        set_ranges(p.items_q);  // dense: items_q holds the number of jobs
+        start_cursor();
+        if (lane == 0)
+            for (int s = 0; s < stages; ++s) issue_next();
+        if (warp == tk::kWarps - 1 && lane < p.M) {
+            const uint16_t* xr = p.x + static_cast<int64_t>(lane) * p.K;
+            prefetch_l2_bulk(xr, static_cast<uint32_t>(p.K) * 2u);
+            prefetch_l2(xr);
+        }
+    } else {
+        if (warp == tk::kWarps - 1 && lane == 0) prefetch_l2(p.ids);
+        const int xrows_all = p.x_per_slot ? p.slots : (p.slots + p.top_k - 1) / p.top_k;
+        if (warp == tk::kWarps - 2 && lane < xrows_all)
+            prefetch_l2_bulk(p.x + static_cast<int64_t>(lane) * p.K, static_cast<uint32_t>(p.K) * 2u);
+    }
+    pdl_launch_dependents();
+    pdl_wait();
+
+    int M = p.M;
+    const int* rowsel = nullptr;
+    if constexpr (MOE) {
+        if (warp == 0) tile_moe_groups(p, tab, lane);
+        __syncthreads();
+        set_ranges(tab->n_groups * tiles);
+        if (warp == 0 && j0 < j1) tile_moe_rows(p, tab, j0 / tiles, (j1 - 1) / tiles, lane);
+        start_cursor();
+        __syncthreads();
+        M = j0 < j1 ? tab->nrows : 0;
+        rowsel = tab->rows;
+    }
+
+    // x, all of K, staged by all eight warps
+    uint8_t* const xs = sbase + p.x_off;
+    float* const e2 = reinterpret_cast<float*>(sbase + p.misc_off);
+    uint32_t* const gmax = reinterpret_cast<uint32_t*>(sbase + p.misc_off + tk::kWarps * 32);
+    bool lossy = false;
+    float e2v = 1.f;
+    if (M > 0 && !stage_x_direct(p.x, rowsel, M, p.K, 0, p.K, xs, p.sstride, gmax + 16, warp, tk::kWarps, 2, lane,
+                                 [] {})) {
+        lossy = stage_x_slice(p.x, rowsel, M, p.K, 0, p.K, xs, p.sstride, e2, gmax, warp, tk::kWarps, 2, lane);
+        e2v = e2[0];
+    }
+    if constexpr (MOE) {
+        if (lane == 0)
+            for (int s = 0; s < stages; ++s) issue_next();
+    }
+    const bool use_f32 = lossy || p.force_f32;
+    if (use_f32 && M > 0 && warp == 0 && lane == 0) atomicAdd(&g_fp32_fallbacks, 1ull);
+
+    const int g = lane >> 2;
+    const int ra = tile_row_perm<NC>(g), rb = ra + 8;
+    const int m0 = 2 * t;
+    const float e2s = use_f32 ? 1.f : e2v;
+    const uint64_t budget = p.wait_ns;
+    bool dead = false;
+
+    auto ncols_of = [&](int grp) -> int {
+        if constexpr (MOE) return tab->count[grp];
+        else return p.M;
+    };
+    auto gscale_of = [&](int grp) -> float {
+        if constexpr (MOE) return __ldg(p.g_dev + tab->expert[grp]);
+        else return p.g[grp];
+    };
+    auto out_at = [&](int grp, int m, int row) -> int64_t {
+        if constexpr (MOE) return static_cast<int64_t>(tab->slot[grp][m]) * p.N + row;
+        else return m * p.ldy + static_cast<int64_t>(grp) * p.N + row;
+    };
+
+    // walk this warp's boxes
+    {
+        int job = j0 + bs / nbox, kb = bs - (bs / nbox) * nbox;
+        int grp = job / tiles, tile = job - grp * tiles;
+        const int first_job = job;
+        bool whole = kb == 0;  // this warp holds the current job's first box
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+        float dd[kTileChains][4];
+#pragma unroll
+        for (int c = 0; c < kTileChains; ++c)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) dd[c][i] = 0.f;
+        float first_rec[4] = {0.f, 0.f, 0.f, 0.f}, last_rec[4] = {0.f, 0.f, 0.f, 0.f};
+        float acc[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+        uint32_t xa = 0;
+        auto set_x = [&]() {
+            int col = min(g, max(M - 1, 0));
+            if constexpr (MOE) col = tab->col[grp][min(g, ncols_of(grp) - 1)];
+            xa = base + p.x_off + static_cast<uint32_t>(col) * p.sstride;
+        };
+        if (bs < be) set_x();
+        for (int b = bs; b < be; ++b) {
+            if (!dead) {
+                const uint32_t st = consumed % stages;
+                const uint32_t ph = (consumed / stages) & 1u;
+                if (!__all_sync(0xffffffffu, budget != 0 && mbar_wait(&bars[st], ph, budget))) {
+                    dead = true;
+                    raise_status(NVFP4_DEV_TIMEOUT, nullptr);
+                } else {
+                    if (!use_f32) {
+                        tile_slot_mma<NC>(ring_w + st * kWBox, ring_s + st * kSBox, xa, kb * NC * 2, ra, t, dd);
+                    } else {
+                        const int* xrow = nullptr;
+                        if constexpr (MOE) xrow = tab->xrow[grp];
+                        tile_slot_f32<NC>(ring_w + st * kWBox, ring_s + st * kSBox, p.x, xrow, p.K, ncols_of(grp),
+                                          kb * NC, ra, t, acc);
+                    }
+                    ++consumed;
+                    __syncwarp();
+                    if (lane == 0) issue_next();
+                }
+            }
+            if (kb == nbox - 1 || b == be - 1) {
+                // this warp's part of the job ends here
+                if (use_f32) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], 1);
+                        acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], 2);
+                    }
+#pragma unroll
+                    for (int m = 0; m < 8; ++m) {
+                        if (m == m0) { d[0] = acc[m]; d[2] = acc[8 + m]; }
+                        if (m == m0 + 1) { d[1] = acc[m]; d[3] = acc[8 + m]; }
+                    }
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+                } else {
+#pragma unroll
+                    for (int c = 0; c < kTileChains; ++c)
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            d[i] += dd[c][i];
+                            dd[c][i] = 0.f;
+                        }
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i) d[i] *= e2s;
+                const int ncols = ncols_of(grp);
+                if (whole && kb == nbox - 1) {
+                    const float gs = gscale_of(grp);
+                    const int rowa = tile * 16 + ra, rowb = tile * 16 + rb;
+                    if (m0 < ncols) {
+                        if (rowa < p.N) store_out(p.y, out_at(grp, m0, rowa), d[0] * gs, p.out_bf16);
+                        if (rowb < p.N) store_out(p.y, out_at(grp, m0, rowb), d[2] * gs, p.out_bf16);
+                    }
+                    if (m0 + 1 < ncols) {
+                        if (rowa < p.N) store_out(p.y, out_at(grp, m0 + 1, rowa), d[1] * gs, p.out_bf16);
+                        if (rowb < p.N) store_out(p.y, out_at(grp, m0 + 1, rowb), d[3] * gs, p.out_bf16);
+                    }
+                } else if (job == first_job) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) first_rec[i] = d[i];  // written once the ring is idle
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) last_rec[i] = d[i];
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i) d[i] = 0.f;
+                // next job
+                kb = 0;
+                whole = true;
+                ++job;
+                if (++tile == tiles) {
+                    tile = 0;
+                    ++grp;
+                }
+                if (b + 1 < be) set_x();
+            } else {
+                ++kb;
+            }
+        }
+        // the ring is idle once every issued copy has landed (only a timed-out warp has any left)
+        if (lane == 0) {
+            while (consumed < issued) {
+                const uint32_t st = consumed % stages;
+                mbar_wait(&bars[st], (consumed / stages) & 1u, kDrainWaitNs);
+                ++consumed;
+            }
+        }
+        __syncwarp();
+        float* r0 = rec_of(warp, 0);
+        float* r1 = rec_of(warp, 1);
+        r0[ra * 8 + m0] = first_rec[0];
+        r0[ra * 8 + m0 + 1] = first_rec[1];
+        r0[rb * 8 + m0] = first_rec[2];
+        r0[rb * 8 + m0 + 1] = first_rec[3];
+        r1[ra * 8 + m0] = last_rec[0];
+        r1[ra * 8 + m0 + 1] = last_rec[1];
+        r1[rb * 8 + m0] = last_rec[2];
+        r1[rb * 8 + m0 + 1] = last_rec[3];
+    }
+    named_bar_sync(1, tk::kThreads);
+    // jobs split between warps: the warp holding a job's first box adds the records in order
+    if (bs < be) {
+        const int jf = j0 + bs / nbox, jl = j0 + (be - 1) / nbox;
+        for (int s = 0; s < 2; ++s) {
+            const int j = s == 0 ? jf : jl;
+            if (s == 1 && jl == jf) break;
+            const int jb = (j - j0) * nbox, je = jb + nbox;  // the job's boxes in CTA units
+            if (jb < bs) continue;                          // starts in an earlier warp
+            if (jb >= bs && je <= be) continue;             // whole: stored already
+            const int grp = j / tiles, tile = j - (j / tiles) * tiles;
+            const int ncols = ncols_of(grp);
+            const float gs = gscale_of(grp);
+            for (int i = lane; i < 16 * ncols; i += 32) {
+                const int r = i / ncols, m = i - r * ncols;
+                float sum = rec_of(warp, s)[r * 8 + m];
+                for (int w = warp + 1; w < tk::kWarps; ++w) {
+                    const int wbs = (w * (j1 - j0) * nbox) >> 3, wbe = ((w + 1) * (j1 - j0) * nbox) >> 3;
+                    if (wbs >= je) break;
+                    if (wbe > wbs) sum += rec_of(w, 0)[r * 8 + m];  // the job is that warp's first one
+                }
+                const int row = tile * 16 + r;
+                if (row < p.N) store_out(p.y, out_at(grp, m, row), sum * gs, p.out_bf16);
+            }
+        }
+    }
+    if (lane == 0) {
+        while (consumed < issued) {
+            const uint32_t st = consumed % stages;
+            mbar_wait(&bars[st], (consumed / stages) & 1u, kDrainWaitNs);
+            ++consumed;
+        }
+    }
+    __syncwarp();
+}
+
 // ------------------------------------------------------------------ byte-load kernel
 
 struct SimpleParams {
@@ -2271,6 +2578,7 @@ struct TilePlan {
     int nc;
     int grid_x, grid_y;  // SM slots x CTAs per slot
     uint32_t smem;
+    bool sk;             // stream-K form (gemv_tile_sk_kernel)
 };
 
 // Tile-kernel plan for a dense (groups = 1) or gate/up (groups = 2) call; false when the
@@ -2369,7 +2677,9 @@ bool plan_tile(TilePlan& tp, int M, int N, int K, int groups, const DeviceInfo& 
                 const long long max_units = std::max<long long>(1, static_cast<long long>(d.sm_count) * per_sm / S);
                 const long long units = std::min(items, max_units);
                 const long long ipu = (items + units - 1) / units;
-                const double spw = 2.0 * nc * nbmax;
+                // (MoE, compared with the stream-K form: each box also costs about half a step of
+                // wait, re-issue and loop)
+                const double spw = 2.0 * nc * nbmax + (moe ? 0.5 * nbmax : 0.0);
                 // measured: a reduction over warps costs ~2 steps, one over a cluster ~10
                 const double ovh = (ksplit > 1 ? (moe ? 4.0 : 2.0) : 0.3) + (S > 1 ? 10.0 : 0.0);
                 const double lat = static_cast<double>(ipu) * (spw + ovh);
@@ -2397,7 +2707,87 @@ bool plan_tile(TilePlan& tp, int M, int N, int K, int groups, const DeviceInfo& 
                     tp.grid_x = static_cast<int>(units) * S;
                     tp.grid_y = 1;
                     tp.smem = smem;
+                    tp.sk = false;
                 }
+            }
+        }
+    }
+    // Stream-K form (MoE): whole K per CTA, jobs (group, tile) split evenly over the CTAs and
+    // boxes evenly over the warps. Many jobs per CTA make it balance far better than items.
+    if (moe && NVFP4_TILE_KSPLIT == 0 && NVFP4_TILE_S == 0) {
+        for (int nc = 2; nc >= 1; --nc) {
+            if (segs % nc || (NVFP4_TILE_NC && nc != NVFP4_TILE_NC)) continue;
+            const int nbox = segs / nc;
+            const long long jobs = static_cast<long long>(groups) * tiles;
+            if (jobs > (1LL << 30) || jobs * nbox > (1LL << 30)) continue;
+            const uint32_t sstride = static_cast<uint32_t>(K) * 2u + 64u;
+            const long long jobs_max = static_cast<long long>(std::max(moe_groups_max, groups)) * tiles;
+            const long long units_lo = std::min<long long>(d.sm_count, jobs);
+            const long long jpc_max = (jobs_max + units_lo - 1) / units_lo;
+            const int rows_cap = static_cast<int>(std::min<long long>(xrows, 8 * ((jpc_max + tiles - 1) / tiles + 1)));
+            const uint32_t x_bytes = align_up(static_cast<uint32_t>(rows_cap) * sstride, 128);
+            int stages = 0, per_sm = 0;
+            uint32_t smem = 0;
+            TileParams lp{};
+            for (int want = 2; want >= 1 && !stages; --want) {
+                for (int st = tk::kMaxStages; st >= 2; --st) {
+                    TileParams q{};
+                    uint32_t off = 0;
+                    q.ring_w = off;
+                    off += static_cast<uint32_t>(tk::kWarps * st * nc) * 2048u;
+                    q.ring_s = off;
+                    off += static_cast<uint32_t>(tk::kWarps * st * nc) * 256u;
+                    q.x_off = off;
+                    off += x_bytes;
+                    q.red_off = off;  // unused: partial records live in the drained rings
+                    q.cpart_off = off;
+                    q.misc_off = off;
+                    off += align_up(tk::kWarps * 32 + tk::kWarps * 32 * 4, 128);
+                    q.bar_off = off;
+                    off += tk::kWarps * tk::kMaxStages * 8;
+                    q.moe_off = align_up(off, 16);
+                    off = q.moe_off + static_cast<uint32_t>(sizeof(TileMoe));
+                    const uint32_t total = off + 1024;
+                    const uint32_t limit = want == 2 ? static_cast<uint32_t>(d.smem_per_sm / 2 - 1024)
+                                                     : static_cast<uint32_t>(d.smem_optin);
+                    if (total <= limit) {
+                        stages = st;
+                        per_sm = want;
+                        smem = total;
+                        lp = q;
+                        break;
+                    }
+                }
+            }
+            if (!stages) continue;
+            const long long units = std::min<long long>(jobs, static_cast<long long>(d.sm_count) * per_sm);
+            const long long jpc = (jobs + units - 1) / units;
+            const double boxes_per_warp = static_cast<double>((jpc * nbox + tk::kWarps - 1) / tk::kWarps);
+            const double lat = boxes_per_warp * (2.0 * nc + 0.5) + 2.0;
+            const double thr = static_cast<double>(jobs) * nbox * (2.0 * nc + 0.5) / (d.sm_count * 16.0) * 1.1 + 2.0;
+            const double cost = std::max(lat, thr) + static_cast<double>(std::min(rows_cap, 8)) * K / 2048.0;
+            if (!found || cost < best - 1e-9) {
+                found = true;
+                best = cost;
+                tp.p = lp;
+                tp.p.M = rows_cap;
+                tp.p.N = N;
+                tp.p.K = K;
+                tp.p.tiles = tiles;
+                tp.p.ksplit_log2 = 0;
+                tp.p.s_log2 = 0;
+                tp.p.tpi = tk::kWarps;
+                tp.p.ipg = tiles;
+                tp.p.items_q = static_cast<int>(jobs);
+                tp.p.items_r = 0;
+                tp.p.nbox = nbox;
+                tp.p.stages = stages;
+                tp.p.sstride = sstride;
+                tp.nc = nc;
+                tp.grid_x = static_cast<int>(units);
+                tp.grid_y = 1;
+                tp.smem = smem;
+                tp.sk = true;
             }
         }
     }
@@ -2432,9 +2822,12 @@ bool encode_tile_maps(CUtensorMap* wmap, CUtensorMap* smap, const uint8_t* w, co
     return true;
 }
 
-template <int NC, bool MOE>
+template <int NC, bool MOE, bool SK>
 cudaError_t launch_tile_nc(const TilePlan& tp, cudaStream_t st) {
-    auto kern = gemv_tile_kernel<NC, MOE>;
+    auto kern = [] {
+        if constexpr (SK) return gemv_tile_sk_kernel<NC, MOE>;
+        else return gemv_tile_kernel<NC, MOE>;
+    }();
     static bool done[64] = {};
     cudaError_t e = allow_max_smem(kern, done);
     if (e != cudaSuccess) return e;
@@ -2463,8 +2856,9 @@ cudaError_t launch_tile_nc(const TilePlan& tp, cudaStream_t st) {
 }
 
 cudaError_t launch_tile(const TilePlan& tp, cudaStream_t st, bool moe) {
-    if (moe) return tp.nc == 2 ? launch_tile_nc<2, true>(tp, st) : launch_tile_nc<1, true>(tp, st);
-    return tp.nc == 2 ? launch_tile_nc<2, false>(tp, st) : launch_tile_nc<1, false>(tp, st);
+    if (moe && tp.sk) return tp.nc == 2 ? launch_tile_nc<2, true, true>(tp, st) : launch_tile_nc<1, true, true>(tp, st);
+    if (moe) return tp.nc == 2 ? launch_tile_nc<2, true, false>(tp, st) : launch_tile_nc<1, true, false>(tp, st);
+    return tp.nc == 2 ? launch_tile_nc<2, false, false>(tp, st) : launch_tile_nc<1, false, false>(tp, st);
 }
 
 cudaError_t launch_simple(const SimpleParams& sp, int64_t cols, cudaStream_t st) {
@@ -2738,22 +3132,24 @@ int nvfp4_describe_plan(int kind, int M, int N, int K, int T, int top_k, char* b
         }
         ok = plan_dense(pl, M, N, K, kind == 0 ? 1 : 2, *d, w, w, fake);
     }
-    if (kind == 2) {
+    if (kind == 2 || kind == 3) {
+        // MoE: M is the number of experts E; kind 3 has one x row per slot
         TilePlan tpl{};
-        const int slots = T * top_k;
-        if (slots <= kTileMoeSlots &&
-            plan_tile(tpl, 8, N, K, expected_groups(288, T, top_k), *d, w, w, fake, true, slots, slots)) {
+        const int slots = T * top_k, E = M;
+        const int xrows = kind == 3 ? slots : T;
+        if (slots <= kTileMoeSlots && E >= 1 && static_cast<int64_t>(E) * N <= (1 << 30) &&
+            plan_tile(tpl, 8, N, K, expected_groups(E, T, top_k), *d, w, w, fake, true, xrows, slots)) {
             return snprintf(buf, buflen,
-                            "tile_moe grid=%d block=%d smem=%u split=1 rows_per_item=%d k_warps=%d mt=8 stages=%d nc=%d",
-                            tpl.grid_x, tk::kThreads, tpl.smem, tpl.p.tpi * 16, 1 << tpl.p.ksplit_log2, tpl.p.stages,
+                            "%s grid=%d block=%d smem=%u split=1 rows_per_item=%d k_warps=%d mt=8 stages=%d nc=%d",
+                            tpl.sk ? "tile_sk_moe" : "tile_moe", tpl.grid_x, tk::kThreads, tpl.smem, tpl.p.tpi * 16, 1 << tpl.p.ksplit_log2, tpl.p.stages,
                             tpl.nc);
         }
-        ok = plan_moe(pl, 288, T, top_k, N, K, *d, fake, fake, fake);
+        ok = plan_moe(pl, E, T, top_k, N, K, *d, fake, fake, fake);
     }
     int n;
     if (!ok) {
         n = snprintf(buf, buflen, "simple grid=%lld block=%d smem=0 split=1 rows_per_item=0 k_warps=0",
-                     static_cast<long long>(((kind == 2 ? static_cast<int64_t>(T) * top_k : (kind == 1 ? 2 : 1)) * N + 7) / 8),
+                     static_cast<long long>(((kind >= 2 ? static_cast<int64_t>(T) * top_k : (kind == 1 ? 2 : 1)) * N + 7) / 8),
                      kSimpleThreads);
     } else {
         n = snprintf(buf, buflen, "%s grid=%d block=%d smem=%u split=%d rows_per_item=%d k_warps=%d mt=%d stages=%d",

@@ -363,8 +363,21 @@ def test_moe_tile_groups_32_slots(x_per_slot):
     E, N, K, T, top_k = 12, 200, 1024, 4, 8
     p = synth.moe_problem(E, N, K, T, top_k, x_per_slot, seed=315, fill="all")
     ids = [5] * 20 + [0, 1, 2, 3, 4, 6, 7, 8, 9, 10, 11, 1]
-    assert nv.describe_plan("moe", 8, N, K, T, top_k).startswith("tile_moe ")
+    assert nv.describe_plan("moe_per_slot" if x_per_slot else "moe", E, N, K, T, top_k).split()[0] in (
+        "tile_moe", "tile_sk_moe")
     st, bad = _moe_check(p, ids, x_per_slot, top_k, torch.bfloat16)
+    assert st == 0 and bad == 0
+
+
+@pytest.mark.parametrize("x_per_slot,N,K,E,T,top_k", [(False, 3072, 4096, 288, 4, 8), (True, 4096, 1536, 288, 4, 8),
+                                                       (True, 200, 1024, 7, 5, 3), (False, 512, 1024, 40, 2, 6)])
+def test_moe_stream_k(x_per_slot, N, K, E, T, top_k):
+    # the stream-K MoE form: jobs (expert group, tile) spread evenly over the CTAs and TMA boxes
+    # over the warps, with tiles that straddle warps combined through shared memory
+    assert nv.describe_plan("moe_per_slot" if x_per_slot else "moe", E, N, K, T, top_k).split()[0] == "tile_sk_moe"
+    # only the routed experts are filled (the rest stay zero): generated on the device
+    p = synth.moe_problem(E, N, K, T, top_k, x_per_slot, seed=316 + N, device=DEV)
+    st, bad = _moe_check(p, p["ids"].tolist(), x_per_slot, top_k, torch.bfloat16)
     assert st == 0 and bad == 0
 
 
