@@ -1861,6 +1861,10 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_kernel(const __grid
     __syncwarp();
 }
 
+#ifndef NVFP4_MOE_EARLY
+#define NVFP4_MOE_EARLY 1  // weight slots a MoE warp requests before x staging (the rest after it)
+#endif
+
 // Stream-K form of the warp-tile kernel, for launches with many tiles per CTA (all 8 warps
 // share one K range: the whole of K). The jobs (group, 16-row tile), group-major, are split
 // into balanced contiguous ranges of whole jobs per CTA; inside a CTA the jobs' TMA boxes are
@@ -1968,6 +1972,8 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_sk_kernel(const __g
         __syncthreads();
         M = j0 < j1 ? tab->nrows : 0;
         rowsel = tab->rows;
+        if (lane == 0)
+            for (int s = 0; s < NVFP4_MOE_EARLY; ++s) issue_next();
     }
 
     // x, all of K, staged by all eight warps
@@ -1983,7 +1989,7 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_sk_kernel(const __g
     }
     if constexpr (MOE) {
         if (lane == 0)
-            for (int s = 0; s < stages; ++s) issue_next();
+            for (int s = NVFP4_MOE_EARLY; s < stages; ++s) issue_next();
     }
     const bool use_f32 = lossy || p.force_f32;
     if (use_f32 && M > 0 && warp == 0 && lane == 0) atomicAdd(&g_fp32_fallbacks, 1ull);
