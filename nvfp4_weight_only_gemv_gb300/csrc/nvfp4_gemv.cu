@@ -15,6 +15,10 @@
 //     mma.sync.m16n8k16 with the weights decoded exactly to f16 (E2M1 * E4M3) and x staged in
 //     f16 per K slice. K may be split over warps (shared-memory reduction) or over a cluster
 //     (DSMEM reduction), both in a fixed order. See the comment above the kernel.
+//   * gemv_tile_sk_kernel (MoE launches with many tiles per CTA): the same warp rings and
+//     decode in a stream-K form. Whole (expert group, tile) jobs are spread evenly over the
+//     CTAs and their TMA boxes evenly over each CTA's warps; a job cut between warps is
+//     summed in a fixed warp order.
 //   * gemv_stream_kernel (K % 32 == 0 otherwise, or up to 256 MoE slots): a producer warp
 //     bulk-copies whole items of rows into a ring, consumer warps decode with the same MMA
 //     scheme and an epilogue warp reduces in a fixed order.
