@@ -1620,6 +1620,15 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_kernel(const __grid
     TileItemWalk iw = first;
     int iss_left = 0, iss_box = 0;
     uint32_t issued = 0, consumed = 0;
+    // ring positions kept incrementally (the ring depth is a launch parameter: no divisions)
+    uint32_t iss_st = 0, cons_st = 0, cons_ph = 0;
+    auto cons_advance = [&]() {
+        ++consumed;
+        if (++cons_st == static_cast<uint32_t>(stages)) {
+            cons_st = 0;
+            cons_ph ^= 1u;
+        }
+    };
     auto issue_next = [&]() {
         while (iss_left > 0 && (iss_box >= nb || iw.t * p.tpi + tin >= p.tiles)) {
             iw.next(p.ipg);
@@ -1627,7 +1636,8 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_kernel(const __grid
             iss_box = 0;
         }
         if (iss_left <= 0) return;
-        const uint32_t st = issued % stages;
+        const uint32_t st = iss_st;
+        if (++iss_st == static_cast<uint32_t>(stages)) iss_st = 0;
         const uint32_t bar = smem_addr(&bars[st]);
         mbar_arrive_expect_tx(&bars[st], kWBox + kSBox);
         const int seg = (b_lo + iss_box) * NC;
@@ -1742,8 +1752,8 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_kernel(const __grid
                 for (int i = 0; i < 16; ++i) acc[i] = 0.f;
             }
             for (int b = 0; b < nb; ++b) {
-                const uint32_t st = consumed % stages;
-                const uint32_t ph = (consumed / stages) & 1u;
+                const uint32_t st = cons_st;
+                const uint32_t ph = cons_ph;
                 // a zero budget takes the timeout path deterministically (copies issued before
                 // x staging have usually landed by now, so one poll would succeed)
                 if (!__all_sync(0xffffffffu, budget != 0 && mbar_wait(&bars[st], ph, budget))) {
@@ -1756,7 +1766,7 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_kernel(const __grid
                     tile_slot_f32<NC>(ring_w + st * kWBox, ring_s + st * kSBox, p.x, xrow, p.K, ncols,
                                       (b_lo + b) * NC, ra, t, acc);
                 }
-                ++consumed;
+                cons_advance();
                 __syncwarp();
                 if (lane == 0) issue_next();
             }
@@ -1857,9 +1867,8 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_kernel(const __grid
     // copies still in flight (only after a timeout) must land before the CTA exits
     if (lane == 0) {
         while (consumed < issued) {
-            const uint32_t st = consumed % stages;
-            mbar_wait(&bars[st], (consumed / stages) & 1u, kDrainWaitNs);
-            ++consumed;
+            mbar_wait(&bars[cons_st], cons_ph, kDrainWaitNs);
+            cons_advance();
         }
     }
     __syncwarp();
@@ -1917,6 +1926,15 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_sk_kernel(const __g
     // issue cursor (lane 0)
     int is_b = 0, is_box = 0, is_tile = 0, is_grp = 0;
     uint32_t issued = 0, consumed = 0;
+    // ring positions kept incrementally (the ring depth is a launch parameter: no divisions)
+    uint32_t iss_st = 0, cons_st = 0, cons_ph = 0;
+    auto cons_advance = [&]() {
+        ++consumed;
+        if (++cons_st == static_cast<uint32_t>(stages)) {
+            cons_st = 0;
+            cons_ph ^= 1u;
+        }
+    };
     auto start_cursor = [&]() {
         is_b = bs;
         const int job = j0 + bs / nbox;
@@ -1926,7 +1944,8 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_sk_kernel(const __g
     };
     auto issue_next = [&]() {
         if (is_b >= be) return;
-        const uint32_t st = issued % stages;
+        const uint32_t st = iss_st;
+        if (++iss_st == static_cast<uint32_t>(stages)) iss_st = 0;
         const uint32_t bar = smem_addr(&bars[st]);
         mbar_arrive_expect_tx(&bars[st], kWBox + kSBox);
         int row0 = is_tile * 16, map = is_grp;
@@ -2031,6 +2050,15 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_sk_kernel(const __g
 #pragma unroll
             for (int i = 0; i < 4; ++i) dd[c][i] = 0.f;
         float first_rec[4] = {0.f, 0.f, 0.f, 0.f}, last_rec[4] = {0.f, 0.f, 0.f, 0.f};
+        // global scales of the groups of this warp's first and last jobs, requested now so that
+        // the load is not waited for at a job's end (other groups load theirs there)
+        int gs_grp0 = grp, gs_grp1 = grp;
+        float gs0 = 1.f, gs1 = 1.f;
+        if (bs < be) {
+            gs_grp1 = (j0 + (be - 1) / nbox) / tiles;
+            gs0 = gscale_of(gs_grp0);
+            gs1 = gscale_of(gs_grp1);
+        }
         float acc[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) acc[i] = 0.f;
@@ -2043,8 +2071,8 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_sk_kernel(const __g
         if (bs < be) set_x();
         for (int b = bs; b < be; ++b) {
             if (!dead) {
-                const uint32_t st = consumed % stages;
-                const uint32_t ph = (consumed / stages) & 1u;
+                const uint32_t st = cons_st;
+                const uint32_t ph = cons_ph;
                 if (!__all_sync(0xffffffffu, budget != 0 && mbar_wait(&bars[st], ph, budget))) {
                     dead = true;
                     raise_status(NVFP4_DEV_TIMEOUT, nullptr);
@@ -2057,7 +2085,7 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_sk_kernel(const __g
                         tile_slot_f32<NC>(ring_w + st * kWBox, ring_s + st * kSBox, p.x, xrow, p.K, ncols_of(grp),
                                           kb * NC, ra, t, acc);
                     }
-                    ++consumed;
+                    cons_advance();
                     __syncwarp();
                     if (lane == 0) issue_next();
                 }
@@ -2090,7 +2118,7 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_sk_kernel(const __g
                 for (int i = 0; i < 4; ++i) d[i] *= e2s;
                 const int ncols = ncols_of(grp);
                 if (whole && kb == nbox - 1) {
-                    const float gs = gscale_of(grp);
+                    const float gs = grp == gs_grp0 ? gs0 : (grp == gs_grp1 ? gs1 : gscale_of(grp));
                     const int rowa = tile * 16 + ra, rowb = tile * 16 + rb;
                     if (m0 < ncols) {
                         if (rowa < p.N) store_out(p.y, out_at(grp, m0, rowa), d[0] * gs, p.out_bf16);
@@ -2125,9 +2153,8 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_sk_kernel(const __g
         // the ring is idle once every issued copy has landed (only a timed-out warp has any left)
         if (lane == 0) {
             while (consumed < issued) {
-                const uint32_t st = consumed % stages;
-                mbar_wait(&bars[st], (consumed / stages) & 1u, kDrainWaitNs);
-                ++consumed;
+                mbar_wait(&bars[cons_st], cons_ph, kDrainWaitNs);
+                cons_advance();
             }
         }
         __syncwarp();
@@ -2170,9 +2197,8 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_sk_kernel(const __g
     }
     if (lane == 0) {
         while (consumed < issued) {
-            const uint32_t st = consumed % stages;
-            mbar_wait(&bars[st], (consumed / stages) & 1u, kDrainWaitNs);
-            ++consumed;
+            mbar_wait(&bars[cons_st], cons_ph, kDrainWaitNs);
+            cons_advance();
         }
     }
     __syncwarp();
