@@ -1287,7 +1287,9 @@ __device__ bool stage_x_direct(const uint16_t* __restrict__ x, const int* rowsel
             ++m;
         }
     };
-    {
+    // batches of kPre loads in flight, so a lane's chunks cost one L2 round trip per batch
+    bool first = true;
+    do {
         uint4 v[kPre];
         int mi[kPre], ci[kPre];
 #pragma unroll
@@ -1298,12 +1300,12 @@ __device__ bool stage_x_direct(const uint16_t* __restrict__ x, const int* rowsel
                          : make_uint4(0u, 0u, 0u, 0u);
             advance();
         }
-        after_issue();  // the caller's own requests queue behind these loads, not in front
+        if (first) after_issue();  // the caller's own requests queue behind these loads, not in front
+        first = false;
 #pragma unroll
         for (int i = 0; i < kPre; ++i)
             if (mi[i] < M) convert(v[i], mi[i], ci[i]);
-    }
-    for (; m < M; advance()) convert(ldg128(x + static_cast<int64_t>(rowsel ? rowsel[m] : m) * K + k0 + c * 8), m, c);
+    } while (m < M);
     bool ok = !__any_sync(0xffffffffu, bad != 0u);
     if (bar_id >= 0) {
         if (lane == 0) vote[gi] = ok ? 1u : 0u;
@@ -1322,8 +1324,8 @@ __device__ bool stage_x_direct(const uint16_t* __restrict__ x, const int* rowsel
 // a slice holding a smaller nonzero value, Inf or NaN is reported lossy
 // and its warps compute in fp32 instead. Because each slice's partial sums are multiplied by
 // its own e2 before slices are added, slices need no common scale and no CTA-wide step.
-// The slice's rows are walked as one flat sequence of 16-byte chunks; the first kPre of each
-// lane are loaded at once and kept in registers for the conversion. Returns (uniform over
+// The slice's rows are walked as one flat sequence of 16-byte chunks, loaded kPre at a time
+// per lane; the first kPre are kept in registers for the conversion. Returns (uniform over
 // the slice's warps) the lossy flag. bar_id < 0: a single warp (no named barrier).
 __device__ bool stage_x_slice(const uint16_t* __restrict__ x, const int* rowsel, int M, int K, int k0, int kn,
                               uint8_t* xs, uint32_t sstride, float* e2, uint32_t* gmax, int gi, int gw, int bar_id,
@@ -1365,7 +1367,17 @@ __device__ bool stage_x_slice(const uint16_t* __restrict__ x, const int* rowsel,
         }
 #pragma unroll
         for (int i = 0; i < kPre; ++i) scan(v[i]);  // zero padding does not move max or min-nonzero
-        for (; m < M; advance(m, c)) scan(ldg128(x + static_cast<int64_t>(rowsel ? rowsel[m] : m) * K + k0 + c * 8));
+        while (m < M) {  // the rest in batches of kPre loads in flight
+            uint4 u[kPre];
+#pragma unroll
+            for (int i = 0; i < kPre; ++i) {
+                u[i] = m < M ? ldg128(x + static_cast<int64_t>(rowsel ? rowsel[m] : m) * K + k0 + c * 8)
+                             : make_uint4(0u, 0u, 0u, 0u);
+                advance(m, c);
+            }
+#pragma unroll
+            for (int i = 0; i < kPre; ++i) scan(u[i]);
+        }
     }
     uint32_t a = max(mx & 0xffffu, mx >> 16), z = min(mn & 0xffffu, mn >> 16);
 #pragma unroll
@@ -1420,8 +1432,21 @@ __device__ bool stage_x_slice(const uint16_t* __restrict__ x, const int* rowsel,
             if (m < M) store(v[i], m, c);
             advance(m, c);
         }
-        for (; m < M; advance(m, c))
-            store(ldg128(x + static_cast<int64_t>(rowsel ? rowsel[m] : m) * K + k0 + c * 8), m, c);
+        while (m < M) {
+            uint4 u[kPre];
+            int mi[kPre], ci[kPre];
+#pragma unroll
+            for (int i = 0; i < kPre; ++i) {
+                mi[i] = m;
+                ci[i] = c;
+                u[i] = m < M ? ldg128(x + static_cast<int64_t>(rowsel ? rowsel[m] : m) * K + k0 + c * 8)
+                             : make_uint4(0u, 0u, 0u, 0u);
+                advance(m, c);
+            }
+#pragma unroll
+            for (int i = 0; i < kPre; ++i)
+                if (mi[i] < M) store(u[i], mi[i], ci[i]);
+        }
     }
     if (bar_id >= 0) named_bar_sync(bar_id, gw * 32);
     else __syncwarp();
@@ -2582,6 +2607,9 @@ cudaError_t dispatch_stream(const Plan& pl, cudaStream_t st) {
 #ifndef NVFP4_TILE_S
 #define NVFP4_TILE_S 0
 #endif
+#ifndef NVFP4_TILE_PER_SM
+#define NVFP4_TILE_PER_SM 0  // nonzero: dense launches use at most this many CTAs per SM
+#endif
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -2710,7 +2738,8 @@ bool plan_tile(TilePlan& tp, int M, int N, int K, int groups, const DeviceInfo& 
                 // items one unit runs in sequence, each with its steps, reductions and barriers)
                 // and a throughput term (all warp steps spread over the SMs at 16 warps each),
                 // plus the staging of x, which shrinks with the K range of one CTA.
-                const long long max_units = std::max<long long>(1, static_cast<long long>(d.sm_count) * per_sm / S);
+                const int per_sm_cap = (NVFP4_TILE_PER_SM && !moe) ? std::min(per_sm, NVFP4_TILE_PER_SM) : per_sm;
+                const long long max_units = std::max<long long>(1, static_cast<long long>(d.sm_count) * per_sm_cap / S);
                 const long long units = std::min(items, max_units);
                 const long long ipu = (items + units - 1) / units;
                 // (MoE, compared with the stream-K form: each box also costs about half a step of
