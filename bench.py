@@ -40,6 +40,8 @@ NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 
 # (kind, N, K, M, seed, out)   kind: dense | gate_up (N per half) | moe_gate_up | moe_down
+SWIGLU_CLAMP = 10.0  # the pages name a clamp in the fused activation but give no limit
+
 WORKLOADS = {
     "attn": ("attention projections N=4096,K=4096 and N=1024,K=4096 at M=1 and M=5, bf16 out",
              [("dense", 4096, 4096, 1, 1, "bf16"), ("dense", 1024, 4096, 1, 3, "bf16"),
@@ -52,6 +54,9 @@ WORKLOADS = {
                [("gate_up", 12288, 4096, 4, 5, "f32"), ("dense", 4096, 12288, 4, 6, "f32")]),
     "ffn_m8": ("FFN gate+up then down at M=8, fp32 out",
                [("gate_up", 12288, 4096, 8, 5, "f32"), ("dense", 4096, 12288, 8, 6, "f32")]),
+    "ffn_swiglu": ("FFN gate+up N=2x12288,K=4096 with the fused SwiGLU (clamp 10, bf16 [1, 12288] out) "
+                   "then down N=4096,K=12288 at M=1, fp32 out",
+                   [("gate_up_swiglu", 12288, 4096, 1, 5, "bf16"), ("dense", 4096, 12288, 1, 6, "f32")]),
     "vocab": ("vocab head N=151936,K=4096,M=1, fp32 out", [("dense", 151936, 4096, 1, 7, "f32")]),
     "moe": ("routed experts: 288 experts, gate_up [3072,4096] then down [4096,1536], "
             "4 tokens x top-8, fp32 per-slot out",
@@ -95,14 +100,14 @@ def kernels_of(calls):
     """Names of the library kernels the step's calls launch (from the library's own plan)."""
     import nvfp4_weight_only_gemv_gb300 as nv
     names = {"tile": "gemv_tile_kernel", "tile_moe": "gemv_tile_kernel (MoE)", "stream": "gemv_stream_kernel",
-             "tile_sk_moe": "gemv_tile_sk_kernel (MoE)", "stream_moe": "gemv_stream_kernel (MoE)",
+             "tile_sk_moe": "gemv_tile_sk_kernel (MoE)", "tile_swiglu": "gemv_tile_kernel (gate/up + SwiGLU)", "stream_moe": "gemv_stream_kernel (MoE)",
              "simple": "gemv_simple_kernel"}
     seen = []
     for c in calls:
         if c.kind.startswith("moe"):
             desc = nv.describe_plan("moe_per_slot" if c.x_per_slot else "moe", c.E, c.N, c.K, c.T, c.top_k)
         else:
-            desc = nv.describe_plan("gate_up" if c.kind == "gate_up" else "dense", c.M, c.N, c.K)
+            desc = nv.describe_plan(c.kind if c.kind in ("gate_up", "gate_up_swiglu") else "dense", c.M, c.N, c.K)
         name = names.get(desc.split()[0], desc.split()[0])
         if name not in seen:
             seen.append(name)
@@ -193,11 +198,11 @@ class Call:
             base = {"w": p["w"], "s": p["s"], "g": p["g"], "x": p["x"]}
             self.rows = self.N
             self.y_shape = (self.M, self.N)
-        elif self.kind == "gate_up":
+        elif self.kind in ("gate_up", "gate_up_swiglu"):
             p = synth.gate_up_problem(self.N, self.K, self.M, self.seed, device=gen_device)
             base = p
             self.rows = 2 * self.N
-            self.y_shape = (self.M, 2 * self.N)
+            self.y_shape = (self.M, self.N if self.kind == "gate_up_swiglu" else 2 * self.N)
         else:
             self.T, self.top_k, self.E = self.M, 8, 288
             self.x_per_slot = self.kind == "moe_down"
@@ -233,7 +238,7 @@ class Call:
 
     def weight_bytes(self, c=0):
         per_row = self.K * 0.5 + self.K / 16
-        if self.kind == "gate_up":
+        if self.kind in ("gate_up", "gate_up_swiglu"):
             return 2 * self.N * per_row
         if self.kind.startswith("moe"):
             return self.unique_experts(c) * self.N * per_row
@@ -245,8 +250,7 @@ class Call:
             slots = self.T * self.top_k
             xrows = slots if self.x_per_slot else self.T
             return self.weight_bytes(c) + xrows * self.K * 2 + slots * self.N * self.out_bytes
-        rows = self.rows
-        return self.weight_bytes(c) + self.M * self.K * 2 + self.M * rows * self.out_bytes
+        return self.weight_bytes(c) + self.M * self.K * 2 + self.M * self.y_shape[1] * self.out_bytes
 
     def x_bytes(self):
         return self.sets[0]["x"].numel() * 2
@@ -264,14 +268,17 @@ class Call:
             nv.gemv(d["w"], d["s"], d["g"], x, out=y)
         elif self.kind == "gate_up":
             nv.gemv_gate_up(d["wg"], d["sg"], d["gg"], d["wu"], d["su"], d["gu"], x, out=y)
+        elif self.kind == "gate_up_swiglu":
+            nv.gemv_gate_up_swiglu(d["wg"], d["sg"], d["gg"], d["wu"], d["su"], d["gu"], x, SWIGLU_CLAMP, out=y)
         else:
             nv.moe_gemv(d["w"], d["s"], d["gs"], d["ids"], x, self.x_per_slot, self.top_k, out=y)
         return y
 
     # oracle ------------------------------------------------------------
     def oracle_rows(self, frac, rng):
-        n = max(1, int(round(self.rows * frac)))
-        return np.sort(rng.choice(self.rows, size=min(n, self.rows), replace=False)).astype(np.int64)
+        cols = self.y_shape[1] if self.kind == "gate_up_swiglu" else self.rows  # output columns
+        n = max(1, int(round(cols * frac)))
+        return np.sort(rng.choice(cols, size=min(n, cols), replace=False)).astype(np.int64)
 
     def run_oracle(self, rows):
         import oracle
@@ -284,6 +291,10 @@ class Call:
             oracle.gemv_gate_up(h["wg"].numpy(), h["sg"].numpy(), h["gg"], h["wu"].numpy(), h["su"].numpy(),
                                 h["gu"], synth.bf16_bits(h["x"]), rows=rows)
             return len(rows) * (self.K * 0.5 + self.K / 16)
+        if self.kind == "gate_up_swiglu":
+            oracle.gate_up_swiglu(h["wg"].numpy(), h["sg"].numpy(), h["gg"], h["wu"].numpy(), h["su"].numpy(),
+                                  h["gu"], synth.bf16_bits(h["x"]), SWIGLU_CLAMP, rows=rows)
+            return 2 * len(rows) * (self.K * 0.5 + self.K / 16)  # a gate and an up row per output
         ids = self.sets[0]["ids"].cpu().numpy()
         oracle.moe_gemv(h["w"].numpy(), h["s"].numpy(), h["gs"].numpy(), ids, synth.bf16_bits(h["x"]),
                         self.x_per_slot, self.top_k, rows=rows)
@@ -296,7 +307,7 @@ def pool_copies(calls_spec, device):
     l2 = getattr(props, "L2_cache_size", 128 << 20) or (128 << 20)
     per_step = 0
     for kind, N, K, M, *_ in calls_spec:
-        rows = 2 * N if kind == "gate_up" else N
+        rows = 2 * N if kind in ("gate_up", "gate_up_swiglu") else N
         if kind.startswith("moe"):
             return 4, l2, "routing rotates over 4 id sets; each step reads ~31 distinct experts (>2x L2)"
         per_step += rows * K * 9 // 16

@@ -96,6 +96,23 @@ nvfp4_status nvfp4_gemv_gate_up(const uint8_t* w_gate, const uint8_t* s_gate, fl
                                 int M, int N, int K, void* stream);
 
 /*
+ * Gate and up projections with the activation fused into the epilogue (the swiglu_clamp
+ * and silu_mul nodes that follow the gate/up projection in "glm-5.3-flash-nvfp4-tp3-512k--gb10
+ * graph.json", block l0.mlp, both "compute f32"; the shared expert's fused group of the same
+ * graph). With gate and up as nvfp4_gemv_gate_up computes them (fp32),
+ *     c(v)    = min(max(v, -clamp_limit), clamp_limit)   (NaN stays NaN)
+ *     y[m, n] = silu(c(gate[m, n])) * c(up[m, n]),   silu(v) = v / (1 + exp(-v)),
+ * evaluated in fp32 and stored as y_type. y is [M, N]: the [M, 2N] gate|up product is never
+ * written. clamp_limit must be > 0; +INFINITY means no clamp. The pages name the clamp but
+ * give no limit, so the limit is the caller's. Returns NVFP4_ERR_SHAPE for clamp_limit <= 0
+ * or NaN. Other arguments, errors and layouts as nvfp4_gemv_gate_up.
+ */
+nvfp4_status nvfp4_gemv_gate_up_swiglu(const uint8_t* w_gate, const uint8_t* s_gate, float g_gate,
+                                       const uint8_t* w_up, const uint8_t* s_up, float g_up,
+                                       const uint16_t* x, float clamp_limit, void* y, nvfp4_out_t y_type,
+                                       int M, int N, int K, void* stream);
+
+/*
  * Routed-expert GEMV over slots (w4a16_gemv_sw_moe, "glm-5.3-flash-nvfp4-tp3-512k--gb10
  * card.json" performance[33]: routed gate or up, 8 slots). For slot s = t*top_k + j
  * (token-major), with e = expert_ids[s]:
@@ -169,7 +186,8 @@ void nvfp4_set_pdl(int enable);
  * Describes the launch the next call with these arguments would make. It writes
  * "kernel grid block smem split rows_per_item k_warps ..." into buf (host memory,
  * NUL-terminated). kind: 0 dense, 1 gate_up, 2 MoE with x shared by a token's slots,
- * 3 MoE with one x row per slot; for the MoE kinds M is the number of experts E.
+ * 3 MoE with one x row per slot, 4 gate_up with the fused activation; for the MoE kinds
+ * M is the number of experts E.
  * Pointers are assumed 256-byte aligned. Returns the number of characters, or -1.
  */
 int nvfp4_describe_plan(int kind, int M, int N, int K, int T, int top_k, char* buf, int buflen);

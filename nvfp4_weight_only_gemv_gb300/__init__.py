@@ -21,7 +21,7 @@ import torch
 
 from . import build as _build
 
-__all__ = ["gemv", "gemv_gate_up", "moe_gemv", "device_status", "set_wait_budget_ns",
+__all__ = ["gemv", "gemv_gate_up", "gemv_gate_up_swiglu", "moe_gemv", "device_status", "set_wait_budget_ns",
            "set_variant", "set_pdl", "fp32_fallbacks", "describe_plan", "library", "library_path", "NVFP4Error",
            "OUT_F32", "OUT_BF16", "DEV_TIMEOUT", "DEV_BAD_EXPERT"]
 
@@ -52,6 +52,9 @@ def _declare(lib):
     lib.nvfp4_gemv_gate_up.argtypes = [u8p, u8p, ctypes.c_float, u8p, u8p, ctypes.c_float, u16p, vp,
                                        i32, i32, i32, i32, vp]
     lib.nvfp4_gemv_gate_up.restype = i32
+    lib.nvfp4_gemv_gate_up_swiglu.argtypes = [u8p, u8p, ctypes.c_float, u8p, u8p, ctypes.c_float, u16p,
+                                              ctypes.c_float, vp, i32, i32, i32, i32, vp]
+    lib.nvfp4_gemv_gate_up_swiglu.restype = i32
     lib.nvfp4_moe_gemv.argtypes = [u8p, u8p, vp, i32, vp, i32, i32, u16p, i32, vp, i32, i32, i32,
                                    vp, vp]
     lib.nvfp4_moe_gemv.restype = i32
@@ -190,6 +193,28 @@ def gemv_gate_up(wg, sg, gg, wu, su, gu, x, out=None, out_dtype=torch.float32,
     return y
 
 
+def gemv_gate_up_swiglu(wg, sg, gg, wu, su, gu, x, clamp_limit: float = float("inf"), out=None,
+                        out_dtype=torch.bfloat16, stream=None) -> torch.Tensor:
+    """y[M, N] = silu(c(gg * W_gate . x)) * c(gu * W_up . x), c = clamp to [-clamp_limit,
+    clamp_limit] (inf: none), in one launch; the gate|up product is never written."""
+    for t, n in ((wg, "w_gate"), (wu, "w_up")):
+        _need(t, n, torch.uint8, 2)
+    for t, n in ((sg, "s_gate"), (su, "s_up")):
+        _need(t, n, torch.uint8, 2)
+    _need(x, "x", torch.bfloat16, 2)
+    N, K = wg.shape[0], wg.shape[1] * 2
+    M = x.shape[0]
+    if tuple(wu.shape) != tuple(wg.shape) or tuple(sg.shape) != (N, K // 16) or \
+            tuple(su.shape) != (N, K // 16) or x.shape[1] != K:
+        raise ValueError("shape mismatch between gate, up and x")
+    y = _out(out, (M, N), out_dtype, x.device)
+    st = library().nvfp4_gemv_gate_up_swiglu(_ptr(wg), _ptr(sg), float(gg), _ptr(wu), _ptr(su), float(gu),
+                                             _ptr(x), float(clamp_limit), _ptr(y), _out_code(y.dtype),
+                                             M, N, K, ctypes.c_void_p(_stream(stream)))
+    _check(st, "nvfp4_gemv_gate_up_swiglu")
+    return y
+
+
 def moe_gemv(w, s, gs, ids, x, x_per_slot: bool, top_k: int, out=None, out_dtype=torch.float32,
              status=None, stream=None) -> torch.Tensor:
     """Routed-expert GEMV: y[T*top_k, N]; slot t*top_k+j uses expert ids[t*top_k+j].
@@ -256,9 +281,10 @@ def set_pdl(enable: bool) -> None:
 
 
 def describe_plan(kind: str, M: int, N: int, K: int, T: int = 0, top_k: int = 0) -> str:
-    """Launch the library would pick: kind in {"dense", "gate_up", "moe", "moe_per_slot"}; for the
-    MoE kinds M is the number of experts (moe_per_slot: one x row per slot)."""
-    code = {"dense": 0, "gate_up": 1, "moe": 2, "moe_per_slot": 3}[kind]
+    """Launch the library would pick: kind in {"dense", "gate_up", "moe", "moe_per_slot",
+    "gate_up_swiglu"}; for the MoE kinds M is the number of experts (moe_per_slot: one x row
+    per slot)."""
+    code = {"dense": 0, "gate_up": 1, "moe": 2, "moe_per_slot": 3, "gate_up_swiglu": 4}[kind]
     buf = ctypes.create_string_buffer(256)
     n = library().nvfp4_describe_plan(code, M, N, K, T, top_k, buf, 256)
     if n < 0:

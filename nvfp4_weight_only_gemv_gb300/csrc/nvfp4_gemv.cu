@@ -8,13 +8,15 @@
 // "glm-5.3-flash-nvfp4-tp3-512k--gb10 graph.json": the weight is widened, multiplied by
 // the bf16 activation and accumulated in f32, and the f32 tensor scale is applied last.
 //
-// Three kernels:
+// Kernels:
 //   * gemv_tile_kernel (default for K % 256 == 0, aligned operands; dense, gate/up and up to
 //     32 MoE slots): every warp owns 16-row tiles and keeps its own ring of TMA tensor copies
 //     (128-byte swizzled codes + scales) full; the products run on the tensor cores as
 //     mma.sync.m16n8k16 with the weights decoded exactly to f16 (E2M1 * E4M3) and x staged in
 //     f16 per K slice. K may be split over warps (shared-memory reduction) or over a cluster
-//     (DSMEM reduction), both in a fixed order. See the comment above the kernel.
+//     (DSMEM reduction), both in a fixed order. See the comment above the kernel. Its third
+//     template flag gives gate/up with the fused SwiGLU: gate and up tiles alternate, so a
+//     pair meets in shared memory and only silu(clamp(gate)) * clamp(up) is stored.
 //   * gemv_tile_sk_kernel (MoE launches with many tiles per CTA): the same warp rings and
 //     decode in a stream-K form. Whole (expert group, tile) jobs are spread evenly over the
 //     CTAs and their TMA boxes evenly over each CTA's warps; a job cut between warps is
@@ -305,6 +307,16 @@ __device__ __forceinline__ void store_out(void* y, int64_t idx, float v, int out
     } else {
         reinterpret_cast<float*>(y)[idx] = v;
     }
+}
+
+// The fused gate/up activation: silu(clamp(gate)) * clamp(up), both clamped to [-lim, lim]
+// (lim = +inf: no clamp), in f32. NaN passes through the clamp. The swiglu_clamp and
+// silu_mul nodes of "glm-5.3-flash-nvfp4-tp3-512k--gb10 graph.json" (l0.mlp), whose steps
+// read "compute f32".
+__device__ __forceinline__ float swiglu_f32(float gate, float up, float lim) {
+    gate = gate > lim ? lim : (gate < -lim ? -lim : gate);
+    up = up > lim ? lim : (up < -lim ? -lim : up);
+    return gate / (1.f + expf(-gate)) * up;
 }
 
 __device__ __forceinline__ void raise_status(int bits, int32_t* user) {
@@ -1175,6 +1187,8 @@ struct TileParams {
     int nbox;                 // TMA boxes per row
     int stages;               // ring slots per warp
     int force_f32;
+    int swiglu;               // gate/up with the fused activation: tile 2j is gate tile j, 2j+1 up tile j
+    float clamp;              // its clamp limit (+inf: none)
     uint32_t sstride;         // bytes between staged x rows of one K slice (64 mod 128)
     uint32_t ring_w, ring_s, x_off, red_off, cpart_off, misc_off, bar_off;  // offsets from the 1024-aligned base
     uint64_t wait_ns;
@@ -1595,7 +1609,7 @@ __device__ void tile_moe_rows(const TileParams& p, TileMoe* tab, int g0, int g1,
     __syncwarp();
 }
 
-template <int NC, bool MOE>
+template <int NC, bool MOE, bool SWI = false>
 __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_kernel(const __grid_constant__ TileParams p) {
     extern __shared__ uint8_t smem_raw[];
     constexpr uint32_t kWBox = NC * 2048;  // 16 rows x NC x 128 B
@@ -1668,6 +1682,10 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_kernel(const __grid
         const int seg = (b_lo + iss_box) * NC;
         int row0 = (iw.t * p.tpi + tin) * 16;
         int map = iw.grp;
+        if constexpr (SWI) {
+            map = (iw.t * p.tpi + tin) & 1;  // tiles alternate gate, up
+            row0 = ((iw.t * p.tpi + tin) >> 1) * 16;
+        }
         if constexpr (MOE) {
             row0 += tab->expert[iw.grp] * p.N;  // experts' rows are back to back
             map = 0;
@@ -1828,6 +1846,64 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_kernel(const __grid
         };
         const int par = (item - ib) & 1;
         float* const cpart = reinterpret_cast<float*>(sbase + p.cpart_off) + par * (tk::kWarps * 16 * 8);
+        if constexpr (SWI) {
+            // gate tile 2j and up tile 2j + 1 of this item meet in cpart ([tile * 16 + row][m]:
+            // this CTA's sums over its K range), then every output combines its pair
+            const int outs = p.tpi * 16 * ncols;
+            const int pair_outs = (p.tpi >> 1) * 16 * ncols;
+            if (ksplit == 1) {
+                float* cp = cpart + tin * 128;
+                cp[ra * 8 + m0] = d[0];
+                cp[ra * 8 + m0 + 1] = d[1];
+                cp[rb * 8 + m0] = d[2];
+                cp[rb * 8 + m0 + 1] = d[3];
+            } else {
+                float* rbuf = red + par * tk::kRedFloats + warp * 128;
+                rbuf[ra * 8 + m0] = d[0];
+                rbuf[ra * 8 + m0 + 1] = d[1];
+                rbuf[rb * 8 + m0] = d[2];
+                rbuf[rb * 8 + m0 + 1] = d[3];
+                named_bar_sync(1, tk::kThreads);
+                const float* rb0 = red + par * tk::kRedFloats;
+                for (int i = tid; i < outs; i += tk::kThreads) {
+                    const int ti = i / (16 * ncols), rem = i - ti * 16 * ncols;
+                    const int r = rem / ncols, m = rem - r * ncols;
+                    float sum = 0.f;
+                    for (int j = 0; j < ksplit; ++j) sum += rb0[((ti << p.ksplit_log2) + j) * 128 + r * 8 + m];
+                    cpart[ti * 128 + r * 8 + m] = sum;
+                }
+            }
+            int o_lo = 0, o_hi = pair_outs, o_step = tk::kThreads;
+            if (S == 1) {
+                named_bar_sync(1, tk::kThreads);
+            } else {
+                // the cluster's K ranges: rank r combines the r-th share of the outputs, adding
+                // the ranks' sums in rank order (DSMEM)
+                cluster_sync_all();
+                o_lo = (rank * pair_outs) >> p.s_log2;
+                o_hi = ((rank + 1) * pair_outs) >> p.s_log2;
+            }
+            for (int i = o_lo + tid; i < o_hi; i += o_step) {
+                const int pi = i / (16 * ncols), rem = i - pi * 16 * ncols;
+                const int r = rem / ncols, m = rem - r * ncols;
+                const int jt = cw.t * (p.tpi >> 1) + pi, row = jt * 16 + r;  // output tile, row
+                if (2 * jt < p.tiles && row < p.N) {
+                    const float* cg = cpart + (2 * pi) * 128 + r * 8 + m;
+                    float sg = 0.f, su = 0.f;
+                    if (S == 1) {
+                        sg = cg[0];
+                        su = cg[128];
+                    } else {
+                        for (int j = 0; j < S; ++j) {
+                            sg += ld_cluster_f32(cg, j);
+                            su += ld_cluster_f32(cg + 128, j);
+                        }
+                    }
+                    store_out(p.y, m * p.ldy + row, swiglu_f32(sg * p.g[0], su * p.g[1], p.clamp), p.out_bf16);
+                }
+            }
+            continue;
+        }
         if (ksplit == 1 && S == 1) {
             if (valid) {
                 const int rowa = tile * 16 + ra, rowb = tile * 16 + rb;
@@ -2244,6 +2320,8 @@ struct SimpleParams {
     int out_bf16;
     int M, N, K, groups;
     int moe, E, top_k, x_per_slot, slots;
+    int swiglu;               // groups == 2: one output silu(clamp(gate)) * clamp(up) per column
+    float clamp;
 };
 
 // One warp per output column (all M rows). Lanes stride over the 16-element blocks of K.
@@ -2278,8 +2356,9 @@ __global__ void __launch_bounds__(kSimpleThreads) gemv_simple_kernel(const __gri
         out_step = 0;
         mrows = 1;
     } else {
-        if (col >= static_cast<int64_t>(p.groups) * p.N) return;
-        const int grp = static_cast<int>(col / p.N);
+        const int64_t cols = p.swiglu ? p.N : static_cast<int64_t>(p.groups) * p.N;
+        if (col >= cols) return;
+        const int grp = p.swiglu ? 0 : static_cast<int>(col / p.N);
         const int64_t n = col - static_cast<int64_t>(grp) * p.N;
         wrow = p.w[grp] + n * Kh;
         srow = p.s[grp] + n * Ks;
@@ -2287,33 +2366,50 @@ __global__ void __launch_bounds__(kSimpleThreads) gemv_simple_kernel(const __gri
         out0 = col;
         out_step = p.ldy;
     }
-    float acc[MT];
+    // acc[m] = sum over K of the row's products with x row xrow0 + m, summed over the warp
+    auto dot = [&](const uint8_t* wr, const uint8_t* sr, float (&acc)[MT]) {
 #pragma unroll
-    for (int m = 0; m < MT; ++m) acc[m] = 0.f;
-    for (int64_t b = lane; b < Ks; b += 32) {
-        const uint32_t shf = cvt_e4m3x2(static_cast<uint16_t>(__ldg(srow + b)));
-        const uint16_t sc = static_cast<uint16_t>(shf & 0xffffu);
-        for (int e = 0; e < 8; ++e) {
-            uint32_t h[4];
-            cvt_e2m1x8(static_cast<uint32_t>(__ldg(wrow + b * 8 + e)), h);
-            const float2 q = widen_scaled(h[0], sc);
-            const int64_t k = b * 16 + 2 * e;
+        for (int m = 0; m < MT; ++m) acc[m] = 0.f;
+        for (int64_t b = lane; b < Ks; b += 32) {
+            const uint32_t shf = cvt_e4m3x2(static_cast<uint16_t>(__ldg(sr + b)));
+            const uint16_t sc = static_cast<uint16_t>(shf & 0xffffu);
+            for (int e = 0; e < 8; ++e) {
+                uint32_t h[4];
+                cvt_e2m1x8(static_cast<uint32_t>(__ldg(wr + b * 8 + e)), h);
+                const float2 q = widen_scaled(h[0], sc);
+                const int64_t k = b * 16 + 2 * e;
 #pragma unroll
-            for (int m = 0; m < MT; ++m) {
-                if (m < mrows) {
-                    const uint16_t* xr = p.x + (xrow0 + m) * p.K + k;
-                    const float x0 = __uint_as_float(static_cast<uint32_t>(__ldg(xr)) << 16);
-                    const float x1 = __uint_as_float(static_cast<uint32_t>(__ldg(xr + 1)) << 16);
-                    acc[m] = fmaf(q.x, x0, acc[m]);
-                    acc[m] = fmaf(q.y, x1, acc[m]);
+                for (int m = 0; m < MT; ++m) {
+                    if (m < mrows) {
+                        const uint16_t* xr = p.x + (xrow0 + m) * p.K + k;
+                        const float x0 = __uint_as_float(static_cast<uint32_t>(__ldg(xr)) << 16);
+                        const float x1 = __uint_as_float(static_cast<uint32_t>(__ldg(xr + 1)) << 16);
+                        acc[m] = fmaf(q.x, x0, acc[m]);
+                        acc[m] = fmaf(q.y, x1, acc[m]);
+                    }
                 }
             }
         }
-    }
 #pragma unroll
-    for (int m = 0; m < MT; ++m) {
+        for (int m = 0; m < MT; ++m) {
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) acc[m] += __shfl_xor_sync(0xffffffffu, acc[m], o);
+            for (int o = 16; o > 0; o >>= 1) acc[m] += __shfl_xor_sync(0xffffffffu, acc[m], o);
+        }
+    };
+    float acc[MT];
+    dot(wrow, srow, acc);
+    if (!p.moe && p.swiglu) {
+        // the same column of the up projection, then the fused activation
+        float accu[MT];
+        dot(p.w[1] + col * Kh, p.s[1] + col * Ks, accu);
+        if (lane == 0) {
+#pragma unroll
+            for (int m = 0; m < MT; ++m)
+                if (m < mrows)
+                    store_out(p.y, out0 + m * out_step, swiglu_f32(g * acc[m], p.g[1] * accu[m], p.clamp),
+                              p.out_bf16);
+        }
+        return;
     }
     if (lane == 0) {
 #pragma unroll
@@ -2651,7 +2747,8 @@ struct TilePlan {
 // the 128-element steps of one warp per item) and a throughput term (items on the busiest
 // SM times the steps each of its warps decodes), both in units of one warp step.
 bool plan_tile(TilePlan& tp, int M, int N, int K, int groups, const DeviceInfo& d, const uint8_t* const* w,
-               const uint8_t* const* s, const void* x, bool moe = false, int moe_rows = 0, int moe_groups_max = 0) {
+               const uint8_t* const* s, const void* x, bool moe = false, int moe_rows = 0, int moe_groups_max = 0,
+               bool swiglu = false) {
     if (g_variant == 1 || g_variant == 3) return false;
     if (K <= 0 || K % 256 != 0 || M < 1 || M > 8 || N < 1 || N > (1 << 27)) return false;
     // MoE: M is the largest number of columns of a group (8), groups the expected number of
@@ -2663,7 +2760,10 @@ bool plan_tile(TilePlan& tp, int M, int N, int K, int groups, const DeviceInfo& 
         if ((reinterpret_cast<uintptr_t>(w[i]) & 15) || (reinterpret_cast<uintptr_t>(s[i]) & 15)) return false;
     if (!tensor_map_encoder()) return false;
     const int segs = K / 256;
-    const int tiles = (N + 15) / 16;
+    // gate/up with the fused activation: one group of 2 * tiles, gate and up tiles alternating,
+    // so that an item (an even number of tiles) holds whole pairs
+    const int tiles = swiglu ? 2 * ((N + 15) / 16) : (N + 15) / 16;
+    const int item_groups = swiglu ? 1 : groups;
     bool found = false;
     double best = 0.0;
     for (int nc = 2; nc >= 1; --nc) {
@@ -2680,8 +2780,9 @@ bool plan_tile(TilePlan& tp, int M, int N, int K, int groups, const DeviceInfo& 
                 if (NVFP4_TILE_KSPLIT && ksplit != NVFP4_TILE_KSPLIT) continue;
                 if (NVFP4_TILE_NC && nc != NVFP4_TILE_NC) continue;
                 const int tpi = tk::kWarps / ksplit;
+                if (swiglu && tpi < 2) continue;
                 const int ipg = (tiles + tpi - 1) / tpi;
-                const long long items = static_cast<long long>(groups) * ipg;
+                const long long items = static_cast<long long>(item_groups) * ipg;
                 if (items > (1LL << 30)) continue;
                 const int nbmax = (nbs + ksplit - 1) / ksplit;  // most boxes of one warp per item
                 const uint32_t sstride = static_cast<uint32_t>(nbmax) * nc * 512u + 64u;
@@ -2714,7 +2815,7 @@ bool plan_tile(TilePlan& tp, int M, int N, int K, int groups, const DeviceInfo& 
                         q.red_off = off;
                         if (ksplit > 1) off += 2u * tk::kRedFloats * 4u;
                         q.cpart_off = off;
-                        if (S > 1) off += 2u * tk::kWarps * 16 * 8 * 4u;
+                        if (S > 1 || swiglu) off += 2u * tk::kWarps * 16 * 8 * 4u;
                         q.misc_off = off;
                         off += align_up(tk::kWarps * 32 + tk::kWarps * 32 * 4, 128);  // e2, extremes, votes
                         q.bar_off = off;
@@ -2887,11 +2988,11 @@ bool encode_tile_maps(CUtensorMap* wmap, CUtensorMap* smap, const uint8_t* w, co
     return true;
 }
 
-template <int NC, bool MOE, bool SK>
+template <int NC, bool MOE, bool SK, bool SWI = false>
 cudaError_t launch_tile_nc(const TilePlan& tp, cudaStream_t st) {
     auto kern = [] {
         if constexpr (SK) return gemv_tile_sk_kernel<NC, MOE>;
-        else return gemv_tile_kernel<NC, MOE>;
+        else return gemv_tile_kernel<NC, MOE, SWI>;
     }();
     static bool done[64] = {};
     cudaError_t e = allow_max_smem(kern, done);
@@ -2923,6 +3024,8 @@ cudaError_t launch_tile_nc(const TilePlan& tp, cudaStream_t st) {
 cudaError_t launch_tile(const TilePlan& tp, cudaStream_t st, bool moe) {
     if (moe && tp.sk) return tp.nc == 2 ? launch_tile_nc<2, true, true>(tp, st) : launch_tile_nc<1, true, true>(tp, st);
     if (moe) return tp.nc == 2 ? launch_tile_nc<2, true, false>(tp, st) : launch_tile_nc<1, true, false>(tp, st);
+    if (tp.p.swiglu)
+        return tp.nc == 2 ? launch_tile_nc<2, false, false, true>(tp, st) : launch_tile_nc<1, false, false, true>(tp, st);
     return tp.nc == 2 ? launch_tile_nc<2, false, false>(tp, st) : launch_tile_nc<1, false, false>(tp, st);
 }
 
@@ -2956,8 +3059,11 @@ nvfp4_status zero_output(void* y, int64_t elems, int y_type, cudaStream_t st) {
     return e == cudaSuccess ? NVFP4_OK : cuda_fail(e);
 }
 
+// Dense (groups = 1) and gate/up (groups = 2) calls; swiglu: gate/up with the fused
+// activation, y [M, N] = silu(clamp(gate)) * clamp(up).
 nvfp4_status run_dense(const uint8_t* const* w, const uint8_t* const* s, const float* g, int groups,
-                       const uint16_t* x, void* y, int y_type, int M, int N, int K, cudaStream_t st) {
+                       const uint16_t* x, void* y, int y_type, int M, int N, int K, cudaStream_t st,
+                       bool swiglu = false, float clamp = 0.f) {
     if (!x || !y) return NVFP4_ERR_NULL;
     for (int i = 0; i < groups; ++i)
         if (!w[i] || !s[i]) return NVFP4_ERR_NULL;
@@ -2965,12 +3071,13 @@ nvfp4_status run_dense(const uint8_t* const* w, const uint8_t* const* s, const f
     const nvfp4_status so = check_out(y_type);
     if (so != NVFP4_OK) return so;
     if (M == 0 || N == 0) return NVFP4_OK;
-    if (K == 0) return zero_output(y, static_cast<int64_t>(M) * groups * N, y_type, st);
+    const int64_t ldy = swiglu ? N : static_cast<int64_t>(groups) * N;  // output columns
+    if (K == 0) return zero_output(y, static_cast<int64_t>(M) * ldy, y_type, st);  // silu(0) * 0 = 0
     int dev = 0;
     const DeviceInfo* d = device_info(&dev);
     if (!d) return cuda_fail(cudaGetLastError());
     TilePlan tpl{};
-    if (plan_tile(tpl, M, N, K, groups, *d, w, s, x)) {
+    if (plan_tile(tpl, M, N, K, groups, *d, w, s, x, false, 0, 0, swiglu)) {
         TileParams& p = tpl.p;
         bool ok = true;
         for (int i = 0; i < groups && ok; ++i) ok = encode_tile_maps(&p.wmap[i], &p.smap[i], w[i], s[i], N, K, tpl.nc);
@@ -2983,7 +3090,9 @@ nvfp4_status run_dense(const uint8_t* const* w, const uint8_t* const* s, const f
             p.y = y;
             p.g[0] = g[0];
             p.g[1] = g[groups > 1 ? 1 : 0];
-            p.ldy = static_cast<int64_t>(groups) * N;
+            p.ldy = ldy;
+            p.swiglu = swiglu ? 1 : 0;
+            p.clamp = clamp;
             p.out_bf16 = y_type == NVFP4_OUT_BF16;
             p.force_f32 = g_variant == 2;
             p.wait_ns = g_wait_ns;
@@ -2994,7 +3103,7 @@ nvfp4_status run_dense(const uint8_t* const* w, const uint8_t* const* s, const f
         }
     }
     Plan pl{};
-    if (plan_dense(pl, M, N, K, groups, *d, w, s, x)) {
+    if (!swiglu && plan_dense(pl, M, N, K, groups, *d, w, s, x)) {
         Params& p = pl.p;
         for (int i = 0; i < 2; ++i) {
             p.w[i] = w[i < groups ? i : 0];
@@ -3018,9 +3127,11 @@ nvfp4_status run_dense(const uint8_t* const* w, const uint8_t* const* s, const f
         sp.s[i] = s[i < groups ? i : 0];
         sp.g[i] = g[i < groups ? i : 0];
     }
-    sp.x = x; sp.y = y; sp.ldy = static_cast<int64_t>(groups) * N; sp.out_bf16 = y_type == NVFP4_OUT_BF16;
+    sp.x = x; sp.y = y; sp.ldy = ldy; sp.out_bf16 = y_type == NVFP4_OUT_BF16;
     sp.M = M; sp.N = N; sp.K = K; sp.groups = groups;
-    const cudaError_t e = launch_simple(sp, static_cast<int64_t>(groups) * N, st);
+    sp.swiglu = swiglu ? 1 : 0;
+    sp.clamp = clamp;
+    const cudaError_t e = launch_simple(sp, ldy, st);
     return e == cudaSuccess ? NVFP4_OK : cuda_fail(e);
 }
 
@@ -3046,6 +3157,17 @@ nvfp4_status nvfp4_gemv_gate_up(const uint8_t* w_gate, const uint8_t* s_gate, fl
     const uint8_t* s[2] = {s_gate, s_up};
     const float g[2] = {g_gate, g_up};
     return run_dense(w, s, g, 2, x, y, y_type, M, N, K, static_cast<cudaStream_t>(stream));
+}
+
+nvfp4_status nvfp4_gemv_gate_up_swiglu(const uint8_t* w_gate, const uint8_t* s_gate, float g_gate,
+                                       const uint8_t* w_up, const uint8_t* s_up, float g_up,
+                                       const uint16_t* x, float clamp_limit, void* y, nvfp4_out_t y_type,
+                                       int M, int N, int K, void* stream) {
+    if (!(clamp_limit > 0.f)) return NVFP4_ERR_SHAPE;  // also rejects NaN
+    const uint8_t* w[2] = {w_gate, w_up};
+    const uint8_t* s[2] = {s_gate, s_up};
+    const float g[2] = {g_gate, g_up};
+    return run_dense(w, s, g, 2, x, y, y_type, M, N, K, static_cast<cudaStream_t>(stream), true, clamp_limit);
 }
 
 nvfp4_status nvfp4_moe_gemv(const uint8_t* w_packed, const uint8_t* w_scales,
@@ -3186,6 +3308,16 @@ int nvfp4_describe_plan(int kind, int M, int N, int K, int T, int top_k, char* b
     // Pointers are only inspected for alignment here; 256-byte aligned stand-ins.
     const uint8_t* fake = reinterpret_cast<const uint8_t*>(static_cast<uintptr_t>(256));
     const uint8_t* w[2] = {fake, fake};
+    if (kind == 4) {  // gate/up with the fused activation: the tile kernel, else the byte-load kernel
+        TilePlan tpl{};
+        if (plan_tile(tpl, M, N, K, 2, *d, w, w, fake, false, 0, 0, true))
+            return snprintf(buf, buflen,
+                            "tile_swiglu grid=%d block=%d smem=%u split=%d rows_per_item=%d k_warps=%d mt=%d stages=%d nc=%d",
+                            tpl.grid_x * tpl.grid_y, tk::kThreads, tpl.smem, 1 << tpl.p.s_log2, tpl.p.tpi * 16,
+                            1 << tpl.p.ksplit_log2, M, tpl.p.stages, tpl.nc);
+        return snprintf(buf, buflen, "simple grid=%lld block=%d smem=0 split=1 rows_per_item=0 k_warps=0",
+                        static_cast<long long>((static_cast<int64_t>(N) + 7) / 8), kSimpleThreads);
+    }
     if (kind == 0 || kind == 1) {
         TilePlan tpl{};
         if (plan_tile(tpl, M, N, K, kind == 0 ? 1 : 2, *d, w, w, fake)) {

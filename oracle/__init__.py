@@ -62,6 +62,13 @@ def _declare(lib):
                                               ctypes.c_int64, ctypes.c_int64, c_i64p,
                                               ctypes.c_int64, c_dp, c_dp]
     lib.nvfp4_oracle_gemv_gate_up.restype = ctypes.c_int
+    lib.nvfp4_oracle_swiglu.argtypes = [ctypes.c_double, ctypes.c_double, ctypes.c_double]
+    lib.nvfp4_oracle_swiglu.restype = ctypes.c_double
+    lib.nvfp4_oracle_gate_up_swiglu.argtypes = [c_u8p, c_u8p, ctypes.c_double, c_u8p, c_u8p,
+                                                ctypes.c_double, c_u16p, ctypes.c_double,
+                                                ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                                c_i64p, ctypes.c_int64, c_dp, c_dp, c_dp, c_dp, c_dp]
+    lib.nvfp4_oracle_gate_up_swiglu.restype = ctypes.c_int
     lib.nvfp4_oracle_moe_gemv.argtypes = [c_u8p, c_u8p, ctypes.POINTER(ctypes.c_float),
                                           ctypes.c_int64, ctypes.POINTER(ctypes.c_int32),
                                           ctypes.c_int64, ctypes.c_int64, c_u16p, ctypes.c_int,
@@ -165,6 +172,34 @@ def gemv_gate_up(wg, sg, gg, wu, su, gu, x_bits, rows=None, lib=None):
     if rc != 0:
         raise ValueError("oracle gate_up: bad arguments")
     return y, ya
+
+
+def swiglu(gate: float, up: float, lim: float = float("inf"), lib=None) -> float:
+    """silu(c(gate)) * c(up) with c the clamp to [-lim, lim], in fp64."""
+    return (lib or load()).nvfp4_oracle_swiglu(float(gate), float(up), float(lim))
+
+
+def gate_up_swiglu(wg, sg, gg, wu, su, gu, x_bits, lim=float("inf"), rows=None, lib=None):
+    """Gate/up GEMVs then the fused activation. Returns y [M, len(rows)] and a dict with the
+    fp64 gate and up values and their |g| * sum |term| scales ("gate", "gate_abs", "up",
+    "up_abs"), each [M, len(rows)]."""
+    lib = lib or load()
+    wg, sg, wu, su, x = _u8(wg), _u8(sg), _u8(wu), _u8(su), _u16(x_bits)
+    N, K = wg.shape[0], wg.shape[1] * 2
+    M = x.shape[0]
+    assert wu.shape == wg.shape and sg.shape == su.shape == (N, K // 16) and x.shape == (M, K)
+    r, rp = _rows(rows)
+    nr = N if r is None else r.shape[0]
+    out = {k: np.empty((M, nr), dtype=np.float64) for k in ("y", "gate", "gate_abs", "up", "up_abs")}
+    rc = lib.nvfp4_oracle_gate_up_swiglu(_ptr(wg, ctypes.c_uint8), _ptr(sg, ctypes.c_uint8), float(gg),
+                                         _ptr(wu, ctypes.c_uint8), _ptr(su, ctypes.c_uint8), float(gu),
+                                         _ptr(x, ctypes.c_uint16), float(lim), M, N, K, rp, nr,
+                                         *[_ptr(out[k], ctypes.c_double)
+                                           for k in ("y", "gate", "gate_abs", "up", "up_abs")])
+    if rc != 0:
+        raise ValueError("oracle gate_up_swiglu: bad arguments")
+    y = out.pop("y")
+    return y, out
 
 
 def moe_gemv(w, s, gs, ids, x_bits, x_per_slot, top_k, rows=None, lib=None):

@@ -182,6 +182,56 @@ int nvfp4_oracle_gemv_gate_up(const uint8_t *wg, const uint8_t *sg, double gg,
 }
 
 /*
+ * The fused gate/up activation (the swiglu_clamp and silu_mul nodes that follow the gate/up
+ * projection in "glm-5.3-flash-nvfp4-tp3-512k--gb10 graph.json", block l0.mlp; the pages name
+ * a clamp but give no limit, so the limit is an argument, +inf for none):
+ *     c(v) = v > lim ? lim : (v < -lim ? -lim : v)      (NaN stays NaN)
+ *     silu(v) = v / (1 + exp(-v))
+ *     swiglu(gate, up) = silu(c(gate)) * c(up).
+ */
+double nvfp4_oracle_swiglu(double gate, double up, double lim) {
+    double gc = gate > lim ? lim : (gate < -lim ? -lim : gate);
+    double uc = up > lim ? lim : (up < -lim ? -lim : up);
+    return gc / (1.0 + exp(-gc)) * uc;
+}
+
+/*
+ * Gate/up GEMVs followed by the fused activation: y[m, i] = swiglu(gate[m, n], up[m, n]) for
+ * the output columns n = rows[i] (NULL = all N), in fp64. The gate and up values and their
+ * |g| * sum |term| scales are returned too ([M, nrows] each; NULL pointers skip them), so a
+ * caller can bound how errors in gate and up carry through the activation.
+ */
+int nvfp4_oracle_gate_up_swiglu(const uint8_t *wg, const uint8_t *sg, double gg,
+                                const uint8_t *wu, const uint8_t *su, double gu,
+                                const uint16_t *x, double lim, int64_t M, int64_t N, int64_t K,
+                                const int64_t *rows, int64_t nrows, double *y,
+                                double *gate, double *gate_abs, double *up, double *up_abs) {
+    if (K % 16 != 0 || M < 0 || N < 0 || K < 0 || !(lim > 0.0)) return -1;
+    if (rows == NULL) nrows = N;
+    for (int64_t i = 0; i < nrows; ++i) {
+        int64_t n = rows ? rows[i] : i;
+        if (n < 0 || n >= N) return -1;
+    }
+    int64_t i;
+#pragma omp parallel for schedule(static)
+    for (i = 0; i < nrows; ++i) {
+        int64_t n = rows ? rows[i] : i;
+        for (int64_t m = 0; m < M; ++m) {
+            double sg_sum, sg_abs, su_sum, su_abs;
+            dot_row(wg + n * (K / 2), sg + n * (K / 16), x + m * K, K, &sg_sum, &sg_abs);
+            dot_row(wu + n * (K / 2), su + n * (K / 16), x + m * K, K, &su_sum, &su_abs);
+            double gv = gg * sg_sum, uv = gu * su_sum;
+            y[m * nrows + i] = nvfp4_oracle_swiglu(gv, uv, lim);
+            if (gate) gate[m * nrows + i] = gv;
+            if (gate_abs) gate_abs[m * nrows + i] = fabs(gg) * sg_abs;
+            if (up) up[m * nrows + i] = uv;
+            if (up_abs) up_abs[m * nrows + i] = fabs(gu) * su_abs;
+        }
+    }
+    return 0;
+}
+
+/*
  * Routed-expert GEMV over slots (the routed gate/up slot GEMV of
  * "glm-5.3-flash-nvfp4-tp3-512k--gb10 card.json", performance[33]).
  * w: [E, N, K/2], s: [E, N, K/16], gs: [E] per-expert global scales (float).

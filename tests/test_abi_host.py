@@ -25,9 +25,9 @@ def lib():
     return nv.library()
 
 
-def test_header_declares_the_three_entry_points():
+def test_header_declares_the_entry_points():
     names = declared_functions()
-    for n in ("nvfp4_gemv", "nvfp4_gemv_gate_up", "nvfp4_moe_gemv"):
+    for n in ("nvfp4_gemv", "nvfp4_gemv_gate_up", "nvfp4_gemv_gate_up_swiglu", "nvfp4_moe_gemv"):
         assert n in names
 
 
@@ -74,6 +74,27 @@ def test_gate_up_validation(lib):
     assert f(FAKE, FAKE, 1.0, None, FAKE, 1.0, FAKE, FAKE, 0, 1, 16, 32, None) == 1
     assert f(FAKE, FAKE, 1.0, FAKE, FAKE, 1.0, FAKE, FAKE, 0, 1, 16, 33, None) == 2
     assert f(FAKE, FAKE, 1.0, FAKE, FAKE, 1.0, FAKE, FAKE, 1, 0, 16, 32, None) == 0
+
+
+def test_gate_up_swiglu_validation(lib):
+    f = lib.nvfp4_gemv_gate_up_swiglu
+    inf = float("inf")
+    ok = [FAKE, FAKE, 1.0, FAKE, FAKE, 1.0, FAKE, inf, FAKE, 0, 1, 16, 32, None]
+    bad = list(ok); bad[3] = None                     # null up weights
+    assert f(*bad) == 1
+    bad = list(ok); bad[8] = None                     # null y
+    assert f(*bad) == 1
+    for lim in (0.0, -1.0, float("nan")):             # the clamp limit must be > 0
+        bad = list(ok); bad[7] = lim
+        assert f(*bad) == 2
+    bad = list(ok); bad[12] = 40                      # K % 16 != 0
+    assert f(*bad) == 2
+    bad = list(ok); bad[10] = 9                       # M > 8
+    assert f(*bad) == 2
+    bad = list(ok); bad[9] = 3                        # bad output type
+    assert f(*bad) == 4
+    empty = list(ok); empty[10] = 0                   # M == 0: nothing to do
+    assert f(*empty) == 0
 
 
 def test_moe_validation(lib):

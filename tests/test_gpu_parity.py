@@ -461,3 +461,118 @@ def test_plan_uses_all_sms_for_large_problems():
     assert desc.split()[0] in ("tile", "stream") and grid % sms == 0 and grid >= sms
     desc = nv.describe_plan("dense", 8, 4096, 12288)
     assert "split=" in desc and "split=1 " not in desc
+
+
+# ------------------------------------------------------------------ fused gate/up activation
+# y = silu(c(gate)) * c(up), c = clamp to [-lim, lim]. The GPU's gate and up carry the GEMV
+# tolerance tg = 1e-5 * A_gate + 1e-6 (tu likewise); the clamp does not enlarge an error,
+# |silu'| <= 1.1 everywhere and |silu(v)| <= max(|v|, 0.28), so an output may differ by
+#   1.1 * |c(up)| * tg + max(|c(gate)|, 0.28) * tu + 1.1 * tg * tu
+# plus the fp32 evaluation of the activation (a few roundings and expf: 1e-6 * |y|), the
+# absolute 1e-6, and one bf16 ulp of y_ref for bf16 output.
+
+def swiglu_tolerance(aux, y_ref, lim, bf16):
+    tg = 1e-5 * aux["gate_abs"] + 1e-6
+    tu = 1e-5 * aux["up_abs"] + 1e-6
+    cg = np.clip(aux["gate"], -lim, lim)
+    cu = np.clip(aux["up"], -lim, lim)
+    tol = 1.1 * np.abs(cu) * tg + np.maximum(np.abs(cg), 0.28) * tu + 1.1 * tg * tu
+    tol = tol + 1e-6 * np.abs(np.nan_to_num(y_ref)) + 1e-6
+    if bf16:
+        tol = tol + ulp_bf16(np.nan_to_num(y_ref))
+    return tol
+
+
+def assert_swiglu_parity(y_gpu, y_ref, aux, lim, what=""):
+    y = y_gpu.detach().float().cpu().numpy().astype(np.float64)
+    assert y.shape == y_ref.shape, (y.shape, y_ref.shape)
+    nan_ref = np.isnan(y_ref)
+    assert np.array_equal(np.isnan(y), nan_ref), f"{what}: NaN positions differ"
+    tol = swiglu_tolerance(aux, y_ref, lim, y_gpu.dtype == torch.bfloat16)
+    err = np.where(nan_ref, 0.0, np.abs(y - y_ref))
+    bad = err > np.where(nan_ref, 1.0, tol)
+    if bad.any():
+        i = np.unravel_index(np.argmax(err - tol), err.shape)
+        raise AssertionError(f"{what}: {bad.sum()} of {bad.size} outside tolerance; worst at {i}: "
+                             f"gpu={y[i]!r} ref={y_ref[i]!r} tol={tol[i]!r}")
+
+
+def run_swiglu(N, K, M, seed, lim, out_dtype, device="cpu", p=None):
+    p = p or synth.gate_up_problem(N, K, M, seed, device=device)
+    wg, sg, wu, su, x = (p[k].to(DEV) for k in ("wg", "sg", "wu", "su", "x"))
+    y = nv.gemv_gate_up_swiglu(wg, sg, p["gg"], wu, su, p["gu"], x, lim, out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    yr, aux = oracle.gate_up_swiglu(host(p["wg"]), host(p["sg"]), p["gg"], host(p["wu"]), host(p["su"]),
+                                    p["gu"], synth.bf16_bits(p["x"]), lim)
+    return y, yr, aux
+
+
+@pytest.mark.parametrize("M", [1, 2, 4, 8])
+@pytest.mark.parametrize("lim", [math.inf, 1.0])
+def test_swiglu_ffn_shape(M, lim):
+    # the FFN gate/up projection (2 x 12288 x 4096); lim = 1 clamps part of gate and up
+    y, yr, aux = run_swiglu(12288, 4096, M, 5, lim, torch.bfloat16, device=DEV)
+    if lim < math.inf:
+        assert (np.abs(aux["gate"]) > lim).any() and (np.abs(aux["up"]) > lim).any()
+    assert_swiglu_parity(y, yr, aux, lim, f"swiglu ffn M={M} lim={lim}")
+
+
+@pytest.mark.parametrize("N,K,M", [(3072, 4096, 4), (4096, 4096, 8), (1000, 1024, 3), (37, 2560, 8),
+                                   (513, 768, 2), (1, 256, 1), (5, 256, 7), (300, 12288, 1),
+                                   (2000, 2048, 8), (4096, 1536, 5)])
+@pytest.mark.parametrize("out", [torch.float32, torch.bfloat16])
+def test_swiglu_tile_plans_and_ragged_rows(N, K, M, out):
+    # plans with a K split over warps, over a cluster (S = 4 and 8), one warp per tile, and
+    # N not a multiple of 16
+    y, yr, aux = run_swiglu(N, K, M, 600 + N % 97 + M, 0.5, out)
+    assert_swiglu_parity(y, yr, aux, 0.5, f"swiglu {N}x{K} M={M}")
+
+
+@pytest.mark.parametrize("variant", [1, 2, 3])
+def test_swiglu_other_kernels(variant):
+    # 1: byte-load kernel; 2: tile kernel in exact fp32; 3: streaming kernel requested (the
+    # fused form has no streaming instantiation, so the byte-load kernel runs)
+    nv.set_variant(variant)
+    for N, K, M in ((300, 512, 1), (129, 1024, 5)):
+        y, yr, aux = run_swiglu(N, K, M, 640 + variant, 0.75, torch.float32)
+        assert_swiglu_parity(y, yr, aux, 0.75, f"swiglu variant {variant} {N}x{K}")
+
+
+@pytest.mark.parametrize("N,K,M", [(77, 528, 3), (40, 96, 1), (3, 16, 8)])
+def test_swiglu_k_not_multiple_of_256(N, K, M):
+    y, yr, aux = run_swiglu(N, K, M, 650 + K, 2.0, torch.bfloat16)
+    assert_swiglu_parity(y, yr, aux, 2.0, f"swiglu {N}x{K}")
+
+
+def test_swiglu_matches_gate_up_then_activation():
+    # the fused call against the unfused gate_up output run through the same fp32 activation
+    p = synth.gate_up_problem(2048, 4096, 2, 660, device=DEV)
+    yf = nv.gemv_gate_up_swiglu(p["wg"], p["sg"], p["gg"], p["wu"], p["su"], p["gu"], p["x"], 1.5,
+                                out_dtype=torch.float32)
+    gu = nv.gemv_gate_up(p["wg"], p["sg"], p["gg"], p["wu"], p["su"], p["gu"], p["x"])
+    torch.cuda.synchronize()
+    g, u = gu[:, :2048].double(), gu[:, 2048:].double()
+    ref = (torch.nn.functional.silu(g.clamp(-1.5, 1.5)) * u.clamp(-1.5, 1.5)).float()
+    assert torch.allclose(yf, ref, rtol=1e-5, atol=1e-5)
+
+
+def test_swiglu_nan_scale_and_empty_inputs():
+    N, K, M = 300, 512, 2
+    p = synth.gate_up_problem(N, K, M, 670)
+    sg = p["sg"].clone()
+    sg[17, 3] = 0x7F                      # NaN gate in row 17
+    su = p["su"].clone()
+    su[200, 0] = 0xFF                     # NaN up in row 200
+    q = dict(p, sg=sg, su=su)
+    y, yr, aux = run_swiglu(N, K, M, 0, 1.0, torch.float32, p=q)
+    assert np.isnan(yr[:, 17]).all() and np.isnan(yr[:, 200]).all()
+    assert_swiglu_parity(y, yr, aux, 1.0, "swiglu nan")
+    # K = 0: gate = up = 0, so y = 0; M = 0 and N = 0 launch nothing
+    z = torch.empty(4, 0, dtype=torch.uint8, device=DEV)
+    x0 = torch.empty(2, 0, dtype=torch.bfloat16, device=DEV)
+    y0 = torch.full((2, 4), 7.0, device=DEV)
+    nv.gemv_gate_up_swiglu(z, z, 1.0, z, z, 1.0, x0, out=y0)
+    torch.cuda.synchronize()
+    assert torch.all(y0 == 0)
+    assert nv.describe_plan("gate_up_swiglu", 1, 12288, 4096).startswith("tile_swiglu ")
+    assert nv.describe_plan("gate_up_swiglu", 1, 100, 528).startswith("simple ")

@@ -6,6 +6,7 @@ index, a dropped term, a transposed operand, and so on. It then builds the copy
 into a scratch library and checks that the pin battery below rejects it. The
 unmodified source must pass the same battery. Everything runs on the CPU.
 """
+import math
 import os
 import subprocess
 
@@ -36,6 +37,14 @@ MUTANTS = {
     "gate_up_swapped": ("int up = r >= N;", "int up = r < N;", 1),
     "moe_x_row": ("int64_t xrow = x_per_slot ? sl : sl / top_k;", "int64_t xrow = x_per_slot ? sl : 0;", 1),
     "moe_global_scale": ("double g = (double)gs[e];", "double g = (double)gs[0];", 1),
+    "silu_sign": ("gc / (1.0 + exp(-gc))", "gc / (1.0 + exp(gc))", 1),
+    "silu_one_dropped": ("gc / (1.0 + exp(-gc))", "gc / exp(-gc)", 1),
+    "gate_clamp_dropped": ("double gc = gate > lim ? lim : (gate < -lim ? -lim : gate);", "double gc = gate;", 1),
+    "up_clamp_one_sided": ("double uc = up > lim ? lim : (up < -lim ? -lim : up);",
+                           "double uc = up > lim ? lim : up;", 1),
+    "swiglu_args_swapped": ("y[m * nrows + i] = nvfp4_oracle_swiglu(gv, uv, lim);",
+                            "y[m * nrows + i] = nvfp4_oracle_swiglu(uv, gv, lim);", 1),
+    "swiglu_up_scale": ("double gv = gg * sg_sum, uv = gu * su_sum;", "double gv = gg * sg_sum, uv = gg * su_sum;", 1),
 }
 
 
@@ -81,6 +90,23 @@ def battery(lib):
             if not np.all(np.abs(y[sl] - refm) <= 1e-12 * np.maximum(ya[sl], 1e-300)):
                 fails.append(f"moe(x_per_slot={xps})")
                 break
+    # the fused activation: closed forms of the logistic function, the clamp, and the hand-worked
+    # gate/up example (gate = ln 3, up = 1); see the pins of the same names
+    ln3 = math.log(3.0)
+    if not (math.isclose(oracle.swiglu(ln3, 1.0, lib=lib), 0.75 * ln3, rel_tol=1e-15) and
+            math.isclose(oracle.swiglu(-ln3, 1.0, lib=lib), -0.25 * ln3, rel_tol=1e-15)):
+        fails.append("silu_closed_form")
+    if not (oracle.swiglu(5.0, 1.0, 2.0, lib=lib) == oracle.swiglu(2.0, 1.0, lib=lib) and
+            oracle.swiglu(1.0, -9.0, 2.0, lib=lib) == oracle.swiglu(1.0, -2.0, lib=lib)):
+        fails.append("swiglu_clamp")
+    w1 = np.full((4, 8), 0x22, dtype=np.uint8)
+    s1 = np.full((4, 1), 0x38, dtype=np.uint8)
+    x1 = np.full((1, 16), 0x3F80, dtype=np.uint16)
+    y1, _ = oracle.gate_up_swiglu(w1, s1, ln3 / 16, w1, s1, 1.0 / 16, x1, lib=lib)
+    y2, _ = oracle.gate_up_swiglu(w1, s1, 1.0 / 16, w1, s1, ln3 / 16, x1, lib=lib)
+    if not (np.allclose(y1, 0.75 * ln3, rtol=1e-15, atol=0) and
+            np.allclose(y2, ln3 / (1.0 + math.exp(-1.0)), rtol=1e-15, atol=0)):
+        fails.append("gate_up_swiglu_hand_worked")
     return fails
 
 

@@ -277,3 +277,75 @@ def test_moe_out_of_range_ids_give_zero_rows():
     assert bad == 2
     assert np.all(y[1] == 0) and np.all(y[2] == 0)
     assert np.any(y[0] != 0) and np.any(y[3] != 0)
+
+
+# ---------------------------------------------------------------- fused gate/up activation
+# The swiglu_clamp and silu_mul nodes after the gate/up projection ("glm-5.3-flash-nvfp4-
+# tp3-512k--gb10 graph.json", block l0.mlp): silu(c(gate)) * c(up), c a clamp whose limit the
+# pages do not give (an argument here; +inf for none).
+
+LN3 = math.log(3.0)
+
+
+def test_silu_closed_forms():
+    # the logistic function is exactly 3/4 at ln 3 (exp(-ln 3) = 1/3) and 1/4 at -ln 3
+    assert oracle.swiglu(LN3, 1.0) == pytest.approx(0.75 * LN3, rel=1e-15)
+    assert oracle.swiglu(-LN3, 1.0) == pytest.approx(-0.25 * LN3, rel=1e-15)
+    assert oracle.swiglu(math.log(1.0 / 7.0), 2.0) == pytest.approx(2.0 * math.log(1.0 / 7.0) / 8.0, rel=1e-15)
+    assert oracle.swiglu(0.0, 5.0) == 0.0
+    # silu(v) tends to v for large v and to 0 for very negative v; its slope at 0 is 1/2
+    assert oracle.swiglu(40.0, 1.0) == pytest.approx(40.0, rel=1e-15)
+    assert abs(oracle.swiglu(-40.0, 1.0)) < 1e-15
+    assert oracle.swiglu(1e-6, 1.0) / 1e-6 == pytest.approx(0.5, rel=1e-5)
+
+
+def test_silu_odd_part_and_linearity_in_up():
+    rng = np.random.default_rng(5)
+    for v in rng.normal(0, 3, 40):
+        # silu(v) - silu(-v) = v (the logistic function satisfies s(v) + s(-v) = 1)
+        assert oracle.swiglu(v, 1.0) - oracle.swiglu(-v, 1.0) == pytest.approx(v, rel=1e-13, abs=1e-15)
+        u = rng.normal()
+        assert oracle.swiglu(v, 4.0 * u) == 4.0 * oracle.swiglu(v, u)  # power of two: exact
+
+
+def test_swiglu_clamp_saturates_both_inputs():
+    lim = 2.0
+    assert oracle.swiglu(5.0, 1.0, lim) == oracle.swiglu(2.0, 1.0)
+    assert oracle.swiglu(-5.0, 1.0, lim) == oracle.swiglu(-2.0, 1.0)
+    assert oracle.swiglu(1.0, 7.0, lim) == oracle.swiglu(1.0, 2.0)
+    assert oracle.swiglu(1.0, -9.0, lim) == oracle.swiglu(1.0, -2.0)
+    assert oracle.swiglu(1.5, -1.25, lim) == oracle.swiglu(1.5, -1.25)  # inside: untouched
+    assert math.isnan(oracle.swiglu(float("nan"), 1.0, lim))
+    assert math.isnan(oracle.swiglu(1.0, float("nan"), lim))
+
+
+def test_gate_up_swiglu_hand_worked():
+    # every code 1.0 (nibble 0x2) with scale 1.0 (0x38), K = 16 and x = 1: each dot product is
+    # 16, so gg = ln 3 / 16 gives gate = ln 3, gu = 1 / 16 gives up = 1, and y = (3/4) ln 3
+    N, K = 4, 16
+    w = np.full((N, K // 2), 0x22, dtype=np.uint8)
+    s = np.full((N, K // 16), 0x38, dtype=np.uint8)
+    x = np.full((2, K), 0x3F80, dtype=np.uint16)
+    y, aux = oracle.gate_up_swiglu(w, s, LN3 / 16, w, s, 1.0 / 16, x)
+    assert y.shape == (2, N)
+    assert np.allclose(y, 0.75 * LN3, rtol=1e-15, atol=0)
+    assert np.allclose(aux["gate"], LN3, rtol=1e-15, atol=0) and np.all(aux["up"] == 1.0)
+    assert np.allclose(aux["gate_abs"], LN3, rtol=1e-15, atol=0) and np.all(aux["up_abs"] == 1.0)
+
+
+@pytest.mark.parametrize("lim", [float("inf"), 0.05])
+def test_gate_up_swiglu_is_the_activation_of_gate_up(lim):
+    p = synth.gate_up_problem(24, 64, 3, 54)
+    wg, sg, wu, su = (p[k].numpy() for k in ("wg", "sg", "wu", "su"))
+    x = synth.bf16_bits(p["x"])
+    y, aux = oracle.gate_up_swiglu(wg, sg, p["gg"], wu, su, p["gu"], x, lim)
+    yg, ya = oracle.gemv_gate_up(wg, sg, p["gg"], wu, su, p["gu"], x)
+    assert np.array_equal(aux["gate"], yg[:, :24]) and np.array_equal(aux["up"], yg[:, 24:])
+    assert np.array_equal(aux["gate_abs"], ya[:, :24]) and np.array_equal(aux["up_abs"], ya[:, 24:])
+    ref = np.array([[oracle.swiglu(g, u, lim) for g, u in zip(gr, ur)] for gr, ur in zip(yg[:, :24], yg[:, 24:])])
+    assert np.array_equal(y, ref)
+    if lim < 1:  # the limit is active for part of the outputs
+        assert np.any(np.abs(yg) > lim)
+    rows = [23, 0, 7]
+    ys, _ = oracle.gate_up_swiglu(wg, sg, p["gg"], wu, su, p["gu"], x, lim, rows=rows)
+    assert np.array_equal(ys, y[:, rows])
