@@ -1331,6 +1331,82 @@ __device__ bool stage_x_direct(const uint16_t* __restrict__ x, const int* rowsel
     return ok;
 }
 
+#ifndef NVFP4_STAGE_BULK
+#define NVFP4_STAGE_BULK 0  // 1: x arrives by bulk copies and is converted in place (not yet validated on a GPU)
+#endif
+
+// stage_x_direct with the slice's rows brought in by bulk copies: lane 0 of the slice's first
+// warp copies each row's K range (raw bf16, kn * 2 bytes) to its place in the staged buffer,
+// completing on the mbarrier `bar` (8 bytes of shared scratch, initialised here). Every
+// 256-byte block (128 elements) is then converted in place by half a warp: its sixteen
+// 16-byte chunks, raw chunk 4t + q holding elements 32t + 8q .. + 7, move to position 4q + t
+// (the mma_x_off order) as f16, with the same exactness check and slice vote. One L2 round
+// trip for the whole slice instead of one per batch of loads. A wait that runs out (budget)
+// sets NVFP4_DEV_TIMEOUT, drains the copy and reports the slice inexact, so the caller
+// re-stages it from global memory. Needs 16-byte aligned x rows and k0 and kn multiples of 128.
+__device__ bool stage_x_bulk(const uint16_t* __restrict__ x, const int* rowsel, int M, int K, int k0, int kn,
+                             uint8_t* xs, uint32_t sstride, uint32_t* vote, uint64_t* bar, int gi, int gw,
+                             int bar_id, int lane, uint64_t budget) {
+    if (gi == 0 && lane == 0) {
+        mbar_init(bar, 1);
+        fence_barrier_init();
+        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(M) * static_cast<uint32_t>(kn) * 2u);
+        for (int m = 0; m < M; ++m)
+            bulk_g2s(xs + m * sstride, x + static_cast<int64_t>(rowsel ? rowsel[m] : m) * K + k0,
+                     static_cast<uint32_t>(kn) * 2u, bar);
+    }
+    if (bar_id >= 0) named_bar_sync(bar_id, gw * 32);  // the barrier is initialised before any wait
+    else __syncwarp();
+    uint32_t bad = 0u;
+    bool landed = true;  // warp-uniform
+    if (!__all_sync(0xffffffffu, budget != 0 && mbar_wait(bar, 0u, budget))) {
+        if (lane == 0) {
+            raise_status(NVFP4_DEV_TIMEOUT, nullptr);
+            mbar_wait(bar, 0u, kDrainWaitNs);  // the copy must not land after the re-staging
+        }
+        __syncwarp();
+        bad = 1u;
+        landed = false;
+    }
+    const int bpr = kn >> 7;  // 128-element blocks per row
+    const int nblk = M * bpr;
+    const int half = lane >> 4, pos = lane & 15;
+    const int t = pos >> 2, q = pos & 3;
+    // the trip count must not depend on the lane: the loop body holds a __syncwarp
+    for (int b0 = gi * 2; landed && b0 < nblk; b0 += gw * 2) {
+        const int b = b0 + half;
+        uint8_t* blk = nullptr;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (b < nblk) {
+            const int m = b / bpr;
+            blk = xs + m * sstride + (b - m * bpr) * 256;
+            v = *reinterpret_cast<const uint4*>(blk + pos * 16);
+        }
+        __syncwarp();  // every chunk of the block is read before any is overwritten
+        if (b < nblk) {
+            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+            uint32_t out[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t mag = w4[i] & 0x7fff7fffu;
+                bad |= (__vcmpltu2(mag, 0x37003700u) & ~__vcmpeq2(mag, 0u)) | __vcmpgeu2(mag, 0x47804780u);
+                const __half2 h = __floats2half2_rn(bf16_lo(w4[i]), bf16_hi(w4[i]));
+                out[i] = *reinterpret_cast<const uint32_t*>(&h);
+            }
+            *reinterpret_cast<uint4*>(blk + (q * 4 + t) * 16) = make_uint4(out[0], out[1], out[2], out[3]);
+        }
+    }
+    bool ok = !__any_sync(0xffffffffu, bad != 0u);
+    if (bar_id >= 0) {
+        if (lane == 0) vote[gi] = ok ? 1u : 0u;
+        named_bar_sync(bar_id, gw * 32);
+        for (int w = 0; w < gw; ++w) ok = ok && vote[w] != 0u;
+    } else {
+        __syncwarp();
+    }
+    return ok;
+}
+
 // Stages x[:, k0 : k0 + kn] for the warps of one K slice (gw warps; this one is number gi
 // of them) in f16 for the tensor cores: rows `sstride` bytes apart at xs, elements at
 // mma_x_off. The slice gets one power of two, x' = x * 2^-E with its largest |x| in
@@ -1746,8 +1822,16 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_kernel(const __grid
     const int xbar = p.tpi > 1 ? 2 + kslice : -1;
     bool lossy = false;
     float e2v = 1.f;
-    if (M > 0 && !stage_x_direct(p.x, rowsel, M, p.K, k0, kn, xs, p.sstride, gmax + 16, tin, p.tpi, xbar, lane,
-                                 [] {})) {
+    bool staged = M == 0;
+    if (M > 0) {
+        if (NVFP4_STAGE_BULK)
+            staged = stage_x_bulk(p.x, rowsel, M, p.K, k0, kn, xs, p.sstride, gmax + 16,
+                                  reinterpret_cast<uint64_t*>(gmax + 24), tin, p.tpi, xbar, lane, p.wait_ns);
+        else
+            staged = stage_x_direct(p.x, rowsel, M, p.K, k0, kn, xs, p.sstride, gmax + 16, tin, p.tpi, xbar, lane,
+                                    [] {});
+    }
+    if (!staged) {
         lossy = stage_x_slice(p.x, rowsel, M, p.K, k0, kn, xs, p.sstride, e2, gmax, tin, p.tpi, xbar, lane);
         e2v = e2[0];
     }
@@ -2106,8 +2190,16 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_sk_kernel(const __g
     uint32_t* const gmax = reinterpret_cast<uint32_t*>(sbase + p.misc_off + tk::kWarps * 32);
     bool lossy = false;
     float e2v = 1.f;
-    if (M > 0 && !stage_x_direct(p.x, rowsel, M, p.K, 0, p.K, xs, p.sstride, gmax + 16, warp, tk::kWarps, 2, lane,
-                                 [] {})) {
+    bool staged = M == 0;
+    if (M > 0) {
+        if (NVFP4_STAGE_BULK)
+            staged = stage_x_bulk(p.x, rowsel, M, p.K, 0, p.K, xs, p.sstride, gmax + 16,
+                                  reinterpret_cast<uint64_t*>(gmax + 24), warp, tk::kWarps, 2, lane, p.wait_ns);
+        else
+            staged = stage_x_direct(p.x, rowsel, M, p.K, 0, p.K, xs, p.sstride, gmax + 16, warp, tk::kWarps, 2,
+                                    lane, [] {});
+    }
+    if (!staged) {
         lossy = stage_x_slice(p.x, rowsel, M, p.K, 0, p.K, xs, p.sstride, e2, gmax, warp, tk::kWarps, 2, lane);
         e2v = e2[0];
     }
