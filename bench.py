@@ -121,6 +121,23 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(x: float, device="cpu") -> float:
+    """The largest x over all ranks (a job takes as long as its slowest replica), followed by a
+    barrier; x itself when no process group is running."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.barrier()
+    return float(t.item())
+
+
+def job_gbps(ws: int, bytes_per_step: float, ms_per_step: float) -> float:
+    """Whole-job throughput: every replica streams bytes_per_step per step (weak scaling)."""
+    return ws * bytes_per_step / (ms_per_step * 1e-3) / 1e9
+
+
 class ClockSampler:
     """nvidia-smi samples of SM clock and throttle reasons while the bench runs."""
 
@@ -504,17 +521,13 @@ def run_ours(args):
         region_ms, host_s, gate_meas = timed_region(calls, copies, args.steps, gate_ms * 1e3 * sm_mhz_guess, stream)
     torch.cuda.synchronize()
     t_wall1 = time.time()
-    if ws > 1:
-        t = torch.tensor([region_ms], device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        region_ms = float(t.item())
-        torch.distributed.barrier()
+    region_ms = max_over_ranks(region_ms, device)
     per_call = per_call_region(calls, copies, min(args.steps, 100), gate_ms * 2e3 * sm_mhz_guess, stream)
 
     ms_per_step = region_ms / args.steps
     wbytes_step = sum(np.mean([c.weight_bytes(k % copies) for k in range(min(copies, args.steps))])
                       for c in calls)
-    value = ws * wbytes_step / (ms_per_step * 1e-3) / 1e9
+    value = job_gbps(ws, wbytes_step, ms_per_step)
 
     peak, peak_kind = measured_peaks()
     call_rows = []
@@ -553,12 +566,14 @@ def run_ours(args):
                       "through the public API, D2H of y), replayed and synchronised every step")
     except Exception as exc:  # capture unavailable: report the eager loop alone
         e2e_ms, e2e_method = e2e_eager_ms, f"eager Python loop (graph capture failed: {exc})"
-    e2e = {"value": round(ws * wbytes_step / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s (NVFP4 weight bytes)",
+    e2e_ms = max_over_ranks(e2e_ms, device)
+    e2e_eager_ms = max_over_ranks(e2e_eager_ms, device)
+    e2e = {"value": round(job_gbps(ws, wbytes_step, e2e_ms), 2), "unit": "GB/s (NVFP4 weight bytes)",
            "ms_per_step": round(e2e_ms, 4),
            "h2d_bytes_per_step": int(sum(c.x_bytes() for c in calls)),
            "d2h_bytes_per_step": int(sum(c.y_bytes() for c in calls)),
            "method": e2e_method,
-           "eager": {"value": round(ws * wbytes_step / (e2e_eager_ms * 1e-3) / 1e9, 2),
+           "eager": {"value": round(job_gbps(ws, wbytes_step, e2e_eager_ms), 2),
                      "ms_per_step": round(e2e_eager_ms, 4),
                      "method": "every copy and call issued from Python each step, then a synchronize"}}
 

@@ -1,0 +1,80 @@
+"""Host logic of bench.py that needs no GPU: the multi-rank reduction (two gloo ranks on the
+CPU), the whole-job throughput, the reference arm's rank rule and the traffic record."""
+import json
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        local = 3.0 + 4.0 * rank          # rank 1 is the slow replica
+        got = bench.max_over_ranks(local)
+        out[rank] = got
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_two_gloo_ranks():
+    ctx = mp.get_context("spawn")
+    with ctx.Manager() as mgr:
+        out = mgr.dict()
+        port = _free_port()
+        procs = [ctx.Process(target=_rank_main, args=(r, 2, port, out)) for r in range(2)]
+        for p in procs:
+            p.start()
+        for p in procs:
+            p.join(120)
+            assert p.exitcode == 0
+        assert dict(out) == {0: 7.0, 1: 7.0}
+
+
+def test_max_over_ranks_without_a_group_is_identity():
+    assert not dist.is_initialized()
+    assert bench.max_over_ranks(2.5) == 2.5
+
+
+def test_job_throughput_is_weak_scaling():
+    one = bench.job_gbps(1, 9.45e6, 0.005)
+    assert one == pytest.approx(1890.0)
+    assert bench.job_gbps(4, 9.45e6, 0.005) == pytest.approx(4 * one)
+
+
+def test_reference_arm_runs_on_rank_zero_only(monkeypatch, capsys):
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setenv("LOCAL_RANK", "1")
+    assert bench.main(["--impl", "reference", "--steps", "1", "--warmup", "3"]) == 0
+    assert capsys.readouterr().out == ""
+
+
+def test_traffic_record_matches_the_kernel_source(monkeypatch):
+    rec = json.load(open(os.path.join(bench.ROOT, "profiles", "traffic.json")))
+    assert rec["kernel_source_sha256"] == bench.kernel_source_sha256()
+    assert bench.kernel_traffic("attn") == rec["dram_bytes_per_launch"]["attn"]
+    monkeypatch.setattr(bench, "kernel_source_sha256", lambda: "0" * 64)
+    assert bench.kernel_traffic("attn") is None
+
+
+def test_workload_byte_accounting():
+    # the fused call reads both weights and writes [M, N]; gate_up writes [M, 2N]
+    calls = {k: bench.Call(spec, "cpu", 1, "cpu") for k, spec in
+             (("sw", ("gate_up_swiglu", 64, 256, 2, 5, "bf16")), ("gu", ("gate_up", 64, 256, 2, 5, "f32")))}
+    per_row = 256 * 0.5 + 256 / 16
+    assert calls["sw"].weight_bytes() == calls["gu"].weight_bytes() == 2 * 64 * per_row
+    assert calls["sw"].alg_bytes() == 2 * 64 * per_row + 2 * 256 * 2 + 2 * 64 * 2
+    assert calls["gu"].alg_bytes() == 2 * 64 * per_row + 2 * 256 * 2 + 2 * 128 * 4
