@@ -192,6 +192,16 @@ void nvfp4_set_pdl(int enable);
  */
 int nvfp4_describe_plan(int kind, int M, int N, int K, int T, int top_k, char* buf, int buflen);
 
+/*
+ * nvfp4_describe_plan for a described device instead of the current one: sm_count SMs,
+ * smem_optin bytes of shared memory a CTA may opt into, smem_per_sm bytes per SM. It runs the
+ * planner on the host only (no GPU or driver needed) and assumes the tile kernel's TMA
+ * tensor-map encoder is available. Returns the number of characters, or -1 for a bad
+ * argument (kind outside 0..4, sizes < 1, smem_per_sm < smem_optin).
+ */
+int nvfp4_describe_plan_host(int sm_count, int smem_optin, int smem_per_sm, int kind, int M, int N, int K,
+                             int T, int top_k, char* buf, int buflen);
+
 /* Library version: major * 10000 + minor * 100 + patch. */
 int nvfp4_version(void);
 

@@ -22,7 +22,7 @@ import torch
 from . import build as _build
 
 __all__ = ["gemv", "gemv_gate_up", "gemv_gate_up_swiglu", "moe_gemv", "device_status", "set_wait_budget_ns",
-           "set_variant", "set_pdl", "fp32_fallbacks", "describe_plan", "library", "library_path", "NVFP4Error",
+           "set_variant", "set_pdl", "fp32_fallbacks", "describe_plan", "describe_plan_host", "library", "library_path", "NVFP4Error",
            "OUT_F32", "OUT_BF16", "DEV_TIMEOUT", "DEV_BAD_EXPERT"]
 
 OUT_F32 = 0
@@ -74,6 +74,8 @@ def _declare(lib):
     lib.nvfp4_fp32_fallbacks.restype = ctypes.c_longlong
     lib.nvfp4_describe_plan.argtypes = [i32, i32, i32, i32, i32, i32, ctypes.c_char_p, i32]
     lib.nvfp4_describe_plan.restype = i32
+    lib.nvfp4_describe_plan_host.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32, i32, ctypes.c_char_p, i32]
+    lib.nvfp4_describe_plan_host.restype = i32
     lib.nvfp4_version.argtypes = []
     lib.nvfp4_version.restype = i32
     return lib
@@ -289,4 +291,15 @@ def describe_plan(kind: str, M: int, N: int, K: int, T: int = 0, top_k: int = 0)
     n = library().nvfp4_describe_plan(code, M, N, K, T, top_k, buf, 256)
     if n < 0:
         raise RuntimeError("describe_plan failed (no CUDA device?)")
+    return buf.value.decode()
+
+
+def describe_plan_host(kind: str, M: int, N: int, K: int, T: int = 0, top_k: int = 0, sm_count: int = 152,
+                       smem_optin: int = 232448, smem_per_sm: int = 233472) -> str:
+    """describe_plan for a described device (defaults: GB300), run on the host only: no GPU needed."""
+    code = {"dense": 0, "gate_up": 1, "moe": 2, "moe_per_slot": 3, "gate_up_swiglu": 4}[kind]
+    buf = ctypes.create_string_buffer(256)
+    n = library().nvfp4_describe_plan_host(sm_count, smem_optin, smem_per_sm, code, M, N, K, T, top_k, buf, 256)
+    if n < 0:
+        raise ValueError("describe_plan_host: bad arguments")
     return buf.value.decode()

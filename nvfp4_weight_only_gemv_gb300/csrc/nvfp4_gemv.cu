@@ -2840,7 +2840,7 @@ struct TilePlan {
 // SM times the steps each of its warps decodes), both in units of one warp step.
 bool plan_tile(TilePlan& tp, int M, int N, int K, int groups, const DeviceInfo& d, const uint8_t* const* w,
                const uint8_t* const* s, const void* x, bool moe = false, int moe_rows = 0, int moe_groups_max = 0,
-               bool swiglu = false) {
+               bool swiglu = false, bool need_encoder = true) {
     if (g_variant == 1 || g_variant == 3) return false;
     if (K <= 0 || K % 256 != 0 || M < 1 || M > 8 || N < 1 || N > (1 << 27)) return false;
     // MoE: M is the largest number of columns of a group (8), groups the expected number of
@@ -2850,7 +2850,7 @@ bool plan_tile(TilePlan& tp, int M, int N, int K, int groups, const DeviceInfo& 
     const int tensors = moe ? 1 : groups;  // weight tensors: one for all experts, else one per group
     for (int i = 0; i < tensors; ++i)
         if ((reinterpret_cast<uintptr_t>(w[i]) & 15) || (reinterpret_cast<uintptr_t>(s[i]) & 15)) return false;
-    if (!tensor_map_encoder()) return false;
+    if (need_encoder && !tensor_map_encoder()) return false;
     const int segs = K / 256;
     // gate/up with the fused activation: one group of 2 * tiles, gate and up tiles alternating,
     // so that an item (an even number of tiles) holds whole pairs
@@ -3391,10 +3391,14 @@ long long nvfp4_fp32_fallbacks(void* stream) {
     return static_cast<long long>(v);
 }
 
-int nvfp4_describe_plan(int kind, int M, int N, int K, int T, int top_k, char* buf, int buflen) {
-    if (!buf || buflen < 1) return -1;
-    const DeviceInfo* d = device_info(nullptr);
-    if (!d) return -1;
+}  // extern "C"
+
+namespace nvfp4 {
+
+// The launch a call would make on device d; host_only: the tile kernel's tensor-map encoder
+// (a driver entry point) is assumed present, so no GPU or driver is needed.
+int describe_plan_on(const DeviceInfo* d, bool host_only, int kind, int M, int N, int K, int T, int top_k,
+                     char* buf, int buflen) {
     Plan pl{};
     bool ok = false;
     // Pointers are only inspected for alignment here; 256-byte aligned stand-ins.
@@ -3402,7 +3406,7 @@ int nvfp4_describe_plan(int kind, int M, int N, int K, int T, int top_k, char* b
     const uint8_t* w[2] = {fake, fake};
     if (kind == 4) {  // gate/up with the fused activation: the tile kernel, else the byte-load kernel
         TilePlan tpl{};
-        if (plan_tile(tpl, M, N, K, 2, *d, w, w, fake, false, 0, 0, true))
+        if (plan_tile(tpl, M, N, K, 2, *d, w, w, fake, false, 0, 0, true, !host_only))
             return snprintf(buf, buflen,
                             "tile_swiglu grid=%d block=%d smem=%u split=%d rows_per_item=%d k_warps=%d mt=%d stages=%d nc=%d",
                             tpl.grid_x * tpl.grid_y, tk::kThreads, tpl.smem, 1 << tpl.p.s_log2, tpl.p.tpi * 16,
@@ -3412,7 +3416,7 @@ int nvfp4_describe_plan(int kind, int M, int N, int K, int T, int top_k, char* b
     }
     if (kind == 0 || kind == 1) {
         TilePlan tpl{};
-        if (plan_tile(tpl, M, N, K, kind == 0 ? 1 : 2, *d, w, w, fake)) {
+        if (plan_tile(tpl, M, N, K, kind == 0 ? 1 : 2, *d, w, w, fake, false, 0, 0, false, !host_only)) {
             return snprintf(buf, buflen,
                             "tile grid=%d block=%d smem=%u split=%d rows_per_item=%d k_warps=%d mt=%d stages=%d nc=%d",
                             tpl.grid_x * tpl.grid_y, tk::kThreads, tpl.smem, 1 << tpl.p.s_log2, tpl.p.tpi * 16,
@@ -3427,7 +3431,8 @@ int nvfp4_describe_plan(int kind, int M, int N, int K, int T, int top_k, char* b
         const int slots = T * top_k, E = M;
         const int xrows = kind == 3 ? slots : T;
         if (slots <= kTileMoeSlots && E >= 1 && static_cast<int64_t>(E) * N <= (1 << 30) &&
-            plan_tile(tpl, 8, N, K, expected_groups(E, T, top_k), *d, w, w, fake, true, xrows, slots)) {
+            plan_tile(tpl, 8, N, K, expected_groups(E, T, top_k), *d, w, w, fake, true, xrows, slots, false,
+                      !host_only)) {
             return snprintf(buf, buflen,
                             "%s grid=%d block=%d smem=%u split=1 rows_per_item=%d k_warps=%d mt=8 stages=%d nc=%d",
                             tpl.sk ? "tile_sk_moe" : "tile_moe", tpl.grid_x, tk::kThreads, tpl.smem, tpl.p.tpi * 16, 1 << tpl.p.ksplit_log2, tpl.p.stages,
@@ -3446,6 +3451,29 @@ int nvfp4_describe_plan(int kind, int M, int N, int K, int T, int top_k, char* b
                      pl.p.ck, pl.mt, pl.p.stages);
     }
     return n;
+}
+
+}  // namespace nvfp4
+
+extern "C" {
+
+int nvfp4_describe_plan(int kind, int M, int N, int K, int T, int top_k, char* buf, int buflen) {
+    if (!buf || buflen < 1) return -1;
+    const DeviceInfo* d = device_info(nullptr);
+    if (!d) return -1;
+    return describe_plan_on(d, false, kind, M, N, K, T, top_k, buf, buflen);
+}
+
+int nvfp4_describe_plan_host(int sm_count, int smem_optin, int smem_per_sm, int kind, int M, int N, int K, int T,
+                             int top_k, char* buf, int buflen) {
+    if (!buf || buflen < 1 || sm_count < 1 || smem_optin < 1 || smem_per_sm < smem_optin) return -1;
+    if (kind < 0 || kind > 4) return -1;
+    DeviceInfo d;
+    d.sm_count = sm_count;
+    d.smem_optin = smem_optin;
+    d.smem_per_sm = smem_per_sm;
+    d.init = true;
+    return describe_plan_on(&d, true, kind, M, N, K, T, top_k, buf, buflen);
 }
 
 int nvfp4_version(void) { return 100; }
