@@ -444,46 +444,6 @@ def test_cuda_graph_capture_and_replay():
     assert_parity(y, yr, ya, "graph replay")
 
 
-def test_graph_of_a_step_with_host_copies():
-    # one captured step: pinned x -> device, a fused gate/up + SwiGLU call and a MoE call
-    # (PDL-chained), y -> pinned host; replayed with new host inputs each time
-    q = synth.gate_up_problem(512, 1024, 2, 323, device=DEV)
-    r = synth.moe_problem(16, 256, 512, 2, 4, True, seed=324, device=DEV, fill="all")
-    hx1 = torch.empty(2, 1024, dtype=torch.bfloat16).pin_memory()
-    hx2 = torch.empty(8, 512, dtype=torch.bfloat16).pin_memory()
-    hy1 = torch.empty(2, 512, dtype=torch.bfloat16).pin_memory()
-    hy2 = torch.empty(8, 256).pin_memory()
-    dx1, dx2 = torch.empty(2, 1024, dtype=torch.bfloat16, device=DEV), torch.empty(8, 512, dtype=torch.bfloat16, device=DEV)
-    y1, y2 = torch.empty(2, 512, dtype=torch.bfloat16, device=DEV), torch.empty(8, 256, device=DEV)
-
-    def step():
-        dx1.copy_(hx1, non_blocking=True)
-        dx2.copy_(hx2, non_blocking=True)
-        nv.gemv_gate_up_swiglu(q["wg"], q["sg"], q["gg"], q["wu"], q["su"], q["gu"], dx1, 0.5, out=y1)
-        nv.moe_gemv(r["w"], r["s"], r["gs"], r["ids"], dx2, True, 4, out=y2)
-        hy1.copy_(y1, non_blocking=True)
-        hy2.copy_(y2, non_blocking=True)
-
-    step()  # warm-up outside capture
-    torch.cuda.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
-        step()
-    for seed in (325, 326):
-        x1 = synth.random_x(2, 1024, seed)
-        x2 = synth.random_x(8, 512, seed + 100)
-        hx1.copy_(x1)
-        hx2.copy_(x2)
-        graph.replay()
-        torch.cuda.synchronize()
-        yr, aux = oracle.gate_up_swiglu(host(q["wg"]), host(q["sg"]), q["gg"], host(q["wu"]), host(q["su"]),
-                                        q["gu"], synth.bf16_bits(x1), 0.5)
-        assert_swiglu_parity(hy1, yr, aux, 0.5, "graph swiglu")
-        ym, ya, _ = oracle.moe_gemv(host(r["w"]), host(r["s"]), host(r["gs"]), host(r["ids"]),
-                                    synth.bf16_bits(x2), True, 4)
-        assert_parity(hy2, ym, ya, "graph moe")
-
-
 def test_side_stream_launch():
     p = synth.dense_problem(1024, 2048, 3, 322, device=DEV)
     s = torch.cuda.Stream()
@@ -616,3 +576,43 @@ def test_swiglu_nan_scale_and_empty_inputs():
     assert torch.all(y0 == 0)
     assert nv.describe_plan("gate_up_swiglu", 1, 12288, 4096).startswith("tile_swiglu ")
     assert nv.describe_plan("gate_up_swiglu", 1, 100, 528).startswith("simple ")
+
+
+def test_graph_of_a_step_with_host_copies():
+    # one captured step: pinned x -> device, a fused gate/up + SwiGLU call and a MoE call
+    # (PDL-chained), y -> pinned host; replayed with new host inputs each time
+    q = synth.gate_up_problem(512, 1024, 2, 323, device=DEV)
+    r = synth.moe_problem(16, 256, 512, 2, 4, True, seed=324, device=DEV, fill="all")
+    hx1 = torch.empty(2, 1024, dtype=torch.bfloat16).pin_memory()
+    hx2 = torch.empty(8, 512, dtype=torch.bfloat16).pin_memory()
+    hy1 = torch.empty(2, 512, dtype=torch.bfloat16).pin_memory()
+    hy2 = torch.empty(8, 256).pin_memory()
+    dx1, dx2 = torch.empty(2, 1024, dtype=torch.bfloat16, device=DEV), torch.empty(8, 512, dtype=torch.bfloat16, device=DEV)
+    y1, y2 = torch.empty(2, 512, dtype=torch.bfloat16, device=DEV), torch.empty(8, 256, device=DEV)
+
+    def step():
+        dx1.copy_(hx1, non_blocking=True)
+        dx2.copy_(hx2, non_blocking=True)
+        nv.gemv_gate_up_swiglu(q["wg"], q["sg"], q["gg"], q["wu"], q["su"], q["gu"], dx1, 0.5, out=y1)
+        nv.moe_gemv(r["w"], r["s"], r["gs"], r["ids"], dx2, True, 4, out=y2)
+        hy1.copy_(y1, non_blocking=True)
+        hy2.copy_(y2, non_blocking=True)
+
+    step()  # warm-up outside capture
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for seed in (325, 326):
+        x1 = synth.random_x(2, 1024, seed)
+        x2 = synth.random_x(8, 512, seed + 100)
+        hx1.copy_(x1)
+        hx2.copy_(x2)
+        graph.replay()
+        torch.cuda.synchronize()
+        yr, aux = oracle.gate_up_swiglu(host(q["wg"]), host(q["sg"]), q["gg"], host(q["wu"]), host(q["su"]),
+                                        q["gu"], synth.bf16_bits(x1), 0.5)
+        assert_swiglu_parity(hy1, yr, aux, 0.5, "graph swiglu")
+        ym, ya, _ = oracle.moe_gemv(host(r["w"]), host(r["s"]), host(r["gs"]), host(r["ids"]),
+                                    synth.bf16_bits(x2), True, 4)
+        assert_parity(hy2, ym, ya, "graph moe")
