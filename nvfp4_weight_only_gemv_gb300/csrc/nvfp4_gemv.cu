@@ -1422,7 +1422,6 @@ __device__ bool stage_x_slice(const uint16_t* __restrict__ x, const int* rowsel,
                               int lane) {
     constexpr int kPre = NVFP4_STAGE_PRE;
     const int cpr = kn >> 3;                      // 16-byte chunks per row of the slice
-    const int total = M * cpr;
     const int tl = gi * 32 + lane, nt = gw * 32;  // this lane among the slice's lanes
     int m0 = 0, c0 = tl;                          // flat chunk tl as (row, chunk)
     while (c0 >= cpr) {
