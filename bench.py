@@ -96,6 +96,25 @@ def kernel_traffic(workload):
         return None
 
 
+def run_env(device):
+    """What a result was measured on: GPU, SMs, CUDA, torch, the kernel source's hash and the git
+    commit when the tree has one."""
+    env = {"kernel_source_sha256": kernel_source_sha256()}
+    try:
+        props = torch.cuda.get_device_properties(device)
+        env.update(gpu=props.name, sm_count=props.multi_processor_count,
+                   cc=f"{props.major}.{props.minor}", cuda=torch.version.cuda, torch=torch.__version__)
+    except Exception:  # no device: the reference arm on a CPU-only host
+        env.update(torch=torch.__version__)
+    try:
+        sha = subprocess.run(["git", "-C", ROOT, "rev-parse", "HEAD"], capture_output=True, text=True,
+                             timeout=10).stdout.strip()
+        env["git_sha"] = sha or None
+    except Exception:
+        env["git_sha"] = None
+    return env
+
+
 def kernels_of(calls):
     """Names of the library kernels the step's calls launch (from the library's own plan)."""
     import nvfp4_weight_only_gemv_gb300 as nv
@@ -479,7 +498,8 @@ def run_reference(args):
             "cpu_baseline": {"value": value, "unit": "GB/s (NVFP4 weight bytes)", "cores": oracle.threads(),
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "GB/s (NVFP4 weight bytes)", "h2d_bytes_per_step": 0,
-                    "d2h_bytes_per_step": 0}}
+                    "d2h_bytes_per_step": 0},
+            "env": run_env(None)}
     print(json.dumps(line))
     return 0
 
@@ -589,7 +609,7 @@ def run_ours(args):
                 "config": {"workload": f"{args.workload}: {desc}", "parallelism": f"replicas x{ws}",
                            "l2": l2_note, "calls_per_step": len(calls)},
                 "calls": call_rows, "roofline": roofline, "cpu_baseline": base, "e2e": e2e,
-                "gpu_launches": args.steps * len(calls), "clocks": clocks,
+                "gpu_launches": args.steps * len(calls), "clocks": clocks, "env": run_env(device),
                 "timing": {"gate_ms": round(gate_meas, 3), "host_enqueue_ms": round(host_s * 1e3, 3),
                            "method": "timed region: steps back to back behind a sleep kernel, events at "
                                      "both ends; calls[].us_isolated: separate pass, events around "
