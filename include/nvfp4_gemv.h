@@ -159,6 +159,8 @@ void nvfp4_set_wait_budget_ns(uint64_t ns);
  * kernel, 2 = automatic kernel with the exact fp32 x path forced (the path a CTA takes
  * when x cannot be staged exactly in f16), 3 = the bulk-copy streaming kernel even where
  * the warp-tile kernel applies. Used by tests to check every path against the oracle.
+ * The environment variable NVFP4_GEMV_FORCE_VARIANT (0..3) sets the value the library starts
+ * with; anything else there is ignored.
  */
 void nvfp4_set_variant(int variant);
 

@@ -36,6 +36,7 @@
 
 #include <cstdint>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <algorithm>
 #include <mutex>
@@ -2521,7 +2522,16 @@ struct DeviceInfo {
 std::mutex g_mu;
 DeviceInfo g_dev[64];
 uint64_t g_wait_ns = kDefaultWaitNs;
-int g_variant = 0;
+// Kernel selection; NVFP4_GEMV_FORCE_VARIANT=0..3 in the environment sets the initial value
+// (for tests and benchmarks), nvfp4_set_variant changes it.
+int initial_variant() {
+    const char* v = std::getenv("NVFP4_GEMV_FORCE_VARIANT");
+    if (!v || !*v) return 0;
+    char* end = nullptr;
+    const long n = std::strtol(v, &end, 10);
+    return (end && *end == '\0' && n >= 0 && n <= 3) ? static_cast<int>(n) : 0;
+}
+int g_variant = initial_variant();
 int g_last_cuda_error = 0;
 
 const DeviceInfo* device_info(int* dev_out) {

@@ -83,3 +83,17 @@ def test_bad_descriptions_are_rejected():
         nv.describe_plan_host("dense", 1, 256, 512, sm_count=0)
     with pytest.raises(ValueError):
         nv.describe_plan_host("dense", 1, 256, 512, smem_optin=4096, smem_per_sm=1024)
+
+
+@pytest.mark.parametrize("value,kernel", [("3", "stream"), ("1", "simple"), ("0", "tile"), ("7", "tile"),
+                                          ("x", "tile")])
+def test_force_variant_environment(value, kernel):
+    # NVFP4_GEMV_FORCE_VARIANT sets the library's starting kernel selection (0..3, else ignored)
+    import subprocess
+    import sys
+    code = ("import nvfp4_weight_only_gemv_gb300 as nv; "
+            "print(nv.describe_plan_host('dense', 1, 4096, 4096).split()[0])")
+    env = dict(__import__("os").environ, NVFP4_GEMV_FORCE_VARIANT=value)
+    out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=300)
+    assert out.returncode == 0, out.stderr
+    assert out.stdout.strip() == kernel
