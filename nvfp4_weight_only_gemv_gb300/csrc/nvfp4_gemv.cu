@@ -1179,7 +1179,7 @@ struct TileParams {
     int64_t ldy;              // y row stride in elements
     int out_bf16;
     int M, N, K;
-    int tiles;                // 16-row tiles per group
+    int tiles;                // 16-row tiles per group (fused gate/up: 2 per output tile, gate then up)
     int ksplit_log2;          // warps sharing one tile (K slices) = 1 << ksplit_log2
     int tpi;                  // tiles per item (= kWarps / ksplit)
     int ipg;                  // items per group
