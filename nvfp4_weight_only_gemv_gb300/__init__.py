@@ -133,6 +133,14 @@ def _need(t: torch.Tensor, name: str, dtype, ndim: int):
         raise ValueError(f"{name} must be contiguous")
 
 
+def _one_device(*tensors):
+    """The kernels run on the current CUDA device and read every operand there."""
+    dev = torch.cuda.current_device()
+    for t in tensors:
+        if t is not None and t.device.index != dev:
+            raise ValueError(f"every tensor must be on the current CUDA device cuda:{dev} (got {t.device})")
+
+
 def _out(out, shape, out_dtype, device):
     """The output tensor: ``out`` when given (its own dtype wins), else a new one."""
     if out is None:
@@ -168,6 +176,7 @@ def gemv(w: torch.Tensor, s: torch.Tensor, g: float, x: torch.Tensor, out=None,
     if tuple(s.shape) != (N, K // 16) or x.shape[1] != K:
         raise ValueError(f"shape mismatch: w {tuple(w.shape)}, s {tuple(s.shape)}, x {tuple(x.shape)}")
     y = _out(out, (M, N), out_dtype, x.device)
+    _one_device(w, s, x, y)
     st = library().nvfp4_gemv(_ptr(w), _ptr(s), float(g), _ptr(x), _ptr(y), _out_code(y.dtype),
                               M, N, K, ctypes.c_void_p(_stream(stream)))
     _check(st, "nvfp4_gemv")
@@ -188,6 +197,7 @@ def gemv_gate_up(wg, sg, gg, wu, su, gu, x, out=None, out_dtype=torch.float32,
             tuple(su.shape) != (N, K // 16) or x.shape[1] != K:
         raise ValueError("shape mismatch between gate, up and x")
     y = _out(out, (M, 2 * N), out_dtype, x.device)
+    _one_device(wg, sg, wu, su, x, y)
     st = library().nvfp4_gemv_gate_up(_ptr(wg), _ptr(sg), float(gg), _ptr(wu), _ptr(su), float(gu),
                                       _ptr(x), _ptr(y), _out_code(y.dtype), M, N, K,
                                       ctypes.c_void_p(_stream(stream)))
@@ -210,6 +220,7 @@ def gemv_gate_up_swiglu(wg, sg, gg, wu, su, gu, x, clamp_limit: float = float("i
             tuple(su.shape) != (N, K // 16) or x.shape[1] != K:
         raise ValueError("shape mismatch between gate, up and x")
     y = _out(out, (M, N), out_dtype, x.device)
+    _one_device(wg, sg, wu, su, x, y)
     st = library().nvfp4_gemv_gate_up_swiglu(_ptr(wg), _ptr(sg), float(gg), _ptr(wu), _ptr(su), float(gu),
                                              _ptr(x), float(clamp_limit), _ptr(y), _out_code(y.dtype),
                                              M, N, K, ctypes.c_void_p(_stream(stream)))
@@ -241,6 +252,7 @@ def moe_gemv(w, s, gs, ids, x, x_per_slot: bool, top_k: int, out=None, out_dtype
     if status is not None:
         _need(status, "status", torch.int32, 1)
     y = _out(out, (slots, N), out_dtype, x.device)
+    _one_device(w, s, gs, ids, x, y, status)
     st = library().nvfp4_moe_gemv(_ptr(w), _ptr(s), _ptr(gs), E, _ptr(ids), T, top_k, _ptr(x),
                                   int(bool(x_per_slot)), _ptr(y), _out_code(y.dtype), N, K,
                                   ctypes.c_void_p(status.data_ptr()) if status is not None else None,
