@@ -61,6 +61,9 @@ WORKLOADS = {
     "moe": ("routed experts: 288 experts, gate_up [3072,4096] then down [4096,1536], "
             "4 tokens x top-8, fp32 per-slot out",
             [("moe_gate_up", 3072, 4096, 4, 8, "f32"), ("moe_down", 4096, 1536, 4, 8, "f32")]),
+    "moe_t32": ("routed experts at a larger batch: 288 experts, gate_up [3072,4096] then down [4096,1536], "
+                "32 tokens x top-8 (256 slots), fp32 per-slot out",
+                [("moe_gate_up", 3072, 4096, 32, 8, "f32"), ("moe_down", 4096, 1536, 32, 8, "f32")]),
 }
 
 
@@ -345,7 +348,8 @@ def pool_copies(calls_spec, device):
     for kind, N, K, M, *_ in calls_spec:
         rows = 2 * N if kind in ("gate_up", "gate_up_swiglu") else N
         if kind.startswith("moe"):
-            return 4, l2, "routing rotates over 4 id sets; each step reads ~31 distinct experts (>2x L2)"
+            return 4, l2, ("routing rotates over 4 id sets; the distinct experts a step reads (counted in "
+                           "the algorithmic bytes) exceed 2x L2")
         per_step += rows * K * 9 // 16
     copies = max(1, math.ceil(2.5 * l2 / per_step))
     return copies, l2, f"{copies} rotating weight copies ({copies * per_step / 1e6:.0f} MB > 2x L2 of {l2 / 1e6:.0f} MB)"
