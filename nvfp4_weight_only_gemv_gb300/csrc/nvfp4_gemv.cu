@@ -2062,6 +2062,9 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_kernel(const __grid
 #ifndef NVFP4_MOE_EARLY
 #define NVFP4_MOE_EARLY 1  // weight slots a MoE warp requests before x staging (the rest after it)
 #endif
+#ifndef NVFP4_SK_GROUP_ALIGNED
+#define NVFP4_SK_GROUP_ALIGNED 0  // 1: the planner may keep each stream-K CTA inside one expert group
+#endif
 
 // Stream-K form of the warp-tile kernel, for launches with many tiles per CTA (all 8 warps
 // share one K range: the whole of K). The jobs (group, 16-row tile), group-major, are split
@@ -2174,7 +2177,30 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_sk_kernel(const __g
     if constexpr (MOE) {
         if (warp == 0) tile_moe_groups(p, tab, lane);
         __syncthreads();
+#if NVFP4_SK_GROUP_ALIGNED
+        if (p.items_r) {
+            // group-aligned: CTAs [G*g/ng, G*(g+1)/ng) share group g's jobs (the planner keeps
+            // G >= the most groups there can be), so a CTA stages one group's x rows (<= 8)
+            const int ng = tab->n_groups, G = static_cast<int>(gridDim.x), b = static_cast<int>(blockIdx.x);
+            if (ng > 0) {
+                const int g = static_cast<int>(((static_cast<long long>(b) + 1) * ng - 1) / G);
+                const int lo = static_cast<int>(static_cast<long long>(G) * g / ng);
+                const int c = static_cast<int>(static_cast<long long>(G) * (g + 1) / ng) - lo;
+                const int i = b - lo;
+                j0 = g * tiles + static_cast<int>(static_cast<long long>(tiles) * i / c);
+                j1 = g * tiles + static_cast<int>(static_cast<long long>(tiles) * (i + 1) / c);
+            } else {
+                j0 = j1 = 0;
+            }
+            const int total = (j1 - j0) * nbox;
+            bs = (warp * total) >> 3;
+            be = ((warp + 1) * total) >> 3;
+        } else {
+            set_ranges(tab->n_groups * tiles);
+        }
+#else
         set_ranges(tab->n_groups * tiles);
+#endif
         if (warp == 0 && j0 < j1) tile_moe_rows(p, tab, j0 / tiles, (j1 - 1) / tiles, lane);
         start_cursor();
         __syncthreads();
@@ -2991,7 +3017,12 @@ bool plan_tile(TilePlan& tp, int M, int N, int K, int groups, const DeviceInfo& 
             const long long jobs_max = static_cast<long long>(std::max(moe_groups_max, groups)) * tiles;
             const long long units_lo = std::min<long long>(d.sm_count, jobs);
             const long long jpc_max = (jobs_max + units_lo - 1) / units_lo;
-            const int rows_cap = static_cast<int>(std::min<long long>(xrows, 8 * ((jpc_max + tiles - 1) / tiles + 1)));
+          for (int aligned = 0; aligned <= NVFP4_SK_GROUP_ALIGNED; ++aligned) {
+            // aligned: every CTA inside one group, so at most 8 staged rows; needs a CTA per
+            // group at least, whatever the routing
+            const int groups_most = std::max(moe_groups_max, groups);
+            const int rows_cap = aligned ? std::min(xrows, 8)
+                                         : static_cast<int>(std::min<long long>(xrows, 8 * ((jpc_max + tiles - 1) / tiles + 1)));
             const uint32_t x_bytes = align_up(static_cast<uint32_t>(rows_cap) * sstride, 128);
             int stages = 0, per_sm = 0;
             uint32_t smem = 0;
@@ -3027,8 +3058,14 @@ bool plan_tile(TilePlan& tp, int M, int N, int K, int groups, const DeviceInfo& 
                 }
             }
             if (!stages) continue;
-            const long long units = std::min<long long>(jobs, static_cast<long long>(d.sm_count) * per_sm);
-            const long long jpc = (jobs + units - 1) / units;
+            long long units = std::min<long long>(jobs, static_cast<long long>(d.sm_count) * per_sm);
+            long long jpc = (jobs + units - 1) / units;
+            if (aligned) {
+                units = static_cast<long long>(d.sm_count) * per_sm;
+                if (units < groups_most) continue;
+                const long long per_group = units / std::max(groups, 1);  // CTAs of the smallest share
+                jpc = (tiles + per_group - 1) / per_group;
+            }
             const double boxes_per_warp = static_cast<double>((jpc * nbox + tk::kWarps - 1) / tk::kWarps);
             const double lat = boxes_per_warp * (2.0 * nc + 0.5) + 2.0;
             const double thr = static_cast<double>(jobs) * nbox * (2.0 * nc + 0.5) / (d.sm_count * 16.0) * 1.1 + 2.0;
@@ -3046,7 +3083,7 @@ bool plan_tile(TilePlan& tp, int M, int N, int K, int groups, const DeviceInfo& 
                 tp.p.tpi = tk::kWarps;
                 tp.p.ipg = tiles;
                 tp.p.items_q = static_cast<int>(jobs);
-                tp.p.items_r = 0;
+                tp.p.items_r = aligned;  // stream-K: 1 = group-aligned CTA ranges
                 tp.p.nbox = nbox;
                 tp.p.stages = stages;
                 tp.p.sstride = sstride;
@@ -3056,6 +3093,7 @@ bool plan_tile(TilePlan& tp, int M, int N, int K, int groups, const DeviceInfo& 
                 tp.smem = smem;
                 tp.sk = true;
             }
+          }
         }
     }
     return found;
@@ -3443,9 +3481,10 @@ int describe_plan_on(const DeviceInfo* d, bool host_only, int kind, int M, int N
             plan_tile(tpl, 8, N, K, expected_groups(E, T, top_k), *d, w, w, fake, true, xrows, slots, false,
                       !host_only)) {
             return snprintf(buf, buflen,
-                            "%s grid=%d block=%d smem=%u split=1 rows_per_item=%d k_warps=%d mt=8 stages=%d nc=%d",
-                            tpl.sk ? "tile_sk_moe" : "tile_moe", tpl.grid_x, tk::kThreads, tpl.smem, tpl.p.tpi * 16, 1 << tpl.p.ksplit_log2, tpl.p.stages,
-                            tpl.nc);
+                            "%s grid=%d block=%d smem=%u split=1 rows_per_item=%d k_warps=%d mt=8 stages=%d nc=%d "
+                            "group_aligned=%d",
+                            tpl.sk ? "tile_sk_moe" : "tile_moe", tpl.grid_x, tk::kThreads, tpl.smem, tpl.p.tpi * 16,
+                            1 << tpl.p.ksplit_log2, tpl.p.stages, tpl.nc, tpl.sk ? tpl.p.items_r : 0);
         }
         ok = plan_moe(pl, E, T, top_k, N, K, *d, fake, fake, fake);
     }

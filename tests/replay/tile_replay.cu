@@ -194,7 +194,8 @@ static void check_swiglu(const TilePlan& tp, int M, int N) {
 }
 
 // The stream-K kernel's box walk and combine: every job stored once, with all of its boxes.
-static void check_sk(const TilePlan& tp, int jobs_total) {
+// Group-aligned plans (items_r != 0) also keep every CTA inside one of the ng groups.
+static void check_sk(const TilePlan& tp, int jobs_total, int ng) {
     const TileParams& p = tp.p;
     const int nbox = p.nbox, G = tp.grid_x;
     CHECK(tp.smem <= (uint32_t)kOptin && p.bar_off + 256 + 1024 <= tp.smem, "stream-K smem");
@@ -205,7 +206,19 @@ static void check_sk(const TilePlan& tp, int jobs_total) {
     std::vector<int> stored(jobs_total, 0), boxes(jobs_total, 0);
     for (int cta = 0; cta < G; ++cta) {
         const int q = jobs_total / G, r = jobs_total % G;
-        const int j0 = cta * q + std::min(cta, r), j1 = j0 + q + (cta < r ? 1 : 0);
+        int j0 = cta * q + std::min(cta, r), j1 = j0 + q + (cta < r ? 1 : 0);
+        if (p.items_r) {  // the kernel's group-aligned ranges
+            CHECK(G >= ng, "a CTA per group");
+            const int g = static_cast<int>((static_cast<long long>(cta) + 1) * ng - 1) / G;
+            const int lo = static_cast<int>(static_cast<long long>(G) * g / ng);
+            const int c = static_cast<int>(static_cast<long long>(G) * (g + 1) / ng) - lo;
+            const int i = cta - lo;
+            CHECK(c >= 1 && i >= 0 && i < c, "group share");
+            j0 = g * p.tiles + static_cast<int>(static_cast<long long>(p.tiles) * i / c);
+            j1 = g * p.tiles + static_cast<int>(static_cast<long long>(p.tiles) * (i + 1) / c);
+            CHECK(j0 >= g * p.tiles && j1 <= (g + 1) * p.tiles, "CTA inside its group");
+            CHECK(p.M >= 1 && p.M <= 8, "aligned row bound");
+        }
         const int total = (j1 - j0) * nbox;
         int bsv[8], bev[8], rjob[8][2], rcnt[8][2];  // records: [warp][first/last] -> (job, boxes)
         for (int w = 0; w < 8; ++w) {
@@ -333,7 +346,7 @@ int main() {
                              {151936, 4096}, {3072, 4096}, {4096, 1536}, {1000, 1024}, {37, 2560},
                              {300, 512},   {1, 256},     {5, 256},     {513, 768},   {50, 256},
                              {2000, 2048}, {64, 256},    {300, 12288}, {4096, 768}};
-    int n_items = 0, n_sw = 0, n_moe = 0;
+    int n_items = 0, n_sw = 0, n_moe = 0, n_aligned = 0;
     for (const auto& s : shapes)
         for (int M = 1; M <= 8; ++M) {
             for (int groups = 1; groups <= 2; ++groups) {
@@ -362,8 +375,9 @@ int main() {
             continue;
         }
         ++n_moe;
+        if (tp.p.items_r && tp.sk) ++n_aligned;
         if (tp.sk) {
-            for (int ng = 1; ng <= 32; ++ng) check_sk(tp, ng * tp.p.tiles);
+            for (int ng = 1; ng <= 32; ++ng) check_sk(tp, ng * tp.p.tiles, ng);
         } else {
             check_items(tp, tp.p.M, mm[1], 30);
         }
@@ -380,6 +394,7 @@ int main() {
         CHECK(tp.p.moe_off % 16 == 0 && tp.p.moe_off >= tp.p.bar_off + 8 * 4 * 8, "group tables offset");
         CHECK(tp.p.moe_off + sizeof(TileMoe) + 1024 <= tp.smem, "group tables inside the allocation");
     }
-    printf("per-item plans %d, fused gate/up plans %d, MoE plans %d, fails %d\n", n_items, n_sw, n_moe, fails);
+    printf("per-item plans %d, fused gate/up plans %d, MoE plans %d, group-aligned %d, fails %d\n", n_items, n_sw,
+           n_moe, n_aligned, fails);
     return fails != 0;
 }

@@ -16,7 +16,9 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 SRC = os.path.join(HERE, "replay", "tile_replay.cu")
 
 
-def test_tile_plans_and_indexes(tmp_path):
+@pytest.mark.parametrize("aligned", [0, 1])
+def test_tile_plans_and_indexes(tmp_path, aligned):
+    # aligned = 1: the build switch that lets the planner keep stream-K CTAs inside one group
     try:
         nvcc = build.nvcc_path()
     except RuntimeError:
@@ -24,7 +26,7 @@ def test_tile_plans_and_indexes(tmp_path):
     exe = str(tmp_path / "tile_replay")
     inc = os.path.join(os.path.dirname(HERE), "include")
     cmd = [nvcc, "-O1", "-std=c++17", "-I", inc, "-gencode=arch=compute_103a,code=compute_103a",
-           "-o", exe, SRC]
+           f"-DNVFP4_SK_GROUP_ALIGNED={aligned}", "-o", exe, SRC]
     res = subprocess.run(cmd, capture_output=True, text=True)
     assert res.returncode == 0, res.stdout + res.stderr
     run = subprocess.run([exe], capture_output=True, text=True, timeout=600)
@@ -33,3 +35,4 @@ def test_tile_plans_and_indexes(tmp_path):
     counts = dict(part.rsplit(" ", 1) for part in out[-1].split(", "))
     assert int(counts["per-item plans"]) >= 300 and int(counts["fused gate/up plans"]) >= 150
     assert int(counts["MoE plans"]) == 5
+    assert (int(counts["group-aligned"]) >= 1) == bool(aligned)
