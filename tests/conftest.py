@@ -22,6 +22,13 @@ def pytest_collection_modifyitems(config, items):
     except Exception:  # pragma: no cover
         have_gpu = False
     if have_gpu:
+        # A kernel that never finished would block the test in a CUDA call forever. Where the
+        # timeout plugin is installed, each GPU test gets a generous limit enforced from a
+        # watchdog thread, which ends the process (and with it the CUDA context) instead.
+        if config.pluginmanager.hasplugin("timeout"):
+            for item in items:
+                if "gpu" in item.keywords and item.get_closest_marker("timeout") is None:
+                    item.add_marker(pytest.mark.timeout(300, method="thread"))
         return
     skip = pytest.mark.skip(reason="no CUDA device visible")
     for item in items:
