@@ -635,6 +635,17 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
+    if argv is None:  # run as a program: a step that never finished must not hold the GPU
+        limit = 900 + 2 * (args.steps + args.warmup)
+        import threading
+
+        def _expire():
+            print(f"bench.py: no result after {limit} s; exiting", file=sys.stderr, flush=True)
+            os._exit(3)
+
+        timer = threading.Timer(limit, _expire)
+        timer.daemon = True
+        timer.start()
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)
