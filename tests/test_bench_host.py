@@ -78,3 +78,12 @@ def test_workload_byte_accounting():
     assert calls["sw"].weight_bytes() == calls["gu"].weight_bytes() == 2 * 64 * per_row
     assert calls["sw"].alg_bytes() == 2 * 64 * per_row + 2 * 256 * 2 + 2 * 64 * 2
     assert calls["gu"].alg_bytes() == 2 * 64 * per_row + 2 * 256 * 2 + 2 * 128 * 4
+
+
+def test_cpu_baseline_reports_the_oracle_on_a_bounded_sample():
+    calls = [bench.Call(("dense", 64, 256, 1, 0, "f32"), "cpu", 1, "cpu"),
+             bench.Call(("gate_up_swiglu", 32, 256, 2, 1, "bf16"), "cpu", 1, "cpu")]
+    base = bench.cpu_baseline(calls, target_s=0.3)
+    assert base["kind"] == "oracle" and base["cores"] >= 1 and base["value"] > 0
+    assert base["unit"].startswith("GB/s")
+    assert "every GEMV of one step" in base["sample"] or "% of the output rows" in base["sample"]
