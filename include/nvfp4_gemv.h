@@ -121,8 +121,10 @@ nvfp4_status nvfp4_gemv_gate_up_swiglu(const uint8_t* w_gate, const uint8_t* s_g
  *   global_scales [E] f32 (device), expert_ids [T*top_k] int32 (device).
  *   x [T, K] (x_per_slot = 0: gate/up, shared by a token's slots) or [T*top_k, K]
  *   (x_per_slot = 1: down, one row per slot). y [T*top_k, N].
- * Slots routed to the same expert are served from one read of that expert's weights
- * (the union of the routed experts, as in glm5next_moe_row_union, card performance[31]).
+ * Slots routed to the same expert share reads of that expert's weights: one read serves up to
+ * 8 of its slots (the tensor-core tile's 8 columns), so an expert with at most 8 slots in the
+ * call is read once (the union of the routed experts, as in glm5next_moe_row_union, card
+ * performance[31]), one with more once per 8 of them.
  * An id outside [0, E) zeroes its slot's row and sets NVFP4_DEV_BAD_EXPERT in the device
  * status word and, if status_dev is not NULL, in *status_dev (device int32, OR-ed in).
  */
