@@ -4,18 +4,22 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload W]
 
 A step is one pass of the hot path over one batch of synthetic input. With the default
-workload ("attn"), a step is the four attention-projection GEMVs at decode batch sizes:
-N x K = 4096 x 4096 and 1024 x 4096, M = 1 and M = 5, bf16 output. These are the
-MUL_MAT shapes of "llama.cpp eval-callback — ggml op level". Weights are ~N(0, 0.02)
-quantised to NVFP4, and x is ~N(0, 1) in bf16. Weight copies rotate through a pool
-larger than twice the L2, so no call finds its weights in cache.
+workload ("vocab"), a step is the vocabulary-head GEMV N x K = 151936 x 4096 at M = 1 with
+fp32 output, the largest single-GPU configuration. Every other target step runs in the same
+invocation and is reported under "per_workload": the attention projections (4096 x 4096 and
+1024 x 4096 at M = 1 and 5, the MUL_MAT shapes of "llama.cpp eval-callback — ggml op level"),
+the FFN gate/up + down pair at M = 1, 2, 4, 8, the pair with the fused SwiGLU, and the
+288-expert MoE layer at 4 and 32 tokens. Weights are ~N(0, 0.02) quantised to NVFP4, and x is
+~N(0, 1) in bf16. Weight copies rotate through a pool larger than twice the L2, so no call
+finds its weights in cache.
 
 The timed region is K steps enqueued behind a short torch sleep kernel. The host queues
 every launch before the GPU starts, so the measurement is device time. CUDA events
-bracket the region and every launch. The script prints one JSON line: the weight-GB/s
-value, per-call microseconds and roofline fractions, the dominant kernel's roofline
-entry, an end-to-end number through the public API with host buffers, the oracle's
-CPU baseline and the SM clocks sampled during the region.
+bracket the region and every launch. After each timed region a sample of every call's output
+is checked against the CPU oracle; a mismatch marks the line invalid and the exit status is 4.
+The script prints one JSON line: the weight-GB/s value, per-call microseconds and roofline
+fractions, the dominant kernel's roofline entry, an end-to-end number through the public API
+with host buffers, the oracle's CPU baseline and the SM clocks sampled during the region.
 """
 from __future__ import annotations
 
@@ -85,12 +89,14 @@ def kernel_source_sha256():
         return hashlib.sha256(f.read()).hexdigest()
 
 
+TRAFFIC_PATH = os.path.join(ROOT, "profiles", "traffic.json")
+
+
 def kernel_traffic(workload):
     """DRAM bytes (read + write) per launch from the committed ncu summary, or None when
     the summary was taken on another version of the kernel source (or is absent)."""
-    prof = os.path.join(ROOT, "profiles", "traffic.json")
     try:
-        with open(prof) as f:
+        with open(TRAFFIC_PATH) as f:
             rec = json.load(f)
         if rec.get("kernel_source_sha256") != kernel_source_sha256():
             return None
@@ -437,11 +443,30 @@ def e2e_region(calls, copies, steps, stream, device, graph=False):
     return (t1 - t0) * 1e3 / steps
 
 
-def cpu_baseline(calls, target_s=6.0):
-    """The oracle on the host cores over a bounded sample of the step: a row fraction of every
-    GEMV, grown until a pass takes about target_s / 3; once every row is in the sample, whole
-    steps are repeated instead."""
-    import oracle
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the platform string)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu model")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def _oracle_pass(calls, target_s):
+    """The oracle over a row sample of every GEMV of the step, the sample grown until one timed
+    pass takes about target_s / 3; once every row is in the sample, whole steps are repeated.
+    Returns (bytes, seconds, sample description)."""
     rng = np.random.default_rng(0)
     frac, reps = 0.002, 1
     t = 0.0
@@ -460,8 +485,84 @@ def cpu_baseline(calls, target_s=6.0):
     what = f"{frac * 100:.3g}% of the output rows of every GEMV of one step"
     if reps > 1:
         what = f"every GEMV of one step, {reps} times"
-    return {"value": byts / t / 1e9, "unit": "GB/s (NVFP4 weight bytes)", "cores": oracle.threads(),
-            "kind": "oracle", "sample": f"{what} ({byts / 1e6:.1f} MB of weights, {t:.2f} s wall)"}
+    return byts, t, f"{what} ({byts / 1e6:.1f} MB of weights, {t:.2f} s wall)"
+
+
+def cpu_baseline(calls, target_s=6.0, single_thread=True):
+    """The oracle on the host cores over a bounded sample of the step (all OpenMP threads), and
+    the same on one thread when single_thread is set."""
+    import oracle
+    byts, t, sample = _oracle_pass(calls, target_s)
+    res = {"value": byts / t / 1e9, "unit": "GB/s (NVFP4 weight bytes)", "cores": oracle.threads(),
+           "kind": "oracle", "sample": sample, "cpu": cpu_model()}
+    if single_thread:
+        n = oracle.threads()
+        oracle.set_threads(1)
+        try:
+            b1, t1, sample1 = _oracle_pass(calls, target_s / 3)
+        finally:
+            oracle.set_threads(n)
+        res["one_thread"] = {"value": b1 / t1 / 1e9, "cores": 1, "sample": sample1}
+    return res
+
+
+# ------------------------------------------------------------------ in-run parity
+
+def _ulp_bf16(v):
+    a = np.abs(v)
+    e = np.maximum(np.floor(np.log2(np.where(a > 0, a, 1.0))), -126)
+    return np.where(a >= 2.0 ** -126, 2.0 ** (e - 7), 2.0 ** -133)
+
+
+def check_outputs(calls, n_cols=48, seed=5):
+    """The timed outputs against the oracle: for every call, copy 0's output (written inside the
+    timed region) on a sample of n_cols output columns, compared with the oracle's value of
+    those columns on the same inputs, under the parity tolerance |y - y_ref| <= 1e-5 * A + 1e-6
+    (A = |g| * sum_k |w_k x_k|), plus one bf16 ulp of y_ref for bf16 output; the fused SwiGLU
+    carries that bound through the activation. NaN must match NaN. Returns a summary dict."""
+    import oracle
+    from nvfp4_weight_only_gemv_gb300 import synth
+    rng = np.random.default_rng(seed)
+    checked, bad = 0, 0
+    worst = 0.0
+    for c in calls:
+        h = c.host
+        cols = c.y_shape[1]
+        rows = np.sort(rng.choice(cols, size=min(n_cols, cols), replace=False)).astype(np.int64)
+        y = c.sets[0]["y"].float().cpu().numpy().astype(np.float64)[:, rows]
+        bf = c.out_dtype == torch.bfloat16
+        if c.kind == "dense":
+            yr, ya = oracle.gemv(h["w"].numpy(), h["s"].numpy(), h["g"], synth.bf16_bits(h["x"]), rows=rows)
+            tol = 1e-5 * ya + 1e-6
+        elif c.kind == "gate_up":
+            yr, ya = oracle.gemv_gate_up(h["wg"].numpy(), h["sg"].numpy(), h["gg"], h["wu"].numpy(),
+                                         h["su"].numpy(), h["gu"], synth.bf16_bits(h["x"]), rows=rows)
+            tol = 1e-5 * ya + 1e-6
+        elif c.kind == "gate_up_swiglu":
+            yr, aux = oracle.gate_up_swiglu(h["wg"].numpy(), h["sg"].numpy(), h["gg"], h["wu"].numpy(),
+                                            h["su"].numpy(), h["gu"], synth.bf16_bits(h["x"]), SWIGLU_CLAMP,
+                                            rows=rows)
+            tg, tu = 1e-5 * aux["gate_abs"] + 1e-6, 1e-5 * aux["up_abs"] + 1e-6
+            cg = np.clip(aux["gate"], -SWIGLU_CLAMP, SWIGLU_CLAMP)
+            cu = np.clip(aux["up"], -SWIGLU_CLAMP, SWIGLU_CLAMP)
+            tol = (1.1 * np.abs(cu) * tg + np.maximum(np.abs(cg), 0.28) * tu + 1.1 * tg * tu
+                   + 1e-6 * np.abs(np.nan_to_num(yr)) + 1e-6)
+        else:
+            ids = c.sets[0]["ids"].cpu().numpy()
+            yr, ya, _ = oracle.moe_gemv(h["w"].numpy(), h["s"].numpy(), h["gs"].numpy(), ids,
+                                        synth.bf16_bits(h["x"]), c.x_per_slot, c.top_k, rows=rows)
+            tol = 1e-5 * ya + 1e-6
+        if bf:
+            tol = tol + _ulp_bf16(np.nan_to_num(yr))
+        nan_r = np.isnan(yr)
+        err = np.where(nan_r, 0.0, np.abs(y - yr))
+        miss = (np.isnan(y) != nan_r) | (err > tol)
+        bad += int(miss.sum())
+        checked += y.size
+        worst = max(worst, float(np.max(np.where(nan_r, 0.0, err / tol))) if y.size else 0.0)
+    return {"ok": bad == 0, "checked": checked, "outside_tolerance": bad, "worst_err_over_tol": round(worst, 4),
+            "method": f"oracle on {n_cols} sampled output columns of every call (copy 0, written in the "
+                      "timed region), parity tolerance"}
 
 
 # ------------------------------------------------------------------ arms
@@ -508,6 +609,87 @@ def run_reference(args):
     return 0
 
 
+PER_WORKLOAD = ["attn", "ffn", "ffn_m2", "ffn_m4", "ffn_m8", "ffn_swiglu", "moe", "moe_t32"]
+
+
+def measure(name, steps, warmup, device, stream, ws, sampler=None):
+    """One workload: build its calls, warm up, time `steps` steps back to back, time every call
+    in isolation, check sampled outputs against the oracle. Returns (calls, copies, record)."""
+    desc, spec = WORKLOADS[name]
+    copies, l2, l2_note = pool_copies(spec, device)
+    calls = [Call(s, device, copies, "cuda") for s in spec]
+
+    # warm-up (also measures the host enqueue rate to size the gate)
+    h0 = time.perf_counter()
+    for st in range(max(3, warmup)):
+        for c in calls:
+            c.launch(st % copies)
+    torch.cuda.synchronize()
+    per_launch_host = (time.perf_counter() - h0) / (max(3, warmup) * len(calls))
+    sm_mhz_guess = 1900.0
+    gate_ms = max(5.0, 3.0 * per_launch_host * 1e3 * steps * len(calls) + 2.0)
+
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    region_ms, host_s, gate_meas = timed_region(calls, copies, steps, gate_ms * 1e3 * sm_mhz_guess, stream)
+    if host_s * 1e3 > gate_meas:   # host could not stay ahead: retry once with a longer gate
+        gate_ms = host_s * 1e3 * 3 + 5
+        region_ms, host_s, gate_meas = timed_region(calls, copies, steps, gate_ms * 1e3 * sm_mhz_guess, stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    region_ms = max_over_ranks(region_ms, device)
+    parity = check_outputs(calls)
+    per_call = per_call_region(calls, copies, min(steps, 100), gate_ms * 2e3 * sm_mhz_guess, stream)
+
+    ms_per_step = region_ms / steps
+    wbytes_step = sum(np.mean([c.weight_bytes(k % copies) for k in range(min(copies, steps))]) for c in calls)
+    value = job_gbps(ws, wbytes_step, ms_per_step)
+
+    peak, peak_kind = measured_peaks()
+    call_rows = []
+    step_alg = 0.0
+    for ci, c in enumerate(calls):
+        ms = float(np.mean(per_call[ci]))
+        alg = float(np.mean([c.alg_bytes(k % copies) for k in range(steps)]))
+        wb = float(np.mean([c.weight_bytes(k % copies) for k in range(steps)]))
+        step_alg += alg
+        call_rows.append({"call": c.kind, "N": c.N, "K": c.K, "M": c.M, "out": str(c.out_dtype).split(".")[-1],
+                          "us_isolated": round(ms * 1e3, 3),
+                          "us_isolated_median": round(float(np.median(per_call[ci])) * 1e3, 3),
+                          "weight_GBps_isolated": round(wb / (ms * 1e-3) / 1e9, 1),
+                          "alg_bytes": int(alg),
+                          "pct_of_8TBps_isolated": round(100 * alg / (ms * 1e-3) / (NOMINAL_HBM_GBS * 1e9), 2)})
+    launches = steps * len(calls)
+    us_per_launch = region_ms * 1e3 / launches
+    achieved = step_alg * steps / (region_ms * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": kernel_traffic(name),
+                "kernel": kernels_of(calls),
+                "us_per_launch": round(us_per_launch, 3),
+                "pct_of_8TBps": round(100 * achieved / NOMINAL_HBM_GBS, 2),
+                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs: copy bandwidth)"}
+    rec = {"workload": f"{name}: {desc}", "value": round(value, 2), "ms_per_step": round(ms_per_step, 6),
+           "steps": steps, "launches": launches, "l2": l2_note, "calls_per_step": len(calls),
+           "calls": call_rows, "roofline": roofline, "parity": parity,
+           "wall": (t_wall0, t_wall1),
+           "timing": {"gate_ms": round(gate_meas, 3), "host_enqueue_ms": round(host_s * 1e3, 3),
+                      "method": "timed region: steps back to back behind a sleep kernel, events at "
+                                "both ends; calls[].us_isolated: separate pass, events around "
+                                f"each launch ({len(per_call[0])} per call)"}}
+    return calls, copies, wbytes_step, rec
+
+
+def release(calls):
+    for c in calls:
+        c.sets.clear()
+        c.host.clear()
+    calls.clear()
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+
+
 def run_ours(args):
     ws, rank, local = dist_env()
     if not torch.cuda.is_available():
@@ -519,66 +701,11 @@ def run_ours(args):
         dist.init_process_group("nccl", device_id=device)
     import nvfp4_weight_only_gemv_gb300 as nv
     nv.library()
-    desc, spec = WORKLOADS[args.workload]
-    copies, l2, l2_note = pool_copies(spec, device)
-    calls = [Call(s, device, copies, "cuda") for s in spec]
     stream = torch.cuda.current_stream(device)
     sampler = ClockSampler(local) if rank == 0 else None
 
-    # warm-up (also measures the host enqueue rate to size the gate)
-    h0 = time.perf_counter()
-    for st in range(max(3, args.warmup)):
-        for c in calls:
-            c.launch(st % copies)
-    torch.cuda.synchronize()
-    per_launch_host = (time.perf_counter() - h0) / (max(3, args.warmup) * len(calls))
-    sm_mhz_guess = 1900.0
-    gate_ms = max(5.0, 3.0 * per_launch_host * 1e3 * args.steps * len(calls) + 2.0)
-
-    if ws > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    t_wall0 = time.time()
-    region_ms, host_s, gate_meas = timed_region(calls, copies, args.steps, gate_ms * 1e3 * sm_mhz_guess, stream)
-    if host_s * 1e3 > gate_meas:   # host could not stay ahead: retry once with a longer gate
-        gate_ms = host_s * 1e3 * 3 + 5
-        region_ms, host_s, gate_meas = timed_region(calls, copies, args.steps, gate_ms * 1e3 * sm_mhz_guess, stream)
-    torch.cuda.synchronize()
-    t_wall1 = time.time()
-    region_ms = max_over_ranks(region_ms, device)
-    per_call = per_call_region(calls, copies, min(args.steps, 100), gate_ms * 2e3 * sm_mhz_guess, stream)
-
-    ms_per_step = region_ms / args.steps
-    wbytes_step = sum(np.mean([c.weight_bytes(k % copies) for k in range(min(copies, args.steps))])
-                      for c in calls)
-    value = job_gbps(ws, wbytes_step, ms_per_step)
-
-    peak, peak_kind = measured_peaks()
-    call_rows = []
-    n_iso = len(per_call[0])
-    step_alg = 0.0
-    for ci, c in enumerate(calls):
-        ms = float(np.mean(per_call[ci]))
-        alg = float(np.mean([c.alg_bytes(k % copies) for k in range(args.steps)]))
-        wb = float(np.mean([c.weight_bytes(k % copies) for k in range(args.steps)]))
-        step_alg += alg
-        call_rows.append({"call": c.kind, "N": c.N, "K": c.K, "M": c.M, "out": str(c.out_dtype).split(".")[-1],
-                          "us_isolated": round(ms * 1e3, 3),
-                          "us_isolated_median": round(float(np.median(per_call[ci])) * 1e3, 3),
-                          "weight_GBps_isolated": round(wb / (ms * 1e-3) / 1e9, 1),
-                          "alg_bytes": int(alg),
-                          "pct_of_8TBps_isolated": round(100 * alg / (ms * 1e-3) / (NOMINAL_HBM_GBS * 1e9), 2)})
-    launches = args.steps * len(calls)
-    us_per_launch = region_ms * 1e3 / launches
-    achieved = step_alg * args.steps / (region_ms * 1e-3) / 1e9
-    traffic = kernel_traffic(args.workload)
-    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "traffic": traffic,
-                "kernel": kernels_of(calls),
-                "us_per_launch": round(us_per_launch, 3),
-                "pct_of_8TBps": round(100 * achieved / NOMINAL_HBM_GBS, 2),
-                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs: copy bandwidth)"}
-
+    calls, copies, wbytes_step, rec = measure(args.workload, args.steps, args.warmup, device, stream, ws)
+    t_wall0, t_wall1 = rec.pop("wall")
     clocks = sampler.summary(t_wall0, t_wall1) if sampler else None
     if sampler:
         sampler.stop()
@@ -601,27 +728,50 @@ def run_ours(args):
                      "ms_per_step": round(e2e_eager_ms, 4),
                      "method": "every copy and call issued from Python each step, then a synchronize"}}
 
-    base = None
-    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        base = cpu_baseline(calls)
+    cpu_on = rank == 0 and ws == 1 and not args.no_cpu_baseline
+    base = cpu_baseline(calls) if cpu_on else None
+    release(calls)
 
+    # every other target step of the same run, each with its own timed region, oracle check
+    # and CPU baseline
+    per = {}
+    if not args.no_per_workload:
+        for name in PER_WORKLOAD:
+            if name == args.workload:
+                continue
+            pc, _, _, prec = measure(name, min(args.steps, 100), args.warmup, device, stream, ws)
+            prec.pop("wall")
+            if cpu_on:
+                b = cpu_baseline(pc, target_s=1.5, single_thread=False)
+                prec["cpu_baseline"] = {k: b[k] for k in ("value", "unit", "cores", "sample")}
+            release(pc)
+            per[name] = prec
+
+    ok = rec["parity"]["ok"] and all(r["parity"]["ok"] for r in per.values())
     if rank == 0:
-        line = {"metric": METRIC, "value": round(value, 2), "unit": "GB/s (NVFP4 weight bytes)",
+        line = {"metric": METRIC, "value": rec["value"], "unit": "GB/s (NVFP4 weight bytes)",
                 "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
-                "ms_per_step": round(ms_per_step, 6), "higher_is_better": True, "scaling": "weak",
+                "ms_per_step": rec["ms_per_step"], "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-                "config": {"workload": f"{args.workload}: {desc}", "parallelism": f"replicas x{ws}",
-                           "l2": l2_note, "calls_per_step": len(calls)},
-                "calls": call_rows, "roofline": roofline, "cpu_baseline": base, "e2e": e2e,
-                "gpu_launches": args.steps * len(calls), "clocks": clocks, "env": run_env(device),
-                "timing": {"gate_ms": round(gate_meas, 3), "host_enqueue_ms": round(host_s * 1e3, 3),
-                           "method": "timed region: steps back to back behind a sleep kernel, events at "
-                                     "both ends; calls[].us_isolated: separate pass, events around "
-                                     f"each launch ({n_iso} per call)"}}
+                "config": {"workload": rec["workload"], "parallelism": f"replicas x{ws}",
+                           "l2": rec["l2"], "calls_per_step": rec["calls_per_step"]},
+                "calls": rec["calls"], "roofline": rec["roofline"], "parity": rec["parity"],
+                "cpu_baseline": base, "e2e": e2e,
+                "gpu_launches": rec["launches"], "clocks": clocks, "env": run_env(device),
+                "timing": rec["timing"],
+                "per_workload": {k: {"workload": v["workload"], "value": v["value"],
+                                     "ms_per_step": v["ms_per_step"], "steps": v["steps"],
+                                     "frac": v["roofline"]["frac"], "us_per_launch": v["roofline"]["us_per_launch"],
+                                     "pct_of_8TBps": v["roofline"]["pct_of_8TBps"],
+                                     "traffic": v["roofline"]["traffic"], "kernel": v["roofline"]["kernel"],
+                                     "calls": v["calls"], "parity": v["parity"],
+                                     "cpu_baseline": v.get("cpu_baseline")} for k, v in per.items()}}
+        if not ok:
+            line["invalid"] = "a timed output is outside the oracle's tolerance (see parity)"
         print(json.dumps(line))
     if ws > 1:
         torch.distributed.destroy_process_group()
-    return 0
+    return 0 if ok else 4
 
 
 def main(argv=None):
@@ -630,8 +780,10 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="attn")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="vocab")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-workload", action="store_true",
+                    help="time only --workload (default: also every other target step, as per_workload)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3

@@ -70,6 +70,7 @@ typedef enum {
 /* Device status bits (see nvfp4_device_status). */
 #define NVFP4_DEV_TIMEOUT 1    /* a pipeline wait exceeded its time budget; y unspecified */
 #define NVFP4_DEV_BAD_EXPERT 2 /* an expert id outside [0, E); those slots are zero */
+#define NVFP4_DEV_INTERNAL 4   /* a launch-plan invariant failed on the device; y unspecified */
 
 /*
  * Dense GEMV: y[M, N] = g * W[N, K] . x[M, K]^T (per element as above).
@@ -205,6 +206,22 @@ int nvfp4_describe_plan(int kind, int M, int N, int K, int T, int top_k, char* b
  */
 int nvfp4_describe_plan_host(int sm_count, int smem_optin, int smem_per_sm, int kind, int M, int N, int K,
                              int T, int top_k, char* buf, int buflen);
+
+/*
+ * Phase trace of the tile kernels (a diagnostic; no counterpart on the pages). A library built
+ * with -DNVFP4_PHASE_TRACE=1 records, for each of the last 16 tile-kernel launches (slot =
+ * launch number mod 16) and each of its first 1024 CTAs, 32 64-bit words: for phase ph = 0..7
+ * word 2ph is %globaltimer (ns) and word 2ph + 1 the SM's clock64, taken by thread 0 at
+ * 0 entry, 1 first weight copies issued, 2 past the dependency wait, 3 x staged, 4 first box
+ * landed, 5 box loop done (stream-K form), 6 outputs stored, 7 exit; word 16 + w is
+ * %globaltimer when warp w left its box loop; word 24 the SM id; word 24 + w (w = 1..7)
+ * %globaltimer when warp w's first box landed. Unrecorded words are zero.
+ * This call synchronises `stream`, copies min(max_words, 16 * 1024 * 32) words in
+ * [slot][cta][word] order to host_out (host memory), clears the trace and restarts the slot
+ * count. Returns the number of words copied, 0 for a library built without tracing (the
+ * default), or -1 on a CUDA error or a NULL host_out.
+ */
+int nvfp4_phase_trace(uint64_t* host_out, int max_words, void* stream);
 
 /* Library version: major * 10000 + minor * 100 + patch. */
 int nvfp4_version(void);

@@ -22,13 +22,14 @@ import torch
 from . import build as _build
 
 __all__ = ["gemv", "gemv_gate_up", "gemv_gate_up_swiglu", "moe_gemv", "device_status", "set_wait_budget_ns",
-           "set_variant", "set_pdl", "fp32_fallbacks", "describe_plan", "describe_plan_host", "library", "library_path", "NVFP4Error",
-           "OUT_F32", "OUT_BF16", "DEV_TIMEOUT", "DEV_BAD_EXPERT"]
+           "set_variant", "set_pdl", "fp32_fallbacks", "phase_trace", "describe_plan", "describe_plan_host", "library", "library_path", "NVFP4Error",
+           "OUT_F32", "OUT_BF16", "DEV_TIMEOUT", "DEV_BAD_EXPERT", "DEV_INTERNAL"]
 
 OUT_F32 = 0
 OUT_BF16 = 1
 DEV_TIMEOUT = 1
 DEV_BAD_EXPERT = 2
+DEV_INTERNAL = 4
 
 _lock = threading.Lock()
 _lib = None
@@ -41,7 +42,9 @@ class NVFP4Error(RuntimeError):
 
 
 def library_path() -> str:
-    return _build.LIB_PATH
+    """The library this process loads: NVFP4_GEMV_LIBRARY if set (a diagnostic or experiment
+    build of the same source), else the in-tree build."""
+    return os.environ.get("NVFP4_GEMV_LIBRARY") or _build.LIB_PATH
 
 
 def _declare(lib):
@@ -76,6 +79,8 @@ def _declare(lib):
     lib.nvfp4_describe_plan.restype = i32
     lib.nvfp4_describe_plan_host.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32, i32, ctypes.c_char_p, i32]
     lib.nvfp4_describe_plan_host.restype = i32
+    lib.nvfp4_phase_trace.argtypes = [vp, i32, vp]
+    lib.nvfp4_phase_trace.restype = i32
     lib.nvfp4_version.argtypes = []
     lib.nvfp4_version.restype = i32
     return lib
@@ -86,8 +91,8 @@ def library(build_if_missing: bool = True):
     global _lib
     with _lock:
         if _lib is None:
-            path = _build.LIB_PATH
-            if build_if_missing and _build.is_stale():
+            path = library_path()
+            if build_if_missing and path == _build.LIB_PATH and _build.is_stale():
                 try:
                     _build.build()
                 except RuntimeError:
@@ -287,6 +292,17 @@ def fp32_fallbacks(stream=None) -> int:
     if v < 0:
         raise NVFP4Error(6, "nvfp4_fp32_fallbacks")
     return int(v)
+
+
+def phase_trace(stream=None):
+    """The phase trace of the last tile-kernel launches as an int64 tensor [16, 1024, 32]
+    ([launch slot, CTA, word]; see nvfp4_phase_trace in the header), then cleared. None when
+    the loaded library was built without tracing."""
+    out = torch.zeros(16 * 1024 * 32, dtype=torch.int64)
+    n = library().nvfp4_phase_trace(ctypes.c_void_p(out.data_ptr()), out.numel(), ctypes.c_void_p(_stream(stream)))
+    if n < 0:
+        raise NVFP4Error(6, "nvfp4_phase_trace")
+    return out.view(16, 1024, 32) if n > 0 else None
 
 
 def set_pdl(enable: bool) -> None:

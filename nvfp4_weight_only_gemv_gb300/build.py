@@ -50,5 +50,26 @@ def build(force: bool = False, verbose: bool = False) -> str:
     return LIB_PATH
 
 
+def variant_path(name: str) -> str:
+    return os.path.join(LIB_DIR, f"libnvfp4gemv_{name}.so")
+
+
+def build_variant(name: str, defines: dict, force: bool = False) -> str:
+    """Builds the same source with extra preprocessor definitions (the phase-trace diagnostic,
+    planner experiments) into _build/libnvfp4gemv_<name>.so and returns its path. Load it by
+    setting NVFP4_GEMV_LIBRARY to that path before the package first loads its library."""
+    out = variant_path(name)
+    if not force and os.path.exists(out) and os.path.getmtime(out) >= max(os.path.getmtime(f) for f in (SRC, HEADER)):
+        return out
+    os.makedirs(LIB_DIR, exist_ok=True)
+    tmp = out + f".tmp{os.getpid()}"
+    cmd = nvcc_command(tmp, tuple(f"-D{k}={v}" for k, v in sorted(defines.items())))
+    res = subprocess.run(cmd, capture_output=True, text=True)
+    if res.returncode != 0:
+        raise RuntimeError("nvcc failed:\n" + " ".join(cmd) + "\n" + res.stdout + res.stderr)
+    os.replace(tmp, out)
+    return out
+
+
 if __name__ == "__main__":
     print(build(force=True, verbose=True))

@@ -62,6 +62,23 @@ enum : int { kModeDense = 0, kModeMoe = 1 };
 __device__ int g_device_status;
 __device__ unsigned long long g_fp32_fallbacks;  // CTAs that staged x in fp32 because f16 was inexact
 
+// Phase trace (diagnostic builds with -DNVFP4_PHASE_TRACE=1 only): the tile kernels write, per
+// launch slot and CTA, kTraceWords 64-bit words: for phase ph = 0..7 word 2ph = %globaltimer (ns)
+// and word 2ph + 1 = clock64 (thread 0); word 16 + w = %globaltimer when warp w leaves its box
+// loop; word 24 = the SM the CTA ran on; word 24 + w (w = 1..7) = %globaltimer when warp w's
+// first box landed (warp 0's is phase 4). Phases: 0 entry, 1 first weight copies issued, 2 past
+// the dependency wait, 3 x staged, 4 warp 0's first box landed, 5 warp 0's loop done, 6 outputs
+// stored, 7 exit. Normal builds compile all of it out.
+#ifndef NVFP4_PHASE_TRACE
+#define NVFP4_PHASE_TRACE 0
+#endif
+constexpr int kTraceLaunches = 16;
+constexpr int kTraceCtas = 1024;
+constexpr int kTraceWords = 32;
+#if NVFP4_PHASE_TRACE
+__device__ unsigned long long g_trace[kTraceLaunches * kTraceCtas * kTraceWords];
+#endif
+
 // ------------------------------------------------------------------ parameters
 
 struct Params {
@@ -318,6 +335,30 @@ __device__ __forceinline__ float swiglu_f32(float gate, float up, float lim) {
     gate = gate > lim ? lim : (gate < -lim ? -lim : gate);
     up = up > lim ? lim : (up < -lim ? -lim : up);
     return gate / (1.f + expf(-gate)) * up;
+}
+
+__device__ __forceinline__ void trace_word(int slot, int word, unsigned long long v) {
+#if NVFP4_PHASE_TRACE
+    if (blockIdx.x < kTraceCtas)
+        g_trace[(static_cast<size_t>(slot) * kTraceCtas + blockIdx.x) * kTraceWords + word] = v;
+#else
+    (void)slot; (void)word; (void)v;
+#endif
+}
+
+// Phase ph of this CTA (call from one thread): %globaltimer and clock64.
+__device__ __forceinline__ void trace_phase(int slot, int ph) {
+#if NVFP4_PHASE_TRACE
+    trace_word(slot, 2 * ph, global_ns());
+    trace_word(slot, 2 * ph + 1, static_cast<unsigned long long>(clock64()));
+    if (ph == 0) {
+        uint32_t sm;
+        asm volatile("mov.u32 %0, %%smid;" : "=r"(sm));
+        trace_word(slot, 24, sm);
+    }
+#else
+    (void)slot; (void)ph;
+#endif
 }
 
 __device__ __forceinline__ void raise_status(int bits, int32_t* user) {
@@ -1199,6 +1240,7 @@ struct TileParams {
     int32_t* status_user;     // optional device status word
     int E, top_k, slots, x_per_slot;
     uint32_t moe_off;         // TileMoe tables
+    int trace_slot;           // phase-trace launch slot (diagnostic builds only)
 };
 
 // Routed-expert groups of one launch, built by every CTA from the ids: a group is one expert
@@ -1345,6 +1387,13 @@ __device__ bool stage_x_direct(const uint16_t* __restrict__ x, const int* rowsel
 // trip for the whole slice instead of one per batch of loads. A wait that runs out (budget)
 // sets NVFP4_DEV_TIMEOUT, drains the copy and reports the slice inexact, so the caller
 // re-stages it from global memory. Needs 16-byte aligned x rows and k0 and kn multiples of 128.
+// Iterations of stage_x_bulk's in-place conversion loop for warp gi of gw sharing nblk 256-byte
+// blocks (two per warp and iteration, one per half-warp). It depends on no lane and no x value:
+// the loop body holds a __syncwarp, so every lane of the warp must run the same count.
+__host__ __device__ __forceinline__ int bulk_convert_trips(int gi, int gw, int nblk) {
+    return gi * 2 < nblk ? (nblk - gi * 2 + gw * 2 - 1) / (gw * 2) : 0;
+}
+
 __device__ bool stage_x_bulk(const uint16_t* __restrict__ x, const int* rowsel, int M, int K, int k0, int kn,
                              uint8_t* xs, uint32_t sstride, uint32_t* vote, uint64_t* bar, int gi, int gw,
                              int bar_id, int lane, uint64_t budget) {
@@ -1374,8 +1423,9 @@ __device__ bool stage_x_bulk(const uint16_t* __restrict__ x, const int* rowsel, 
     const int half = lane >> 4, pos = lane & 15;
     const int t = pos >> 2, q = pos & 3;
     // the trip count must not depend on the lane: the loop body holds a __syncwarp
-    for (int b0 = gi * 2; landed && b0 < nblk; b0 += gw * 2) {
-        const int b = b0 + half;
+    const int trips = landed ? bulk_convert_trips(gi, gw, nblk) : 0;
+    for (int it = 0; it < trips; ++it) {
+        const int b = gi * 2 + it * gw * 2 + half;
         uint8_t* blk = nullptr;
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
         if (b < nblk) {
@@ -1700,6 +1750,7 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_kernel(const __grid
     const uint32_t ring_w = base + p.ring_w + static_cast<uint32_t>(warp * stages) * kWBox;
     const uint32_t ring_s = base + p.ring_s + static_cast<uint32_t>(warp * stages) * kSBox;
     TileMoe* const tab = reinterpret_cast<TileMoe*>(sbase + p.moe_off);
+    if (tid == 0) trace_phase(p.trace_slot, 0);
 
     const int S = 1 << p.s_log2;
     const int rank = S > 1 ? static_cast<int>(cluster_rank()) : 0;
@@ -1793,8 +1844,10 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_kernel(const __grid
             prefetch_l2_bulk(p.x + static_cast<int64_t>(lane) * p.K + kb, static_cast<uint32_t>(kbytes));
         }
     }
+    if (tid == 0) trace_phase(p.trace_slot, 1);
     pdl_launch_dependents();
     pdl_wait();
+    if (tid == 0) trace_phase(p.trace_slot, 2);
 
     int M = p.M;                 // x rows staged by this CTA
     const int* rowsel = nullptr; // their global row numbers (MoE)
@@ -1843,6 +1896,8 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_kernel(const __grid
     }
     const bool use_f32 = lossy || p.force_f32;
     if (use_f32 && M > 0 && tin == 0 && lane == 0) atomicAdd(&g_fp32_fallbacks, 1ull);
+    if (tid == 0) trace_phase(p.trace_slot, 3);
+    bool traced_first = false;
 
     const int g = lane >> 2;
     const int ra = tile_row_perm<NC>(g), rb = ra + 8;
@@ -1886,6 +1941,11 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_kernel(const __grid
                 if (!__all_sync(0xffffffffu, budget != 0 && mbar_wait(&bars[st], ph, budget))) {
                     dead = true;  // warp-uniform: stop computing, keep the CTA's barrier count
                     break;
+                }
+                if (NVFP4_PHASE_TRACE && lane == 0 && !traced_first) {
+                    if (warp == 0) trace_phase(p.trace_slot, 4);
+                    else trace_word(p.trace_slot, 24 + warp, global_ns());
+                    traced_first = true;
                 }
                 if (!use_f32) {
                     tile_slot_mma<NC>(ring_w + st * kWBox, ring_s + st * kSBox, xa, b * NC * 2, ra, t, dd);
@@ -2047,6 +2107,8 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_kernel(const __grid
             }
         }
     }
+    if (lane == 0) trace_word(p.trace_slot, 16 + warp, global_ns());
+    if (tid == 0) trace_phase(p.trace_slot, 6);
     // no CTA may leave while another rank of its cluster can still read its partial sums
     if (S > 1) cluster_sync_all();
     // copies still in flight (only after a timeout) must land before the CTA exits
@@ -2057,13 +2119,14 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_kernel(const __grid
         }
     }
     __syncwarp();
+    if (tid == 0) trace_phase(p.trace_slot, 7);
 }
 
 #ifndef NVFP4_MOE_EARLY
 #define NVFP4_MOE_EARLY 1  // weight slots a MoE warp requests before x staging (the rest after it)
 #endif
 #ifndef NVFP4_SK_GROUP_ALIGNED
-#define NVFP4_SK_GROUP_ALIGNED 0  // 1: the planner may keep each stream-K CTA inside one expert group
+#define NVFP4_SK_GROUP_ALIGNED 1  // 1: the planner may keep each stream-K CTA inside one expert group (0: never)
 #endif
 
 // Stream-K form of the warp-tile kernel, for launches with many tiles per CTA (all 8 warps
@@ -2090,6 +2153,7 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_sk_kernel(const __g
     const uint32_t ring_w = base + p.ring_w + static_cast<uint32_t>(warp * stages) * kWBox;
     const uint32_t ring_s = base + p.ring_s + static_cast<uint32_t>(warp * stages) * kSBox;
     TileMoe* const tab = reinterpret_cast<TileMoe*>(sbase + p.moe_off);
+    if (tid == 0) trace_phase(p.trace_slot, 0);
     // partial records of warp w: the first 1 KB of its own ring, free once its boxes are consumed
     auto rec_of = [&](int w, int slot) -> float* {
         return reinterpret_cast<float*>(sbase + p.ring_w + static_cast<uint32_t>(w * stages) * kWBox) + slot * 128;
@@ -2169,8 +2233,10 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_sk_kernel(const __g
         if (warp == tk::kWarps - 2 && lane < xrows_all)
             prefetch_l2_bulk(p.x + static_cast<int64_t>(lane) * p.K, static_cast<uint32_t>(p.K) * 2u);
     }
+    if (tid == 0) trace_phase(p.trace_slot, 1);
     pdl_launch_dependents();
     pdl_wait();
+    if (tid == 0) trace_phase(p.trace_slot, 2);
 
     int M = p.M;
     const int* rowsel = nullptr;
@@ -2187,8 +2253,14 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_sk_kernel(const __g
                 const int lo = static_cast<int>(static_cast<long long>(G) * g / ng);
                 const int c = static_cast<int>(static_cast<long long>(G) * (g + 1) / ng) - lo;
                 const int i = b - lo;
-                j0 = g * tiles + static_cast<int>(static_cast<long long>(tiles) * i / c);
-                j1 = g * tiles + static_cast<int>(static_cast<long long>(tiles) * (i + 1) / c);
+                if (c > 0 && i >= 0 && i < c) {
+                    j0 = g * tiles + static_cast<int>(static_cast<long long>(tiles) * i / c);
+                    j1 = g * tiles + static_cast<int>(static_cast<long long>(tiles) * (i + 1) / c);
+                } else {
+                    // fewer CTAs than groups (the planner rules it out): no work, flagged
+                    j0 = j1 = 0;
+                    if (tid == 0) raise_status(NVFP4_DEV_INTERNAL, p.status_user);
+                }
             } else {
                 j0 = j1 = 0;
             }
@@ -2235,6 +2307,8 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_sk_kernel(const __g
     }
     const bool use_f32 = lossy || p.force_f32;
     if (use_f32 && M > 0 && warp == 0 && lane == 0) atomicAdd(&g_fp32_fallbacks, 1ull);
+    if (tid == 0) trace_phase(p.trace_slot, 3);
+    bool traced_first = false;
 
     const int g = lane >> 2;
     const int ra = tile_row_perm<NC>(g), rb = ra + 8;
@@ -2296,6 +2370,11 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_sk_kernel(const __g
                     dead = true;
                     raise_status(NVFP4_DEV_TIMEOUT, nullptr);
                 } else {
+                    if (NVFP4_PHASE_TRACE && lane == 0 && !traced_first) {
+                        if (warp == 0) trace_phase(p.trace_slot, 4);
+                        else trace_word(p.trace_slot, 24 + warp, global_ns());
+                        traced_first = true;
+                    }
                     if (!use_f32) {
                         tile_slot_mma<NC>(ring_w + st * kWBox, ring_s + st * kSBox, xa, kb * NC * 2, ra, t, dd);
                     } else {
@@ -2369,6 +2448,8 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_sk_kernel(const __g
                 ++kb;
             }
         }
+        if (lane == 0) trace_word(p.trace_slot, 16 + warp, global_ns());
+        if (tid == 0) trace_phase(p.trace_slot, 5);
         // the ring is idle once every issued copy has landed (only a timed-out warp has any left)
         if (lane == 0) {
             while (consumed < issued) {
@@ -2414,6 +2495,7 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_sk_kernel(const __g
             }
         }
     }
+    if (tid == 0) trace_phase(p.trace_slot, 6);
     if (lane == 0) {
         while (consumed < issued) {
             mbar_wait(&bars[cons_st], cons_ph, kDrainWaitNs);
@@ -2421,6 +2503,7 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_sk_kernel(const __g
         }
     }
     __syncwarp();
+    if (tid == 0) trace_phase(p.trace_slot, 7);
 }
 
 // ------------------------------------------------------------------ byte-load kernel
@@ -3160,7 +3243,16 @@ cudaError_t launch_tile_nc(const TilePlan& tp, cudaStream_t st) {
     return cudaLaunchKernelEx(&cfg, kern, tp.p);
 }
 
-cudaError_t launch_tile(const TilePlan& tp, cudaStream_t st, bool moe) {
+// Launch slot of the phase trace: consecutive tile-kernel launches use consecutive slots.
+int g_trace_next = 0;
+
+cudaError_t launch_tile(const TilePlan& tp_in, cudaStream_t st, bool moe) {
+    TilePlan tp = tp_in;
+    if (NVFP4_PHASE_TRACE) {
+        std::lock_guard<std::mutex> lk(g_mu);
+        tp.p.trace_slot = g_trace_next;
+        g_trace_next = (g_trace_next + 1) % kTraceLaunches;
+    }
     if (moe && tp.sk) return tp.nc == 2 ? launch_tile_nc<2, true, true>(tp, st) : launch_tile_nc<1, true, true>(tp, st);
     if (moe) return tp.nc == 2 ? launch_tile_nc<2, true, false>(tp, st) : launch_tile_nc<1, true, false>(tp, st);
     if (tp.p.swiglu)
@@ -3198,6 +3290,70 @@ nvfp4_status zero_output(void* y, int64_t elems, int y_type, cudaStream_t st) {
     return e == cudaSuccess ? NVFP4_OK : cuda_fail(e);
 }
 
+// Tile-kernel plans with their encoded tensor maps, reused by later calls with the same device,
+// shape, kernel selection and weight pointers (a tensor map holds nothing else: the same
+// pointer and shape always give the same map). Direct-mapped; a colliding call replaces the
+// entry. Per-call values (x, y, scales, output type) are filled in after the lookup.
+struct PlanKey {
+    int dev, kind, M, N, K, groups, variant, E, T, top_k, xps;
+    const void* w[2];
+    const void* s[2];
+    bool operator==(const PlanKey& o) const { return std::memcmp(this, &o, sizeof(PlanKey)) == 0; }
+};
+struct PlanEntry {
+    PlanKey key;
+    bool used;
+    bool tile;       // false: the tile kernel does not take this call
+    TilePlan tp;
+};
+constexpr int kPlanCacheSize = 64;
+PlanEntry g_plan_cache[kPlanCacheSize];
+
+PlanKey make_key(int dev, int kind, int M, int N, int K, int groups, const uint8_t* const* w,
+                 const uint8_t* const* s, int E = 0, int T = 0, int top_k = 0, int xps = 0) {
+    PlanKey k;
+    std::memset(&k, 0, sizeof k);  // padding included: keys compare as bytes
+    k.dev = dev; k.kind = kind; k.M = M; k.N = N; k.K = K; k.groups = groups; k.variant = g_variant;
+    k.E = E; k.T = T; k.top_k = top_k; k.xps = xps;
+    for (int i = 0; i < 2; ++i) {
+        k.w[i] = w[i < groups ? i : 0];
+        k.s[i] = s[i < groups ? i : 0];
+    }
+    return k;
+}
+
+uint32_t key_slot(const PlanKey& k) {
+    const unsigned char* b = reinterpret_cast<const unsigned char*>(&k);
+    uint32_t h = 2166136261u;  // FNV-1a over the key's bytes
+    for (size_t i = 0; i < sizeof k; ++i) h = (h ^ b[i]) * 16777619u;
+    return h % kPlanCacheSize;
+}
+
+// The cached tile plan for key k, built by `make` (returns false when the tile kernel does not
+// take the call) on a miss. Returns whether the tile kernel takes the call; *out gets the plan.
+template <typename F>
+bool cached_tile_plan(const PlanKey& k, TilePlan* out, F&& make) {
+    const uint32_t slot = key_slot(k);
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        const PlanEntry& e = g_plan_cache[slot];
+        if (e.used && e.key == k) {
+            if (e.tile) *out = e.tp;
+            return e.tile;
+        }
+    }
+    TilePlan tp{};
+    const bool tile = make(tp);
+    std::lock_guard<std::mutex> lk(g_mu);
+    PlanEntry& e = g_plan_cache[slot];
+    e.key = k;
+    e.used = true;
+    e.tile = tile;
+    e.tp = tp;
+    if (tile) *out = tp;
+    return tile;
+}
+
 // Dense (groups = 1) and gate/up (groups = 2) calls; swiglu: gate/up with the fused
 // activation, y [M, N] = silu(clamp(gate)) * clamp(up).
 nvfp4_status run_dense(const uint8_t* const* w, const uint8_t* const* s, const float* g, int groups,
@@ -3216,30 +3372,34 @@ nvfp4_status run_dense(const uint8_t* const* w, const uint8_t* const* s, const f
     const DeviceInfo* d = device_info(&dev);
     if (!d) return cuda_fail(cudaGetLastError());
     TilePlan tpl{};
-    if (plan_tile(tpl, M, N, K, groups, *d, w, s, x, false, 0, 0, swiglu)) {
-        TileParams& p = tpl.p;
-        bool ok = true;
-        for (int i = 0; i < groups && ok; ++i) ok = encode_tile_maps(&p.wmap[i], &p.smap[i], w[i], s[i], N, K, tpl.nc);
-        if (ok) {
-            if (groups == 1) {
-                p.wmap[1] = p.wmap[0];
-                p.smap[1] = p.smap[0];
-            }
-            p.x = x;
-            p.y = y;
-            p.g[0] = g[0];
-            p.g[1] = g[groups > 1 ? 1 : 0];
-            p.ldy = ldy;
-            p.swiglu = swiglu ? 1 : 0;
-            p.clamp = clamp;
-            p.out_bf16 = y_type == NVFP4_OUT_BF16;
-            p.force_f32 = g_variant == 2;
-            p.wait_ns = g_wait_ns;
-            const cudaError_t e = launch_tile(tpl, st, false);
-            if (e != cudaSuccess) return cuda_fail(e);
-            const cudaError_t e2 = cudaGetLastError();
-            return e2 == cudaSuccess ? NVFP4_OK : cuda_fail(e2);
+    const bool x_ok = (reinterpret_cast<uintptr_t>(x) & 15) == 0;  // the only x property a plan reads
+    const PlanKey key = make_key(dev, (swiglu ? 4 : groups) + (x_ok ? 0 : 8), M, N, K, groups, w, s);
+    const bool tile = cached_tile_plan(key, &tpl, [&](TilePlan& tp) {
+        if (!plan_tile(tp, M, N, K, groups, *d, w, s, x, false, 0, 0, swiglu)) return false;
+        for (int i = 0; i < groups; ++i)
+            if (!encode_tile_maps(&tp.p.wmap[i], &tp.p.smap[i], w[i], s[i], N, K, tp.nc)) return false;
+        if (groups == 1) {
+            tp.p.wmap[1] = tp.p.wmap[0];
+            tp.p.smap[1] = tp.p.smap[0];
         }
+        return true;
+    });
+    if (tile) {
+        TileParams& p = tpl.p;
+        p.x = x;
+        p.y = y;
+        p.g[0] = g[0];
+        p.g[1] = g[groups > 1 ? 1 : 0];
+        p.ldy = ldy;
+        p.swiglu = swiglu ? 1 : 0;
+        p.clamp = clamp;
+        p.out_bf16 = y_type == NVFP4_OUT_BF16;
+        p.force_f32 = g_variant == 2;
+        p.wait_ns = g_wait_ns;
+        const cudaError_t e = launch_tile(tpl, st, false);
+        if (e != cudaSuccess) return cuda_fail(e);
+        const cudaError_t e2 = cudaGetLastError();
+        return e2 == cudaSuccess ? NVFP4_OK : cuda_fail(e2);
     }
     Plan pl{};
     if (!swiglu && plan_dense(pl, M, N, K, groups, *d, w, s, x)) {
@@ -3324,7 +3484,8 @@ nvfp4_status nvfp4_moe_gemv(const uint8_t* w_packed, const uint8_t* w_scales,
     const int slots = T * top_k;
     if (slots == 0 || N == 0) return NVFP4_OK;
     if (K == 0) return zero_output(y, static_cast<int64_t>(slots) * N, y_type, st);
-    const DeviceInfo* d = device_info(nullptr);
+    int dev = 0;
+    const DeviceInfo* d = device_info(&dev);
     if (!d) return cuda_fail(cudaGetLastError());
     if (slots <= kTileMoeSlots && static_cast<int64_t>(E) * N <= (1 << 30)) {
         // warp-tile kernel: every routed expert's slab is read once for all of its slots
@@ -3332,12 +3493,19 @@ nvfp4_status nvfp4_moe_gemv(const uint8_t* w_packed, const uint8_t* w_scales,
         const uint8_t* wv[1] = {w_packed};
         const uint8_t* sv[1] = {w_scales};
         const int xrows = x_per_slot ? slots : T;
-        if (plan_tile(tpl, 8, N, K, expected_groups(E, T, top_k), *d, wv, sv, x, true, xrows, slots) &&
-            encode_tile_maps(&tpl.p.wmap[0], &tpl.p.smap[0], w_packed, w_scales, static_cast<int64_t>(E) * N, K,
-                             tpl.nc)) {
+        const bool x_ok = (reinterpret_cast<uintptr_t>(x) & 15) == 0;
+        const PlanKey key = make_key(dev, 5 + (x_ok ? 0 : 8), 8, N, K, 1, wv, sv, E, T, top_k, x_per_slot ? 1 : 0);
+        const bool tile = cached_tile_plan(key, &tpl, [&](TilePlan& tp) {
+            if (!plan_tile(tp, 8, N, K, expected_groups(E, T, top_k), *d, wv, sv, x, true, xrows, slots)) return false;
+            if (!encode_tile_maps(&tp.p.wmap[0], &tp.p.smap[0], w_packed, w_scales, static_cast<int64_t>(E) * N, K,
+                                  tp.nc))
+                return false;
+            tp.p.wmap[1] = tp.p.wmap[0];
+            tp.p.smap[1] = tp.p.smap[0];
+            return true;
+        });
+        if (tile) {
             TileParams& p = tpl.p;
-            p.wmap[1] = p.wmap[0];
-            p.smap[1] = p.smap[0];
             p.x = x;
             p.y = y;
             p.ldy = N;
@@ -3427,6 +3595,29 @@ void nvfp4_set_wait_budget_ns(uint64_t ns) { g_wait_ns = ns == UINT64_MAX ? kDef
 void nvfp4_set_variant(int variant) { g_variant = variant; }
 
 void nvfp4_set_pdl(int enable) { g_pdl = enable != 0; }
+
+int nvfp4_phase_trace(uint64_t* host_out, int max_words, void* stream) {
+#if NVFP4_PHASE_TRACE
+    if (!host_out || max_words < 0) return -1;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(st) != cudaSuccess) return -1;
+    const int total = kTraceLaunches * kTraceCtas * kTraceWords;
+    const int n = std::min(total, max_words);
+    if (n > 0 && cudaMemcpyFromSymbol(host_out, g_trace, static_cast<size_t>(n) * 8) != cudaSuccess) return -1;
+    void* dev = nullptr;
+    if (cudaGetSymbolAddress(&dev, g_trace) != cudaSuccess) return -1;
+    if (cudaMemset(dev, 0, static_cast<size_t>(total) * 8) != cudaSuccess) return -1;
+    if (cudaDeviceSynchronize() != cudaSuccess) return -1;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        g_trace_next = 0;
+    }
+    return n;
+#else
+    (void)host_out; (void)max_words; (void)stream;
+    return 0;
+#endif
+}
 
 long long nvfp4_fp32_fallbacks(void* stream) {
     cudaStream_t st = static_cast<cudaStream_t>(stream);

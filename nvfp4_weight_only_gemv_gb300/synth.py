@@ -127,15 +127,17 @@ def routing(T: int, top_k: int, E: int, seed: int) -> torch.Tensor:
 
 
 def moe_problem(E: int, N: int, K: int, T: int, top_k: int, x_per_slot: bool, seed: int,
-                device="cpu", fill: str = "routed"):
+                device="cpu", fill: str = "routed", ids=None):
     """Routed-expert problem: w [E, N, K/2], s [E, N, K/16], gs [E] f32, ids, x.
 
     Expert e's weight comes from seed ``seed * 1000 + e``. ``fill="routed"``
     generates only the experts that ``ids`` names. The others keep zero bytes
     (code 0, scale 0) and a global scale of 1. That is enough for anything that reads only the routed
-    slabs, and it keeps CPU generation fast. ``fill="all"`` generates every expert.
+    slabs, and it keeps CPU generation fast. ``fill="all"`` generates every expert. ``ids``
+    (T * top_k ints) replaces the seeded routing when given.
     """
-    ids = routing(T, top_k, E, seed)
+    ids = routing(T, top_k, E, seed) if ids is None else torch.as_tensor(ids, dtype=torch.int32).reshape(-1).cpu()
+    assert ids.numel() == T * top_k
     w = torch.zeros(E, N, K // 2, dtype=torch.uint8, device=device)
     s = torch.zeros(E, N, K // 16, dtype=torch.uint8, device=device)
     gs = torch.ones(E, dtype=torch.float32)

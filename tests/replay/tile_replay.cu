@@ -53,6 +53,30 @@ static void check_bulk(const TileParams& p, int slices, int rows, int kn_max, in
         CHECK((k0_step * 2) % 16 == 0 && (kn_max * 2) % 16 == 0, "bulk source alignment and size");
         CHECK(rows * kn_max * 2 < (1 << 20), "mbarrier transaction count");
     }
+    // the in-place conversion: one trip count per warp whatever the lane or the x values (the
+    // loop's only inputs are the warp's number, the slice's warps and the block count), and the
+    // blocks its half-warps take cover the slice exactly once
+    for (int gw = 1; gw <= 8; gw *= 2) {
+        for (int nblk = 0; nblk <= 16 * 96; nblk += (nblk < 64 ? 1 : 37)) {
+            std::vector<int> seen(nblk, 0);
+            for (int gi = 0; gi < gw; ++gi) {
+                const int trips = bulk_convert_trips(gi, gw, nblk);
+                for (int lane = 0; lane < 32; ++lane) {
+                    const int half = lane >> 4;
+                    int own = 0;
+                    for (int it = 0; it < trips; ++it) {
+                        const int b = gi * 2 + it * gw * 2 + half;
+                        if (b < nblk && (lane & 15) == 0) ++seen[b];
+                        own += b < nblk;
+                    }
+                    CHECK(own <= trips, "trip count %d gw %d nblk %d", trips, gw, nblk);
+                }
+                // the last trip still has work for the warp: no trip is wasted on every lane
+                CHECK(trips == 0 || gi * 2 + (trips - 1) * gw * 2 < nblk, "trips gi %d gw %d nblk %d", gi, gw, nblk);
+            }
+            for (int b = 0; b < nblk; ++b) CHECK(seen[b] == 1, "block %d of %d converted %d times (gw %d)", b, nblk, seen[b], gw);
+        }
+    }
     // raw chunk 4t + q holds elements 32t + 8q .. + 7; the staged order puts them at chunk 4q + t
     for (int pos = 0; pos < 16; ++pos) {
         const int t = pos >> 2, q = pos & 3;

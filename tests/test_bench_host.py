@@ -62,12 +62,19 @@ def test_reference_arm_runs_on_rank_zero_only(monkeypatch, capsys):
     assert capsys.readouterr().out == ""
 
 
-def test_traffic_record_matches_the_kernel_source(monkeypatch):
-    rec = json.load(open(os.path.join(bench.ROOT, "profiles", "traffic.json")))
-    assert rec["kernel_source_sha256"] == bench.kernel_source_sha256()
-    assert bench.kernel_traffic("attn") == rec["dram_bytes_per_launch"]["attn"]
+def test_traffic_record_is_used_only_for_the_source_it_was_measured_on(monkeypatch, tmp_path):
+    # the committed record carries the kernel source's sha256 it was captured on; bench.py
+    # reports its figures only while the source is unchanged, and null otherwise
+    rec = json.load(open(bench.TRAFFIC_PATH))
+    assert len(rec["kernel_source_sha256"]) == 64 and rec["dram_bytes_per_launch"]
+    fake = dict(rec, kernel_source_sha256=bench.kernel_source_sha256())
+    path = tmp_path / "traffic.json"
+    path.write_text(json.dumps(fake))
+    monkeypatch.setattr(bench, "TRAFFIC_PATH", str(path))
+    name = next(iter(rec["dram_bytes_per_launch"]))
+    assert bench.kernel_traffic(name) == rec["dram_bytes_per_launch"][name]
     monkeypatch.setattr(bench, "kernel_source_sha256", lambda: "0" * 64)
-    assert bench.kernel_traffic("attn") is None
+    assert bench.kernel_traffic(name) is None
 
 
 def test_workload_byte_accounting():
@@ -87,3 +94,24 @@ def test_cpu_baseline_reports_the_oracle_on_a_bounded_sample():
     assert base["kind"] == "oracle" and base["cores"] >= 1 and base["value"] > 0
     assert base["unit"].startswith("GB/s")
     assert "every GEMV of one step" in base["sample"] or "% of the output rows" in base["sample"]
+
+
+def test_in_run_output_check_accepts_oracle_outputs_and_flags_a_wrong_one():
+    # bench.py checks a sample of every timed output against the oracle; here the "timed"
+    # outputs are the oracle's own values (accepted), then one column is spoiled (flagged)
+    import oracle
+    from nvfp4_weight_only_gemv_gb300 import synth
+    calls = [bench.Call(("dense", 40, 256, 2, 3, "bf16"), "cpu", 1, "cpu"),
+             bench.Call(("gate_up_swiglu", 24, 256, 1, 4, "f32"), "cpu", 1, "cpu")]
+    h = calls[0].host
+    yr, _ = oracle.gemv(h["w"].numpy(), h["s"].numpy(), h["g"], synth.bf16_bits(h["x"]))
+    calls[0].sets[0]["y"].copy_(torch.from_numpy(yr).to(torch.bfloat16))
+    h = calls[1].host
+    yr, _ = oracle.gate_up_swiglu(h["wg"].numpy(), h["sg"].numpy(), h["gg"], h["wu"].numpy(), h["su"].numpy(),
+                                  h["gu"], synth.bf16_bits(h["x"]), bench.SWIGLU_CLAMP)
+    calls[1].sets[0]["y"].copy_(torch.from_numpy(yr).float())
+    res = bench.check_outputs(calls, n_cols=64)
+    assert res["ok"] and res["checked"] == 2 * 40 + 24 and res["outside_tolerance"] == 0
+    calls[0].sets[0]["y"][1, 7] += 0.5
+    res = bench.check_outputs(calls, n_cols=64)
+    assert not res["ok"] and res["outside_tolerance"] == 1
