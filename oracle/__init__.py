@@ -75,6 +75,19 @@ def _declare(lib):
                                           ctypes.c_int64, ctypes.c_int64, c_i64p, ctypes.c_int64,
                                           c_dp, c_dp, c_i64p]
     lib.nvfp4_oracle_moe_gemv.restype = ctypes.c_int
+    lib.nvfp4_oracle_sdict_index.argtypes = [c_u8p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64]
+    lib.nvfp4_oracle_sdict_index.restype = ctypes.c_int
+    lib.nvfp4_oracle_sdict_idx_bytes.argtypes = [ctypes.c_int64, ctypes.c_int64]
+    lib.nvfp4_oracle_sdict_idx_bytes.restype = ctypes.c_int64
+    lib.nvfp4_oracle_gemv_sdict.argtypes = [c_u8p, c_u8p, c_u8p, ctypes.c_double, c_u16p, ctypes.c_int64,
+                                            ctypes.c_int64, ctypes.c_int64, c_i64p, ctypes.c_int64, c_dp, c_dp]
+    lib.nvfp4_oracle_gemv_sdict.restype = ctypes.c_int
+    lib.nvfp4_oracle_moe_gemv_sdict.argtypes = [c_u8p, c_u8p, c_u8p, ctypes.POINTER(ctypes.c_float),
+                                                ctypes.c_int64, ctypes.POINTER(ctypes.c_int32),
+                                                ctypes.c_int64, ctypes.c_int64, c_u16p, ctypes.c_int,
+                                                ctypes.c_int64, ctypes.c_int64, c_i64p, ctypes.c_int64,
+                                                c_dp, c_dp, c_i64p]
+    lib.nvfp4_oracle_moe_gemv_sdict.restype = ctypes.c_int
     return lib
 
 
@@ -229,4 +242,65 @@ def moe_gemv(w, s, gs, ids, x_bits, x_per_slot, top_k, rows=None, lib=None):
                                    _ptr(ya, ctypes.c_double), _ptr(bad, ctypes.c_int64))
     if rc != 0:
         raise ValueError("oracle moe: bad arguments")
+    return y, ya, int(bad[0])
+
+
+def sdict_idx_bytes(N: int, K: int, lib=None) -> int:
+    """Bytes of the index plane of one [N, K] dictionary-scaled tensor."""
+    return int((lib or load()).nvfp4_oracle_sdict_idx_bytes(int(N), int(K)))
+
+
+def sdict_index(idx, K: int, n: int, b: int, lib=None) -> int:
+    """The 5-bit dictionary index of block b of row n (index layout in nvfp4_oracle.c)."""
+    idx = _u8(idx).reshape(-1)
+    return int((lib or load()).nvfp4_oracle_sdict_index(_ptr(idx, ctypes.c_uint8), int(K), int(n), int(b)))
+
+
+def gemv_sdict(w, idx, sdict, g, x_bits, rows=None, lib=None):
+    """Dense oracle with dictionary scales: w [N, K/2] u8, idx the packed 5-bit index plane
+    (sdict_idx_bytes(N, K) bytes), sdict [32] E4M3 codes. Returns y, yabs like gemv."""
+    lib = lib or load()
+    w, x = _u8(w), _u16(x_bits)
+    idx, sdict = _u8(idx).reshape(-1), _u8(sdict).reshape(-1)
+    N, K = w.shape[0], w.shape[1] * 2
+    M = x.shape[0]
+    assert idx.size == sdict_idx_bytes(N, K, lib) and sdict.size == 32 and x.shape == (M, K)
+    r, rp = _rows(rows)
+    nr = N if r is None else r.shape[0]
+    y = np.empty((M, nr), dtype=np.float64)
+    ya = np.empty((M, nr), dtype=np.float64)
+    rc = lib.nvfp4_oracle_gemv_sdict(_ptr(w, ctypes.c_uint8), _ptr(idx, ctypes.c_uint8), _ptr(sdict, ctypes.c_uint8),
+                                     float(g), _ptr(x, ctypes.c_uint16), M, N, K, rp, nr,
+                                     _ptr(y, ctypes.c_double), _ptr(ya, ctypes.c_double))
+    if rc != 0:
+        raise ValueError("oracle gemv_sdict: bad arguments")
+    return y, ya
+
+
+def moe_gemv_sdict(w, idx, sdict, gs, ids, x_bits, x_per_slot, top_k, rows=None, lib=None):
+    """Routed-expert oracle with dictionary scales: w [E, N, K/2], idx [E, sdict_idx_bytes(N, K)],
+    sdict [E, 32]. Returns y, yabs and the count of out-of-range ids, like moe_gemv."""
+    lib = lib or load()
+    w, x = _u8(w), _u16(x_bits)
+    E, N, K = w.shape[0], w.shape[1], w.shape[2] * 2
+    idx, sdict = _u8(idx).reshape(-1), _u8(sdict).reshape(-1)
+    gs = np.ascontiguousarray(np.asarray(gs), dtype=np.float32)
+    ids = np.ascontiguousarray(np.asarray(ids).reshape(-1), dtype=np.int32)
+    assert idx.size == E * sdict_idx_bytes(N, K, lib) and sdict.size == 32 * E and gs.shape == (E,)
+    slots = ids.shape[0]
+    assert slots % top_k == 0
+    T = slots // top_k
+    assert x.shape == ((slots if x_per_slot else T), K)
+    r, rp = _rows(rows)
+    nr = N if r is None else r.shape[0]
+    y = np.empty((slots, nr), dtype=np.float64)
+    ya = np.empty((slots, nr), dtype=np.float64)
+    bad = np.zeros(1, dtype=np.int64)
+    rc = lib.nvfp4_oracle_moe_gemv_sdict(_ptr(w, ctypes.c_uint8), _ptr(idx, ctypes.c_uint8),
+                                         _ptr(sdict, ctypes.c_uint8), _ptr(gs, ctypes.c_float), E,
+                                         _ptr(ids, ctypes.c_int32), T, top_k, _ptr(x, ctypes.c_uint16),
+                                         int(bool(x_per_slot)), N, K, rp, nr, _ptr(y, ctypes.c_double),
+                                         _ptr(ya, ctypes.c_double), _ptr(bad, ctypes.c_int64))
+    if rc != 0:
+        raise ValueError("oracle moe_gemv_sdict: bad arguments")
     return y, ya, int(bad[0])

@@ -34,6 +34,7 @@
  */
 #include <math.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 #ifdef _OPENMP
 #include <omp.h>
@@ -276,6 +277,121 @@ int nvfp4_oracle_moe_gemv(const uint8_t *w, const uint8_t *s, const float *gs, i
             y[sl * nrows + i] = g * sum;
             yabs[sl * nrows + i] = fabs(g) * abs_sum;
         }
+    }
+    return 0;
+}
+
+/*
+ * Scale-dictionary NVFP4 ("glm-5.3-flash-nvfp4-tp3-512k--gb10 card.json", performance[64],
+ * field `note`: routed gate+up weights at 4.3125 bit/weight with a scale dictionary, while a
+ * tensor kept plain reads 4.5). Reading (the pages give only the bit budget):
+ *   - the E2M1 codes stay [N, K/2] bytes (4 bits per weight);
+ *   - the [N, K/16] E4M3 block scales are replaced by one 5-bit index per 16-element block
+ *     into a table `dict` of 32 E4M3 codes for the whole tensor: 4 + 5/16 = 4.3125 bits per
+ *     weight. A tensor whose scales need more than 32 codes stays plain (4 + 8/16 = 4.5), so
+ *     the coding is exact: block b of row n has the scale E4M3(dict[index(n, b)]);
+ *   - index layout: K % 256 == 0; for each 16-row tile r (rows 16r .. 16r + 15; N rounded up
+ *     to a multiple of 16) and 256-column segment c (blocks 16c .. 16c + 15) a 160-byte record
+ *     at byte (r * (K / 256) + c) * 160 holds the 256 indices of (row 16r + i, block 16c + j)
+ *     at position q = 16 i + j, as bits 5q .. 5q + 4 (least significant first) of the record
+ *     read as a bit stream in which bit p is bit p % 8 of byte p / 8.
+ */
+int nvfp4_oracle_sdict_index(const uint8_t *idx, int64_t K, int64_t n, int64_t b) {
+    const uint8_t *rec = idx + ((n / 16) * (K / 256) + b / 16) * 160;
+    int64_t q = (n % 16) * 16 + (b % 16);
+    int v = 0;
+    for (int i = 0; i < 5; ++i) {
+        int64_t bit = 5 * q + i;
+        v |= ((rec[bit / 8] >> (bit % 8)) & 1) << i;
+    }
+    return v;
+}
+
+/* Bytes of the index plane of one [N, K] tensor. */
+int64_t nvfp4_oracle_sdict_idx_bytes(int64_t N, int64_t K) {
+    return ((N + 15) / 16) * (K / 256) * 160;
+}
+
+/* Row n's block scales as plain E4M3 codes: srow[b] = dict[index(n, b)]. */
+static void sdict_scale_row(const uint8_t *idx, const uint8_t *dict, int64_t K, int64_t n, uint8_t *srow) {
+    for (int64_t b = 0; b < K / 16; ++b) srow[b] = dict[nvfp4_oracle_sdict_index(idx, K, n, b)];
+}
+
+/*
+ * Dense GEMV with dictionary scales: w [N, K/2], idx (layout above), dict [32] E4M3 codes.
+ * Otherwise as nvfp4_oracle_gemv. Returns 0, or -1 on a bad argument (K % 256 != 0 included).
+ */
+int nvfp4_oracle_gemv_sdict(const uint8_t *w, const uint8_t *idx, const uint8_t *dict, double g,
+                            const uint16_t *x, int64_t M, int64_t N, int64_t K, const int64_t *rows,
+                            int64_t nrows, double *y, double *yabs) {
+    if (K % 256 != 0 || M < 0 || N < 0 || K < 0) return -1;
+    if (rows == NULL) nrows = N;
+    for (int64_t i = 0; i < nrows; ++i) {
+        int64_t n = rows ? rows[i] : i;
+        if (n < 0 || n >= N) return -1;
+    }
+    int64_t i;
+#pragma omp parallel for schedule(static)
+    for (i = 0; i < nrows; ++i) {
+        int64_t n = rows ? rows[i] : i;
+        uint8_t srow[4096];
+        uint8_t *sr = K / 16 <= 4096 ? srow : (uint8_t *)malloc((size_t)(K / 16));
+        sdict_scale_row(idx, dict, K, n, sr);
+        for (int64_t m = 0; m < M; ++m) {
+            double sum, abs_sum;
+            dot_row(w + n * (K / 2), sr, x + m * K, K, &sum, &abs_sum);
+            y[m * nrows + i] = g * sum;
+            yabs[m * nrows + i] = fabs(g) * abs_sum;
+        }
+        if (sr != srow) free(sr);
+    }
+    return 0;
+}
+
+/*
+ * Routed-expert GEMV with dictionary scales: expert e's index plane starts at
+ * idx + e * nvfp4_oracle_sdict_idx_bytes(N, K) and its table at dict + 32 e. Otherwise as
+ * nvfp4_oracle_moe_gemv.
+ */
+int nvfp4_oracle_moe_gemv_sdict(const uint8_t *w, const uint8_t *idx, const uint8_t *dict, const float *gs,
+                                int64_t E, const int32_t *ids, int64_t T, int64_t top_k,
+                                const uint16_t *x, int x_per_slot, int64_t N, int64_t K,
+                                const int64_t *rows, int64_t nrows, double *y, double *yabs,
+                                int64_t *bad_ids) {
+    if (K % 256 != 0 || E < 0 || T < 0 || top_k < 0 || N < 0 || K < 0) return -1;
+    if (rows == NULL) nrows = N;
+    for (int64_t i = 0; i < nrows; ++i) {
+        int64_t n = rows ? rows[i] : i;
+        if (n < 0 || n >= N) return -1;
+    }
+    int64_t slots = T * top_k;
+    int64_t bad = 0;
+    for (int64_t sl = 0; sl < slots; ++sl)
+        if (ids[sl] < 0 || ids[sl] >= E) ++bad;
+    if (bad_ids) *bad_ids = bad;
+    int64_t plane = nvfp4_oracle_sdict_idx_bytes(N, K);
+    int64_t sl;
+#pragma omp parallel for schedule(static)
+    for (sl = 0; sl < slots; ++sl) {
+        int64_t e = ids[sl];
+        int64_t xrow = x_per_slot ? sl : sl / top_k;
+        uint8_t srow[4096];
+        uint8_t *sr = K / 16 <= 4096 ? srow : (uint8_t *)malloc((size_t)(K / 16));
+        for (int64_t i = 0; i < nrows; ++i) {
+            if (e < 0 || e >= E) {
+                y[sl * nrows + i] = 0.0;
+                yabs[sl * nrows + i] = 0.0;
+                continue;
+            }
+            int64_t n = rows ? rows[i] : i;
+            sdict_scale_row(idx + e * plane, dict + 32 * e, K, n, sr);
+            double g = (double)gs[e];
+            double sum, abs_sum;
+            dot_row(w + (e * N + n) * (K / 2), sr, x + xrow * K, K, &sum, &abs_sum);
+            y[sl * nrows + i] = g * sum;
+            yabs[sl * nrows + i] = fabs(g) * abs_sum;
+        }
+        if (sr != srow) free(sr);
     }
     return 0;
 }

@@ -17,6 +17,7 @@ import oracle
 from nvfp4_weight_only_gemv_gb300 import synth
 
 from test_oracle_pins import E2M1_TABLE, _arrays, _golden, dequant, torch_bf16, torch_e4m3
+from test_oracle_sdict import _golden as _sdict_golden, pack_indices, random_case
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "nvfp4_oracle.c")
 
@@ -45,6 +46,17 @@ MUTANTS = {
     "swiglu_args_swapped": ("y[m * nrows + i] = nvfp4_oracle_swiglu(gv, uv, lim);",
                             "y[m * nrows + i] = nvfp4_oracle_swiglu(uv, gv, lim);", 1),
     "swiglu_up_scale": ("double gv = gg * sg_sum, uv = gu * su_sum;", "double gv = gg * sg_sum, uv = gg * su_sum;", 1),
+    "sdict_index_width": ("    for (int i = 0; i < 5; ++i) {\n        int64_t bit", "    for (int i = 0; i < 4; ++i) {\n        int64_t bit", 1),
+    "sdict_index_stride": ("int64_t bit = 5 * q + i;", "int64_t bit = 6 * q + i;", 1),
+    "sdict_bit_order": ("v |= ((rec[bit / 8] >> (bit % 8)) & 1) << i;", "v |= ((rec[bit / 8] >> (7 - bit % 8)) & 1) << i;", 1),
+    "sdict_table_offset": ("srow[b] = dict[nvfp4_oracle_sdict_index(idx, K, n, b)];",
+                           "srow[b] = dict[(nvfp4_oracle_sdict_index(idx, K, n, b) + 1) & 31];", 1),
+    "sdict_position_transposed": ("int64_t q = (n % 16) * 16 + (b % 16);", "int64_t q = (b % 16) * 16 + (n % 16);", 1),
+    "sdict_record_order": ("((n / 16) * (K / 256) + b / 16) * 160", "((b / 16) * (K / 256) + n / 16) * 160", 1),
+    "sdict_moe_plane": ("sdict_scale_row(idx + e * plane, dict + 32 * e, K, n, sr);",
+                        "sdict_scale_row(idx, dict + 32 * e, K, n, sr);", 1),
+    "sdict_moe_table": ("sdict_scale_row(idx + e * plane, dict + 32 * e, K, n, sr);",
+                        "sdict_scale_row(idx + e * plane, dict, K, n, sr);", 1),
 }
 
 
@@ -107,6 +119,36 @@ def battery(lib):
     if not (np.allclose(y1, 0.75 * ln3, rtol=1e-15, atol=0) and
             np.allclose(y2, ln3 / (1.0 + math.exp(-1.0)), rtol=1e-15, atol=0)):
         fails.append("gate_up_swiglu_hand_worked")
+    # the dictionary form: hand-worked layouts, and exact equality with the plain form (dense,
+    # ragged N; routed experts with a table and index plane per expert)
+    for ex in _sdict_golden()["examples"]:
+        N, K = ex["N"], ex["K"]
+        wd = np.frombuffer(bytes.fromhex(ex["w_row"]) * N, dtype=np.uint8).reshape(N, K // 2)
+        idx = np.frombuffer(bytes.fromhex(ex["idx"]), dtype=np.uint8)
+        sd = np.array([int(v, 16) for v in ex["dict"]], dtype=np.uint8)
+        xd = np.full((ex["M"], K), int(ex["x_value"], 16), dtype=np.uint16)
+        y, _ = oracle.gemv_sdict(wd, idx, sd, ex["g"], xd, lib=lib)
+        if not np.array_equal(y, np.array([ex["y"]])):
+            fails.append("sdict_hand_worked:" + ex["name"])
+    wd, sd, ind, xd = random_case(40, 512, 2, 61)
+    y, _ = oracle.gemv_sdict(wd, pack_indices(ind, 40, 512), sd, 0.5, xd, lib=lib)
+    yp, _ = oracle.gemv(wd, sd[ind].astype(np.uint8), 0.5, xd, lib=lib)
+    if not np.array_equal(y, yp):
+        fails.append("sdict_equals_plain")
+    rng = np.random.default_rng(62)
+    E, N, K = 3, 20, 256
+    wm = rng.integers(0, 256, (E, N, K // 2), dtype=np.uint8)
+    sdm = np.stack([rng.permutation(np.arange(0x20, 0x60))[:32] for _ in range(E)]).astype(np.uint8)
+    indm = rng.integers(0, 32, (E, N, K // 16))
+    planes = np.stack([pack_indices(indm[e], N, K) for e in range(E)])
+    sm = np.stack([sdm[e][indm[e]] for e in range(E)]).astype(np.uint8)
+    gs = np.array([0.5, 1.0, 2.0], dtype=np.float32)
+    ids = np.array([2, 0, 1, 2], dtype=np.int32)
+    xm = synth.bf16_bits(synth.random_x(2, K, 63))
+    y, _, _ = oracle.moe_gemv_sdict(wm, planes, sdm, gs, ids, xm, False, 2, lib=lib)
+    yp, _, _ = oracle.moe_gemv(wm, sm, gs, ids, xm, False, 2, lib=lib)
+    if not np.array_equal(y, yp):
+        fails.append("sdict_moe_equals_plain")
     return fails
 
 
