@@ -65,6 +65,11 @@ WORKLOADS = {
     "moe": ("routed experts: 288 experts, gate_up [3072,4096] then down [4096,1536], "
             "4 tokens x top-8, fp32 per-slot out",
             [("moe_gate_up", 3072, 4096, 4, 8, "f32"), ("moe_down", 4096, 1536, 4, 8, "f32")]),
+    "moe_sdict": ("routed experts with dictionary scales (4.3125 bit/weight): 288 experts, gate_up [3072,4096] "
+                  "then down [4096,1536], 4 tokens x top-8, fp32 per-slot out",
+                  [("moe_sdict_gate_up", 3072, 4096, 4, 8, "f32"), ("moe_sdict_down", 4096, 1536, 4, 8, "f32")]),
+    "vocab_sdict": ("vocab head with dictionary scales (4.3125 bit/weight) N=151936,K=4096,M=1, fp32 out",
+                    [("dense_sdict", 151936, 4096, 1, 7, "f32")]),
     "moe_t32": ("routed experts at a larger batch: 288 experts, gate_up [3072,4096] then down [4096,1536], "
                 "32 tokens x top-8 (256 slots), fp32 per-slot out",
                 [("moe_gate_up", 3072, 4096, 32, 8, "f32"), ("moe_down", 4096, 1536, 32, 8, "f32")]),
@@ -128,14 +133,18 @@ def kernels_of(calls):
     """Names of the library kernels the step's calls launch (from the library's own plan)."""
     import nvfp4_weight_only_gemv_gb300 as nv
     names = {"tile": "gemv_tile_kernel", "tile_moe": "gemv_tile_kernel (MoE)", "stream": "gemv_stream_kernel",
-             "tile_sk_moe": "gemv_tile_sk_kernel (MoE)", "tile_swiglu": "gemv_tile_kernel (gate/up + SwiGLU)", "stream_moe": "gemv_stream_kernel (MoE)",
-             "simple": "gemv_simple_kernel"}
+             "tile_sk_moe": "gemv_tile_sk_kernel (MoE)", "tile_swiglu": "gemv_tile_kernel (gate/up + SwiGLU)",
+             "stream_moe": "gemv_stream_kernel (MoE)", "simple": "gemv_simple_kernel",
+             "tile_sdict": "gemv_tile_kernel (dictionary scales)",
+             "tile_sk_moe_sdict": "gemv_tile_sk_kernel (MoE, dictionary scales)"}
     seen = []
     for c in calls:
         if c.kind.startswith("moe"):
-            desc = nv.describe_plan("moe_per_slot" if c.x_per_slot else "moe", c.E, c.N, c.K, c.T, c.top_k)
+            kind = ("moe_per_slot" if c.x_per_slot else "moe") + ("_sdict" if c.sd else "")
+            desc = nv.describe_plan(kind, c.E, c.N, c.K, c.T, c.top_k)
         else:
-            desc = nv.describe_plan(c.kind if c.kind in ("gate_up", "gate_up_swiglu") else "dense", c.M, c.N, c.K)
+            kind = c.kind if c.kind in ("gate_up", "gate_up_swiglu", "dense_sdict") else "dense"
+            desc = nv.describe_plan(kind, c.M, c.N, c.K)
         name = names.get(desc.split()[0], desc.split()[0])
         if name not in seen:
             seen.append(name)
@@ -238,9 +247,16 @@ class Call:
         self.out_bytes = 2 if out == "bf16" else 4
         self.device = device
         self.sets = []
+        self.sd = "sdict" in self.kind    # dictionary scales: s is the index plane, sd its table
         if self.kind == "dense":
             p = synth.dense_problem(self.N, self.K, self.M, self.seed, device=gen_device)
             base = {"w": p["w"], "s": p["s"], "g": p["g"], "x": p["x"]}
+            self.rows = self.N
+            self.y_shape = (self.M, self.N)
+        elif self.kind == "dense_sdict":
+            p = synth.sdict_problem(self.N, self.K, self.M, self.seed, device=gen_device)
+            plane, table = synth.sdict_form(p["s"])
+            base = {"w": p["w"], "s": plane, "sd": table, "g": p["g"], "x": p["x"]}
             self.rows = self.N
             self.y_shape = (self.M, self.N)
         elif self.kind in ("gate_up", "gate_up_swiglu"):
@@ -250,11 +266,13 @@ class Call:
             self.y_shape = (self.M, self.N if self.kind == "gate_up_swiglu" else 2 * self.N)
         else:
             self.T, self.top_k, self.E = self.M, 8, 288
-            self.x_per_slot = self.kind == "moe_down"
+            self.x_per_slot = self.kind.endswith("_down")
             p = synth.moe_problem(self.E, self.N, self.K, self.T, self.top_k, self.x_per_slot,
                                   seed=self.seed, device=gen_device,
-                                  fill="all" if copies > 1 else "routed")
-            base = p
+                                  fill="all" if copies > 1 else "routed", max_codes=32 if self.sd else None)
+            base = dict(p)
+            if self.sd:
+                base["s"], base["sd"] = synth.sdict_form(p["s"])
             self.rows = self.N
             self.y_shape = (self.T * self.top_k, self.N)
         self.host = {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in base.items()}
@@ -262,7 +280,7 @@ class Call:
             d = {}
             for k, v in base.items():
                 if isinstance(v, torch.Tensor):
-                    if self.kind.startswith("moe") and k in ("w", "s") and c > 0:
+                    if self.kind.startswith("moe") and k in ("w", "s", "sd") and c > 0:
                         d[k] = self.sets[0][k]          # expert tensors are already > 2x L2
                     else:
                         d[k] = v.to(device).clone()
@@ -282,12 +300,13 @@ class Call:
         return self._uniq[c]
 
     def weight_bytes(self, c=0):
-        per_row = self.K * 0.5 + self.K / 16
+        # dictionary scales: a 5-bit index per 16 weights (plus a 32-byte table per tensor)
+        per_row = self.K * 0.5 + (self.K * 5 / 128 if self.sd else self.K / 16)
         if self.kind in ("gate_up", "gate_up_swiglu"):
             return 2 * self.N * per_row
         if self.kind.startswith("moe"):
-            return self.unique_experts(c) * self.N * per_row
-        return self.N * per_row
+            return self.unique_experts(c) * (self.N * per_row + (32 if self.sd else 0))
+        return self.N * per_row + (32 if self.sd else 0)
 
     def alg_bytes(self, c=0):
         """Bytes of the roofline formula: weights + x + y."""
@@ -311,6 +330,10 @@ class Call:
         y = d["y"] if y is None else y
         if self.kind == "dense":
             nv.gemv(d["w"], d["s"], d["g"], x, out=y)
+        elif self.kind == "dense_sdict":
+            nv.gemv_sdict(d["w"], d["s"], d["sd"], d["g"], x, out=y)
+        elif self.sd:
+            nv.moe_gemv_sdict(d["w"], d["s"], d["sd"], d["gs"], d["ids"], x, self.x_per_slot, self.top_k, out=y)
         elif self.kind == "gate_up":
             nv.gemv_gate_up(d["wg"], d["sg"], d["gg"], d["wu"], d["su"], d["gu"], x, out=y)
         elif self.kind == "gate_up_swiglu":
@@ -332,6 +355,10 @@ class Call:
         if self.kind == "dense":
             oracle.gemv(h["w"].numpy(), h["s"].numpy(), h["g"], synth.bf16_bits(h["x"]), rows=rows)
             return len(rows) * (self.K * 0.5 + self.K / 16)
+        if self.kind == "dense_sdict":
+            oracle.gemv_sdict(h["w"].numpy(), h["s"].numpy(), h["sd"].numpy(), h["g"], synth.bf16_bits(h["x"]),
+                              rows=rows)
+            return len(rows) * (self.K * 0.5 + self.K * 5 / 128)
         if self.kind == "gate_up":
             oracle.gemv_gate_up(h["wg"].numpy(), h["sg"].numpy(), h["gg"], h["wu"].numpy(), h["su"].numpy(),
                                 h["gu"], synth.bf16_bits(h["x"]), rows=rows)
@@ -341,10 +368,14 @@ class Call:
                                   h["gu"], synth.bf16_bits(h["x"]), SWIGLU_CLAMP, rows=rows)
             return 2 * len(rows) * (self.K * 0.5 + self.K / 16)  # a gate and an up row per output
         ids = self.sets[0]["ids"].cpu().numpy()
-        oracle.moe_gemv(h["w"].numpy(), h["s"].numpy(), h["gs"].numpy(), ids, synth.bf16_bits(h["x"]),
-                        self.x_per_slot, self.top_k, rows=rows)
+        if self.sd:
+            oracle.moe_gemv_sdict(h["w"].numpy(), h["s"].numpy(), h["sd"].numpy(), h["gs"].numpy(), ids,
+                                  synth.bf16_bits(h["x"]), self.x_per_slot, self.top_k, rows=rows)
+        else:
+            oracle.moe_gemv(h["w"].numpy(), h["s"].numpy(), h["gs"].numpy(), ids, synth.bf16_bits(h["x"]),
+                            self.x_per_slot, self.top_k, rows=rows)
         # the oracle walks every slot; count the bytes of the slots it read
-        return len(ids) * len(rows) * (self.K * 0.5 + self.K / 16)
+        return len(ids) * len(rows) * (self.K * 0.5 + (self.K * 5 / 128 if self.sd else self.K / 16))
 
 
 def pool_copies(calls_spec, device):
@@ -534,6 +565,10 @@ def check_outputs(calls, n_cols=48, seed=5):
         if c.kind == "dense":
             yr, ya = oracle.gemv(h["w"].numpy(), h["s"].numpy(), h["g"], synth.bf16_bits(h["x"]), rows=rows)
             tol = 1e-5 * ya + 1e-6
+        elif c.kind == "dense_sdict":
+            yr, ya = oracle.gemv_sdict(h["w"].numpy(), h["s"].numpy(), h["sd"].numpy(), h["g"],
+                                       synth.bf16_bits(h["x"]), rows=rows)
+            tol = 1e-5 * ya + 1e-6
         elif c.kind == "gate_up":
             yr, ya = oracle.gemv_gate_up(h["wg"].numpy(), h["sg"].numpy(), h["gg"], h["wu"].numpy(),
                                          h["su"].numpy(), h["gu"], synth.bf16_bits(h["x"]), rows=rows)
@@ -549,8 +584,12 @@ def check_outputs(calls, n_cols=48, seed=5):
                    + 1e-6 * np.abs(np.nan_to_num(yr)) + 1e-6)
         else:
             ids = c.sets[0]["ids"].cpu().numpy()
-            yr, ya, _ = oracle.moe_gemv(h["w"].numpy(), h["s"].numpy(), h["gs"].numpy(), ids,
-                                        synth.bf16_bits(h["x"]), c.x_per_slot, c.top_k, rows=rows)
+            if c.sd:
+                yr, ya, _ = oracle.moe_gemv_sdict(h["w"].numpy(), h["s"].numpy(), h["sd"].numpy(), h["gs"].numpy(),
+                                                  ids, synth.bf16_bits(h["x"]), c.x_per_slot, c.top_k, rows=rows)
+            else:
+                yr, ya, _ = oracle.moe_gemv(h["w"].numpy(), h["s"].numpy(), h["gs"].numpy(), ids,
+                                            synth.bf16_bits(h["x"]), c.x_per_slot, c.top_k, rows=rows)
             tol = 1e-5 * ya + 1e-6
         if bf:
             tol = tol + _ulp_bf16(np.nan_to_num(yr))
@@ -609,7 +648,8 @@ def run_reference(args):
     return 0
 
 
-PER_WORKLOAD = ["attn", "ffn", "ffn_m2", "ffn_m4", "ffn_m8", "ffn_swiglu", "moe", "moe_t32"]
+PER_WORKLOAD = ["attn", "ffn", "ffn_m2", "ffn_m4", "ffn_m8", "ffn_swiglu", "moe", "moe_t32", "moe_sdict",
+                "vocab_sdict"]
 
 
 def measure(name, steps, warmup, device, stream, ws, sampler=None):

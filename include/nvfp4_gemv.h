@@ -136,6 +136,60 @@ nvfp4_status nvfp4_moe_gemv(const uint8_t* w_packed, const uint8_t* w_scales,
                             void* y, nvfp4_out_t y_type, int N, int K,
                             int32_t* status_dev, void* stream);
 
+/*
+ * Scale-dictionary NVFP4 ("glm-5.3-flash-nvfp4-tp3-512k--gb10 card.json", performance[64],
+ * note: routed gate+up weights at 4.3125 bit/weight with a scale dictionary, a tensor kept
+ * plain at 4.5). The E2M1 codes are as above; each 16-element block's E4M3 scale code is
+ * dict[index] for a 5-bit index and a per-tensor table `scale_dict` of 32 E4M3 codes, so a
+ * weight costs 4 + 5/16 bits. The pages give only the bit budget; the layout is this library's
+ * reading:
+ *   - K % 256 == 0. The index plane has nvfp4_sdict_plane_bytes(N, K) bytes: one 160-byte
+ *     record per 16-row tile r (N rounded up to a multiple of 16) and 256-column segment c, at
+ *     byte (r * (K / 256) + c) * 160. The index of (row 16r + i, block 16c + j) sits at
+ *     position q = 16 i + j as bits 5q .. 5q + 4 of the record, least significant first, where
+ *     bit p of a record is bit p % 8 of byte p / 8. Indices of padding rows are ignored.
+ *   - A tensor whose block scales take more than 32 distinct codes has no dictionary form (it
+ *     stays plain), so the product equals nvfp4_gemv's on the scales dict[index], exactly up
+ *     to the fp32 summation order.
+ * The index plane must be 16-byte aligned for the tile kernel (else the byte-load kernel
+ * runs); the table has no alignment rule. Both are weights: the kernel reads them before the
+ * dependency wait (see nvfp4_set_pdl).
+ */
+
+/*
+ * Dense GEMV with dictionary scales: w_packed [N, K/2], scale_idx (index plane), scale_dict
+ * [32] E4M3 codes, all device memory; otherwise as nvfp4_gemv. Returns NVFP4_ERR_SHAPE when
+ * K % 256 != 0.
+ */
+nvfp4_status nvfp4_gemv_sdict(const uint8_t* w_packed, const uint8_t* scale_idx, const uint8_t* scale_dict,
+                              float global_scale, const uint16_t* x, void* y, nvfp4_out_t y_type,
+                              int M, int N, int K, void* stream);
+
+/*
+ * Routed-expert GEMV with dictionary scales: expert e's index plane starts at
+ * scale_idx + e * nvfp4_sdict_plane_bytes(N, K) and its table at scale_dict + 32 e; every
+ * other argument, layout and status as nvfp4_moe_gemv. Returns NVFP4_ERR_SHAPE when
+ * K % 256 != 0. Up to 32 slots run the stream-K tile kernel (each CTA inside one expert group,
+ * so one table serves it); larger routings run the byte-load kernel.
+ */
+nvfp4_status nvfp4_moe_gemv_sdict(const uint8_t* w_packed, const uint8_t* scale_idx, const uint8_t* scale_dict,
+                                  const float* global_scales, int E, const int32_t* expert_ids, int T, int top_k,
+                                  const uint16_t* x, int x_per_slot, void* y, nvfp4_out_t y_type, int N, int K,
+                                  int32_t* status_dev, void* stream);
+
+/* Bytes of the index plane of one [N, K] tensor, or -1 when N < 0, K < 0 or K % 256 != 0. */
+int64_t nvfp4_sdict_plane_bytes(int N, int K);
+
+/*
+ * Host-side encoder (no GPU): from plain E4M3 block scales [N, K/16] (host memory) writes the
+ * index plane (plane_out, nvfp4_sdict_plane_bytes(N, K) bytes of host memory) and the table
+ * (dict_out, 32 bytes): the distinct codes in increasing byte order, the rest of the table
+ * filled with the last one. Returns the number of distinct codes (0..32), -1 when there are
+ * more than 32 (the tensor stays plain; the outputs are not written), or -2 for a bad argument
+ * (NULL dict_out, NULL scales or plane_out for a non-empty tensor, negative size, K % 256 != 0).
+ */
+int nvfp4_sdict_encode(const uint8_t* scales, int N, int K, uint8_t* plane_out, uint8_t* dict_out);
+
 /* Human-readable name of a status code. The returned string is static. */
 const char* nvfp4_status_string(int status);
 
@@ -191,8 +245,9 @@ void nvfp4_set_pdl(int enable);
  * Describes the launch the next call with these arguments would make. It writes
  * "kernel grid block smem split rows_per_item k_warps ..." into buf (host memory,
  * NUL-terminated). kind: 0 dense, 1 gate_up, 2 MoE with x shared by a token's slots,
- * 3 MoE with one x row per slot, 4 gate_up with the fused activation; for the MoE kinds
- * M is the number of experts E.
+ * 3 MoE with one x row per slot, 4 gate_up with the fused activation, 5 dense with dictionary
+ * scales, 6 and 7 MoE with dictionary scales (x shared / one x row per slot); for the MoE
+ * kinds M is the number of experts E.
  * Pointers are assumed 256-byte aligned. Returns the number of characters, or -1.
  */
 int nvfp4_describe_plan(int kind, int M, int N, int K, int T, int top_k, char* buf, int buflen);
@@ -202,7 +257,7 @@ int nvfp4_describe_plan(int kind, int M, int N, int K, int T, int top_k, char* b
  * smem_optin bytes of shared memory a CTA may opt into, smem_per_sm bytes per SM. It runs the
  * planner on the host only (no GPU or driver needed) and assumes the tile kernel's TMA
  * tensor-map encoder is available. Returns the number of characters, or -1 for a bad
- * argument (kind outside 0..4, sizes < 1, smem_per_sm < smem_optin).
+ * argument (kind outside 0..7, sizes < 1, smem_per_sm < smem_optin).
  */
 int nvfp4_describe_plan_host(int sm_count, int smem_optin, int smem_per_sm, int kind, int M, int N, int K,
                              int T, int top_k, char* buf, int buflen);
@@ -210,13 +265,16 @@ int nvfp4_describe_plan_host(int sm_count, int smem_optin, int smem_per_sm, int 
 /*
  * Phase trace of the tile kernels (a diagnostic; no counterpart on the pages). A library built
  * with -DNVFP4_PHASE_TRACE=1 records, for each of the last 16 tile-kernel launches (slot =
- * launch number mod 16) and each of its first 1024 CTAs, 32 64-bit words: for phase ph = 0..7
+ * launch number mod 16) and each of its first 1024 CTAs, 40 64-bit words: for phase ph = 0..7
  * word 2ph is %globaltimer (ns) and word 2ph + 1 the SM's clock64, taken by thread 0 at
  * 0 entry, 1 first weight copies issued, 2 past the dependency wait, 3 x staged, 4 first box
  * landed, 5 box loop done (stream-K form), 6 outputs stored, 7 exit; word 16 + w is
  * %globaltimer when warp w left its box loop; word 24 the SM id; word 24 + w (w = 1..7)
- * %globaltimer when warp w's first box landed. Unrecorded words are zero.
- * This call synchronises `stream`, copies min(max_words, 16 * 1024 * 32) words in
+ * %globaltimer when warp w's first box landed; words 32..37 thread 0's clock64 when the barriers
+ * were initialised, the work range known, the first and all initial weight copies issued
+ * (dense launches), the MoE groups built, and the copies that follow x staging issued. Phase 3
+ * is taken right after x staging. Unrecorded words are zero.
+ * This call synchronises `stream`, copies min(max_words, 16 * 1024 * 40) words in
  * [slot][cta][word] order to host_out (host memory), clears the trace and restarts the slot
  * count. Returns the number of words copied, 0 for a library built without tracing (the
  * default), or -1 on a CUDA error or a NULL host_out.

@@ -21,7 +21,8 @@ import torch
 
 from . import build as _build
 
-__all__ = ["gemv", "gemv_gate_up", "gemv_gate_up_swiglu", "moe_gemv", "device_status", "set_wait_budget_ns",
+__all__ = ["gemv", "gemv_gate_up", "gemv_gate_up_swiglu", "moe_gemv", "gemv_sdict", "moe_gemv_sdict",
+           "sdict_plane_bytes", "sdict_encode", "device_status", "set_wait_budget_ns",
            "set_variant", "set_pdl", "fp32_fallbacks", "phase_trace", "describe_plan", "describe_plan_host", "library", "library_path", "NVFP4Error",
            "OUT_F32", "OUT_BF16", "DEV_TIMEOUT", "DEV_BAD_EXPERT", "DEV_INTERNAL"]
 
@@ -79,6 +80,14 @@ def _declare(lib):
     lib.nvfp4_describe_plan.restype = i32
     lib.nvfp4_describe_plan_host.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32, i32, ctypes.c_char_p, i32]
     lib.nvfp4_describe_plan_host.restype = i32
+    lib.nvfp4_gemv_sdict.argtypes = [u8p, u8p, u8p, ctypes.c_float, u16p, vp, i32, i32, i32, i32, vp]
+    lib.nvfp4_gemv_sdict.restype = i32
+    lib.nvfp4_moe_gemv_sdict.argtypes = [u8p, u8p, u8p, vp, i32, vp, i32, i32, u16p, i32, vp, i32, i32, i32, vp, vp]
+    lib.nvfp4_moe_gemv_sdict.restype = i32
+    lib.nvfp4_sdict_plane_bytes.argtypes = [i32, i32]
+    lib.nvfp4_sdict_plane_bytes.restype = ctypes.c_int64
+    lib.nvfp4_sdict_encode.argtypes = [vp, i32, i32, vp, vp]
+    lib.nvfp4_sdict_encode.restype = i32
     lib.nvfp4_phase_trace.argtypes = [vp, i32, vp]
     lib.nvfp4_phase_trace.restype = i32
     lib.nvfp4_version.argtypes = []
@@ -266,6 +275,90 @@ def moe_gemv(w, s, gs, ids, x, x_per_slot: bool, top_k: int, out=None, out_dtype
     return y
 
 
+def sdict_plane_bytes(N: int, K: int) -> int:
+    """Bytes of the dictionary index plane of one [N, K] weight (K % 256 == 0)."""
+    n = library(build_if_missing=False).nvfp4_sdict_plane_bytes(int(N), int(K))
+    if n < 0:
+        raise ValueError("dictionary scales need N >= 0 and K % 256 == 0")
+    return int(n)
+
+
+def sdict_encode(s: torch.Tensor):
+    """Dictionary form of plain E4M3 block scales s uint8 [N, K/16] (or [E, N, K/16], one
+    dictionary per expert), on the host: returns (index plane uint8 [sdict_plane_bytes(N, K)]
+    ([E, ...] for experts), table uint8 [32] ([E, 32])) as CPU tensors. Raises ValueError when
+    a tensor's scales take more than 32 distinct codes (it has no dictionary form)."""
+    if s.dtype != torch.uint8 or s.dim() not in (2, 3):
+        raise TypeError("s must be a uint8 tensor [N, K/16] or [E, N, K/16]")
+    src = s.detach().to("cpu").contiguous()
+    experts = src.unsqueeze(0) if src.dim() == 2 else src
+    N, K = experts.shape[1], experts.shape[2] * 16
+    lib = library(build_if_missing=False)
+    planes = torch.zeros(experts.shape[0], sdict_plane_bytes(N, K), dtype=torch.uint8)
+    tables = torch.zeros(experts.shape[0], 32, dtype=torch.uint8)
+    for e in range(experts.shape[0]):
+        rc = lib.nvfp4_sdict_encode(ctypes.c_void_p(experts[e].data_ptr()), N, K, ctypes.c_void_p(planes[e].data_ptr()),
+                                    ctypes.c_void_p(tables[e].data_ptr()))
+        if rc == -1:
+            raise ValueError(f"tensor {e}: more than 32 distinct scale codes (no dictionary form)")
+        if rc < 0:
+            raise ValueError("sdict_encode: bad arguments")
+    if src.dim() == 2:
+        return planes[0], tables[0]
+    return planes, tables
+
+
+def gemv_sdict(w: torch.Tensor, idx: torch.Tensor, sdict: torch.Tensor, g: float, x: torch.Tensor, out=None,
+               out_dtype=torch.float32, stream=None) -> torch.Tensor:
+    """gemv with dictionary scales: w uint8 [N, K/2], idx uint8 index plane [sdict_plane_bytes(N, K)],
+    sdict uint8 [32] E4M3 codes."""
+    _need(w, "w", torch.uint8, 2)
+    _need(idx, "idx", torch.uint8, 1)
+    _need(sdict, "sdict", torch.uint8, 1)
+    _need(x, "x", torch.bfloat16, 2)
+    N, K = w.shape[0], w.shape[1] * 2
+    M = x.shape[0]
+    if idx.numel() != sdict_plane_bytes(N, K) or sdict.numel() != 32 or x.shape[1] != K:
+        raise ValueError(f"shape mismatch: w {tuple(w.shape)}, idx {tuple(idx.shape)}, sdict {tuple(sdict.shape)}, "
+                         f"x {tuple(x.shape)}")
+    y = _out(out, (M, N), out_dtype, x.device)
+    _one_device(w, idx, sdict, x, y)
+    st = library().nvfp4_gemv_sdict(_ptr(w), _ptr(idx), _ptr(sdict), float(g), _ptr(x), _ptr(y), _out_code(y.dtype),
+                                    M, N, K, ctypes.c_void_p(_stream(stream)))
+    _check(st, "nvfp4_gemv_sdict")
+    return y
+
+
+def moe_gemv_sdict(w, idx, sdict, gs, ids, x, x_per_slot: bool, top_k: int, out=None, out_dtype=torch.float32,
+                   status=None, stream=None) -> torch.Tensor:
+    """moe_gemv with dictionary scales: idx uint8 [E, sdict_plane_bytes(N, K)], sdict uint8 [E, 32]."""
+    _need(w, "w", torch.uint8, 3)
+    _need(idx, "idx", torch.uint8, 2)
+    _need(sdict, "sdict", torch.uint8, 2)
+    _need(gs, "global_scales", torch.float32, 1)
+    _need(ids, "expert_ids", torch.int32, 1)
+    _need(x, "x", torch.bfloat16, 2)
+    E, N, K = w.shape[0], w.shape[1], w.shape[2] * 2
+    slots = ids.shape[0]
+    if top_k <= 0 or slots % top_k:
+        raise ValueError("expert_ids length must be a multiple of top_k")
+    T = slots // top_k
+    rows = slots if x_per_slot else T
+    if (tuple(idx.shape) != (E, sdict_plane_bytes(N, K)) or tuple(sdict.shape) != (E, 32) or gs.shape[0] != E
+            or tuple(x.shape) != (rows, K)):
+        raise ValueError("shape mismatch in moe_gemv_sdict arguments")
+    if status is not None:
+        _need(status, "status", torch.int32, 1)
+    y = _out(out, (slots, N), out_dtype, x.device)
+    _one_device(w, idx, sdict, gs, ids, x, y, status)
+    st = library().nvfp4_moe_gemv_sdict(_ptr(w), _ptr(idx), _ptr(sdict), _ptr(gs), E, _ptr(ids), T, top_k, _ptr(x),
+                                        int(bool(x_per_slot)), _ptr(y), _out_code(y.dtype), N, K,
+                                        ctypes.c_void_p(status.data_ptr()) if status is not None else None,
+                                        ctypes.c_void_p(_stream(stream)))
+    _check(st, "nvfp4_moe_gemv_sdict")
+    return y
+
+
 def device_status(stream=None) -> int:
     """Synchronise the stream, then read and clear the library's device status bits."""
     v = ctypes.c_int32(0)
@@ -295,14 +388,14 @@ def fp32_fallbacks(stream=None) -> int:
 
 
 def phase_trace(stream=None):
-    """The phase trace of the last tile-kernel launches as an int64 tensor [16, 1024, 32]
+    """The phase trace of the last tile-kernel launches as an int64 tensor [16, 1024, 40]
     ([launch slot, CTA, word]; see nvfp4_phase_trace in the header), then cleared. None when
     the loaded library was built without tracing."""
-    out = torch.zeros(16 * 1024 * 32, dtype=torch.int64)
+    out = torch.zeros(16 * 1024 * 40, dtype=torch.int64)
     n = library().nvfp4_phase_trace(ctypes.c_void_p(out.data_ptr()), out.numel(), ctypes.c_void_p(_stream(stream)))
     if n < 0:
         raise NVFP4Error(6, "nvfp4_phase_trace")
-    return out.view(16, 1024, 32) if n > 0 else None
+    return out.view(16, 1024, 40) if n > 0 else None
 
 
 def set_pdl(enable: bool) -> None:
@@ -310,11 +403,15 @@ def set_pdl(enable: bool) -> None:
     library().nvfp4_set_pdl(int(bool(enable)))
 
 
+KINDS = {"dense": 0, "gate_up": 1, "moe": 2, "moe_per_slot": 3, "gate_up_swiglu": 4, "dense_sdict": 5,
+         "moe_sdict": 6, "moe_per_slot_sdict": 7}
+
+
 def describe_plan(kind: str, M: int, N: int, K: int, T: int = 0, top_k: int = 0) -> str:
     """Launch the library would pick: kind in {"dense", "gate_up", "moe", "moe_per_slot",
     "gate_up_swiglu"}; for the MoE kinds M is the number of experts (moe_per_slot: one x row
     per slot)."""
-    code = {"dense": 0, "gate_up": 1, "moe": 2, "moe_per_slot": 3, "gate_up_swiglu": 4}[kind]
+    code = KINDS[kind]
     buf = ctypes.create_string_buffer(256)
     n = library().nvfp4_describe_plan(code, M, N, K, T, top_k, buf, 256)
     if n < 0:
@@ -325,7 +422,7 @@ def describe_plan(kind: str, M: int, N: int, K: int, T: int = 0, top_k: int = 0)
 def describe_plan_host(kind: str, M: int, N: int, K: int, T: int = 0, top_k: int = 0, sm_count: int = 152,
                        smem_optin: int = 232448, smem_per_sm: int = 233472) -> str:
     """describe_plan for a described device (defaults: GB300), run on the host only: no GPU needed."""
-    code = {"dense": 0, "gate_up": 1, "moe": 2, "moe_per_slot": 3, "gate_up_swiglu": 4}[kind]
+    code = KINDS[kind]
     buf = ctypes.create_string_buffer(256)
     n = library().nvfp4_describe_plan_host(sm_count, smem_optin, smem_per_sm, code, M, N, K, T, top_k, buf, 256)
     if n < 0:

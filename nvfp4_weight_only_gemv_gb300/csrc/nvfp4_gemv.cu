@@ -66,7 +66,9 @@ __device__ unsigned long long g_fp32_fallbacks;  // CTAs that staged x in fp32 b
 // launch slot and CTA, kTraceWords 64-bit words: for phase ph = 0..7 word 2ph = %globaltimer (ns)
 // and word 2ph + 1 = clock64 (thread 0); word 16 + w = %globaltimer when warp w leaves its box
 // loop; word 24 = the SM the CTA ran on; word 24 + w (w = 1..7) = %globaltimer when warp w's
-// first box landed (warp 0's is phase 4). Phases: 0 entry, 1 first weight copies issued, 2 past
+// first box landed (warp 0's is phase 4); words 32.. = clock64 of thread 0 at finer points of
+// the prologue (32 barriers initialised, 33 work range known, 34 first copy issued, 35 all
+// initial copies issued, 36 MoE groups built, 37 copies after x staging issued). Phases: 0 entry, 1 first weight copies issued, 2 past
 // the dependency wait, 3 x staged, 4 warp 0's first box landed, 5 warp 0's loop done, 6 outputs
 // stored, 7 exit. Normal builds compile all of it out.
 #ifndef NVFP4_PHASE_TRACE
@@ -74,7 +76,7 @@ __device__ unsigned long long g_fp32_fallbacks;  // CTAs that staged x in fp32 b
 #endif
 constexpr int kTraceLaunches = 16;
 constexpr int kTraceCtas = 1024;
-constexpr int kTraceWords = 32;
+constexpr int kTraceWords = 40;
 #if NVFP4_PHASE_TRACE
 __device__ unsigned long long g_trace[kTraceLaunches * kTraceCtas * kTraceWords];
 #endif
@@ -304,6 +306,30 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t sel) {
     uint32_t d;
     asm("prmt.b32 %0, %1, 0, %2;" : "=r"(d) : "r"(a), "r"(sel));
     return d;
+}
+
+// ------------------------------------------------------------------ scale dictionary
+// Scale-dictionary NVFP4 ("glm-5.3-flash-nvfp4-tp3-512k--gb10 card.json", performance[64],
+// note: routed experts at 4.3125 bit/weight with a scale dictionary): each 16-element block's
+// E4M3 scale code is dict[index] for a 5-bit index and a 32-entry table per tensor. Index plane
+// layout (K % 256 == 0): one 160-byte record per 16-row tile r and 256-column segment c at byte
+// (r * K/256 + c) * 160; (row 16r + i, block 16c + j) at q = 16i + j, bits 5q .. 5q + 4, least
+// significant first, bit p of a record being bit p % 8 of byte p / 8.
+constexpr int kSdRecord = 160;     // bytes of one (tile, segment) record
+constexpr int kSdPairs = 1024;     // entries of the pair table: two 5-bit indices
+
+__host__ __device__ __forceinline__ int64_t sd_plane_bytes(int64_t N, int64_t K) {
+    return (N + 15) / 16 * (K / 256) * kSdRecord;
+}
+
+// The scale code of block b of row n (byte loads; the byte-load kernel).
+__device__ __forceinline__ uint32_t sd_code(const uint8_t* plane, const uint8_t* dict, int64_t K, int64_t n,
+                                            int64_t b) {
+    const uint8_t* rec = plane + ((n >> 4) * (K >> 8) + (b >> 4)) * kSdRecord;
+    const uint32_t bit = static_cast<uint32_t>(((n & 15) * 16 + (b & 15)) * 5);
+    uint32_t v = __ldg(rec + (bit >> 3));
+    if ((bit & 7) > 3) v |= static_cast<uint32_t>(__ldg(rec + (bit >> 3) + 1)) << 8;  // the field spans two bytes
+    return __ldg(dict + ((v >> (bit & 7)) & 31u));
 }
 
 // D += A * B for one m16n8k16 tile: A 16x16 f16 (row), B 16x8 f16 (col), D 16x8 f32.
@@ -1241,14 +1267,33 @@ struct TileParams {
     int E, top_k, slots, x_per_slot;
     uint32_t moe_off;         // TileMoe tables
     int trace_slot;           // phase-trace launch slot (diagnostic builds only)
+    // dictionary scales: smap[] views the index planes; table of E4M3 codes [32] ([E][32] MoE)
+    const uint8_t* sd_dict;
+    int sd_tiles;             // 16-row tiles per expert in the index plane (MoE)
+    uint32_t sdtab_off;       // the pair table: 1024 f16x2 scale pairs
 };
+
+// Bytes of one ring slot's scale box: NC 16-byte rows of E4M3 codes per tile row, or (dictionary
+// scales) NC 160-byte index records, padded to 128 bytes.
+template <int NC, bool SD>
+__host__ __device__ constexpr uint32_t scale_box_bytes() {
+    return SD ? (NC * kSdRecord + 127) / 128 * 128 : NC * 256;
+}
+
+// Bytes one scale box copy delivers.
+template <int NC, bool SD>
+__host__ __device__ constexpr uint32_t scale_box_tx() {
+    return SD ? NC * kSdRecord : NC * 256;
+}
 
 // Routed-expert groups of one launch, built by every CTA from the ids: a group is one expert
 // and up to 8 of its slots (the MMA's 8 columns), groups ordered by their first slot.
 constexpr int kTileMoeSlots = 32;
+constexpr int kMoeWindow = 4;                 // groups a stream-K CTA may touch when slots > 32
 struct TileMoe {
     int n_groups;
     int nrows;                                // x rows this CTA stages
+    int g0;                                   // group of entry 0 (the arrays hold groups g0, g0 + 1, ...)
     int expert[kTileMoeSlots];
     int count[kTileMoeSlots];
     int slot[kTileMoeSlots][8];               // member slots, slot order
@@ -1262,6 +1307,33 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
     asm volatile(
         "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
         ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar) : "memory");
+}
+
+#ifndef NVFP4_PARAM_WARM
+#define NVFP4_PARAM_WARM 0  // 1: touch every 64-byte line of the launch parameters at kernel entry
+#endif
+
+// Loads one word of every 64-byte line of the launch parameters' scalar part at once, so that
+// their first-touch misses overlap instead of arriving one at a time through the prologue.
+template <typename P, typename F>
+__device__ __forceinline__ void warm_params(const P& p, const F& first_scalar) {
+    const char* b = reinterpret_cast<const char*>(&first_scalar);
+    const char* e = reinterpret_cast<const char*>(&p) + sizeof(P);
+    uint32_t acc = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        if (b + 64 * i + 4 <= e) acc ^= *reinterpret_cast<const uint32_t*>(b + 64 * i);
+    asm volatile("" ::"r"(acc));
+}
+
+#ifndef NVFP4_PREFETCH_TMAP
+#define NVFP4_PREFETCH_TMAP 1  // 1: fetch the launch's tensor-map descriptors at kernel entry
+#endif
+
+// Starts fetching a tensor-map descriptor (kernel parameter space) into the descriptor cache, so
+// the first copy that uses it does not wait for the fetch.
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
 __device__ __forceinline__ void named_bar_sync(int id, int count) {
@@ -1302,6 +1374,9 @@ __host__ __device__ __forceinline__ int tile_row_perm(int g) {
 
 #ifndef NVFP4_STAGE_PRE
 #define NVFP4_STAGE_PRE 2
+#endif
+#ifndef NVFP4_DENSE_EARLY
+#define NVFP4_DENSE_EARLY 4  // ring slots a dense warp requests before the dependency wait (the rest after x staging)
 #endif
 
 // Fast staging of x[:, k0 : k0 + kn] for the warps of one K slice: every bf16 value is
@@ -1603,9 +1678,37 @@ __device__ bool stage_x_slice(const uint16_t* __restrict__ x, const int* rowsel,
 #endif
 constexpr int kTileChains = NVFP4_TILE_CHAINS;  // independent MMA accumulator chains per warp
 
-template <int NC>
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+
+// The f16x2 scales of blocks 8h + 2t and 8h + 2t + 1 (low half first) of tile row `row` in
+// segment c of a ring slot's scale box: two E4M3 codes, or (SD) the 10-bit pair of dictionary
+// indices at bit 5q, q = 16 row + 8h + 2t, looked up in the pair table at `tab`.
+template <int NC, bool SD>
+__device__ __forceinline__ uint32_t slot_scale2(uint32_t sst, int c, int row, int h, int t, uint32_t tab) {
+    if constexpr (SD) {
+        const uint32_t bit = static_cast<uint32_t>(row * 80 + h * 40 + t * 10);
+        const uint32_t a = sst + c * kSdRecord + ((bit >> 5) << 2);
+        const uint32_t pair = __funnelshift_r(lds32(a), lds32(a + 4), bit & 31u) & 0x3ffu;
+        return lds32(tab + pair * 4);
+    } else {
+        return cvt_e4m3x2(lds16(sst + (row * NC + c) * 16 + h * 8 + 2 * t));
+    }
+}
+
+// Fills the pair table at tab (1024 words): entry i1 * 32 + i0 holds the f16x2 of
+// (E4M3(dict[i0]), E4M3(dict[i1])). Called by all `nthreads` threads; the caller synchronises.
+__device__ __forceinline__ void build_pair_table(uint32_t* tab, const uint8_t* dict, int tid, int nthreads) {
+    for (int e = tid; e < kSdPairs; e += nthreads)
+        tab[e] = cvt_e4m3x2(static_cast<uint16_t>(__ldg(dict + (e & 31)) | (__ldg(dict + (e >> 5)) << 8)));
+}
+
+template <int NC, bool SD = false>
 __device__ __forceinline__ void tile_slot_mma(uint32_t wst, uint32_t sst, uint32_t xa, int chunk0, int ra, int t,
-                                              float (&dd)[kTileChains][4]) {
+                                              float (&dd)[kTileChains][4], uint32_t tab = 0) {
     const int rb = ra + 8;
 #pragma unroll
     for (int c = 0; c < NC; ++c) {
@@ -1615,8 +1718,8 @@ __device__ __forceinline__ void tile_slot_mma(uint32_t wst, uint32_t sst, uint32
             const int u = h * 4 + t;
             const uint4 wa = lds128(wst + la * 128 + ((u ^ (la & 7)) << 4));
             const uint4 wb = lds128(wst + lb * 128 + ((u ^ (lb & 7)) << 4));
-            const uint32_t sa = cvt_e4m3x2(lds16(sst + la * 16 + h * 8 + 2 * t));
-            const uint32_t sb = cvt_e4m3x2(lds16(sst + lb * 16 + h * 8 + 2 * t));
+            const uint32_t sa = slot_scale2<NC, SD>(sst, c, ra, h, t, tab);
+            const uint32_t sb = slot_scale2<NC, SD>(sst, c, rb, h, t, tab);
             const int chunk = chunk0 + c * 2 + h;
             uint4 xq[4];
 #pragma unroll
@@ -1641,9 +1744,10 @@ __device__ __forceinline__ void tile_slot_mma(uint32_t wst, uint32_t sst, uint32
 // The same slot in exact fp32 on the CUDA cores, x read from global memory (bf16): column m
 // uses x row xrow[m] (row m when xrow is null). acc[r][m] collects rows ra (r = 0) and
 // rb (r = 1) for column m, over this lane's 32-code pieces.
-template <int NC>
+template <int NC, bool SD = false>
 __device__ __noinline__ void tile_slot_f32(uint32_t wst, uint32_t sst, const uint16_t* __restrict__ x,
-                                           const int* xrow, int K, int M, int kseg0, int ra, int t, float* acc) {
+                                           const int* xrow, int K, int M, int kseg0, int ra, int t, float* acc,
+                                           uint32_t tab = 0) {
     const int rb = ra + 8;
     for (int c = 0; c < NC; ++c) {
         const int la = ra * NC + c, lb = rb * NC + c;
@@ -1651,8 +1755,8 @@ __device__ __noinline__ void tile_slot_f32(uint32_t wst, uint32_t sst, const uin
             const int u = h * 4 + t;
             const uint4 wv[2] = {lds128(wst + la * 128 + ((u ^ (la & 7)) << 4)),
                                  lds128(wst + lb * 128 + ((u ^ (lb & 7)) << 4))};
-            const uint32_t sh[2] = {cvt_e4m3x2(lds16(sst + la * 16 + h * 8 + 2 * t)),
-                                    cvt_e4m3x2(lds16(sst + lb * 16 + h * 8 + 2 * t))};
+            const uint32_t sh[2] = {slot_scale2<NC, SD>(sst, c, ra, h, t, tab),
+                                    slot_scale2<NC, SD>(sst, c, rb, h, t, tab)};
             const int k0 = ((kseg0 + c) * 2 + h) * 128 + 32 * t;
             for (int w = 0; w < 4; ++w) {
                 for (int m = 0; m < M; ++m) {
@@ -1714,7 +1818,10 @@ __device__ void tile_moe_groups(const TileParams& p, TileMoe* tab, int lane) {
             tab->count[g] = min(8, __popc(same) - rank);
         }
     }
-    if (lane == 0) tab->n_groups = __popc(leaders);
+    if (lane == 0) {
+        tab->n_groups = __popc(leaders);
+        tab->g0 = 0;
+    }
     if (!valid && s < p.slots && blockIdx.x == 0) {
         raise_status(NVFP4_DEV_BAD_EXPERT, p.status_user);
         for (int n = 0; n < p.N; ++n) store_out(p.y, static_cast<int64_t>(s) * p.N + n, 0.f, p.out_bf16);
@@ -1723,6 +1830,119 @@ __device__ void tile_moe_groups(const TileParams& p, TileMoe* tab, int lane) {
 }
 
 // The x rows that groups [g0, g1] need, staged in increasing row order (at most 32 rows).
+// Routed-expert groups of a stream-K launch with more than 32 slots (up to kMaxMoeSlots), built
+// by all threads: a leader is an expert's first slot; the expert's slots form groups of up to 8 in
+// slot order, numbered from ngr[leader], leaders in slot order. Scratch: ids, cnt, ngr, each
+// kMaxMoeSlots ints. Invalid ids form no group: CTA 0 zeroes their outputs and flags them.
+__device__ void tile_moe_groups_big(const TileParams& p, TileMoe* tab, int* scratch, int tid) {
+    int* ids = scratch;
+    int* cnt = scratch + kMaxMoeSlots;
+    int* ngr = scratch + 2 * kMaxMoeSlots;
+    for (int t = tid; t < p.slots; t += tk::kThreads) {
+        const int id = __ldg(p.ids + t);
+        ids[t] = (id >= 0 && id < p.E) ? id : -1;
+        if (!(id >= 0 && id < p.E) && blockIdx.x == 0) {
+            raise_status(NVFP4_DEV_BAD_EXPERT, p.status_user);
+            for (int n = 0; n < p.N; ++n) store_out(p.y, static_cast<int64_t>(t) * p.N + n, 0.f, p.out_bf16);
+        }
+    }
+    __syncthreads();
+    for (int t = tid; t < p.slots; t += tk::kThreads) {
+        const int id = ids[t];
+        bool leader = id >= 0;
+        for (int u = 0; u < t && leader; ++u) leader = ids[u] != id;
+        int c = 0;
+        if (leader)
+            for (int u = t; u < p.slots; ++u) c += ids[u] == id;
+        cnt[t] = c;
+        ngr[t] = (c + 7) / 8;
+    }
+    __syncthreads();
+    if (tid < 32) {
+        // exclusive scan of the group counts over slots, 8 slots per lane
+        int local[8];
+        int sum = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int t = tid * 8 + i;
+            local[i] = t < p.slots ? ngr[t] : 0;
+            sum += local[i];
+        }
+        int incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (tid >= o) incl += v;
+        }
+        int run = incl - sum;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int t = tid * 8 + i;
+            if (t < p.slots) ngr[t] = run;  // now: the first group of leader t
+            run += local[i];
+        }
+        if (tid == 31) tab->n_groups = incl;
+    }
+    __syncthreads();
+}
+
+// The groups g_lo .. g_hi (at most kMoeWindow; none when g_lo > g_hi) of the CTA's job range from
+// tile_moe_groups_big's scratch into tab (entry g - g_lo), then their x rows, distinct and in
+// increasing order, and each member's staged column. All threads; ends with __syncthreads.
+__device__ void tile_moe_window(const TileParams& p, TileMoe* tab, const int* scratch, int g_lo, int g_hi, int tid) {
+    const int* ids = scratch;
+    const int* cnt = scratch + kMaxMoeSlots;
+    const int* ngr = scratch + 2 * kMaxMoeSlots;
+    if (g_hi - g_lo + 1 > kMoeWindow) {  // the planner bounds the span: flag it, keep in bounds
+        if (tid == 0) raise_status(NVFP4_DEV_INTERNAL, p.status_user);
+        g_hi = g_lo + kMoeWindow - 1;
+    }
+    if (tid == 0) tab->g0 = g_lo;
+    for (int t = tid; t < p.slots; t += tk::kThreads) {
+        const int c = cnt[t];
+        if (c == 0) continue;  // not a leader
+        const int gf = ngr[t], gl = gf + (c + 7) / 8 - 1;
+        if (gl < g_lo || gf > g_hi) continue;
+        const int id = ids[t];
+        int i = 0;  // member number within the expert
+        for (int u = t; u < p.slots && i < c; ++u) {
+            if (ids[u] != id) continue;
+            const int g = gf + (i >> 3), j = i & 7;
+            if (g >= g_lo && g <= g_hi) {
+                const int lg = g - g_lo;
+                tab->slot[lg][j] = u;
+                tab->xrow[lg][j] = p.x_per_slot ? u : u / p.top_k;
+                if (j == 0) {
+                    tab->expert[lg] = id;
+                    tab->count[lg] = min(8, c - i);
+                }
+            }
+            ++i;
+        }
+    }
+    __syncthreads();
+    if (tid < 32) {
+        // lane m holds member m % 8 of window entry m / 8; a row is staged once, at the
+        // position given by the number of distinct rows below it
+        const int ng = g_hi - g_lo + 1;
+        const int lg = tid >> 3, j = tid & 7;
+        const bool has = lg < ng && j < tab->count[lg];
+        const int r = has ? tab->xrow[lg][j] : 0x7fffffff;
+        const uint32_t same = __match_any_sync(0xffffffffu, r);
+        const bool first = has && (__ffs(same) - 1) == tid;
+        const uint32_t firsts = __ballot_sync(0xffffffffu, first);
+        int below = 0;
+        for (int l = 0; l < 32; ++l) {
+            const int v = __shfl_sync(0xffffffffu, r, l);
+            below += static_cast<int>((firsts >> l) & 1u) & static_cast<int>(v < r);
+        }
+        if (first) tab->rows[below] = r;
+        if (has) tab->col[lg][j] = below;
+        if (tid == 0) tab->nrows = __popc(firsts);
+    }
+    __syncthreads();
+}
+
 __device__ void tile_moe_rows(const TileParams& p, TileMoe* tab, int g0, int g1, int lane) {
     uint32_t want = 0u;
     for (int g = g0; g <= g1; ++g)
@@ -1735,11 +1955,11 @@ __device__ void tile_moe_rows(const TileParams& p, TileMoe* tab, int g0, int g1,
     __syncwarp();
 }
 
-template <int NC, bool MOE, bool SWI = false>
+template <int NC, bool MOE, bool SWI = false, bool SD = false>
 __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_kernel(const __grid_constant__ TileParams p) {
     extern __shared__ uint8_t smem_raw[];
     constexpr uint32_t kWBox = NC * 2048;  // 16 rows x NC x 128 B
-    constexpr uint32_t kSBox = NC * 256;   // 16 rows x NC x 16 B
+    constexpr uint32_t kSBox = scale_box_bytes<NC, SD>();  // 16 rows x NC x 16 B, or NC index records
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int t = lane & 3;
     const uint32_t raw_base = smem_addr(smem_raw);
@@ -1750,7 +1970,9 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_kernel(const __grid
     const uint32_t ring_w = base + p.ring_w + static_cast<uint32_t>(warp * stages) * kWBox;
     const uint32_t ring_s = base + p.ring_s + static_cast<uint32_t>(warp * stages) * kSBox;
     TileMoe* const tab = reinterpret_cast<TileMoe*>(sbase + p.moe_off);
+    if (NVFP4_PARAM_WARM) warm_params(p, p.x);
     if (tid == 0) trace_phase(p.trace_slot, 0);
+    if (NVFP4_PREFETCH_TMAP && warp == 0 && lane < 4) prefetch_tmap(lane < 2 ? &p.wmap[lane] : &p.smap[lane - 2]);
 
     const int S = 1 << p.s_log2;
     const int rank = S > 1 ? static_cast<int>(cluster_rank()) : 0;
@@ -1766,6 +1988,7 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_kernel(const __grid
         fence_barrier_init();
     }
     __syncwarp();
+    if (tid == 0) trace_word(p.trace_slot, 32, static_cast<unsigned long long>(clock64()));
 
     // this unit's items: a balanced contiguous block (MoE: counted once the groups are known)
     int ib = 0, ie = 0;
@@ -1805,7 +2028,7 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_kernel(const __grid
         const uint32_t st = iss_st;
         if (++iss_st == static_cast<uint32_t>(stages)) iss_st = 0;
         const uint32_t bar = smem_addr(&bars[st]);
-        mbar_arrive_expect_tx(&bars[st], kWBox + kSBox);
+        mbar_arrive_expect_tx(&bars[st], kWBox + scale_box_tx<NC, SD>());
         const int seg = (b_lo + iss_box) * NC;
         int row0 = (iw.t * p.tpi + tin) * 16;
         int map = iw.grp;
@@ -1818,7 +2041,7 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_kernel(const __grid
             map = 0;
         }
         tma_load_3d(ring_w + st * kWBox, &p.wmap[map], 0, seg, row0, bar);
-        tma_load_3d(ring_s + st * kSBox, &p.smap[map], 0, seg, row0, bar);
+        tma_load_3d(ring_s + st * kSBox, &p.smap[map], 0, seg, SD ? (row0 >> 4) : row0, bar);
         ++iss_box;
         ++issued;
     };
@@ -1827,8 +2050,18 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_kernel(const __grid
         // wait; x may, so only an L2 prefetch of this CTA's K range of it goes out before it
         iss_left = ie - ib;
         iw = first;
+        if (tid == 0) trace_word(p.trace_slot, 33, static_cast<unsigned long long>(clock64()));
         if (lane == 0)
-            for (int s = 0; s < stages; ++s) issue_next();
+            for (int s = 0; s < min(stages, NVFP4_DENSE_EARLY); ++s) {
+                issue_next();
+                if (tid == 0 && s == 0) trace_word(p.trace_slot, 34, static_cast<unsigned long long>(clock64()));
+            }
+        if (tid == 0) trace_word(p.trace_slot, 35, static_cast<unsigned long long>(clock64()));
+        if constexpr (SD) {
+            // the table is a weight too: built before the dependency wait
+            build_pair_table(reinterpret_cast<uint32_t*>(sbase + p.sdtab_off), p.sd_dict, tid, tk::kThreads);
+            __syncthreads();
+        }
         if (warp == tk::kWarps - 1 && lane < p.M) {
             const int kb = c_lo * NC * 256, kbytes = c_n * NC * 512;
             const uint16_t* xr = p.x + static_cast<int64_t>(lane) * p.K + kb;
@@ -1863,6 +2096,7 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_kernel(const __grid
         __syncthreads();
         M = ib < ie ? tab->nrows : 0;
         rowsel = tab->rows;
+        if (tid == 0) trace_word(p.trace_slot, 36, static_cast<unsigned long long>(clock64()));
     }
 
     // x for this warp's K slice, staged by the tpi warps that share the slice
@@ -1888,15 +2122,19 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_kernel(const __grid
         lossy = stage_x_slice(p.x, rowsel, M, p.K, k0, kn, xs, p.sstride, e2, gmax, tin, p.tpi, xbar, lane);
         e2v = e2[0];
     }
+    if (tid == 0) trace_phase(p.trace_slot, 3);
     if constexpr (MOE) {
         // the weights of this CTA's experts: issued after staging, because a thread that issues
         // bulk copies can stall while the copy engine is busy, and staging waits for every warp
         if (lane == 0)
             for (int s = 0; s < stages; ++s) issue_next();
+    } else {
+        if (lane == 0)  // the rest of the ring, when only part of it went out before the wait
+            for (int s = min(stages, NVFP4_DENSE_EARLY); s < stages; ++s) issue_next();
     }
+    if (tid == 0) trace_word(p.trace_slot, 37, static_cast<unsigned long long>(clock64()));
     const bool use_f32 = lossy || p.force_f32;
     if (use_f32 && M > 0 && tin == 0 && lane == 0) atomicAdd(&g_fp32_fallbacks, 1ull);
-    if (tid == 0) trace_phase(p.trace_slot, 3);
     bool traced_first = false;
 
     const int g = lane >> 2;
@@ -1948,10 +2186,11 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_kernel(const __grid
                     traced_first = true;
                 }
                 if (!use_f32) {
-                    tile_slot_mma<NC>(ring_w + st * kWBox, ring_s + st * kSBox, xa, b * NC * 2, ra, t, dd);
+                    tile_slot_mma<NC, SD>(ring_w + st * kWBox, ring_s + st * kSBox, xa, b * NC * 2, ra, t, dd,
+                                          base + p.sdtab_off);
                 } else {
-                    tile_slot_f32<NC>(ring_w + st * kWBox, ring_s + st * kSBox, p.x, xrow, p.K, ncols,
-                                      (b_lo + b) * NC, ra, t, acc);
+                    tile_slot_f32<NC, SD>(ring_w + st * kWBox, ring_s + st * kSBox, p.x, xrow, p.K, ncols,
+                                          (b_lo + b) * NC, ra, t, acc, base + p.sdtab_off);
                 }
                 cons_advance();
                 __syncwarp();
@@ -2138,11 +2377,11 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_kernel(const __grid
 // writes into its own ring once all its copies are consumed. After one CTA barrier the warp
 // that holds a job's first box adds the records of the following warps in warp order and
 // stores the sum. Balance is one TMA box per warp instead of one item per CTA.
-template <int NC, bool MOE>
+template <int NC, bool MOE, bool SD = false>
 __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_sk_kernel(const __grid_constant__ TileParams p) {
     extern __shared__ uint8_t smem_raw[];
     constexpr uint32_t kWBox = NC * 2048;
-    constexpr uint32_t kSBox = NC * 256;
+    constexpr uint32_t kSBox = scale_box_bytes<NC, SD>();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int t = lane & 3;
     const uint32_t raw_base = smem_addr(smem_raw);
@@ -2153,7 +2392,9 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_sk_kernel(const __g
     const uint32_t ring_w = base + p.ring_w + static_cast<uint32_t>(warp * stages) * kWBox;
     const uint32_t ring_s = base + p.ring_s + static_cast<uint32_t>(warp * stages) * kSBox;
     TileMoe* const tab = reinterpret_cast<TileMoe*>(sbase + p.moe_off);
+    if (NVFP4_PARAM_WARM) warm_params(p, p.x);
     if (tid == 0) trace_phase(p.trace_slot, 0);
+    if (NVFP4_PREFETCH_TMAP && warp == 0 && lane < 4) prefetch_tmap(lane < 2 ? &p.wmap[lane] : &p.smap[lane - 2]);
     // partial records of warp w: the first 1 KB of its own ring, free once its boxes are consumed
     auto rec_of = [&](int w, int slot) -> float* {
         return reinterpret_cast<float*>(sbase + p.ring_w + static_cast<uint32_t>(w * stages) * kWBox) + slot * 128;
@@ -2194,19 +2435,21 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_sk_kernel(const __g
         is_grp = job / tiles;
         is_tile = job - is_grp * tiles;
     };
+    int gw0 = 0;  // MoE: the group held by entry 0 of the tables
     auto issue_next = [&]() {
         if (is_b >= be) return;
         const uint32_t st = iss_st;
         if (++iss_st == static_cast<uint32_t>(stages)) iss_st = 0;
         const uint32_t bar = smem_addr(&bars[st]);
-        mbar_arrive_expect_tx(&bars[st], kWBox + kSBox);
-        int row0 = is_tile * 16, map = is_grp;
+        mbar_arrive_expect_tx(&bars[st], kWBox + scale_box_tx<NC, SD>());
+        int row0 = is_tile * 16, map = is_grp, srow = SD ? is_tile : row0;
         if constexpr (MOE) {
-            row0 += tab->expert[is_grp] * p.N;
+            row0 += tab->expert[is_grp - gw0] * p.N;
+            srow += tab->expert[is_grp - gw0] * (SD ? p.sd_tiles : p.N);
             map = 0;
         }
         tma_load_3d(ring_w + st * kWBox, &p.wmap[map], 0, is_box * NC, row0, bar);
-        tma_load_3d(ring_s + st * kSBox, &p.smap[map], 0, is_box * NC, row0, bar);
+        tma_load_3d(ring_s + st * kSBox, &p.smap[map], 0, is_box * NC, srow, bar);
         ++issued;
         ++is_b;
         if (++is_box == nbox) {
@@ -2240,8 +2483,14 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_sk_kernel(const __g
 
     int M = p.M;
     const int* rowsel = nullptr;
+    bool x_overflow = false;  // the CTA computes in fp32 with x from global memory
     if constexpr (MOE) {
-        if (warp == 0) tile_moe_groups(p, tab, lane);
+        // more than 32 slots: all threads build the groups, with scratch in the x region (free
+        // until x is staged); each CTA then keeps only the groups of its own job range
+        const bool big = p.slots > kTileMoeSlots;
+        int* scratch = reinterpret_cast<int*>(sbase + p.x_off);
+        if (big) tile_moe_groups_big(p, tab, scratch, tid);
+        else if (warp == 0) tile_moe_groups(p, tab, lane);
         __syncthreads();
 #if NVFP4_SK_GROUP_ALIGNED
         if (p.items_r) {
@@ -2273,11 +2522,36 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_sk_kernel(const __g
 #else
         set_ranges(tab->n_groups * tiles);
 #endif
-        if (warp == 0 && j0 < j1) tile_moe_rows(p, tab, j0 / tiles, (j1 - 1) / tiles, lane);
-        start_cursor();
+        if (big) {
+            if (j0 < j1 && (j1 - 1) / tiles - j0 / tiles + 1 > kMoeWindow) {
+                // more groups than the window holds (the planner rules it out): no work, flagged
+                if (tid == 0) raise_status(NVFP4_DEV_INTERNAL, p.status_user);
+                j0 = j1 = 0;
+                bs = be = 0;
+            }
+            tile_moe_window(p, tab, scratch, j0 < j1 ? j0 / tiles : 1, j0 < j1 ? (j1 - 1) / tiles : 0, tid);
+        } else if (warp == 0 && j0 < j1) {
+            tile_moe_rows(p, tab, j0 / tiles, (j1 - 1) / tiles, lane);
+        }
         __syncthreads();
+        gw0 = tab->g0;
+        start_cursor();
+        if constexpr (SD) {
+            // dictionary scales: the planner keeps the CTA inside one group (group-aligned
+            // ranges), so one pair table serves all of its jobs
+            if (j0 < j1)
+                build_pair_table(reinterpret_cast<uint32_t*>(sbase + p.sdtab_off),
+                                 p.sd_dict + 32 * tab->expert[j0 / tiles - gw0], tid, tk::kThreads);
+            if (tid == 0 && j0 < j1 && (j1 - 1) / tiles != j0 / tiles) raise_status(NVFP4_DEV_INTERNAL, p.status_user);
+            __syncthreads();
+        }
         M = j0 < j1 ? tab->nrows : 0;
         rowsel = tab->rows;
+        if (M > p.M) {  // more x rows than the staging buffer holds (more than 32 slots only)
+            x_overflow = true;
+            M = 0;
+        }
+        if (tid == 0) trace_word(p.trace_slot, 36, static_cast<unsigned long long>(clock64()));
         if (lane == 0)
             for (int s = 0; s < NVFP4_MOE_EARLY; ++s) issue_next();
     }
@@ -2301,13 +2575,14 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_sk_kernel(const __g
         lossy = stage_x_slice(p.x, rowsel, M, p.K, 0, p.K, xs, p.sstride, e2, gmax, warp, tk::kWarps, 2, lane);
         e2v = e2[0];
     }
+    if (tid == 0) trace_phase(p.trace_slot, 3);
     if constexpr (MOE) {
         if (lane == 0)
             for (int s = NVFP4_MOE_EARLY; s < stages; ++s) issue_next();
     }
-    const bool use_f32 = lossy || p.force_f32;
-    if (use_f32 && M > 0 && warp == 0 && lane == 0) atomicAdd(&g_fp32_fallbacks, 1ull);
-    if (tid == 0) trace_phase(p.trace_slot, 3);
+    if (tid == 0) trace_word(p.trace_slot, 37, static_cast<unsigned long long>(clock64()));
+    const bool use_f32 = lossy || p.force_f32 || x_overflow;
+    if (use_f32 && (M > 0 || x_overflow) && warp == 0 && lane == 0) atomicAdd(&g_fp32_fallbacks, 1ull);
     bool traced_first = false;
 
     const int g = lane >> 2;
@@ -2318,15 +2593,15 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_sk_kernel(const __g
     bool dead = false;
 
     auto ncols_of = [&](int grp) -> int {
-        if constexpr (MOE) return tab->count[grp];
+        if constexpr (MOE) return tab->count[grp - gw0];
         else return p.M;
     };
     auto gscale_of = [&](int grp) -> float {
-        if constexpr (MOE) return __ldg(p.g_dev + tab->expert[grp]);
+        if constexpr (MOE) return __ldg(p.g_dev + tab->expert[grp - gw0]);
         else return p.g[grp];
     };
     auto out_at = [&](int grp, int m, int row) -> int64_t {
-        if constexpr (MOE) return static_cast<int64_t>(tab->slot[grp][m]) * p.N + row;
+        if constexpr (MOE) return static_cast<int64_t>(tab->slot[grp - gw0][m]) * p.N + row;
         else return m * p.ldy + static_cast<int64_t>(grp) * p.N + row;
     };
 
@@ -2358,7 +2633,7 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_sk_kernel(const __g
         uint32_t xa = 0;
         auto set_x = [&]() {
             int col = min(g, max(M - 1, 0));
-            if constexpr (MOE) col = tab->col[grp][min(g, ncols_of(grp) - 1)];
+            if constexpr (MOE) col = tab->col[grp - gw0][min(g, ncols_of(grp) - 1)];
             xa = base + p.x_off + static_cast<uint32_t>(col) * p.sstride;
         };
         if (bs < be) set_x();
@@ -2376,12 +2651,13 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_sk_kernel(const __g
                         traced_first = true;
                     }
                     if (!use_f32) {
-                        tile_slot_mma<NC>(ring_w + st * kWBox, ring_s + st * kSBox, xa, kb * NC * 2, ra, t, dd);
+                        tile_slot_mma<NC, SD>(ring_w + st * kWBox, ring_s + st * kSBox, xa, kb * NC * 2, ra, t, dd,
+                                              base + p.sdtab_off);
                     } else {
                         const int* xrow = nullptr;
-                        if constexpr (MOE) xrow = tab->xrow[grp];
-                        tile_slot_f32<NC>(ring_w + st * kWBox, ring_s + st * kSBox, p.x, xrow, p.K, ncols_of(grp),
-                                          kb * NC, ra, t, acc);
+                        if constexpr (MOE) xrow = tab->xrow[grp - gw0];
+                        tile_slot_f32<NC, SD>(ring_w + st * kWBox, ring_s + st * kSBox, p.x, xrow, p.K, ncols_of(grp),
+                                              kb * NC, ra, t, acc, base + p.sdtab_off);
                     }
                     cons_advance();
                     __syncwarp();
@@ -2523,6 +2799,8 @@ struct SimpleParams {
     int moe, E, top_k, x_per_slot, slots;
     int swiglu;               // groups == 2: one output silu(clamp(gate)) * clamp(up) per column
     float clamp;
+    int sd;                   // 1: s[] are dictionary index planes (dense: one; MoE: one per expert)
+    const uint8_t* sd_dict;   // their tables: [32] (dense) or [E][32] (MoE)
 };
 
 // One warp per output column (all M rows). Lanes stride over the 16-element blocks of K.
@@ -2537,6 +2815,8 @@ __global__ void __launch_bounds__(kSimpleThreads) gemv_simple_kernel(const __gri
     int64_t xrow0 = 0;
     int64_t out0, out_step;
     int mrows = p.M;
+    int64_t sd_row = 0;                  // dictionary scales: row of the index plane at srow
+    const uint8_t* sd_tab = p.sd_dict;   // and its table
     if (p.moe) {
         if (col >= static_cast<int64_t>(p.slots) * p.N) return;
         const int sl = static_cast<int>(col / p.N);
@@ -2551,6 +2831,11 @@ __global__ void __launch_bounds__(kSimpleThreads) gemv_simple_kernel(const __gri
         }
         wrow = p.w[0] + (static_cast<int64_t>(e) * p.N + n) * Kh;
         srow = p.s[0] + (static_cast<int64_t>(e) * p.N + n) * Ks;
+        if (p.sd) {
+            srow = p.s[0] + e * sd_plane_bytes(p.N, p.K);
+            sd_row = n;
+            sd_tab = p.sd_dict + 32 * e;
+        }
         g = __ldg(p.g_dev + e);
         xrow0 = p.x_per_slot ? sl : sl / p.top_k;
         out0 = sl * p.ldy + n;
@@ -2564,6 +2849,10 @@ __global__ void __launch_bounds__(kSimpleThreads) gemv_simple_kernel(const __gri
         wrow = p.w[grp] + n * Kh;
         srow = p.s[grp] + n * Ks;
         g = p.g[grp];
+        if (p.sd) {
+            srow = p.s[grp];
+            sd_row = n;
+        }
         out0 = col;
         out_step = p.ldy;
     }
@@ -2572,7 +2861,8 @@ __global__ void __launch_bounds__(kSimpleThreads) gemv_simple_kernel(const __gri
 #pragma unroll
         for (int m = 0; m < MT; ++m) acc[m] = 0.f;
         for (int64_t b = lane; b < Ks; b += 32) {
-            const uint32_t shf = cvt_e4m3x2(static_cast<uint16_t>(__ldg(sr + b)));
+            const uint32_t code = p.sd ? sd_code(sr, sd_tab, p.K, sd_row, b) : __ldg(sr + b);
+            const uint32_t shf = cvt_e4m3x2(static_cast<uint16_t>(code));
             const uint16_t sc = static_cast<uint16_t>(shf & 0xffffu);
             for (int e = 0; e < 8; ++e) {
                 uint32_t h[4];
@@ -2958,8 +3248,14 @@ struct TilePlan {
 // SM times the steps each of its warps decodes), both in units of one warp step.
 bool plan_tile(TilePlan& tp, int M, int N, int K, int groups, const DeviceInfo& d, const uint8_t* const* w,
                const uint8_t* const* s, const void* x, bool moe = false, int moe_rows = 0, int moe_groups_max = 0,
-               bool swiglu = false, bool need_encoder = true) {
+               bool swiglu = false, bool need_encoder = true, bool sd = false) {
     if (g_variant == 1 || g_variant == 3) return false;
+    if (sd && (swiglu || (!moe && groups != 1))) return false;  // dictionary scales: dense or MoE
+    // scale box per ring slot and the pair table (dictionary scales)
+    auto sbox = [&](int nc) -> uint32_t {
+        return sd ? (nc == 2 ? scale_box_bytes<2, true>() : scale_box_bytes<1, true>()) : static_cast<uint32_t>(nc) * 256u;
+    };
+    const uint32_t sdtab = sd ? kSdPairs * 4u : 0u;
     if (K <= 0 || K % 256 != 0 || M < 1 || M > 8 || N < 1 || N > (1 << 27)) return false;
     // MoE: M is the largest number of columns of a group (8), groups the expected number of
     // groups (cost only), moe_groups_max the most there can be; moe_rows x rows exist in all
@@ -2981,7 +3277,8 @@ bool plan_tile(TilePlan& tp, int M, int N, int K, int groups, const DeviceInfo& 
         const int nbox = segs / nc;
         for (int sl = 0; (1 << sl) <= 8; ++sl) {
             const int S = 1 << sl;
-            if (S > nbox || (moe && S > 1)) break;
+            // MoE with dictionary scales or more than 32 slots: stream-K only
+            if (S > nbox || (moe && S > 1) || (moe && sd) || (moe && moe_groups_max > kTileMoeSlots)) break;
             if (NVFP4_TILE_S && S != NVFP4_TILE_S) continue;
             const int nbs = (nbox + S - 1) / S;  // most boxes of one rank
             for (int lg = 0; (1 << lg) <= tk::kWarps; ++lg) {
@@ -3019,7 +3316,9 @@ bool plan_tile(TilePlan& tp, int M, int N, int K, int groups, const DeviceInfo& 
                         q.ring_w = off;
                         off += static_cast<uint32_t>(tk::kWarps * st * nc) * 2048u;
                         q.ring_s = off;
-                        off += static_cast<uint32_t>(tk::kWarps * st * nc) * 256u;
+                        off += static_cast<uint32_t>(tk::kWarps * st) * sbox(nc);
+                        q.sdtab_off = off;
+                        off += sdtab;
                         q.x_off = off;
                         off += x_bytes;
                         q.red_off = off;
@@ -3100,13 +3399,22 @@ bool plan_tile(TilePlan& tp, int M, int N, int K, int groups, const DeviceInfo& 
             const long long jobs_max = static_cast<long long>(std::max(moe_groups_max, groups)) * tiles;
             const long long units_lo = std::min<long long>(d.sm_count, jobs);
             const long long jpc_max = (jobs_max + units_lo - 1) / units_lo;
-          for (int aligned = 0; aligned <= NVFP4_SK_GROUP_ALIGNED; ++aligned) {
+          // (dictionary scales need group-aligned ranges: one pair table per CTA)
+          for (int aligned = sd ? 1 : 0; aligned <= NVFP4_SK_GROUP_ALIGNED; ++aligned) {
             // aligned: every CTA inside one group, so at most 8 staged rows; needs a CTA per
             // group at least, whatever the routing
             const int groups_most = std::max(moe_groups_max, groups);
-            const int rows_cap = aligned ? std::min(xrows, 8)
-                                         : static_cast<int>(std::min<long long>(xrows, 8 * ((jpc_max + tiles - 1) / tiles + 1)));
-            const uint32_t x_bytes = align_up(static_cast<uint32_t>(rows_cap) * sstride, 128);
+            // groups one CTA's job range can touch: more than 32 slots keep them in a window of
+            // kMoeWindow table entries, and build the groups in the x region (3 KB of scratch).
+            // Their staging buffer holds 8 x rows, a window's rows for the usual routings (an
+            // expert has a few slots); a CTA whose window needs more computes in exact fp32
+            // with x read from global memory instead.
+            const long long span = aligned ? 1 : (jpc_max + tiles - 1) / tiles + 1;
+            const bool big = moe_groups_max > kTileMoeSlots;
+            if (big && span > kMoeWindow) continue;
+            const int rows_cap = static_cast<int>(std::min<long long>(xrows, big ? 8 : 8 * span));
+            uint32_t x_bytes = align_up(static_cast<uint32_t>(rows_cap) * sstride, 128);
+            if (big) x_bytes = std::max<uint32_t>(x_bytes, 3u * kMaxMoeSlots * 4u);
             int stages = 0, per_sm = 0;
             uint32_t smem = 0;
             TileParams lp{};
@@ -3117,7 +3425,9 @@ bool plan_tile(TilePlan& tp, int M, int N, int K, int groups, const DeviceInfo& 
                     q.ring_w = off;
                     off += static_cast<uint32_t>(tk::kWarps * st * nc) * 2048u;
                     q.ring_s = off;
-                    off += static_cast<uint32_t>(tk::kWarps * st * nc) * 256u;
+                    off += static_cast<uint32_t>(tk::kWarps * st) * sbox(nc);
+                    q.sdtab_off = off;
+                    off += sdtab;
                     q.x_off = off;
                     off += x_bytes;
                     q.red_off = off;  // unused: partial records live in the drained rings
@@ -3189,7 +3499,7 @@ bool encode_tile_maps(CUtensorMap* wmap, CUtensorMap* smap, const uint8_t* w, co
     auto enc = tensor_map_encoder();
     if (!enc) return false;
     const cuuint32_t estr[3] = {1, 1, 1};
-    {
+    if (wmap) {
         const cuuint64_t dims[3] = {128, static_cast<cuuint64_t>(K / 256), static_cast<cuuint64_t>(rows)};
         const cuuint64_t strides[2] = {128, static_cast<cuuint64_t>(K / 2)};
         const cuuint32_t box[3] = {128, static_cast<cuuint32_t>(nc), 16};
@@ -3198,7 +3508,7 @@ bool encode_tile_maps(CUtensorMap* wmap, CUtensorMap* smap, const uint8_t* w, co
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return false;
     }
-    {
+    if (smap) {
         const cuuint64_t dims[3] = {16, static_cast<cuuint64_t>(K / 256), static_cast<cuuint64_t>(rows)};
         const cuuint64_t strides[2] = {16, static_cast<cuuint64_t>(K / 16)};
         const cuuint32_t box[3] = {16, static_cast<cuuint32_t>(nc), 16};
@@ -3210,11 +3520,25 @@ bool encode_tile_maps(CUtensorMap* wmap, CUtensorMap* smap, const uint8_t* w, co
     return true;
 }
 
-template <int NC, bool MOE, bool SK, bool SWI = false>
+// Index plane of dictionary scales viewed as (160 B, K/256, tiles): one record per box segment.
+bool encode_sd_map(CUtensorMap* smap, const uint8_t* plane, int64_t tiles, int K, int nc) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kSdRecord), static_cast<cuuint64_t>(K / 256),
+                                static_cast<cuuint64_t>(tiles)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kSdRecord), static_cast<cuuint64_t>(K / 256) * kSdRecord};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(kSdRecord), static_cast<cuuint32_t>(nc), 1};
+    return enc(smap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(plane), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int NC, bool MOE, bool SK, bool SWI = false, bool SD = false>
 cudaError_t launch_tile_nc(const TilePlan& tp, cudaStream_t st) {
     auto kern = [] {
-        if constexpr (SK) return gemv_tile_sk_kernel<NC, MOE>;
-        else return gemv_tile_kernel<NC, MOE, SWI>;
+        if constexpr (SK) return gemv_tile_sk_kernel<NC, MOE, SD>;
+        else return gemv_tile_kernel<NC, MOE, SWI, SD>;
     }();
     static bool done[64] = {};
     cudaError_t e = allow_max_smem(kern, done);
@@ -3246,12 +3570,21 @@ cudaError_t launch_tile_nc(const TilePlan& tp, cudaStream_t st) {
 // Launch slot of the phase trace: consecutive tile-kernel launches use consecutive slots.
 int g_trace_next = 0;
 
-cudaError_t launch_tile(const TilePlan& tp_in, cudaStream_t st, bool moe) {
+cudaError_t launch_tile(const TilePlan& tp_in, cudaStream_t st, bool moe, bool sd = false) {
     TilePlan tp = tp_in;
     if (NVFP4_PHASE_TRACE) {
         std::lock_guard<std::mutex> lk(g_mu);
         tp.p.trace_slot = g_trace_next;
         g_trace_next = (g_trace_next + 1) % kTraceLaunches;
+    }
+    if (sd) {
+        if (moe) {
+            if (!tp.sk) return cudaErrorInvalidValue;
+            return tp.nc == 2 ? launch_tile_nc<2, true, true, false, true>(tp, st)
+                              : launch_tile_nc<1, true, true, false, true>(tp, st);
+        }
+        return tp.nc == 2 ? launch_tile_nc<2, false, false, false, true>(tp, st)
+                          : launch_tile_nc<1, false, false, false, true>(tp, st);
     }
     if (moe && tp.sk) return tp.nc == 2 ? launch_tile_nc<2, true, true>(tp, st) : launch_tile_nc<1, true, true>(tp, st);
     if (moe) return tp.nc == 2 ? launch_tile_nc<2, true, false>(tp, st) : launch_tile_nc<1, true, false>(tp, st);
@@ -3434,11 +3767,186 @@ nvfp4_status run_dense(const uint8_t* const* w, const uint8_t* const* s, const f
     return e == cudaSuccess ? NVFP4_OK : cuda_fail(e);
 }
 
+// Dense GEMV with dictionary scales: the tile kernel's SD form, else the byte-load kernel.
+nvfp4_status run_sdict_dense(const uint8_t* w, const uint8_t* plane, const uint8_t* dict, float g, const uint16_t* x,
+                             void* y, int y_type, int M, int N, int K, cudaStream_t st) {
+    if (!w || !plane || !dict || !x || !y) return NVFP4_ERR_NULL;
+    if (M < 0 || N < 0 || K < 0 || M > 8 || K % 256 != 0) return NVFP4_ERR_SHAPE;
+    const nvfp4_status so = check_out(y_type);
+    if (so != NVFP4_OK) return so;
+    if (M == 0 || N == 0) return NVFP4_OK;
+    if (K == 0) return zero_output(y, static_cast<int64_t>(M) * N, y_type, st);
+    int dev = 0;
+    const DeviceInfo* d = device_info(&dev);
+    if (!d) return cuda_fail(cudaGetLastError());
+    const uint8_t* wv[1] = {w};
+    const uint8_t* sv[1] = {plane};
+    const bool x_ok = (reinterpret_cast<uintptr_t>(x) & 15) == 0;
+    TilePlan tpl{};
+    const PlanKey key = make_key(dev, 16 + (x_ok ? 0 : 8), M, N, K, 1, wv, sv);
+    const bool tile = cached_tile_plan(key, &tpl, [&](TilePlan& tp) {
+        if (!plan_tile(tp, M, N, K, 1, *d, wv, sv, x, false, 0, 0, false, true, true)) return false;
+        if (!encode_tile_maps(&tp.p.wmap[0], nullptr, w, nullptr, N, K, tp.nc)) return false;
+        if (!encode_sd_map(&tp.p.smap[0], plane, (N + 15) / 16, K, tp.nc)) return false;
+        tp.p.wmap[1] = tp.p.wmap[0];
+        tp.p.smap[1] = tp.p.smap[0];
+        return true;
+    });
+    if (tile) {
+        TileParams& p = tpl.p;
+        p.x = x;
+        p.y = y;
+        p.g[0] = p.g[1] = g;
+        p.ldy = N;
+        p.out_bf16 = y_type == NVFP4_OUT_BF16;
+        p.force_f32 = g_variant == 2;
+        p.wait_ns = g_wait_ns;
+        p.sd_dict = dict;
+        const cudaError_t e = launch_tile(tpl, st, false, true);
+        if (e != cudaSuccess) return cuda_fail(e);
+        const cudaError_t e2 = cudaGetLastError();
+        return e2 == cudaSuccess ? NVFP4_OK : cuda_fail(e2);
+    }
+    SimpleParams sp{};
+    sp.w[0] = sp.w[1] = w;
+    sp.s[0] = sp.s[1] = plane;
+    sp.g[0] = sp.g[1] = g;
+    sp.x = x; sp.y = y; sp.ldy = N; sp.out_bf16 = y_type == NVFP4_OUT_BF16;
+    sp.M = M; sp.N = N; sp.K = K; sp.groups = 1;
+    sp.sd = 1;
+    sp.sd_dict = dict;
+    const cudaError_t e = launch_simple(sp, N, st);
+    return e == cudaSuccess ? NVFP4_OK : cuda_fail(e);
+}
+
+// Routed-expert GEMV with dictionary scales: the stream-K tile kernel's SD form with
+// group-aligned ranges for up to 32 slots, else the byte-load kernel.
+nvfp4_status run_sdict_moe(const uint8_t* w, const uint8_t* plane, const uint8_t* dict, const float* gs, int E,
+                           const int32_t* ids, int T, int top_k, const uint16_t* x, int x_per_slot, void* y,
+                           int y_type, int N, int K, int32_t* status_dev, cudaStream_t st) {
+    if (!w || !plane || !dict || !gs || !ids || !x || !y) return NVFP4_ERR_NULL;
+    if (E < 1 || T < 0 || top_k < 0 || N < 0 || K < 0 || K % 256 != 0) return NVFP4_ERR_SHAPE;
+    if (static_cast<int64_t>(T) * top_k > (1 << 24)) return NVFP4_ERR_UNSUPPORTED;
+    const nvfp4_status so = check_out(y_type);
+    if (so != NVFP4_OK) return so;
+    const int slots = T * top_k;
+    if (slots == 0 || N == 0) return NVFP4_OK;
+    if (K == 0) return zero_output(y, static_cast<int64_t>(slots) * N, y_type, st);
+    int dev = 0;
+    const DeviceInfo* d = device_info(&dev);
+    if (!d) return cuda_fail(cudaGetLastError());
+    const int64_t tiles_n = (N + 15) / 16;
+    if (slots <= kMaxMoeSlots && static_cast<int64_t>(E) * N <= (1 << 30)) {
+        TilePlan tpl{};
+        const uint8_t* wv[1] = {w};
+        const uint8_t* sv[1] = {plane};
+        const int xrows = x_per_slot ? slots : T;
+        const bool x_ok = (reinterpret_cast<uintptr_t>(x) & 15) == 0;
+        const PlanKey key = make_key(dev, 17 + (x_ok ? 0 : 8), 8, N, K, 1, wv, sv, E, T, top_k, x_per_slot ? 1 : 0);
+        const bool tile = cached_tile_plan(key, &tpl, [&](TilePlan& tp) {
+            if (!plan_tile(tp, 8, N, K, expected_groups(E, T, top_k), *d, wv, sv, x, true, xrows, slots, false, true,
+                           true))
+                return false;
+            if (!tp.sk || !tp.p.items_r) return false;  // group-aligned stream-K only
+            if (!encode_tile_maps(&tp.p.wmap[0], nullptr, w, nullptr, static_cast<int64_t>(E) * N, K, tp.nc))
+                return false;
+            if (!encode_sd_map(&tp.p.smap[0], plane, static_cast<int64_t>(E) * tiles_n, K, tp.nc)) return false;
+            tp.p.wmap[1] = tp.p.wmap[0];
+            tp.p.smap[1] = tp.p.smap[0];
+            return true;
+        });
+        if (tile) {
+            TileParams& p = tpl.p;
+            p.x = x;
+            p.y = y;
+            p.ldy = N;
+            p.out_bf16 = y_type == NVFP4_OUT_BF16;
+            p.force_f32 = g_variant == 2;
+            p.wait_ns = g_wait_ns;
+            p.ids = ids;
+            p.g_dev = gs;
+            p.status_user = status_dev;
+            p.E = E;
+            p.top_k = top_k;
+            p.slots = slots;
+            p.x_per_slot = x_per_slot ? 1 : 0;
+            p.sd_dict = dict;
+            p.sd_tiles = static_cast<int>(tiles_n);
+            const cudaError_t e = launch_tile(tpl, st, true, true);
+            if (e != cudaSuccess) return cuda_fail(e);
+            const cudaError_t e2 = cudaGetLastError();
+            return e2 == cudaSuccess ? NVFP4_OK : cuda_fail(e2);
+        }
+    }
+    SimpleParams sp{};
+    sp.w[0] = sp.w[1] = w;
+    sp.s[0] = sp.s[1] = plane;
+    sp.g_dev = gs;
+    sp.ids = ids;
+    sp.status_user = status_dev;
+    sp.x = x; sp.y = y; sp.ldy = N; sp.out_bf16 = y_type == NVFP4_OUT_BF16;
+    sp.M = 1; sp.N = N; sp.K = K; sp.groups = 1;
+    sp.moe = 1; sp.E = E; sp.top_k = top_k; sp.x_per_slot = x_per_slot ? 1 : 0; sp.slots = slots;
+    sp.sd = 1;
+    sp.sd_dict = dict;
+    const cudaError_t e = launch_simple(sp, static_cast<int64_t>(slots) * N, st);
+    return e == cudaSuccess ? NVFP4_OK : cuda_fail(e);
+}
+
 }  // namespace nvfp4
 
 using namespace nvfp4;
 
 extern "C" {
+
+nvfp4_status nvfp4_gemv_sdict(const uint8_t* w_packed, const uint8_t* scale_idx, const uint8_t* scale_dict,
+                              float global_scale, const uint16_t* x, void* y, nvfp4_out_t y_type, int M, int N,
+                              int K, void* stream) {
+    return run_sdict_dense(w_packed, scale_idx, scale_dict, global_scale, x, y, y_type, M, N, K,
+                           static_cast<cudaStream_t>(stream));
+}
+
+nvfp4_status nvfp4_moe_gemv_sdict(const uint8_t* w_packed, const uint8_t* scale_idx, const uint8_t* scale_dict,
+                                  const float* global_scales, int E, const int32_t* expert_ids, int T, int top_k,
+                                  const uint16_t* x, int x_per_slot, void* y, nvfp4_out_t y_type, int N, int K,
+                                  int32_t* status_dev, void* stream) {
+    return run_sdict_moe(w_packed, scale_idx, scale_dict, global_scales, E, expert_ids, T, top_k, x, x_per_slot, y,
+                         y_type, N, K, status_dev, static_cast<cudaStream_t>(stream));
+}
+
+int64_t nvfp4_sdict_plane_bytes(int N, int K) {
+    if (N < 0 || K < 0 || K % 256 != 0) return -1;
+    return sd_plane_bytes(N, K);
+}
+
+int nvfp4_sdict_encode(const uint8_t* scales, int N, int K, uint8_t* plane_out, uint8_t* dict_out) {
+    if (!dict_out || N < 0 || K < 0 || K % 256 != 0 || (N > 0 && K > 0 && (!scales || !plane_out))) return -2;
+    const int64_t blocks = static_cast<int64_t>(K) / 16;
+    bool used[256] = {};
+    for (int64_t i = 0; i < static_cast<int64_t>(N) * blocks; ++i) used[scales[i]] = true;
+    int index_of[256];
+    int count = 0;
+    uint8_t table[32] = {};
+    for (int c = 0; c < 256; ++c) {
+        if (!used[c]) continue;
+        if (count == 32) return -1;  // more than 32 codes: the tensor stays plain
+        index_of[c] = count;
+        table[count++] = static_cast<uint8_t>(c);
+    }
+    for (int i = count; i < 32; ++i) table[i] = count ? table[count - 1] : 0;
+    std::memcpy(dict_out, table, 32);
+    if (sd_plane_bytes(N, K) > 0) std::memset(plane_out, 0, static_cast<size_t>(sd_plane_bytes(N, K)));
+    for (int64_t n = 0; n < N; ++n) {
+        for (int64_t b = 0; b < blocks; ++b) {
+            const uint32_t v = static_cast<uint32_t>(index_of[scales[n * blocks + b]]);
+            uint8_t* rec = plane_out + ((n >> 4) * (K >> 8) + (b >> 4)) * kSdRecord;
+            const uint32_t bit = static_cast<uint32_t>(((n & 15) * 16 + (b & 15)) * 5);
+            for (int i = 0; i < 5; ++i)
+                if ((v >> i) & 1u) rec[(bit + i) >> 3] |= static_cast<uint8_t>(1u << ((bit + i) & 7));
+        }
+    }
+    return count;
+}
 
 nvfp4_status nvfp4_gemv(const uint8_t* w_packed, const uint8_t* w_scales, float global_scale,
                         const uint16_t* x, void* y, nvfp4_out_t y_type, int M, int N, int K, void* stream) {
@@ -3487,8 +3995,9 @@ nvfp4_status nvfp4_moe_gemv(const uint8_t* w_packed, const uint8_t* w_scales,
     int dev = 0;
     const DeviceInfo* d = device_info(&dev);
     if (!d) return cuda_fail(cudaGetLastError());
-    if (slots <= kTileMoeSlots && static_cast<int64_t>(E) * N <= (1 << 30)) {
-        // warp-tile kernel: every routed expert's slab is read once for all of its slots
+    if (slots <= kMaxMoeSlots && static_cast<int64_t>(E) * N <= (1 << 30)) {
+        // warp-tile kernel: every routed expert's slab is read once for up to 8 of its slots
+        // (more than 32 slots: the stream-K form only)
         TilePlan tpl{};
         const uint8_t* wv[1] = {w_packed};
         const uint8_t* sv[1] = {w_scales};
@@ -3642,6 +4151,31 @@ int describe_plan_on(const DeviceInfo* d, bool host_only, int kind, int M, int N
     // Pointers are only inspected for alignment here; 256-byte aligned stand-ins.
     const uint8_t* fake = reinterpret_cast<const uint8_t*>(static_cast<uintptr_t>(256));
     const uint8_t* w[2] = {fake, fake};
+    if (kind == 5) {  // dense with dictionary scales: the tile kernel's SD form, else the byte-load kernel
+        TilePlan tpl{};
+        if (K % 256 == 0 && plan_tile(tpl, M, N, K, 1, *d, w, w, fake, false, 0, 0, false, !host_only, true))
+            return snprintf(buf, buflen,
+                            "tile_sdict grid=%d block=%d smem=%u split=%d rows_per_item=%d k_warps=%d mt=%d stages=%d nc=%d",
+                            tpl.grid_x * tpl.grid_y, tk::kThreads, tpl.smem, 1 << tpl.p.s_log2, tpl.p.tpi * 16,
+                            1 << tpl.p.ksplit_log2, M, tpl.p.stages, tpl.nc);
+        return snprintf(buf, buflen, "simple grid=%lld block=%d smem=0 split=1 rows_per_item=0 k_warps=0",
+                        static_cast<long long>((static_cast<int64_t>(N) + 7) / 8), kSimpleThreads);
+    }
+    if (kind == 6 || kind == 7) {  // MoE with dictionary scales (M = E; 7: one x row per slot)
+        TilePlan tpl{};
+        const int slots = T * top_k, E = M;
+        const int xrows = kind == 7 ? slots : T;
+        if (K % 256 == 0 && slots <= kMaxMoeSlots && E >= 1 && static_cast<int64_t>(E) * N <= (1 << 30) &&
+            plan_tile(tpl, 8, N, K, expected_groups(E, T, top_k), *d, w, w, fake, true, xrows, slots, false,
+                      !host_only, true) &&
+            tpl.sk && tpl.p.items_r)
+            return snprintf(buf, buflen,
+                            "tile_sk_moe_sdict grid=%d block=%d smem=%u split=1 rows_per_item=%d k_warps=1 mt=8 "
+                            "stages=%d nc=%d group_aligned=1",
+                            tpl.grid_x, tk::kThreads, tpl.smem, tpl.p.tpi * 16, tpl.p.stages, tpl.nc);
+        return snprintf(buf, buflen, "simple grid=%lld block=%d smem=0 split=1 rows_per_item=0 k_warps=0",
+                        static_cast<long long>((static_cast<int64_t>(slots) * N + 7) / 8), kSimpleThreads);
+    }
     if (kind == 4) {  // gate/up with the fused activation: the tile kernel, else the byte-load kernel
         TilePlan tpl{};
         if (plan_tile(tpl, M, N, K, 2, *d, w, w, fake, false, 0, 0, true, !host_only))
@@ -3668,7 +4202,7 @@ int describe_plan_on(const DeviceInfo* d, bool host_only, int kind, int M, int N
         TilePlan tpl{};
         const int slots = T * top_k, E = M;
         const int xrows = kind == 3 ? slots : T;
-        if (slots <= kTileMoeSlots && E >= 1 && static_cast<int64_t>(E) * N <= (1 << 30) &&
+        if (slots <= kMaxMoeSlots && E >= 1 && static_cast<int64_t>(E) * N <= (1 << 30) &&
             plan_tile(tpl, 8, N, K, expected_groups(E, T, top_k), *d, w, w, fake, true, xrows, slots, false,
                       !host_only)) {
             return snprintf(buf, buflen,
@@ -3706,7 +4240,7 @@ int nvfp4_describe_plan(int kind, int M, int N, int K, int T, int top_k, char* b
 int nvfp4_describe_plan_host(int sm_count, int smem_optin, int smem_per_sm, int kind, int M, int N, int K, int T,
                              int top_k, char* buf, int buflen) {
     if (!buf || buflen < 1 || sm_count < 1 || smem_optin < 1 || smem_per_sm < smem_optin) return -1;
-    if (kind < 0 || kind > 4) return -1;
+    if (kind < 0 || kind > 7) return -1;
     DeviceInfo d;
     d.sm_count = sm_count;
     d.smem_optin = smem_optin;

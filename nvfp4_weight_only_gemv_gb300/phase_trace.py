@@ -95,7 +95,7 @@ def launch(nv, c, d, x=None):
 
 
 def summarise(tr, launches, calls_meta):
-    """tr: [16, 1024, 32] int64. Returns the report lines."""
+    """tr: [16, 1024, 40] int64. Returns the report lines."""
     tr = tr.numpy().astype(np.int64)
     entries = tr[:launches, :, 0]
     origin = entries[entries > 0].min()

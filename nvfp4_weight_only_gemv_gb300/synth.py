@@ -97,6 +97,81 @@ def random_weight(N: int, K: int, seed: int, device="cpu", std: float = 0.02):
     return packed, scales, g
 
 
+def _quantize_with_codes(w: torch.Tensor, g: float, codes: torch.Tensor):
+    """quantize() with every block scale drawn from ``codes`` (u8 E4M3 codes, increasing in
+    value): the smallest code whose value is >= amax_b / (6 g), else the largest code."""
+    N, K = w.shape
+    blocks = w.to(torch.float32).reshape(N, K // 16, 16)
+    need = blocks.abs().amax(dim=-1) / (6.0 * g)
+    vals = codes.view(torch.float8_e4m3fn).to(torch.float32)
+    pick = torch.searchsorted(vals, need.contiguous()).clamp(max=codes.numel() - 1)
+    scales = codes[pick]
+    denom = scales.view(torch.float8_e4m3fn).to(torch.float32) * g
+    safe = torch.where(denom > 0, denom, torch.ones_like(denom))
+    q = torch.where((denom > 0)[..., None], blocks / safe[..., None], torch.zeros_like(blocks))
+    c = _encode_e2m1(q.clamp(-E2M1_MAX, E2M1_MAX)).reshape(N, K)
+    return (c[:, 0::2] | (c[:, 1::2] << 4)).contiguous(), scales.contiguous()
+
+
+def random_weight_sdict(N: int, K: int, seed: int, device="cpu", std: float = 0.02, max_codes: int = 32):
+    """random_weight() whose block scales take at most ``max_codes`` distinct E4M3 codes, so that
+    the tensor has a scale-dictionary form. When the plain recipe gives more, the most frequent
+    codes are kept and every block takes the smallest kept code that still covers its amax
+    (no E2M1 clipping), the codes requantised with it."""
+    packed, scales, g = random_weight(N, K, seed, device, std)
+    vals, counts = torch.unique(scales, return_counts=True)
+    if vals.numel() <= max_codes:
+        return packed, scales, g
+    keep = vals[counts.argsort(descending=True)[:max_codes]]
+    keep = keep[keep.view(torch.float8_e4m3fn).to(torch.float32).argsort()]
+    rows = max(1, _CHUNK_ELEMS // max(K, 1))
+    gen = _gen(seed, device)  # the stream random_weight quantised, drawn again chunk by chunk
+    for r0 in range(0, N, rows):
+        n = min(rows, N - r0)
+        w = torch.randn(n, K, generator=gen, device=device) * std
+        packed[r0:r0 + n], scales[r0:r0 + n] = _quantize_with_codes(w, g, keep)
+    return packed, scales, g
+
+
+def sdict_problem(N: int, K: int, M: int, seed: int, device="cpu"):
+    """A dense problem whose weight has at most 32 scale codes: dict(w, s, g, x), s plain."""
+    w, s, g = random_weight_sdict(N, K, seed * 2 + 1, device)
+    return {"w": w, "s": s, "g": g, "x": random_x(M, K, seed * 2 + 2, device), "N": N, "K": K, "M": M}
+
+
+def sdict_pack(ind: torch.Tensor, N: int, K: int) -> torch.Tensor:
+    """Index plane of a scale-dictionary tensor from its block indices ind [N, K/16] (0..31):
+    one 160-byte record per 16-row tile r and 256-column segment c at byte (r * K/256 + c) * 160,
+    the index of (row 16r + i, block 16c + j) at bits 5q .. 5q + 4 (q = 16i + j, least significant
+    first; bit p of a record is bit p % 8 of byte p / 8). The 8 indices q = 8p .. 8p + 7 fill
+    bytes 5p .. 5p + 4. Returns uint8 [((N + 15) // 16) * (K // 256) * 160] on the CPU."""
+    segs, tiles = K // 256, (N + 15) // 16
+    full = torch.zeros(tiles * 16, K // 16, dtype=torch.int64)
+    full[:N] = ind.to("cpu", torch.int64)
+    rec = full.reshape(tiles, 16, segs, 16).permute(0, 2, 1, 3).reshape(tiles, segs, 32, 8)
+    v = torch.zeros(rec.shape[:3], dtype=torch.int64)
+    for k in range(8):
+        v |= rec[..., k] << (5 * k)
+    out = torch.stack([(v >> (8 * m)) & 0xFF for m in range(5)], dim=-1).to(torch.uint8)
+    return out.reshape(-1)
+
+
+def sdict_form(s: torch.Tensor):
+    """Dictionary form of plain block scales s [N, K/16] with at most 32 distinct codes: the
+    table holds the codes in increasing byte order (its tail repeats the last one), each block
+    its code's position. Returns (index plane, table [32]) as uint8 tensors on s's device.
+    For s [E, N, K/16] (one dictionary per expert) returns ([E, plane], [E, 32])."""
+    if s.dim() == 3:
+        forms = [sdict_form(s[e]) for e in range(s.shape[0])]
+        return torch.stack([f[0] for f in forms]), torch.stack([f[1] for f in forms])
+    codes = torch.unique(s.to("cpu"))
+    if not 0 < codes.numel() <= 32:
+        raise ValueError(f"{codes.numel()} distinct scale codes: no dictionary form")
+    table = torch.cat([codes, codes[-1:].repeat(32 - codes.numel())]).to(torch.uint8)
+    ind = torch.searchsorted(codes, s.to("cpu").contiguous())
+    return sdict_pack(ind, s.shape[0], s.shape[1] * 16).to(s.device), table.to(s.device)
+
+
 def random_x(M: int, K: int, seed: int, device="cpu") -> torch.Tensor:
     """bf16 activations ~N(0, 1), shape [M, K]."""
     return torch.randn(M, K, generator=_gen(seed, device), device=device).to(torch.bfloat16)
@@ -127,14 +202,15 @@ def routing(T: int, top_k: int, E: int, seed: int) -> torch.Tensor:
 
 
 def moe_problem(E: int, N: int, K: int, T: int, top_k: int, x_per_slot: bool, seed: int,
-                device="cpu", fill: str = "routed", ids=None):
+                device="cpu", fill: str = "routed", ids=None, max_codes: int | None = None):
     """Routed-expert problem: w [E, N, K/2], s [E, N, K/16], gs [E] f32, ids, x.
 
     Expert e's weight comes from seed ``seed * 1000 + e``. ``fill="routed"``
     generates only the experts that ``ids`` names. The others keep zero bytes
     (code 0, scale 0) and a global scale of 1. That is enough for anything that reads only the routed
     slabs, and it keeps CPU generation fast. ``fill="all"`` generates every expert. ``ids``
-    (T * top_k ints) replaces the seeded routing when given.
+    (T * top_k ints) replaces the seeded routing when given. ``max_codes`` limits each expert's
+    block scales to that many distinct codes (random_weight_sdict).
     """
     ids = routing(T, top_k, E, seed) if ids is None else torch.as_tensor(ids, dtype=torch.int32).reshape(-1).cpu()
     assert ids.numel() == T * top_k
@@ -143,7 +219,10 @@ def moe_problem(E: int, N: int, K: int, T: int, top_k: int, x_per_slot: bool, se
     gs = torch.ones(E, dtype=torch.float32)
     experts = range(E) if fill == "all" else sorted(set(int(e) for e in ids.tolist()))
     for e in experts:
-        we, se, ge = random_weight(N, K, seed * 1000 + e, device)
+        if max_codes is None:
+            we, se, ge = random_weight(N, K, seed * 1000 + e, device)
+        else:
+            we, se, ge = random_weight_sdict(N, K, seed * 1000 + e, device, max_codes=max_codes)
         w[e], s[e], gs[e] = we, se, ge
     rows = T * top_k if x_per_slot else T
     x = random_x(rows, K, seed * 1000 + E + 7, device)

@@ -17,6 +17,7 @@
 
 #include "../../nvfp4_weight_only_gemv_gb300/csrc/nvfp4_gemv.cu"
 
+#include <algorithm>
 #include <array>
 #include <vector>
 
@@ -358,6 +359,76 @@ static void check_moe_groups(int slots, int E, int top_k, bool per_slot, unsigne
     for (int s = 0; s < slots; ++s) CHECK(seen[s] == ((ids[s] >= 0 && ids[s] < E) ? 1 : 0), "slot %d seen %d", s, seen[s]);
 }
 
+// tile_moe_groups_big and tile_moe_window on the host, step for step: leaders are experts' first
+// slots, groups of up to 8 slots numbered by an exclusive scan over the leaders; every valid slot
+// lands in exactly one window entry when the CTA ranges walk all groups in windows.
+static void check_moe_groups_big(int slots, int E, int top_k, bool per_slot, unsigned seed) {
+    std::vector<int> ids(slots), cnt(slots), ngr(slots);
+    unsigned r = seed;
+    for (int s = 0; s < slots; ++s) {
+        r = r * 1103515245u + 12345u;
+        const int hot = (r >> 8) % 4 == 0;  // a quarter of the slots go to three hot experts
+        ids[s] = hot ? (int)((r >> 4) % 3) : (int)((r >> 12) % (E + 2)) - 1;  // some invalid (-1, E)
+    }
+    std::vector<int> sid(slots);
+    for (int s = 0; s < slots; ++s) sid[s] = (ids[s] >= 0 && ids[s] < E) ? ids[s] : -1;
+    for (int t = 0; t < slots; ++t) {
+        bool leader = sid[t] >= 0;
+        for (int u = 0; u < t && leader; ++u) leader = sid[u] != sid[t];
+        int c = 0;
+        if (leader)
+            for (int u = t; u < slots; ++u) c += sid[u] == sid[t];
+        cnt[t] = c;
+        ngr[t] = (c + 7) / 8;
+    }
+    int run = 0;
+    for (int t = 0; t < slots; ++t) {
+        const int v = ngr[t];
+        ngr[t] = run;
+        run += v;
+    }
+    const int ngroups = run;
+    std::vector<int> seen(slots, 0);
+    for (int g_lo = 0; g_lo < ngroups; g_lo += kMoeWindow) {
+        const int g_hi = std::min(ngroups - 1, g_lo + kMoeWindow - 1);
+        int count[kMoeWindow] = {}, expert[kMoeWindow], slot[kMoeWindow][8];
+        for (int t = 0; t < slots; ++t) {
+            const int c = cnt[t];
+            if (c == 0) continue;
+            const int gf = ngr[t], gl = gf + (c + 7) / 8 - 1;
+            if (gl < g_lo || gf > g_hi) continue;
+            int i = 0;
+            for (int u = t; u < slots && i < c; ++u) {
+                if (sid[u] != sid[t]) continue;
+                const int g = gf + (i >> 3), j = i & 7;
+                if (g >= g_lo && g <= g_hi) {
+                    slot[g - g_lo][j] = u;
+                    if (j == 0) {
+                        expert[g - g_lo] = sid[t];
+                        count[g - g_lo] = std::min(8, c - i);
+                    }
+                }
+                ++i;
+            }
+        }
+        std::vector<int> rows;
+        for (int lg = 0; lg <= g_hi - g_lo; ++lg) {
+            CHECK(count[lg] >= 1 && count[lg] <= 8, "big group size %d", count[lg]);
+            for (int j = 0; j < count[lg]; ++j) {
+                const int u = slot[lg][j];
+                CHECK(u >= 0 && u < slots && sid[u] == expert[lg], "big member");
+                if (j) CHECK(slot[lg][j] > slot[lg][j - 1], "big slot order");
+                seen[u]++;
+                rows.push_back(per_slot ? u : u / top_k);
+            }
+        }
+        std::sort(rows.begin(), rows.end());
+        rows.erase(std::unique(rows.begin(), rows.end()), rows.end());
+        CHECK(rows.size() <= 32, "window rows %zu", rows.size());
+    }
+    for (int s = 0; s < slots; ++s) CHECK(seen[s] == (sid[s] >= 0 ? 1 : 0), "big slot %d seen %d", s, seen[s]);
+}
+
 int main() {
     DeviceInfo d;
     d.sm_count = kSms;
@@ -418,7 +489,38 @@ int main() {
         CHECK(tp.p.moe_off % 16 == 0 && tp.p.moe_off >= tp.p.bar_off + 8 * 4 * 8, "group tables offset");
         CHECK(tp.p.moe_off + sizeof(TileMoe) + 1024 <= tp.smem, "group tables inside the allocation");
     }
-    printf("per-item plans %d, fused gate/up plans %d, MoE plans %d, group-aligned %d, fails %d\n", n_items, n_sw,
-           n_moe, n_aligned, fails);
+    // more than 32 slots: the stream-K form, scratch room in the x region, windows of groups
+    int n_big = 0;
+    for (unsigned seed = 1; seed < 400; ++seed)
+        for (int slots : {33, 40, 64, 128, 200, 256})
+            for (int E : {3, 40, 288}) check_moe_groups_big(slots, E, 8, seed & 1, seed * 131 + slots + E);
+    for (const auto& mm : std::vector<std::array<int, 2>>{{3072, 4096}, {4096, 1536}, {200, 1024}, {64, 256}}) {
+        for (int slots : {40, 64, 128, 256}) {
+            for (int per_slot = 0; per_slot < 2; ++per_slot) {
+                TilePlan tp{};
+                const int xrows = per_slot ? slots : slots / 8;
+                if (!plan_tile(tp, 8, mm[0], mm[1], expected_groups(288, slots / 8, 8), d, w, w, fake, true, xrows,
+                               slots, false, false)) {
+                    CHECK(false, "no MoE plan for %d x %d, %d slots", mm[0], mm[1], slots);
+                    continue;
+                }
+                ++n_big;
+                CHECK(tp.sk, "more than 32 slots take the stream-K form");
+                CHECK(tp.p.misc_off - tp.p.x_off >= 3u * kMaxMoeSlots * 4u, "group-building scratch in the x region");
+                CHECK(tp.p.M <= 8 && tp.p.M >= 1, "x rows staged");
+                for (int ng = 1; ng <= slots; ng += (ng < 16 ? 1 : 7)) {
+                    check_sk(tp, ng * tp.p.tiles, ng);
+                    const int jobs = ng * tp.p.tiles, G = tp.grid_x;
+                    for (int cta = 0; cta < G && !tp.p.items_r; ++cta) {
+                        const int q = jobs / G, r = jobs % G;
+                        const int j0 = cta * q + std::min(cta, r), j1 = j0 + q + (cta < r ? 1 : 0);
+                        if (j0 < j1) CHECK((j1 - 1) / tp.p.tiles - j0 / tp.p.tiles + 1 <= kMoeWindow, "window span");
+                    }
+                }
+            }
+        }
+    }
+    printf("per-item plans %d, fused gate/up plans %d, MoE plans %d, group-aligned %d, large MoE plans %d, fails %d\n",
+           n_items, n_sw, n_moe, n_aligned, n_big, fails);
     return fails != 0;
 }

@@ -14,6 +14,7 @@ import os
 
 import numpy as np
 import pytest
+import torch
 
 import oracle
 from nvfp4_weight_only_gemv_gb300 import synth
@@ -79,6 +80,24 @@ def test_index_extraction_matches_an_independent_reader(N, K):
         for b in range(K // 16):
             assert read_index(plane, K, n, b) == ind[n, b]
             assert oracle.sdict_index(plane, K, n, b) == ind[n, b]
+
+
+@pytest.mark.parametrize("N,K", [(16, 256), (40, 512), (33, 768), (1, 256), (130, 4096)])
+def test_generator_packer_matches_the_bitwise_one(N, K):
+    # the input generator's vectorised packer (which GPU tests and the benchmark use) writes
+    # the same bytes as this file's bit-by-bit packer
+    _, _, ind, _ = random_case(N, K, 1, 3 + N)
+    assert np.array_equal(synth.sdict_pack(torch.from_numpy(ind), N, K).numpy(), pack_indices(ind, N, K))
+
+
+def test_generator_dictionary_form_round_trips():
+    w, s, g = synth.random_weight_sdict(300, 1024, 5, max_codes=12)
+    plane, table = synth.sdict_form(s)
+    codes = np.unique(s.numpy())
+    assert codes.size <= 12 and np.array_equal(table.numpy()[:codes.size], codes)
+    for n in (0, 17, 299):
+        for b in (0, 5, 63):
+            assert table[oracle.sdict_index(plane.numpy(), 1024, n, b)] == s[n, b]
 
 
 @pytest.mark.parametrize("N,K,M", [(16, 256, 1), (40, 512, 3), (77, 1024, 2), (5, 256, 8)])

@@ -61,7 +61,8 @@ def test_routed_experts_take_the_stream_k_form(kind, T, N, K):
 
 
 def test_fallback_kernels():
-    assert plan("moe", 288, 3072, 4096, 8, 8)[0] == "stream_moe"      # 64 slots: above the tile limit
+    assert plan("moe", 288, 3072, 4064, 8, 8)[0] == "stream_moe"      # K % 256 != 0, K % 32 == 0
+    assert plan("moe", 40, 64, 256, 100, 3)[0] == "simple"            # 300 slots: above every tiled limit
     assert plan("dense", 1, 100, 4064)[0] == "stream"                  # K % 256 != 0, K % 32 == 0
     assert plan("dense", 1, 100, 528)[0] == "simple"                   # K % 32 != 0
     assert plan("gate_up_swiglu", 1, 100, 4064)[0] == "simple"         # no streaming form fused
@@ -97,3 +98,12 @@ def test_force_variant_environment(value, kernel):
     out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=300)
     assert out.returncode == 0, out.stderr
     assert out.stdout.strip() == kernel
+
+
+@pytest.mark.parametrize("x_per_slot,N,K", [(False, 3072, 4096), (True, 4096, 1536)])
+@pytest.mark.parametrize("T", [5, 8, 16, 32])
+def test_larger_moe_routings_take_the_stream_k_form(x_per_slot, N, K, T):
+    # 40..256 slots: the stream-K tile kernel (groups built by the whole CTA, a window of up
+    # to 4 of them per CTA), no longer the streaming kernel
+    name, f = plan("moe_per_slot" if x_per_slot else "moe", 288, N, K, T, 8)
+    assert name == "tile_sk_moe" and fits(f) and f["mt"] == 8

@@ -34,5 +34,5 @@ def test_tile_plans_and_indexes(tmp_path, aligned):
     assert run.returncode == 0 and out and out[-1].endswith("fails 0"), run.stdout[-3000:]
     counts = dict(part.rsplit(" ", 1) for part in out[-1].split(", "))
     assert int(counts["per-item plans"]) >= 300 and int(counts["fused gate/up plans"]) >= 150
-    assert int(counts["MoE plans"]) == 5
+    assert int(counts["MoE plans"]) == 5 and int(counts["large MoE plans"]) == 32
     assert (int(counts["group-aligned"]) >= 1) == bool(aligned)
