@@ -79,6 +79,10 @@ constexpr int kTraceCtas = 1024;
 constexpr int kTraceWords = 40;
 #if NVFP4_PHASE_TRACE
 __device__ unsigned long long g_trace[kTraceLaunches * kTraceCtas * kTraceWords];
+// The CTA's words collect in shared memory and go to g_trace at exit (trace_flush): a global
+// store here would hold up the next release-ordered operation (an mbarrier fence or arrive) for
+// its round trip and so distort the phases it measures.
+__shared__ unsigned long long s_trace[kTraceWords];
 #endif
 
 // ------------------------------------------------------------------ parameters
@@ -365,10 +369,31 @@ __device__ __forceinline__ float swiglu_f32(float gate, float up, float lim) {
 
 __device__ __forceinline__ void trace_word(int slot, int word, unsigned long long v) {
 #if NVFP4_PHASE_TRACE
-    if (blockIdx.x < kTraceCtas)
-        g_trace[(static_cast<size_t>(slot) * kTraceCtas + blockIdx.x) * kTraceWords + word] = v;
+    (void)slot;
+    s_trace[word] = v;
 #else
     (void)slot; (void)word; (void)v;
+#endif
+}
+
+// Clears the CTA's trace words (all threads, before any trace_word; ends with __syncthreads).
+__device__ __forceinline__ void trace_begin(int tid) {
+#if NVFP4_PHASE_TRACE
+    if (tid < kTraceWords) s_trace[tid] = 0;
+    __syncthreads();
+#else
+    (void)tid;
+#endif
+}
+
+// Writes the CTA's trace words to its slot (all threads, at exit).
+__device__ __forceinline__ void trace_flush(int slot, int tid) {
+#if NVFP4_PHASE_TRACE
+    __syncthreads();
+    if (tid < kTraceWords && blockIdx.x < kTraceCtas)
+        g_trace[(static_cast<size_t>(slot) * kTraceCtas + blockIdx.x) * kTraceWords + tid] = s_trace[tid];
+#else
+    (void)slot; (void)tid;
 #endif
 }
 
@@ -1309,23 +1334,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
         ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar) : "memory");
 }
 
-#ifndef NVFP4_PARAM_WARM
-#define NVFP4_PARAM_WARM 0  // 1: touch every 64-byte line of the launch parameters at kernel entry
-#endif
-
-// Loads one word of every 64-byte line of the launch parameters' scalar part at once, so that
-// their first-touch misses overlap instead of arriving one at a time through the prologue.
-template <typename P, typename F>
-__device__ __forceinline__ void warm_params(const P& p, const F& first_scalar) {
-    const char* b = reinterpret_cast<const char*>(&first_scalar);
-    const char* e = reinterpret_cast<const char*>(&p) + sizeof(P);
-    uint32_t acc = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-        if (b + 64 * i + 4 <= e) acc ^= *reinterpret_cast<const uint32_t*>(b + 64 * i);
-    asm volatile("" ::"r"(acc));
-}
-
 #ifndef NVFP4_PREFETCH_TMAP
 #define NVFP4_PREFETCH_TMAP 1  // 1: fetch the launch's tensor-map descriptors at kernel entry
 #endif
@@ -1375,6 +1383,9 @@ __host__ __device__ __forceinline__ int tile_row_perm(int g) {
 #ifndef NVFP4_STAGE_PRE
 #define NVFP4_STAGE_PRE 2
 #endif
+#ifndef NVFP4_SK_STAGE_PRE
+#define NVFP4_SK_STAGE_PRE 2  // loads in flight per lane when the stream-K form stages x (8 measured no better)
+#endif
 #ifndef NVFP4_DENSE_EARLY
 #define NVFP4_DENSE_EARLY 4  // ring slots a dense warp requests before the dependency wait (the rest after x staging)
 #endif
@@ -1386,11 +1397,10 @@ __host__ __device__ __forceinline__ int tile_row_perm(int g) {
 // value converted exactly (uniform over the slice's warps); otherwise the caller re-stages
 // with a power-of-two scale. `vote` is gw words of shared scratch; bar_id < 0: one warp.
 // after_issue() runs once the first loads are out (M > 0 or not).
-template <typename F>
+template <int kPre = NVFP4_STAGE_PRE, typename F>
 __device__ bool stage_x_direct(const uint16_t* __restrict__ x, const int* rowsel, int M, int K, int k0, int kn,
                                uint8_t* xs, uint32_t sstride, uint32_t* vote, int gi, int gw, int bar_id, int lane,
                                F&& after_issue) {
-    constexpr int kPre = NVFP4_STAGE_PRE;
     const int cpr = kn >> 3;
     const int tl = gi * 32 + lane, nt = gw * 32;
     int m = 0, c = tl;
@@ -1831,31 +1841,48 @@ __device__ void tile_moe_groups(const TileParams& p, TileMoe* tab, int lane) {
 
 // The x rows that groups [g0, g1] need, staged in increasing row order (at most 32 rows).
 // Routed-expert groups of a stream-K launch with more than 32 slots (up to kMaxMoeSlots), built
-// by all threads: a leader is an expert's first slot; the expert's slots form groups of up to 8 in
-// slot order, numbered from ngr[leader], leaders in slot order. Scratch: ids, cnt, ngr, each
-// kMaxMoeSlots ints. Invalid ids form no group: CTA 0 zeroes their outputs and flags them.
+// by all threads: one pass over the ids (in shared memory, four at a time) gives each slot its
+// rank among the earlier slots of its expert, its expert's slot count and first slot (the
+// leader); the expert's slots form groups of up to 8 in slot order, numbered from ngr[leader],
+// leaders in slot order. Scratch: ids, rank, cnt, lead, ngr, each kMaxMoeSlots ints (5 KB).
+// Invalid ids form no group: CTA 0 zeroes their outputs and flags them.
+constexpr int kMoeScratchInts = 5 * kMaxMoeSlots;
 __device__ void tile_moe_groups_big(const TileParams& p, TileMoe* tab, int* scratch, int tid) {
     int* ids = scratch;
-    int* cnt = scratch + kMaxMoeSlots;
-    int* ngr = scratch + 2 * kMaxMoeSlots;
-    for (int t = tid; t < p.slots; t += tk::kThreads) {
-        const int id = __ldg(p.ids + t);
-        ids[t] = (id >= 0 && id < p.E) ? id : -1;
-        if (!(id >= 0 && id < p.E) && blockIdx.x == 0) {
-            raise_status(NVFP4_DEV_BAD_EXPERT, p.status_user);
-            for (int n = 0; n < p.N; ++n) store_out(p.y, static_cast<int64_t>(t) * p.N + n, 0.f, p.out_bf16);
+    int* rank = scratch + kMaxMoeSlots;
+    int* cnt = scratch + 2 * kMaxMoeSlots;
+    int* lead = scratch + 3 * kMaxMoeSlots;
+    int* ngr = scratch + 4 * kMaxMoeSlots;
+    for (int t = tid; t < kMaxMoeSlots; t += tk::kThreads) {
+        int v = -2 - t;  // past the slots: matches nothing
+        if (t < p.slots) {
+            const int id = __ldg(p.ids + t);
+            v = (id >= 0 && id < p.E) ? id : -2 - t;
+            if (!(id >= 0 && id < p.E) && blockIdx.x == 0) {
+                raise_status(NVFP4_DEV_BAD_EXPERT, p.status_user);
+                for (int n = 0; n < p.N; ++n) store_out(p.y, static_cast<int64_t>(t) * p.N + n, 0.f, p.out_bf16);
+            }
         }
+        ids[t] = v;
     }
     __syncthreads();
     for (int t = tid; t < p.slots; t += tk::kThreads) {
         const int id = ids[t];
-        bool leader = id >= 0;
-        for (int u = 0; u < t && leader; ++u) leader = ids[u] != id;
-        int c = 0;
-        if (leader)
-            for (int u = t; u < p.slots; ++u) c += ids[u] == id;
-        cnt[t] = c;
-        ngr[t] = (c + 7) / 8;
+        int r = 0, c = 0, first = t;
+        const int4* ids4 = reinterpret_cast<const int4*>(ids);
+        for (int q = 0; q < (p.slots + 3) / 4; ++q) {
+            const int4 v = ids4[q];
+            const int u = 4 * q;
+            const int e0 = v.x == id, e1 = v.y == id, e2 = v.z == id, e3 = v.w == id;
+            c += e0 + e1 + e2 + e3;
+            r += (e0 & (u < t)) + (e1 & (u + 1 < t)) + (e2 & (u + 2 < t)) + (e3 & (u + 3 < t));
+            first = min(first, min(min(e0 ? u : t, e1 ? u + 1 : t), min(e2 ? u + 2 : t, e3 ? u + 3 : t)));
+        }
+        const bool valid = id >= 0;
+        rank[t] = r;
+        cnt[t] = valid ? c : 0;
+        lead[t] = first;
+        ngr[t] = valid && r == 0 ? (c + 7) / 8 : 0;
     }
     __syncthreads();
     if (tid < 32) {
@@ -1878,7 +1905,7 @@ __device__ void tile_moe_groups_big(const TileParams& p, TileMoe* tab, int* scra
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const int t = tid * 8 + i;
-            if (t < p.slots) ngr[t] = run;  // now: the first group of leader t
+            if (t < p.slots) ngr[t] = run;  // now: the first group of the expert that t leads
             run += local[i];
         }
         if (tid == 31) tab->n_groups = incl;
@@ -1891,33 +1918,26 @@ __device__ void tile_moe_groups_big(const TileParams& p, TileMoe* tab, int* scra
 // increasing order, and each member's staged column. All threads; ends with __syncthreads.
 __device__ void tile_moe_window(const TileParams& p, TileMoe* tab, const int* scratch, int g_lo, int g_hi, int tid) {
     const int* ids = scratch;
-    const int* cnt = scratch + kMaxMoeSlots;
-    const int* ngr = scratch + 2 * kMaxMoeSlots;
+    const int* rank = scratch + kMaxMoeSlots;
+    const int* cnt = scratch + 2 * kMaxMoeSlots;
+    const int* lead = scratch + 3 * kMaxMoeSlots;
+    const int* ngr = scratch + 4 * kMaxMoeSlots;
     if (g_hi - g_lo + 1 > kMoeWindow) {  // the planner bounds the span: flag it, keep in bounds
         if (tid == 0) raise_status(NVFP4_DEV_INTERNAL, p.status_user);
         g_hi = g_lo + kMoeWindow - 1;
     }
     if (tid == 0) tab->g0 = g_lo;
-    for (int t = tid; t < p.slots; t += tk::kThreads) {
-        const int c = cnt[t];
-        if (c == 0) continue;  // not a leader
-        const int gf = ngr[t], gl = gf + (c + 7) / 8 - 1;
-        if (gl < g_lo || gf > g_hi) continue;
-        const int id = ids[t];
-        int i = 0;  // member number within the expert
-        for (int u = t; u < p.slots && i < c; ++u) {
-            if (ids[u] != id) continue;
-            const int g = gf + (i >> 3), j = i & 7;
-            if (g >= g_lo && g <= g_hi) {
-                const int lg = g - g_lo;
-                tab->slot[lg][j] = u;
-                tab->xrow[lg][j] = p.x_per_slot ? u : u / p.top_k;
-                if (j == 0) {
-                    tab->expert[lg] = id;
-                    tab->count[lg] = min(8, c - i);
-                }
-            }
-            ++i;
+    for (int u = tid; u < p.slots; u += tk::kThreads) {
+        if (ids[u] < 0) continue;  // invalid id: no group
+        const int r = rank[u];
+        const int g = ngr[lead[u]] + (r >> 3), j = r & 7;
+        if (g < g_lo || g > g_hi) continue;
+        const int lg = g - g_lo;
+        tab->slot[lg][j] = u;
+        tab->xrow[lg][j] = p.x_per_slot ? u : u / p.top_k;
+        if (j == 0) {
+            tab->expert[lg] = ids[u];
+            tab->count[lg] = min(8, cnt[u] - r);
         }
     }
     __syncthreads();
@@ -1970,7 +1990,7 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_kernel(const __grid
     const uint32_t ring_w = base + p.ring_w + static_cast<uint32_t>(warp * stages) * kWBox;
     const uint32_t ring_s = base + p.ring_s + static_cast<uint32_t>(warp * stages) * kSBox;
     TileMoe* const tab = reinterpret_cast<TileMoe*>(sbase + p.moe_off);
-    if (NVFP4_PARAM_WARM) warm_params(p, p.x);
+    trace_begin(tid);
     if (tid == 0) trace_phase(p.trace_slot, 0);
     if (NVFP4_PREFETCH_TMAP && warp == 0 && lane < 4) prefetch_tmap(lane < 2 ? &p.wmap[lane] : &p.smap[lane - 2]);
 
@@ -2359,6 +2379,7 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_kernel(const __grid
     }
     __syncwarp();
     if (tid == 0) trace_phase(p.trace_slot, 7);
+    trace_flush(p.trace_slot, tid);
 }
 
 #ifndef NVFP4_MOE_EARLY
@@ -2392,7 +2413,7 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_sk_kernel(const __g
     const uint32_t ring_w = base + p.ring_w + static_cast<uint32_t>(warp * stages) * kWBox;
     const uint32_t ring_s = base + p.ring_s + static_cast<uint32_t>(warp * stages) * kSBox;
     TileMoe* const tab = reinterpret_cast<TileMoe*>(sbase + p.moe_off);
-    if (NVFP4_PARAM_WARM) warm_params(p, p.x);
+    trace_begin(tid);
     if (tid == 0) trace_phase(p.trace_slot, 0);
     if (NVFP4_PREFETCH_TMAP && warp == 0 && lane < 4) prefetch_tmap(lane < 2 ? &p.wmap[lane] : &p.smap[lane - 2]);
     // partial records of warp w: the first 1 KB of its own ring, free once its boxes are consumed
@@ -2568,8 +2589,8 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_sk_kernel(const __g
             staged = stage_x_bulk(p.x, rowsel, M, p.K, 0, p.K, xs, p.sstride, gmax + 16,
                                   reinterpret_cast<uint64_t*>(gmax + 24), warp, tk::kWarps, 2, lane, p.wait_ns);
         else
-            staged = stage_x_direct(p.x, rowsel, M, p.K, 0, p.K, xs, p.sstride, gmax + 16, warp, tk::kWarps, 2,
-                                    lane, [] {});
+            staged = stage_x_direct<NVFP4_SK_STAGE_PRE>(p.x, rowsel, M, p.K, 0, p.K, xs, p.sstride, gmax + 16,
+                                                         warp, tk::kWarps, 2, lane, [] {});
     }
     if (!staged) {
         lossy = stage_x_slice(p.x, rowsel, M, p.K, 0, p.K, xs, p.sstride, e2, gmax, warp, tk::kWarps, 2, lane);
@@ -2780,6 +2801,7 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_sk_kernel(const __g
     }
     __syncwarp();
     if (tid == 0) trace_phase(p.trace_slot, 7);
+    trace_flush(p.trace_slot, tid);
 }
 
 // ------------------------------------------------------------------ byte-load kernel
@@ -3131,7 +3153,12 @@ cudaError_t allow_max_smem(Kern kern, bool (&done)[64]) {
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lk(g_mu);
     if (!done[dev]) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, g_dev[dev].smem_optin);
+        // the opt-in limit covers static and dynamic shared memory together
+        cudaFuncAttributes fa{};
+        e = cudaFuncGetAttributes(&fa, kern);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 g_dev[dev].smem_optin - static_cast<int>(fa.sharedSizeBytes));
         if (e != cudaSuccess) return e;
         done[dev] = true;
     }
@@ -3203,6 +3230,9 @@ cudaError_t dispatch_stream(const Plan& pl, cudaStream_t st) {
 #ifndef NVFP4_TILE_S
 #define NVFP4_TILE_S 0
 #endif
+#ifndef NVFP4_DENSE_SK
+#define NVFP4_DENSE_SK 0  // 1: dense and gate/up launches take the stream-K form (measurement switch)
+#endif
 #ifndef NVFP4_TILE_PER_SM
 #define NVFP4_TILE_PER_SM 0  // nonzero: dense launches use at most this many CTAs per SM
 #endif
@@ -3272,7 +3302,7 @@ bool plan_tile(TilePlan& tp, int M, int N, int K, int groups, const DeviceInfo& 
     const int item_groups = swiglu ? 1 : groups;
     bool found = false;
     double best = 0.0;
-    for (int nc = 2; nc >= 1; --nc) {
+    for (int nc = 2; nc >= 1 && !(NVFP4_DENSE_SK && !moe && !swiglu); --nc) {
         if (segs % nc) continue;
         const int nbox = segs / nc;
         for (int sl = 0; (1 << sl) <= 8; ++sl) {
@@ -3389,7 +3419,7 @@ bool plan_tile(TilePlan& tp, int M, int N, int K, int groups, const DeviceInfo& 
     }
     // Stream-K form (MoE): whole K per CTA, jobs (group, tile) split evenly over the CTAs and
     // boxes evenly over the warps. Many jobs per CTA make it balance far better than items.
-    if (moe && NVFP4_TILE_KSPLIT == 0 && NVFP4_TILE_S == 0) {
+    if ((moe || (NVFP4_DENSE_SK && !swiglu)) && NVFP4_TILE_KSPLIT == 0 && NVFP4_TILE_S == 0) {
         for (int nc = 2; nc >= 1; --nc) {
             if (segs % nc || (NVFP4_TILE_NC && nc != NVFP4_TILE_NC)) continue;
             const int nbox = segs / nc;
@@ -3405,7 +3435,7 @@ bool plan_tile(TilePlan& tp, int M, int N, int K, int groups, const DeviceInfo& 
             // group at least, whatever the routing
             const int groups_most = std::max(moe_groups_max, groups);
             // groups one CTA's job range can touch: more than 32 slots keep them in a window of
-            // kMoeWindow table entries, and build the groups in the x region (3 KB of scratch).
+            // kMoeWindow table entries, and build the groups in the x region (5 KB of scratch).
             // Their staging buffer holds 8 x rows, a window's rows for the usual routings (an
             // expert has a few slots); a CTA whose window needs more computes in exact fp32
             // with x read from global memory instead.
@@ -3414,7 +3444,7 @@ bool plan_tile(TilePlan& tp, int M, int N, int K, int groups, const DeviceInfo& 
             if (big && span > kMoeWindow) continue;
             const int rows_cap = static_cast<int>(std::min<long long>(xrows, big ? 8 : 8 * span));
             uint32_t x_bytes = align_up(static_cast<uint32_t>(rows_cap) * sstride, 128);
-            if (big) x_bytes = std::max<uint32_t>(x_bytes, 3u * kMaxMoeSlots * 4u);
+            if (big) x_bytes = std::max<uint32_t>(x_bytes, kMoeScratchInts * 4u);
             int stages = 0, per_sm = 0;
             uint32_t smem = 0;
             TileParams lp{};
@@ -3587,6 +3617,9 @@ cudaError_t launch_tile(const TilePlan& tp_in, cudaStream_t st, bool moe, bool s
                           : launch_tile_nc<1, false, false, false, true>(tp, st);
     }
     if (moe && tp.sk) return tp.nc == 2 ? launch_tile_nc<2, true, true>(tp, st) : launch_tile_nc<1, true, true>(tp, st);
+#if NVFP4_DENSE_SK
+    if (tp.sk) return tp.nc == 2 ? launch_tile_nc<2, false, true>(tp, st) : launch_tile_nc<1, false, true>(tp, st);
+#endif
     if (moe) return tp.nc == 2 ? launch_tile_nc<2, true, false>(tp, st) : launch_tile_nc<1, true, false>(tp, st);
     if (tp.p.swiglu)
         return tp.nc == 2 ? launch_tile_nc<2, false, false, true>(tp, st) : launch_tile_nc<1, false, false, true>(tp, st);

@@ -506,7 +506,7 @@ int main() {
                 }
                 ++n_big;
                 CHECK(tp.sk, "more than 32 slots take the stream-K form");
-                CHECK(tp.p.misc_off - tp.p.x_off >= 3u * kMaxMoeSlots * 4u, "group-building scratch in the x region");
+                CHECK(tp.p.misc_off - tp.p.x_off >= kMoeScratchInts * 4u, "group-building scratch in the x region");
                 CHECK(tp.p.M <= 8 && tp.p.M >= 1, "x rows staged");
                 for (int ng = 1; ng <= slots; ng += (ng < 16 ? 1 : 7)) {
                     check_sk(tp, ng * tp.p.tiles, ng);
