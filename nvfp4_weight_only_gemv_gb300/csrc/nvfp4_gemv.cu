@@ -1327,11 +1327,31 @@ struct TileMoe {
     int rows[kTileMoeSlots];                  // global x row of each staged row
 };
 
+#ifndef NVFP4_EVICT_FIRST
+#define NVFP4_EVICT_FIRST 1  // 1: weight copies carry an L2 evict-first policy (read once; vocab 0.93 -> 0.98 of the copy peak)
+#endif
+
+// An L2 policy that evicts the lines it tags first: weights are streamed once, so they should not
+// push x, the expert ids or the outputs out of L2.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2,
                                             uint32_t bar) {
+#if NVFP4_EVICT_FIRST
+    const uint64_t pol = l2_evict_first_policy();
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1, {%2, %3, %4}], [%5], %6;"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar), "l"(pol) : "memory");
+#else
     asm volatile(
         "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
         ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar) : "memory");
+#endif
 }
 
 #ifndef NVFP4_PREFETCH_TMAP
@@ -3230,9 +3250,6 @@ cudaError_t dispatch_stream(const Plan& pl, cudaStream_t st) {
 #ifndef NVFP4_TILE_S
 #define NVFP4_TILE_S 0
 #endif
-#ifndef NVFP4_DENSE_SK
-#define NVFP4_DENSE_SK 0  // 1: dense and gate/up launches take the stream-K form (measurement switch)
-#endif
 #ifndef NVFP4_TILE_PER_SM
 #define NVFP4_TILE_PER_SM 0  // nonzero: dense launches use at most this many CTAs per SM
 #endif
@@ -3302,7 +3319,7 @@ bool plan_tile(TilePlan& tp, int M, int N, int K, int groups, const DeviceInfo& 
     const int item_groups = swiglu ? 1 : groups;
     bool found = false;
     double best = 0.0;
-    for (int nc = 2; nc >= 1 && !(NVFP4_DENSE_SK && !moe && !swiglu); --nc) {
+    for (int nc = 2; nc >= 1; --nc) {
         if (segs % nc) continue;
         const int nbox = segs / nc;
         for (int sl = 0; (1 << sl) <= 8; ++sl) {
@@ -3419,7 +3436,7 @@ bool plan_tile(TilePlan& tp, int M, int N, int K, int groups, const DeviceInfo& 
     }
     // Stream-K form (MoE): whole K per CTA, jobs (group, tile) split evenly over the CTAs and
     // boxes evenly over the warps. Many jobs per CTA make it balance far better than items.
-    if ((moe || (NVFP4_DENSE_SK && !swiglu)) && NVFP4_TILE_KSPLIT == 0 && NVFP4_TILE_S == 0) {
+    if (moe && NVFP4_TILE_KSPLIT == 0 && NVFP4_TILE_S == 0) {
         for (int nc = 2; nc >= 1; --nc) {
             if (segs % nc || (NVFP4_TILE_NC && nc != NVFP4_TILE_NC)) continue;
             const int nbox = segs / nc;
@@ -3617,9 +3634,6 @@ cudaError_t launch_tile(const TilePlan& tp_in, cudaStream_t st, bool moe, bool s
                           : launch_tile_nc<1, false, false, false, true>(tp, st);
     }
     if (moe && tp.sk) return tp.nc == 2 ? launch_tile_nc<2, true, true>(tp, st) : launch_tile_nc<1, true, true>(tp, st);
-#if NVFP4_DENSE_SK
-    if (tp.sk) return tp.nc == 2 ? launch_tile_nc<2, false, true>(tp, st) : launch_tile_nc<1, false, true>(tp, st);
-#endif
     if (moe) return tp.nc == 2 ? launch_tile_nc<2, true, false>(tp, st) : launch_tile_nc<1, true, false>(tp, st);
     if (tp.p.swiglu)
         return tp.nc == 2 ? launch_tile_nc<2, false, false, true>(tp, st) : launch_tile_nc<1, false, false, true>(tp, st);
