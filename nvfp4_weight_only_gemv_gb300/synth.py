@@ -193,6 +193,17 @@ def gate_up_problem(N: int, K: int, M: int, seed: int, device="cpu"):
             "N": N, "K": K, "M": M}
 
 
+def ffn_problem(H: int, I: int, M: int, seed: int, device="cpu"):
+    """An FFN block: gate and up weights [I, H], down weight [H, I], each with its own global
+    scale, and x [M, H]."""
+    wg, sg, gg = random_weight(I, H, seed * 4 + 1, device)
+    wu, su, gu = random_weight(I, H, seed * 4 + 2, device)
+    wd, sd, gd = random_weight(H, I, seed * 4 + 3, device)
+    x = random_x(M, H, seed * 4 + 4, device)
+    return {"wg": wg, "sg": sg, "gg": gg, "wu": wu, "su": su, "gu": gu, "wd": wd, "sd": sd, "gd": gd, "x": x,
+            "H": H, "I": I, "M": M}
+
+
 def routing(T: int, top_k: int, E: int, seed: int) -> torch.Tensor:
     """Expert ids [T * top_k] int32, token-major. Each token draws top_k distinct experts
     uniformly without replacement (a seeded permutation, first top_k entries)."""

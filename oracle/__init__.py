@@ -6,8 +6,10 @@ never import it, and it imports nothing from them.
 
 The arithmetic lives in ``nvfp4_oracle.c`` (plain C, fp64). This module only
 compiles that file with the host C compiler and marshals numpy arrays through
-ctypes. Every function returns ``(y, yabs)``. ``y`` is the fp64 result.
+ctypes. The GEMV functions return ``(y, yabs)``. ``y`` is the fp64 result.
 ``yabs`` is ``|g| * sum_k |term|``, the scale that the parity tolerance uses.
+``ffn_swiglu`` returns the same pair for its down projection plus the FFN's
+intermediates.
 """
 from __future__ import annotations
 
@@ -88,6 +90,13 @@ def _declare(lib):
                                                 ctypes.c_int64, ctypes.c_int64, c_i64p, ctypes.c_int64,
                                                 c_dp, c_dp, c_i64p]
     lib.nvfp4_oracle_moe_gemv_sdict.restype = ctypes.c_int
+    lib.nvfp4_oracle_bf16_rne.argtypes = [ctypes.c_double]
+    lib.nvfp4_oracle_bf16_rne.restype = ctypes.c_uint16
+    lib.nvfp4_oracle_ffn_swiglu.argtypes = [c_u8p, c_u8p, ctypes.c_double, c_u8p, c_u8p, ctypes.c_double, c_u8p,
+                                            c_u8p, ctypes.c_double, c_u16p, ctypes.c_double, ctypes.c_int64,
+                                            ctypes.c_int64, ctypes.c_int64, c_i64p, ctypes.c_int64, c_dp, c_dp,
+                                            c_dp, c_u16p, c_dp]
+    lib.nvfp4_oracle_ffn_swiglu.restype = ctypes.c_int
     return lib
 
 
@@ -304,3 +313,47 @@ def moe_gemv_sdict(w, idx, sdict, gs, ids, x_bits, x_per_slot, top_k, rows=None,
     if rc != 0:
         raise ValueError("oracle moe_gemv_sdict: bad arguments")
     return y, ya, int(bad[0])
+
+
+def bf16_rne(v, lib=None) -> np.ndarray:
+    """fp64 values rounded to the nearest bf16, ties to even: uint16 bit patterns, same shape."""
+    lib = lib or load()
+    a = np.asarray(v, dtype=np.float64)
+    out = np.empty(a.shape, dtype=np.uint16)
+    flat, o = a.reshape(-1), out.reshape(-1)
+    for i in range(flat.size):
+        o[i] = lib.nvfp4_oracle_bf16_rne(float(flat[i]))
+    return out
+
+
+def ffn_swiglu(wg, sg, gg, wu, su, gu, wd, sd, gd, x_bits, lim=float("inf"), rows=None, lib=None):
+    """The FFN block: h = bf16(silu(clamp(gate)) * clamp(up)), then y = gd * W_down . h.
+
+    wg, wu [I, H/2], sg, su [I, H/16]; wd [H, I/2], sd [H, I/16]; x_bits [M, H]. Returns y and
+    yabs [M, len(rows)] (yabs: the down GEMV's |gd| * sum |term| on the bf16 h) and a dict with
+    h (fp64, before rounding), h_bits (the bf16 h the down GEMV reads) and gate, gate_abs, up,
+    up_abs, each [M, I]."""
+    lib = lib or load()
+    wg, sg, wu, su, wd, sd, x = _u8(wg), _u8(sg), _u8(wu), _u8(su), _u8(wd), _u8(sd), _u16(x_bits)
+    I, H = wg.shape[0], wg.shape[1] * 2
+    M = x.shape[0]
+    assert wu.shape == wg.shape and sg.shape == su.shape == (I, H // 16) and x.shape == (M, H)
+    assert wd.shape == (H, I // 2) and sd.shape == (H, I // 16)
+    r, rp = _rows(rows)
+    nr = H if r is None else r.shape[0]
+    y = np.empty((M, nr), dtype=np.float64)
+    ya = np.empty((M, nr), dtype=np.float64)
+    h = np.empty((M, I), dtype=np.float64)
+    hb = np.empty((M, I), dtype=np.uint16)
+    aux = np.empty((4, M, I), dtype=np.float64)
+    rc = lib.nvfp4_oracle_ffn_swiglu(_ptr(wg, ctypes.c_uint8), _ptr(sg, ctypes.c_uint8), float(gg),
+                                     _ptr(wu, ctypes.c_uint8), _ptr(su, ctypes.c_uint8), float(gu),
+                                     _ptr(wd, ctypes.c_uint8), _ptr(sd, ctypes.c_uint8), float(gd),
+                                     _ptr(x, ctypes.c_uint16), float(lim), M, H, I, rp, nr,
+                                     _ptr(y, ctypes.c_double), _ptr(ya, ctypes.c_double),
+                                     _ptr(h, ctypes.c_double), _ptr(hb, ctypes.c_uint16),
+                                     _ptr(aux, ctypes.c_double))
+    if rc != 0:
+        raise ValueError("oracle ffn_swiglu: bad arguments")
+    out = {"h": h, "h_bits": hb, "gate": aux[0], "gate_abs": aux[1], "up": aux[2], "up_abs": aux[3]}
+    return y, ya, out

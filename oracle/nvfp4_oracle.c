@@ -27,6 +27,10 @@
  *   - MoE: slot s = t * top_k + j uses expert ids[s] and its own g; x row t
  *     (shared per token) or row s (one row per slot).
  *
+ * The FFN block (nvfp4_oracle_ffn_swiglu) composes these: gate/up GEMVs, the clamped SiLU
+ * product in fp64, bf16 rounding of that product (nearest, ties to even), then the down GEMV
+ * on the rounded values.
+ *
  * Decoders follow the bit definitions of the two minifloat formats (OCP
  * Microscaling Formats v1.0): E2M1 has 1 sign, 2 exponent (bias 1) and
  * 1 mantissa bit; E4M3 has 1 sign, 4 exponent (bias 7) and 3 mantissa bits,
@@ -394,4 +398,71 @@ int nvfp4_oracle_moe_gemv_sdict(const uint8_t *w, const uint8_t *idx, const uint
         if (sr != srow) free(sr);
     }
     return 0;
+}
+
+/*
+ * bf16 nearest-even rounding of an fp64 value, returned as the bf16 bit pattern. bf16 has 8
+ * significant bits and binary32's exponent range: the quantum is 2^(e - 7) for
+ * 2^e <= |v| < 2^(e + 1), e >= -126, and 2^-133 below 2^-126. A value that rounds to 2^128 or
+ * more is infinite; NaN maps to the quiet NaN 0x7FC0. This is the rounding of the silu_mul
+ * node's bf16 output in "glm-5.3-flash-nvfp4-tp3-512k--gb10 graph.json" (l3.moe.shared_act).
+ */
+uint16_t nvfp4_oracle_bf16_rne(double v) {
+    if (isnan(v)) return 0x7FC0;
+    uint16_t sign = signbit(v) ? 0x8000 : 0;
+    double a = fabs(v);
+    if (isinf(a)) return sign | 0x7F80;
+    if (a == 0.0) return sign;
+    int e;
+    frexp(a, &e);  /* a = f * 2^e with 0.5 <= f < 1, so 2^(e - 1) <= a < 2^e */
+    int ex = e - 1;
+    double q = ex >= -126 ? ldexp(1.0, ex - 7) : ldexp(1.0, -133);
+    double m = rint(a / q);  /* nearest, ties to even (the default rounding mode) */
+    double r = m * q;
+    if (r >= ldexp(1.0, 128)) return sign | 0x7F80;
+    float f = (float)r;      /* exact: r has at most 8 significant bits */
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    return sign | (uint16_t)(u >> 16);
+}
+
+/*
+ * The shared-expert FFN of "glm-5.3-flash-nvfp4-tp3-512k--gb10 graph.json" (block l3.moe,
+ * nodes shared_gate_up, shared_clamp, shared_act and shared_down, which the plan runs as one
+ * group), in the nodes' order:
+ *   1. gate and up GEMVs over x [M, H] (weights [I, H/2], scales [I, H/16]);
+ *   2. h = silu(clamp(gate)) * clamp(up) (nvfp4_oracle_swiglu), in fp64;
+ *   3. h rounded to bf16 (the silu_mul node's output precision);
+ *   4. the down GEMV y = gd * W_down . h (weights [H, I/2], scales [H, I/16]).
+ * rows: output columns of y to compute (NULL = all H). h_out (fp64, before rounding) and
+ * hbits_out (the bf16 h of step 3) are [M, I] and may be NULL; gate, up and their
+ * |g| * sum |term| scales go to aux [4][M, I] when aux is not NULL (order: gate, gate_abs,
+ * up, up_abs). y and yabs are [M, nrows]; yabs is the down GEMV's |gd| * sum |term| on h.
+ */
+int nvfp4_oracle_ffn_swiglu(const uint8_t *wg, const uint8_t *sg, double gg,
+                            const uint8_t *wu, const uint8_t *su, double gu,
+                            const uint8_t *wd, const uint8_t *sd, double gd,
+                            const uint16_t *x, double lim, int64_t M, int64_t H, int64_t I,
+                            const int64_t *rows, int64_t nrows, double *y, double *yabs,
+                            double *h_out, uint16_t *hbits_out, double *aux) {
+    if (H % 16 != 0 || I % 16 != 0 || M < 0 || H < 0 || I < 0 || !(lim > 0.0)) return -1;
+    double *h = (double *)malloc(sizeof(double) * (size_t)(M * I > 0 ? M * I : 1));
+    uint16_t *hb = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)(M * I > 0 ? M * I : 1));
+    if (!h || !hb) {
+        free(h);
+        free(hb);
+        return -2;
+    }
+    int rc = nvfp4_oracle_gate_up_swiglu(wg, sg, gg, wu, su, gu, x, lim, M, I, H, NULL, I, h,
+                                         aux ? aux : NULL, aux ? aux + M * I : NULL,
+                                         aux ? aux + 2 * M * I : NULL, aux ? aux + 3 * M * I : NULL);
+    if (rc == 0) {
+        for (int64_t j = 0; j < M * I; ++j) hb[j] = nvfp4_oracle_bf16_rne(h[j]);
+        rc = nvfp4_oracle_gemv(wd, sd, gd, hb, M, H, I, rows, nrows, y, yabs);
+        if (h_out) memcpy(h_out, h, sizeof(double) * (size_t)(M * I));
+        if (hbits_out) memcpy(hbits_out, hb, sizeof(uint16_t) * (size_t)(M * I));
+    }
+    free(h);
+    free(hb);
+    return rc;
 }

@@ -12,12 +12,14 @@ import subprocess
 
 import numpy as np
 import pytest
+import torch
 
 import oracle
 from nvfp4_weight_only_gemv_gb300 import synth
 
 from test_oracle_pins import E2M1_TABLE, _arrays, _golden, dequant, torch_bf16, torch_e4m3
 from test_oracle_sdict import _golden as _sdict_golden, pack_indices, random_case
+from test_oracle_ffn import hand_worked_ffn
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "nvfp4_oracle.c")
 
@@ -57,6 +59,16 @@ MUTANTS = {
                         "sdict_scale_row(idx, dict + 32 * e, K, n, sr);", 1),
     "sdict_moe_table": ("sdict_scale_row(idx + e * plane, dict + 32 * e, K, n, sr);",
                         "sdict_scale_row(idx + e * plane, dict, K, n, sr);", 1),
+    "bf16_ties_away": ("double m = rint(a / q);", "double m = round(a / q);", 1),
+    "bf16_truncates": ("double m = rint(a / q);", "double m = floor(a / q);", 1),
+    "bf16_mantissa_bits": ("ldexp(1.0, ex - 7)", "ldexp(1.0, ex - 8)", 1),
+    "bf16_subnormal_step": ("ldexp(1.0, -133)", "ldexp(1.0, -134)", 1),
+    "bf16_sign_dropped": ("return sign | (uint16_t)(u >> 16);", "return (uint16_t)(u >> 16);", 1),
+    "ffn_h_truncated": ("hb[j] = nvfp4_oracle_bf16_rne(h[j]);",
+                        "{ float f = (float)h[j]; uint32_t u; memcpy(&u, &f, 4); hb[j] = (uint16_t)(u >> 16); }", 1),
+    "ffn_down_scale": ("rc = nvfp4_oracle_gemv(wd, sd, gd, hb,", "rc = nvfp4_oracle_gemv(wd, sd, gg, hb,", 1),
+    "ffn_gate_up_swapped": ("nvfp4_oracle_gate_up_swiglu(wg, sg, gg, wu, su, gu, x, lim, M, I, H,",
+                            "nvfp4_oracle_gate_up_swiglu(wu, su, gu, wg, sg, gg, x, lim, M, I, H,", 1),
 }
 
 
@@ -149,6 +161,24 @@ def battery(lib):
     yp, _, _ = oracle.moe_gemv(wm, sm, gs, ids, xm, False, 2, lib=lib)
     if not np.array_equal(y, yp):
         fails.append("sdict_moe_equals_plain")
+    # bf16 rounding of the FFN's h: round trips, ties to even, PyTorch's float32 conversion, and
+    # the FFN's closed form (see test_oracle_ffn.py)
+    bits = np.arange(0, 0x7F80, 61, dtype=np.uint16)
+    vals = np.array([oracle.bf16(int(b), lib) for b in bits])
+    if not np.array_equal(oracle.bf16_rne(-vals, lib), bits | 0x8000):
+        fails.append("bf16_round_trip")
+    lo = np.arange(0, 0x7F7F, 37, dtype=np.int64)
+    mid = (np.array([oracle.bf16(int(b), lib) for b in lo]) + np.array([oracle.bf16(int(b) + 1, lib) for b in lo])) / 2
+    if not np.array_equal(oracle.bf16_rne(mid, lib).astype(np.int64), np.where(lo % 2 == 0, lo, lo + 1)):
+        fails.append("bf16_ties_to_even")
+    v = np.random.default_rng(64).standard_normal(4000).astype(np.float32) * np.float32(3.0)
+    v = np.concatenate([v, np.float32(2.0 ** -140) * v[:500]])
+    if not np.array_equal(oracle.bf16_rne(v.astype(np.float64), lib),
+                          torch.from_numpy(v).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)):
+        fails.append("bf16_vs_pytorch")
+    y, y_exp, hb, hb_exp, _, _ = hand_worked_ffn(lib)
+    if not (np.array_equal(y, y_exp) and np.array_equal(hb, hb_exp)):
+        fails.append("ffn_hand_worked")
     return fails
 
 
