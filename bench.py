@@ -61,6 +61,15 @@ WORKLOADS = {
     "ffn_swiglu": ("FFN gate+up N=2x12288,K=4096 with the fused SwiGLU (clamp 10, bf16 [1, 12288] out) "
                    "then down N=4096,K=12288 at M=1, fp32 out",
                    [("gate_up_swiglu", 12288, 4096, 1, 5, "bf16"), ("dense", 4096, 12288, 1, 6, "f32")]),
+    "ffn_fused": ("FFN block in one call: gate+up 2x12288x4096 with the SwiGLU (clamp 10) into a bf16 h, "
+                  "then down 4096x12288, M=1, fp32 out",
+                  [("ffn_block", 4096, 12288, 1, 5, "f32")]),
+    "ffn_fused_m2": ("FFN block in one call at M=2, fp32 out", [("ffn_block", 4096, 12288, 2, 5, "f32")]),
+    "ffn_shared": ("shared-expert FFN in two calls: gate+up N=2x768,K=4096 with the fused SwiGLU (clamp 10, bf16 "
+                   "[2, 768] out), then down N=4096,K=768, M=2, bf16 out",
+                   [("gate_up_swiglu", 768, 4096, 2, 9, "bf16"), ("dense", 4096, 768, 2, 10, "bf16")]),
+    "ffn_shared_fused": ("shared-expert FFN in one call (gate+up 2x768x4096, SwiGLU, bf16 h, down 4096x768), "
+                         "M=2, bf16 out", [("ffn_block", 4096, 768, 2, 9, "bf16")]),
     "vocab": ("vocab head N=151936,K=4096,M=1, fp32 out", [("dense", 151936, 4096, 1, 7, "f32")]),
     "moe": ("routed experts: 288 experts, gate_up [3072,4096] then down [4096,1536], "
             "4 tokens x top-8, fp32 per-slot out",
@@ -136,12 +145,16 @@ def kernels_of(calls):
              "tile_sk_moe": "gemv_tile_sk_kernel (MoE)", "tile_swiglu": "gemv_tile_kernel (gate/up + SwiGLU)",
              "stream_moe": "gemv_stream_kernel (MoE)", "simple": "gemv_simple_kernel",
              "tile_sdict": "gemv_tile_kernel (dictionary scales)",
-             "tile_sk_moe_sdict": "gemv_tile_sk_kernel (MoE, dictionary scales)"}
+             "tile_sk_moe_sdict": "gemv_tile_sk_kernel (MoE, dictionary scales)",
+             "ffn_fused": "gemv_ffn_kernel (gate/up + SwiGLU, grid barrier, down)",
+             "ffn_two_launch": "gemv_tile_kernel (gate/up + SwiGLU, then down)"}
     seen = []
     for c in calls:
         if c.kind.startswith("moe"):
             kind = ("moe_per_slot" if c.x_per_slot else "moe") + ("_sdict" if c.sd else "")
             desc = nv.describe_plan(kind, c.E, c.N, c.K, c.T, c.top_k)
+        elif c.kind == "ffn_block":
+            desc = nv.describe_plan("ffn", c.M, c.N, c.K)
         else:
             kind = c.kind if c.kind in ("gate_up", "gate_up_swiglu", "dense_sdict") else "dense"
             desc = nv.describe_plan(kind, c.M, c.N, c.K)
@@ -264,6 +277,12 @@ class Call:
             base = p
             self.rows = 2 * self.N
             self.y_shape = (self.M, self.N if self.kind == "gate_up_swiglu" else 2 * self.N)
+        elif self.kind == "ffn_block":
+            # N = H (x and y width), K = I (the intermediate width)
+            p = synth.ffn_problem(self.N, self.K, self.M, self.seed, device=gen_device)
+            base = {k: v for k, v in p.items() if k not in ("H", "I", "M")}
+            self.rows = self.N
+            self.y_shape = (self.M, self.N)
         else:
             self.T, self.top_k, self.E = self.M, 8, 288
             self.x_per_slot = self.kind.endswith("_down")
@@ -289,6 +308,9 @@ class Call:
             if self.kind.startswith("moe") and c > 0:
                 d["ids"] = synth.routing(self.T, self.top_k, self.E, self.seed * 7919 + c).to(device)
             d["y"] = torch.empty(self.y_shape, dtype=self.out_dtype, device=device)
+            if self.kind == "ffn_block":
+                import nvfp4_weight_only_gemv_gb300 as nv
+                d["ws"] = nv.ffn_workspace(self.M, self.K, device)
             self.sets.append(d)
 
     # bytes -------------------------------------------------------------
@@ -304,6 +326,8 @@ class Call:
         per_row = self.K * 0.5 + (self.K * 5 / 128 if self.sd else self.K / 16)
         if self.kind in ("gate_up", "gate_up_swiglu"):
             return 2 * self.N * per_row
+        if self.kind == "ffn_block":
+            return 3 * self.N * per_row  # gate and up [I, H], down [H, I]: 3 * H * I weights
         if self.kind.startswith("moe"):
             return self.unique_experts(c) * (self.N * per_row + (32 if self.sd else 0))
         return self.N * per_row + (32 if self.sd else 0)
@@ -314,6 +338,8 @@ class Call:
             slots = self.T * self.top_k
             xrows = slots if self.x_per_slot else self.T
             return self.weight_bytes(c) + xrows * self.K * 2 + slots * self.N * self.out_bytes
+        if self.kind == "ffn_block":  # x [M, H] in, y [M, H] out; h stays inside the call
+            return self.weight_bytes(c) + self.M * self.N * (2 + self.out_bytes)
         return self.weight_bytes(c) + self.M * self.K * 2 + self.M * self.y_shape[1] * self.out_bytes
 
     def x_bytes(self):
@@ -338,6 +364,9 @@ class Call:
             nv.gemv_gate_up(d["wg"], d["sg"], d["gg"], d["wu"], d["su"], d["gu"], x, out=y)
         elif self.kind == "gate_up_swiglu":
             nv.gemv_gate_up_swiglu(d["wg"], d["sg"], d["gg"], d["wu"], d["su"], d["gu"], x, SWIGLU_CLAMP, out=y)
+        elif self.kind == "ffn_block":
+            nv.ffn_swiglu(d["wg"], d["sg"], d["gg"], d["wu"], d["su"], d["gu"], d["wd"], d["sd"], d["gd"], x,
+                          SWIGLU_CLAMP, workspace=d["ws"], out=y)
         else:
             nv.moe_gemv(d["w"], d["s"], d["gs"], d["ids"], x, self.x_per_slot, self.top_k, out=y)
         return y
@@ -367,6 +396,10 @@ class Call:
             oracle.gate_up_swiglu(h["wg"].numpy(), h["sg"].numpy(), h["gg"], h["wu"].numpy(), h["su"].numpy(),
                                   h["gu"], synth.bf16_bits(h["x"]), SWIGLU_CLAMP, rows=rows)
             return 2 * len(rows) * (self.K * 0.5 + self.K / 16)  # a gate and an up row per output
+        if self.kind == "ffn_block":
+            oracle.ffn_swiglu(*ffn_host_args(h), synth.bf16_bits(h["x"]), SWIGLU_CLAMP, rows=rows)
+            # every gate and up row (h is needed whole), and the sampled down rows
+            return (2 * self.K + len(rows)) * (self.N * 0.5 + self.N / 16)
         ids = self.sets[0]["ids"].cpu().numpy()
         if self.sd:
             oracle.moe_gemv_sdict(h["w"].numpy(), h["s"].numpy(), h["sd"].numpy(), h["gs"].numpy(), ids,
@@ -383,7 +416,7 @@ def pool_copies(calls_spec, device):
     l2 = getattr(props, "L2_cache_size", 128 << 20) or (128 << 20)
     per_step = 0
     for kind, N, K, M, *_ in calls_spec:
-        rows = 2 * N if kind in ("gate_up", "gate_up_swiglu") else N
+        rows = {"gate_up": 2 * N, "gate_up_swiglu": 2 * N, "ffn_block": 3 * N}.get(kind, N)
         if kind.startswith("moe"):
             return 4, l2, ("routing rotates over 4 id sets; the distinct experts a step reads (counted in "
                            "the algorithmic bytes) exceed 2x L2")
@@ -539,6 +572,40 @@ def cpu_baseline(calls, target_s=6.0, single_thread=True):
 
 # ------------------------------------------------------------------ in-run parity
 
+def ffn_host_args(h):
+    return [h[k].numpy() if isinstance(h[k], torch.Tensor) else h[k] for k in
+            ("wg", "sg", "gg", "wu", "su", "gu", "wd", "sd", "gd")]
+
+
+def _swiglu_bound(aux, y_ref, lim):
+    """The fused activation's bound: the GEMV bound of gate and up carried through the clamp and
+    silu (|silu'| <= 1.1, |silu(v)| <= max(|v|, 0.28)), plus the fp32 evaluation."""
+    tg, tu = 1e-5 * aux["gate_abs"] + 1e-6, 1e-5 * aux["up_abs"] + 1e-6
+    cg = np.clip(aux["gate"], -lim, lim)
+    cu = np.clip(aux["up"], -lim, lim)
+    return (1.1 * np.abs(cu) * tg + np.maximum(np.abs(cg), 0.28) * tu + 1.1 * tg * tu
+            + 1e-6 * np.abs(np.nan_to_num(y_ref)) + 1e-6)
+
+
+def _ffn_flip_bound(h, aux, rows, lim):
+    """The FFN's extra term: where a bf16 rounding boundary lies within the activation's bound of
+    the oracle's h, the GPU's bf16 h may differ by that bound plus two bf16 steps; the down
+    GEMV's A-scale on those differences (oracle only) bounds what they move y."""
+    import oracle
+    hh, hb = aux["h"], aux["h_bits"]
+    e = _swiglu_bound(aux, hh, lim)
+    mb = (hb & 0x7FFF).astype(np.int64)
+    val = lambda b: (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    hv = val(mb.astype(np.uint16))
+    lo = np.where(mb > 0, val(np.maximum(mb - 1, 0).astype(np.uint16)), -2.0 ** -133)
+    hi = val(np.minimum(mb + 1, 0x7F80).astype(np.uint16))
+    a = np.abs(hh)
+    near = ((a - (lo + hv) / 2 <= e) | ((hv + hi) / 2 - a <= e)) & np.isfinite(hh)
+    d = np.where(near, e + 2 * np.maximum(hv - lo, hi - hv), 0.0)
+    _, bound = oracle.gemv(h["wd"].numpy(), h["sd"].numpy(), h["gd"], oracle.bf16_rne(d * (1 + 2.0 ** -7)), rows=rows)
+    return np.nan_to_num(bound)
+
+
 def _ulp_bf16(v):
     a = np.abs(v)
     e = np.maximum(np.floor(np.log2(np.where(a > 0, a, 1.0))), -126)
@@ -577,11 +644,10 @@ def check_outputs(calls, n_cols=48, seed=5):
             yr, aux = oracle.gate_up_swiglu(h["wg"].numpy(), h["sg"].numpy(), h["gg"], h["wu"].numpy(),
                                             h["su"].numpy(), h["gu"], synth.bf16_bits(h["x"]), SWIGLU_CLAMP,
                                             rows=rows)
-            tg, tu = 1e-5 * aux["gate_abs"] + 1e-6, 1e-5 * aux["up_abs"] + 1e-6
-            cg = np.clip(aux["gate"], -SWIGLU_CLAMP, SWIGLU_CLAMP)
-            cu = np.clip(aux["up"], -SWIGLU_CLAMP, SWIGLU_CLAMP)
-            tol = (1.1 * np.abs(cu) * tg + np.maximum(np.abs(cg), 0.28) * tu + 1.1 * tg * tu
-                   + 1e-6 * np.abs(np.nan_to_num(yr)) + 1e-6)
+            tol = _swiglu_bound(aux, yr, SWIGLU_CLAMP)
+        elif c.kind == "ffn_block":
+            yr, ya, aux = oracle.ffn_swiglu(*ffn_host_args(h), synth.bf16_bits(h["x"]), SWIGLU_CLAMP, rows=rows)
+            tol = 1e-5 * ya + 1e-6 + _ffn_flip_bound(h, aux, rows, SWIGLU_CLAMP)
         else:
             ids = c.sets[0]["ids"].cpu().numpy()
             if c.sd:
@@ -648,8 +714,8 @@ def run_reference(args):
     return 0
 
 
-PER_WORKLOAD = ["attn", "ffn", "ffn_m2", "ffn_m4", "ffn_m8", "ffn_swiglu", "moe", "moe_t32", "moe_sdict",
-                "vocab_sdict"]
+PER_WORKLOAD = ["attn", "ffn", "ffn_m2", "ffn_m4", "ffn_m8", "ffn_swiglu", "ffn_fused", "ffn_shared",
+                "ffn_shared_fused", "moe", "moe_t32", "moe_sdict", "vocab_sdict"]
 
 
 def measure(name, steps, warmup, device, stream, ws, sampler=None):

@@ -55,7 +55,8 @@ typedef enum {
     NVFP4_OK = 0,
     NVFP4_ERR_NULL = 1,        /* a required pointer is NULL */
     NVFP4_ERR_SHAPE = 2,       /* M > 8, negative size, K % 16 != 0, top_k/T/E invalid */
-    NVFP4_ERR_ALIGN = 3,       /* reserved: misalignment is handled by the byte-load kernel */
+    NVFP4_ERR_ALIGN = 3,       /* an FFN workspace not 256-byte aligned (other misalignment runs
+                                  the byte-load kernel) */
     NVFP4_ERR_DTYPE = 4,       /* y_type is not one of nvfp4_out_t */
     NVFP4_ERR_UNSUPPORTED = 5, /* a size beyond what any kernel here can take */
     NVFP4_ERR_CUDA = 6,        /* the CUDA runtime reported an error (see nvfp4_last_cuda_error) */
@@ -112,6 +113,43 @@ nvfp4_status nvfp4_gemv_gate_up_swiglu(const uint8_t* w_gate, const uint8_t* s_g
                                        const uint8_t* w_up, const uint8_t* s_up, float g_up,
                                        const uint16_t* x, float clamp_limit, void* y, nvfp4_out_t y_type,
                                        int M, int N, int K, void* stream);
+
+/*
+ * The FFN block as one call: the shared-expert group of "glm-5.3-flash-nvfp4-tp3-512k--gb10
+ * graph.json" (block l3.moe, nodes shared_gate_up, shared_clamp, shared_act and shared_down, which
+ * the plan runs as one fused group):
+ *     h[m, i] = bf16(silu(c(gate[m, i])) * c(up[m, i]))        (nvfp4_gemv_gate_up_swiglu, bf16)
+ *     y[m, n] = g_down * sum_i W_down[n, i] * h[m, i]          (nvfp4_gemv on h)
+ * with gate = g_gate * W_gate . x and up = g_up * W_up . x in fp32, and h rounded to nearest
+ * even (the silu_mul node's bf16 output).
+ *   w_gate, w_up [I, H/2] and s_gate, s_up [I, H/16]; w_down [H, I/2] and s_down [H, I/16];
+ *   x [M, H] bf16 bits; y [M, H] of y_type. clamp_limit as nvfp4_gemv_gate_up_swiglu.
+ *   workspace: caller-owned device memory of nvfp4_ffn_workspace_bytes(M, I) bytes, 256-byte
+ *   aligned (else NVFP4_ERR_ALIGN). Its first 2048 bytes are counters (finished CTAs, and how
+ *   much of each slice of h is written): they must be zero before the first call that uses the
+ *   workspace, and every call leaves them at zero for the next. h [M, I] bf16 follows at byte
+ *   2048. Calls that share a workspace must be ordered (one stream, or events): two in flight at
+ *   once corrupt each other's h and counters.
+ * Shapes: 0 <= M <= 8, H, I >= 0, H % 16 == 0, I % 16 == 0. M == 0 or H == 0 launch nothing;
+ * I == 0 sets y to zero.
+ * Execution: one launch when H % 512 == 0, I % 512 == 0, the weights and x are 16-byte aligned
+ * and a plan with two CTAs per SM fits in shared memory (at H = 4096, I = 12288: M = 1): gate/up
+ * and the activation, then down, whose warps each wait only until the slice of h they read is
+ * complete (the gate/up items that write it count themselves in the workspace) and whose first
+ * weight copies are in flight before that. That launch needs all its CTAs resident at once; if
+ * other work on the GPU keeps some of them from starting within the wait budget, the call sets
+ * NVFP4_DEV_TIMEOUT and y is unspecified. Otherwise two launches (gate/up + activation into the
+ * workspace's h, then down), with the same results within tolerance.
+ */
+nvfp4_status nvfp4_ffn_swiglu(const uint8_t* w_gate, const uint8_t* s_gate, float g_gate,
+                              const uint8_t* w_up, const uint8_t* s_up, float g_up,
+                              const uint8_t* w_down, const uint8_t* s_down, float g_down,
+                              const uint16_t* x, float clamp_limit, void* workspace,
+                              void* y, nvfp4_out_t y_type, int M, int H, int I, void* stream);
+
+/* Bytes of workspace nvfp4_ffn_swiglu needs: 2048 + M * I * 2 rounded up to 256; -1 when M is
+ * outside 0..8 or I < 0. */
+int64_t nvfp4_ffn_workspace_bytes(int M, int I);
 
 /*
  * Routed-expert GEMV over slots (w4a16_gemv_sw_moe, "glm-5.3-flash-nvfp4-tp3-512k--gb10
@@ -246,8 +284,8 @@ void nvfp4_set_pdl(int enable);
  * "kernel grid block smem split rows_per_item k_warps ..." into buf (host memory,
  * NUL-terminated). kind: 0 dense, 1 gate_up, 2 MoE with x shared by a token's slots,
  * 3 MoE with one x row per slot, 4 gate_up with the fused activation, 5 dense with dictionary
- * scales, 6 and 7 MoE with dictionary scales (x shared / one x row per slot); for the MoE
- * kinds M is the number of experts E.
+ * scales, 6 and 7 MoE with dictionary scales (x shared / one x row per slot), 8 the FFN block
+ * (nvfp4_ffn_swiglu with N = H, K = I); for the MoE kinds M is the number of experts E.
  * Pointers are assumed 256-byte aligned. Returns the number of characters, or -1.
  */
 int nvfp4_describe_plan(int kind, int M, int N, int K, int T, int top_k, char* buf, int buflen);
@@ -257,7 +295,7 @@ int nvfp4_describe_plan(int kind, int M, int N, int K, int T, int top_k, char* b
  * smem_optin bytes of shared memory a CTA may opt into, smem_per_sm bytes per SM. It runs the
  * planner on the host only (no GPU or driver needed) and assumes the tile kernel's TMA
  * tensor-map encoder is available. Returns the number of characters, or -1 for a bad
- * argument (kind outside 0..7, sizes < 1, smem_per_sm < smem_optin).
+ * argument (kind outside 0..8, sizes < 1, smem_per_sm < smem_optin).
  */
 int nvfp4_describe_plan_host(int sm_count, int smem_optin, int smem_per_sm, int kind, int M, int N, int K,
                              int T, int top_k, char* buf, int buflen);

@@ -21,7 +21,8 @@ import torch
 
 from . import build as _build
 
-__all__ = ["gemv", "gemv_gate_up", "gemv_gate_up_swiglu", "moe_gemv", "gemv_sdict", "moe_gemv_sdict",
+__all__ = ["gemv", "gemv_gate_up", "gemv_gate_up_swiglu", "ffn_swiglu", "ffn_workspace", "ffn_workspace_bytes",
+           "moe_gemv", "gemv_sdict", "moe_gemv_sdict",
            "sdict_plane_bytes", "sdict_encode", "device_status", "set_wait_budget_ns",
            "set_variant", "set_pdl", "fp32_fallbacks", "phase_trace", "describe_plan", "describe_plan_host", "library", "library_path", "NVFP4Error",
            "OUT_F32", "OUT_BF16", "DEV_TIMEOUT", "DEV_BAD_EXPERT", "DEV_INTERNAL"]
@@ -58,6 +59,11 @@ def _declare(lib):
     lib.nvfp4_gemv_gate_up.restype = i32
     lib.nvfp4_gemv_gate_up_swiglu.argtypes = [u8p, u8p, ctypes.c_float, u8p, u8p, ctypes.c_float, u16p,
                                               ctypes.c_float, vp, i32, i32, i32, i32, vp]
+    lib.nvfp4_ffn_swiglu.argtypes = [u8p, u8p, ctypes.c_float, u8p, u8p, ctypes.c_float, u8p, u8p, ctypes.c_float,
+                                     u16p, ctypes.c_float, vp, vp, i32, i32, i32, i32, vp]
+    lib.nvfp4_ffn_swiglu.restype = i32
+    lib.nvfp4_ffn_workspace_bytes.argtypes = [i32, i32]
+    lib.nvfp4_ffn_workspace_bytes.restype = ctypes.c_int64
     lib.nvfp4_gemv_gate_up_swiglu.restype = i32
     lib.nvfp4_moe_gemv.argtypes = [u8p, u8p, vp, i32, vp, i32, i32, u16p, i32, vp, i32, i32, i32,
                                    vp, vp]
@@ -242,6 +248,53 @@ def gemv_gate_up_swiglu(wg, sg, gg, wu, su, gu, x, clamp_limit: float = float("i
     return y
 
 
+def ffn_workspace_bytes(M: int, I: int) -> int:
+    """Bytes of workspace ffn_swiglu needs for M rows and intermediate size I."""
+    n = int(library().nvfp4_ffn_workspace_bytes(int(M), int(I)))
+    if n < 0:
+        raise ValueError(f"no FFN workspace for M={M}, I={I}")
+    return n
+
+
+def ffn_workspace(M: int, I: int, device=None) -> torch.Tensor:
+    """A zeroed workspace for ffn_swiglu (uint8, 256-byte aligned by the caching allocator).
+    Reuse it across calls: every call leaves its counters at zero for the next."""
+    return torch.zeros(ffn_workspace_bytes(M, I), dtype=torch.uint8, device=device or "cuda")
+
+
+def ffn_swiglu(wg, sg, gg, wu, su, gu, wd, sd, gd, x, clamp_limit: float = float("inf"), workspace=None,
+               out=None, out_dtype=torch.float32, stream=None) -> torch.Tensor:
+    """The FFN block: h = bf16(silu(c(gg * W_gate . x)) * c(gu * W_up . x)), y = gd * W_down . h.
+
+    wg, wu uint8 [I, H/2], sg, su [I, H/16]; wd [H, I/2], sd [H, I/16]; x bf16 [M, H]; y [M, H].
+    ``workspace`` (from ffn_workspace) holds the launch's counters and h (bf16 [M, I] at byte
+    2048); None allocates a zeroed one for this call. Calls sharing a workspace must be ordered."""
+    for t, n in ((wg, "w_gate"), (wu, "w_up"), (wd, "w_down")):
+        _need(t, n, torch.uint8, 2)
+    for t, n in ((sg, "s_gate"), (su, "s_up"), (sd, "s_down")):
+        _need(t, n, torch.uint8, 2)
+    _need(x, "x", torch.bfloat16, 2)
+    I, H = wg.shape[0], wg.shape[1] * 2
+    M = x.shape[0]
+    if tuple(wu.shape) != tuple(wg.shape) or tuple(sg.shape) != (I, H // 16) or \
+            tuple(su.shape) != (I, H // 16) or x.shape[1] != H:
+        raise ValueError("shape mismatch between gate, up and x")
+    if tuple(wd.shape) != (H, I // 2) or tuple(sd.shape) != (H, I // 16):
+        raise ValueError("down weight must be [H, I/2] with scales [H, I/16]")
+    if workspace is None:
+        workspace = ffn_workspace(M, I, x.device)
+    _need(workspace, "workspace", torch.uint8, 1)
+    if workspace.numel() < ffn_workspace_bytes(M, I):
+        raise ValueError("workspace too small")
+    y = _out(out, (M, H), out_dtype, x.device)
+    _one_device(wg, sg, wu, su, wd, sd, x, workspace, y)
+    st = library().nvfp4_ffn_swiglu(_ptr(wg), _ptr(sg), float(gg), _ptr(wu), _ptr(su), float(gu), _ptr(wd),
+                                    _ptr(sd), float(gd), _ptr(x), float(clamp_limit), _ptr(workspace), _ptr(y),
+                                    _out_code(y.dtype), M, H, I, ctypes.c_void_p(_stream(stream)))
+    _check(st, "nvfp4_ffn_swiglu")
+    return y
+
+
 def moe_gemv(w, s, gs, ids, x, x_per_slot: bool, top_k: int, out=None, out_dtype=torch.float32,
              status=None, stream=None) -> torch.Tensor:
     """Routed-expert GEMV: y[T*top_k, N]; slot t*top_k+j uses expert ids[t*top_k+j].
@@ -404,16 +457,15 @@ def set_pdl(enable: bool) -> None:
 
 
 KINDS = {"dense": 0, "gate_up": 1, "moe": 2, "moe_per_slot": 3, "gate_up_swiglu": 4, "dense_sdict": 5,
-         "moe_sdict": 6, "moe_per_slot_sdict": 7}
+         "moe_sdict": 6, "moe_per_slot_sdict": 7, "ffn": 8}
 
 
 def describe_plan(kind: str, M: int, N: int, K: int, T: int = 0, top_k: int = 0) -> str:
-    """Launch the library would pick: kind in {"dense", "gate_up", "moe", "moe_per_slot",
-    "gate_up_swiglu"}; for the MoE kinds M is the number of experts (moe_per_slot: one x row
-    per slot)."""
+    """Launch the library would pick: kind is a key of KINDS; for the MoE kinds M is the number
+    of experts (moe_per_slot: one x row per slot); for "ffn" N = H and K = I."""
     code = KINDS[kind]
-    buf = ctypes.create_string_buffer(256)
-    n = library().nvfp4_describe_plan(code, M, N, K, T, top_k, buf, 256)
+    buf = ctypes.create_string_buffer(512)
+    n = library().nvfp4_describe_plan(code, M, N, K, T, top_k, buf, 512)
     if n < 0:
         raise RuntimeError("describe_plan failed (no CUDA device?)")
     return buf.value.decode()
@@ -423,8 +475,8 @@ def describe_plan_host(kind: str, M: int, N: int, K: int, T: int = 0, top_k: int
                        smem_optin: int = 232448, smem_per_sm: int = 233472) -> str:
     """describe_plan for a described device (defaults: GB300), run on the host only: no GPU needed."""
     code = KINDS[kind]
-    buf = ctypes.create_string_buffer(256)
-    n = library().nvfp4_describe_plan_host(sm_count, smem_optin, smem_per_sm, code, M, N, K, T, top_k, buf, 256)
+    buf = ctypes.create_string_buffer(512)
+    n = library().nvfp4_describe_plan_host(sm_count, smem_optin, smem_per_sm, code, M, N, K, T, top_k, buf, 512)
     if n < 0:
         raise ValueError("describe_plan_host: bad arguments")
     return buf.value.decode()

@@ -39,6 +39,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <algorithm>
+#include <type_traits>
 #include <mutex>
 
 #include "nvfp4_gemv.h"
@@ -1375,6 +1376,21 @@ __device__ __forceinline__ uint4 ldg128(const void* p) {
     return v;
 }
 
+// The same load cached in L2 only: for data that other CTAs of the same launch wrote (the FFN's
+// h), so no L1 line from before their writes can answer it.
+__device__ __forceinline__ uint4 ldcg128(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p) : "memory");
+    return v;
+}
+
+template <bool kCG>
+__device__ __forceinline__ uint4 ldx128(const void* p) {
+    if constexpr (kCG) return ldcg128(p);
+    else return ldg128(p);
+}
+
 // Brings [p, p + bytes) into L2 (a hint: no data is returned, so it is safe even while
 // another kernel may still write that memory; L2 stays coherent with those writes).
 __device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
@@ -1417,7 +1433,7 @@ __host__ __device__ __forceinline__ int tile_row_perm(int g) {
 // value converted exactly (uniform over the slice's warps); otherwise the caller re-stages
 // with a power-of-two scale. `vote` is gw words of shared scratch; bar_id < 0: one warp.
 // after_issue() runs once the first loads are out (M > 0 or not).
-template <int kPre = NVFP4_STAGE_PRE, typename F>
+template <int kPre = NVFP4_STAGE_PRE, bool kCG = false, typename F>
 __device__ bool stage_x_direct(const uint16_t* __restrict__ x, const int* rowsel, int M, int K, int k0, int kn,
                                uint8_t* xs, uint32_t sstride, uint32_t* vote, int gi, int gw, int bar_id, int lane,
                                F&& after_issue) {
@@ -1458,7 +1474,7 @@ __device__ bool stage_x_direct(const uint16_t* __restrict__ x, const int* rowsel
         for (int i = 0; i < kPre; ++i) {
             mi[i] = m;
             ci[i] = c;
-            v[i] = m < M ? ldg128(x + static_cast<int64_t>(rowsel ? rowsel[m] : m) * K + k0 + c * 8)
+            v[i] = m < M ? ldx128<kCG>(x + static_cast<int64_t>(rowsel ? rowsel[m] : m) * K + k0 + c * 8)
                          : make_uint4(0u, 0u, 0u, 0u);
             advance();
         }
@@ -1573,6 +1589,7 @@ __device__ bool stage_x_bulk(const uint16_t* __restrict__ x, const int* rowsel, 
 // The slice's rows are walked as one flat sequence of 16-byte chunks, loaded kPre at a time
 // per lane; the first kPre are kept in registers for the conversion. Returns (uniform over
 // the slice's warps) the lossy flag. bar_id < 0: a single warp (no named barrier).
+template <bool kCG = false>
 __device__ bool stage_x_slice(const uint16_t* __restrict__ x, const int* rowsel, int M, int K, int k0, int kn,
                               uint8_t* xs, uint32_t sstride, float* e2, uint32_t* gmax, int gi, int gw, int bar_id,
                               int lane) {
@@ -1606,7 +1623,7 @@ __device__ bool stage_x_slice(const uint16_t* __restrict__ x, const int* rowsel,
         int m = m0, c = c0;
 #pragma unroll
         for (int i = 0; i < kPre; ++i) {
-            v[i] = m < M ? ldg128(x + static_cast<int64_t>(rowsel ? rowsel[m] : m) * K + k0 + c * 8)
+            v[i] = m < M ? ldx128<kCG>(x + static_cast<int64_t>(rowsel ? rowsel[m] : m) * K + k0 + c * 8)
                          : make_uint4(0u, 0u, 0u, 0u);
             advance(m, c);
         }
@@ -1616,7 +1633,7 @@ __device__ bool stage_x_slice(const uint16_t* __restrict__ x, const int* rowsel,
             uint4 u[kPre];
 #pragma unroll
             for (int i = 0; i < kPre; ++i) {
-                u[i] = m < M ? ldg128(x + static_cast<int64_t>(rowsel ? rowsel[m] : m) * K + k0 + c * 8)
+                u[i] = m < M ? ldx128<kCG>(x + static_cast<int64_t>(rowsel ? rowsel[m] : m) * K + k0 + c * 8)
                              : make_uint4(0u, 0u, 0u, 0u);
                 advance(m, c);
             }
@@ -1684,7 +1701,7 @@ __device__ bool stage_x_slice(const uint16_t* __restrict__ x, const int* rowsel,
             for (int i = 0; i < kPre; ++i) {
                 mi[i] = m;
                 ci[i] = c;
-                u[i] = m < M ? ldg128(x + static_cast<int64_t>(rowsel ? rowsel[m] : m) * K + k0 + c * 8)
+                u[i] = m < M ? ldx128<kCG>(x + static_cast<int64_t>(rowsel ? rowsel[m] : m) * K + k0 + c * 8)
                              : make_uint4(0u, 0u, 0u, 0u);
                 advance(m, c);
             }
@@ -1774,7 +1791,7 @@ __device__ __forceinline__ void tile_slot_mma(uint32_t wst, uint32_t sst, uint32
 // The same slot in exact fp32 on the CUDA cores, x read from global memory (bf16): column m
 // uses x row xrow[m] (row m when xrow is null). acc[r][m] collects rows ra (r = 0) and
 // rb (r = 1) for column m, over this lane's 32-code pieces.
-template <int NC, bool SD = false>
+template <int NC, bool SD = false, bool kCG = false>
 __device__ __noinline__ void tile_slot_f32(uint32_t wst, uint32_t sst, const uint16_t* __restrict__ x,
                                            const int* xrow, int K, int M, int kseg0, int ra, int t, float* acc,
                                            uint32_t tab = 0) {
@@ -1790,7 +1807,7 @@ __device__ __noinline__ void tile_slot_f32(uint32_t wst, uint32_t sst, const uin
             const int k0 = ((kseg0 + c) * 2 + h) * 128 + 32 * t;
             for (int w = 0; w < 4; ++w) {
                 for (int m = 0; m < M; ++m) {
-                    const uint4 xv = ldg128(x + static_cast<int64_t>(xrow ? xrow[m] : m) * K + k0 + w * 8);
+                    const uint4 xv = ldx128<kCG>(x + static_cast<int64_t>(xrow ? xrow[m] : m) * K + k0 + w * 8);
                     const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
                     for (int r = 0; r < 2; ++r) {
                         const uint32_t word = w == 0 ? wv[r].x : (w == 1 ? wv[r].y : (w == 2 ? wv[r].z : wv[r].w));
@@ -1814,7 +1831,7 @@ __device__ __noinline__ void tile_slot_f32(uint32_t wst, uint32_t sst, const uin
 // Position in a CTA's block of items, walked without divisions.
 struct TileItemWalk {
     int grp, t;  // group (dense: 0 gate / 1 up; MoE: expert group) and item index within it
-    __device__ __forceinline__ void next(int ipg) {
+    __host__ __device__ __forceinline__ void next(int ipg) {
         if (++t == ipg) {
             t = 0;
             ++grp;
@@ -2400,6 +2417,479 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_kernel(const __grid
     __syncwarp();
     if (tid == 0) trace_phase(p.trace_slot, 7);
     trace_flush(p.trace_slot, tid);
+}
+
+// ------------------------------------------------------------------ the FFN block in one launch
+
+// The shared-expert FFN group of "glm-5.3-flash-nvfp4-tp3-512k--gb10 graph.json" (block l3.moe:
+// shared_gate_up, shared_clamp, shared_act, shared_down) as one launch. Phase A is the gate/up
+// GEMV with the fused SwiGLU (wmap/smap [0] gate, [1] up; y = h, bf16 [M, I]); phase B is the
+// down GEMV (wmap/smap [0]; x = h; y = the block's output). Both phases use one ring (NC,
+// stages), one grid with every CTA resident at once (two per SM) and no clusters.
+//
+// The phases meet through readiness counters instead of a grid barrier: phase B's warp with K
+// slice s needs only h[:, slice s], which a known number of phase-A items write. Every A item,
+// once its h rows are stored, adds one to its slice's counter (release); a B warp waits
+// (acquire, bounded) until its slice's counter holds all of them. A items are dealt round-robin
+// over the CTAs, so the low slices fill early, and B items go first to the CTAs with fewer A
+// items. `sync` is the caller's workspace: word 0 counts the CTAs that are done with the
+// counters, word 32 (s + 1) is slice s's counter (each in its own 128-byte line); the last CTA
+// done sets them all back to zero for the next launch.
+//
+// A ninth warp does every release and acquire-release operation on these words, so no compute
+// warp ever waits for a GPU-scope fence. After storing an item's h rows each compute warp adds
+// one to a shared-memory count (release, CTA scope); the ninth warp waits (acquire) until all
+// eight have, then counts the item in. Once all compute warps have passed their slice waits
+// (a second shared count), it counts the CTA as done. Both shared counts only grow, so the
+// ninth warp may fall any number of items behind.
+struct FfnParams {
+    TileParams a, b;
+    uint32_t* sync;
+};
+
+constexpr int kFfnSyncBytes = 2048;   // workspace bytes before h: the counters' lines
+constexpr int kFfnSlices = 8;         // B's K slices (one counter each)
+constexpr int kFfnThreads = tk::kThreads + 32;  // 8 compute warps and the signalling warp
+constexpr int64_t kFfnFusedMaxBytes = 12ll << 20;  // weights of the largest block run as one launch
+
+#ifndef NVFP4_FFN_H_PRE
+#define NVFP4_FFN_H_PRE 6  // loads in flight per lane when phase B stages h (one batch at M = 1, I = 12288)
+#endif
+
+// One phase's share of a warp: its tile within an item, its box range (K slice), and its CTA's
+// items first, first + stride, ... (count of them). Phase A deals items round-robin (item i to
+// CTA i mod units); phase B in reverse (item j to CTA units - 1 - j mod units), so B's items
+// land first on the CTAs that drew one A item fewer.
+struct FfnGeo {
+    int tin, kslice, b_lo, nb, first, count, stride;
+};
+
+__host__ __device__ __forceinline__ FfnGeo ffn_geo(const TileParams& q, int warp, int unit, int units, bool rev) {
+    FfnGeo g;
+    const int ksplit = 1 << q.ksplit_log2;
+    g.kslice = warp & (ksplit - 1);
+    g.tin = warp >> q.ksplit_log2;
+    g.b_lo = (g.kslice * q.nbox) >> q.ksplit_log2;
+    g.nb = (((g.kslice + 1) * q.nbox) >> q.ksplit_log2) - g.b_lo;
+    const int items = q.items_q * units + q.items_r;
+    g.first = rev ? units - 1 - unit : unit;
+    g.count = g.first < items ? (items - g.first + units - 1) / units : 0;
+    g.stride = units;
+    return g;
+}
+
+// Rows of h one phase-A item writes (its gate/up tile pairs x 16), and the A items whose rows
+// fall in phase B's K slice s (slices start at multiples of 256 rows, which R divides).
+__host__ __device__ __forceinline__ int ffn_item_rows(const TileParams& a) { return (a.tpi >> 1) * 16; }
+
+__host__ __device__ __forceinline__ int ffn_slice_lo(const TileParams& b, int s, int nc) {
+    return ((s * b.nbox) >> b.ksplit_log2) * nc * 256;
+}
+
+__host__ __device__ __forceinline__ int ffn_slice_items(const TileParams& a, const TileParams& b, int s, int nc) {
+    const int lo = ffn_slice_lo(b, s, nc), hi = min(ffn_slice_lo(b, s + 1, nc), b.K);
+    const int r = ffn_item_rows(a);
+    return (hi - lo + r - 1) / r;
+}
+
+// B's K slice holding h row `row` (the slice whose range contains it).
+__host__ __device__ __forceinline__ int ffn_slice_of(const TileParams& b, int row, int nc) {
+    const int ks = 1 << b.ksplit_log2;
+    int s = 0;
+    while (s + 1 < ks && ffn_slice_lo(b, s + 1, nc) <= row) ++s;
+    return s;
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t* p, uint32_t v) {
+    uint32_t old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
+__device__ __forceinline__ void red_add_release_gpu(uint32_t* p, uint32_t v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_relaxed_gpu(uint32_t* p, uint32_t v) {
+    asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void red_add_release_cta_shared(uint32_t* p, uint32_t v) {
+    asm volatile("red.release.cta.shared::cta.add.u32 [%0], %1;" ::"r"(smem_addr(p)), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_cta_shared(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_addr(p)) : "memory");
+    return v;
+}
+
+// One thread waits (acquire, CTA scope) until the shared count *c reaches want, for at most
+// `budget` ns. False when it ran out (the count is the CTA's own: only a defect leaves it short).
+__device__ bool ffn_wait_shared(const uint32_t* c, uint32_t want, uint64_t budget) {
+    if (ld_acquire_cta_shared(c) >= want) return true;
+    const uint64_t t0 = global_ns();
+    while (ld_acquire_cta_shared(c) < want) {
+        if (global_ns() - t0 > budget) return false;
+        __nanosleep(64);
+    }
+    return true;
+}
+
+// Waits (every lane, acquire) until *cnt >= want, for at most `budget` ns (0: one look).
+// Returns whether it got there (uniform over the warp: all lanes read the same word, and the
+// warp votes).
+__device__ bool ffn_wait_count(const uint32_t* cnt, uint32_t want, uint64_t budget) {
+    bool ok = ld_acquire_gpu(cnt) >= want;
+    if (__all_sync(0xffffffffu, ok)) return true;
+    const uint64_t t0 = global_ns();
+    uint32_t ns = 32;
+    for (;;) {
+        ok = ld_acquire_gpu(cnt) >= want;
+        if (__all_sync(0xffffffffu, ok)) return true;
+        if (budget == 0 || global_ns() - t0 > budget) return false;
+        __nanosleep(ns);
+        ns = ns < 256 ? 2 * ns : 256;
+    }
+}
+
+template <int NC>
+__global__ void __launch_bounds__(kFfnThreads, 2) gemv_ffn_kernel(const __grid_constant__ FfnParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ uint32_t s_sig[2];  // compute warps that stored an A item's h rows / passed their slice wait
+    constexpr uint32_t kWBox = NC * 2048;
+    constexpr uint32_t kSBox = scale_box_bytes<NC, false>();
+    const TileParams& A = p.a;
+    const TileParams& B = p.b;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int t = lane & 3;
+    const uint32_t raw_base = smem_addr(smem_raw);
+    const uint32_t base = (raw_base + 1023u) & ~1023u;
+    uint8_t* const sbase = smem_raw + (base - raw_base);
+    const int stages = A.stages;  // one ring for both phases
+    uint64_t* const bars = reinterpret_cast<uint64_t*>(sbase + A.bar_off) + warp * tk::kMaxStages;
+    const uint32_t ring_w = base + A.ring_w + static_cast<uint32_t>(warp * stages) * kWBox;
+    const uint32_t ring_s = base + A.ring_s + static_cast<uint32_t>(warp * stages) * kSBox;
+    const int slot = A.trace_slot;
+    if (tid == 0) s_sig[0] = s_sig[1] = 0u;
+    __syncthreads();
+    trace_begin(tid);
+    if (tid == 0) trace_phase(slot, 0);
+    const int unit = blockIdx.x, units = gridDim.x;
+    if (warp == tk::kWarps) {
+        // the signalling warp: counts every A item into its B slice once the compute warps have
+        // stored its h rows, then counts the CTA as done once they are past their slice waits
+        pdl_launch_dependents();
+        pdl_wait();
+        const FfnGeo ga = ffn_geo(A, 0, unit, units, false);
+        for (int j = 0; j < ga.count && lane == 0; ++j) {
+            if (!ffn_wait_shared(&s_sig[0], static_cast<uint32_t>(tk::kWarps * (j + 1)), kDrainWaitNs))
+                raise_status(NVFP4_DEV_INTERNAL, nullptr);
+            const int item = ga.first + j * ga.stride;
+            if (2 * item * (A.tpi >> 1) < A.tiles)
+                red_add_release_gpu(p.sync + 32 * (1 + ffn_slice_of(B, item * ffn_item_rows(A), NC)), 1u);
+        }
+        if (lane == 0) {
+            if (!ffn_wait_shared(&s_sig[1], static_cast<uint32_t>(tk::kWarps), kDrainWaitNs))
+                raise_status(NVFP4_DEV_INTERNAL, nullptr);
+            // the last CTA done puts the counters back to zero: every CTA counted its A items and
+            // passed its waits before it counts itself here (acq_rel chain on word 0)
+            const uint32_t done = atom_add_acq_rel_gpu(p.sync, 1u);
+            if (done == static_cast<uint32_t>(units) - 1u) {
+                for (int s = 0; s < kFfnSlices; ++s) st_relaxed_gpu(p.sync + 32 * (1 + s), 0u);
+                st_relaxed_gpu(p.sync, 0u);
+            }
+        }
+        __syncwarp();
+        trace_flush(slot, tid);
+        return;
+    }
+    if (NVFP4_PREFETCH_TMAP && warp == 0 && lane < 3) prefetch_tmap(lane < 2 ? &A.wmap[lane] : &B.wmap[0]);
+    if (NVFP4_PREFETCH_TMAP && warp == 1 && lane < 3) prefetch_tmap(lane < 2 ? &A.smap[lane] : &B.smap[0]);
+    const FfnGeo ga = ffn_geo(A, warp, unit, units, false);
+    const FfnGeo gb = ffn_geo(B, warp, unit, units, true);
+    if (lane == 0) {
+        for (int s = 0; s < stages; ++s) mbar_init(&bars[s], 1);
+        fence_barrier_init();
+    }
+    __syncwarp();
+
+    // lane 0's issue cursor walks phase A's boxes, then phase B's: neither depends on x or h, so
+    // B's first boxes stream in while A finishes
+    int iph = 0;
+    int iss_j = 0, iss_box = 0;
+    uint32_t issued = 0, consumed = 0;
+    uint32_t iss_st = 0, cons_st = 0, cons_ph = 0;
+    auto cons_advance = [&]() {
+        ++consumed;
+        if (++cons_st == static_cast<uint32_t>(stages)) {
+            cons_st = 0;
+            cons_ph ^= 1u;
+        }
+    };
+    auto issue_next = [&]() {
+        for (;;) {
+            if (iph == 2) return;
+            const bool pa = iph == 0;
+            const FfnGeo& g = pa ? ga : gb;
+            const int tpi = pa ? A.tpi : B.tpi, tiles = pa ? A.tiles : B.tiles;
+            while (iss_j < g.count && (iss_box >= g.nb || (g.first + iss_j * g.stride) * tpi + g.tin >= tiles)) {
+                ++iss_j;
+                iss_box = 0;
+            }
+            if (iss_j < g.count) break;
+            iph = pa ? 1 : 2;
+            iss_j = 0;
+            iss_box = 0;
+        }
+        const uint32_t st = iss_st;
+        if (++iss_st == static_cast<uint32_t>(stages)) iss_st = 0;
+        const uint32_t bar = smem_addr(&bars[st]);
+        mbar_arrive_expect_tx(&bars[st], kWBox + scale_box_tx<NC, false>());
+        if (iph == 0) {
+            const int tile = (ga.first + iss_j * ga.stride) * A.tpi + ga.tin;  // tiles alternate gate, up
+            const int seg = (ga.b_lo + iss_box) * NC, row0 = (tile >> 1) * 16;
+            tma_load_3d(ring_w + st * kWBox, &A.wmap[tile & 1], 0, seg, row0, bar);
+            tma_load_3d(ring_s + st * kSBox, &A.smap[tile & 1], 0, seg, row0, bar);
+        } else {
+            const int tile = (gb.first + iss_j * gb.stride) * B.tpi + gb.tin;
+            const int seg = (gb.b_lo + iss_box) * NC;
+            tma_load_3d(ring_w + st * kWBox, &B.wmap[0], 0, seg, tile * 16, bar);
+            tma_load_3d(ring_s + st * kSBox, &B.smap[0], 0, seg, tile * 16, bar);
+        }
+        ++iss_box;
+        ++issued;
+    };
+    // gate/up weights before the dependency wait (x may come from the preceding kernel; only an
+    // L2 prefetch of it goes out before the wait)
+    if (lane == 0)
+        for (int s = 0; s < min(stages, NVFP4_DENSE_EARLY); ++s) issue_next();
+    const int M = A.M;
+    if (warp == tk::kWarps - 1 && lane < M) {
+        const uint16_t* xr = A.x + static_cast<int64_t>(lane) * A.K;
+        prefetch_l2_bulk(xr, static_cast<uint32_t>(A.K) * 2u);
+        prefetch_l2(xr);
+    }
+    if (tid == 0) trace_phase(slot, 1);
+    pdl_launch_dependents();
+    pdl_wait();
+    if (tid == 0) trace_phase(slot, 2);
+
+    bool dead = false;  // warp-uniform: a wait ran out of time
+    // One phase: stage this warp's K slice of x (A) or h (B), then run the CTA's items.
+    auto phase = [&](auto swi_tag, const TileParams& q, const FfnGeo& g) {
+        constexpr bool SWI = decltype(swi_tag)::value;
+        const int ksplit = 1 << q.ksplit_log2;
+        const int kslice = g.kslice, tin = g.tin;
+        const uint32_t slice_bytes = static_cast<uint32_t>(M) * q.sstride;
+        uint8_t* const xs = sbase + q.x_off + kslice * slice_bytes;
+        float* const e2 = reinterpret_cast<float*>(sbase + q.misc_off) + kslice * 8;
+        uint32_t* const gmax = reinterpret_cast<uint32_t*>(sbase + q.misc_off + tk::kWarps * 32) + kslice * 32;
+        const int k0 = g.b_lo * NC * 256, kn = g.nb * NC * 256;
+        const int xbar = q.tpi > 1 ? 2 + kslice : -1;
+        if constexpr (!SWI) {
+            // h[:, slice] is complete once every A item of the slice has counted itself in; the
+            // staging runs even after a timeout, so the slice's warps keep their barrier counts
+            if (g.count > 0 && !dead &&
+                !ffn_wait_count(p.sync + 32 * (1 + kslice), static_cast<uint32_t>(ffn_slice_items(A, B, kslice, NC)),
+                                q.wait_ns)) {
+                dead = true;
+                if (lane == 0) raise_status(NVFP4_DEV_TIMEOUT, nullptr);
+            }
+            if (tid == 0) trace_word(slot, 38, global_ns());
+            __syncwarp();  // every lane is done reading the counters
+            if (lane == 0) red_add_release_cta_shared(&s_sig[1], 1u);
+        }
+        bool lossy = false;
+        float e2v = 1.f;
+        // h was written by other CTAs of this launch: read it through L2 only
+        const bool staged = SWI ? stage_x_direct<NVFP4_STAGE_PRE, false>(q.x, nullptr, M, q.K, k0, kn, xs, q.sstride,
+                                                                         gmax + 16, tin, q.tpi, xbar, lane, [] {})
+                                : stage_x_direct<NVFP4_FFN_H_PRE, true>(q.x, nullptr, M, q.K, k0, kn, xs, q.sstride,
+                                                                        gmax + 16, tin, q.tpi, xbar, lane, [] {});
+        if (!staged) {
+            lossy = SWI ? stage_x_slice<false>(q.x, nullptr, M, q.K, k0, kn, xs, q.sstride, e2, gmax, tin, q.tpi,
+                                               xbar, lane)
+                        : stage_x_slice<true>(q.x, nullptr, M, q.K, k0, kn, xs, q.sstride, e2, gmax, tin, q.tpi,
+                                              xbar, lane);
+            e2v = e2[0];
+        }
+        if constexpr (SWI) {
+            if (tid == 0) trace_phase(slot, 3);
+            if (lane == 0)  // the rest of the ring
+                for (int s = min(stages, NVFP4_DENSE_EARLY); s < stages; ++s) issue_next();
+        } else {
+            if (tid == 0) trace_word(slot, 39, global_ns());
+        }
+        const bool use_f32 = lossy || q.force_f32;
+        if (use_f32 && tin == 0 && lane == 0) atomicAdd(&g_fp32_fallbacks, 1ull);
+        const int g8 = lane >> 2;
+        const int ra = tile_row_perm<NC>(g8), rb = ra + 8;
+        const uint32_t xa = base + q.x_off + kslice * slice_bytes + static_cast<uint32_t>(min(g8, M - 1)) * q.sstride;
+        const int m0 = 2 * t;
+        const float e2s = use_f32 ? 1.f : e2v;
+        float* const red = reinterpret_cast<float*>(sbase + q.red_off);
+        const uint64_t budget = q.wait_ns;
+        bool traced_first = false;
+        for (int j = 0; j < g.count; ++j) {
+            const int item = g.first + j * g.stride;
+            const int tile = item * q.tpi + tin;
+            const bool valid = tile < q.tiles;
+            float d[4] = {0.f, 0.f, 0.f, 0.f};
+            if (valid && !dead) {
+                float dd[kTileChains][4];
+#pragma unroll
+                for (int c = 0; c < kTileChains; ++c)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) dd[c][i] = 0.f;
+                float acc[16];
+                if (use_f32) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+                }
+                for (int b = 0; b < g.nb; ++b) {
+                    const uint32_t st = cons_st;
+                    const uint32_t ph = cons_ph;
+                    if (!__all_sync(0xffffffffu, budget != 0 && mbar_wait(&bars[st], ph, budget))) {
+                        dead = true;  // stop computing, keep the CTA's barrier counts
+                        break;
+                    }
+                    if (NVFP4_PHASE_TRACE && SWI && warp == 0 && lane == 0 && !traced_first) {
+                        trace_phase(slot, 4);
+                        traced_first = true;
+                    }
+                    if (!use_f32) {
+                        tile_slot_mma<NC>(ring_w + st * kWBox, ring_s + st * kSBox, xa, b * NC * 2, ra, t, dd);
+                    } else {
+                        tile_slot_f32<NC, false, !SWI>(ring_w + st * kWBox, ring_s + st * kSBox, q.x, nullptr, q.K,
+                                                       M, (g.b_lo + b) * NC, ra, t, acc);
+                    }
+                    cons_advance();
+                    __syncwarp();
+                    if (lane == 0) issue_next();
+                }
+                if (use_f32) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], 1);
+                        acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], 2);
+                    }
+#pragma unroll
+                    for (int m = 0; m < 8; ++m) {
+                        if (m == m0) { d[0] = acc[m]; d[2] = acc[8 + m]; }
+                        if (m == m0 + 1) { d[1] = acc[m]; d[3] = acc[8 + m]; }
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < kTileChains; ++c)
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) d[i] += dd[c][i];
+                }
+                if (dead && lane == 0) raise_status(NVFP4_DEV_TIMEOUT, nullptr);
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) d[i] *= e2s;
+            const int par = j & 1;
+            float* const cpart = reinterpret_cast<float*>(sbase + q.cpart_off) + par * (tk::kWarps * 16 * 8);
+            if constexpr (SWI) {
+                // gate tile 2j and up tile 2j + 1 meet in cpart ([tile * 16 + row][m]), then every
+                // output combines its pair into one bf16 h
+                const int outs = q.tpi * 16 * M;
+                const int pair_outs = (q.tpi >> 1) * 16 * M;
+                if (ksplit == 1) {
+                    float* cp = cpart + tin * 128;
+                    cp[ra * 8 + m0] = d[0];
+                    cp[ra * 8 + m0 + 1] = d[1];
+                    cp[rb * 8 + m0] = d[2];
+                    cp[rb * 8 + m0 + 1] = d[3];
+                } else {
+                    float* rbuf = red + par * tk::kRedFloats + warp * 128;
+                    rbuf[ra * 8 + m0] = d[0];
+                    rbuf[ra * 8 + m0 + 1] = d[1];
+                    rbuf[rb * 8 + m0] = d[2];
+                    rbuf[rb * 8 + m0 + 1] = d[3];
+                    named_bar_sync(1, tk::kThreads);
+                    const float* rb0 = red + par * tk::kRedFloats;
+                    for (int i = tid; i < outs; i += tk::kThreads) {
+                        const int ti = i / (16 * M), rem = i - ti * 16 * M;
+                        const int r = rem / M, m = rem - r * M;
+                        float sum = 0.f;
+                        for (int jj = 0; jj < ksplit; ++jj) sum += rb0[((ti << q.ksplit_log2) + jj) * 128 + r * 8 + m];
+                        cpart[ti * 128 + r * 8 + m] = sum;
+                    }
+                }
+                named_bar_sync(1, tk::kThreads);
+                for (int i = tid; i < pair_outs; i += tk::kThreads) {
+                    const int pi = i / (16 * M), rem = i - pi * 16 * M;
+                    const int r = rem / M, m = rem - r * M;
+                    const int jt = item * (q.tpi >> 1) + pi, row = jt * 16 + r;  // output tile, row
+                    if (2 * jt < q.tiles && row < q.N) {
+                        const float* cg = cpart + (2 * pi) * 128 + r * 8 + m;
+                        store_out(q.y, m * q.ldy + row, swiglu_f32(cg[0] * q.g[0], cg[128] * q.g[1], q.clamp),
+                                  q.out_bf16);
+                    }
+                }
+                // the item's h rows are stored: the signalling warp counts them in once all eight
+                // warps have said so (the warp barrier orders the lanes' stores before lane 0's
+                // release)
+                __syncwarp();
+                if (lane == 0) red_add_release_cta_shared(&s_sig[0], 1u);
+            } else {
+                const float gs = q.g[0];
+                if (ksplit == 1) {
+                    if (valid) {
+                        const int rowa = tile * 16 + ra, rowb = tile * 16 + rb;
+                        if (m0 < M) {
+                            if (rowa < q.N) store_out(q.y, m0 * q.ldy + rowa, d[0] * gs, q.out_bf16);
+                            if (rowb < q.N) store_out(q.y, m0 * q.ldy + rowb, d[2] * gs, q.out_bf16);
+                        }
+                        if (m0 + 1 < M) {
+                            if (rowa < q.N) store_out(q.y, (m0 + 1) * q.ldy + rowa, d[1] * gs, q.out_bf16);
+                            if (rowb < q.N) store_out(q.y, (m0 + 1) * q.ldy + rowb, d[3] * gs, q.out_bf16);
+                        }
+                    }
+                } else {
+                    const int outs = q.tpi * 16 * M;
+                    float* rbuf = red + par * tk::kRedFloats + warp * 128;
+                    rbuf[ra * 8 + m0] = d[0];
+                    rbuf[ra * 8 + m0 + 1] = d[1];
+                    rbuf[rb * 8 + m0] = d[2];
+                    rbuf[rb * 8 + m0 + 1] = d[3];
+                    named_bar_sync(1, tk::kThreads);
+                    const float* rb0 = red + par * tk::kRedFloats;
+                    for (int i = tid; i < outs; i += tk::kThreads) {
+                        const int ti = i / (16 * M), rem = i - ti * 16 * M;
+                        const int r = rem / M, m = rem - r * M;
+                        float sum = 0.f;
+                        for (int jj = 0; jj < ksplit; ++jj) sum += rb0[((ti << q.ksplit_log2) + jj) * 128 + r * 8 + m];
+                        const int tl = item * q.tpi + ti, row = tl * 16 + r;
+                        if (tl < q.tiles && row < q.N) store_out(q.y, m * q.ldy + row, sum * gs, q.out_bf16);
+                    }
+                }
+            }
+        }
+    };
+
+    phase(std::integral_constant<bool, true>{}, A, ga);
+    if (tid == 0) trace_phase(slot, 5);
+    phase(std::integral_constant<bool, false>{}, B, gb);
+    if (tid == 0) trace_phase(slot, 6);
+    // copies still in flight (only after a timeout) land before the CTA exits
+    if (lane == 0) {
+        while (consumed < issued) {
+            mbar_wait(&bars[cons_st], cons_ph, kDrainWaitNs);
+            cons_advance();
+        }
+    }
+    __syncwarp();
+    if (tid == 0) trace_phase(slot, 7);
+    trace_flush(slot, tid);
 }
 
 #ifndef NVFP4_MOE_EARLY
@@ -3295,7 +3785,7 @@ struct TilePlan {
 // SM times the steps each of its warps decodes), both in units of one warp step.
 bool plan_tile(TilePlan& tp, int M, int N, int K, int groups, const DeviceInfo& d, const uint8_t* const* w,
                const uint8_t* const* s, const void* x, bool moe = false, int moe_rows = 0, int moe_groups_max = 0,
-               bool swiglu = false, bool need_encoder = true, bool sd = false) {
+               bool swiglu = false, bool need_encoder = true, bool sd = false, double* cost_out = nullptr) {
     if (g_variant == 1 || g_variant == 3) return false;
     if (sd && (swiglu || (!moe && groups != 1))) return false;  // dictionary scales: dense or MoE
     // scale box per ring slot and the pair table (dictionary scales)
@@ -3536,6 +4026,7 @@ bool plan_tile(TilePlan& tp, int M, int N, int K, int groups, const DeviceInfo& 
           }
         }
     }
+    if (found && cost_out) *cost_out = best;
     return found;
 }
 
@@ -3940,6 +4431,290 @@ nvfp4_status run_sdict_moe(const uint8_t* w, const uint8_t* plane, const uint8_t
     return e == cudaSuccess ? NVFP4_OK : cuda_fail(e);
 }
 
+// ------------------------------------------------------------------ the FFN block (host)
+
+// Bytes of the FFN workspace: the counters' lines (kFfnSyncBytes: the finished-CTA count, then
+// one counter per phase-B K slice, each in its own 128-byte line), then h as bf16 [M, I] (rows of
+// 2 I bytes, back to back), rounded up to 256 bytes.
+int64_t ffn_workspace_bytes(int M, int I) {
+    return kFfnSyncBytes + (static_cast<int64_t>(M) * I * 2 + 255) / 256 * 256;
+}
+
+struct FfnPlan {
+    FfnParams p;
+    int nc;
+    int grid;
+    uint32_t smem;
+};
+
+// Cost of one phase in units of a warp's 128-element step, as plan_tile prices a per-item
+// plan on `units` CTAs: the larger of the latency term (items of the busiest CTA, each with its
+// steps and reduction) and the throughput term, plus the staging of x.
+double ffn_phase_cost(long long items, int ksplit, int nc, int nbmax, int M, int K, long long units, int sms) {
+    const long long ipu = (items + units - 1) / units;
+    const double spw = 2.0 * nc * nbmax;
+    const double lat = static_cast<double>(ipu) * (spw + (ksplit > 1 ? 2.0 : 0.3));
+    const double thr = static_cast<double>(items) * tk::kWarps * spw / (sms * 16.0) * 1.1;
+    return std::max(lat, thr) + static_cast<double>(M) * K / 2048.0;
+}
+
+// One-launch plan for the FFN block: phase A (gate/up + SwiGLU, K = H, I outputs) and phase B
+// (down, K = I, H outputs) on 2 CTAs per SM, one ring for both, and x/h staging that fits beside
+// it. The x region holds the larger of A's x slices plus its pair buffer (cpart) and B's h
+// slices: a CTA's warps are past its last A item's barrier, so done with both, before any of them
+// stages h. False when the block's weights exceed kFfnFusedMaxBytes or no such plan fits.
+bool plan_ffn(FfnPlan& fp, int M, int H, int I, const DeviceInfo& d) {
+    if (g_variant == 1 || g_variant == 3) return false;
+    if (M < 1 || M > 8 || H <= 0 || I <= 0 || H % 256 || I % 256 || H > (1 << 27) || I > (1 << 27)) return false;
+    // each phase priced as the separate launch would be: a fused plan whose phase costs far
+    // more (a decomposition squeezed to fit beside the other phase's x) is not taken
+    const uint8_t* fake = reinterpret_cast<const uint8_t*>(static_cast<uintptr_t>(256));
+    const uint8_t* fw[2] = {fake, fake};
+    double solo_a = 0.0, solo_b = 0.0;
+    TilePlan solo{};
+    if (!plan_tile(solo, M, I, H, 2, d, fw, fw, fake, false, 0, 0, true, false, false, &solo_a) ||
+        !plan_tile(solo, M, H, I, 1, d, fw, fw, fake, false, 0, 0, false, false, false, &solo_b))
+        return false;
+    const long long units = static_cast<long long>(d.sm_count) * 2;
+    const uint32_t limit = static_cast<uint32_t>(d.smem_per_sm / 2 - 1024);
+    bool found = false;
+    double best = 0.0;
+    // one launch only for latency-bound blocks: measured, the shared expert (H = 4096, I = 768,
+    // M = 2, 5.3 MB) ran 10.7 us a step in one launch and 10.8 in two, while the 12288-wide FFN
+    // (85 MB) ran 26.5 to 27.8 in one and 23.2 in two
+    if (3.0 * H * I * 9.0 / 16.0 > static_cast<double>(kFfnFusedMaxBytes)) return false;
+    for (int nc = 2; nc >= 1; --nc) {
+        if ((H / 256) % nc || (I / 256) % nc) continue;
+        if (NVFP4_TILE_NC && nc != NVFP4_TILE_NC) continue;
+        const int nbox_a = H / 256 / nc, nbox_b = I / 256 / nc;
+        const int tiles_a = 2 * ((I + 15) / 16), tiles_b = (H + 15) / 16;
+        for (int la = 0; la <= 2; ++la) {       // A: tpi >= 2 (whole gate/up pairs)
+            const int ka = 1 << la;
+            if (ka > nbox_a) break;
+            const int tpi_a = tk::kWarps / ka;
+            const long long items_a = (tiles_a + tpi_a - 1) / tpi_a;
+            const int nbmax_a = (nbox_a + ka - 1) / ka;
+            const uint32_t sstride_a = static_cast<uint32_t>(nbmax_a) * nc * 512u + 64u;
+            const uint32_t xa = align_up(static_cast<uint32_t>(ka * M) * sstride_a, 128);
+            for (int lb = 0; lb <= 3; ++lb) {
+                const int kb = 1 << lb;
+                if (kb > nbox_b) break;
+                const int tpi_b = tk::kWarps / kb;
+                const long long items_b = (tiles_b + tpi_b - 1) / tpi_b;
+                const int nbmax_b = (nbox_b + kb - 1) / kb;
+                const uint32_t sstride_b = static_cast<uint32_t>(nbmax_b) * nc * 512u + 64u;
+                const uint32_t xb = align_up(static_cast<uint32_t>(kb * M) * sstride_b, 128);
+                const uint32_t cpart = 2u * tk::kWarps * 16 * 8 * 4u;
+                const uint32_t xreg = std::max(xa + cpart, xb);
+                const uint32_t red = (ka > 1 || kb > 1) ? 2u * tk::kRedFloats * 4u : 0u;
+                for (int st = tk::kMaxStages; st >= 2; --st) {
+                    TileParams q{};
+                    uint32_t off = 0;
+                    q.ring_w = off;
+                    off += static_cast<uint32_t>(tk::kWarps * st * nc) * 2048u;
+                    q.ring_s = off;
+                    off += static_cast<uint32_t>(tk::kWarps * st * nc) * 256u;
+                    q.x_off = off;
+                    q.cpart_off = off + xa;
+                    off += xreg;
+                    q.red_off = off;
+                    off += red;
+                    q.misc_off = off;
+                    off += align_up(tk::kWarps * 32 + tk::kWarps * 32 * 4, 128);
+                    q.bar_off = off;
+                    off += tk::kWarps * tk::kMaxStages * 8;
+                    q.moe_off = q.sdtab_off = off;
+                    const uint32_t total = off + 1024;
+                    if (total > limit) continue;
+                    const double ca = ffn_phase_cost(items_a, ka, nc, nbmax_a, M, H, units, d.sm_count);
+                    const double cb = ffn_phase_cost(items_b, kb, nc, nbmax_b, M, I, units, d.sm_count);
+                    const double cost = ca + cb;
+                    if (ca > 1.5 * solo_a || cb > 1.5 * solo_b) break;
+                    if (!found || cost < best - 1e-9) {
+                        found = true;
+                        best = cost;
+                        TileParams a = q, b = q;
+                        a.M = b.M = M;
+                        a.N = I; a.K = H; a.tiles = tiles_a; a.ksplit_log2 = la; a.tpi = tpi_a;
+                        a.ipg = static_cast<int>(items_a);
+                        a.items_q = static_cast<int>(items_a / units);
+                        a.items_r = static_cast<int>(items_a % units);
+                        a.nbox = nbox_a; a.sstride = sstride_a; a.swiglu = 1;
+                        b.N = H; b.K = I; b.tiles = tiles_b; b.ksplit_log2 = lb; b.tpi = tpi_b;
+                        b.ipg = static_cast<int>(items_b);
+                        b.items_q = static_cast<int>(items_b / units);
+                        b.items_r = static_cast<int>(items_b % units);
+                        b.nbox = nbox_b; b.sstride = sstride_b;
+                        a.stages = b.stages = st;
+                        fp.p.a = a;
+                        fp.p.b = b;
+                        fp.nc = nc;
+                        fp.grid = static_cast<int>(units);
+                        fp.smem = total;
+                    }
+                    break;  // the deepest ring that fits
+                }
+            }
+        }
+    }
+    return found;
+}
+
+template <int NC>
+cudaError_t launch_ffn_nc(const FfnPlan& fp, cudaStream_t st) {
+    auto kern = gemv_ffn_kernel<NC>;
+    static bool done[64] = {};
+    cudaError_t e = allow_max_smem(kern, done);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(fp.grid);
+    cfg.blockDim = dim3(kFfnThreads);
+    cfg.dynamicSmemBytes = fp.smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    int na = 0;
+    if (g_pdl) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
+    return cudaLaunchKernelEx(&cfg, kern, fp.p);
+}
+
+// Whether the fused kernel keeps two CTAs per SM resident at this shared-memory size (the grid
+// barrier needs every CTA of the launch resident at once).
+template <int NC>
+bool ffn_two_per_sm(uint32_t smem) {
+    static bool done[64] = {};
+    if (allow_max_smem(gemv_ffn_kernel<NC>, done) != cudaSuccess) return false;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gemv_ffn_kernel<NC>, kFfnThreads, smem) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return n >= 2;
+}
+
+struct FfnKey {
+    int dev, M, H, I, variant;
+    const void* w[3];
+    const void* s[3];
+    bool operator==(const FfnKey& o) const { return std::memcmp(this, &o, sizeof(FfnKey)) == 0; }
+};
+struct FfnEntry {
+    FfnKey key;
+    bool used;
+    bool fused;
+    FfnPlan fp;
+};
+constexpr int kFfnCacheSize = 16;
+FfnEntry g_ffn_cache[kFfnCacheSize];
+
+// The FFN block: one fused launch when a plan fits with every CTA resident (2 per SM), else the
+// gate/up + SwiGLU launch writing h into the workspace, then the down launch reading it.
+nvfp4_status run_ffn(const uint8_t* const* w, const uint8_t* const* s, const float* g, const uint16_t* x,
+                     float clamp, void* workspace, void* y, int y_type, int M, int H, int I, cudaStream_t st) {
+    if (!x || !y || !workspace) return NVFP4_ERR_NULL;
+    for (int i = 0; i < 3; ++i)
+        if (!w[i] || !s[i]) return NVFP4_ERR_NULL;
+    if (!(clamp > 0.f)) return NVFP4_ERR_SHAPE;  // also rejects NaN
+    if (M < 0 || H < 0 || I < 0 || M > 8 || H % 16 != 0 || I % 16 != 0) return NVFP4_ERR_SHAPE;
+    if (reinterpret_cast<uintptr_t>(workspace) & 255) return NVFP4_ERR_ALIGN;
+    const nvfp4_status so = check_out(y_type);
+    if (so != NVFP4_OK) return so;
+    if (M == 0 || H == 0) return NVFP4_OK;
+    if (I == 0) return zero_output(y, static_cast<int64_t>(M) * H, y_type, st);  // an empty down sum
+    int dev = 0;
+    const DeviceInfo* d = device_info(&dev);
+    if (!d) return cuda_fail(cudaGetLastError());
+    uint16_t* h = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(workspace) + kFfnSyncBytes);
+    FfnKey key;
+    std::memset(&key, 0, sizeof key);
+    key.dev = dev; key.M = M; key.H = H; key.I = I; key.variant = g_variant;
+    for (int i = 0; i < 3; ++i) {
+        key.w[i] = w[i];
+        key.s[i] = s[i];
+    }
+    const bool x_ok = (reinterpret_cast<uintptr_t>(x) & 15) == 0;
+    bool w_ok = true;
+    for (int i = 0; i < 3; ++i)
+        w_ok = w_ok && !(reinterpret_cast<uintptr_t>(w[i]) & 15) && !(reinterpret_cast<uintptr_t>(s[i]) & 15);
+    FfnPlan fp{};
+    bool fused = false;
+    if (x_ok && w_ok) {
+        uint32_t slot = 2166136261u;
+        const unsigned char* kb = reinterpret_cast<const unsigned char*>(&key);
+        for (size_t i = 0; i < sizeof key; ++i) slot = (slot ^ kb[i]) * 16777619u;
+        slot %= kFfnCacheSize;
+        bool hit = false;
+        {
+            std::lock_guard<std::mutex> lk(g_mu);
+            const FfnEntry& e = g_ffn_cache[slot];
+            if (e.used && e.key == key) {
+                hit = true;
+                fused = e.fused;
+                if (fused) fp = e.fp;
+            }
+        }
+        if (!hit) {
+            fused = tensor_map_encoder() && plan_ffn(fp, M, H, I, *d);
+            if (fused) fused = fp.nc == 2 ? ffn_two_per_sm<2>(fp.smem) : ffn_two_per_sm<1>(fp.smem);
+            if (fused) {
+                fused = encode_tile_maps(&fp.p.a.wmap[0], &fp.p.a.smap[0], w[0], s[0], I, H, fp.nc) &&
+                        encode_tile_maps(&fp.p.a.wmap[1], &fp.p.a.smap[1], w[1], s[1], I, H, fp.nc) &&
+                        encode_tile_maps(&fp.p.b.wmap[0], &fp.p.b.smap[0], w[2], s[2], H, I, fp.nc);
+                fp.p.b.wmap[1] = fp.p.b.wmap[0];
+                fp.p.b.smap[1] = fp.p.b.smap[0];
+            }
+            std::lock_guard<std::mutex> lk(g_mu);
+            FfnEntry& e = g_ffn_cache[slot];
+            e.key = key;
+            e.used = true;
+            e.fused = fused;
+            e.fp = fp;
+        }
+    }
+    if (fused) {
+        TileParams& a = fp.p.a;
+        TileParams& b = fp.p.b;
+        a.x = x;
+        a.y = h;
+        a.g[0] = g[0];
+        a.g[1] = g[1];
+        a.ldy = I;
+        a.clamp = clamp;
+        a.out_bf16 = 1;
+        b.x = h;
+        b.y = y;
+        b.g[0] = b.g[1] = g[2];
+        b.ldy = H;
+        b.out_bf16 = y_type == NVFP4_OUT_BF16;
+        a.force_f32 = b.force_f32 = g_variant == 2;
+        a.wait_ns = b.wait_ns = g_wait_ns;
+        fp.p.sync = static_cast<uint32_t*>(workspace);
+        if (NVFP4_PHASE_TRACE) {
+            std::lock_guard<std::mutex> lk(g_mu);
+            a.trace_slot = g_trace_next;
+            g_trace_next = (g_trace_next + 1) % kTraceLaunches;
+        }
+        const cudaError_t e = fp.nc == 2 ? launch_ffn_nc<2>(fp, st) : launch_ffn_nc<1>(fp, st);
+        if (e != cudaSuccess) return cuda_fail(e);
+        const cudaError_t e2 = cudaGetLastError();
+        return e2 == cudaSuccess ? NVFP4_OK : cuda_fail(e2);
+    }
+    const uint8_t* wgu[2] = {w[0], w[1]};
+    const uint8_t* sgu[2] = {s[0], s[1]};
+    const float ggu[2] = {g[0], g[1]};
+    nvfp4_status r = run_dense(wgu, sgu, ggu, 2, x, h, NVFP4_OUT_BF16, M, I, H, st, true, clamp);
+    if (r != NVFP4_OK) return r;
+    const uint8_t* wd[1] = {w[2]};
+    const uint8_t* sd[1] = {s[2]};
+    const float gd[1] = {g[2]};
+    return run_dense(wd, sd, gd, 1, h, y, y_type, M, H, I, st);
+}
+
 }  // namespace nvfp4
 
 using namespace nvfp4;
@@ -4022,6 +4797,22 @@ nvfp4_status nvfp4_gemv_gate_up_swiglu(const uint8_t* w_gate, const uint8_t* s_g
     const uint8_t* s[2] = {s_gate, s_up};
     const float g[2] = {g_gate, g_up};
     return run_dense(w, s, g, 2, x, y, y_type, M, N, K, static_cast<cudaStream_t>(stream), true, clamp_limit);
+}
+
+int64_t nvfp4_ffn_workspace_bytes(int M, int I) {
+    if (M < 0 || M > 8 || I < 0) return -1;
+    return ffn_workspace_bytes(M, I);
+}
+
+nvfp4_status nvfp4_ffn_swiglu(const uint8_t* w_gate, const uint8_t* s_gate, float g_gate,
+                              const uint8_t* w_up, const uint8_t* s_up, float g_up,
+                              const uint8_t* w_down, const uint8_t* s_down, float g_down,
+                              const uint16_t* x, float clamp_limit, void* workspace,
+                              void* y, nvfp4_out_t y_type, int M, int H, int I, void* stream) {
+    const uint8_t* w[3] = {w_gate, w_up, w_down};
+    const uint8_t* s[3] = {s_gate, s_up, s_down};
+    const float g[3] = {g_gate, g_up, g_down};
+    return run_ffn(w, s, g, x, clamp_limit, workspace, y, y_type, M, H, I, static_cast<cudaStream_t>(stream));
 }
 
 nvfp4_status nvfp4_moe_gemv(const uint8_t* w_packed, const uint8_t* w_scales,
@@ -4223,6 +5014,20 @@ int describe_plan_on(const DeviceInfo* d, bool host_only, int kind, int M, int N
         return snprintf(buf, buflen, "simple grid=%lld block=%d smem=0 split=1 rows_per_item=0 k_warps=0",
                         static_cast<long long>((static_cast<int64_t>(slots) * N + 7) / 8), kSimpleThreads);
     }
+    if (kind == 8) {  // the FFN block (N = H, K = I): one fused launch, else gate/up + activation, then down
+        FfnPlan fp{};
+        if (N % 16 == 0 && K % 16 == 0 && plan_ffn(fp, M, N, K, *d) &&
+            (host_only || (fp.nc == 2 ? ffn_two_per_sm<2>(fp.smem) : ffn_two_per_sm<1>(fp.smem))))
+            return snprintf(buf, buflen,
+                            "ffn_fused grid=%d block=%d smem=%u split=1 rows_per_item=%d k_warps=%d mt=%d stages=%d "
+                            "nc=%d down_rows_per_item=%d down_k_warps=%d",
+                            fp.grid, tk::kThreads, fp.smem, fp.p.a.tpi * 16, 1 << fp.p.a.ksplit_log2, M,
+                            fp.p.a.stages, fp.nc, fp.p.b.tpi * 16, 1 << fp.p.b.ksplit_log2);
+        char a[200], b[200];
+        describe_plan_on(d, host_only, 4, M, K, N, 0, 0, a, sizeof a);
+        describe_plan_on(d, host_only, 0, M, N, K, 0, 0, b, sizeof b);
+        return snprintf(buf, buflen, "ffn_two_launch gate_up=[%s] down=[%s]", a, b);
+    }
     if (kind == 4) {  // gate/up with the fused activation: the tile kernel, else the byte-load kernel
         TilePlan tpl{};
         if (plan_tile(tpl, M, N, K, 2, *d, w, w, fake, false, 0, 0, true, !host_only))
@@ -4287,7 +5092,7 @@ int nvfp4_describe_plan(int kind, int M, int N, int K, int T, int top_k, char* b
 int nvfp4_describe_plan_host(int sm_count, int smem_optin, int smem_per_sm, int kind, int M, int N, int K, int T,
                              int top_k, char* buf, int buflen) {
     if (!buf || buflen < 1 || sm_count < 1 || smem_optin < 1 || smem_per_sm < smem_optin) return -1;
-    if (kind < 0 || kind > 7) return -1;
+    if (kind < 0 || kind > 8) return -1;
     DeviceInfo d;
     d.sm_count = sm_count;
     d.smem_optin = smem_optin;

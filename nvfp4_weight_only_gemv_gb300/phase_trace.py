@@ -2,8 +2,8 @@
 
     python -m nvfp4_weight_only_gemv_gb300.phase_trace [--steps S] [--no-pdl] CALL [CALL ...]
 
-CALL is ``dense:N:K:M[:bf16]``, ``gate_up:N:K:M``, ``swiglu:N:K:M`` or ``moe:E:N:K:T:TOPK:XPS``
-(XPS 1: one x row per slot). The library is rebuilt with ``-DNVFP4_PHASE_TRACE=1`` into its own
+CALL is ``dense:N:K:M[:bf16]``, ``gate_up:N:K:M``, ``swiglu:N:K:M``, ``ffn:H:I:M`` (the FFN block
+in one call) or ``moe:E:N:K:T:TOPK:XPS`` (XPS 1: one x row per slot). The library is rebuilt with ``-DNVFP4_PHASE_TRACE=1`` into its own
 file and loaded instead of the normal build. The calls of a step run back to back behind a
 sleep kernel, as bench.py times them, with weight copies rotating through more than twice the
 L2, for a few warm-up steps and then S traced steps (S * calls <= 16, the trace's launch slots).
@@ -32,7 +32,7 @@ PHASES = ["entry", "issued", "dep_wait", "x_staged", "first_box", "loop_done", "
 def parse_call(spec: str):
     f = spec.split(":")
     kind = f[0]
-    if kind in ("dense", "gate_up", "swiglu"):
+    if kind in ("dense", "gate_up", "swiglu", "ffn"):
         N, K, M = (int(v) for v in f[1:4])
         bf16 = len(f) > 4 and f[4] == "bf16"
         return {"kind": kind, "N": N, "K": K, "M": M, "bf16": bf16}
@@ -49,6 +49,8 @@ def make_sets(c, copies, seed, dev):
         base = synth.dense_problem(c["N"], c["K"], c["M"], seed, device=dev)
     elif c["kind"] in ("gate_up", "swiglu"):
         base = synth.gate_up_problem(c["N"], c["K"], c["M"], seed, device=dev)
+    elif c["kind"] == "ffn":
+        base = synth.ffn_problem(c["N"], c["K"], c["M"], seed, device=dev)
     else:
         base = synth.moe_problem(c["E"], c["N"], c["K"], c["T"], c["top_k"], c["xps"], seed=seed, device=dev,
                                   fill="all")
@@ -58,6 +60,9 @@ def make_sets(c, copies, seed, dev):
         if c["kind"] == "moe" and i > 0:
             d = dict(sets[0])
             d["ids"] = synth.routing(c["T"], c["top_k"], c["E"], seed * 7919 + i).to(dev)
+        if c["kind"] == "ffn":
+            import nvfp4_weight_only_gemv_gb300 as nv
+            d["ws"] = nv.ffn_workspace(c["M"], c["K"], dev)
         sets.append(d)
     return sets
 
@@ -66,6 +71,8 @@ def weight_bytes(c, d):
     per_row = c["K"] * 0.5 + c["K"] / 16
     if c["kind"] in ("gate_up", "swiglu"):
         return 2 * c["N"] * per_row
+    if c["kind"] == "ffn":
+        return 3 * c["N"] * per_row  # gate and up [I, H], down [H, I]: 3 * H * I weights
     if c["kind"] == "moe":
         return len(set(d["ids"].tolist())) * c["N"] * per_row
     return c["N"] * per_row
@@ -77,6 +84,8 @@ def alg_bytes(c, d):
         slots = c["T"] * c["top_k"]
         xr = slots if c["xps"] else c["T"]
         return weight_bytes(c, d) + xr * c["K"] * 2 + slots * c["N"] * ob
+    if c["kind"] == "ffn":  # x [M, H] in, y [M, H] out (h stays inside the call)
+        return weight_bytes(c, d) + c["M"] * c["N"] * (2 + ob)
     cols = c["N"] * (2 if c["kind"] == "gate_up" else 1)
     return weight_bytes(c, d) + c["M"] * c["K"] * 2 + c["M"] * cols * ob
 
@@ -91,6 +100,9 @@ def launch(nv, c, d, x=None):
         return nv.gemv_gate_up(d["wg"], d["sg"], d["gg"], d["wu"], d["su"], d["gu"], x, out_dtype=dt)
     if c["kind"] == "swiglu":
         return nv.gemv_gate_up_swiglu(d["wg"], d["sg"], d["gg"], d["wu"], d["su"], d["gu"], x, 10.0, out_dtype=dt)
+    if c["kind"] == "ffn":
+        return nv.ffn_swiglu(d["wg"], d["sg"], d["gg"], d["wu"], d["su"], d["gu"], d["wd"], d["sd"], d["gd"], x,
+                             10.0, workspace=d["ws"], out_dtype=dt)
     return nv.moe_gemv(d["w"], d["s"], d["gs"], d["ids"], x, c["xps"], c["top_k"], out_dtype=dt)
 
 
@@ -157,6 +169,23 @@ def summarise(tr, launches, calls_meta):
             d = np.where(ok, a - xs, np.nan)
             return f"{np.nanmedian(d) / 1e3:.2f}/{np.nanmax(d) / 1e3:.2f}" if ok.any() else "-"
         lines.append(f"{calls_meta[l][0]:<28}{stat(first):>38}{stat(loop):>40}")
+    # the FFN block's own phases: gate/up done (phase 5), past the grid barrier (word 38), h staged
+    # (word 39), down done (phase 6)
+    ffn = [l for l in range(launches) if calls_meta[l][0].startswith("ffn")]
+    if ffn:
+        lines.append("")
+        lines.append(f"{'launch':<28}" + "".join(f"{h:>20}" for h in
+                                                 ("x_staged->gu_done", "gu_done->barrier", "barrier->h_staged",
+                                                  "h_staged->down_done", "barrier last-first")))
+        for l in ffn:
+            rows = tr[l][tr[l, :, 0] > 0]
+            def dd(a, b):
+                ok = (a > 0) & (b > 0)
+                return f"{np.median(b[ok] - a[ok]) / 1e3:.2f}" if ok.any() else "-"
+            bar = rows[:, 38][rows[:, 38] > 0]
+            spread = f"{(bar.max() - bar.min()) / 1e3:.2f}" if len(bar) else "-"
+            lines.append(f"{calls_meta[l][0]:<28}{dd(rows[:, 6], rows[:, 10]):>20}{dd(rows[:, 10], rows[:, 38]):>20}"
+                         f"{dd(rows[:, 38], rows[:, 39]):>20}{dd(rows[:, 39], rows[:, 12]):>20}{spread:>20}")
     return lines
 
 
@@ -190,7 +219,7 @@ def main(argv=None):
     l2 = getattr(props, "L2_cache_size", 128 << 20) or (128 << 20)
     step_w = 0
     for c in calls:
-        rows = c["N"] * (2 if c["kind"] in ("gate_up", "swiglu") else 1)
+        rows = c["N"] * {"gate_up": 2, "swiglu": 2, "ffn": 3}.get(c["kind"], 1)
         step_w += 0 if c["kind"] == "moe" else rows * c["K"] * 9 // 16
     copies = max(steps + 1, math.ceil(2.5 * l2 / step_w)) if step_w else 4
     sets = [make_sets(c, copies, 11 + i, dev) for i, c in enumerate(calls)]

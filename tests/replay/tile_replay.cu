@@ -90,6 +90,8 @@ static void check_bulk(const TileParams& p, int slices, int rows, int kn_max, in
 }
 
 // A per-item plan (gemv_tile_kernel): layout, partitions, lane indexes, bank conflicts.
+static void check_walk(const TilePlan& tp, int M, int K, int groups);
+
 static void check_items(const TilePlan& tp, int M, int K, int groups) {
     const TileParams& p = tp.p;
     const int ksplit = 1 << p.ksplit_log2, S = 1 << p.s_log2;
@@ -102,6 +104,14 @@ static void check_items(const TilePlan& tp, int M, int K, int groups) {
     CHECK(p.misc_off >= p.cpart_off + (S > 1 ? 8192u : 0u), "misc_off");
     CHECK(p.bar_off >= p.misc_off + 256 + 8 * 128 && p.bar_off % 8 == 0, "bar_off");
     CHECK(p.bar_off + 8 * 4 * 8 + 1024 <= tp.smem, "total");
+    check_walk(tp, M, K, groups);
+}
+
+// The partition and index checks of a per-item plan, whatever its shared-memory layout.
+static void check_walk(const TilePlan& tp, int M, int K, int groups) {
+    const TileParams& p = tp.p;
+    const int ksplit = 1 << p.ksplit_log2, S = 1 << p.s_log2;
+    const uint32_t kWBox = tp.nc * 2048, kSBox = tp.nc * 256;
     CHECK(p.sstride % 128 == 64, "sstride");
     CHECK(p.stages >= 2 && p.stages <= 4, "stages");
     CHECK(p.nbox * tp.nc * 256 == K, "nbox");
@@ -117,7 +127,7 @@ static void check_items(const TilePlan& tp, int M, int K, int groups) {
     std::vector<int> seen(items, 0);
     for (int u = 0; u < units; ++u) {
         const int ib = u * p.items_q + std::min(u, p.items_r), ie = ib + p.items_q + (u < p.items_r ? 1 : 0);
-        CHECK(ib >= 0 && ie <= items && ib < ie, "unit range");
+        CHECK(ib >= 0 && ie <= items && (ib < ie || items < units), "unit range");  // (fused FFN: idle units)
         for (int i = ib; i < ie; ++i) seen[i]++;
         int grp = ib / p.ipg, t = ib - grp * p.ipg;
         for (int it = ib; it < ie; ++it) {
@@ -180,14 +190,16 @@ static void check_items(const TilePlan& tp, int M, int K, int groups) {
 }
 
 // Fused gate/up: gate tile j and up tile j form tiles 2j, 2j + 1 of one item.
-static void check_swiglu(const TilePlan& tp, int M, int N) {
+static void check_swiglu(const TilePlan& tp, int M, int N, bool separate_layout = true) {
     const TileParams& p = tp.p;
     const int ksplit = 1 << p.ksplit_log2, S = 1 << p.s_log2;
     const int rt = (N + 15) / 16;
     CHECK(p.tiles == 2 * rt, "tiles %d", p.tiles);
     CHECK(p.tpi % 2 == 0, "tiles per item %d", p.tpi);
-    CHECK(p.misc_off >= p.cpart_off + 8192u, "partial sums allocated");
-    CHECK(p.cpart_off >= p.red_off + (ksplit > 1 ? 8192u : 0u), "partial sums after the reduction buffer");
+    if (separate_layout) {
+        CHECK(p.misc_off >= p.cpart_off + 8192u, "partial sums allocated");
+        CHECK(p.cpart_off >= p.red_off + (ksplit > 1 ? 8192u : 0u), "partial sums after the reduction buffer");
+    }
     const int units = tp.grid_x / S;
     std::vector<int> rows(N, 0);
     for (int u = 0; u < units; ++u) {
@@ -429,6 +441,117 @@ static void check_moe_groups_big(int slots, int E, int top_k, bool per_slot, uns
     for (int s = 0; s < slots; ++s) CHECK(seen[s] == (sid[s] >= 0 ? 1 : 0), "big slot %d seen %d", s, seen[s]);
 }
 
+// The fused FFN launch: both phases share the ring; A's x slices and pair buffer and B's h
+// slices share the x region; each phase's indexes pass the per-item checks; A's round-robin and
+// B's reversed round-robin item deals cover every item exactly once; the readiness counts add up
+// (every A item counts into the B slice holding its h rows, and each slice expects exactly the
+// items it gets); and the issue order (A's boxes, then B's, skipping tiles past the end) is
+// exactly the order in which the phases consume them.
+static void check_ffn(const FfnPlan& fp, int M, int H, int I) {
+    const TileParams& A = fp.p.a;
+    const TileParams& B = fp.p.b;
+    const int nc = fp.nc, st = A.stages;
+    const int ka = 1 << A.ksplit_log2, kb = 1 << B.ksplit_log2;
+    CHECK(fp.grid == 2 * kSms, "grid %d", fp.grid);
+    CHECK(A.s_log2 == 0 && B.s_log2 == 0 && A.stages == B.stages, "one ring, no clusters");
+    for (uint32_t TileParams::*f : {&TileParams::ring_w, &TileParams::ring_s, &TileParams::x_off, &TileParams::red_off,
+                                    &TileParams::cpart_off, &TileParams::misc_off, &TileParams::bar_off})
+        CHECK(A.*f == B.*f, "shared layout");
+    CHECK(A.ring_s == A.ring_w + 8u * st * nc * 2048 && A.x_off == A.ring_s + 8u * st * nc * 256, "rings");
+    CHECK(A.x_off % 128 == 0 && A.cpart_off % 128 == 0, "x region alignment");
+    CHECK(A.cpart_off >= A.x_off + (uint32_t)(ka * M) * A.sstride, "A's x slices before its pair buffer");
+    CHECK(A.red_off >= A.cpart_off + 8192u, "pair buffer inside the x region");
+    CHECK(A.red_off >= A.x_off + (uint32_t)(kb * M) * B.sstride, "B's h slices inside the x region");
+    CHECK(A.misc_off >= A.red_off + ((ka > 1 || kb > 1) ? 8192u : 0u), "reduction buffer");
+    CHECK(A.bar_off >= A.misc_off + 256 + 8 * 128 && A.bar_off % 8 == 0, "bar_off");
+    CHECK(A.bar_off + 8 * 4 * 8 + 1024 <= fp.smem && fp.smem <= (uint32_t)(kPerSm / 2 - 1024), "two CTAs per SM");
+    CHECK(A.M == M && B.M == M && A.K == H && A.N == I && B.K == I && B.N == H && A.swiglu == 1, "shapes");
+    CHECK(kb <= kFfnSlices && 32 * (1 + kFfnSlices) * 4 <= kFfnSyncBytes, "counters inside the workspace header");
+    TilePlan ta{}, tb{};
+    ta.p = A; ta.nc = nc; ta.grid_x = fp.grid; ta.grid_y = 1; ta.smem = fp.smem;
+    tb.p = B; tb.nc = nc; tb.grid_x = fp.grid; tb.grid_y = 1; tb.smem = fp.smem;
+    check_walk(ta, M, H, 1);
+    check_swiglu(ta, M, I, false);
+    check_walk(tb, M, I, 1);
+    const int units = fp.grid;
+    // the deals: every item of each phase on exactly one CTA
+    for (int ph = 0; ph < 2; ++ph) {
+        const TileParams& q = ph ? B : A;
+        const int items = q.items_q * units + q.items_r;
+        std::vector<int> seen(items, 0);
+        for (int u = 0; u < units; ++u) {
+            const FfnGeo g = ffn_geo(q, 0, u, units, ph == 1);
+            for (int j = 0; j < g.count; ++j) {
+                const int it = g.first + j * g.stride;
+                CHECK(it >= 0 && it < items, "phase %d item %d", ph, it);
+                if (it >= 0 && it < items) seen[it]++;
+            }
+        }
+        for (int i = 0; i < items; ++i) CHECK(seen[i] == 1, "phase %d item %d dealt %d times", ph, i, seen[i]);
+    }
+    // readiness counts: A items per B slice, as counted and as expected
+    {
+        const int items_a = A.items_q * units + A.items_r;
+        std::vector<int> got(kb, 0);
+        for (int it = 0; it < items_a; ++it) {
+            if (!(2 * it * (A.tpi >> 1) < A.tiles)) continue;
+            const int r0 = it * ffn_item_rows(A);
+            const int s = ffn_slice_of(B, r0, nc);
+            CHECK(s >= 0 && s < kb && ffn_slice_lo(B, s, nc) <= r0 && r0 < ffn_slice_lo(B, s + 1, nc), "slice of row %d", r0);
+            CHECK(r0 + ffn_item_rows(A) <= ffn_slice_lo(B, s + 1, nc) || r0 + ffn_item_rows(A) > I,
+                  "item %d straddles slices", it);
+            if (s >= 0 && s < kb) got[s]++;
+        }
+        for (int s = 0; s < kb; ++s) CHECK(got[s] == ffn_slice_items(A, B, s, nc), "slice %d counts %d, expects %d", s,
+                                           got[s], ffn_slice_items(A, B, s, nc));
+        for (int w = 0; w < 8; ++w) {
+            const FfnGeo g = ffn_geo(B, w, 0, units, true);
+            CHECK(ffn_slice_lo(B, g.kslice, nc) == g.b_lo * nc * 256 &&
+                  ffn_slice_lo(B, g.kslice + 1, nc) == (g.b_lo + g.nb) * nc * 256, "warp %d slice bounds", w);
+        }
+    }
+    // issue order against consumption order, per CTA and warp
+    for (int unit = 0; unit < units; unit += (unit < 8 || unit > units - 8) ? 1 : 13) {
+        for (int warp = 0; warp < 8; ++warp) {
+            const FfnGeo ga = ffn_geo(A, warp, unit, units, false), gb = ffn_geo(B, warp, unit, units, true);
+            std::vector<std::array<int, 3>> cons, iss;
+            for (int ph = 0; ph < 2; ++ph) {
+                const TileParams& q = ph ? B : A;
+                const FfnGeo& g = ph ? gb : ga;
+                for (int j = 0; j < g.count; ++j) {
+                    const int tile = (g.first + j * g.stride) * q.tpi + g.tin;
+                    if (tile < q.tiles)
+                        for (int b = 0; b < g.nb; ++b) cons.push_back({ph, tile, g.b_lo + b});
+                }
+            }
+            int iph = 0, jj = 0, box = 0;
+            for (int guard = 0; guard < 1000000; ++guard) {
+                bool done = false;
+                for (;;) {
+                    if (iph == 2) { done = true; break; }
+                    const bool pa = iph == 0;
+                    const FfnGeo& g = pa ? ga : gb;
+                    const int tpi = pa ? A.tpi : B.tpi, tiles = pa ? A.tiles : B.tiles;
+                    while (jj < g.count && (box >= g.nb || (g.first + jj * g.stride) * tpi + g.tin >= tiles)) {
+                        ++jj;
+                        box = 0;
+                    }
+                    if (jj < g.count) break;
+                    iph = pa ? 1 : 2;
+                    jj = 0;
+                    box = 0;
+                }
+                if (done) break;
+                const TileParams& q = iph ? B : A;
+                const FfnGeo& g = iph ? gb : ga;
+                iss.push_back({iph, (g.first + jj * g.stride) * q.tpi + g.tin, g.b_lo + box});
+                ++box;
+            }
+            CHECK(iss == cons, "unit %d warp %d: %zu boxes issued, %zu consumed", unit, warp, iss.size(), cons.size());
+        }
+    }
+}
+
 int main() {
     DeviceInfo d;
     d.sm_count = kSms;
@@ -520,7 +643,18 @@ int main() {
             }
         }
     }
-    printf("per-item plans %d, fused gate/up plans %d, MoE plans %d, group-aligned %d, large MoE plans %d, fails %d\n",
-           n_items, n_sw, n_moe, n_aligned, n_big, fails);
+    // the FFN block in one launch: {H, I}
+    int n_ffn = 0;
+    for (const auto& f : std::vector<std::array<int, 2>>{{4096, 12288}, {4096, 1536}, {1024, 512}, {256, 256},
+                                                         {2048, 768}, {4096, 4096}, {768, 3072}})
+        for (int M = 1; M <= 8; ++M) {
+            FfnPlan fp{};
+            if (!plan_ffn(fp, M, f[0], f[1], d)) continue;
+            check_ffn(fp, M, f[0], f[1]);
+            ++n_ffn;
+        }
+    printf("per-item plans %d, fused gate/up plans %d, MoE plans %d, group-aligned %d, large MoE plans %d, "
+           "FFN plans %d, fails %d\n",
+           n_items, n_sw, n_moe, n_aligned, n_big, n_ffn, fails);
     return fails != 0;
 }
