@@ -152,6 +152,27 @@ nvfp4_status nvfp4_ffn_swiglu(const uint8_t* w_gate, const uint8_t* s_gate, floa
 int64_t nvfp4_ffn_workspace_bytes(int M, int I);
 
 /*
+ * nvfp4_ffn_swiglu without a caller workspace: the same operation and arguments, with the
+ * workspace taken from a 256 KB array in the library's own device memory (one per device and
+ * process), so the call allocates nothing and needs nothing allocated by the caller. This entry
+ * point has no counterpart in the source pages: it is for callers that cannot provide a workspace,
+ * such as a C caller with no device allocator of its own, or one whose allocator must not run on
+ * its decode path.
+ *   Limit: nvfp4_ffn_workspace_bytes(M, I) <= 262144 (M * I <= 130048: M = 8 at I = 12288);
+ *   larger returns NVFP4_ERR_UNSUPPORTED before anything is enqueued.
+ *   Set-up: the first call on a device looks the array up (cudaGetSymbolAddress) and zeroes its
+ *   counters on `stream`; make that first call before any stream capture on the device.
+ *   Races: every call on a device uses the same array, so calls must not overlap in time (keep
+ *   them on one stream, or order them with events); overlapping calls corrupt each other's h and
+ *   counters.
+ */
+nvfp4_status nvfp4_ffn_swiglu_static(const uint8_t* w_gate, const uint8_t* s_gate, float g_gate,
+                                     const uint8_t* w_up, const uint8_t* s_up, float g_up,
+                                     const uint8_t* w_down, const uint8_t* s_down, float g_down,
+                                     const uint16_t* x, float clamp_limit, void* y, nvfp4_out_t y_type,
+                                     int M, int H, int I, void* stream);
+
+/*
  * Routed-expert GEMV over slots (w4a16_gemv_sw_moe, "glm-5.3-flash-nvfp4-tp3-512k--gb10
  * card.json" performance[33]: routed gate or up, 8 slots). For slot s = t*top_k + j
  * (token-major), with e = expert_ids[s]:

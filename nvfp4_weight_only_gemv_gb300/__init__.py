@@ -21,7 +21,8 @@ import torch
 
 from . import build as _build
 
-__all__ = ["gemv", "gemv_gate_up", "gemv_gate_up_swiglu", "ffn_swiglu", "ffn_workspace", "ffn_workspace_bytes",
+__all__ = ["gemv", "gemv_gate_up", "gemv_gate_up_swiglu", "ffn_swiglu", "ffn_swiglu_static", "ffn_workspace",
+           "ffn_workspace_bytes",
            "moe_gemv", "gemv_sdict", "moe_gemv_sdict",
            "sdict_plane_bytes", "sdict_encode", "device_status", "set_wait_budget_ns",
            "set_variant", "set_pdl", "fp32_fallbacks", "phase_trace", "describe_plan", "describe_plan_host", "library", "library_path", "NVFP4Error",
@@ -62,6 +63,9 @@ def _declare(lib):
     lib.nvfp4_ffn_swiglu.argtypes = [u8p, u8p, ctypes.c_float, u8p, u8p, ctypes.c_float, u8p, u8p, ctypes.c_float,
                                      u16p, ctypes.c_float, vp, vp, i32, i32, i32, i32, vp]
     lib.nvfp4_ffn_swiglu.restype = i32
+    lib.nvfp4_ffn_swiglu_static.argtypes = [u8p, u8p, ctypes.c_float, u8p, u8p, ctypes.c_float, u8p, u8p,
+                                            ctypes.c_float, u16p, ctypes.c_float, vp, i32, i32, i32, i32, vp]
+    lib.nvfp4_ffn_swiglu_static.restype = i32
     lib.nvfp4_ffn_workspace_bytes.argtypes = [i32, i32]
     lib.nvfp4_ffn_workspace_bytes.restype = ctypes.c_int64
     lib.nvfp4_gemv_gate_up_swiglu.restype = i32
@@ -292,6 +296,31 @@ def ffn_swiglu(wg, sg, gg, wu, su, gu, wd, sd, gd, x, clamp_limit: float = float
                                     _ptr(sd), float(gd), _ptr(x), float(clamp_limit), _ptr(workspace), _ptr(y),
                                     _out_code(y.dtype), M, H, I, ctypes.c_void_p(_stream(stream)))
     _check(st, "nvfp4_ffn_swiglu")
+    return y
+
+
+def ffn_swiglu_static(wg, sg, gg, wu, su, gu, wd, sd, gd, x, clamp_limit: float = float("inf"), out=None,
+                      out_dtype=torch.float32, stream=None) -> torch.Tensor:
+    """ffn_swiglu with the library's own 256 KB device array as the workspace (nothing allocated
+    by the caller). Calls on a device share that array: they must not overlap in time."""
+    for t, n in ((wg, "w_gate"), (wu, "w_up"), (wd, "w_down")):
+        _need(t, n, torch.uint8, 2)
+    for t, n in ((sg, "s_gate"), (su, "s_up"), (sd, "s_down")):
+        _need(t, n, torch.uint8, 2)
+    _need(x, "x", torch.bfloat16, 2)
+    I, H = wg.shape[0], wg.shape[1] * 2
+    M = x.shape[0]
+    if tuple(wu.shape) != tuple(wg.shape) or tuple(sg.shape) != (I, H // 16) or \
+            tuple(su.shape) != (I, H // 16) or x.shape[1] != H:
+        raise ValueError("shape mismatch between gate, up and x")
+    if tuple(wd.shape) != (H, I // 2) or tuple(sd.shape) != (H, I // 16):
+        raise ValueError("down weight must be [H, I/2] with scales [H, I/16]")
+    y = _out(out, (M, H), out_dtype, x.device)
+    _one_device(wg, sg, wu, su, wd, sd, x, y)
+    st = library().nvfp4_ffn_swiglu_static(_ptr(wg), _ptr(sg), float(gg), _ptr(wu), _ptr(su), float(gu), _ptr(wd),
+                                           _ptr(sd), float(gd), _ptr(x), float(clamp_limit), _ptr(y),
+                                           _out_code(y.dtype), M, H, I, ctypes.c_void_p(_stream(stream)))
+    _check(st, "nvfp4_ffn_swiglu_static")
     return y
 
 

@@ -4715,6 +4715,31 @@ nvfp4_status run_ffn(const uint8_t* const* w, const uint8_t* const* s, const flo
     return run_dense(wd, sd, gd, 1, h, y, y_type, M, H, I, st);
 }
 
+// ------------------------------------------------------------------ the FFN block without a caller workspace
+
+// The FFN block's workspace as a file-scope device array, for callers that cannot hand the
+// library a workspace: a C caller with no device allocator of its own, or one whose allocator
+// must not run on its decode path. 256 KB holds the counters and h up to M * I = 130048 (M = 8 at
+// I = 12288). One array per device and process: calls that overlap in time (other streams, other
+// host threads without ordering) share it and corrupt each other's h and counters.
+constexpr int64_t kFfnStaticScratchBytes = 256ll << 10;
+static __device__ __align__(256) uint8_t g_ffn_scratch[kFfnStaticScratchBytes];
+
+// The array's device address on the current device, looked up once per device; the first lookup
+// also zeroes the counters on `st` (the array is zero at load; this makes it explicit).
+void* ffn_static_scratch(int dev, cudaStream_t st) {
+    static void* addr[64] = {};
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (dev < 0 || dev >= 64) return nullptr;
+    if (!addr[dev]) {
+        void* a = nullptr;
+        if (cudaGetSymbolAddress(&a, g_ffn_scratch) != cudaSuccess) return nullptr;
+        if (cudaMemsetAsync(a, 0, kFfnSyncBytes, st) != cudaSuccess) return nullptr;
+        addr[dev] = a;
+    }
+    return addr[dev];
+}
+
 }  // namespace nvfp4
 
 using namespace nvfp4;
@@ -4813,6 +4838,22 @@ nvfp4_status nvfp4_ffn_swiglu(const uint8_t* w_gate, const uint8_t* s_gate, floa
     const uint8_t* s[3] = {s_gate, s_up, s_down};
     const float g[3] = {g_gate, g_up, g_down};
     return run_ffn(w, s, g, x, clamp_limit, workspace, y, y_type, M, H, I, static_cast<cudaStream_t>(stream));
+}
+
+nvfp4_status nvfp4_ffn_swiglu_static(const uint8_t* w_gate, const uint8_t* s_gate, float g_gate,
+                                     const uint8_t* w_up, const uint8_t* s_up, float g_up,
+                                     const uint8_t* w_down, const uint8_t* s_down, float g_down,
+                                     const uint16_t* x, float clamp_limit, void* y, nvfp4_out_t y_type,
+                                     int M, int H, int I, void* stream) {
+    if (M < 0 || M > 8 || I < 0) return NVFP4_ERR_SHAPE;
+    if (ffn_workspace_bytes(M, I) > kFfnStaticScratchBytes) return NVFP4_ERR_UNSUPPORTED;
+    int dev = 0;
+    const cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    void* ws = ffn_static_scratch(dev, static_cast<cudaStream_t>(stream));
+    if (!ws) return cuda_fail(cudaGetLastError());
+    return nvfp4_ffn_swiglu(w_gate, s_gate, g_gate, w_up, s_up, g_up, w_down, s_down, g_down, x, clamp_limit, ws, y,
+                            y_type, M, H, I, stream);
 }
 
 nvfp4_status nvfp4_moe_gemv(const uint8_t* w_packed, const uint8_t* w_scales,
