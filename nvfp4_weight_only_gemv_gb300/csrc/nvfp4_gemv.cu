@@ -3084,7 +3084,7 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_sk_kernel(const __g
         }
         if (tid == 0) trace_word(p.trace_slot, 36, static_cast<unsigned long long>(clock64()));
         if (lane == 0)
-            for (int s = 0; s < NVFP4_MOE_EARLY; ++s) issue_next();
+            for (int s = 0; s < min(stages, NVFP4_MOE_EARLY); ++s) issue_next();
     }
 
     // x, all of K, staged by all eight warps
@@ -3109,7 +3109,7 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_sk_kernel(const __g
     if (tid == 0) trace_phase(p.trace_slot, 3);
     if constexpr (MOE) {
         if (lane == 0)
-            for (int s = NVFP4_MOE_EARLY; s < stages; ++s) issue_next();
+            for (int s = min(stages, NVFP4_MOE_EARLY); s < stages; ++s) issue_next();
     }
     if (tid == 0) trace_word(p.trace_slot, 37, static_cast<unsigned long long>(clock64()));
     const bool use_f32 = lossy || p.force_f32 || x_overflow;
