@@ -169,14 +169,14 @@ def summarise(tr, launches, calls_meta):
             d = np.where(ok, a - xs, np.nan)
             return f"{np.nanmedian(d) / 1e3:.2f}/{np.nanmax(d) / 1e3:.2f}" if ok.any() else "-"
         lines.append(f"{calls_meta[l][0]:<28}{stat(first):>38}{stat(loop):>40}")
-    # the FFN block's own phases: gate/up done (phase 5), past the grid barrier (word 38), h staged
-    # (word 39), down done (phase 6)
+    # the FFN block's own phases (thread 0, so warp 0's K slice): gate/up done (phase 5), its
+    # slice of h complete (word 38), that slice staged (word 39), down done (phase 6)
     ffn = [l for l in range(launches) if calls_meta[l][0].startswith("ffn")]
     if ffn:
         lines.append("")
         lines.append(f"{'launch':<28}" + "".join(f"{h:>20}" for h in
-                                                 ("x_staged->gu_done", "gu_done->barrier", "barrier->h_staged",
-                                                  "h_staged->down_done", "barrier last-first")))
+                                                 ("x_staged->gu_done", "gu_done->slice_ready",
+                                                  "ready->h_staged", "h_staged->down_done", "ready last-first")))
         for l in ffn:
             rows = tr[l][tr[l, :, 0] > 0]
             def dd(a, b):
