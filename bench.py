@@ -70,6 +70,12 @@ WORKLOADS = {
                    [("gate_up_swiglu", 768, 4096, 2, 9, "bf16"), ("dense", 4096, 768, 2, 10, "bf16")]),
     "ffn_shared_fused": ("shared-expert FFN in one call (gate+up 2x768x4096, SwiGLU, bf16 h, down 4096x768), "
                          "M=2, bf16 out", [("ffn_block", 4096, 768, 2, 9, "bf16")]),
+    "card_m2": ("the card's W4A16 calls at decode: KDA in-proj N=8726,K=4096 M=2; KDA o_proj N=4096,K=2816 M=2; "
+                "shared gate|up N=768+768,K=4096 M=2; shared down N=4096,K=768 M=2 (bf16 out); routed gate or up, "
+                "8 slots of 288 experts, N=704,K=4096 (fp32 out)",
+                [("dense", 8726, 4096, 2, 11, "bf16"), ("dense", 4096, 2816, 2, 12, "bf16"),
+                 ("gate_up", 768, 4096, 2, 13, "bf16"), ("dense", 4096, 768, 2, 14, "bf16"),
+                 ("moe_gate_up", 704, 4096, 1, 15, "f32")]),
     "vocab": ("vocab head N=151936,K=4096,M=1, fp32 out", [("dense", 151936, 4096, 1, 7, "f32")]),
     "moe": ("routed experts: 288 experts, gate_up [3072,4096] then down [4096,1536], "
             "4 tokens x top-8, fp32 per-slot out",
@@ -414,15 +420,22 @@ class Call:
 def pool_copies(calls_spec, device):
     props = torch.cuda.get_device_properties(device)
     l2 = getattr(props, "L2_cache_size", 128 << 20) or (128 << 20)
-    per_step = 0
+    per_step, moe = 0, False
     for kind, N, K, M, *_ in calls_spec:
         rows = {"gate_up": 2 * N, "gate_up_swiglu": 2 * N, "ffn_block": 3 * N}.get(kind, N)
         if kind.startswith("moe"):
-            return 4, l2, ("routing rotates over 4 id sets; the distinct experts a step reads (counted in "
-                           "the algorithmic bytes) exceed 2x L2")
-        per_step += rows * K * 9 // 16
-    copies = max(1, math.ceil(2.5 * l2 / per_step))
-    return copies, l2, f"{copies} rotating weight copies ({copies * per_step / 1e6:.0f} MB > 2x L2 of {l2 / 1e6:.0f} MB)"
+            moe = True
+        else:
+            per_step += rows * K * 9 // 16
+    notes = []
+    copies = 4 if moe else 1
+    if per_step:
+        copies = max(copies, math.ceil(2.5 * l2 / per_step))
+        notes.append(f"{copies} rotating weight copies ({copies * per_step / 1e6:.0f} MB > 2x L2 of {l2 / 1e6:.0f} MB)")
+    if moe:
+        notes.append(f"routing rotates over {copies} id sets; the expert tensors (all experts, counted by the "
+                     "distinct experts a step reads) exceed 2x L2")
+    return copies, l2, "; ".join(notes)
 
 
 # ------------------------------------------------------------------ timing
@@ -714,7 +727,7 @@ def run_reference(args):
     return 0
 
 
-PER_WORKLOAD = ["attn", "ffn", "ffn_m2", "ffn_m4", "ffn_m8", "ffn_swiglu", "ffn_fused", "ffn_shared",
+PER_WORKLOAD = ["attn", "card_m2", "ffn", "ffn_m2", "ffn_m4", "ffn_m8", "ffn_swiglu", "ffn_fused", "ffn_shared",
                 "ffn_shared_fused", "moe", "moe_t32", "moe_sdict", "vocab_sdict"]
 
 
