@@ -544,16 +544,20 @@ def test_swiglu_k_not_multiple_of_256(N, K, M):
     assert_swiglu_parity(y, yr, aux, 2.0, f"swiglu {N}x{K}")
 
 
-def test_swiglu_matches_gate_up_then_activation():
-    # the fused call against the unfused gate_up output run through the same fp32 activation
+def test_swiglu_and_gate_up_agree_with_the_oracle_on_the_same_inputs():
+    # the fused call and the unfused gate_up call on the same weights and x, each against the
+    # oracle: gate_up against the oracle's gate and up (GEMV tolerance), the fused output against
+    # the oracle's activation of them (SwiGLU tolerance)
     p = synth.gate_up_problem(2048, 4096, 2, 660, device=DEV)
     yf = nv.gemv_gate_up_swiglu(p["wg"], p["sg"], p["gg"], p["wu"], p["su"], p["gu"], p["x"], 1.5,
                                 out_dtype=torch.float32)
     gu = nv.gemv_gate_up(p["wg"], p["sg"], p["gg"], p["wu"], p["su"], p["gu"], p["x"])
     torch.cuda.synchronize()
-    g, u = gu[:, :2048].double(), gu[:, 2048:].double()
-    ref = (torch.nn.functional.silu(g.clamp(-1.5, 1.5)) * u.clamp(-1.5, 1.5)).float()
-    assert torch.allclose(yf, ref, rtol=1e-5, atol=1e-5)
+    args = (host(p["wg"]), host(p["sg"]), p["gg"], host(p["wu"]), host(p["su"]), p["gu"], synth.bf16_bits(p["x"]))
+    yr, aux = oracle.gate_up_swiglu(*args, 1.5)
+    assert_parity(gu, np.concatenate([aux["gate"], aux["up"]], 1),
+                  np.concatenate([aux["gate_abs"], aux["up_abs"]], 1), "gate_up beside the fused call")
+    assert_swiglu_parity(yf, yr, aux, 1.5, "fused SwiGLU beside gate_up")
 
 
 def test_swiglu_nan_scale_and_empty_inputs():
