@@ -12,7 +12,8 @@
 //     and its in-place transpose of 16-byte chunks lands on the tensor-core order;
 //   * fused gate/up items hold whole gate/up tile pairs and write every output row once;
 //   * the stream-K combine stores every job exactly once with all of its boxes;
-//   * the MoE group building places every valid slot in exactly one group of its expert.
+//   * the MoE group building places every valid slot in exactly one group of its expert;
+//   * the same holds for a seeded random sweep of dense, gate/up and FFN-block shapes.
 // Prints "... fails N" and exits non-zero when any check fails.
 
 #include "../../nvfp4_weight_only_gemv_gb300/csrc/nvfp4_gemv.cu"
@@ -643,10 +644,36 @@ int main() {
             }
         }
     }
+    // a seeded random sweep of shapes: N up to 40000, K a multiple of 256 up to 16384, M 1..8
+    int n_rand = 0;
+    uint32_t rs = 12345u;
+    auto rnd = [&](uint32_t n) {
+        rs = rs * 1664525u + 1013904223u;
+        return (rs >> 8) % n;
+    };
+    for (int it = 0; it < 240; ++it) {
+        const int N = 1 + static_cast<int>(rnd(40000)), K = 256 * (1 + static_cast<int>(rnd(64))),
+                  M = 1 + static_cast<int>(rnd(8));
+        const int groups = 1 + static_cast<int>(rnd(2));
+        TilePlan tp{};
+        if (plan_tile(tp, M, N, K, groups, d, w, w, fake, false, 0, 0, false, false) && !tp.sk) {
+            check_items(tp, M, K, groups);
+            ++n_rand;
+        }
+        TilePlan ts{};
+        if (plan_tile(ts, M, N, K, 2, d, w, w, fake, false, 0, 0, true, false)) {
+            check_items(ts, M, K, 1);
+            check_swiglu(ts, M, N);
+            ++n_rand;
+        }
+    }
     // the FFN block in one launch: {H, I}
     int n_ffn = 0;
-    for (const auto& f : std::vector<std::array<int, 2>>{{4096, 12288}, {4096, 1536}, {1024, 512}, {256, 256},
-                                                         {2048, 768}, {4096, 4096}, {768, 3072}})
+    std::vector<std::array<int, 2>> ffn_shapes{{4096, 12288}, {4096, 1536}, {1024, 512}, {256, 256},
+                                               {2048, 768}, {4096, 4096}, {768, 3072}, {4096, 768}};
+    for (int it = 0; it < 40; ++it)
+        ffn_shapes.push_back({256 * (1 + static_cast<int>(rnd(16))), 256 * (1 + static_cast<int>(rnd(24)))});
+    for (const auto& f : ffn_shapes)
         for (int M = 1; M <= 8; ++M) {
             FfnPlan fp{};
             if (!plan_ffn(fp, M, f[0], f[1], d)) continue;
@@ -654,7 +681,7 @@ int main() {
             ++n_ffn;
         }
     printf("per-item plans %d, fused gate/up plans %d, MoE plans %d, group-aligned %d, large MoE plans %d, "
-           "FFN plans %d, fails %d\n",
-           n_items, n_sw, n_moe, n_aligned, n_big, n_ffn, fails);
+           "FFN plans %d, random plans %d, fails %d\n",
+           n_items, n_sw, n_moe, n_aligned, n_big, n_ffn, n_rand, fails);
     return fails != 0;
 }
