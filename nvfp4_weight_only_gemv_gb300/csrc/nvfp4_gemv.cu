@@ -69,7 +69,9 @@ __device__ unsigned long long g_fp32_fallbacks;  // CTAs that staged x in fp32 b
 // loop; word 24 = the SM the CTA ran on; word 24 + w (w = 1..7) = %globaltimer when warp w's
 // first box landed (warp 0's is phase 4); words 32.. = clock64 of thread 0 at finer points of
 // the prologue (32 barriers initialised, 33 work range known, 34 first copy issued, 35 all
-// initial copies issued, 36 MoE groups built, 37 copies after x staging issued). Phases: 0 entry, 1 first weight copies issued, 2 past
+// initial copies issued, 36 MoE groups built, 37 copies after x staging issued; the FFN block:
+// 38 its slice of h complete, 39 that slice staged; more than 32 MoE slots: 38 ids in shared
+// memory, 39 ranks and counts done). Phases: 0 entry, 1 first weight copies issued, 2 past
 // the dependency wait, 3 x staged, 4 warp 0's first box landed, 5 warp 0's loop done, 6 outputs
 // stored, 7 exit. Normal builds compile all of it out.
 #ifndef NVFP4_PHASE_TRACE
@@ -1878,12 +1880,80 @@ __device__ void tile_moe_groups(const TileParams& p, TileMoe* tab, int lane) {
 
 // The x rows that groups [g0, g1] need, staged in increasing row order (at most 32 rows).
 // Routed-expert groups of a stream-K launch with more than 32 slots (up to kMaxMoeSlots), built
-// by all threads: one pass over the ids (in shared memory, four at a time) gives each slot its
-// rank among the earlier slots of its expert, its expert's slot count and first slot (the
-// leader); the expert's slots form groups of up to 8 in slot order, numbered from ngr[leader],
-// leaders in slot order. Scratch: ids, rank, cnt, lead, ngr, each kMaxMoeSlots ints (5 KB).
-// Invalid ids form no group: CTA 0 zeroes their outputs and flags them.
-constexpr int kMoeScratchInts = 5 * kMaxMoeSlots;
+// by all threads: a sort of the (expert, slot) keys (moe_rank_by_sort) gives each slot its rank
+// among the earlier slots of its expert, its expert's slot count and first slot (the leader); the
+// expert's slots form groups of up to 8 in slot order, numbered from ngr[leader], leaders in slot
+// order. Scratch: kMoeScratchInts ints (10.1 KB) at the start of the x region. Invalid ids form no
+// group: CTA 0 zeroes their outputs and flags them.
+// scratch: ids, rank, cnt, lead, ngr (5 x kMaxMoeSlots ints), two buffers of sort keys (2 x
+// kMaxMoeSlots 64-bit words), the run lengths (kMaxMoeSlots ints) and the warps' scan tops (32 ints)
+constexpr int kMoeScratchInts = 5 * kMaxMoeSlots + 4 * kMaxMoeSlots + kMaxMoeSlots + 32;
+static_assert(kMaxMoeSlots == tk::kThreads, "the group builder sorts one slot per thread");
+
+// Rank, expert count, leader and group count of every slot, by sorting (expert, slot) keys: after
+// a bitonic sort of the kMaxMoeSlots keys (one per thread), the slots of an expert form a run in
+// slot order, so a slot's rank is its distance from the run's start, its count the run's length
+// and its leader the slot at the run's start. Invalid ids (negative in `ids`) and padding sort
+// after every expert and form no run. All threads; ends with __syncthreads.
+__device__ void moe_rank_by_sort(const int* ids, int nslots, int* rank, int* cnt, int* lead, int* ngr,
+                                 unsigned long long* keys, int* runs, int* wtop, int tid) {
+    const int id0 = tid < nslots ? ids[tid] : -1;
+    unsigned long long key = (id0 >= 0 ? static_cast<unsigned long long>(static_cast<uint32_t>(id0)) << 32
+                                       : 0xffffffffull << 32) | static_cast<uint32_t>(tid);
+    // bitonic sort, one key per thread: partners within a warp swap through shuffles; partners
+    // 32 or more positions apart through two alternating shared buffers (one barrier per stage)
+    int buf = 0;
+    for (int k = 2; k <= kMaxMoeSlots; k <<= 1) {
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            unsigned long long other;
+            if (j >= 32) {
+                unsigned long long* b = keys + buf * kMaxMoeSlots;
+                b[tid] = key;
+                __syncthreads();
+                other = b[tid ^ j];
+                buf ^= 1;
+            } else {
+                const uint32_t lo = __shfl_xor_sync(0xffffffffu, static_cast<uint32_t>(key), j);
+                const uint32_t hw = __shfl_xor_sync(0xffffffffu, static_cast<uint32_t>(key >> 32), j);
+                other = (static_cast<unsigned long long>(hw) << 32) | lo;
+            }
+            // the lower position of an ascending pair (bit k of the position clear) keeps the
+            // smaller key, of a descending pair the larger
+            const bool keep_min = ((tid & j) == 0) == ((tid & k) == 0);
+            key = keep_min ? (key < other ? key : other) : (key > other ? key : other);
+        }
+    }
+    keys += buf * kMaxMoeSlots;  // the buffer the last shared stage did not use
+    keys[tid] = key;
+    __syncthreads();
+    const uint32_t hi = static_cast<uint32_t>(key >> 32);
+    const bool valid = hi != 0xffffffffu;
+    const bool start = tid == 0 || static_cast<uint32_t>(keys[tid - 1] >> 32) != hi;
+    const bool last = tid == kMaxMoeSlots - 1 || static_cast<uint32_t>(keys[tid + 1] >> 32) != hi;
+    // the start of every position's run: an inclusive max-scan of (start ? position : 0)
+    int v = start ? tid : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, v, o);
+        if ((tid & 31) >= o) v = max(v, u);
+    }
+    if ((tid & 31) == 31) wtop[tid >> 5] = v;
+    __syncthreads();
+    for (int w = 0; w < (tid >> 5); ++w) v = max(v, wtop[w]);
+    if (last) runs[v] = tid - v + 1;  // the run's length, at its start
+    __syncthreads();
+    const int slot = static_cast<int>(static_cast<uint32_t>(key));
+    if (slot < nslots) {
+        const int r = valid ? tid - v : 0;
+        const int c = valid ? runs[v] : 0;
+        rank[slot] = r;
+        cnt[slot] = c;
+        lead[slot] = valid ? static_cast<int>(static_cast<uint32_t>(keys[v])) : slot;
+        ngr[slot] = valid && r == 0 ? (c + 7) / 8 : 0;
+    }
+    __syncthreads();
+}
+
 __device__ void tile_moe_groups_big(const TileParams& p, TileMoe* tab, int* scratch, int tid) {
     int* ids = scratch;
     int* rank = scratch + kMaxMoeSlots;
@@ -1903,25 +1973,10 @@ __device__ void tile_moe_groups_big(const TileParams& p, TileMoe* tab, int* scra
         ids[t] = v;
     }
     __syncthreads();
-    for (int t = tid; t < p.slots; t += tk::kThreads) {
-        const int id = ids[t];
-        int r = 0, c = 0, first = t;
-        const int4* ids4 = reinterpret_cast<const int4*>(ids);
-        for (int q = 0; q < (p.slots + 3) / 4; ++q) {
-            const int4 v = ids4[q];
-            const int u = 4 * q;
-            const int e0 = v.x == id, e1 = v.y == id, e2 = v.z == id, e3 = v.w == id;
-            c += e0 + e1 + e2 + e3;
-            r += (e0 & (u < t)) + (e1 & (u + 1 < t)) + (e2 & (u + 2 < t)) + (e3 & (u + 3 < t));
-            first = min(first, min(min(e0 ? u : t, e1 ? u + 1 : t), min(e2 ? u + 2 : t, e3 ? u + 3 : t)));
-        }
-        const bool valid = id >= 0;
-        rank[t] = r;
-        cnt[t] = valid ? c : 0;
-        lead[t] = first;
-        ngr[t] = valid && r == 0 ? (c + 7) / 8 : 0;
-    }
-    __syncthreads();
+    if (tid == 0) trace_word(p.trace_slot, 38, static_cast<unsigned long long>(clock64()));
+    moe_rank_by_sort(ids, p.slots, rank, cnt, lead, ngr, reinterpret_cast<unsigned long long*>(scratch + 5 * kMaxMoeSlots),
+                     scratch + 9 * kMaxMoeSlots, scratch + 10 * kMaxMoeSlots, tid);
+    if (tid == 0) trace_word(p.trace_slot, 39, static_cast<unsigned long long>(clock64()));
     if (tid < 32) {
         // exclusive scan of the group counts over slots, 8 slots per lane
         int local[8];

@@ -228,7 +228,7 @@ def moe_problem(E: int, N: int, K: int, T: int, top_k: int, x_per_slot: bool, se
     w = torch.zeros(E, N, K // 2, dtype=torch.uint8, device=device)
     s = torch.zeros(E, N, K // 16, dtype=torch.uint8, device=device)
     gs = torch.ones(E, dtype=torch.float32)
-    experts = range(E) if fill == "all" else sorted(set(int(e) for e in ids.tolist()))
+    experts = range(E) if fill == "all" else sorted(set(int(e) for e in ids.tolist() if 0 <= int(e) < E))
     for e in experts:
         if max_codes is None:
             we, se, ge = random_weight(N, K, seed * 1000 + e, device)

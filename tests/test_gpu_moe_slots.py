@@ -139,3 +139,41 @@ def test_moe_timeout_path_on_tile_kernels(case):
                                   synth.bf16_bits(p["x"]), xps, top_k)
     assert bad == 0
     assert_parity(y, yr, ya, f"after timeout ({case})")
+
+
+def test_moe_many_slots_with_invalid_ids_and_odd_counts():
+    # 37 tokens x top-3 = 111 slots (no multiple of 32): some ids out of range (-1, E, E + 7)
+    # zero their slots and set DEV_BAD_EXPERT; the others match the oracle
+    T, top_k = 37, 3
+    N, K = 512, 1024
+    ids = synth.routing(T, top_k, E, 940).clone()
+    ids[5], ids[40], ids[77], ids[110] = -1, E, E + 7, -1
+    p = synth.moe_problem(E, N, K, T, top_k, True, seed=940, device=DEV, ids=ids)
+    assert nv.describe_plan("moe_per_slot", E, N, K, T, top_k).split()[0] == "tile_sk_moe"
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    y = nv.moe_gemv(p["w"], p["s"], p["gs"], p["ids"], p["x"], True, top_k, out_dtype=torch.float32, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & nv.DEV_BAD_EXPERT
+    assert nv.device_status() & nv.DEV_BAD_EXPERT  # read and cleared here
+    yr, ya, bad = oracle.moe_gemv(host(p["w"]), host(p["s"]), host(p["gs"]), host(p["ids"]),
+                                  synth.bf16_bits(p["x"]), True, top_k)
+    assert bad == 4
+    assert not torch.any(y[[5, 40, 77, 110]])
+    assert_parity(y, yr, ya, "111 slots with invalid ids")
+
+
+@pytest.mark.parametrize("routing", ["one_expert", "all_distinct"])
+def test_moe_256_slots_extreme_routings(routing):
+    # every slot on one expert (32 groups of 8) or every slot on its own expert
+    T, top_k = 256, 1
+    N, K = 256, 512
+    ids = torch.full((T,), 17, dtype=torch.int32) if routing == "one_expert" else torch.arange(T, dtype=torch.int32)
+    p = synth.moe_problem(E, N, K, T, top_k, True, seed=950, device=DEV, ids=ids)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    y = nv.moe_gemv(p["w"], p["s"], p["gs"], p["ids"], p["x"], True, top_k, out_dtype=torch.float32, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    yr, ya, bad = oracle.moe_gemv(host(p["w"]), host(p["s"]), host(p["gs"]), host(p["ids"]),
+                                  synth.bf16_bits(p["x"]), True, top_k)
+    assert bad == 0
+    assert_parity(y, yr, ya, f"256 slots, {routing}")
