@@ -37,7 +37,7 @@ METRICS = ["gpu__time_duration.sum", "dram__bytes_read.sum", "dram__bytes_write.
            "sm__warps_active.avg.pct_of_peak_sustained_active"]
 # launches of one step of each workload (captured after the warm-up launches)
 LAUNCHES = {"vocab": 1, "vocab_sdict": 1, "attn": 4, "ffn": 2, "ffn_m8": 2, "ffn_swiglu": 2, "ffn_fused": 2,
-            "ffn_shared": 2, "ffn_shared_fused": 1, "moe": 2, "moe_sdict": 2, "moe_t32": 2}
+            "ffn_shared": 2, "ffn_shared_fused": 1, "moe": 2, "moe_sdict": 2, "moe_t32": 2, "card_m2": 5}
 WARMUP = 3
 
 
@@ -74,8 +74,8 @@ def parse(csv_text: str):
 
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
-    ap.add_argument("--workloads", default="vocab,attn,ffn,ffn_swiglu,ffn_shared,ffn_shared_fused,moe,moe_t32,"
-                                           "vocab_sdict,moe_sdict")
+    ap.add_argument("--workloads", default="vocab,attn,card_m2,ffn,ffn_swiglu,ffn_shared,ffn_shared_fused,moe,"
+                                           "moe_t32,vocab_sdict,moe_sdict")
     ap.add_argument("--out", default=os.path.join(ROOT, "gpurun_out", "ncu_traffic"))
     args = ap.parse_args(argv)
     os.makedirs(args.out, exist_ok=True)
