@@ -29,7 +29,8 @@
  *     where a comment says otherwise. The library frees nothing it did not allocate.
  *   - A call allocates no memory and does not synchronise. It validates its arguments on
  *     the host, enqueues its kernel(s) on `stream` (a cudaStream_t; NULL = legacy default
- *     stream) and returns. Calls can be captured into CUDA graphs.
+ *     stream) and returns. Calls that take all their memory from the caller can be captured
+ *     into CUDA graphs.
  *   - Shapes: 0 <= M <= 8, N >= 0, K >= 0, K % 16 == 0. M == 0, N == 0 or an empty MoE
  *     routing launch nothing. K == 0 sets y to zero.
  *   - Fast path: w/s base pointers 16-byte aligned and K % 32 == 0. Anything else runs a
