@@ -70,8 +70,9 @@ __device__ unsigned long long g_fp32_fallbacks;  // CTAs that staged x in fp32 b
 // first box landed (warp 0's is phase 4); words 32.. = clock64 of thread 0 at finer points of
 // the prologue (32 barriers initialised, 33 work range known, 34 first copy issued, 35 all
 // initial copies issued, 36 MoE groups built, 37 copies after x staging issued; the FFN block:
-// 38 its slice of h complete, 39 that slice staged; more than 32 MoE slots: 38 ids in shared
-// memory, 39 ranks and counts done). Phases: 0 entry, 1 first weight copies issued, 2 past
+// 38 its slice of h complete, 39 that slice staged; MoE with more than 32 slots: 38 ids in
+// shared memory, 39 ranks and counts done; with up to 32: 38 warp 0's groups built, 39 the CTA
+// past the barrier after them). Phases: 0 entry, 1 first weight copies issued, 2 past
 // the dependency wait, 3 x staged, 4 warp 0's first box landed, 5 warp 0's loop done, 6 outputs
 // stored, 7 exit. Normal builds compile all of it out.
 #ifndef NVFP4_PHASE_TRACE
@@ -2056,14 +2057,20 @@ __device__ void tile_moe_window(const TileParams& p, TileMoe* tab, const int* sc
 }
 
 __device__ void tile_moe_rows(const TileParams& p, TileMoe* tab, int g0, int g1, int lane) {
+    // lane l takes member l % 8 of group base + l / 8: four groups per pass, one pass for the
+    // usual window (a serial scan of the members took about 0.6 us of the launch's set-up)
     uint32_t want = 0u;
-    for (int g = g0; g <= g1; ++g)
-        for (int j = 0; j < tab->count[g]; ++j) want |= 1u << tab->xrow[g][j];
+    for (int base = g0; base <= g1; base += 4) {
+        const int g = base + (lane >> 3), j = lane & 7;
+        const bool has = g <= g1 && j < tab->count[g];
+        want |= __reduce_or_sync(0xffffffffu, has ? 1u << tab->xrow[g][j] : 0u);
+    }
     if (lane == 0) tab->nrows = __popc(want);
-    if (lane < 32 && ((want >> lane) & 1u)) tab->rows[__popc(want & ((1u << lane) - 1u))] = lane;
-    __syncwarp();
-    for (int g = g0; g <= g1; ++g)
-        if (lane < tab->count[g]) tab->col[g][lane] = __popc(want & ((1u << tab->xrow[g][lane]) - 1u));
+    if ((want >> lane) & 1u) tab->rows[__popc(want & ((1u << lane) - 1u))] = lane;
+    for (int base = g0; base <= g1; base += 4) {
+        const int g = base + (lane >> 3), j = lane & 7;
+        if (g <= g1 && j < tab->count[g]) tab->col[g][j] = __popc(want & ((1u << tab->xrow[g][j]) - 1u));
+    }
     __syncwarp();
 }
 
@@ -3077,20 +3084,33 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_sk_kernel(const __g
         int* scratch = reinterpret_cast<int*>(sbase + p.x_off);
         if (big) tile_moe_groups_big(p, tab, scratch, tid);
         else if (warp == 0) tile_moe_groups(p, tab, lane);
+        if (!big && tid == 0) trace_word(p.trace_slot, 38, static_cast<unsigned long long>(clock64()));
         __syncthreads();
+        if (!big && tid == 0) trace_word(p.trace_slot, 39, static_cast<unsigned long long>(clock64()));
 #if NVFP4_SK_GROUP_ALIGNED
         if (p.items_r) {
             // group-aligned: CTAs [G*g/ng, G*(g+1)/ng) share group g's jobs (the planner keeps
             // G >= the most groups there can be), so a CTA stages one group's x rows (<= 8)
             const int ng = tab->n_groups, G = static_cast<int>(gridDim.x), b = static_cast<int>(blockIdx.x);
             if (ng > 0) {
-                const int g = static_cast<int>(((static_cast<long long>(b) + 1) * ng - 1) / G);
-                const int lo = static_cast<int>(static_cast<long long>(G) * g / ng);
-                const int c = static_cast<int>(static_cast<long long>(G) * (g + 1) / ng) - lo;
+                // 32-bit unsigned arithmetic: b < G and ng <= kMaxMoeSlots keep (b + 1) * ng and
+                // G * (g + 1) far below 2^32, and tiles * k (k <= c) too while tiles < 2^22 and
+                // c <= 1024 (else 64-bit)
+                const uint32_t ug = (static_cast<uint32_t>(b + 1) * static_cast<uint32_t>(ng) - 1u) /
+                                    static_cast<uint32_t>(G);
+                const int g = static_cast<int>(ug);
+                const int lo = static_cast<int>(static_cast<uint32_t>(G) * ug / static_cast<uint32_t>(ng));
+                const int c = static_cast<int>(static_cast<uint32_t>(G) * (ug + 1u) / static_cast<uint32_t>(ng)) - lo;
                 const int i = b - lo;
+                auto part = [&](int k) -> int {  // tiles * k / c
+                    if (tiles < (1 << 22) && c <= 1024)
+                        return static_cast<int>(static_cast<uint32_t>(tiles) * static_cast<uint32_t>(k) /
+                                                static_cast<uint32_t>(c));
+                    return static_cast<int>(static_cast<long long>(tiles) * k / c);
+                };
                 if (c > 0 && i >= 0 && i < c) {
-                    j0 = g * tiles + static_cast<int>(static_cast<long long>(tiles) * i / c);
-                    j1 = g * tiles + static_cast<int>(static_cast<long long>(tiles) * (i + 1) / c);
+                    j0 = g * tiles + part(i);
+                    j1 = g * tiles + part(i + 1);
                 } else {
                     // fewer CTAs than groups (the planner rules it out): no work, flagged
                     j0 = j1 = 0;
