@@ -72,11 +72,16 @@ __device__ unsigned long long g_fp32_fallbacks;  // CTAs that staged x in fp32 b
 // initial copies issued, 36 MoE groups built, 37 copies after x staging issued; the FFN block:
 // 38 its slice of h complete, 39 that slice staged; MoE with more than 32 slots: 38 ids in
 // shared memory, 39 ranks and counts done; with up to 32: 38 warp 0's groups built, 39 the CTA
-// past the barrier after them). Phases: 0 entry, 1 first weight copies issued, 2 past
+// past the barrier after them; dense tile launches: 38 just before and 39 just after warp 0's
+// wait for its first box, and with -DNVFP4_TRACE_BOX_LANDED=1 word 36 = %globaltimer when that
+// box, requested before the dependency wait, landed). Phases: 0 entry, 1 first weight copies issued, 2 past
 // the dependency wait, 3 x staged, 4 warp 0's first box landed, 5 warp 0's loop done, 6 outputs
 // stored, 7 exit. Normal builds compile all of it out.
 #ifndef NVFP4_PHASE_TRACE
 #define NVFP4_PHASE_TRACE 0
+#endif
+#ifndef NVFP4_TRACE_BOX_LANDED
+#define NVFP4_TRACE_BOX_LANDED 0  // traced builds: dense word 36 = %globaltimer when the first box landed
 #endif
 constexpr int kTraceLaunches = 16;
 constexpr int kTraceCtas = 1024;
@@ -2198,6 +2203,13 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_kernel(const __grid
     }
     if (tid == 0) trace_phase(p.trace_slot, 1);
     pdl_launch_dependents();
+#if NVFP4_PHASE_TRACE && NVFP4_TRACE_BOX_LANDED
+    // when the first box, requested before the dependency wait, lands (thread 0 waits for it
+    // here, so this build delays warp 0 until then)
+    if constexpr (!MOE)
+        if (tid == 0 && ib < ie && nb > 0 && mbar_wait(&bars[0], 0, p.wait_ns))
+            trace_word(p.trace_slot, 36, global_ns());
+#endif
     pdl_wait();
     if (tid == 0) trace_phase(p.trace_slot, 2);
 
@@ -2293,12 +2305,16 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_kernel(const __grid
             for (int b = 0; b < nb; ++b) {
                 const uint32_t st = cons_st;
                 const uint32_t ph = cons_ph;
+                if (NVFP4_PHASE_TRACE && !MOE && tid == 0 && !traced_first)
+                    trace_word(p.trace_slot, 38, static_cast<unsigned long long>(clock64()));
                 // a zero budget takes the timeout path deterministically (copies issued before
                 // x staging have usually landed by now, so one poll would succeed)
                 if (!__all_sync(0xffffffffu, budget != 0 && mbar_wait(&bars[st], ph, budget))) {
                     dead = true;  // warp-uniform: stop computing, keep the CTA's barrier count
                     break;
                 }
+                if (NVFP4_PHASE_TRACE && !MOE && tid == 0 && !traced_first)
+                    trace_word(p.trace_slot, 39, static_cast<unsigned long long>(clock64()));
                 if (NVFP4_PHASE_TRACE && lane == 0 && !traced_first) {
                     if (warp == 0) trace_phase(p.trace_slot, 4);
                     else trace_word(p.trace_slot, 24 + warp, global_ns());

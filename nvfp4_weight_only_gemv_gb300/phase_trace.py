@@ -169,6 +169,39 @@ def summarise(tr, launches, calls_meta):
             d = np.where(ok, a - xs, np.nan)
             return f"{np.nanmedian(d) / 1e3:.2f}/{np.nanmax(d) / 1e3:.2f}" if ok.any() else "-"
         lines.append(f"{calls_meta[l][0]:<28}{stat(first):>38}{stat(loop):>40}")
+    # the tail: when CTAs stored their outputs (phase 6) relative to the launch's median, and the
+    # SMs (word 24) of the last four
+    lines.append("")
+    lines.append(f"{'launch':<28}{'stored p90-med (us)':>22}{'stored last-med (us)':>22}{'SMs of the last 4 CTAs':>30}")
+    for l in range(launches):
+        rows = tr[l][tr[l, :, 0] > 0]
+        st = rows[:, 12]
+        ok = st > 0
+        if ok.sum() < 4:
+            continue
+        med = np.median(st[ok])
+        last4 = np.argsort(np.where(ok, st, 0))[-4:]
+        lines.append(f"{calls_meta[l][0]:<28}{(np.percentile(st[ok], 90) - med) / 1e3:>22.2f}"
+                     f"{(st[ok].max() - med) / 1e3:>22.2f}{' '.join(str(int(rows[i, 24])) for i in last4):>30}")
+    # dense launches, thread 0 in SM cycles: x staged (phase 3's clock) to just before the wait
+    # for its first box (word 38), and that wait (word 38 to 39)
+    dense = [l for l in range(launches) if calls_meta[l][0].startswith(("dense", "gate_up", "swiglu"))]
+    if dense:
+        lines.append("")
+        lines.append(f"{'launch':<28}{'x_staged->box wait (cycles)':>30}{'box wait (cycles)':>20}"
+                     f"{'issued->landed (us)':>22}{'landed->dep_wait (us)':>24}")
+        for l in dense:
+            rows = tr[l][tr[l, :, 0] > 0]
+            ok = (rows[:, 7] > 0) & (rows[:, 38] > 0) & (rows[:, 39] > 0)
+            if not ok.any():
+                continue
+            r = rows[ok]
+            # word 36: when the first box landed (builds with NVFP4_TRACE_BOX_LANDED=1 only)
+            land = r[r[:, 36] > 0]
+            il = f"{np.median(land[:, 36] - land[:, 2]) / 1e3:.2f}" if len(land) else "-"
+            ld = f"{np.median(land[:, 4] - land[:, 36]) / 1e3:.2f}" if len(land) else "-"
+            lines.append(f"{calls_meta[l][0]:<28}{np.median(r[:, 38] - r[:, 7]):>30.0f}"
+                         f"{np.median(r[:, 39] - r[:, 38]):>20.0f}{il:>22}{ld:>24}")
     # the FFN block's own phases (thread 0, so warp 0's K slice): gate/up done (phase 5), its
     # slice of h complete (word 38), that slice staged (word 39), down done (phase 6)
     ffn = [l for l in range(launches) if calls_meta[l][0].startswith("ffn")]
