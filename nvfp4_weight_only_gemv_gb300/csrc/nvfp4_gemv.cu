@@ -1305,22 +1305,7 @@ struct TileParams {
     const uint8_t* sd_dict;
     int sd_tiles;             // 16-row tiles per expert in the index plane (MoE)
     uint32_t sdtab_off;       // the pair table: 1024 f16x2 scale pairs
-    // dense launches: the weight codes [N, K/2] and E4M3 scales [N, K/16] of each group (null:
-    // not given; dictionary scales give no sraw), for L2 prefetches of the first boxes
-    const uint8_t* wraw[2];
-    const uint8_t* sraw[2];
-    int wprefetch;            // 1: prefetch them (launches with more weight bytes than kWeightPrefetchMinBytes)
 };
-
-// Dense launches with at least this many weight bytes also prefetch their first boxes into L2
-// with plain prefetches before the dependency wait. Bulk copies requested there are served late
-// while the preceding grid still runs (traced: they land when it completes, however idle the
-// memory is), plain prefetches are not; a long launch that follows another one fills the
-// latter's tail with its first weights that way (vocabulary head 151936x4096: 52.57 -> 52.04 us).
-// Shorter launches lose by it (the prefetches compete with the preceding grid's own loads:
-// attention projections 20.4 -> 21.2 us, 2x12288x4096 gate/up with the down projection 23.1 ->
-// 23.3 us a step).
-constexpr long long kWeightPrefetchMinBytes = 128ll << 20;
 
 // Bytes of one ring slot's scale box: NC 16-byte rows of E4M3 codes per tile row, or (dictionary
 // scales) NC 160-byte index records, padded to 128 bytes.
@@ -2196,29 +2181,6 @@ __global__ void __launch_bounds__(tk::kThreads, 2) gemv_tile_kernel(const __grid
                 if (tid == 0 && s == 0) trace_word(p.trace_slot, 34, static_cast<unsigned long long>(clock64()));
             }
         if (tid == 0) trace_word(p.trace_slot, 35, static_cast<unsigned long long>(clock64()));
-        // long launches: the same boxes of the warp's first item again, as plain L2 prefetches
-        // (lane l: row l % 16 of the box, 128-byte segment l / 16 of the row's NC); rows < N and
-        // segments inside the row only
-        if (p.wprefetch && ib < ie && p.wraw[0] != nullptr) {
-            const int tile = first.t * p.tpi + tin;
-            if (tile < p.tiles) {
-                int map = first.grp, row0 = tile * 16;
-                if constexpr (SWI) {
-                    map = tile & 1;
-                    row0 = (tile >> 1) * 16;
-                }
-                const int row = row0 + (lane & 15), h = lane >> 4;
-                const int nbx = min(min(stages, NVFP4_DENSE_EARLY), nb), segs = p.K >> 8;
-                if (row < p.N && h < NC)
-                    for (int b = 0; b < nbx; ++b) {
-                        const int seg = (b_lo + b) * NC;
-                        if (seg + h >= segs) break;
-                        prefetch_l2(p.wraw[map] + static_cast<int64_t>(row) * (p.K >> 1) + (seg + h) * 128);
-                        if (!SD && h == 0 && p.sraw[map] != nullptr)
-                            prefetch_l2(p.sraw[map] + static_cast<int64_t>(row) * (p.K >> 4) + seg * 16);
-                    }
-            }
-        }
         if constexpr (SD) {
             // the table is a weight too: built before the dependency wait
             build_pair_table(reinterpret_cast<uint32_t*>(sbase + p.sdtab_off), p.sd_dict, tid, tk::kThreads);
@@ -4396,11 +4358,6 @@ nvfp4_status run_dense(const uint8_t* const* w, const uint8_t* const* s, const f
         p.out_bf16 = y_type == NVFP4_OUT_BF16;
         p.force_f32 = g_variant == 2;
         p.wait_ns = g_wait_ns;
-        for (int i = 0; i < 2; ++i) {
-            p.wraw[i] = w[groups > 1 ? i : 0];
-            p.sraw[i] = s[groups > 1 ? i : 0];
-        }
-        p.wprefetch = static_cast<long long>(groups) * N * (K / 2 + K / 16) >= kWeightPrefetchMinBytes;
         const cudaError_t e = launch_tile(tpl, st, false);
         if (e != cudaSuccess) return cuda_fail(e);
         const cudaError_t e2 = cudaGetLastError();
@@ -4474,8 +4431,6 @@ nvfp4_status run_sdict_dense(const uint8_t* w, const uint8_t* plane, const uint8
         p.force_f32 = g_variant == 2;
         p.wait_ns = g_wait_ns;
         p.sd_dict = dict;
-        p.wraw[0] = p.wraw[1] = w;
-        p.wprefetch = static_cast<long long>(N) * (K / 2 + K / 16) >= kWeightPrefetchMinBytes;
         const cudaError_t e = launch_tile(tpl, st, false, true);
         if (e != cudaSuccess) return cuda_fail(e);
         const cudaError_t e2 = cudaGetLastError();
