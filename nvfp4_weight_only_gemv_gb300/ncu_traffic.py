@@ -16,7 +16,7 @@ of the library's kernels (``-k regex:gemv_``, after the warm-up launches) with t
 It writes ``traffic.json`` (per workload: DRAM read + write bytes per launch, averaged over the
 captured launches, tied to the sha256 of the kernel source it measured; bench.py reports it as
 ``roofline.traffic`` only while the source is unchanged) and ``counters.md`` (a table of every
-captured launch) into DIR (default: gpurun_out/ncu_traffic). The raw CSVs stay in DIR.
+captured launch) into DIR (default: the package's _build/ncu_traffic). The raw CSVs stay in DIR.
 """
 from __future__ import annotations
 
@@ -76,7 +76,7 @@ def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--workloads", default="vocab,attn,card_m2,ffn,ffn_swiglu,ffn_shared,ffn_shared_fused,moe,"
                                            "moe_t32,vocab_sdict,moe_sdict")
-    ap.add_argument("--out", default=os.path.join(ROOT, "gpurun_out", "ncu_traffic"))
+    ap.add_argument("--out", default=os.path.join(ROOT, "nvfp4_weight_only_gemv_gb300", "_build", "ncu_traffic"))
     args = ap.parse_args(argv)
     os.makedirs(args.out, exist_ok=True)
     sha = source_sha256()
