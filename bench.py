@@ -59,7 +59,7 @@ WORKLOADS = {
     "ffn_m8": ("FFN gate+up then down at M=8, fp32 out",
                [("gate_up", 12288, 4096, 8, 5, "f32"), ("dense", 4096, 12288, 8, 6, "f32")]),
     "ffn_swiglu": ("FFN gate+up N=2x12288,K=4096 with the fused SwiGLU (clamp 10, bf16 [1, 12288] out) "
-                   "then down N=4096,K=12288 at M=1, fp32 out",
+                   "then down N=4096,K=12288 at M=1 on its own x input, fp32 out",
                    [("gate_up_swiglu", 12288, 4096, 1, 5, "bf16"), ("dense", 4096, 12288, 1, 6, "f32")]),
     "ffn_fused": ("FFN block in one call: gate+up 2x12288x4096 with the SwiGLU (clamp 10) into a bf16 h, "
                   "then down 4096x12288, M=1, fp32 out",
@@ -152,7 +152,7 @@ def kernels_of(calls):
              "stream_moe": "gemv_stream_kernel (MoE)", "simple": "gemv_simple_kernel",
              "tile_sdict": "gemv_tile_kernel (dictionary scales)",
              "tile_sk_moe_sdict": "gemv_tile_sk_kernel (MoE, dictionary scales)",
-             "ffn_fused": "gemv_ffn_kernel (gate/up + SwiGLU, grid barrier, down)",
+             "ffn_fused": "gemv_ffn_kernel (gate/up + SwiGLU, readiness counters, down)",
              "ffn_two_launch": "gemv_tile_kernel (gate/up + SwiGLU, then down)"}
     seen = []
     for c in calls:
