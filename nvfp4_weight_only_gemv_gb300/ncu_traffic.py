@@ -36,8 +36,9 @@ METRICS = ["gpu__time_duration.sum", "dram__bytes_read.sum", "dram__bytes_write.
            "l1tex__t_sectors_pipe_lsu_mem_global_op_ld.sum", "l1tex__t_requests_pipe_lsu_mem_global_op_ld.sum",
            "sm__warps_active.avg.pct_of_peak_sustained_active"]
 # launches of one step of each workload (captured after the warm-up launches)
-LAUNCHES = {"vocab": 1, "vocab_sdict": 1, "attn": 4, "ffn": 2, "ffn_m8": 2, "ffn_swiglu": 2, "ffn_fused": 2,
-            "ffn_shared": 2, "ffn_shared_fused": 1, "moe": 2, "moe_sdict": 2, "moe_t32": 2, "card_m2": 5}
+LAUNCHES = {"vocab": 1, "vocab_sdict": 1, "attn": 4, "ffn": 2, "ffn_m2": 2, "ffn_m4": 2, "ffn_m8": 2, "ffn_swiglu": 2,
+            "ffn_fused": 2, "ffn_shared": 2, "ffn_shared_fused": 1, "moe": 2, "moe_sdict": 2, "moe_t32": 2,
+            "card_m2": 5}
 WARMUP = 3
 
 
@@ -74,8 +75,8 @@ def parse(csv_text: str):
 
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
-    ap.add_argument("--workloads", default="vocab,attn,card_m2,ffn,ffn_swiglu,ffn_shared,ffn_shared_fused,moe,"
-                                           "moe_t32,vocab_sdict,moe_sdict")
+    ap.add_argument("--workloads", default="vocab,attn,card_m2,ffn,ffn_m2,ffn_m4,ffn_m8,ffn_swiglu,ffn_fused,"
+                                           "ffn_shared,ffn_shared_fused,moe,moe_t32,vocab_sdict,moe_sdict")
     ap.add_argument("--out", default=os.path.join(ROOT, "nvfp4_weight_only_gemv_gb300", "_build", "ncu_traffic"))
     args = ap.parse_args(argv)
     os.makedirs(args.out, exist_ok=True)
