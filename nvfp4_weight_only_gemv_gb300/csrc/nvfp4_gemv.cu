@@ -1504,7 +1504,7 @@ __device__ bool stage_x_direct(const uint16_t* __restrict__ x, const int* rowsel
 }
 
 #ifndef NVFP4_STAGE_BULK
-#define NVFP4_STAGE_BULK 0  // 1: x arrives by bulk copies and is converted in place (not yet validated on a GPU)
+#define NVFP4_STAGE_BULK 0  // 1: x arrives by bulk copies and is converted in place (correct, but measured slower)
 #endif
 
 // stage_x_direct with the slice's rows brought in by bulk copies: lane 0 of the slice's first
