@@ -133,14 +133,16 @@ nvfp4_status nvfp4_gemv_gate_up_swiglu(const uint8_t* w_gate, const uint8_t* s_g
  *   once corrupt each other's h and counters.
  * Shapes: 0 <= M <= 8, H, I >= 0, H % 16 == 0, I % 16 == 0. M == 0 or H == 0 launch nothing;
  * I == 0 sets y to zero.
- * Execution: one launch when H % 512 == 0, I % 512 == 0, the weights and x are 16-byte aligned
- * and a plan with two CTAs per SM fits in shared memory (at H = 4096, I = 12288: M = 1): gate/up
- * and the activation, then down, whose warps each wait only until the slice of h they read is
- * complete (the gate/up items that write it count themselves in the workspace) and whose first
- * weight copies are in flight before that. That launch needs all its CTAs resident at once; if
- * other work on the GPU keeps some of them from starting within the wait budget, the call sets
- * NVFP4_DEV_TIMEOUT and y is unspecified. Otherwise two launches (gate/up + activation into the
- * workspace's h, then down), with the same results within tolerance.
+ * Execution: one launch when H % 512 == 0, I % 512 == 0, the weights and x are 16-byte aligned,
+ * the three weights take at most 12 MiB (3 * H * I * 9/16 bytes; larger blocks are faster as two
+ * launches) and a plan with two CTAs per SM fits in shared memory (the shared expert H = 4096,
+ * I = 768: M = 1 to 4). That launch runs gate/up and the activation, then down, whose warps each
+ * wait only until the slice of h they read is complete (the gate/up items that write it count
+ * themselves in the workspace) and whose first weight copies are in flight before that. It needs
+ * all its CTAs resident at once; if other work on the GPU keeps some of them from starting
+ * within the wait budget, the call sets NVFP4_DEV_TIMEOUT and y is unspecified. Otherwise two
+ * launches (gate/up + activation into the workspace's h, then down), with the same results
+ * within tolerance.
  */
 nvfp4_status nvfp4_ffn_swiglu(const uint8_t* w_gate, const uint8_t* s_gate, float g_gate,
                               const uint8_t* w_up, const uint8_t* s_up, float g_up,
