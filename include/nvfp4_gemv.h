@@ -231,7 +231,7 @@ nvfp4_status nvfp4_gemv_sdict(const uint8_t* w_packed, const uint8_t* scale_idx,
  * Routed-expert GEMV with dictionary scales: expert e's index plane starts at
  * scale_idx + e * nvfp4_sdict_plane_bytes(N, K) and its table at scale_dict + 32 e; every
  * other argument, layout and status as nvfp4_moe_gemv. Returns NVFP4_ERR_SHAPE when
- * K % 256 != 0. Up to 32 slots run the stream-K tile kernel (each CTA inside one expert group,
+ * K % 256 != 0. Up to 256 slots run the stream-K tile kernel (each CTA inside one expert group,
  * so one table serves it); larger routings run the byte-load kernel.
  */
 nvfp4_status nvfp4_moe_gemv_sdict(const uint8_t* w_packed, const uint8_t* scale_idx, const uint8_t* scale_dict,
@@ -334,8 +334,12 @@ int nvfp4_describe_plan_host(int sm_count, int smem_optin, int smem_per_sm, int 
  * %globaltimer when warp w left its box loop; word 24 the SM id; word 24 + w (w = 1..7)
  * %globaltimer when warp w's first box landed; words 32..37 thread 0's clock64 when the barriers
  * were initialised, the work range known, the first and all initial weight copies issued
- * (dense launches), the MoE groups built, and the copies that follow x staging issued. Phase 3
- * is taken right after x staging. Unrecorded words are zero.
+ * (dense launches), the MoE groups built, and the copies that follow x staging issued. Words 38
+ * and 39: dense launches, thread 0's clock64 just before and just after its first box wait; MoE
+ * launches, the group builder's steps; the FFN block, its slice of h complete and staged. A
+ * build with -DNVFP4_TRACE_BOX_LANDED=1 also has thread 0 of a dense launch wait for its first
+ * box before the dependency wait and record %globaltimer then in word 36. Phase 3 is taken right
+ * after x staging. Unrecorded words are zero.
  * This call synchronises `stream`, copies min(max_words, 16 * 1024 * 40) words in
  * [slot][cta][word] order to host_out (host memory), clears the trace and restarts the slot
  * count. Returns the number of words copied, 0 for a library built without tracing (the
